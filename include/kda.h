@@ -1,0 +1,122 @@
+/*
+ * libkda -- Kimi Delta Attention (KDA) chunked forward pass for one NVIDIA
+ * GB300 (sm_103a).  Plain C ABI: device pointers, sizes, a CUDA stream.
+ *
+ * The operation (per sequence n and head h, state S in R^{V x K}, row =
+ * value index, column = key index):
+ *     a_t = gate(g_t + dt_bias[h])        per key channel, natural log, <= 0
+ *     S   = S * Diag(exp(a_t))
+ *     S   = S + beta_t (v_t - S k_t) k_t^T,   beta_t = sigmoid(beta logit)
+ *     o_t = scale * S q_t
+ * with q, k optionally L2-normalised per token (q / sqrt(|q|^2 + 1e-6)).
+ * Gate forms (flash-linear-attention skills, fla-kda SKILL.md, "Gate
+ * contracts"; fla-kda skill page):
+ *     safe   : a = lower_bound * sigmoid(exp(A_log[h]) * z), -5 <= lb < 0,
+ *              A_log may be NULL (multiplier 1)
+ *     unsafe : a = -exp(A_log[h]) * softplus(z), A_log required
+ * Argument table and constraints follow the flashkda.fwd table of the
+ * FlashKDA page ("Core Kernel API flashkda.fwd"): K == V == 128, bf16 q/k/v/g
+ * and beta logits, fp32 A_log [H] and dt_bias [H, K], states [N, H, V, K] in
+ * fp32 or bf16 (same dtype when both given), int64 cu_seqlens [N+1] with
+ * B == 1 ("Variable-Length (Packed) Batching").  Chaining final_state into
+ * the next call's initial_state continues a stream ("Stateful Inference").
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes (every violation is reported before any launch) ---- */
+#define KDA_OK 0
+#define KDA_ERR_NULL_ARG 1        /* a required pointer is NULL */
+#define KDA_ERR_HEAD_DIM 2        /* K or V is not 128 */
+#define KDA_ERR_SHAPE 3           /* negative size, or N inconsistent with B */
+#define KDA_ERR_GATE_FLAGS 4      /* not exactly one of KDA_GATE_SAFE / KDA_GATE_UNSAFE */
+#define KDA_ERR_LOWER_BOUND 5     /* safe gate with lower_bound outside [-5, 0) */
+#define KDA_ERR_A_LOG_REQUIRED 6  /* unsafe gate with A_log == NULL */
+#define KDA_ERR_STATE_DTYPE 7     /* state_dtype not KDA_DTYPE_F32 / KDA_DTYPE_BF16 */
+#define KDA_ERR_VARLEN_BATCH 8    /* cu_seqlens given with B != 1 */
+#define KDA_ERR_ALIGNMENT 9       /* a tensor pointer is not 16-byte aligned */
+#define KDA_ERR_WORKSPACE 10      /* workspace NULL, misaligned or too small */
+#define KDA_ERR_LAUNCH 11         /* a CUDA launch failed (cudaGetLastError) */
+
+/* ---- flags ---- */
+#define KDA_GATE_SAFE 0x1u   /* lower_bound * sigmoid(exp(A_log) * (g + dt_bias)) */
+#define KDA_GATE_UNSAFE 0x2u /* -exp(A_log) * softplus(g + dt_bias) */
+#define KDA_QK_L2NORM 0x4u   /* L2-normalise q and k per token inside the kernel */
+
+/* ---- state dtypes ---- */
+#define KDA_DTYPE_F32 0
+#define KDA_DTYPE_BF16 1
+
+/*
+ * Arguments of one forward call.  All tensors are dense, row-major and live
+ * in device memory owned by the caller; the library never allocates device
+ * memory and keeps no pointer after the call returns (work is asynchronous
+ * on the given stream, so buffers must stay valid until it completes).
+ *
+ *  q, k, g : bf16 [B, T, H, 128]      v, out : bf16 [B, T, H, 128]
+ *  beta    : bf16 [B, T, H]  (logits; sigmoid applied inside)
+ *  out     : written completely for every token of every sequence
+ *  A_log   : fp32 [H]       (NULL only with KDA_GATE_SAFE -> multiplier 1)
+ *  dt_bias : fp32 [H, 128]  (NULL -> 0)
+ *  initial_state, final_state : [N, H, 128(V), 128(K)] in state_dtype, or
+ *            NULL (initial NULL -> zero state; final NULL -> not written).
+ *            bf16 final states are rounded to nearest-even from fp32.
+ *  cu_seqlens : int64 [N+1] device array or NULL.  With it B must be 1, T is
+ *            the packed token total, cu[0] = 0, non-decreasing, cu[N] = T
+ *            (the values are the caller's duty; they are not read on the host).
+ *            Without it N must equal B and sequence n is batch row n.
+ *  All sizes are int64; tensor pointers must be 16-byte aligned.
+ */
+typedef struct kda_fwd_args {
+  const void *q, *k, *v, *g, *beta;
+  float scale;
+  void *out;
+  const float *A_log;
+  const float *dt_bias;
+  float lower_bound;
+  const void *initial_state;
+  void *final_state;
+  int32_t state_dtype;
+  const int64_t *cu_seqlens;
+  int64_t B, T, H, N;
+  int64_t K, V;
+  uint32_t flags;
+} kda_fwd_args;
+
+/*
+ * Device scratch (bytes) that kda_fwd needs for these arguments: per-chunk
+ * intermediates of the WY form (W, U, gated queries, end-decayed keys, the
+ * intra-chunk read-out matrix and the chunk decay) plus the chunk index of
+ * packed sequences.  Depends only on sizes and on whether cu_seqlens is
+ * given.  Returns 0 for argument sets that kda_fwd would reject.
+ */
+size_t kda_fwd_workspace_bytes(const kda_fwd_args *args);
+
+/*
+ * Enqueue the forward pass on `stream` (a cudaStream_t; NULL = legacy default
+ * stream).  `workspace` is caller-owned device memory of at least
+ * kda_fwd_workspace_bytes(args) bytes, 256-byte aligned; its contents need no
+ * initialisation and are garbage afterwards.  Calls that share a workspace
+ * must be ordered on the device.  Returns KDA_OK or an error code; on error
+ * nothing is launched and nothing is written.
+ */
+int kda_fwd(const kda_fwd_args *args, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Human-readable text of a status code (static storage). */
+const char *kda_error_string(int code);
+
+/* Library version, e.g. 100 for 0.1.0. */
+int kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,197 @@
+// Host side of libkda: argument validation, workspace layout, launches.
+// Declared in include/kda.h.
+#include <atomic>
+#include <cmath>
+
+#include "../../include/kda.h"
+#include "kda_common.cuh"
+#include "kda_kernels.cuh"
+
+namespace kda {
+
+// Exclusive prefix of per-sequence chunk counts ceil(L_n / 64), one block.
+__global__ void __launch_bounds__(1024) kda_chunk_offsets_kernel(const int64_t* cu, int64_t N,
+                                                                  int64_t* chunk_off) {
+  __shared__ int64_t warp_sums[32];
+  __shared__ int64_t carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) { carry = 0; chunk_off[0] = 0; }
+  __syncthreads();
+  for (int64_t base = 0; base < N; base += 1024) {
+    const int64_t n = base + tid;
+    int64_t cnt = 0;
+    if (n < N) cnt = (cu[n + 1] - cu[n] + kChunk - 1) / kChunk;
+    int64_t x = cnt;  // inclusive warp scan
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int64_t w = warp_sums[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      warp_sums[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const int64_t incl = x + (warp > 0 ? warp_sums[warp - 1] : 0) + carry;
+    if (n < N) chunk_off[n + 1] = incl;
+    __syncthreads();
+    if (tid == 1023) carry = incl;
+    __syncthreads();
+  }
+}
+
+void launch_chunk_offsets(const int64_t* cu, int64_t N, int64_t* chunk_off, cudaStream_t s) {
+  kda_chunk_offsets_kernel<<<1, 1024, 0, s>>>(cu, N, chunk_off);
+}
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_prepared[kMaxDevices];
+
+bool aligned(const void* p, uintptr_t a) { return p == nullptr || (((uintptr_t)p) % a) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Validates everything that can be checked on the host.  Returns KDA_OK or an
+// error code; fills the slot count (chunk capacity) on success.
+int validate(const kda_fwd_args* a, int64_t* num_slots, size_t* header_bytes) {
+  if (!a) return KDA_ERR_NULL_ARG;
+  if (!a->q || !a->k || !a->v || !a->g || !a->beta || !a->out) return KDA_ERR_NULL_ARG;
+  if (a->K != kHeadDim || a->V != kHeadDim) return KDA_ERR_HEAD_DIM;
+  if (a->B < 0 || a->T < 0 || a->H < 0 || a->N < 0 || a->H > 65535) return KDA_ERR_SHAPE;
+  const uint32_t gate = a->flags & (KDA_GATE_SAFE | KDA_GATE_UNSAFE);
+  if (gate != KDA_GATE_SAFE && gate != KDA_GATE_UNSAFE) return KDA_ERR_GATE_FLAGS;
+  if (a->flags & ~(KDA_GATE_SAFE | KDA_GATE_UNSAFE | KDA_QK_L2NORM)) return KDA_ERR_GATE_FLAGS;
+  if (gate == KDA_GATE_SAFE && !(a->lower_bound >= -5.0f && a->lower_bound < 0.0f))
+    return KDA_ERR_LOWER_BOUND;
+  if (gate == KDA_GATE_UNSAFE && !a->A_log) return KDA_ERR_A_LOG_REQUIRED;
+  if ((a->initial_state || a->final_state) && a->state_dtype != KDA_DTYPE_F32 &&
+      a->state_dtype != KDA_DTYPE_BF16)
+    return KDA_ERR_STATE_DTYPE;
+  if (a->cu_seqlens) {
+    if (a->B != 1) return KDA_ERR_VARLEN_BATCH;
+  } else if (a->N != a->B) {
+    return KDA_ERR_SHAPE;
+  }
+  if (!aligned(a->q, 16) || !aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->g, 16) ||
+      !aligned(a->out, 16) || !aligned(a->beta, 2) || !aligned(a->A_log, 4) ||
+      !aligned(a->dt_bias, 16) || !aligned(a->initial_state, 16) ||
+      !aligned(a->final_state, 16) || !aligned(a->cu_seqlens, 8))
+    return KDA_ERR_ALIGNMENT;
+  if (a->cu_seqlens) {
+    *num_slots = ceil_div(a->T, kChunk) + a->N;
+    *header_bytes = (size_t)(((a->N + 1) * 8 + 255) / 256 * 256);
+  } else {
+    *num_slots = a->B * ceil_div(a->T, kChunk);
+    *header_bytes = 0;
+  }
+  return KDA_OK;
+}
+
+}  // namespace
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" size_t kda_fwd_workspace_bytes(const kda_fwd_args* args) {
+  int64_t slots = 0;
+  size_t header = 0;
+  if (validate(args, &slots, &header) != KDA_OK) return 0;
+  return header + (size_t)slots * (size_t)args->H * (size_t)kSlotBytes;
+}
+
+extern "C" int kda_fwd(const kda_fwd_args* a, void* workspace, size_t workspace_bytes,
+                       void* stream_ptr) {
+  int64_t slots = 0;
+  size_t header = 0;
+  int rc = validate(a, &slots, &header);
+  if (rc != KDA_OK) return rc;
+  if (a->N == 0 || a->H == 0) return KDA_OK;
+  const size_t need = header + (size_t)slots * (size_t)a->H * (size_t)kSlotBytes;
+  if (need > 0 && (!workspace || !aligned(workspace, 256) || workspace_bytes < need))
+    return KDA_ERR_WORKSPACE;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_LAUNCH;
+  if (dev >= 0 && dev < kMaxDevices && g_prepared[dev].load() == 0) {
+    if (prepare_chunk_kernel() != cudaSuccess || prepare_state_kernel() != cudaSuccess)
+      return KDA_ERR_LAUNCH;
+    g_prepared[dev].store(1);
+  }
+
+  unsigned char* ws = reinterpret_cast<unsigned char*>(workspace);
+  int64_t* chunk_off = a->cu_seqlens ? reinterpret_cast<int64_t*>(ws) : nullptr;
+  unsigned char* slots_base = ws + header;
+  const int64_t NT = ceil_div(a->T, kChunk);
+
+  if (a->cu_seqlens) launch_chunk_offsets(a->cu_seqlens, a->N, chunk_off, stream);
+
+  if (slots > 0) {
+    ChunkParams cp;
+    cp.q = static_cast<const uint16_t*>(a->q);
+    cp.k = static_cast<const uint16_t*>(a->k);
+    cp.v = static_cast<const uint16_t*>(a->v);
+    cp.g = static_cast<const uint16_t*>(a->g);
+    cp.beta = static_cast<const uint16_t*>(a->beta);
+    cp.A_log = a->A_log;
+    cp.dt_bias = a->dt_bias;
+    cp.lower_bound = a->lower_bound;
+    cp.gate_unsafe = (a->flags & KDA_GATE_UNSAFE) ? 1 : 0;
+    cp.l2norm = (a->flags & KDA_QK_L2NORM) ? 1 : 0;
+    cp.cu = a->cu_seqlens;
+    cp.chunk_off = chunk_off;
+    cp.N = a->N;
+    cp.T = a->T;
+    cp.H = a->H;
+    cp.NT = NT;
+    cp.ws = slots_base;
+    launch_chunk_kernel(cp, slots, stream);
+  }
+
+  StateParams sp;
+  sp.out = static_cast<uint16_t*>(a->out);
+  sp.init = a->initial_state;
+  sp.final_state = a->final_state;
+  sp.state_bf16 = a->state_dtype == KDA_DTYPE_BF16 ? 1 : 0;
+  sp.scale = a->scale;
+  sp.cu = a->cu_seqlens;
+  sp.chunk_off = chunk_off;
+  sp.N = a->N;
+  sp.T = a->T;
+  sp.H = a->H;
+  sp.NT = NT;
+  sp.ws = slots_base;
+  launch_state_kernel(sp, stream);
+
+  if (cudaGetLastError() != cudaSuccess) return KDA_ERR_LAUNCH;
+  return KDA_OK;
+}
+
+extern "C" const char* kda_error_string(int code) {
+  switch (code) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_NULL_ARG: return "a required pointer is NULL";
+    case KDA_ERR_HEAD_DIM: return "K and V must both be 128";
+    case KDA_ERR_SHAPE: return "invalid sizes (negative, H > 65535, or N != B without cu_seqlens)";
+    case KDA_ERR_GATE_FLAGS: return "flags must select exactly one gate form and no unknown bits";
+    case KDA_ERR_LOWER_BOUND: return "safe gate requires -5 <= lower_bound < 0";
+    case KDA_ERR_A_LOG_REQUIRED: return "unsafe gate requires A_log";
+    case KDA_ERR_STATE_DTYPE: return "state_dtype must be KDA_DTYPE_F32 or KDA_DTYPE_BF16";
+    case KDA_ERR_VARLEN_BATCH: return "cu_seqlens requires B == 1";
+    case KDA_ERR_ALIGNMENT: return "tensor pointers must be 16-byte aligned";
+    case KDA_ERR_WORKSPACE: return "workspace missing, not 256-byte aligned, or too small";
+    case KDA_ERR_LAUNCH: return "CUDA launch failed";
+    default: return "unknown status code";
+  }
+}
+
+extern "C" int kda_version(void) { return 100; }

@@ -1,0 +1,134 @@
+// Shared device helpers for the KDA forward kernels (sm_103a).
+//
+// Layout conventions
+//  * A "tile128" is a [rows][128] bf16 tile in shared memory with a 256-byte
+//    row pitch whose 16-byte chunks are XOR-swizzled by (row & 7), so that
+//    ldmatrix reads of 8 consecutive rows hit 8 different bank groups.
+//  * A "tile64" is the same for [rows][64] bf16 with a 128-byte pitch.
+//  * Fragments follow the m16n8k16 bf16 mma.sync register layouts:
+//      A (16x16, row-major): a0a1 = (g, 2q..2q+1), a2a3 = (g+8, ..),
+//                            a4a5 = (g, 2q+8..), a6a7 = (g+8, 2q+8..)
+//      B (16x8, k x n):      b0b1 = (k=2q..2q+1, n=g), b2b3 = (k=2q+8.., n=g)
+//      C (16x8, fp32):       c0c1 = (g, 2q..2q+1), c2c3 = (g+8, 2q..2q+1)
+//    with g = lane / 4, q = lane % 4.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+constexpr int kHeadDim = 128;  // K == V == 128
+constexpr int kChunk = 64;     // tokens per chunk
+constexpr int kSub = 16;       // tokens per diagonal sub-chunk
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---- per-(chunk, head) workspace slot ----
+// Intermediates written by the chunk kernel and read by the state kernel.
+constexpr int kSlotW = 0;                       // bf16 [64][128]  W = T (K * gamma)
+constexpr int kSlotU = kSlotW + 64 * 128 * 2;   // bf16 [64][128]  U = T V
+constexpr int kSlotQg = kSlotU + 64 * 128 * 2;  // bf16 [64][128]  q * gamma
+constexpr int kSlotKh = kSlotQg + 64 * 128 * 2; // bf16 [64][128]  k * gamma_C / gamma
+constexpr int kSlotP = kSlotKh + 64 * 128 * 2;  // bf16 [64][64]   intra read-out matrix
+constexpr int kSlotGc = kSlotP + 64 * 64 * 2;   // fp32 [128]      gamma_C (chunk decay)
+constexpr int kSlotBytes = kSlotGc + 128 * 4;   // 74240 (multiple of 256)
+static_assert(kSlotBytes % 256 == 0, "slot must keep 256-byte alignment");
+
+// ---- swizzled shared-memory addressing ----
+__device__ __forceinline__ uint32_t swz128(int row, int col) {  // byte offset
+  return (uint32_t)(row * 256 + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1));
+}
+__device__ __forceinline__ uint32_t swz64(int row, int col) {
+  return (uint32_t)(row * 128 + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1));
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// ---- bf16 packing ----
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
+  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&u);
+  return __bfloat1622float2(v);
+}
+__device__ __forceinline__ float bf16_to_f(uint16_t u) {
+  return __uint_as_float(((uint32_t)u) << 16);
+}
+
+// ---- hardware approximations (single MUFU instructions) ----
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---- tensor-core and data-movement primitives ----
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// 16-byte async copy global -> shared; src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+               "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// A fragment (16x16) of a swizzled tile128 / tile64 at (row0, col0).
+__device__ __forceinline__ void lda_128(uint32_t (&a)[4], uint32_t base, int row0, int col0,
+                                        int lane) {
+  ldsm_x4(a, base + swz128(row0 + (lane & 15), col0 + ((lane >> 4) << 3)));
+}
+__device__ __forceinline__ void lda_64(uint32_t (&a)[4], uint32_t base, int row0, int col0,
+                                       int lane) {
+  ldsm_x4(a, base + swz64(row0 + (lane & 15), col0 + ((lane >> 4) << 3)));
+}
+// B fragments for two n8 tiles (n0, n0+8) x k16 at k0, from storage [n][k]
+// (k contiguous).  b[0..1] -> tile n0, b[2..3] -> tile n0+8.
+__device__ __forceinline__ void ldb_nk_128(uint32_t (&b)[4], uint32_t base, int n0, int k0,
+                                           int lane) {
+  int mi = lane >> 3;
+  ldsm_x4(b, base + swz128(n0 + ((mi >> 1) << 3) + (lane & 7), k0 + ((mi & 1) << 3)));
+}
+__device__ __forceinline__ void ldb_nk_64(uint32_t (&b)[4], uint32_t base, int n0, int k0,
+                                          int lane) {
+  int mi = lane >> 3;
+  ldsm_x4(b, base + swz64(n0 + ((mi >> 1) << 3) + (lane & 7), k0 + ((mi & 1) << 3)));
+}
+// Same, from storage [k][n] (n contiguous), via the transposing load.
+__device__ __forceinline__ void ldb_kn_128(uint32_t (&b)[4], uint32_t base, int n0, int k0,
+                                           int lane) {
+  int mi = lane >> 3;
+  ldsm_x4_t(b, base + swz128(k0 + ((mi & 1) << 3) + (lane & 7), n0 + ((mi >> 1) << 3)));
+}
+
+}  // namespace kda

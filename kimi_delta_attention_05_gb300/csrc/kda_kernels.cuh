@@ -1,0 +1,42 @@
+// Kernel parameter blocks and launch entry points shared by the host API.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+// Intra-chunk stage (one CTA per (chunk slot, head)).
+struct ChunkParams {
+  const uint16_t *q, *k, *v, *g, *beta;  // bf16 [tokens, H, 128] / [tokens, H]
+  const float* A_log;                     // [H] or nullptr (safe gate only)
+  const float* dt_bias;                   // [H, 128] or nullptr
+  float lower_bound;
+  int gate_unsafe;                        // 1: -exp(A_log) softplus, 0: lb sigmoid
+  int l2norm;
+  const int64_t* cu;                      // [N+1] or nullptr (dense)
+  const int64_t* chunk_off;               // [N+1] chunk prefix (varlen only)
+  int64_t N, T, H;
+  int64_t NT;                             // chunks per row (dense)
+  unsigned char* ws;                      // first workspace slot
+};
+
+// Recurrent stage (one CTA per (sequence, head, 64-wide value tile)).
+struct StateParams {
+  uint16_t* out;                          // bf16 [tokens, H, 128]
+  const void* init;                       // [N, H, 128, 128] or nullptr
+  void* final_state;                      // [N, H, 128, 128] or nullptr
+  int state_bf16;
+  float scale;
+  const int64_t* cu;
+  const int64_t* chunk_off;
+  int64_t N, T, H, NT;
+  const unsigned char* ws;
+};
+
+void launch_chunk_offsets(const int64_t* cu, int64_t N, int64_t* chunk_off, cudaStream_t s);
+void launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t s);
+void launch_state_kernel(const StateParams& p, cudaStream_t s);
+cudaError_t prepare_chunk_kernel();
+cudaError_t prepare_state_kernel();
+
+}  // namespace kda

@@ -1,0 +1,154 @@
+"""Thin Python binding of libkda (include/kda.h).
+
+Argument marshalling only: every step of the forward pass runs in the CUDA
+library.  PyTorch supplies device memory and the stream.  If the library is
+missing this raises; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+KDA_GATE_SAFE = 0x1
+KDA_GATE_UNSAFE = 0x2
+KDA_QK_L2NORM = 0x4
+KDA_DTYPE_F32 = 0
+KDA_DTYPE_BF16 = 1
+HEAD_DIM = 128
+
+
+class KdaError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"kda_fwd failed with status {code}: {msg}")
+        self.code = code
+
+
+class kda_fwd_args(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p),
+        ("scale", ctypes.c_float),
+        ("out", ctypes.c_void_p),
+        ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+        ("lower_bound", ctypes.c_float),
+        ("initial_state", ctypes.c_void_p), ("final_state", ctypes.c_void_p),
+        ("state_dtype", ctypes.c_int32),
+        ("cu_seqlens", ctypes.c_void_p),
+        ("B", ctypes.c_int64), ("T", ctypes.c_int64), ("H", ctypes.c_int64), ("N", ctypes.c_int64),
+        ("K", ctypes.c_int64), ("V", ctypes.c_int64),
+        ("flags", ctypes.c_uint32),
+    ]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(build_if_missing: bool = True):
+    """Load libkda.so (building it first if asked and needed)."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB
+        if build_if_missing:
+            path = _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libkda.so not found at {path}; run __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        lib.kda_fwd.restype = ctypes.c_int
+        lib.kda_fwd.argtypes = [ctypes.POINTER(kda_fwd_args), P, ctypes.c_size_t, P]
+        lib.kda_fwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.kda_fwd_workspace_bytes.argtypes = [ctypes.POINTER(kda_fwd_args)]
+        lib.kda_error_string.restype = ctypes.c_char_p
+        lib.kda_error_string.argtypes = [ctypes.c_int]
+        lib.kda_version.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def make_args(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bound=None,
+              initial_state=None, final_state=None, cu_seqlens=None, qk_l2norm=False,
+              gate=None) -> kda_fwd_args:
+    """Build the C argument block from tensors (no checks beyond shapes;
+    the library validates)."""
+    B, T, H, K = q.shape
+    V = v.shape[-1]
+    if gate is None:
+        gate = "unsafe" if lower_bound is None else "safe"
+    flags = KDA_GATE_SAFE if gate == "safe" else KDA_GATE_UNSAFE
+    if qk_l2norm:
+        flags |= KDA_QK_L2NORM
+    N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else B
+    st = initial_state if initial_state is not None else final_state
+    sd = KDA_DTYPE_BF16 if (st is not None and st.dtype == torch.bfloat16) else KDA_DTYPE_F32
+    a = kda_fwd_args()
+    a.q, a.k, a.v, a.g, a.beta = _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta)
+    a.scale = float(scale)
+    a.out = _ptr(out)
+    a.A_log, a.dt_bias = _ptr(A_log), _ptr(dt_bias)
+    a.lower_bound = float(lower_bound if lower_bound is not None else 0.0)
+    a.initial_state, a.final_state = _ptr(initial_state), _ptr(final_state)
+    a.state_dtype = sd
+    a.cu_seqlens = _ptr(cu_seqlens)
+    a.B, a.T, a.H, a.N, a.K, a.V = B, T, H, N, K, V
+    a.flags = flags
+    return a
+
+
+def workspace_bytes(args: kda_fwd_args) -> int:
+    return int(load_library().kda_fwd_workspace_bytes(ctypes.byref(args)))
+
+
+def kda_fwd(q, k, v, g, beta, scale, out=None, A_log=None, dt_bias=None, lower_bound=None,
+            initial_state=None, final_state=None, cu_seqlens=None, *, qk_l2norm=False,
+            gate=None, workspace=None, stream=None):
+    """KDA chunked forward on device tensors; returns ``out``.
+
+    Mirrors the flashkda.fwd argument list: q, k, g [B,T,H,128] bf16, v
+    [B,T,H,128] bf16, beta [B,T,H] bf16 logits, out [B,T,H,128] bf16
+    (allocated here if None), A_log [H] fp32, dt_bias [H,128] fp32,
+    lower_bound (None -> unsafe softplus gate), initial/final state
+    [N,H,128,128] fp32 or bf16, cu_seqlens [N+1] int64.  ``workspace`` is an
+    optional pre-allocated uint8 device tensor; ``stream`` a torch stream.
+    """
+    lib = load_library()
+    if out is None:
+        out = torch.empty_like(v)
+    a = make_args(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
+                  final_state, cu_seqlens, qk_l2norm, gate)
+    need = int(lib.kda_fwd_workspace_bytes(ctypes.byref(a)))
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    rc = lib.kda_fwd(ctypes.byref(a), ctypes.c_void_p(workspace.data_ptr()), need,
+                     ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise KdaError(rc, lib.kda_error_string(rc).decode())
+    return out
+
+
+def kda_fwd_host(inputs: dict, *, stream=None, device="cuda"):
+    """End-to-end call on host (CPU, ideally pinned) tensors: copy inputs to
+    the device, run kda_fwd, copy the output (and final state) back."""
+    dev = torch.device(device)
+    d = {k: (v.to(dev, non_blocking=True) if torch.is_tensor(v) else v) for k, v in inputs.items()}
+    fin = None
+    if inputs.get("final_state_dtype") is not None:
+        fin = torch.empty((inputs["N"], d["q"].shape[2], HEAD_DIM, HEAD_DIM),
+                          dtype=inputs["final_state_dtype"], device=dev)
+    out = kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], None, d.get("A_log"),
+                  d.get("dt_bias"), d.get("lower_bound"), d.get("initial_state"), fin,
+                  d.get("cu_seqlens"), qk_l2norm=d.get("qk_l2norm", False), gate=d.get("gate"),
+                  stream=stream)
+    return out.to("cpu", non_blocking=True), (None if fin is None else fin.to("cpu", non_blocking=True))

@@ -1,0 +1,98 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+declared in include/kda.h, and rejects each invalid argument set with its
+error code before anything is launched (no call below has a valid argument
+set, so no kernel can start)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from kimi_delta_attention_05_gb300 import kda as K
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 0x7F0000000000  # 256-byte aligned, never dereferenced
+
+
+def declared_functions():
+    names = []
+    for hdr in os.listdir(os.path.join(ROOT, "include")):
+        if hdr.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", hdr)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w \*]*?\b(kda_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_declared_symbols():
+    lib = K.load_library()
+    names = declared_functions()
+    assert {"kda_fwd", "kda_fwd_workspace_bytes", "kda_error_string", "kda_version"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+    out = subprocess.run(["nm", "-D", "--defined-only", K.library_path()], capture_output=True,
+                         text=True).stdout
+    for n in names:
+        assert re.search(rf"\bT {n}\b", out), f"{n} missing from the dynamic symbol table"
+
+
+def _valid_args(**over):
+    a = K.kda_fwd_args()
+    for f in ("q", "k", "v", "g", "beta", "out"):
+        setattr(a, f, FAKE)
+    a.scale = 0.088
+    a.A_log = FAKE
+    a.dt_bias = FAKE
+    a.lower_bound = -5.0
+    a.state_dtype = K.KDA_DTYPE_F32
+    a.B, a.T, a.H, a.N, a.K, a.V = 2, 100, 4, 2, 128, 128
+    a.flags = K.KDA_GATE_SAFE | K.KDA_QK_L2NORM
+    for k_, v in over.items():
+        setattr(a, k_, v)
+    return a
+
+
+def _call(a, ws=None, nbytes=0):
+    lib = K.load_library()
+    return lib.kda_fwd(ctypes.byref(a), ws, nbytes, None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), 1), (dict(out=None), 1), (dict(beta=None), 1),
+    (dict(K=64), 2), (dict(V=256), 2),
+    (dict(T=-1), 3), (dict(N=3), 3), (dict(H=70000), 3),
+    (dict(flags=0), 4), (dict(flags=3), 4), (dict(flags=1 | 0x100), 4),
+    (dict(lower_bound=0.0), 5), (dict(lower_bound=-5.5), 5), (dict(lower_bound=float("nan")), 5),
+    (dict(flags=K.KDA_GATE_UNSAFE, A_log=None), 6),
+    (dict(initial_state=FAKE, state_dtype=7), 7),
+    (dict(cu_seqlens=FAKE, B=2), 8),
+    (dict(q=FAKE + 2), 9), (dict(initial_state=FAKE + 8), 9), (dict(cu_seqlens=FAKE + 4, B=1), 9),
+])
+def test_invalid_arguments_rejected(over, code):
+    a = _valid_args(**over)
+    assert _call(a, FAKE, 1 << 40) == code
+    assert K.load_library().kda_fwd_workspace_bytes(ctypes.byref(a)) == 0
+
+
+def test_workspace_checked_before_launch():
+    a = _valid_args()
+    need = K.load_library().kda_fwd_workspace_bytes(ctypes.byref(a))
+    assert need == 2 * 2 * 4 * 74240  # B * ceil(T/64) * H slots of 74240 bytes
+    assert _call(a, None, need) == 10
+    assert _call(a, FAKE, need - 1) == 10
+    assert _call(a, FAKE + 16, need) == 10  # not 256-byte aligned
+
+
+def test_workspace_varlen_size():
+    a = _valid_args(B=1, T=1000, N=5, cu_seqlens=FAKE)
+    need = K.load_library().kda_fwd_workspace_bytes(ctypes.byref(a))
+    assert need == 256 + (16 + 5) * 4 * 74240
+
+
+def test_error_strings():
+    lib = K.load_library()
+    for c in range(12):
+        assert lib.kda_error_string(c)
+    assert b"unknown" in lib.kda_error_string(99)
+    assert lib.kda_version() >= 100

@@ -1,0 +1,167 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the
+same seeded inputs.  Small cases compare every element; the full-size
+workloads compare sampled (sequence, head) units, computed by the oracle one
+by one, in the same launch configuration that the benchmark times."""
+import numpy as np
+import pytest
+import torch
+
+from kimi_delta_attention_05_gb300.workloads import WORKLOADS, make_inputs
+from tests import kda_testlib as tl
+
+pytestmark = pytest.mark.gpu
+
+
+def _full_check(inp, tag, a_log=True, dt_bias=True):
+    o, f = tl.run_gpu(inp, a_log=a_log, dt_bias=dt_bias)
+    ro, rf = tl.run_oracle(inp, a_log=a_log, dt_bias=dt_bias)
+    tl.check_out(o, ro, tag)
+    if f is not None:
+        tl.check_state(f, rf, tag)
+    return o, f
+
+
+def test_tiny():
+    _full_check(make_inputs(WORKLOADS["tiny"]), "tiny")
+
+
+@pytest.mark.parametrize("T", [1, 7, 16, 17, 63, 64, 65, 200])
+def test_dense_ragged_lengths(T):
+    inp = make_inputs(WORKLOADS["dense_batch"], B=2, T=T, H=3, seed=T)
+    _full_check(inp, f"dense T={T}")
+
+
+@pytest.mark.parametrize("T", [5, 130, 300])
+def test_unsafe_gate(T):
+    inp = make_inputs(WORKLOADS["long_context"], T=T, H=2, seed=100 + T)
+    inp["final_state"] = "f32"
+    _full_check(inp, f"unsafe T={T}")
+
+
+def test_varlen_edge_lengths():
+    lens = [1, 15, 16, 17, 63, 64, 65, 130, 2]
+    inp = make_inputs(WORKLOADS["packed_varlen"], lengths=lens, H=2, seed=7)
+    _full_check(inp, "varlen")
+
+
+def test_extremes_reduced():
+    inp = make_inputs(WORKLOADS["extremes"], B=2, T=333, H=2, seed=3)
+    _full_check(inp, "extremes")
+
+
+@pytest.mark.parametrize("lb", [-5.0, -1e-3])
+@pytest.mark.parametrize("sat", [1e4, -1e4])
+def test_saturated_gate_logits(lb, sat):
+    inp = make_inputs(WORKLOADS["dense_batch"], B=1, T=150, H=2, seed=11)
+    g = inp["g"].float()
+    g[:, ::3] = sat  # every third token saturated
+    inp["g"] = g.to(torch.bfloat16)
+    inp["lower_bound"] = lb
+    _full_check(inp, f"saturated lb={lb} g={sat}")
+
+
+def test_unsafe_saturated_logits():
+    inp = make_inputs(WORKLOADS["long_context"], T=200, H=2, seed=12)
+    g = inp["g"].float()
+    g[:, 5::7] = 60.0
+    g[:, 3::11] = -1e4
+    inp["g"] = g.to(torch.bfloat16)
+    inp["final_state"] = "f32"
+    _full_check(inp, "unsafe saturated")
+
+
+def test_safe_without_a_log_and_dt_bias():
+    inp = make_inputs(WORKLOADS["dense_batch"], B=1, T=100, H=2, seed=13)
+    _full_check(inp, "no A_log", a_log=False)
+    _full_check(inp, "no dt_bias", dt_bias=False)
+
+
+def test_no_l2norm_unit_scale():
+    inp = make_inputs(WORKLOADS["extremes"], B=1, T=128, H=1, seed=14)
+    inp["initial_state"] = None
+    inp["final_state"] = "f32"
+    _full_check(inp, "no l2norm")
+
+
+def test_route_parity_safe_vs_unsafe_on_bounded_gates():
+    """Both gate routes on gates whose decays agree: safe with lb = -ln 2 * 2
+    at z = 0 and unsafe with A_log = 0 at z = 0 give the same a = -ln 2."""
+    inp = make_inputs(WORKLOADS["dense_batch"], B=1, T=96, H=2, seed=15)
+    inp["g"] = torch.zeros_like(inp["g"])
+    inp["dt_bias"] = torch.zeros_like(inp["dt_bias"])
+    inp["A_log"] = torch.zeros_like(inp["A_log"])
+    a = dict(inp, lower_bound=-2 * float(np.log(2.0)), gate="safe")
+    b = dict(inp, gate="unsafe")
+    oa, fa = tl.run_gpu(a)
+    ob, fb = tl.run_gpu(b)
+    assert tl.rel_rms(oa, ob) < 1e-3 and tl.rel_rms(fa, fb) < 1e-3
+    ro, rf = tl.run_oracle(a)
+    tl.check_out(ob, ro, "unsafe route")
+
+
+def test_split_chain_on_gpu():
+    """Running [0, s) then [s, T) with final -> initial equals one call."""
+    inp = make_inputs(WORKLOADS["dense_batch"], B=1, T=300, H=2, seed=16)
+    o, f = tl.run_gpu(inp)
+    s = 100
+    first = {k: (v[:, :s] if (torch.is_tensor(v) and v.dim() >= 3 and k != "initial_state") else v)
+             for k, v in inp.items()}
+    o1, f1 = tl.run_gpu(first)
+    second = {k: (v[:, s:] if (torch.is_tensor(v) and v.dim() >= 3 and k != "initial_state") else v)
+              for k, v in inp.items()}
+    second["initial_state"] = torch.from_numpy(f1).float()
+    o2, f2 = tl.run_gpu(second)
+    tl.check_out(np.concatenate([o1, o2], axis=1), o, "split/chain")
+    tl.check_state(f2, f, "split/chain")
+
+
+def test_varlen_equals_separate_calls_bitwise():
+    lens = [40, 64, 1, 129]
+    inp = make_inputs(WORKLOADS["packed_varlen"], lengths=lens, H=2, seed=17)
+    o, f = tl.run_gpu(inp)
+    cu = inp["cu_seqlens"]
+    for n in range(len(lens)):
+        sl = slice(int(cu[n]), int(cu[n + 1]))
+        one = {k: (v[:, sl] if (torch.is_tensor(v) and v.dim() >= 3 and k != "initial_state")
+                   else v) for k, v in inp.items()}
+        one["cu_seqlens"] = None
+        one["initial_state"] = inp["initial_state"][n:n + 1]
+        one["N"] = 1
+        on, fn = tl.run_gpu(one)
+        np.testing.assert_array_equal(on, o[:, sl])
+        np.testing.assert_array_equal(fn[0], f[n])
+
+
+def test_deterministic():
+    inp = make_inputs(WORKLOADS["dense_batch"], B=1, T=256, H=2, seed=18)
+    o1, f1 = tl.run_gpu(inp)
+    o2, f2 = tl.run_gpu(inp)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(f1, f2)
+
+
+def test_empty_sequences_write_initial_state():
+    lens = [0, 5, 0]
+    inp = make_inputs(WORKLOADS["packed_varlen"], lengths=lens, H=2, seed=19)
+    o, f = tl.run_gpu(inp)
+    np.testing.assert_array_equal(f[0], inp["initial_state"][0].double().numpy())
+    np.testing.assert_array_equal(f[2], inp["initial_state"][2].double().numpy())
+    ro, rf = tl.run_oracle(inp)
+    tl.check_out(o, ro, "with empty sequences")
+
+
+# ---- full-size workloads: sampled units against the oracle ----
+
+@pytest.mark.parametrize("name,units", [
+    ("dense_batch", [0, 17, 63]),
+    ("long_context", [0, 13, 31]),
+    ("packed_varlen", [0, 5 * 16 + 3, 63 * 16 + 15]),
+    ("extremes", [0, 15]),
+])
+def test_full_size_sampled(name, units):
+    inp = make_inputs(WORKLOADS[name])
+    o, f = tl.run_gpu(inp)
+    assert np.isfinite(o).all()
+    if f is not None:
+        assert np.isfinite(f).all()
+    tl.compare_units(inp, o, f, units, name)
