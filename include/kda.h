@@ -109,6 +109,20 @@ size_t kda_fwd_workspace_bytes(const kda_fwd_args *args);
  */
 int kda_fwd(const kda_fwd_args *args, void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * kda_fwd, additionally recording three caller-created CUDA events
+ * (cudaEvent_t, each may be NULL) on `stream`: events[0] before the first
+ * launch, events[1] after the intra-chunk stage (chunk index + per-chunk WY
+ * quantities), events[2] after the recurrent stage.  For measurement only;
+ * the computation is identical to kda_fwd.
+ */
+int kda_fwd_profiled(const kda_fwd_args *args, void *workspace, size_t workspace_bytes,
+                     void *stream, void *const events[3]);
+
+/* Number of kernel launches kda_fwd makes for these arguments (0 if none or
+ * if the arguments are invalid). */
+int kda_fwd_launches(const kda_fwd_args *args);
+
 /* Human-readable text of a status code (static storage). */
 const char *kda_error_string(int code);
 

@@ -108,8 +108,8 @@ extern "C" size_t kda_fwd_workspace_bytes(const kda_fwd_args* args) {
   return header + (size_t)slots * (size_t)args->H * (size_t)kSlotBytes;
 }
 
-extern "C" int kda_fwd(const kda_fwd_args* a, void* workspace, size_t workspace_bytes,
-                       void* stream_ptr) {
+static int fwd_impl(const kda_fwd_args* a, void* workspace, size_t workspace_bytes,
+                    void* stream_ptr, void* const* events) {
   int64_t slots = 0;
   size_t header = 0;
   int rc = validate(a, &slots, &header);
@@ -133,6 +133,10 @@ extern "C" int kda_fwd(const kda_fwd_args* a, void* workspace, size_t workspace_
   unsigned char* slots_base = ws + header;
   const int64_t NT = ceil_div(a->T, kChunk);
 
+  auto mark = [&](int i) {
+    if (events && events[i]) cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), stream);
+  };
+  mark(0);
   if (a->cu_seqlens) launch_chunk_offsets(a->cu_seqlens, a->N, chunk_off, stream);
 
   if (slots > 0) {
@@ -157,6 +161,7 @@ extern "C" int kda_fwd(const kda_fwd_args* a, void* workspace, size_t workspace_
     launch_chunk_kernel(cp, slots, stream);
   }
 
+  mark(1);
   StateParams sp;
   sp.out = static_cast<uint16_t*>(a->out);
   sp.init = a->initial_state;
@@ -171,9 +176,27 @@ extern "C" int kda_fwd(const kda_fwd_args* a, void* workspace, size_t workspace_
   sp.NT = NT;
   sp.ws = slots_base;
   launch_state_kernel(sp, stream);
+  mark(2);
 
   if (cudaGetLastError() != cudaSuccess) return KDA_ERR_LAUNCH;
   return KDA_OK;
+}
+
+extern "C" int kda_fwd(const kda_fwd_args* a, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  return fwd_impl(a, workspace, workspace_bytes, stream, nullptr);
+}
+
+extern "C" int kda_fwd_profiled(const kda_fwd_args* a, void* workspace, size_t workspace_bytes,
+                                void* stream, void* const events[3]) {
+  return fwd_impl(a, workspace, workspace_bytes, stream, events);
+}
+
+extern "C" int kda_fwd_launches(const kda_fwd_args* a) {
+  int64_t slots = 0;
+  size_t header = 0;
+  if (validate(a, &slots, &header) != KDA_OK || a->N == 0 || a->H == 0) return 0;
+  return 1 + (slots > 0 ? 1 : 0) + (a->cu_seqlens ? 1 : 0);
 }
 
 extern "C" const char* kda_error_string(int code) {

@@ -17,10 +17,18 @@
 //
 // Decay factors inside a sub-chunk come from running products of
 // d_t = exp(a_t), so every exponent is taken once per (token, channel).
-// For the diagonal sub-blocks the factors are formed from d_t clamped below
-// at exp(-10) so that the midpoint-offset operands stay finite for any gate;
-// with the safe gate (a_t >= -5) the clamp never acts.  Where it acts, the
-// true pair factor and the clamped one are both below exp(-10).
+// The A and P operands are stored relative to the cumulative decay at the
+// sub-chunk midpoint (after its 8th token); off-diagonal sub-blocks multiply
+// in per-channel factors (midpoint -> sub-chunk end -> ... -> next midpoint),
+// all <= 1.  For these operands d_t is clamped below at exp(-10), so that the
+// midpoint-relative values stay within [e^-80, e^80] for any gate; with the
+// safe gate (a_t >= -5) the clamp never acts.  Where it acts, the true pair
+// factor and the clamped one are both below exp(-10).  The recurrent-state
+// quantities (q gamma, K gamma, k gamma_C / gamma, gamma_C) use the exact d_t.
+//
+// Precision: the A / P operands are bf16 (they need its exponent range); the
+// solve is fp32; T, K gamma, V, W, U and everything written to the workspace
+// are fp16 (11-bit significand) with fp32 accumulation.
 #include "kda_common.cuh"
 #include "kda_kernels.cuh"
 
@@ -30,19 +38,18 @@ namespace kda {
 constexpr float kDiagDecayFloor = 4.5399929762484854e-05f;
 
 // shared-memory map (bytes)
-constexpr int kCsQ = 0;          // tile128: raw q, then q_hat * x (clamped)
-constexpr int kCsK = 16384;      // tile128: raw k, then k_hat * x (clamped)
-constexpr int kCsKy = 32768;     // tile128: k_hat * y (clamped)
-constexpr int kCsKg = 49152;     // tile128: raw g, then k_hat * gamma
-constexpr int kCsV = 65536;      // tile128: v
+constexpr int kCsQ = 0;          // tile128: raw q, then bf16 q_hat * xr
+constexpr int kCsK = 16384;      // tile128: raw k, then bf16 k_hat * xr
+constexpr int kCsKy = 32768;     // tile128: bf16 k_hat * yr
+constexpr int kCsKg = 49152;     // tile128: raw g, then fp16 k_hat * gamma
+constexpr int kCsV = 65536;      // tile128: v, converted in place to fp16
 constexpr int kCsA = 81920;      // fp32 [64][64]: A (lower blocks)
 constexpr int kCsInv = 98304;    // fp32 [64][64]: (I + A)^-1 (lower blocks)
-constexpr int kCsT = 114688;     // tile64: T = (I + A)^-1 Diag(beta), bf16
+constexpr int kCsT = 114688;     // tile64: T = (I + A)^-1 Diag(beta), fp16
 constexpr int kCsM = 122880;     // fp32 [3][16][16]: solve scratch
 constexpr int kCsD = 125952;     // fp32 [4][128]: exact sub-chunk decay products
-constexpr int kCsDc = 128000;    // fp32 [4][128]: clamped sub-chunk decay products
-constexpr int kCsIxm = 130048;   // fp32 [4][128]: 1 / clamped forward product at the midpoint
-constexpr int kCsIym = 132096;   // fp32 [4][128]: 1 / clamped backward product at the midpoint
+constexpr int kCsXm = 128000;    // fp32 [4][128]: clamped product over tokens 0..7 of a sub-chunk
+constexpr int kCsYm = 130048;    // fp32 [4][128]: clamped product over tokens 8..15
 constexpr int kCsBeta = 134144;  // fp32 [64]
 constexpr int kCsRq = 134400;    // fp32 [64]: 1 / |q| (or 1)
 constexpr int kCsRk = 134656;    // fp32 [64]: 1 / |k| (or 1)
@@ -63,6 +70,9 @@ __device__ __forceinline__ float ld_tile128(const unsigned char* base, int row, 
 }
 __device__ __forceinline__ void st_tile128(unsigned char* base, int row, int col, float x) {
   *reinterpret_cast<__nv_bfloat16*>(base + swz128(row, col)) = __float2bfloat16_rn(x);
+}
+__device__ __forceinline__ void st_tile128_f16(unsigned char* base, int row, int col, float x) {
+  *reinterpret_cast<__half*>(base + swz128(row, col)) = __float2half_rn(x);
 }
 
 // Scale the 8 bf16 values of an A fragment (columns ch, ch+1, ch+8, ch+9) by
@@ -162,16 +172,15 @@ __global__ void __launch_bounds__(256, 1) kda_chunk_kernel(ChunkParams p) {
   const int rb0 = tid >> 7;
   float d[2][kSub];
   float* sD = reinterpret_cast<float*>(smem + kCsD);
-  float* sDc = reinterpret_cast<float*>(smem + kCsDc);
-  float* sIxm = reinterpret_cast<float*>(smem + kCsIxm);
-  float* sIym = reinterpret_cast<float*>(smem + kCsIym);
+  float* sXm = reinterpret_cast<float*>(smem + kCsXm);
+  float* sYm = reinterpret_cast<float*>(smem + kCsYm);
   {
     const float dtb = p.dt_bias ? p.dt_bias[h * kHeadDim + c] : 0.0f;
     const float amul = p.A_log ? expf(p.A_log[h]) : 1.0f;
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
       const int rb = rb0 + 2 * b;
-      float D = 1.f, Dc = 1.f, xm = 1.f, ym = 1.f;
+      float D = 1.f, xm = 1.f, ym = 1.f;
 #pragma unroll
       for (int j = 0; j < kSub; ++j) {
         const int t = rb * kSub + j;
@@ -185,27 +194,23 @@ __global__ void __launch_bounds__(256, 1) kda_chunk_kernel(ChunkParams p) {
         }
         float dj = t < L ? ex2(a * kLog2e) : 1.0f;
         d[b][j] = dj;
-        float dcj = fmaxf(dj, kDiagDecayFloor);
         D *= dj;
-        Dc *= dcj;
-        if (j < 8) xm *= dcj; else ym *= dcj;
+        if (j < 8) xm *= fmaxf(dj, kDiagDecayFloor); else ym *= fmaxf(dj, kDiagDecayFloor);
       }
       sD[rb * 128 + c] = D;
-      sDc[rb * 128 + c] = Dc;
-      sIxm[rb * 128 + c] = __frcp_rn(xm);
-      sIym[rb * 128 + c] = __frcp_rn(ym);
+      sXm[rb * 128 + c] = xm;
+      sYm[rb * 128 + c] = ym;
     }
   }
   __syncthreads();
 
-  // ---- operands: K x, Q x (clamped, sub-chunk relative), K y (clamped),
-  //      K gamma (exact, chunk relative); q gamma and k gamma_C/gamma to the
-  //      workspace ----
+  // ---- operands ----
+  //  exact, chunk relative:   gamma_j = prod_{s<=j} d_s   -> K gamma (smem), q gamma (ws)
+  //  exact, chunk-end rel.:   gamma_C / gamma_j            -> k_hat (ws)
+  //  clamped, midpoint rel.:  xr_j = e^{lam_j - lam_7}, yr_j = 1 / xr_j  -> A / P operands
   {
-    const float* sRqc = sRq;
-    const float* sRkc = sRk;
-    __nv_bfloat16* gQg = reinterpret_cast<__nv_bfloat16*>(ws + kSlotQg);
-    __nv_bfloat16* gKh = reinterpret_cast<__nv_bfloat16*>(ws + kSlotKh);
+    __half* gQg = reinterpret_cast<__half*>(ws + kSlotQg);
+    __half* gKh = reinterpret_cast<__half*>(ws + kSlotKh);
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
       const int rb = rb0 + 2 * b;
@@ -215,30 +220,37 @@ __global__ void __launch_bounds__(256, 1) kda_chunk_kernel(ChunkParams p) {
         if (s < rb) pre *= Ds;
         if (s > rb) suf *= Ds;
       }
-      // backward products y_j = prod_{s=j+1..15} d_s (reads raw k)
-      float y = 1.f, yc = 1.f;
+      float xe[kSub], ye[kSub], mr[kSub];
+      {
+        float x = pre;
 #pragma unroll
-      for (int j = kSub - 1; j >= 0; --j) {
-        const int t = rb * kSub + j;
-        const float kh = ld_tile128(smem + kCsK, t, c) * sRkc[t];
-        st_tile128(smem + kCsKy, t, c, kh * yc);
-        gKh[t * kHeadDim + c] = __float2bfloat16_rn(kh * y * suf);
-        y *= d[b][j];
-        yc *= fmaxf(d[b][j], kDiagDecayFloor);
+        for (int jj = 0; jj < kSub; ++jj) { x *= d[b][jj]; xe[jj] = x; }
+        float y = suf;
+#pragma unroll
+        for (int jj = kSub - 1; jj >= 0; --jj) { ye[jj] = y; y *= d[b][jj]; }
+        // mr_j = prod_{s=j+1..7} dc_s for j <= 7, prod_{s=8..j} dc_s for j >= 8
+        float m = 1.f;
+#pragma unroll
+        for (int jj = 7; jj >= 0; --jj) { mr[jj] = m; m *= fmaxf(d[b][jj], kDiagDecayFloor); }
+        m = 1.f;
+#pragma unroll
+        for (int jj = 8; jj < kSub; ++jj) { m *= fmaxf(d[b][jj], kDiagDecayFloor); mr[jj] = m; }
       }
-      // forward products x_j = prod_{s=0..j} d_s (overwrites raw q, k, g)
-      float x = 1.f, xc = 1.f;
 #pragma unroll
-      for (int j = 0; j < kSub; ++j) {
-        const int t = rb * kSub + j;
-        x *= d[b][j];
-        xc *= fmaxf(d[b][j], kDiagDecayFloor);
-        const float kh = ld_tile128(smem + kCsK, t, c) * sRkc[t];
-        const float qh = ld_tile128(smem + kCsQ, t, c) * sRqc[t];
-        st_tile128(smem + kCsK, t, c, kh * xc);
-        st_tile128(smem + kCsQ, t, c, qh * xc);
-        st_tile128(smem + kCsKg, t, c, kh * (pre * x));
-        gQg[t * kHeadDim + c] = __float2bfloat16_rn(qh * (pre * x));
+      for (int jj = 0; jj < kSub; ++jj) {
+        const int t = rb * kSub + jj;
+        const float kh = ld_tile128(smem + kCsK, t, c) * sRk[t];
+        const float qh = ld_tile128(smem + kCsQ, t, c) * sRq[t];
+        const float inv = __frcp_rn(mr[jj]);
+        const float xr = jj < 8 ? inv : mr[jj];
+        const float yr = jj < 8 ? mr[jj] : inv;
+        st_tile128(smem + kCsK, t, c, kh * xr);
+        st_tile128(smem + kCsQ, t, c, qh * xr);
+        st_tile128(smem + kCsKy, t, c, kh * yr);
+        st_tile128_f16(smem + kCsKg, t, c, kh * xe[jj]);
+        st_tile128_f16(smem + kCsV, t, c, ld_tile128(smem + kCsV, t, c));
+        gQg[t * kHeadDim + c] = __float2half_rn(qh * xe[jj]);
+        gKh[t * kHeadDim + c] = __float2half_rn(kh * ye[jj]);
       }
     }
     if (rb0 == 0) {
@@ -254,9 +266,14 @@ __global__ void __launch_bounds__(256, 1) kda_chunk_kernel(ChunkParams p) {
   float* sInv = reinterpret_cast<float*>(smem + kCsInv);
 
   // ---- A (warps 0-3) and P (warps 4-7): row sub-block r, column sub-blocks c <= r ----
+  // Diagonal sub-blocks: the midpoint-relative operands multiply directly.
+  // Off-diagonal (cb < r): the left operands get the per-channel factor
+  //   xm[r] * prod_{cb<s<r} xm[s] ym[s]   (-> relative to the end of sub-chunk cb)
+  // and the right operands ym[cb] (-> relative to the end of sub-chunk cb), so
+  // each side is <= |k| and underflows only where the pair factor itself does.
   {
     const int mat = warp >> 2, r = warp & 3;
-    __nv_bfloat16* gP = reinterpret_cast<__nv_bfloat16*>(ws + kSlotP);
+    __half* gP = reinterpret_cast<__half*>(ws + kSlotP);
     for (int cb = 0; cb < 4; ++cb) {
       float acc[2][4];
 #pragma unroll
@@ -269,29 +286,22 @@ __global__ void __launch_bounds__(256, 1) kda_chunk_kernel(ChunkParams p) {
         for (int kk = 0; kk < 8; ++kk) {
           uint32_t a[4];
           lda_128(a, sbase + (mat ? kCsQ : kCsK), 16 * r, 16 * kk, lane);
-          const int ch = 16 * kk + 2 * q4;
-          const int chs[4] = {ch, ch + 1, ch + 8, ch + 9};
           uint32_t b[4];
           ldb_nk_128(b, sbase + kCsKy, 16 * cb, 16 * kk, lane);
-          if (cb == r) {  // diagonal sub-block: midpoint offsets on both sides
-            float fx[4], fy[4];
+          if (cb < r) {
+            const int ch = 16 * kk + 2 * q4;
+            const int chs[4] = {ch, ch + 1, ch + 8, ch + 9};
+            float fa[4], fb[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              fx[u] = sIxm[r * 128 + chs[u]];
-              fy[u] = sIym[r * 128 + chs[u]];
+              float e = sXm[r * 128 + chs[u]];
+              for (int s = cb + 1; s < r; ++s) e *= sXm[s * 128 + chs[u]] * sYm[s * 128 + chs[u]];
+              fa[u] = e;
+              fb[u] = sYm[cb * 128 + chs[u]];
             }
-            scale_afrag(a, fx);
-            scale_bfrag(b[0], b[1], fy);
-            scale_bfrag(b[2], b[3], fy);
-          } else if (cb < r - 1) {  // decay of the sub-chunks in between
-            float fe[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              float e = 1.f;
-              for (int s = cb + 1; s < r; ++s) e *= sDc[s * 128 + chs[u]];
-              fe[u] = e;
-            }
-            scale_afrag(a, fe);
+            scale_afrag(a, fa);
+            scale_bfrag(b[0], b[1], fb);
+            scale_bfrag(b[2], b[3], fb);
           }
           mma_bf16(acc[0], a, b[0], b[1]);
           mma_bf16(acc[1], a, b[2], b[3]);
@@ -314,7 +324,7 @@ __global__ void __launch_bounds__(256, 1) kda_chunk_kernel(ChunkParams p) {
             const bool k0 = active && (cb < r || col <= row);
             const bool k1 = active && (cb < r || col + 1 <= row);
             *reinterpret_cast<uint32_t*>(gP + row * 64 + col) =
-                pack_bf16(k0 ? v0 : 0.f, k1 ? v1 : 0.f);
+                pack_f16(k0 ? v0 : 0.f, k1 ? v1 : 0.f);
           }
         }
       }
@@ -365,15 +375,15 @@ __global__ void __launch_bounds__(256, 1) kda_chunk_kernel(ChunkParams p) {
       __syncthreads();
     }
   }
-  // ---- T = Inv Diag(beta) as a bf16 operand ----
+  // ---- T = Inv Diag(beta) as an fp16 operand ----
   for (int idx = tid; idx < 64 * 64; idx += 256) {
     const int ii = idx >> 6, jj = idx & 63;
     const float val = jj <= ii ? sInv[ii * 64 + jj] * sBeta[jj] : 0.f;
-    *reinterpret_cast<__nv_bfloat16*>(smem + kCsT + swz64(ii, jj)) = __float2bfloat16_rn(val);
+    *reinterpret_cast<__half*>(smem + kCsT + swz64(ii, jj)) = __float2half_rn(val);
   }
   __syncthreads();
 
-  // ---- W = T (K gamma) (warps 0-3) and U = T V (warps 4-7), row sub-block r ----
+  // ---- W = T (K gamma) (warps 0-3) and U = T V (warps 4-7), row sub-block r, fp16 ----
   {
     const int mat = warp >> 2, r = warp & 3;
     float acc[16][4];
@@ -388,17 +398,17 @@ __global__ void __launch_bounds__(256, 1) kda_chunk_kernel(ChunkParams p) {
       for (int np = 0; np < 8; ++np) {
         uint32_t b[4];
         ldb_kn_128(b, sbase + (mat ? kCsV : kCsKg), 16 * np, 16 * cb, lane);
-        mma_bf16(acc[2 * np], a, b[0], b[1]);
-        mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
+        mma_f16(acc[2 * np], a, b[0], b[1]);
+        mma_f16(acc[2 * np + 1], a, b[2], b[3]);
       }
     }
-    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(ws + (mat ? kSlotU : kSlotW));
+    __half* out = reinterpret_cast<__half*>(ws + (mat ? kSlotU : kSlotW));
 #pragma unroll
     for (int nt = 0; nt < 16; ++nt) {
       const int row = 16 * r + g, col = 8 * nt + 2 * q4;
-      *reinterpret_cast<uint32_t*>(out + row * kHeadDim + col) = pack_bf16(acc[nt][0], acc[nt][1]);
+      *reinterpret_cast<uint32_t*>(out + row * kHeadDim + col) = pack_f16(acc[nt][0], acc[nt][1]);
       *reinterpret_cast<uint32_t*>(out + (row + 8) * kHeadDim + col) =
-          pack_bf16(acc[nt][2], acc[nt][3]);
+          pack_f16(acc[nt][2], acc[nt][3]);
     }
   }
 }

@@ -13,6 +13,7 @@
 //    with g = lane / 4, q = lane % 4.
 #pragma once
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -24,12 +25,14 @@ constexpr int kSub = 16;       // tokens per diagonal sub-chunk
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---- per-(chunk, head) workspace slot ----
-// Intermediates written by the chunk kernel and read by the state kernel.
-constexpr int kSlotW = 0;                       // bf16 [64][128]  W = T (K * gamma)
-constexpr int kSlotU = kSlotW + 64 * 128 * 2;   // bf16 [64][128]  U = T V
-constexpr int kSlotQg = kSlotU + 64 * 128 * 2;  // bf16 [64][128]  q * gamma
-constexpr int kSlotKh = kSlotQg + 64 * 128 * 2; // bf16 [64][128]  k * gamma_C / gamma
-constexpr int kSlotP = kSlotKh + 64 * 128 * 2;  // bf16 [64][64]   intra read-out matrix
+// Intermediates written by the chunk kernel and read by the state kernel, all
+// fp16 (11-bit significand: these feed the recurrent state, where bf16's 8
+// bits cost more accuracy than the tolerance allows).
+constexpr int kSlotW = 0;                       // fp16 [64][128]  W = T (K * gamma)
+constexpr int kSlotU = kSlotW + 64 * 128 * 2;   // fp16 [64][128]  U = T V
+constexpr int kSlotQg = kSlotU + 64 * 128 * 2;  // fp16 [64][128]  q * gamma
+constexpr int kSlotKh = kSlotQg + 64 * 128 * 2; // fp16 [64][128]  k * gamma_C / gamma
+constexpr int kSlotP = kSlotKh + 64 * 128 * 2;  // fp16 [64][64]   intra read-out matrix
 constexpr int kSlotGc = kSlotP + 64 * 64 * 2;   // fp32 [128]      gamma_C (chunk decay)
 constexpr int kSlotBytes = kSlotGc + 128 * 4;   // 74240 (multiple of 256)
 static_assert(kSlotBytes % 256 == 0, "slot must keep 256-byte alignment");
@@ -58,6 +61,17 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
 __device__ __forceinline__ float bf16_to_f(uint16_t u) {
   return __uint_as_float(((uint32_t)u) << 16);
 }
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float2 unpack_f16(uint32_t u) {
+  __half2 v = *reinterpret_cast<__half2*>(&u);
+  return __half22float2(v);
+}
+__device__ __forceinline__ float f16_to_f(uint16_t u) {
+  return __half2float(__ushort_as_half(u));
+}
 
 // ---- hardware approximations (single MUFU instructions) ----
 __device__ __forceinline__ float ex2(float x) {
@@ -76,6 +90,16 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], 
                                          uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Same shape with fp16 operands (11-bit significand, same issue rate).
+__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));

@@ -8,8 +8,10 @@
 //                                          the chunk_o stage of the fla code map)
 //   S     = S Diag(gamma_C) + U_new^T K_hat   (chunk_delta_h state update)
 // Each warp owns 16 value rows of S in mma accumulator registers (fp32); the
-// accumulator layout is reused directly as the bf16 left operand of the next
-// product, so the sequential chain never leaves the register file.
+// accumulator layout is reused directly as the fp16 left operand of the next
+// product, so the sequential chain never leaves the register file.  All
+// operands are fp16 (11-bit significand) with fp32 accumulation; the state
+// itself stays fp32.
 #include "kda_common.cuh"
 #include "kda_kernels.cuh"
 
@@ -121,14 +123,14 @@ __global__ void __launch_bounds__(128, 1) kda_state_kernel(StateParams p) {
     cp_async_wait<1>();
     __syncthreads();
 
-    // state -> bf16 left operand over the key dimension (8 k16 steps)
+    // state -> fp16 left operand over the key dimension (8 k16 steps)
     uint32_t sa[8][4];
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
-      sa[kk][0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
-      sa[kk][1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
-      sa[kk][2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-      sa[kk][3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+      sa[kk][0] = pack_f16(s[2 * kk][0], s[2 * kk][1]);
+      sa[kk][1] = pack_f16(s[2 * kk][2], s[2 * kk][3]);
+      sa[kk][2] = pack_f16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+      sa[kk][3] = pack_f16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
     }
 
     // X = S W^T  [16 v x 64 t];  U_new^T = U^T - X
@@ -143,8 +145,8 @@ __global__ void __launch_bounds__(128, 1) kda_state_kernel(StateParams p) {
       for (int np = 0; np < 4; ++np) {
         uint32_t b[4];
         ldb_nk_128(b, bufa + kStW, 16 * np, 16 * kk, lane);
-        mma_bf16(un[2 * np], sa[kk], b[0], b[1]);
-        mma_bf16(un[2 * np + 1], sa[kk], b[2], b[3]);
+        mma_f16(un[2 * np], sa[kk], b[0], b[1]);
+        mma_f16(un[2 * np + 1], sa[kk], b[2], b[3]);
       }
     }
     const int vl = 16 * warp + g;
@@ -154,17 +156,17 @@ __global__ void __launch_bounds__(128, 1) kda_state_kernel(StateParams p) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int tt = t + (e & 1), vv = vl + 8 * (e >> 1);
-        const float u = bf16_to_f(*reinterpret_cast<const uint16_t*>(buf + kStU + swz64(tt, vv)));
+        const float u = f16_to_f(*reinterpret_cast<const uint16_t*>(buf + kStU + swz64(tt, vv)));
         un[j][e] = u - un[j][e];
       }
     }
     uint32_t ua[4][4];
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
-      ua[kk][0] = pack_bf16(un[2 * kk][0], un[2 * kk][1]);
-      ua[kk][1] = pack_bf16(un[2 * kk][2], un[2 * kk][3]);
-      ua[kk][2] = pack_bf16(un[2 * kk + 1][0], un[2 * kk + 1][1]);
-      ua[kk][3] = pack_bf16(un[2 * kk + 1][2], un[2 * kk + 1][3]);
+      ua[kk][0] = pack_f16(un[2 * kk][0], un[2 * kk][1]);
+      ua[kk][1] = pack_f16(un[2 * kk][2], un[2 * kk][3]);
+      ua[kk][2] = pack_f16(un[2 * kk + 1][0], un[2 * kk + 1][1]);
+      ua[kk][3] = pack_f16(un[2 * kk + 1][2], un[2 * kk + 1][3]);
     }
 
     // O^T = S Qg^T + U_new^T P^T  [16 v x 64 t]
@@ -179,8 +181,8 @@ __global__ void __launch_bounds__(128, 1) kda_state_kernel(StateParams p) {
       for (int np = 0; np < 4; ++np) {
         uint32_t b[4];
         ldb_nk_128(b, bufa + kStQg, 16 * np, 16 * kk, lane);
-        mma_bf16(o[2 * np], sa[kk], b[0], b[1]);
-        mma_bf16(o[2 * np + 1], sa[kk], b[2], b[3]);
+        mma_f16(o[2 * np], sa[kk], b[0], b[1]);
+        mma_f16(o[2 * np + 1], sa[kk], b[2], b[3]);
       }
     }
 #pragma unroll
@@ -189,8 +191,8 @@ __global__ void __launch_bounds__(128, 1) kda_state_kernel(StateParams p) {
       for (int np = 0; np < 4; ++np) {
         uint32_t b[4];
         ldb_nk_64(b, bufa + kStP, 16 * np, 16 * kk, lane);
-        mma_bf16(o[2 * np], ua[kk], b[0], b[1]);
-        mma_bf16(o[2 * np + 1], ua[kk], b[2], b[3]);
+        mma_f16(o[2 * np], ua[kk], b[0], b[1]);
+        mma_f16(o[2 * np + 1], ua[kk], b[2], b[3]);
       }
     }
 #pragma unroll
@@ -217,8 +219,8 @@ __global__ void __launch_bounds__(128, 1) kda_state_kernel(StateParams p) {
       for (int np = 0; np < 8; ++np) {
         uint32_t b[4];
         ldb_kn_128(b, bufa + kStKh, 16 * np, 16 * kk, lane);
-        mma_bf16(s[2 * np], ua[kk], b[0], b[1]);
-        mma_bf16(s[2 * np + 1], ua[kk], b[2], b[3]);
+        mma_f16(s[2 * np], ua[kk], b[0], b[1]);
+        mma_f16(s[2 * np + 1], ua[kk], b[2], b[3]);
       }
     }
     __syncthreads();

@@ -69,6 +69,11 @@ def load_library(build_if_missing: bool = True):
         lib.kda_error_string.restype = ctypes.c_char_p
         lib.kda_error_string.argtypes = [ctypes.c_int]
         lib.kda_version.restype = ctypes.c_int
+        lib.kda_fwd_profiled.restype = ctypes.c_int
+        lib.kda_fwd_profiled.argtypes = [ctypes.POINTER(kda_fwd_args), P, ctypes.c_size_t, P,
+                                         ctypes.POINTER(ctypes.c_void_p)]
+        lib.kda_fwd_launches.restype = ctypes.c_int
+        lib.kda_fwd_launches.argtypes = [ctypes.POINTER(kda_fwd_args)]
         _lib = lib
     return _lib
 
@@ -136,6 +141,23 @@ def kda_fwd(q, k, v, g, beta, scale, out=None, A_log=None, dt_bias=None, lower_b
     if rc != 0:
         raise KdaError(rc, lib.kda_error_string(rc).decode())
     return out
+
+
+def kda_fwd_args_call(args: kda_fwd_args, workspace, stream, events=None) -> None:
+    """Call the library on a prepared argument block (used by the benchmark to
+    keep Python marshalling out of the timed loop).  ``events``: optional
+    three raw cudaEvent_t handles (ints) for kda_fwd_profiled."""
+    lib = load_library()
+    need = int(lib.kda_fwd_workspace_bytes(ctypes.byref(args)))
+    wptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else None
+    if events is None:
+        rc = lib.kda_fwd(ctypes.byref(args), wptr, need, ctypes.c_void_p(stream.cuda_stream))
+    else:
+        arr = (ctypes.c_void_p * 3)(*[ctypes.c_void_p(e) if e else None for e in events])
+        rc = lib.kda_fwd_profiled(ctypes.byref(args), wptr, need,
+                                  ctypes.c_void_p(stream.cuda_stream), arr)
+    if rc != 0:
+        raise KdaError(rc, lib.kda_error_string(rc).decode())
 
 
 def kda_fwd_host(inputs: dict, *, stream=None, device="cuda"):
