@@ -44,6 +44,7 @@ extern "C" {
 #define KDA_ERR_ALIGNMENT 9       /* a tensor pointer is not 16-byte aligned */
 #define KDA_ERR_WORKSPACE 10      /* workspace NULL, misaligned or too small */
 #define KDA_ERR_LAUNCH 11         /* a CUDA launch failed (cudaGetLastError) */
+#define KDA_ERR_NOALLOC_LIMIT 12  /* kda_fwd_noalloc: problem needs more scratch than built in */
 
 /* ---- flags ---- */
 #define KDA_GATE_SAFE 0x1u   /* lower_bound * sigmoid(exp(A_log) * (g + dt_bias)) */
@@ -122,6 +123,32 @@ int kda_fwd_profiled(const kda_fwd_args *args, void *workspace, size_t workspace
 /* Number of kernel launches kda_fwd makes for these arguments (0 if none or
  * if the arguments are invalid). */
 int kda_fwd_launches(const kda_fwd_args *args);
+
+/*
+ * kda_fwd without a caller-provided workspace.  No counterpart in the pages:
+ * this exists for callers that cannot allocate device memory when they run
+ * the forward pass (host callbacks or plugins without an allocator, code
+ * that must not touch the owning framework's caching allocator, fixed
+ * memory budgets that forbid runtime cudaMalloc).  The workspace comes from a
+ * buffer of KDA_NOALLOC_SCRATCH_BYTES compiled into the library, held on every
+ * GPU that loads the library until the process exits.  The call itself
+ * allocates nothing.
+ *
+ *  - Limit: problems whose kda_fwd_workspace_bytes(args) exceeds
+ *    KDA_NOALLOC_SCRATCH_BYTES are rejected with KDA_ERR_NOALLOC_LIMIT before
+ *    anything runs (32 MiB holds 451 (64-token chunk, head) slots, e.g.
+ *    T * H <= 28,864 token-heads for dense inputs).
+ *  - Set-up: the first call on a device looks up the buffer's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Sharing: every call on a device uses the same buffer, which keeps the
+ *    previous call's contents.  Nothing in it needs to start at zero, but
+ *    calls that can overlap on the GPU (different streams, no ordering) race
+ *    on it: order them.
+ * Other arguments, ownership and errors are as for kda_fwd.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int kda_fwd_noalloc(const kda_fwd_args *args, void *stream);
 
 /* Human-readable text of a status code (static storage). */
 const char *kda_error_string(int code);

@@ -1,0 +1,78 @@
+"""kda_fwd_noalloc: the forward pass for callers that cannot allocate device
+memory when they run it (host callbacks, plugins without an allocator, fixed
+memory budgets).  It takes its workspace from a buffer built into the library
+instead of from the caller.
+
+Checked here through the C ABI: two calls in a row (different shapes, one
+packed varlen) give the same result as kda_fwd with a caller workspace, to the
+parity tolerances of the other GPU tests; a problem larger than the built-in
+buffer is rejected before anything runs.  This file sorts last so that a run
+stopping at the first failure has already run every other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from kimi_delta_attention_05_gb300 import kda as K
+from kimi_delta_attention_05_gb300.workloads import WORKLOADS, make_inputs
+from tests import kda_testlib as tl
+
+pytestmark = pytest.mark.gpu
+
+KDA_ERR_NOALLOC_LIMIT = 12
+
+
+def _lib():
+    lib = K.load_library()
+    lib.kda_fwd_noalloc.restype = ctypes.c_int
+    lib.kda_fwd_noalloc.argtypes = [ctypes.POINTER(K.kda_fwd_args), ctypes.c_void_p]
+    return lib
+
+
+def _run(inp, use_noalloc):
+    d = tl.to_device(inp)
+    out = torch.full_like(d["v"], float("nan"))
+    fin = torch.full((inp["N"], d["q"].shape[2], 128, 128), float("nan"), device="cuda")
+    lb = inp["lower_bound"] if inp["gate"] == "safe" else None
+    args = K.make_args(d["q"], d["k"], d["v"], d["g"], d["beta"], inp["scale"], out, d["A_log"],
+                       d["dt_bias"], lb, d["initial_state"], fin, d["cu_seqlens"],
+                       inp["qk_l2norm"], inp["gate"])
+    stream = torch.cuda.current_stream()
+    if use_noalloc:
+        rc = _lib().kda_fwd_noalloc(ctypes.byref(args), ctypes.c_void_p(stream.cuda_stream))
+        assert rc == 0, _lib().kda_error_string(rc)
+    else:
+        K.kda_fwd_args_call(args, torch.empty(K.workspace_bytes(args), dtype=torch.uint8,
+                                              device="cuda"), stream)
+    torch.cuda.synchronize()
+    return out.double().cpu().numpy(), fin.double().cpu().numpy()
+
+
+def test_noalloc_matches_kda_fwd_on_two_calls_in_a_row():
+    first = make_inputs(WORKLOADS["dense_batch"], B=2, T=300, H=3, seed=41)
+    first["final_state"] = "f32"
+    second = make_inputs(WORKLOADS["packed_varlen"], lengths=[70, 5, 130, 64], H=2, seed=42)
+    for inp in (first, second):
+        o_ref, f_ref = _run(inp, use_noalloc=False)
+        o, f = _run(inp, use_noalloc=True)
+        tl.check_out(o, o_ref, "noalloc vs kda_fwd")
+        tl.check_state(f, f_ref, "noalloc vs kda_fwd")
+        ro, rf = tl.run_oracle(inp)
+        tl.check_out(o, ro, "noalloc vs oracle")
+        tl.check_state(f, rf, "noalloc vs oracle")
+
+
+def test_noalloc_rejects_problems_beyond_its_buffer():
+    a = K.kda_fwd_args()
+    fake = 0x7F0000000000  # never dereferenced: the size check comes first
+    for name in ("q", "k", "v", "g", "beta", "out"):
+        setattr(a, name, fake)
+    a.scale, a.lower_bound = 0.088, -5.0
+    a.B, a.T, a.H, a.N, a.K, a.V = 1, 8192, 32, 1, 128, 128
+    a.flags = K.KDA_GATE_SAFE
+    assert K.workspace_bytes(a) > 32 * 1024 * 1024
+    rc = _lib().kda_fwd_noalloc(ctypes.byref(a), None)
+    assert rc == KDA_ERR_NOALLOC_LIMIT
+    assert b"built-in" in _lib().kda_error_string(rc)
