@@ -6,54 +6,59 @@
 //     stage of the fla-kda code map: gate activation + cumulative decay),
 //   * optional q/k L2 normalisation,
 //   * A (beta-scaled strictly-lower decayed K K^T) and P (lower decayed Q K^T)
-//     from 16-token sub-chunks: off-diagonal sub-blocks use paired decay
-//     factors whose exponents are both <= 0, diagonal sub-blocks use an
-//     offset at the sub-chunk midpoint (fla-kda SKILL.md, "Numerical
-//     invariants"; fla-kda skill page on the midpoint offset),
-//   * T = (I + A)^-1 Diag(beta) by 16x16 diagonal inverses and block merges
-//     (the "solve_tril" / triangular block merge stage),
-//   * W = T (K * gamma) and U = T V (the "wy_fast" WY recompute),
-//   * q * gamma, k * gamma_C / gamma and gamma_C for the state stage.
+//     from 16-token sub-chunks: diagonal sub-blocks use an offset at the
+//     sub-chunk midpoint, off-diagonal sub-blocks paired decay factors that
+//     are both <= 1 (fla-kda SKILL.md, "Numerical invariants"; fla-kda skill
+//     page on the midpoint offset),
+//   * [W | U] = (I + A)^-1 Diag(beta) [K gamma | V] by block forward
+//     substitution over the four sub-chunks: 16x16 diagonal inverses by
+//     forward substitution, then Y_r = X_r (B_r - sum_{c<r} A_rc Y_c)
+//     (the "solve_tril" triangular block merges and the "wy_fast" WY
+//     recompute of the fla-kda code map, fused),
+//   * q gamma, k gamma_C / gamma and gamma_C for the state stage.
 //
 // Decay factors inside a sub-chunk come from running products of
 // d_t = exp(a_t), so every exponent is taken once per (token, channel).
 // The A and P operands are stored relative to the cumulative decay at the
 // sub-chunk midpoint (after its 8th token); off-diagonal sub-blocks multiply
-// in per-channel factors (midpoint -> sub-chunk end -> ... -> next midpoint),
-// all <= 1.  For these operands d_t is clamped below at exp(-10), so that the
+// in per-channel factors that move each side to the end of the earlier
+// sub-chunk.  For these operands d_t is clamped below at exp(-10), so that the
 // midpoint-relative values stay within [e^-80, e^80] for any gate; with the
 // safe gate (a_t >= -5) the clamp never acts.  Where it acts, the true pair
 // factor and the clamped one are both below exp(-10).  The recurrent-state
 // quantities (q gamma, K gamma, k gamma_C / gamma, gamma_C) use the exact d_t.
 //
 // Precision: the A / P operands are bf16 (they need its exponent range); the
-// solve is fp32; T, K gamma, V, W, U and everything written to the workspace
-// are fp16 (11-bit significand) with fp32 accumulation.
+// diagonal inverses are fp32; everything else is fp16 (11-bit significand)
+// with fp32 accumulation.
 #include "kda_common.cuh"
 #include "kda_kernels.cuh"
 
 namespace kda {
 
-// exp(-10): floor of the per-token decay inside the diagonal-block factors.
+// exp(-10): floor of the per-token decay inside the A / P operands.
 constexpr float kDiagDecayFloor = 4.5399929762484854e-05f;
 
-// shared-memory map (bytes)
+// ---- shared-memory map (bytes) ----
+// phase 1 (until the A / P products are done)
 constexpr int kCsQ = 0;          // tile128: raw q, then bf16 q_hat * xr
 constexpr int kCsK = 16384;      // tile128: raw k, then bf16 k_hat * xr
 constexpr int kCsKy = 32768;     // tile128: bf16 k_hat * yr
-constexpr int kCsKg = 49152;     // tile128: raw g, then fp16 k_hat * gamma
-constexpr int kCsV = 65536;      // tile128: v, converted in place to fp16
-constexpr int kCsA = 81920;      // fp32 [64][64]: A (lower blocks)
-constexpr int kCsInv = 98304;    // fp32 [64][64]: (I + A)^-1 (lower blocks)
-constexpr int kCsT = 114688;     // tile64: T = (I + A)^-1 Diag(beta), fp16
-constexpr int kCsM = 122880;     // fp32 [3][16][16]: solve scratch
-constexpr int kCsD = 125952;     // fp32 [4][128]: exact sub-chunk decay products
-constexpr int kCsXm = 128000;    // fp32 [4][128]: clamped product over tokens 0..7 of a sub-chunk
-constexpr int kCsYm = 130048;    // fp32 [4][128]: clamped product over tokens 8..15
-constexpr int kCsBeta = 134144;  // fp32 [64]
-constexpr int kCsRq = 134400;    // fp32 [64]: 1 / |q| (or 1)
-constexpr int kCsRk = 134656;    // fp32 [64]: 1 / |k| (or 1)
-constexpr int kChunkSmem = 134912;
+constexpr int kCsG = 49152;      // tile128: raw g, then fp16 beta k_hat gamma, then W
+constexpr int kCsV = 65536;      // tile128: raw v, then fp16 beta v, then U
+// phase 2 (aliases the q / k operand tiles once A and P are in registers)
+constexpr int kCsA16 = 0;        // tile64 fp16: A (lower sub-blocks)
+constexpr int kCsAd = 8192;      // fp32 [4][16][16]: diagonal sub-blocks of A
+constexpr int kCsX = 16384;      // tile64 fp16 [16][64]: inverse of sub-block r at cols 16r..
+// small arrays
+constexpr int kCsD = 81920;      // fp32 [4][128]: exact sub-chunk decay products
+constexpr int kCsXm = 83968;     // fp32 [4][128]: clamped product over tokens 0..7
+constexpr int kCsYm = 86016;     // fp32 [4][128]: clamped product over tokens 8..15
+constexpr int kCsFa = 88064;     // fp32 [6][128]: left factors of the off-diagonal sub-blocks
+constexpr int kCsBeta = 91136;   // fp32 [64]
+constexpr int kCsRq = 91392;     // fp32 [64]: 1 / |q| (or 1)
+constexpr int kCsRk = 91648;     // fp32 [64]: 1 / |k| (or 1)
+constexpr int kChunkSmem = 91904;
 
 __device__ __forceinline__ float sigmoidf_fast(float x) {
   return __frcp_rn(1.0f + ex2(-x * kLog2e));
@@ -65,14 +70,8 @@ __device__ __forceinline__ float log1p_small(float e) {
   return lg2(1.0f + e) * 0.69314718055994531f;
 }
 
-__device__ __forceinline__ float ld_tile128(const unsigned char* base, int row, int col) {
-  return bf16_to_f(*reinterpret_cast<const uint16_t*>(base + swz128(row, col)));
-}
-__device__ __forceinline__ void st_tile128(unsigned char* base, int row, int col, float x) {
-  *reinterpret_cast<__nv_bfloat16*>(base + swz128(row, col)) = __float2bfloat16_rn(x);
-}
-__device__ __forceinline__ void st_tile128_f16(unsigned char* base, int row, int col, float x) {
-  *reinterpret_cast<__half*>(base + swz128(row, col)) = __float2half_rn(x);
+__device__ __forceinline__ uint32_t& u32_at(unsigned char* base, uint32_t off) {
+  return *reinterpret_cast<uint32_t*>(base + off);
 }
 
 // Scale the 8 bf16 values of an A fragment (columns ch, ch+1, ch+8, ch+9) by
@@ -91,7 +90,18 @@ __device__ __forceinline__ void scale_bfrag(uint32_t& b0, uint32_t& b1, const fl
   v = unpack_bf16(b1); b1 = pack_bf16(v.x * f[2], v.y * f[3]);
 }
 
-__global__ void __launch_bounds__(256, 1) kda_chunk_kernel(ChunkParams p) {
+__device__ __forceinline__ float gate_decay(float z, float amul, float lb, int unsafe) {
+  float a;
+  if (unsafe) {
+    const float e = ex2(-fabsf(z) * kLog2e);
+    a = -amul * (fmaxf(z, 0.0f) + log1p_small(e));
+  } else {
+    a = lb * sigmoidf_fast(amul * z);
+  }
+  return ex2(a * kLog2e);
+}
+
+__global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t slot = blockIdx.x;
@@ -120,17 +130,18 @@ __global__ void __launch_bounds__(256, 1) kda_chunk_kernel(ChunkParams p) {
   const int64_t t0 = bos + i * kChunk;
   const int L = (int)min((int64_t)kChunk, seqlen - i * kChunk);
   unsigned char* ws = p.ws + (slot * H + h) * (int64_t)kSlotBytes;
+  const uint32_t sbase = smem_u32(smem);
 
-  // ---- stage q, k, g, v into swizzled tiles (rows >= L zero-filled) ----
+  // ---- S0: stage q, k, g, v into swizzled tiles (rows >= L zero-filled) ----
   {
     const uint16_t* src[4] = {p.q, p.k, p.g, p.v};
-    const int dstoff[4] = {kCsQ, kCsK, kCsKg, kCsV};
-    const uint32_t sbase = smem_u32(smem);
+    const int dstoff[4] = {kCsQ, kCsK, kCsG, kCsV};
+#pragma unroll 4
     for (int idx = tid; idx < 4 * 1024; idx += 256) {
-      int tsr = idx >> 10, row = (idx >> 4) & 63, ch = idx & 15;
-      bool ok = row < L;
+      const int tsr = idx >> 10, row = (idx >> 4) & 63, ch = idx & 15;
+      const bool ok = row < L;
       const uint16_t* s = ok ? src[tsr] + ((t0 + row) * H + h) * kHeadDim + ch * 8 : src[tsr];
-      cp_async16(sbase + dstoff[tsr] + row * 256 + (((ch ^ (row & 7))) << 4), s, ok ? 16 : 0);
+      cp_async16(sbase + dstoff[tsr] + row * 256 + ((ch ^ (row & 7)) << 4), s, ok ? 16 : 0);
     }
     cp_async_commit();
   }
@@ -140,21 +151,19 @@ __global__ void __launch_bounds__(256, 1) kda_chunk_kernel(ChunkParams p) {
   cp_async_wait<0>();
   __syncthreads();
 
-  // ---- per-token inverse norms of q and k (warp per token) ----
+  // ---- S1: per-token inverse norms of q and k (warp per token) ----
   float* sRq = reinterpret_cast<float*>(smem + kCsRq);
   float* sRk = reinterpret_cast<float*>(smem + kCsRk);
   for (int t = warp; t < kChunk; t += 8) {
     float rq = 1.0f, rk = 1.0f;
     if (p.l2norm) {
-      float sq = 0.f, sk = 0.f;
-      int c = lane * 4;
-      uint32_t off = swz128(t, c);
-      uint2 qv = *reinterpret_cast<const uint2*>(smem + kCsQ + off);
-      uint2 kv = *reinterpret_cast<const uint2*>(smem + kCsK + off);
-      float2 a0 = unpack_bf16(qv.x), a1 = unpack_bf16(qv.y);
-      float2 b0 = unpack_bf16(kv.x), b1 = unpack_bf16(kv.y);
-      sq = a0.x * a0.x + a0.y * a0.y + a1.x * a1.x + a1.y * a1.y;
-      sk = b0.x * b0.x + b0.y * b0.y + b1.x * b1.x + b1.y * b1.y;
+      const uint32_t off = swz128(t, lane * 4);
+      const uint2 qv = *reinterpret_cast<const uint2*>(smem + kCsQ + off);
+      const uint2 kv = *reinterpret_cast<const uint2*>(smem + kCsK + off);
+      const float2 a0 = unpack_bf16(qv.x), a1 = unpack_bf16(qv.y);
+      const float2 b0 = unpack_bf16(kv.x), b1 = unpack_bf16(kv.y);
+      float sq = a0.x * a0.x + a0.y * a0.y + a1.x * a1.x + a1.y * a1.y;
+      float sk = b0.x * b0.x + b0.y * b0.y + b1.x * b1.x + b1.y * b1.y;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         sq += __shfl_xor_sync(0xffffffffu, sq, o);
@@ -166,114 +175,138 @@ __global__ void __launch_bounds__(256, 1) kda_chunk_kernel(ChunkParams p) {
     if (lane == 0) { sRq[t] = rq; sRk[t] = rk; }
   }
 
-  // ---- gate activation and per-sub-chunk decay products ----
-  // thread -> channel c, sub-chunks rb0 and rb0 + 2
-  const int c = tid & 127;
-  const int rb0 = tid >> 7;
-  float d[2][kSub];
+  // ---- S2: gate activation, per-token decays d (registers), sub-chunk products ----
+  // thread -> sub-chunk rb, channel pair (c0, c0 + 1)
+  const int rb = tid >> 6;
+  const int c0 = 2 * (tid & 63);
   float* sD = reinterpret_cast<float*>(smem + kCsD);
   float* sXm = reinterpret_cast<float*>(smem + kCsXm);
   float* sYm = reinterpret_cast<float*>(smem + kCsYm);
+  float* sFa = reinterpret_cast<float*>(smem + kCsFa);
+  float d0[kSub], d1[kSub];
   {
-    const float dtb = p.dt_bias ? p.dt_bias[h * kHeadDim + c] : 0.0f;
+    const float2 dtb = p.dt_bias ? *reinterpret_cast<const float2*>(p.dt_bias + h * kHeadDim + c0)
+                                 : make_float2(0.f, 0.f);
     const float amul = p.A_log ? expf(p.A_log[h]) : 1.0f;
+    float D0 = 1.f, D1 = 1.f, xm0 = 1.f, xm1 = 1.f, ym0 = 1.f, ym1 = 1.f;
 #pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      const int rb = rb0 + 2 * b;
-      float D = 1.f, xm = 1.f, ym = 1.f;
+    for (int j = 0; j < kSub; ++j) {
+      const int t = rb * kSub + j;
+      const float2 gz = unpack_bf16(u32_at(smem + kCsG, swz128(t, c0)));
+      float e0 = gate_decay(gz.x + dtb.x, amul, p.lower_bound, p.gate_unsafe);
+      float e1 = gate_decay(gz.y + dtb.y, amul, p.lower_bound, p.gate_unsafe);
+      if (t >= L) { e0 = 1.f; e1 = 1.f; }
+      d0[j] = e0;
+      d1[j] = e1;
+      D0 *= e0;
+      D1 *= e1;
+      if (j < 8) {
+        xm0 *= fmaxf(e0, kDiagDecayFloor);
+        xm1 *= fmaxf(e1, kDiagDecayFloor);
+      } else {
+        ym0 *= fmaxf(e0, kDiagDecayFloor);
+        ym1 *= fmaxf(e1, kDiagDecayFloor);
+      }
+    }
+    *reinterpret_cast<float2*>(sD + rb * 128 + c0) = make_float2(D0, D1);
+    *reinterpret_cast<float2*>(sXm + rb * 128 + c0) = make_float2(xm0, xm1);
+    *reinterpret_cast<float2*>(sYm + rb * 128 + c0) = make_float2(ym0, ym1);
+  }
+  __syncthreads();
+
+  // ---- S3: operands (thread = sub-chunk rb, channel pair c0, c0 + 1) ----
+  //  exact, chunk relative:     gamma_j = prod_{s<=j} d_s  -> beta K gamma (smem), q gamma (ws)
+  //  exact, chunk-end relative: gamma_C / gamma_j           -> k_hat (ws)
+  //  clamped, midpoint relative: xr_j = e^{lam_j - lam_7}, yr_j = 1 / xr_j -> A / P operands
+  {
+    float pre0 = 1.f, pre1 = 1.f, suf0 = 1.f, suf1 = 1.f;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const float2 Ds = *reinterpret_cast<const float2*>(sD + s * 128 + c0);
+      if (s < rb) { pre0 *= Ds.x; pre1 *= Ds.y; }
+      if (s > rb) { suf0 *= Ds.x; suf1 *= Ds.y; }
+    }
+    if (rb == 0) {  // left factors of the off-diagonal sub-blocks (r, cb), cb < r
+#pragma unroll
+      for (int r = 1; r < 4; ++r)
+#pragma unroll
+        for (int cb = 0; cb < r; ++cb) {
+          float e0 = sXm[r * 128 + c0], e1 = sXm[r * 128 + c0 + 1];
+          for (int s = cb + 1; s < r; ++s) {
+            e0 *= sXm[s * 128 + c0] * sYm[s * 128 + c0];
+            e1 *= sXm[s * 128 + c0 + 1] * sYm[s * 128 + c0 + 1];
+          }
+          const int idx = r * (r - 1) / 2 + cb;
+          *reinterpret_cast<float2*>(sFa + idx * 128 + c0) = make_float2(e0, e1);
+        }
+    }
+    const float ixm0 = __frcp_rn(sXm[rb * 128 + c0]), ixm1 = __frcp_rn(sXm[rb * 128 + c0 + 1]);
+    const float iym0 = __frcp_rn(sYm[rb * 128 + c0]), iym1 = __frcp_rn(sYm[rb * 128 + c0 + 1]);
+    __half2* gQg = reinterpret_cast<__half2*>(ws + kSlotQg);
+    __half2* gKh = reinterpret_cast<__half2*>(ws + kSlotKh);
+    // backward over the sub-chunk (reads the raw k)
+    {
+      float y0 = suf0, y1 = suf1, yc0 = 1.f, yc1 = 1.f, p70 = 1.f, p71 = 1.f;
+#pragma unroll
+      for (int j = kSub - 1; j >= 0; --j) {
+        const int t = rb * kSub + j;
+        const uint32_t off = swz128(t, c0);
+        const float rk = sRk[t];
+        const float2 kr = unpack_bf16(u32_at(smem + kCsK, off));
+        const float k0 = kr.x * rk, k1 = kr.y * rk;
+        const float yr0 = j >= 8 ? yc0 * iym0 : p70;
+        const float yr1 = j >= 8 ? yc1 * iym1 : p71;
+        u32_at(smem + kCsKy, off) = pack_bf16(k0 * yr0, k1 * yr1);
+        gKh[(t * kHeadDim + c0) >> 1] = __floats2half2_rn(k0 * y0, k1 * y1);
+        const float dc0 = fmaxf(d0[j], kDiagDecayFloor), dc1 = fmaxf(d1[j], kDiagDecayFloor);
+        y0 *= d0[j];
+        y1 *= d1[j];
+        yc0 *= dc0;
+        yc1 *= dc1;
+        if (j <= 7) { p70 *= dc0; p71 *= dc1; }
+      }
+    }
+    // forward over the sub-chunk (overwrites raw q, k, g, v)
+    {
+      float x0 = pre0, x1 = pre1, xc0 = 1.f, xc1 = 1.f, q80 = 1.f, q81 = 1.f;
 #pragma unroll
       for (int j = 0; j < kSub; ++j) {
         const int t = rb * kSub + j;
-        const float z = ld_tile128(smem + kCsKg, t, c) + dtb;
-        float a;
-        if (p.gate_unsafe) {
-          float e = ex2(-fabsf(z) * kLog2e);
-          a = -amul * (fmaxf(z, 0.0f) + log1p_small(e));
-        } else {
-          a = p.lower_bound * sigmoidf_fast(amul * z);
-        }
-        float dj = t < L ? ex2(a * kLog2e) : 1.0f;
-        d[b][j] = dj;
-        D *= dj;
-        if (j < 8) xm *= fmaxf(dj, kDiagDecayFloor); else ym *= fmaxf(dj, kDiagDecayFloor);
+        const uint32_t off = swz128(t, c0);
+        const float dc0 = fmaxf(d0[j], kDiagDecayFloor), dc1 = fmaxf(d1[j], kDiagDecayFloor);
+        x0 *= d0[j];
+        x1 *= d1[j];
+        if (j < 8) { xc0 *= dc0; xc1 *= dc1; } else { q80 *= dc0; q81 *= dc1; }
+        const float xr0 = j < 8 ? xc0 * ixm0 : q80;
+        const float xr1 = j < 8 ? xc1 * ixm1 : q81;
+        const float rk = sRk[t], rq = sRq[t], bt = sBeta[t];
+        const float2 kr = unpack_bf16(u32_at(smem + kCsK, off));
+        const float2 qr = unpack_bf16(u32_at(smem + kCsQ, off));
+        const float2 vr = unpack_bf16(u32_at(smem + kCsV, off));
+        const float k0 = kr.x * rk, k1 = kr.y * rk, q0 = qr.x * rq, q1 = qr.y * rq;
+        u32_at(smem + kCsK, off) = pack_bf16(k0 * xr0, k1 * xr1);
+        u32_at(smem + kCsQ, off) = pack_bf16(q0 * xr0, q1 * xr1);
+        u32_at(smem + kCsG, off) = pack_f16(bt * k0 * x0, bt * k1 * x1);
+        u32_at(smem + kCsV, off) = pack_f16(bt * vr.x, bt * vr.y);
+        gQg[(t * kHeadDim + c0) >> 1] = __floats2half2_rn(q0 * x0, q1 * x1);
       }
-      sD[rb * 128 + c] = D;
-      sXm[rb * 128 + c] = xm;
-      sYm[rb * 128 + c] = ym;
+    }
+    if (rb == 0) {
+      float g0 = 1.f, g1 = 1.f;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) { g0 *= sD[s * 128 + c0]; g1 *= sD[s * 128 + c0 + 1]; }
+      *reinterpret_cast<float2*>(reinterpret_cast<float*>(ws + kSlotGc) + c0) = make_float2(g0, g1);
     }
   }
   __syncthreads();
 
-  // ---- operands ----
-  //  exact, chunk relative:   gamma_j = prod_{s<=j} d_s   -> K gamma (smem), q gamma (ws)
-  //  exact, chunk-end rel.:   gamma_C / gamma_j            -> k_hat (ws)
-  //  clamped, midpoint rel.:  xr_j = e^{lam_j - lam_7}, yr_j = 1 / xr_j  -> A / P operands
-  {
-    __half* gQg = reinterpret_cast<__half*>(ws + kSlotQg);
-    __half* gKh = reinterpret_cast<__half*>(ws + kSlotKh);
-#pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      const int rb = rb0 + 2 * b;
-      float pre = 1.f, suf = 1.f;
-      for (int s = 0; s < 4; ++s) {
-        float Ds = sD[s * 128 + c];
-        if (s < rb) pre *= Ds;
-        if (s > rb) suf *= Ds;
-      }
-      float xe[kSub], ye[kSub], mr[kSub];
-      {
-        float x = pre;
-#pragma unroll
-        for (int jj = 0; jj < kSub; ++jj) { x *= d[b][jj]; xe[jj] = x; }
-        float y = suf;
-#pragma unroll
-        for (int jj = kSub - 1; jj >= 0; --jj) { ye[jj] = y; y *= d[b][jj]; }
-        // mr_j = prod_{s=j+1..7} dc_s for j <= 7, prod_{s=8..j} dc_s for j >= 8
-        float m = 1.f;
-#pragma unroll
-        for (int jj = 7; jj >= 0; --jj) { mr[jj] = m; m *= fmaxf(d[b][jj], kDiagDecayFloor); }
-        m = 1.f;
-#pragma unroll
-        for (int jj = 8; jj < kSub; ++jj) { m *= fmaxf(d[b][jj], kDiagDecayFloor); mr[jj] = m; }
-      }
-#pragma unroll
-      for (int jj = 0; jj < kSub; ++jj) {
-        const int t = rb * kSub + jj;
-        const float kh = ld_tile128(smem + kCsK, t, c) * sRk[t];
-        const float qh = ld_tile128(smem + kCsQ, t, c) * sRq[t];
-        const float inv = __frcp_rn(mr[jj]);
-        const float xr = jj < 8 ? inv : mr[jj];
-        const float yr = jj < 8 ? mr[jj] : inv;
-        st_tile128(smem + kCsK, t, c, kh * xr);
-        st_tile128(smem + kCsQ, t, c, qh * xr);
-        st_tile128(smem + kCsKy, t, c, kh * yr);
-        st_tile128_f16(smem + kCsKg, t, c, kh * xe[jj]);
-        st_tile128_f16(smem + kCsV, t, c, ld_tile128(smem + kCsV, t, c));
-        gQg[t * kHeadDim + c] = __float2half_rn(qh * xe[jj]);
-        gKh[t * kHeadDim + c] = __float2half_rn(kh * ye[jj]);
-      }
-    }
-    if (rb0 == 0) {
-      float gc = sD[c] * sD[128 + c] * sD[256 + c] * sD[384 + c];
-      reinterpret_cast<float*>(ws + kSlotGc)[c] = gc;
-    }
-  }
-  __syncthreads();
-
-  const uint32_t sbase = smem_u32(smem);
+  // ---- S4: A (warps 0-3) and P (warps 4-7), row sub-block r, column sub-blocks cb <= r ----
   const int g = lane >> 2, q4 = lane & 3;
-  float* sA = reinterpret_cast<float*>(smem + kCsA);
-  float* sInv = reinterpret_cast<float*>(smem + kCsInv);
-
-  // ---- A (warps 0-3) and P (warps 4-7): row sub-block r, column sub-blocks c <= r ----
-  // Diagonal sub-blocks: the midpoint-relative operands multiply directly.
-  // Off-diagonal (cb < r): the left operands get the per-channel factor
-  //   xm[r] * prod_{cb<s<r} xm[s] ym[s]   (-> relative to the end of sub-chunk cb)
-  // and the right operands ym[cb] (-> relative to the end of sub-chunk cb), so
-  // each side is <= |k| and underflows only where the pair factor itself does.
+  float accA[4][2][4];
   {
     const int mat = warp >> 2, r = warp & 3;
     __half* gP = reinterpret_cast<__half*>(ws + kSlotP);
+#pragma unroll
     for (int cb = 0; cb < 4; ++cb) {
       float acc[2][4];
 #pragma unroll
@@ -282,23 +315,20 @@ __global__ void __launch_bounds__(256, 1) kda_chunk_kernel(ChunkParams p) {
         for (int e = 0; e < 4; ++e) acc[a][e] = 0.f;
       const bool active = cb <= r;
       if (active) {
+        const int fidx = r * (r - 1) / 2 + cb;
 #pragma unroll 2
         for (int kk = 0; kk < 8; ++kk) {
-          uint32_t a[4];
+          uint32_t a[4], b[4];
           lda_128(a, sbase + (mat ? kCsQ : kCsK), 16 * r, 16 * kk, lane);
-          uint32_t b[4];
           ldb_nk_128(b, sbase + kCsKy, 16 * cb, 16 * kk, lane);
           if (cb < r) {
             const int ch = 16 * kk + 2 * q4;
-            const int chs[4] = {ch, ch + 1, ch + 8, ch + 9};
-            float fa[4], fb[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              float e = sXm[r * 128 + chs[u]];
-              for (int s = cb + 1; s < r; ++s) e *= sXm[s * 128 + chs[u]] * sYm[s * 128 + chs[u]];
-              fa[u] = e;
-              fb[u] = sYm[cb * 128 + chs[u]];
-            }
+            const float2 fa01 = *reinterpret_cast<const float2*>(sFa + fidx * 128 + ch);
+            const float2 fa89 = *reinterpret_cast<const float2*>(sFa + fidx * 128 + ch + 8);
+            const float2 fb01 = *reinterpret_cast<const float2*>(sYm + cb * 128 + ch);
+            const float2 fb89 = *reinterpret_cast<const float2*>(sYm + cb * 128 + ch + 8);
+            const float fa[4] = {fa01.x, fa01.y, fa89.x, fa89.y};
+            const float fb[4] = {fb01.x, fb01.y, fb89.x, fb89.y};
             scale_afrag(a, fa);
             scale_bfrag(b[0], b[1], fb);
             scale_bfrag(b[2], b[3], fb);
@@ -313,13 +343,11 @@ __global__ void __launch_bounds__(256, 1) kda_chunk_kernel(ChunkParams p) {
         for (int hf = 0; hf < 2; ++hf) {
           const int row = 16 * r + g + 8 * hf;
           const int col = 16 * cb + 8 * nt + 2 * q4;
-          float v0 = acc[nt][2 * hf], v1 = acc[nt][2 * hf + 1];
+          const float v0 = acc[nt][2 * hf], v1 = acc[nt][2 * hf + 1];
           if (mat == 0) {
-            const bool k0 = active && (cb < r || col < row);
-            const bool k1 = active && (cb < r || col + 1 < row);
             const float bt = sBeta[row];
-            sA[row * 64 + col] = k0 ? v0 * bt : 0.f;
-            sA[row * 64 + col + 1] = k1 ? v1 * bt : 0.f;
+            accA[cb][nt][2 * hf] = (active && (cb < r || col < row)) ? v0 * bt : 0.f;
+            accA[cb][nt][2 * hf + 1] = (active && (cb < r || col + 1 < row)) ? v1 * bt : 0.f;
           } else {
             const bool k0 = active && (cb < r || col <= row);
             const bool k1 = active && (cb < r || col + 1 <= row);
@@ -330,86 +358,118 @@ __global__ void __launch_bounds__(256, 1) kda_chunk_kernel(ChunkParams p) {
       }
     }
   }
+  __syncthreads();  // the q / k operand tiles are dead from here on
+
+  // ---- S5: A as an fp16 operand tile and its fp32 diagonal sub-blocks ----
+  float* sAd = reinterpret_cast<float*>(smem + kCsAd);
+  if (warp < 4) {
+    const int r = warp;
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int row = 16 * r + g + 8 * hf;
+          const int col = 16 * cb + 8 * nt + 2 * q4;
+          const float v0 = accA[cb][nt][2 * hf], v1 = accA[cb][nt][2 * hf + 1];
+          u32_at(smem + kCsA16, swz64(row, col)) = pack_f16(v0, v1);
+          if (cb == r) {
+            sAd[r * 256 + (row - 16 * r) * 16 + (col - 16 * r)] = v0;
+            sAd[r * 256 + (row - 16 * r) * 16 + (col - 16 * r) + 1] = v1;
+          }
+        }
+  }
   __syncthreads();
 
-  // ---- solve: inverses of the four 16x16 unit-lower diagonal blocks ----
+  // ---- S6: X_r = (I + A_rr)^-1 by forward substitution (warp r, lane = column) ----
   if (warp < 4 && lane < 16) {
-    const int j = lane, o = 16 * warp;
+    const int j = lane;
+    const float* Ad = sAd + warp * 256;
     float x[kSub];
 #pragma unroll
     for (int ii = 0; ii < kSub; ++ii) {
       float acc = 0.f;
 #pragma unroll
-      for (int s = 0; s < ii; ++s) acc += sA[(o + ii) * 64 + o + s] * x[s];
+      for (int s = 0; s < ii; ++s) acc += Ad[ii * 16 + s] * x[s];
       x[ii] = (ii == j) ? 1.f : (ii < j ? 0.f : -acc);
     }
 #pragma unroll
-    for (int ii = 0; ii < kSub; ++ii) sInv[(o + ii) * 64 + o + j] = x[ii];
-  }
-  __syncthreads();
-  // ---- block merges: Inv_rc = -X_r * sum_{s=c}^{r-1} A_rs Inv_sc, by distance r-c ----
-  {
-    float* sM = reinterpret_cast<float*>(smem + kCsM);
-    for (int dist = 1; dist < 4; ++dist) {
-      const int cnt = 4 - dist;
-      for (int idx = tid; idx < cnt * 256; idx += 256) {
-        const int tile = idx >> 8, e = idx & 255, ii = e >> 4, jj = e & 15;
-        const int r = dist + tile, cb = r - dist;
-        float acc = 0.f;
-        for (int s = cb; s < r; ++s)
-#pragma unroll
-          for (int u = 0; u < 16; ++u)
-            acc += sA[(16 * r + ii) * 64 + 16 * s + u] * sInv[(16 * s + u) * 64 + 16 * cb + jj];
-        sM[tile * 256 + e] = acc;
-      }
-      __syncthreads();
-      for (int idx = tid; idx < cnt * 256; idx += 256) {
-        const int tile = idx >> 8, e = idx & 255, ii = e >> 4, jj = e & 15;
-        const int r = dist + tile, cb = r - dist;
-        float acc = 0.f;
-#pragma unroll
-        for (int u = 0; u < 16; ++u)
-          acc += sInv[(16 * r + ii) * 64 + 16 * r + u] * sM[tile * 256 + u * 16 + jj];
-        sInv[(16 * r + ii) * 64 + 16 * cb + jj] = -acc;
-      }
-      __syncthreads();
-    }
-  }
-  // ---- T = Inv Diag(beta) as an fp16 operand ----
-  for (int idx = tid; idx < 64 * 64; idx += 256) {
-    const int ii = idx >> 6, jj = idx & 63;
-    const float val = jj <= ii ? sInv[ii * 64 + jj] * sBeta[jj] : 0.f;
-    *reinterpret_cast<__half*>(smem + kCsT + swz64(ii, jj)) = __float2half_rn(val);
+    for (int ii = 0; ii < kSub; ++ii)
+      *reinterpret_cast<__half*>(smem + kCsX + swz64(ii, 16 * warp + j)) = __float2half_rn(x[ii]);
   }
   __syncthreads();
 
-  // ---- W = T (K gamma) (warps 0-3) and U = T V (warps 4-7), row sub-block r, fp16 ----
+  // ---- S7: [W | U] rows of sub-chunk r = X_r (B_r - sum_{c<r} A_rc Y_c), in place ----
+  // warp -> 32 columns of B = [beta K gamma | beta V]; private, so only __syncwarp.
   {
-    const int mat = warp >> 2, r = warp & 3;
-    float acc[16][4];
+    const int mat = warp >> 2, cbase = 32 * (warp & 3);
+    unsigned char* buf = smem + (mat ? kCsV : kCsG);
+    const uint32_t bufa = sbase + (mat ? kCsV : kCsG);
 #pragma unroll
-    for (int a = 0; a < 16; ++a)
+    for (int r = 0; r < 4; ++r) {
+      if (r > 0) {
+        float acc[4][4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[a][e] = 0.f;
-    for (int cb = 0; cb <= r; ++cb) {
-      uint32_t a[4];
-      lda_64(a, sbase + kCsT, 16 * r, 16 * cb, lane);
+        for (int a = 0; a < 4; ++a)
 #pragma unroll
-      for (int np = 0; np < 8; ++np) {
-        uint32_t b[4];
-        ldb_kn_128(b, sbase + (mat ? kCsV : kCsKg), 16 * np, 16 * cb, lane);
-        mma_f16(acc[2 * np], a, b[0], b[1]);
-        mma_f16(acc[2 * np + 1], a, b[2], b[3]);
+          for (int e = 0; e < 4; ++e) acc[a][e] = 0.f;
+#pragma unroll
+        for (int c = 0; c < r; ++c) {
+          uint32_t a[4];
+          lda_64(a, sbase + kCsA16, 16 * r, 16 * c, lane);
+#pragma unroll
+          for (int np = 0; np < 2; ++np) {
+            uint32_t b[4];
+            ldb_kn_128(b, bufa, cbase + 16 * np, 16 * c, lane);
+            mma_f16(acc[2 * np], a, b[0], b[1]);
+            mma_f16(acc[2 * np + 1], a, b[2], b[3]);
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const uint32_t off = swz128(16 * r + g + 8 * hf, cbase + 8 * nt + 2 * q4);
+            const float2 bv = unpack_f16(u32_at(buf, off));
+            u32_at(buf, off) = pack_f16(bv.x - acc[nt][2 * hf], bv.y - acc[nt][2 * hf + 1]);
+          }
+        __syncwarp();
       }
-    }
-    __half* out = reinterpret_cast<__half*>(ws + (mat ? kSlotU : kSlotW));
+      float y[4][4];
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      const int row = 16 * r + g, col = 8 * nt + 2 * q4;
-      *reinterpret_cast<uint32_t*>(out + row * kHeadDim + col) = pack_f16(acc[nt][0], acc[nt][1]);
-      *reinterpret_cast<uint32_t*>(out + (row + 8) * kHeadDim + col) =
-          pack_f16(acc[nt][2], acc[nt][3]);
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) y[a][e] = 0.f;
+      uint32_t a[4];
+      lda_64(a, sbase + kCsX, 0, 16 * r, lane);
+#pragma unroll
+      for (int np = 0; np < 2; ++np) {
+        uint32_t b[4];
+        ldb_kn_128(b, bufa, cbase + 16 * np, 16 * r, lane);
+        mma_f16(y[2 * np], a, b[0], b[1]);
+        mma_f16(y[2 * np + 1], a, b[2], b[3]);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const uint32_t off = swz128(16 * r + g + 8 * hf, cbase + 8 * nt + 2 * q4);
+          u32_at(buf, off) = pack_f16(y[nt][2 * hf], y[nt][2 * hf + 1]);
+        }
+      __syncwarp();
     }
+  }
+  __syncthreads();
+
+  // ---- S8: W and U to the workspace (16-byte stores) ----
+#pragma unroll 4
+  for (int idx = tid; idx < 2048; idx += 256) {
+    const int m = idx >> 10, row = (idx >> 4) & 63, ch = idx & 15;
+    const uint4 val = *reinterpret_cast<const uint4*>(smem + (m ? kCsV : kCsG) + row * 256 +
+                                                       ((ch ^ (row & 7)) << 4));
+    *reinterpret_cast<uint4*>(ws + (m ? kSlotU : kSlotW) + row * 256 + ch * 16) = val;
   }
 }
 
