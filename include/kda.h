@@ -45,6 +45,7 @@ extern "C" {
 #define KDA_ERR_WORKSPACE 10      /* workspace NULL, misaligned or too small */
 #define KDA_ERR_LAUNCH 11         /* a CUDA launch failed (cudaGetLastError) */
 #define KDA_ERR_NOALLOC_LIMIT 12  /* kda_fwd_noalloc: problem needs more scratch than built in */
+#define KDA_ERR_DEVICE_TIMEOUT 13 /* (device status) a kernel gave up waiting for its operands */
 
 /* ---- flags ---- */
 #define KDA_GATE_SAFE 0x1u   /* lower_bound * sigmoid(exp(A_log) * (g + dt_bias)) */
@@ -149,6 +150,15 @@ int kda_fwd_launches(const kda_fwd_args *args);
  */
 #define KDA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 int kda_fwd_noalloc(const kda_fwd_args *args, void *stream);
+
+/*
+ * Device-side status of the kernels on the current device: KDA_OK, or
+ * KDA_ERR_DEVICE_TIMEOUT if a CTA gave up waiting (bounded wait, about a
+ * second of SM cycles) for its asynchronous operand copies and returned
+ * without finishing its work.  Sticky until read with clear != 0.  Reads
+ * device memory synchronously; returns -1 if that read fails.
+ */
+int kda_get_status(int clear);
 
 /* Human-readable text of a status code (static storage). */
 const char *kda_error_string(int code);

@@ -213,6 +213,8 @@ extern "C" const char* kda_error_string(int code) {
     case KDA_ERR_ALIGNMENT: return "tensor pointers must be 16-byte aligned";
     case KDA_ERR_WORKSPACE: return "workspace missing, not 256-byte aligned, or too small";
     case KDA_ERR_LAUNCH: return "CUDA launch failed";
+    case KDA_ERR_DEVICE_TIMEOUT:
+      return "a kernel gave up waiting for its operand copies (device status)";
     case KDA_ERR_NOALLOC_LIMIT:
       return "problem needs more scratch than kda_fwd_noalloc's built-in buffer holds";
     default: return "unknown status code";

@@ -27,15 +27,19 @@ constexpr float kLog2e = 1.4426950408889634f;
 // ---- per-(chunk, head) workspace slot ----
 // Intermediates written by the chunk kernel and read by the state kernel, all
 // fp16 (11-bit significand: these feed the recurrent state, where bf16's 8
-// bits cost more accuracy than the tolerance allows).
-constexpr int kSlotW = 0;                       // fp16 [64][128]  W = T (K * gamma)
-constexpr int kSlotU = kSlotW + 64 * 128 * 2;   // fp16 [64][128]  U = T V
-constexpr int kSlotQg = kSlotU + 64 * 128 * 2;  // fp16 [64][128]  q * gamma
-constexpr int kSlotKh = kSlotQg + 64 * 128 * 2; // fp16 [64][128]  k * gamma_C / gamma
-constexpr int kSlotP = kSlotKh + 64 * 128 * 2;  // fp16 [64][64]   intra read-out matrix
-constexpr int kSlotGc = kSlotP + 64 * 64 * 2;   // fp32 [128]      gamma_C (chunk decay)
-constexpr int kSlotBytes = kSlotGc + 128 * 4;   // 74240 (multiple of 256)
+// bits cost more accuracy than the tolerance allows).  Each block is stored
+// as the exact shared-memory image the state kernel uses (swizzled tiles), so
+// that a chunk arrives with two flat bulk copies: bytes [0, kSlotUt) and the
+// consumer's 4 KB U^T tile.
+constexpr int kSlotW = 0;                       // tile128 image [64 t][128 k]  W = T (K gamma)
+constexpr int kSlotQg = kSlotW + 64 * 128 * 2;  // tile128 image [64 t][128 k]  q gamma
+constexpr int kSlotKh = kSlotQg + 64 * 128 * 2; // tile128 image [64 t][128 k]  k gamma_C / gamma
+constexpr int kSlotP = kSlotKh + 64 * 128 * 2;  // tile64 image  [64 t][64 s]   intra read-out
+constexpr int kSlotGc = kSlotP + 64 * 64 * 2;   // fp32 [128]                   gamma_C
+constexpr int kSlotUt = kSlotGc + 128 * 4;      // 4 x tile64 image [32 v][64 t]  U^T per value tile
+constexpr int kSlotBytes = kSlotUt + 4 * 32 * 64 * 2;  // 74240 (multiple of 256)
 static_assert(kSlotBytes % 256 == 0, "slot must keep 256-byte alignment");
+static_assert(kSlotUt % 16 == 0, "bulk copies need 16-byte sizes and offsets");
 
 // ---- swizzled shared-memory addressing ----
 __device__ __forceinline__ uint32_t swz128(int row, int col) {  // byte offset
@@ -153,6 +157,47 @@ __device__ __forceinline__ void ldb_kn_128(uint32_t (&b)[4], uint32_t base, int 
                                            int lane) {
   int mi = lane >> 3;
   ldsm_x4_t(b, base + swz128(k0 + ((mi & 1) << 3) + (lane & 7), n0 + ((mi >> 1) << 3)));
+}
+
+// ---- mbarrier + bulk-copy (TMA engine) primitives ----
+__device__ __forceinline__ void mbar_init(uint32_t addr, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(addr), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t addr, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(addr), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase with the given parity to complete; gives up (returns
+// false) after about 2^31 SM cycles instead of spinning forever.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t addr, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(addr, parity))
+    if (clock64() - t0 > (1LL << 31)) return false;
+  return true;
+}
+// Flat global -> shared copy by the bulk-copy engine, completing `bytes`
+// transaction bytes on the mbarrier.  Addresses and size: multiples of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(mbar)
+      : "memory");
+}
+// Order this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
 
 }  // namespace kda

@@ -1,5 +1,5 @@
 // Recurrent stage of the KDA forward pass: one CTA per (sequence, head,
-// 64-wide value tile), walking the chunks of its sequence in order.
+// 32-wide value tile), walking the chunks of its sequence in order.
 //
 // Per chunk, with S the state (rows = value index, columns = key index) at
 // the chunk start and the intra-chunk quantities of the workspace slot:
@@ -7,62 +7,65 @@
 //   O     = scale (Q_gamma S^T + P U_new)  (inter + intra read-out, fused as in
 //                                          the chunk_o stage of the fla code map)
 //   S     = S Diag(gamma_C) + U_new^T K_hat   (chunk_delta_h state update)
-// Each warp owns 16 value rows of S in mma accumulator registers (fp32); the
-// accumulator layout is reused directly as the fp16 left operand of the next
-// product, so the sequential chain never leaves the register file.  All
-// operands are fp16 (11-bit significand) with fp32 accumulation; the state
-// itself stays fp32.
+//
+// Work split: the CTA holds two "slabs" of 16 value rows; each slab is worked
+// by four warps.  Warp q of a slab computes U_new and O for tokens
+// 16q..16q+15 and owns key columns 32q..32q+31 of S (fp32, in mma
+// accumulator registers).  Per chunk the slab's warps exchange S and U_new
+// as fp16 operand tiles in shared memory (double-buffered by chunk parity),
+// so the sequential chain per chunk is 2 x 16 mma.sync per warp plus one
+// slab barrier and two CTA barriers.  Operands are fp16 (11-bit
+// significand) with fp32 accumulation; the state itself stays fp32.
 #include "kda_common.cuh"
 #include "kda_kernels.cuh"
 
 namespace kda {
 
-constexpr int kStW = 0;
-constexpr int kStQg = 16384;
-constexpr int kStKh = 32768;
-constexpr int kStP = 49152;     // tile64 [t][s]
-constexpr int kStU = 57344;     // tile64 [t][v_local]
-constexpr int kStGc = 65536;    // fp32 [128]
-constexpr int kStBuf = 66048;   // one chunk's operands
-constexpr int kStO = 2 * kStBuf;  // tile64 [t][v_local] output staging
-constexpr int kStateSmem = kStO + 8192;
-constexpr int kVTile = 64;
+// one chunk's operands (per buffer): the workspace slot image [0, kSlotUt)
+// followed by this CTA's U^T tile
+constexpr int kStW = kSlotW;     // tile128 [64 t][128 k] fp16
+constexpr int kStQg = kSlotQg;   // tile128 [64 t][128 k] fp16
+constexpr int kStKh = kSlotKh;   // tile128 [64 t][128 k] fp16
+constexpr int kStP = kSlotP;     // tile64 [64 t][64 s] fp16
+constexpr int kStGc = kSlotGc;   // fp32 [128]
+constexpr int kStUt = kSlotUt;   // tile64 [32 v][64 t] fp16
+constexpr int kStBuf = kSlotUt + 4096;
+constexpr int kStages = 3;                     // operand pipeline depth
+// exchange tiles, output staging, barriers
+constexpr int kStS = kStages * kStBuf;         // [2 slab][2 parity] tile128 [16][128] fp16
+constexpr int kStUn = kStS + 4 * 4096;         // [2 slab][2 parity] tile64 [16][64] fp16
+constexpr int kStO = kStUn + 4 * 2048;         // [8 warps][16 t][16 v] bf16 output staging
+constexpr int kStBar = kStO + 8 * 512;         // full[kStages], empty[kStages] mbarriers
+constexpr int kStAbort = kStBar + 16 * kStages;
+constexpr int kStateSmem = kStAbort + 16;
+constexpr int kVTile = 32;
 
-__device__ __forceinline__ void load_chunk_operands(unsigned char* buf, const unsigned char* src,
-                                                    int v0, int tid) {
-  const uint32_t dbase = smem_u32(buf);
-  for (int idx = tid; idx < 4128; idx += 128) {
-    uint32_t dst;
-    const unsigned char* s;
-    if (idx < 3072) {
-      const int m = idx >> 10, row = (idx >> 4) & 63, ch = idx & 15;
-      const int soff = m == 0 ? kSlotW : (m == 1 ? kSlotQg : kSlotKh);
-      dst = dbase + m * 16384 + row * 256 + ((ch ^ (row & 7)) << 4);
-      s = src + soff + row * 256 + ch * 16;
-    } else if (idx < 3584) {
-      const int e = idx - 3072, row = e >> 3, ch = e & 7;
-      dst = dbase + kStP + row * 128 + ((ch ^ (row & 7)) << 4);
-      s = src + kSlotP + row * 128 + ch * 16;
-    } else if (idx < 4096) {
-      const int e = idx - 3584, row = e >> 3, ch = e & 7;
-      dst = dbase + kStU + row * 128 + ((ch ^ (row & 7)) << 4);
-      s = src + kSlotU + row * 256 + ((v0 >> 3) + ch) * 16;
-    } else {
-      const int e = idx - 4096;
-      dst = dbase + kStGc + e * 16;
-      s = src + kSlotGc + e * 16;
-    }
-    cp_async16(dst, s, 16);
-  }
+// Sticky device status: set to KDA_ERR_DEVICE_TIMEOUT (13) by a CTA that gave
+// up waiting for its operand copies; read and cleared by kda_get_status.
+__device__ int g_kda_status = 0;
+
+// One elected thread: bring chunk operands into a buffer with two bulk copies.
+__device__ __forceinline__ void issue_chunk_copy(uint32_t dbase, uint32_t bar,
+                                                 const unsigned char* slot, int vt) {
+  fence_proxy_async_smem();
+  mbar_expect_tx(bar, (uint32_t)kStBuf);
+  bulk_g2s(dbase, slot, (uint32_t)kSlotUt, bar);
+  bulk_g2s(dbase + kStUt, slot + kSlotUt + vt * 4096, 4096u, bar);
 }
 
-__global__ void __launch_bounds__(128, 1) kda_state_kernel(StateParams p) {
+__device__ __forceinline__ void slab_barrier(int slab) {
+  asm volatile("bar.sync %0, 128;\n" ::"r"(1 + slab));
+}
+
+__global__ void __launch_bounds__(256, 1) kda_state_kernel(StateParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, q4 = lane & 3;
+  const int slab = warp >> 2, qd = warp & 3;
   const int64_t H = p.H;
-  const int64_t unit = blockIdx.x >> 1;
-  const int v0 = (blockIdx.x & 1) * kVTile;
+  const int64_t unit = blockIdx.x >> 2;
+  const int vt = blockIdx.x & 3;
+  const int v0 = vt * kVTile;
   const int64_t n = unit / H;
   const int h = (int)(unit - n * H);
 
@@ -77,192 +80,235 @@ __global__ void __launch_bounds__(128, 1) kda_state_kernel(StateParams p) {
     slot0 = n * p.NT;
   }
   const int64_t nch = (len + kChunk - 1) / kChunk;
+  const uint32_t sb = smem_u32(smem);
+  const int vrow = v0 + 16 * slab + g;  // value rows vrow and vrow + 8
+  const int kc0 = 32 * qd;              // this warp's key columns kc0 .. kc0 + 31
+  const int64_t sbase = (n * H + h) * (int64_t)(kHeadDim * kHeadDim);
 
-  // ---- initial state into accumulator fragments ----
-  float s[16][4];
-  const int vr0 = v0 + 16 * warp + g;  // value rows vr0 and vr0 + 8
-  {
-    const int64_t sbase = (n * H + h) * (int64_t)(kHeadDim * kHeadDim);
+  // ---- initial state: s[nt] covers columns kc0 + 8 nt .. + 7 ----
+  float s[4][4];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int col = 8 * j + 2 * q4;
+  for (int nt = 0; nt < 4; ++nt) {
+    const int col = kc0 + 8 * nt + 2 * q4;
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      float x0 = 0.f, x1 = 0.f;
+      if (p.init) {
+        const int64_t off = sbase + (int64_t)(vrow + 8 * hf) * kHeadDim + col;
+        float2 f;
+        if (p.state_bf16)
+          f = unpack_bf16(*reinterpret_cast<const uint32_t*>(
+              reinterpret_cast<const uint16_t*>(p.init) + off));
+        else
+          f = *reinterpret_cast<const float2*>(reinterpret_cast<const float*>(p.init) + off);
+        x0 = f.x;
+        x1 = f.y;
+      }
+      s[nt][2 * hf] = x0;
+      s[nt][2 * hf + 1] = x1;
+    }
+  }
+  auto publish_state = [&](int par) {
+    unsigned char* t = smem + kStS + (slab * 2 + par) * 4096;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf)
+        *reinterpret_cast<uint32_t*>(t + swz128(g + 8 * hf, kc0 + 8 * nt + 2 * q4)) =
+            pack_f16(s[nt][2 * hf], s[nt][2 * hf + 1]);
+  };
+  publish_state(0);
+
+  auto slot_ptr = [&](int64_t ci) {
+    return p.ws + ((slot0 + ci) * H + h) * (int64_t)kSlotBytes;
+  };
+  const uint32_t full0 = sb + kStBar, empty0 = sb + kStBar + 8 * kStages;
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kStAbort);
+  if (tid == 0) {
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(full0 + 8 * st, 1);
+      mbar_init(empty0 + 8 * st, 8);  // one arrival per warp
+    }
+    *s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+  int64_t next_issue = 0, next_landed = 0;  // bookkeeping of thread 0 (the copy issuer)
+  if (tid == 0)
+    for (; next_issue < kStages && next_issue < nch; ++next_issue)
+      issue_chunk_copy(sb + next_issue * kStBuf, full0 + 8 * next_issue, slot_ptr(next_issue), vt);
+  // A timed-out wait sets the device status and switches the CTA to skip all
+  // further waits: it finishes with garbage but never hangs.
+  auto wait_or_abort = [&](uint32_t bar, uint32_t parity) {
+    if (*s_abort) return;
+    if (!mbar_wait_bounded(bar, parity)) {
+      atomicExch(&g_kda_status, 13);
+      *s_abort = 1;
+    }
+  };
+  unsigned char* stage_o = smem + kStO + warp * 512;
+
+  for (int64_t ci = 0; ci < nch; ++ci) {
+    const int st = (int)(ci % kStages);
+    const uint32_t ph = (uint32_t)((ci / kStages) & 1);
+    const int par = (int)(ci & 1);
+    const uint32_t bufa = sb + st * kStBuf;
+    const unsigned char* buf = smem + st * kStBuf;
+    const uint32_t Sa = sb + kStS + (slab * 2 + par) * 4096;
+    const uint32_t Ua = sb + kStUn + (slab * 2 + par) * 2048;
+    unsigned char* Un = smem + kStUn + (slab * 2 + par) * 2048;
+    wait_or_abort(full0 + 8 * st, ph);
+    if (tid == 0 && !*s_abort) next_landed = ci + 1;
+    slab_barrier(slab);  // S of this chunk (published by the slab's four warps) is visible
+
+    // U_new^T [16 v x 16 t] = U^T - S W^T for tokens 16 qd .. 16 qd + 15
+    uint32_t ut[4];  // U^T tile in accumulator layout (the A-fragment layout matches it)
+    lda_64(ut, bufa + kStUt, 16 * slab, 16 * qd, lane);
+    float x[2][2][4];
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int b = 0; b < 2; ++b)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[a][b][e] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t a[4], b[4];
+      lda_128(a, Sa, 0, 16 * kk, lane);
+      ldb_nk_128(b, bufa + kStW, 16 * qd, 16 * kk, lane);
+      mma_f16(x[kk & 1][0], a, b[0], b[1]);
+      mma_f16(x[kk & 1][1], a, b[2], b[3]);
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        float x0 = 0.f, x1 = 0.f;
-        if (p.init) {
-          const int64_t off = sbase + (int64_t)(vr0 + 8 * hf) * kHeadDim + col;
-          if (p.state_bf16) {
-            float2 f = unpack_bf16(*reinterpret_cast<const uint32_t*>(
-                reinterpret_cast<const uint16_t*>(p.init) + off));
-            x0 = f.x; x1 = f.y;
-          } else {
-            float2 f = *reinterpret_cast<const float2*>(reinterpret_cast<const float*>(p.init) + off);
-            x0 = f.x; x1 = f.y;
-          }
-        }
-        s[j][2 * hf] = x0;
-        s[j][2 * hf + 1] = x1;
+        const int t = 16 * qd + 8 * nt + 2 * q4;
+        const float2 u = unpack_f16(ut[2 * nt + hf]);
+        const float n0 = u.x - (x[0][nt][2 * hf] + x[1][nt][2 * hf]);
+        const float n1 = u.y - (x[0][nt][2 * hf + 1] + x[1][nt][2 * hf + 1]);
+        *reinterpret_cast<uint32_t*>(Un + swz64(g + 8 * hf, t)) = pack_f16(n0, n1);
       }
-    }
-  }
+    slab_barrier(slab);  // U_new of the slab is visible
 
-  const unsigned char* ws = p.ws;
-  auto slot_ptr = [&](int64_t ci) {
-    return ws + ((slot0 + ci) * H + h) * (int64_t)kSlotBytes;
-  };
-  if (nch > 0) load_chunk_operands(smem, slot_ptr(0), v0, tid);
-  cp_async_commit();
-  if (nch > 1) load_chunk_operands(smem + kStBuf, slot_ptr(1), v0, tid);
-  cp_async_commit();
-
-  const uint32_t sb = smem_u32(smem);
-  for (int64_t ci = 0; ci < nch; ++ci) {
-    const int cur = (int)(ci & 1);
-    const uint32_t bufa = sb + cur * kStBuf;
-    const unsigned char* buf = smem + cur * kStBuf;
-    cp_async_wait<1>();
-    __syncthreads();
-
-    // state -> fp16 left operand over the key dimension (8 k16 steps)
-    uint32_t sa[8][4];
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      sa[kk][0] = pack_f16(s[2 * kk][0], s[2 * kk][1]);
-      sa[kk][1] = pack_f16(s[2 * kk][2], s[2 * kk][3]);
-      sa[kk][2] = pack_f16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-      sa[kk][3] = pack_f16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-    }
-
-    // X = S W^T  [16 v x 64 t];  U_new^T = U^T - X
-    float un[8][4];
-#pragma unroll
-    for (int a = 0; a < 8; ++a)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) un[a][e] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        uint32_t b[4];
-        ldb_nk_128(b, bufa + kStW, 16 * np, 16 * kk, lane);
-        mma_f16(un[2 * np], sa[kk], b[0], b[1]);
-        mma_f16(un[2 * np + 1], sa[kk], b[2], b[3]);
-      }
-    }
-    const int vl = 16 * warp + g;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int t = 8 * j + 2 * q4;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int tt = t + (e & 1), vv = vl + 8 * (e >> 1);
-        const float u = f16_to_f(*reinterpret_cast<const uint16_t*>(buf + kStU + swz64(tt, vv)));
-        un[j][e] = u - un[j][e];
-      }
-    }
-    uint32_t ua[4][4];
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      ua[kk][0] = pack_f16(un[2 * kk][0], un[2 * kk][1]);
-      ua[kk][1] = pack_f16(un[2 * kk][2], un[2 * kk][3]);
-      ua[kk][2] = pack_f16(un[2 * kk + 1][0], un[2 * kk + 1][1]);
-      ua[kk][3] = pack_f16(un[2 * kk + 1][2], un[2 * kk + 1][3]);
-    }
-
-    // O^T = S Qg^T + U_new^T P^T  [16 v x 64 t]
-    float o[8][4];
-#pragma unroll
-    for (int a = 0; a < 8; ++a)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[a][e] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        uint32_t b[4];
-        ldb_nk_128(b, bufa + kStQg, 16 * np, 16 * kk, lane);
-        mma_f16(o[2 * np], sa[kk], b[0], b[1]);
-        mma_f16(o[2 * np + 1], sa[kk], b[2], b[3]);
-      }
-    }
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        uint32_t b[4];
-        ldb_nk_64(b, bufa + kStP, 16 * np, 16 * kk, lane);
-        mma_f16(o[2 * np], ua[kk], b[0], b[1]);
-        mma_f16(o[2 * np + 1], ua[kk], b[2], b[3]);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int t = 8 * j + 2 * q4;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int tt = t + (e & 1), vv = vl + 8 * (e >> 1);
-        *reinterpret_cast<__nv_bfloat16*>(smem + kStO + swz64(tt, vv)) =
-            __float2bfloat16_rn(o[j][e] * p.scale);
-      }
-    }
-
-    // S = S Diag(gamma_C) + U_new^T K_hat
+    // S[:, kc0 ..] = S Diag(gamma_C) + U_new^T K_hat[:, kc0 ..]; publish for the next chunk
     const float* gc = reinterpret_cast<const float*>(buf + kStGc);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float g0 = gc[8 * j + 2 * q4], g1 = gc[8 * j + 2 * q4 + 1];
-      s[j][0] *= g0; s[j][1] *= g1; s[j][2] *= g0; s[j][3] *= g1;
+    for (int nt = 0; nt < 4; ++nt) {
+      const float2 gg = *reinterpret_cast<const float2*>(gc + kc0 + 8 * nt + 2 * q4);
+      s[nt][0] *= gg.x; s[nt][1] *= gg.y; s[nt][2] *= gg.x; s[nt][3] *= gg.y;
     }
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
+      uint32_t a[4];
+      lda_64(a, Ua, 0, 16 * kk, lane);
 #pragma unroll
-      for (int np = 0; np < 8; ++np) {
+      for (int np = 0; np < 2; ++np) {
         uint32_t b[4];
-        ldb_kn_128(b, bufa + kStKh, 16 * np, 16 * kk, lane);
-        mma_f16(s[2 * np], ua[kk], b[0], b[1]);
-        mma_f16(s[2 * np + 1], ua[kk], b[2], b[3]);
+        ldb_kn_128(b, bufa + kStKh, kc0 + 16 * np, 16 * kk, lane);
+        mma_f16(s[2 * np], a, b[0], b[1]);
+        mma_f16(s[2 * np + 1], a, b[2], b[3]);
       }
     }
-    __syncthreads();
+    publish_state(par ^ 1);
 
-    // output rows t < L of this chunk (coalesced 16-byte stores)
-    const int L = (int)min((int64_t)kChunk, len - ci * kChunk);
-    const int64_t tok0 = bos + ci * kChunk;
-    for (int idx = tid; idx < 64 * 8; idx += 128) {
-      const int t = idx >> 3, ch = idx & 7;
+    // O^T [16 v x 16 t] = S Qg^T + U_new^T P^T for tokens 16 qd .. (S of the chunk start)
+    float o[2][2][4];
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int b = 0; b < 2; ++b)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[a][b][e] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t a[4], b[4];
+      lda_128(a, Sa, 0, 16 * kk, lane);
+      ldb_nk_128(b, bufa + kStQg, 16 * qd, 16 * kk, lane);
+      mma_f16(o[kk & 1][0], a, b[0], b[1]);
+      mma_f16(o[kk & 1][1], a, b[2], b[3]);
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      uint32_t a[4], b[4];
+      lda_64(a, Ua, 0, 16 * kk, lane);
+      ldb_nk_64(b, bufa + kStP, 16 * qd, 16 * kk, lane);
+      mma_f16(o[kk & 1][0], a, b[0], b[1]);
+      mma_f16(o[kk & 1][1], a, b[2], b[3]);
+    }
+    __syncwarp();
+    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(empty0 + 8 * st)
+                                : "memory");
+    // this warp's 16 x 16 output tile -> staging [16 t][16 v] -> 32-byte row segments
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tl = 8 * nt + 2 * q4 + (e & 1);
+        const int vl = g + 8 * (e >> 1);
+        *reinterpret_cast<__nv_bfloat16*>(stage_o + tl * 32 + vl * 2) =
+            __float2bfloat16_rn((o[0][nt][e] + o[1][nt][e]) * p.scale);
+      }
+    __syncwarp();
+    {
+      const int L = (int)min((int64_t)kChunk, len - ci * kChunk);
+      const int tl = lane >> 1, half = lane & 1;
+      const int t = 16 * qd + tl;
       if (t < L) {
-        const uint4 val = *reinterpret_cast<const uint4*>(smem + kStO + t * 128 + ((ch ^ (t & 7)) << 4));
-        *reinterpret_cast<uint4*>(p.out + ((tok0 + t) * H + h) * kHeadDim + v0 + ch * 8) = val;
+        const int64_t tok = bos + ci * kChunk + t;
+        *reinterpret_cast<uint4*>(p.out + (tok * H + h) * kHeadDim + v0 + 16 * slab + 8 * half) =
+            *reinterpret_cast<const uint4*>(stage_o + tl * 32 + half * 16);
       }
     }
-    if (ci + 2 < nch) load_chunk_operands(smem + cur * kStBuf, slot_ptr(ci + 2), v0, tid);
-    cp_async_commit();
+    __syncwarp();
+    // refill this stage with chunk ci + kStages once all eight warps released it
+    if (tid == 0 && ci + kStages < nch) {
+      wait_or_abort(empty0 + 8 * st, ph);
+      if (!*s_abort) {
+        issue_chunk_copy(bufa, full0 + 8 * st, slot_ptr(ci + kStages), vt);
+        next_issue = ci + kStages + 1;
+      }
+    }
   }
-  cp_async_wait<0>();
+  // no bulk copy may still be landing when the CTA exits (only possible after
+  // a timed-out wait): drain the issued ones, again with bounded waits
+  if (tid == 0)
+    for (int64_t c = next_landed; c < next_issue; ++c)
+      mbar_wait_bounded(full0 + 8 * (int)(c % kStages), (uint32_t)((c / kStages) & 1));
+  __syncthreads();
 
   // ---- final state ----
   if (p.final_state) {
-    const int64_t sbase = (n * H + h) * (int64_t)(kHeadDim * kHeadDim);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int col = 8 * j + 2 * q4;
+    for (int nt = 0; nt < 4; ++nt) {
+      const int col = kc0 + 8 * nt + 2 * q4;
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        const int64_t off = sbase + (int64_t)(vr0 + 8 * hf) * kHeadDim + col;
+        const int64_t off = sbase + (int64_t)(vrow + 8 * hf) * kHeadDim + col;
         if (p.state_bf16)
           *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(p.final_state) + off) =
-              pack_bf16(s[j][2 * hf], s[j][2 * hf + 1]);
+              pack_bf16(s[nt][2 * hf], s[nt][2 * hf + 1]);
         else
           *reinterpret_cast<float2*>(reinterpret_cast<float*>(p.final_state) + off) =
-              make_float2(s[j][2 * hf], s[j][2 * hf + 1]);
+              make_float2(s[nt][2 * hf], s[nt][2 * hf + 1]);
       }
     }
   }
 }
 
+extern "C" int kda_get_status(int clear) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_kda_status, sizeof(int)) != cudaSuccess) return -1;
+  if (clear && v != 0) {
+    const int z = 0;
+    if (cudaMemcpyToSymbol(g_kda_status, &z, sizeof(int)) != cudaSuccess) return -1;
+  }
+  return v;
+}
+
 void launch_state_kernel(const StateParams& p, cudaStream_t stream) {
-  const int64_t blocks = p.N * p.H * 2;
-  kda_state_kernel<<<(unsigned)blocks, 128, kStateSmem, stream>>>(p);
+  const int64_t blocks = p.N * p.H * (kHeadDim / kVTile);
+  kda_state_kernel<<<(unsigned)blocks, 256, kStateSmem, stream>>>(p);
 }
 
 cudaError_t prepare_state_kernel() {

@@ -74,6 +74,8 @@ def load_library(build_if_missing: bool = True):
                                          ctypes.POINTER(ctypes.c_void_p)]
         lib.kda_fwd_launches.restype = ctypes.c_int
         lib.kda_fwd_launches.argtypes = [ctypes.POINTER(kda_fwd_args)]
+        lib.kda_get_status.restype = ctypes.c_int
+        lib.kda_get_status.argtypes = [ctypes.c_int]
         _lib = lib
     return _lib
 
