@@ -46,10 +46,10 @@ constexpr int kCsK = 16384;      // tile128: raw k, then bf16 k_hat * xr
 constexpr int kCsKy = 32768;     // tile128: bf16 k_hat * yr
 constexpr int kCsG = 49152;      // tile128: raw g, then fp16 beta k_hat gamma, then W
 constexpr int kCsV = 65536;      // tile128: raw v
-// phase 2 (aliases the q / k operand tiles once A and P are in registers)
-constexpr int kCsA16 = 0;        // tile64 fp16: A (lower sub-blocks)
-constexpr int kCsAd = 8192;      // fp32 [4][16][16]: diagonal sub-blocks of A
-constexpr int kCsX = 16384;      // tile64 fp16 [16][64]: inverse of sub-block r at cols 16r..
+// phase 2 (in the raw v tile, dead once the operand pass has read it)
+constexpr int kCsA16 = kCsV;            // tile64 fp16: A (lower sub-blocks)
+constexpr int kCsAd = kCsV + 8192;      // fp32 [4][16][16]: diagonal sub-blocks of A
+constexpr int kCsX = kCsV + 12288;      // tile64 fp16 [16][64]: inverse of sub-block r at cols 16r..
 // small arrays
 constexpr int kCsD = 81920;      // fp32 [4][128]: exact sub-chunk decay products
 constexpr int kCsXm = 83968;     // fp32 [4][128]: clamped product over tokens 0..7
@@ -91,7 +91,7 @@ __device__ __forceinline__ void scale_bfrag(uint32_t& b0, uint32_t& b1, const fl
   v = unpack_bf16(b1); b1 = pack_bf16(v.x * f[2], v.y * f[3]);
 }
 
-__device__ __forceinline__ float gate_decay(float z, float amul, float lb, int unsafe) {
+__device__ __forceinline__ float gate_decay(float z, float amul, float lb, bool unsafe) {
   float a;
   if (unsafe) {
     const float e = ex2(-fabsf(z) * kLog2e);
@@ -102,6 +102,7 @@ __device__ __forceinline__ float gate_decay(float z, float amul, float lb, int u
   return ex2(a * kLog2e);
 }
 
+template <bool kUnsafe, bool kL2>
 __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -155,9 +156,10 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
   // ---- S1: per-token inverse norms of q and k (warp per token) ----
   float* sRq = reinterpret_cast<float*>(smem + kCsRq);
   float* sRk = reinterpret_cast<float*>(smem + kCsRk);
+#pragma unroll
   for (int t = warp; t < kChunk; t += 8) {
     float rq = 1.0f, rk = 1.0f;
-    if (p.l2norm) {
+    if (kL2) {
       const uint32_t off = swz128(t, lane * 4);
       const uint2 qv = *reinterpret_cast<const uint2*>(smem + kCsQ + off);
       const uint2 kv = *reinterpret_cast<const uint2*>(smem + kCsK + off);
@@ -194,8 +196,8 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
     for (int j = 0; j < kSub; ++j) {
       const int t = rb * kSub + j;
       const float2 gz = unpack_bf16(u32_at(smem + kCsG, swz128(t, c0)));
-      float e0 = gate_decay(gz.x + dtb.x, amul, p.lower_bound, p.gate_unsafe);
-      float e1 = gate_decay(gz.y + dtb.y, amul, p.lower_bound, p.gate_unsafe);
+      float e0 = gate_decay(gz.x + dtb.x, amul, p.lower_bound, kUnsafe);
+      float e1 = gate_decay(gz.y + dtb.y, amul, p.lower_bound, kUnsafe);
       if (t >= L) { e0 = 1.f; e1 = 1.f; }
       d0[j] = e0;
       d1[j] = e1;
@@ -302,9 +304,10 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
   }
   __syncthreads();
 
-  // ---- S4: A (warps 0-3) and P (warps 4-7), row sub-block r, column sub-blocks cb <= r ----
+  // ---- S4: A (warps 0-3) and P (warps 4-7), row sub-block r, column sub-blocks cb <= r.
+  //      A goes to an fp16 operand tile (plus fp32 diagonal sub-blocks), P to the workspace.
   const int g = lane >> 2, q4 = lane & 3;
-  float accA[4][2][4];
+  float* sAd = reinterpret_cast<float*>(smem + kCsAd);
   {
     const int mat = warp >> 2, r = warp & 3;
     unsigned char* gP = ws + kSlotP;  // tile64 image
@@ -348,8 +351,13 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
           const float v0 = acc[nt][2 * hf], v1 = acc[nt][2 * hf + 1];
           if (mat == 0) {
             const float bt = sBeta[row];
-            accA[cb][nt][2 * hf] = (active && (cb < r || col < row)) ? v0 * bt : 0.f;
-            accA[cb][nt][2 * hf + 1] = (active && (cb < r || col + 1 < row)) ? v1 * bt : 0.f;
+            const float a0 = (active && (cb < r || col < row)) ? v0 * bt : 0.f;
+            const float a1 = (active && (cb < r || col + 1 < row)) ? v1 * bt : 0.f;
+            u32_at(smem + kCsA16, swz64(row, col)) = pack_f16(a0, a1);
+            if (cb == r) {
+              sAd[r * 256 + (row - 16 * r) * 16 + (col - 16 * r)] = a0;
+              sAd[r * 256 + (row - 16 * r) * 16 + (col - 16 * r) + 1] = a1;
+            }
           } else {
             const bool k0 = active && (cb < r || col <= row);
             const bool k1 = active && (cb < r || col + 1 <= row);
@@ -358,28 +366,6 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
         }
       }
     }
-  }
-  __syncthreads();  // the q / k operand tiles are dead from here on
-
-  // ---- S5: A as an fp16 operand tile and its fp32 diagonal sub-blocks ----
-  float* sAd = reinterpret_cast<float*>(smem + kCsAd);
-  if (warp < 4) {
-    const int r = warp;
-#pragma unroll
-    for (int cb = 0; cb < 4; ++cb)
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const int row = 16 * r + g + 8 * hf;
-          const int col = 16 * cb + 8 * nt + 2 * q4;
-          const float v0 = accA[cb][nt][2 * hf], v1 = accA[cb][nt][2 * hf + 1];
-          u32_at(smem + kCsA16, swz64(row, col)) = pack_f16(v0, v1);
-          if (cb == r) {
-            sAd[r * 256 + (row - 16 * r) * 16 + (col - 16 * r)] = v0;
-            sAd[r * 256 + (row - 16 * r) * 16 + (col - 16 * r) + 1] = v1;
-          }
-        }
   }
   __syncthreads();
 
@@ -545,12 +531,24 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
 }
 
 void launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t stream) {
-  kda_chunk_kernel<<<dim3((unsigned)num_slots, (unsigned)p.H), 256, kChunkSmem, stream>>>(p);
+  const dim3 grid((unsigned)num_slots, (unsigned)p.H);
+  if (p.gate_unsafe) {
+    if (p.l2norm) kda_chunk_kernel<true, true><<<grid, 256, kChunkSmem, stream>>>(p);
+    else kda_chunk_kernel<true, false><<<grid, 256, kChunkSmem, stream>>>(p);
+  } else {
+    if (p.l2norm) kda_chunk_kernel<false, true><<<grid, 256, kChunkSmem, stream>>>(p);
+    else kda_chunk_kernel<false, false><<<grid, 256, kChunkSmem, stream>>>(p);
+  }
 }
 
 cudaError_t prepare_chunk_kernel() {
-  return cudaFuncSetAttribute(kda_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kChunkSmem);
+  cudaError_t e = cudaSuccess;
+  const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kda_chunk_kernel<true, true>, attr, kChunkSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kda_chunk_kernel<true, false>, attr, kChunkSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kda_chunk_kernel<false, true>, attr, kChunkSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kda_chunk_kernel<false, false>, attr, kChunkSmem);
+  return e;
 }
 
 }  // namespace kda
