@@ -35,8 +35,8 @@ constexpr int kStages = 3;                     // operand pipeline depth
 constexpr int kStS = kStages * kStBuf;         // [2 slab][2 parity] tile128 [16][128] fp16
 constexpr int kStUn = kStS + 4 * 4096;         // [2 slab][2 parity] tile64 [16][64] fp16
 constexpr int kStO = kStUn + 4 * 2048;         // [8 warps][16 t][16 v] bf16 output staging
-constexpr int kStBar = kStO + 8 * 512;         // full[kStages], empty[kStages] mbarriers
-constexpr int kStAbort = kStBar + 16 * kStages;
+constexpr int kStBar = kStO + 8 * 512;         // full, empty (CTA), empty (cluster) per stage
+constexpr int kStAbort = kStBar + 24 * kStages;
 constexpr int kStateSmem = kStAbort + 16;
 constexpr int kVTile = 32;
 
@@ -44,12 +44,21 @@ constexpr int kVTile = 32;
 // up waiting for its operand copies; read and cleared by kda_get_status.
 __device__ int g_kda_status = 0;
 
-// One elected thread: bring chunk operands into a buffer with two bulk copies.
+// The four CTAs of a cluster are the four value tiles of one (sequence,
+// head); they need the same W / q gamma / k_hat / P / gamma_C block per chunk.
+// Each CTA's elected thread fetches one quarter of that block and multicasts
+// it to all four, plus its own U^T tile, all completing on the stage's full
+// mbarrier of every destination CTA (same offsets everywhere).
+constexpr int kClusterCtas = 4;
+constexpr int kShareQuarter = kSlotUt / kClusterCtas;
+static_assert(kShareQuarter % 16 == 0, "multicast pieces must be 16-byte multiples");
+
 __device__ __forceinline__ void issue_chunk_copy(uint32_t dbase, uint32_t bar,
                                                  const unsigned char* slot, int vt) {
   fence_proxy_async_smem();
   mbar_expect_tx(bar, (uint32_t)kStBuf);
-  bulk_g2s(dbase, slot, (uint32_t)kSlotUt, bar);
+  const uint32_t off = (uint32_t)vt * kShareQuarter;  // vt == rank in the cluster
+  bulk_g2s_multicast(dbase + off, slot + off, (uint32_t)kShareQuarter, bar, 0xF);
   bulk_g2s(dbase + kStUt, slot + kSlotUt + vt * 4096, 4096u, bar);
 }
 
@@ -57,7 +66,10 @@ __device__ __forceinline__ void slab_barrier(int slab) {
   asm volatile("bar.sync %0, 128;\n" ::"r"(1 + slab));
 }
 
-__global__ void __launch_bounds__(256, 1) kda_state_kernel(StateParams p) {
+// 8 consumer warps (two slabs x four) + 1 producer warp that only moves data.
+constexpr int kStateThreads = 288;
+
+__global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, q4 = lane & 3;
@@ -85,6 +97,63 @@ __global__ void __launch_bounds__(256, 1) kda_state_kernel(StateParams p) {
   const int kc0 = 32 * qd;              // this warp's key columns kc0 .. kc0 + 31
   const int64_t sbase = (n * H + h) * (int64_t)(kHeadDim * kHeadDim);
 
+  auto slot_ptr = [&](int64_t ci) {
+    return p.ws + ((slot0 + ci) * H + h) * (int64_t)kSlotBytes;
+  };
+  const uint32_t full0 = sb + kStBar, empty0 = sb + kStBar + 8 * kStages;
+  const uint32_t cempty0 = sb + kStBar + 16 * kStages;
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kStAbort);
+  if (tid == 0) {
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(full0 + 8 * st, 1);
+      mbar_init(empty0 + 8 * st, 8);               // one arrival per consumer warp
+      mbar_init(cempty0 + 8 * st, kClusterCtas);   // one arrival per CTA of the cluster
+    }
+    *s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  cluster_sync();  // every CTA's barriers exist before any multicast lands
+  // A timed-out wait sets the device status and switches the CTA to skip all
+  // further waits: it finishes with garbage but never hangs.
+  auto wait_or_abort = [&](uint32_t bar, uint32_t parity) {
+    if (*s_abort) return;
+    if (!mbar_wait_bounded(bar, parity)) {
+      atomicExch(&g_kda_status, 13);
+      *s_abort = 1;
+    }
+  };
+  if (warp == 8) {
+    // ---- producer warp: one elected lane streams chunk operands through the stages ----
+    if (lane == 0) {
+      int64_t issued = 0;
+      for (int64_t ci = 0; ci < nch; ++ci) {
+        const int st = (int)(ci % kStages);
+        if (ci >= kStages) {
+          const uint32_t ph = (uint32_t)(((ci - kStages) / kStages) & 1);
+          wait_or_abort(empty0 + 8 * st, ph);  // this CTA's eight warps released it
+#pragma unroll
+          for (int rk = 0; rk < kClusterCtas; ++rk)
+            asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];\n" ::"r"(
+                             mapa_cluster(cempty0 + 8 * st, rk))
+                         : "memory");
+          if (!*s_abort && !mbar_wait_cluster_bounded(cempty0 + 8 * st, ph)) {
+            atomicExch(&g_kda_status, 13);
+            *s_abort = 1;
+          }
+        }
+        if (*s_abort) break;
+        issue_chunk_copy(sb + st * kStBuf, full0 + 8 * st, slot_ptr(ci), vt);
+        issued = ci + 1;
+      }
+      // after a timeout, let this CTA's own issued copies land before leaving
+      if (*s_abort)
+        for (int64_t c = 0; c < issued; ++c)
+          mbar_wait_bounded(full0 + 8 * (int)(c % kStages), (uint32_t)((c / kStages) & 1));
+    }
+    __syncwarp();
+    cluster_sync();
+    return;
+  }
   // ---- initial state: s[nt] covers columns kc0 + 8 nt .. + 7 ----
   float s[4][4];
 #pragma unroll
@@ -119,33 +188,6 @@ __global__ void __launch_bounds__(256, 1) kda_state_kernel(StateParams p) {
   };
   publish_state(0);
 
-  auto slot_ptr = [&](int64_t ci) {
-    return p.ws + ((slot0 + ci) * H + h) * (int64_t)kSlotBytes;
-  };
-  const uint32_t full0 = sb + kStBar, empty0 = sb + kStBar + 8 * kStages;
-  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kStAbort);
-  if (tid == 0) {
-    for (int st = 0; st < kStages; ++st) {
-      mbar_init(full0 + 8 * st, 1);
-      mbar_init(empty0 + 8 * st, 8);  // one arrival per warp
-    }
-    *s_abort = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-  }
-  __syncthreads();
-  int64_t next_issue = 0, next_landed = 0;  // bookkeeping of thread 0 (the copy issuer)
-  if (tid == 0)
-    for (; next_issue < kStages && next_issue < nch; ++next_issue)
-      issue_chunk_copy(sb + next_issue * kStBuf, full0 + 8 * next_issue, slot_ptr(next_issue), vt);
-  // A timed-out wait sets the device status and switches the CTA to skip all
-  // further waits: it finishes with garbage but never hangs.
-  auto wait_or_abort = [&](uint32_t bar, uint32_t parity) {
-    if (*s_abort) return;
-    if (!mbar_wait_bounded(bar, parity)) {
-      atomicExch(&g_kda_status, 13);
-      *s_abort = 1;
-    }
-  };
   unsigned char* stage_o = smem + kStO + warp * 512;
 
   for (int64_t ci = 0; ci < nch; ++ci) {
@@ -158,7 +200,6 @@ __global__ void __launch_bounds__(256, 1) kda_state_kernel(StateParams p) {
     const uint32_t Ua = sb + kStUn + (slab * 2 + par) * 2048;
     unsigned char* Un = smem + kStUn + (slab * 2 + par) * 2048;
     wait_or_abort(full0 + 8 * st, ph);
-    if (tid == 0 && !*s_abort) next_landed = ci + 1;
     slab_barrier(slab);  // S of this chunk (published by the slab's four warps) is visible
 
     // U_new^T [16 v x 16 t] = U^T - S W^T for tokens 16 qd .. 16 qd + 15
@@ -237,8 +278,8 @@ __global__ void __launch_bounds__(256, 1) kda_state_kernel(StateParams p) {
       mma_f16(o[kk & 1][1], a, b[2], b[3]);
     }
     __syncwarp();
-    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(empty0 + 8 * st)
-                                : "memory");
+    if (lane == 0)  // release the stage (the producer forwards it to the cluster)
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(empty0 + 8 * st) : "memory");
     // this warp's 16 x 16 output tile -> staging [16 t][16 v] -> 32-byte row segments
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
@@ -261,21 +302,8 @@ __global__ void __launch_bounds__(256, 1) kda_state_kernel(StateParams p) {
       }
     }
     __syncwarp();
-    // refill this stage with chunk ci + kStages once all eight warps released it
-    if (tid == 0 && ci + kStages < nch) {
-      wait_or_abort(empty0 + 8 * st, ph);
-      if (!*s_abort) {
-        issue_chunk_copy(bufa, full0 + 8 * st, slot_ptr(ci + kStages), vt);
-        next_issue = ci + kStages + 1;
-      }
-    }
   }
-  // no bulk copy may still be landing when the CTA exits (only possible after
-  // a timed-out wait): drain the issued ones, again with bounded waits
-  if (tid == 0)
-    for (int64_t c = next_landed; c < next_issue; ++c)
-      mbar_wait_bounded(full0 + 8 * (int)(c % kStages), (uint32_t)((c / kStages) & 1));
-  __syncthreads();
+  cluster_sync();  // no CTA leaves while others may still write into its shared memory
 
   // ---- final state ----
   if (p.final_state) {
@@ -308,7 +336,19 @@ extern "C" int kda_get_status(int clear) {
 
 void launch_state_kernel(const StateParams& p, cudaStream_t stream) {
   const int64_t blocks = p.N * p.H * (kHeadDim / kVTile);
-  kda_state_kernel<<<(unsigned)blocks, 256, kStateSmem, stream>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kStateThreads);
+  cfg.dynamicSmemBytes = kStateSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kClusterCtas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, kda_state_kernel, p);
 }
 
 cudaError_t prepare_state_kernel() {
