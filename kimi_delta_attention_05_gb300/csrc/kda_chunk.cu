@@ -153,29 +153,24 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
   cp_async_wait<0>();
   __syncthreads();
 
-  // ---- S1: per-token inverse norms of q and k (warp per token) ----
+  // ---- S1: per-token inverse norms of q and k (two threads per row, 64 channels each) ----
   float* sRq = reinterpret_cast<float*>(smem + kCsRq);
   float* sRk = reinterpret_cast<float*>(smem + kCsRk);
-#pragma unroll
-  for (int t = warp; t < kChunk; t += 8) {
-    float rq = 1.0f, rk = 1.0f;
+  {
+    const int row = tid >> 1, half = tid & 1;  // rows 0..63 of q, 64..127 of k
+    const int t = row & 63;
+    float ss = 0.f;
     if (kL2) {
-      const uint32_t off = swz128(t, lane * 4);
-      const uint2 qv = *reinterpret_cast<const uint2*>(smem + kCsQ + off);
-      const uint2 kv = *reinterpret_cast<const uint2*>(smem + kCsK + off);
-      const float2 a0 = unpack_bf16(qv.x), a1 = unpack_bf16(qv.y);
-      const float2 b0 = unpack_bf16(kv.x), b1 = unpack_bf16(kv.y);
-      float sq = a0.x * a0.x + a0.y * a0.y + a1.x * a1.x + a1.y * a1.y;
-      float sk = b0.x * b0.x + b0.y * b0.y + b1.x * b1.x + b1.y * b1.y;
+      const unsigned char* tile = smem + (row < 64 ? kCsQ : kCsK);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        sq += __shfl_xor_sync(0xffffffffu, sq, o);
-        sk += __shfl_xor_sync(0xffffffffu, sk, o);
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(tile + t * 256 + (((8 * half + c) ^ (t & 7)) << 4));
+        const float2 a = unpack_bf16(v.x), b = unpack_bf16(v.y), e = unpack_bf16(v.z), f = unpack_bf16(v.w);
+        ss += a.x * a.x + a.y * a.y + b.x * b.x + b.y * b.y + e.x * e.x + e.y * e.y + f.x * f.x + f.y * f.y;
       }
-      rq = rsqrtf(sq + 1e-6f);
-      rk = rsqrtf(sk + 1e-6f);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
     }
-    if (lane == 0) { sRq[t] = rq; sRk[t] = rk; }
+    if (half == 0) (row < 64 ? sRq : sRk)[t] = kL2 ? rsqrtf(ss + 1e-6f) : 1.0f;
   }
 
   // ---- S2: gate activation, per-token decays d (registers), sub-chunk products ----
@@ -309,35 +304,54 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
   const int g = lane >> 2, q4 = lane & 3;
   float* sAd = reinterpret_cast<float*>(smem + kCsAd);
   {
-    const int mat = warp >> 2, r = warp & 3;
+    // 20 tiles (A and P, sub-blocks cb <= r); off-diagonal tiles cost ~5x a diagonal one
+    // (operand scaling).  Warp w takes tiles w, w + 8 and w + 16 of this order, so each
+    // warp gets one or two scaled tiles:
+    //   0..11: off-diagonal (A then P, (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)), 12..19: diagonal
     unsigned char* gP = ws + kSlotP;  // tile64 image
-#pragma unroll
-    for (int cb = 0; cb < 4; ++cb) {
+#pragma unroll 1
+    for (int tile = warp; tile < 20; tile += 8) {
+      int mat, r, cb;
+      if (tile < 12) {
+        mat = tile / 6;
+        const int o = tile % 6;  // (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+        r = o < 1 ? 1 : (o < 3 ? 2 : 3);
+        cb = o - (r * (r - 1)) / 2;
+      } else {
+        mat = (tile - 12) >> 2;
+        r = cb = (tile - 12) & 3;
+      }
       float acc[2][4];
 #pragma unroll
       for (int a = 0; a < 2; ++a)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[a][e] = 0.f;
-      const bool active = cb <= r;
-      if (active) {
-        const int fidx = r * (r - 1) / 2 + cb;
+      const int fidx = r * (r - 1) / 2 + cb;
+      if (cb < r) {
 #pragma unroll 2
         for (int kk = 0; kk < 8; ++kk) {
           uint32_t a[4], b[4];
           lda_128(a, sbase + (mat ? kCsQ : kCsK), 16 * r, 16 * kk, lane);
           ldb_nk_128(b, sbase + kCsKy, 16 * cb, 16 * kk, lane);
-          if (cb < r) {
-            const int ch = 16 * kk + 2 * q4;
-            const float2 fa01 = *reinterpret_cast<const float2*>(sFa + fidx * 128 + ch);
-            const float2 fa89 = *reinterpret_cast<const float2*>(sFa + fidx * 128 + ch + 8);
-            const float2 fb01 = *reinterpret_cast<const float2*>(sYm + cb * 128 + ch);
-            const float2 fb89 = *reinterpret_cast<const float2*>(sYm + cb * 128 + ch + 8);
-            const float fa[4] = {fa01.x, fa01.y, fa89.x, fa89.y};
-            const float fb[4] = {fb01.x, fb01.y, fb89.x, fb89.y};
-            scale_afrag(a, fa);
-            scale_bfrag(b[0], b[1], fb);
-            scale_bfrag(b[2], b[3], fb);
-          }
+          const int ch = 16 * kk + 2 * q4;
+          const float2 fa01 = *reinterpret_cast<const float2*>(sFa + fidx * 128 + ch);
+          const float2 fa89 = *reinterpret_cast<const float2*>(sFa + fidx * 128 + ch + 8);
+          const float2 fb01 = *reinterpret_cast<const float2*>(sYm + cb * 128 + ch);
+          const float2 fb89 = *reinterpret_cast<const float2*>(sYm + cb * 128 + ch + 8);
+          const float fa[4] = {fa01.x, fa01.y, fa89.x, fa89.y};
+          const float fb[4] = {fb01.x, fb01.y, fb89.x, fb89.y};
+          scale_afrag(a, fa);
+          scale_bfrag(b[0], b[1], fb);
+          scale_bfrag(b[2], b[3], fb);
+          mma_bf16(acc[0], a, b[0], b[1]);
+          mma_bf16(acc[1], a, b[2], b[3]);
+        }
+      } else {
+#pragma unroll 4
+        for (int kk = 0; kk < 8; ++kk) {
+          uint32_t a[4], b[4];
+          lda_128(a, sbase + (mat ? kCsQ : kCsK), 16 * r, 16 * kk, lane);
+          ldb_nk_128(b, sbase + kCsKy, 16 * cb, 16 * kk, lane);
           mma_bf16(acc[0], a, b[0], b[1]);
           mma_bf16(acc[1], a, b[2], b[3]);
         }
@@ -351,20 +365,29 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
           const float v0 = acc[nt][2 * hf], v1 = acc[nt][2 * hf + 1];
           if (mat == 0) {
             const float bt = sBeta[row];
-            const float a0 = (active && (cb < r || col < row)) ? v0 * bt : 0.f;
-            const float a1 = (active && (cb < r || col + 1 < row)) ? v1 * bt : 0.f;
+            const float a0 = (cb < r || col < row) ? v0 * bt : 0.f;
+            const float a1 = (cb < r || col + 1 < row) ? v1 * bt : 0.f;
             u32_at(smem + kCsA16, swz64(row, col)) = pack_f16(a0, a1);
             if (cb == r) {
               sAd[r * 256 + (row - 16 * r) * 16 + (col - 16 * r)] = a0;
               sAd[r * 256 + (row - 16 * r) * 16 + (col - 16 * r) + 1] = a1;
             }
           } else {
-            const bool k0 = active && (cb < r || col <= row);
-            const bool k1 = active && (cb < r || col + 1 <= row);
+            const bool k0 = cb < r || col <= row;
+            const bool k1 = cb < r || col + 1 <= row;
             u32_at(gP, swz64(row, col)) = pack_f16(k0 ? v0 : 0.f, k1 ? v1 : 0.f);
           }
         }
       }
+    }
+    // tiles above the diagonal: zero in A (read by the substitution) and in P
+    for (int idx = tid; idx < 6 * 128; idx += 256) {
+      const int o = idx >> 7, e = idx & 127;  // upper sub-block pairs (r, cb), cb > r
+      const int r = o < 3 ? 0 : (o < 5 ? 1 : 2);
+      const int cb = r + 1 + (o - (r == 0 ? 0 : (r == 1 ? 3 : 5)));
+      const int row = 16 * r + (e >> 3), col = 16 * cb + 2 * (e & 7);
+      u32_at(smem + kCsA16, swz64(row, col)) = 0u;
+      u32_at(gP, swz64(row, col)) = 0u;
     }
   }
   __syncthreads();
