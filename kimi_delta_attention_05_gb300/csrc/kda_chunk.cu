@@ -75,20 +75,25 @@ __device__ __forceinline__ uint32_t& u32_at(unsigned char* base, uint32_t off) {
   return *reinterpret_cast<uint32_t*>(base + off);
 }
 
-// Scale the 8 bf16 values of an A fragment (columns ch, ch+1, ch+8, ch+9) by
-// per-column factors f[0..3].
-__device__ __forceinline__ void scale_afrag(uint32_t (&a)[4], const float (&f)[4]) {
-  float2 v;
-  v = unpack_bf16(a[0]); a[0] = pack_bf16(v.x * f[0], v.y * f[1]);
-  v = unpack_bf16(a[1]); a[1] = pack_bf16(v.x * f[0], v.y * f[1]);
-  v = unpack_bf16(a[2]); a[2] = pack_bf16(v.x * f[2], v.y * f[3]);
-  v = unpack_bf16(a[3]); a[3] = pack_bf16(v.x * f[2], v.y * f[3]);
+// Packed bf16x2 multiply (fp32 exponent range, so a factor that underflows
+// does so only where the scaled value is below ~1e-38 anyway).
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
-// Scale a B fragment pair (rows k = ch, ch+1 | ch+8, ch+9) by f[0..3].
-__device__ __forceinline__ void scale_bfrag(uint32_t& b0, uint32_t& b1, const float (&f)[4]) {
-  float2 v;
-  v = unpack_bf16(b0); b0 = pack_bf16(v.x * f[0], v.y * f[1]);
-  v = unpack_bf16(b1); b1 = pack_bf16(v.x * f[2], v.y * f[3]);
+// Scale an A fragment (columns ch, ch+1 | ch+8, ch+9) by packed factors
+// f01 = (f[ch], f[ch+1]), f89 = (f[ch+8], f[ch+9]).
+__device__ __forceinline__ void scale_afrag(uint32_t (&a)[4], uint32_t f01, uint32_t f89) {
+  a[0] = mul_bf16x2(a[0], f01);
+  a[1] = mul_bf16x2(a[1], f01);
+  a[2] = mul_bf16x2(a[2], f89);
+  a[3] = mul_bf16x2(a[3], f89);
+}
+// Scale a B fragment pair (rows k = ch, ch+1 | ch+8, ch+9) likewise.
+__device__ __forceinline__ void scale_bfrag(uint32_t& b0, uint32_t& b1, uint32_t f01, uint32_t f89) {
+  b0 = mul_bf16x2(b0, f01);
+  b1 = mul_bf16x2(b1, f89);
 }
 
 __device__ __forceinline__ float gate_decay(float z, float amul, float lb, bool unsafe) {
@@ -328,7 +333,7 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
         for (int e = 0; e < 4; ++e) acc[a][e] = 0.f;
       const int fidx = r * (r - 1) / 2 + cb;
       if (cb < r) {
-#pragma unroll 2
+#pragma unroll 4
         for (int kk = 0; kk < 8; ++kk) {
           uint32_t a[4], b[4];
           lda_128(a, sbase + (mat ? kCsQ : kCsK), 16 * r, 16 * kk, lane);
@@ -338,11 +343,11 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
           const float2 fa89 = *reinterpret_cast<const float2*>(sFa + fidx * 128 + ch + 8);
           const float2 fb01 = *reinterpret_cast<const float2*>(sYm + cb * 128 + ch);
           const float2 fb89 = *reinterpret_cast<const float2*>(sYm + cb * 128 + ch + 8);
-          const float fa[4] = {fa01.x, fa01.y, fa89.x, fa89.y};
-          const float fb[4] = {fb01.x, fb01.y, fb89.x, fb89.y};
-          scale_afrag(a, fa);
-          scale_bfrag(b[0], b[1], fb);
-          scale_bfrag(b[2], b[3], fb);
+          const uint32_t pa01 = pack_bf16(fa01.x, fa01.y), pa89 = pack_bf16(fa89.x, fa89.y);
+          const uint32_t pb01 = pack_bf16(fb01.x, fb01.y), pb89 = pack_bf16(fb89.x, fb89.y);
+          scale_afrag(a, pa01, pa89);
+          scale_bfrag(b[0], b[1], pb01, pb89);
+          scale_bfrag(b[2], b[3], pb01, pb89);
           mma_bf16(acc[0], a, b[0], b[1]);
           mma_bf16(acc[1], a, b[2], b[3]);
         }
