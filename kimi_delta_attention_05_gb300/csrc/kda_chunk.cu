@@ -58,7 +58,7 @@ constexpr int kCsFa = 88064;     // fp32 [6][128]: left factors of the off-diago
 constexpr int kCsBeta = 91136;   // fp32 [64]
 constexpr int kCsRq = 91392;     // fp32 [64]: 1 / |q| (or 1)
 constexpr int kCsRk = 91648;     // fp32 [64]: 1 / |k| (or 1)
-constexpr int kCsVt = 91904;     // tile64 [128 v][64 t] fp16: beta V^T, then U^T
+constexpr int kCsVt = 91904;     // tile128 [64 t][128 v] fp16: beta V, then U
 constexpr int kChunkSmem = kCsVt + 16384;
 
 __device__ __forceinline__ float sigmoidf_fast(float x) {
@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
     }
     const float ixm0 = __frcp_rn(sXm[rb * 128 + c0]), ixm1 = __frcp_rn(sXm[rb * 128 + c0 + 1]);
     const float iym0 = __frcp_rn(sYm[rb * 128 + c0]), iym1 = __frcp_rn(sYm[rb * 128 + c0 + 1]);
-    unsigned char* gQg = ws + kSlotQg;  // tile128 images, same swizzle as shared memory
+    unsigned char* gQg = ws + kSlotA1;  // rows 0..63 of the [q gamma; W] image
     unsigned char* gKh = ws + kSlotKh;
     // backward over the sub-chunk (reads the raw k)
     {
@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
         const float yr0 = j >= 8 ? yc0 * iym0 : p70;
         const float yr1 = j >= 8 ? yc1 * iym1 : p71;
         u32_at(smem + kCsKy, off) = pack_bf16(k0 * yr0, k1 * yr1);
-        u32_at(gKh, off) = pack_f16(k0 * y0, k1 * y1);
+        u32_at(gKh, kmaj_off(t, c0, 64)) = pack_f16(k0 * y0, k1 * y1);
         const float dc0 = fmaxf(d0[j], kDiagDecayFloor), dc1 = fmaxf(d1[j], kDiagDecayFloor);
         y0 *= d0[j];
         y1 *= d1[j];
@@ -290,9 +290,8 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
         u32_at(smem + kCsK, off) = pack_bf16(k0 * xr0, k1 * xr1);
         u32_at(smem + kCsQ, off) = pack_bf16(q0 * xr0, q1 * xr1);
         u32_at(smem + kCsG, off) = pack_f16(bt * k0 * x0, bt * k1 * x1);
-        *reinterpret_cast<__half*>(smem + kCsVt + swz64(c0, t)) = __float2half_rn(bt * vr.x);
-        *reinterpret_cast<__half*>(smem + kCsVt + swz64(c0 + 1, t)) = __float2half_rn(bt * vr.y);
-        u32_at(gQg, off) = pack_f16(q0 * x0, q1 * x1);
+        u32_at(smem + kCsVt, off) = pack_f16(bt * vr.x, bt * vr.y);
+        u32_at(gQg, kmaj_off(t, c0, 128)) = pack_f16(q0 * x0, q1 * x1);
       }
     }
     if (rb == 0) {
@@ -313,7 +312,7 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
     // (operand scaling).  Warp w takes tiles w, w + 8 and w + 16 of this order, so each
     // warp gets one or two scaled tiles:
     //   0..11: off-diagonal (A then P, (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)), 12..19: diagonal
-    unsigned char* gP = ws + kSlotP;  // tile64 image
+    unsigned char* gP = ws + kSlotP;  // kmaj image R=64, K=64
 #pragma unroll 1
     for (int tile = warp; tile < 20; tile += 8) {
       int mat, r, cb;
@@ -380,7 +379,7 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
           } else {
             const bool k0 = cb < r || col <= row;
             const bool k1 = cb < r || col + 1 <= row;
-            u32_at(gP, swz64(row, col)) = pack_f16(k0 ? v0 : 0.f, k1 ? v1 : 0.f);
+            u32_at(gP, kmaj_off(row, col, 64)) = pack_f16(k0 ? v0 : 0.f, k1 ? v1 : 0.f);
           }
         }
       }
@@ -392,7 +391,7 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
       const int cb = r + 1 + (o - (r == 0 ? 0 : (r == 1 ? 3 : 5)));
       const int row = 16 * r + (e >> 3), col = 16 * cb + 2 * (e & 7);
       u32_at(smem + kCsA16, swz64(row, col)) = 0u;
-      u32_at(gP, swz64(row, col)) = 0u;
+      u32_at(gP, kmaj_off(row, col, 64)) = 0u;
     }
   }
   __syncthreads();
@@ -415,14 +414,12 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
   }
   __syncthreads();
 
-  // ---- S7: block forward substitution, in place, warp-private columns ----
-  //  warps 0-3: W rows of sub-chunk r = X_r (B_r - sum_{c<r} A_rc Y_c) on 32 key columns
-  //  warps 4-7: the same for U, transposed: U_r^T = (B_r^T - sum_{c<r} Y_c^T A_rc^T) X_r^T
-  //             on 32 value rows, so that U^T leaves as contiguous per-tile images
-  if (warp < 4) {
-    const int cbase = 32 * warp;
-    unsigned char* buf = smem + kCsG;
-    const uint32_t bufa = sbase + kCsG;
+  // ---- S7: [W | U] rows of sub-chunk r = X_r (B_r - sum_{c<r} A_rc Y_c), in place;
+  //      warp -> 32 columns of B = [beta K gamma | beta V] (warp-private: only __syncwarp)
+  {
+    const int cbase = 32 * (warp & 3);
+    unsigned char* buf = smem + (warp < 4 ? kCsG : kCsVt);
+    const uint32_t bufa = sbase + (warp < 4 ? kCsG : kCsVt);
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       if (r > 0) {
@@ -477,84 +474,22 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
         }
       __syncwarp();
     }
-  } else {
-    const int vbase = 32 * (warp - 4);
-    unsigned char* buf = smem + kCsVt;
-    const uint32_t bufa = sbase + kCsVt;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      if (r > 0) {
-        float acc[2][2][4];  // [value m-tile][token n-tile]
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-          for (int b = 0; b < 2; ++b)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[a][b][e] = 0.f;
-#pragma unroll
-        for (int c = 0; c < r; ++c) {
-          uint32_t b[4];
-          ldb_nk_64(b, sbase + kCsA16, 16 * r, 16 * c, lane);  // B[s][t] = A_rc[t][s]
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt) {
-            uint32_t a[4];
-            lda_64(a, bufa, vbase + 16 * mt, 16 * c, lane);  // Y_c^T [v][s]
-            mma_f16(acc[mt][0], a, b[0], b[1]);
-            mma_f16(acc[mt][1], a, b[2], b[3]);
-          }
-        }
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-              const uint32_t off = swz64(vbase + 16 * mt + g + 8 * hf, 16 * r + 8 * nt + 2 * q4);
-              const float2 bv = unpack_f16(u32_at(buf, off));
-              u32_at(buf, off) =
-                  pack_f16(bv.x - acc[mt][nt][2 * hf], bv.y - acc[mt][nt][2 * hf + 1]);
-            }
-        __syncwarp();
-      }
-      float y[2][2][4];
-#pragma unroll
-      for (int a = 0; a < 2; ++a)
-#pragma unroll
-        for (int b = 0; b < 2; ++b)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) y[a][b][e] = 0.f;
-      uint32_t b[4];
-      ldb_nk_64(b, sbase + kCsX, 0, 16 * r, lane);  // B[s][t] = X_r[t][s]
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-        uint32_t a[4];
-        lda_64(a, bufa, vbase + 16 * mt, 16 * r, lane);  // M_r^T [v][s]
-        mma_f16(y[mt][0], a, b[0], b[1]);
-        mma_f16(y[mt][1], a, b[2], b[3]);
-      }
-      __syncwarp();
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            const uint32_t off = swz64(vbase + 16 * mt + g + 8 * hf, 16 * r + 8 * nt + 2 * q4);
-            u32_at(buf, off) = pack_f16(y[mt][nt][2 * hf], y[mt][nt][2 * hf + 1]);
-          }
-      __syncwarp();
-    }
   }
   __syncthreads();
 
-  // ---- S8: W (tile128 image) and U^T (four tile64 images [32 v][64 t]) to the
-  //      workspace as they sit in shared memory, 16-byte stores ----
+  // ---- S8: W into rows 64..127 of the [q gamma; W] image, U into the four
+  //      per-value-tile images; 16-byte chunks remapped from the tile128 layout ----
 #pragma unroll 4
   for (int idx = tid; idx < 2048; idx += 256) {
-    const uint32_t off = (uint32_t)(idx & 1023) * 16;
-    const bool u = idx >= 1024;
-    *reinterpret_cast<uint4*>(ws + (u ? kSlotUt : kSlotW) + off) =
-        *reinterpret_cast<const uint4*>(smem + (u ? kCsVt : kCsG) + off);
+    const int m = idx >> 10, t = (idx >> 4) & 63, c = idx & 15;
+    const uint4 val = *reinterpret_cast<const uint4*>(smem + (m ? kCsVt : kCsG) + t * 256 +
+                                                       ((c ^ (t & 7)) << 4));
+    uint32_t dst;
+    if (m == 0)
+      dst = kSlotA1 + (c >> 3) * 16384 + (64 + t) * 128 + (((c & 7) ^ (t & 7)) << 4);
+    else
+      dst = kSlotU + (c >> 2) * 4096 + utile_off(t, (c & 3) * 8);
+    *reinterpret_cast<uint4*>(ws + dst) = val;
   }
 }
 

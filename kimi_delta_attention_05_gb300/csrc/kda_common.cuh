@@ -27,19 +27,33 @@ constexpr float kLog2e = 1.4426950408889634f;
 // ---- per-(chunk, head) workspace slot ----
 // Intermediates written by the chunk kernel and read by the state kernel, all
 // fp16 (11-bit significand: these feed the recurrent state, where bf16's 8
-// bits cost more accuracy than the tolerance allows).  Each block is stored
-// as the exact shared-memory image the state kernel uses (swizzled tiles), so
-// that a chunk arrives with two flat bulk copies: bytes [0, kSlotUt) and the
-// consumer's 4 KB U^T tile.
-constexpr int kSlotW = 0;                       // tile128 image [64 t][128 k]  W = T (K gamma)
-constexpr int kSlotQg = kSlotW + 64 * 128 * 2;  // tile128 image [64 t][128 k]  q gamma
-constexpr int kSlotKh = kSlotQg + 64 * 128 * 2; // tile128 image [64 t][128 k]  k gamma_C / gamma
-constexpr int kSlotP = kSlotKh + 64 * 128 * 2;  // tile64 image  [64 t][64 s]   intra read-out
-constexpr int kSlotGc = kSlotP + 64 * 64 * 2;   // fp32 [128]                   gamma_C
-constexpr int kSlotUt = kSlotGc + 128 * 4;      // 4 x tile64 image [32 v][64 t]  U^T per value tile
-constexpr int kSlotBytes = kSlotUt + 4 * 32 * 64 * 2;  // 74240 (multiple of 256)
+// bits cost more accuracy than the tolerance allows).  Every block is stored
+// as the exact shared-memory image the state kernel's tensor-core operands
+// use ("kmaj" images: 128-byte-swizzled, K-major, see kmaj_off), so a chunk
+// arrives with flat bulk copies.
+constexpr int kSlotA1 = 0;       // kmaj R=128, K=128: rows 0-63 q gamma, rows 64-127 W
+constexpr int kSlotKh = 32768;   // kmaj R=64 (t), K=128 (k): k gamma_C / gamma
+constexpr int kSlotP = 49152;    // kmaj R=64 (t), K=64 (s): intra read-out matrix P
+constexpr int kSlotGc = 57344;   // fp32 [128]: gamma_C
+constexpr int kSlotU = 57856;    // 4 x [64 t][32 v] fp16 (chunk-swizzled, see utile_off): U per value tile
+constexpr int kSlotBytes = kSlotU + 4 * 64 * 32 * 2;  // 74240 (multiple of 256)
+constexpr int kSlotShared = kSlotU;                   // bytes shared by all value tiles
 static_assert(kSlotBytes % 256 == 0, "slot must keep 256-byte alignment");
-static_assert(kSlotUt % 16 == 0, "bulk copies need 16-byte sizes and offsets");
+
+// Byte offset of element (row, k) in a "kmaj" image of R rows and K columns
+// (K a multiple of 64): 64-column halves of R rows x 128 bytes each, the 16-byte
+// chunks of a row XOR-swizzled by (row % 8).  This is the K-major layout the
+// tensor cores read with the 128-byte swizzle (8-row groups 1024 bytes apart);
+// read as an MN-major operand it is [K][R] with 64-wide halves R*128 bytes apart.
+__device__ __forceinline__ uint32_t kmaj_off(int row, int k, int R) {
+  return (uint32_t)((k >> 6) * (R * 128) + row * 128 + ((((k & 63) >> 3) ^ (row & 7)) << 4) +
+                    (k & 7) * 2);
+}
+// Byte offset of element (t, v) (v < 32) in a U tile [64 t][32 v] fp16: 64-byte
+// rows, 16-byte chunks XOR-swizzled by (t / 2) % 4 (conflict-free row reads).
+__device__ __forceinline__ uint32_t utile_off(int t, int v) {
+  return (uint32_t)(t * 64 + ((((v >> 3) ^ ((t >> 1) & 3))) << 4) + (v & 7) * 2);
+}
 
 // ---- swizzled shared-memory addressing ----
 __device__ __forceinline__ uint32_t swz128(int row, int col) {  // byte offset

@@ -1,5 +1,8 @@
-// Recurrent stage of the KDA forward pass: one CTA per (sequence, head,
-// 32-wide value tile), walking the chunks of its sequence in order.
+// Recurrent stage of the KDA forward pass on the 5th-generation tensor cores
+// (tcgen05, accumulators in tensor memory): one CTA per (sequence, head,
+// 32-wide value tile), walking the chunks of its sequence in order; the four
+// value-tile CTAs of a head form a cluster and share each chunk's operand
+// block by multicast bulk copies.
 //
 // Per chunk, with S the state (rows = value index, columns = key index) at
 // the chunk start and the intra-chunk quantities of the workspace slot:
@@ -7,80 +10,114 @@
 //   O     = scale (Q_gamma S^T + P U_new)  (inter + intra read-out, fused as in
 //                                          the chunk_o stage of the fla code map)
 //   S     = S Diag(gamma_C) + U_new^T K_hat   (chunk_delta_h state update)
-//
-// Work split: the CTA holds two "slabs" of 16 value rows; each slab is worked
-// by four warps.  Warp q of a slab computes U_new and O for tokens
-// 16q..16q+15 and owns key columns 32q..32q+31 of S (fp32, in mma
-// accumulator registers).  Per chunk the slab's warps exchange S and U_new
-// as fp16 operand tiles in shared memory (double-buffered by chunk parity),
-// so the sequential chain per chunk is 2 x 16 mma.sync per warp plus one
-// slab barrier and two CTA barriers.  Operands are fp16 (11-bit
-// significand) with fp32 accumulation; the state itself stays fp32.
+// as three tensor-core products, each issued by one thread:
+//   MMA1: D1 [128 x 32]  = [Q_gamma; W] (128 x 128) . S^T        (rows 64.. = W S^T)
+//   MMA2: D3 [128 x 32]  = K_hat^T (128 x 64)       . U_new       (state delta, row = key)
+//   MMA3: D1[0..63]     += [P; 0]   (128 x 64)       . U_new       (output rows)
+// The state master copy is fp32 in the registers of the four epilogue warps
+// (thread = key index = tensor-memory lane); each chunk it is published as an
+// fp16 operand tile for the next MMA1.  Roles: warps 0-3 epilogue, warp 4 bulk
+// copies, warp 5 tensor-core issue.  Every wait is bounded: a CTA that gives
+// up sets the device status word and stops waiting, so it cannot hang.
 #include "kda_common.cuh"
 #include "kda_kernels.cuh"
 
 namespace kda {
 
-// one chunk's operands (per buffer): the workspace slot image [0, kSlotUt)
-// followed by this CTA's U^T tile
-constexpr int kStW = kSlotW;     // tile128 [64 t][128 k] fp16
-constexpr int kStQg = kSlotQg;   // tile128 [64 t][128 k] fp16
-constexpr int kStKh = kSlotKh;   // tile128 [64 t][128 k] fp16
-constexpr int kStP = kSlotP;     // tile64 [64 t][64 s] fp16
-constexpr int kStGc = kSlotGc;   // fp32 [128]
-constexpr int kStUt = kSlotUt;   // tile64 [32 v][64 t] fp16
-constexpr int kStBuf = kSlotUt + 4096;
-constexpr int kStages = 3;                     // operand pipeline depth
-// exchange tiles, output staging, barriers
-constexpr int kStS = kStages * kStBuf;         // [2 slab][2 parity] tile128 [16][128] fp16
-constexpr int kStUn = kStS + 4 * 4096;         // [2 slab][2 parity] tile64 [16][64] fp16
-constexpr int kStO = kStUn + 4 * 2048;         // [8 warps][16 t][16 v] bf16 output staging
-constexpr int kStBar = kStO + 8 * 512;         // full, empty (CTA), empty (cluster) per stage
-constexpr int kStAbort = kStBar + 24 * kStages;
-constexpr int kStateSmem = kStAbort + 16;
+// ---- per-stage shared memory (one chunk's operands), 1024-aligned ----
+constexpr int kSA1 = 0;          // kmaj R=128 K=128: [q gamma; W]
+constexpr int kSKh = 32768;      // kmaj R=64 (t) K=128 (k): k_hat (MN-major A of MMA2)
+constexpr int kSP = 49152;       // kmaj R=64 K=64: P  (rows 0..63 of the A operand of MMA3)
+constexpr int kSZero = 57344;    // 8 KB of zeros: rows 64..127 of that A operand
+constexpr int kSGc = 65536;      // fp32 [128] gamma_C
+constexpr int kSU = 66048;       // U tile [64 t][32 v] fp16 (utile_off)
+constexpr int kStageBytes = 70656;  // 69 KB
+constexpr int kStages = 3;
+static_assert(kStageBytes % 1024 == 0, "stage bases must stay 1024-aligned");
+// ---- operand tiles written by the epilogue, barriers ----
+constexpr int kSS = kStages * kStageBytes;   // kmaj R=32 (v) K=128 (k): S (B of MMA1)
+constexpr int kSUn = kSS + 8192;              // kmaj R=32 (v) K=64 (t): U_new^T (B of MMA2/3)
+constexpr int kSBar = kSUn + 4096;            // mbarriers
+constexpr int kBarFull = 0, kBarEmpty = 3, kBarCEmpty = 6, kBarMma1 = 9, kBarMma23 = 10,
+              kBarUn = 11, kBarS = 12, kNumBars = 13;
+constexpr int kSTmem = kSBar + 8 * kNumBars;  // tensor-memory base address (written by alloc)
+constexpr int kSAbort = kSTmem + 8;
+constexpr int kStateSmem = kSAbort + 8;
 constexpr int kVTile = 32;
+constexpr int kClusterCtas = 4;
+constexpr int kPiece = kSP + 8192 - kSA1;    // 57344: the shared block minus gamma_C
+constexpr int kPieceQuarter = kPiece / kClusterCtas;  // 14336
+static_assert(kPieceQuarter % 16 == 0, "bulk copy sizes must be 16-byte multiples");
+constexpr uint32_t kStageTx = kPiece + 512 + 4096;    // bytes landing per stage per CTA
+constexpr int kStateThreads = 192;
+constexpr uint32_t kTmemCols = 128;  // D1 (2 x 32 cols), D3 (32 cols)
 
 // Sticky device status: set to KDA_ERR_DEVICE_TIMEOUT (13) by a CTA that gave
-// up waiting for its operand copies; read and cleared by kda_get_status.
+// up waiting; read and cleared by kda_get_status.
 __device__ int g_kda_status = 0;
 
-// The four CTAs of a cluster are the four value tiles of one (sequence,
-// head); they need the same W / q gamma / k_hat / P / gamma_C block per chunk.
-// Each CTA's elected thread fetches one quarter of that block and multicasts
-// it to all four, plus its own U^T tile, all completing on the stage's full
-// mbarrier of every destination CTA (same offsets everywhere).
-constexpr int kClusterCtas = 4;
-constexpr int kShareQuarter = kSlotUt / kClusterCtas;
-static_assert(kShareQuarter % 16 == 0, "multicast pieces must be 16-byte multiples");
-
-__device__ __forceinline__ void issue_chunk_copy(uint32_t dbase, uint32_t bar,
-                                                 const unsigned char* slot, int vt) {
-  fence_proxy_async_smem();
-  mbar_expect_tx(bar, (uint32_t)kStBuf);
-  const uint32_t off = (uint32_t)vt * kShareQuarter;  // vt == rank in the cluster
-  bulk_g2s_multicast(dbase + off, slot + off, (uint32_t)kShareQuarter, bar, 0xF);
-  bulk_g2s(dbase + kStUt, slot + kSlotUt + vt * 4096, 4096u, bar);
+// ---- tcgen05 helpers ----
+// Shared-memory matrix descriptor: 128-byte swizzle, given leading / stride
+// byte offsets.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((addr >> 4) & 0x3FFF);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version
+  d |= (uint64_t)2 << 61;  // 128-byte swizzle
+  return d;
 }
-
-__device__ __forceinline__ void slab_barrier(int slab) {
-  asm volatile("bar.sync %0, 128;\n" ::"r"(1 + slab));
+// Instruction descriptor: fp16 x fp16 -> fp32, M x N, A K-major or MN-major, B K-major.
+__device__ __forceinline__ uint32_t idesc_f16(int m, int n, bool a_mn_major) {
+  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
 }
-
-// 8 consumer warps (two slabs x four) + 1 producer warp that only moves data.
-constexpr int kStateThreads = 288;
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void tc_commit(uint32_t mbar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(mbar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+// 32 consecutive fp32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+__device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
 
 __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams p) {
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane >> 2, q4 = lane & 3;
-  const int slab = warp >> 2, qd = warp & 3;
   const int64_t H = p.H;
   const int64_t unit = blockIdx.x >> 2;
-  const int vt = blockIdx.x & 3;
+  const int vt = blockIdx.x & 3;  // == rank in the cluster of four
   const int v0 = vt * kVTile;
   const int64_t n = unit / H;
   const int h = (int)(unit - n * H);
-
   int64_t bos, len, slot0;
   if (p.cu) {
     bos = p.cu[n];
@@ -93,235 +130,230 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
   }
   const int64_t nch = (len + kChunk - 1) / kChunk;
   const uint32_t sb = smem_u32(smem);
-  const int vrow = v0 + 16 * slab + g;  // value rows vrow and vrow + 8
-  const int kc0 = 32 * qd;              // this warp's key columns kc0 .. kc0 + 31
-  const int64_t sbase = (n * H + h) * (int64_t)(kHeadDim * kHeadDim);
-
+  const uint32_t bar = sb + kSBar;
+  auto B = [&](int i) { return bar + 8 * i; };
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kSAbort);
   auto slot_ptr = [&](int64_t ci) {
     return p.ws + ((slot0 + ci) * H + h) * (int64_t)kSlotBytes;
   };
-  const uint32_t full0 = sb + kStBar, empty0 = sb + kStBar + 8 * kStages;
-  const uint32_t cempty0 = sb + kStBar + 16 * kStages;
-  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kStAbort);
+
+  // ---- set-up: barriers, zero tiles, tensor memory ----
   if (tid == 0) {
     for (int st = 0; st < kStages; ++st) {
-      mbar_init(full0 + 8 * st, 1);
-      mbar_init(empty0 + 8 * st, 8);               // one arrival per consumer warp
-      mbar_init(cempty0 + 8 * st, kClusterCtas);   // one arrival per CTA of the cluster
+      mbar_init(B(kBarFull + st), 1);
+      mbar_init(B(kBarEmpty + st), 1 + 4);          // MMA commit + four epilogue warps
+      mbar_init(B(kBarCEmpty + st), kClusterCtas);  // one per CTA of the cluster
     }
-    *s_abort = 0;
+    mbar_init(B(kBarMma1), 1);
+    mbar_init(B(kBarMma23), 1);
+    mbar_init(B(kBarUn), 2);
+    mbar_init(B(kBarS), 4);
+    *s_abort = (sb & 1023) ? 1 : 0;  // the swizzled operand images need 1024-byte alignment
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
+  for (int i = tid; i < kStages * 512; i += kStateThreads)
+    reinterpret_cast<uint4*>(smem + (i >> 9) * kStageBytes + kSZero)[i & 511] = make_uint4(0, 0, 0, 0);
+  if (warp == 5) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+                     sb + kSTmem),
+                 "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
   cluster_sync();  // every CTA's barriers exist before any multicast lands
-  // A timed-out wait sets the device status and switches the CTA to skip all
-  // further waits: it finishes with garbage but never hangs.
-  auto wait_or_abort = [&](uint32_t bar, uint32_t parity) {
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kSTmem);
+  if (*s_abort && tid == 0) atomicExch(&g_kda_status, 13);
+
+  auto wait = [&](uint32_t b, uint32_t parity) {
     if (*s_abort) return;
-    if (!mbar_wait_bounded(bar, parity)) {
+    if (!mbar_wait_bounded(b, parity)) {
       atomicExch(&g_kda_status, 13);
       *s_abort = 1;
     }
   };
-  if (warp == 8) {
-    // ---- producer warp: one elected lane streams chunk operands through the stages ----
+
+  if (warp == 4) {
+    // ---- bulk-copy producer ----
     if (lane == 0) {
       int64_t issued = 0;
       for (int64_t ci = 0; ci < nch; ++ci) {
         const int st = (int)(ci % kStages);
         if (ci >= kStages) {
           const uint32_t ph = (uint32_t)(((ci - kStages) / kStages) & 1);
-          wait_or_abort(empty0 + 8 * st, ph);  // this CTA's eight warps released it
+          wait(B(kBarEmpty + st), ph);  // this CTA is done with the stage
 #pragma unroll
           for (int rk = 0; rk < kClusterCtas; ++rk)
             asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];\n" ::"r"(
-                             mapa_cluster(cempty0 + 8 * st, rk))
+                             mapa_cluster(B(kBarCEmpty + st), rk))
                          : "memory");
-          if (!*s_abort && !mbar_wait_cluster_bounded(cempty0 + 8 * st, ph)) {
+          if (!*s_abort && !mbar_wait_cluster_bounded(B(kBarCEmpty + st), ph)) {
             atomicExch(&g_kda_status, 13);
             *s_abort = 1;
           }
         }
         if (*s_abort) break;
-        issue_chunk_copy(sb + st * kStBuf, full0 + 8 * st, slot_ptr(ci), vt);
+        const uint32_t dst = sb + st * kStageBytes;
+        const unsigned char* src = slot_ptr(ci);
+        fence_proxy_async_smem();
+        mbar_expect_tx(B(kBarFull + st), kStageTx);
+        bulk_g2s_multicast(dst + vt * kPieceQuarter, src + vt * kPieceQuarter, kPieceQuarter,
+                           B(kBarFull + st), 0xF);
+        if (vt == 0)
+          bulk_g2s_multicast(dst + kSGc, src + kSlotGc, 512u, B(kBarFull + st), 0xF);
+        bulk_g2s(dst + kSU, src + kSlotU + vt * 4096, 4096u, B(kBarFull + st));
         issued = ci + 1;
       }
-      // after a timeout, let this CTA's own issued copies land before leaving
-      if (*s_abort)
+      if (*s_abort)  // after a timeout: let this CTA's issued copies land before leaving
         for (int64_t c = 0; c < issued; ++c)
-          mbar_wait_bounded(full0 + 8 * (int)(c % kStages), (uint32_t)((c / kStages) & 1));
+          mbar_wait_bounded(B(kBarFull + (int)(c % kStages)), (uint32_t)((c / kStages) & 1));
     }
-    __syncwarp();
-    cluster_sync();
-    return;
-  }
-  // ---- initial state: s[nt] covers columns kc0 + 8 nt .. + 7 ----
-  float s[4][4];
+  } else if (warp == 5) {
+    // ---- tensor-core issuer ----
+    if (lane == 0) {
+      const uint32_t id1 = idesc_f16(128, 32, false);
+      const uint32_t id2 = idesc_f16(128, 32, true);
+      const uint32_t d3 = tmem + 64;
+      for (int64_t ci = 0; ci < nch; ++ci) {
+        const int st = (int)(ci % kStages);
+        const uint32_t par = (uint32_t)(ci & 1);
+        const uint32_t stg = sb + st * kStageBytes;
+        const uint32_t d1 = tmem + 32 * par;
+        wait(B(kBarFull + st), (uint32_t)((ci / kStages) & 1));
+        wait(B(kBarS), par);  // S of this chunk published
+        tc_fence_after();
 #pragma unroll
-  for (int nt = 0; nt < 4; ++nt) {
-    const int col = kc0 + 8 * nt + 2 * q4;
+        for (int ks = 0; ks < 8; ++ks)
+          tc_mma(d1, smem_desc(stg + kSA1 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                 smem_desc(sb + kSS + (ks >> 2) * 4096 + (ks & 3) * 32, 16, 1024), id1, ks > 0);
+        tc_commit(B(kBarMma1));
+        wait(B(kBarUn), par);  // U_new of this chunk published
+        tc_fence_after();
 #pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      float x0 = 0.f, x1 = 0.f;
-      if (p.init) {
-        const int64_t off = sbase + (int64_t)(vrow + 8 * hf) * kHeadDim + col;
-        float2 f;
-        if (p.state_bf16)
-          f = unpack_bf16(*reinterpret_cast<const uint32_t*>(
-              reinterpret_cast<const uint16_t*>(p.init) + off));
-        else
-          f = *reinterpret_cast<const float2*>(reinterpret_cast<const float*>(p.init) + off);
-        x0 = f.x;
-        x1 = f.y;
+        for (int ks = 0; ks < 4; ++ks)
+          tc_mma(d3, smem_desc(stg + kSKh + ks * 2048, 8192, 1024),
+                 smem_desc(sb + kSUn + ks * 32, 16, 1024), id2, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          tc_mma(d1, smem_desc(stg + kSP + ks * 32, 16, 1024),
+                 smem_desc(sb + kSUn + ks * 32, 16, 1024), id1, 1);
+        tc_commit(B(kBarMma23));
+        tc_commit(B(kBarEmpty + st));  // the stage's operands are no longer read by the tensor core
       }
-      s[nt][2 * hf] = x0;
-      s[nt][2 * hf + 1] = x1;
+      if (nch > 0)  // the last products must be complete before tensor memory is freed
+        mbar_wait_bounded(B(kBarMma23), (uint32_t)((nch - 1) & 1));
     }
-  }
-  auto publish_state = [&](int par) {
-    unsigned char* t = smem + kStS + (slab * 2 + par) * 4096;
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf)
-        *reinterpret_cast<uint32_t*>(t + swz128(g + 8 * hf, kc0 + 8 * nt + 2 * q4)) =
-            pack_f16(s[nt][2 * hf], s[nt][2 * hf + 1]);
-  };
-  publish_state(0);
-
-  unsigned char* stage_o = smem + kStO + warp * 512;
-
-  for (int64_t ci = 0; ci < nch; ++ci) {
-    const int st = (int)(ci % kStages);
-    const uint32_t ph = (uint32_t)((ci / kStages) & 1);
-    const int par = (int)(ci & 1);
-    const uint32_t bufa = sb + st * kStBuf;
-    const unsigned char* buf = smem + st * kStBuf;
-    const uint32_t Sa = sb + kStS + (slab * 2 + par) * 4096;
-    const uint32_t Ua = sb + kStUn + (slab * 2 + par) * 2048;
-    unsigned char* Un = smem + kStUn + (slab * 2 + par) * 2048;
-    wait_or_abort(full0 + 8 * st, ph);
-    slab_barrier(slab);  // S of this chunk (published by the slab's four warps) is visible
-
-    // U_new^T [16 v x 16 t] = U^T - S W^T for tokens 16 qd .. 16 qd + 15
-    uint32_t ut[4];  // U^T tile in accumulator layout (the A-fragment layout matches it)
-    lda_64(ut, bufa + kStUt, 16 * slab, 16 * qd, lane);
-    float x[2][2][4];
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-#pragma unroll
-      for (int b = 0; b < 2; ++b)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) x[a][b][e] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      uint32_t a[4], b[4];
-      lda_128(a, Sa, 0, 16 * kk, lane);
-      ldb_nk_128(b, bufa + kStW, 16 * qd, 16 * kk, lane);
-      mma_f16(x[kk & 1][0], a, b[0], b[1]);
-      mma_f16(x[kk & 1][1], a, b[2], b[3]);
-    }
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int t = 16 * qd + 8 * nt + 2 * q4;
-        const float2 u = unpack_f16(ut[2 * nt + hf]);
-        const float n0 = u.x - (x[0][nt][2 * hf] + x[1][nt][2 * hf]);
-        const float n1 = u.y - (x[0][nt][2 * hf + 1] + x[1][nt][2 * hf + 1]);
-        *reinterpret_cast<uint32_t*>(Un + swz64(g + 8 * hf, t)) = pack_f16(n0, n1);
-      }
-    slab_barrier(slab);  // U_new of the slab is visible
-
-    // S[:, kc0 ..] = S Diag(gamma_C) + U_new^T K_hat[:, kc0 ..]; publish for the next chunk
-    const float* gc = reinterpret_cast<const float*>(buf + kStGc);
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const float2 gg = *reinterpret_cast<const float2*>(gc + kc0 + 8 * nt + 2 * q4);
-      s[nt][0] *= gg.x; s[nt][1] *= gg.y; s[nt][2] *= gg.x; s[nt][3] *= gg.y;
-    }
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      uint32_t a[4];
-      lda_64(a, Ua, 0, 16 * kk, lane);
-#pragma unroll
-      for (int np = 0; np < 2; ++np) {
-        uint32_t b[4];
-        ldb_kn_128(b, bufa + kStKh, kc0 + 16 * np, 16 * kk, lane);
-        mma_f16(s[2 * np], a, b[0], b[1]);
-        mma_f16(s[2 * np + 1], a, b[2], b[3]);
-      }
-    }
-    publish_state(par ^ 1);
-
-    // O^T [16 v x 16 t] = S Qg^T + U_new^T P^T for tokens 16 qd .. (S of the chunk start)
-    float o[2][2][4];
-#pragma unroll
-    for (int a = 0; a < 2; ++a)
-#pragma unroll
-      for (int b = 0; b < 2; ++b)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[a][b][e] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      uint32_t a[4], b[4];
-      lda_128(a, Sa, 0, 16 * kk, lane);
-      ldb_nk_128(b, bufa + kStQg, 16 * qd, 16 * kk, lane);
-      mma_f16(o[kk & 1][0], a, b[0], b[1]);
-      mma_f16(o[kk & 1][1], a, b[2], b[3]);
-    }
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      uint32_t a[4], b[4];
-      lda_64(a, Ua, 0, 16 * kk, lane);
-      ldb_nk_64(b, bufa + kStP, 16 * qd, 16 * kk, lane);
-      mma_f16(o[kk & 1][0], a, b[0], b[1]);
-      mma_f16(o[kk & 1][1], a, b[2], b[3]);
-    }
-    __syncwarp();
-    if (lane == 0)  // release the stage (the producer forwards it to the cluster)
-      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(empty0 + 8 * st) : "memory");
-    // this warp's 16 x 16 output tile -> staging [16 t][16 v] -> 32-byte row segments
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int tl = 8 * nt + 2 * q4 + (e & 1);
-        const int vl = g + 8 * (e >> 1);
-        *reinterpret_cast<__nv_bfloat16*>(stage_o + tl * 32 + vl * 2) =
-            __float2bfloat16_rn((o[0][nt][e] + o[1][nt][e]) * p.scale);
-      }
-    __syncwarp();
+  } else {
+    // ---- epilogue warps 0-3: thread = tensor-memory lane (key index / token) ----
+    const int k = tid;  // 0..127
+    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    float s[32];  // S[v0 + j][k], j = 0..31
     {
-      const int L = (int)min((int64_t)kChunk, len - ci * kChunk);
-      const int tl = lane >> 1, half = lane & 1;
-      const int t = 16 * qd + tl;
-      if (t < L) {
-        const int64_t tok = bos + ci * kChunk + t;
-        *reinterpret_cast<uint4*>(p.out + (tok * H + h) * kHeadDim + v0 + 16 * slab + 8 * half) =
-            *reinterpret_cast<const uint4*>(stage_o + tl * 32 + half * 16);
+      const int64_t sbase = (n * H + h) * (int64_t)(kHeadDim * kHeadDim);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        float x = 0.f;
+        if (p.init) {
+          const int64_t off = sbase + (int64_t)(v0 + j) * kHeadDim + k;
+          x = p.state_bf16 ? bf16_to_f(reinterpret_cast<const uint16_t*>(p.init)[off])
+                           : reinterpret_cast<const float*>(p.init)[off];
+        }
+        s[j] = x;
       }
     }
-    __syncwarp();
-  }
-  cluster_sync();  // no CTA leaves while others may still write into its shared memory
+    auto publish_state = [&]() {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        *reinterpret_cast<__half*>(smem + kSS + kmaj_off(j, k, 32)) = __float2half_rn(s[j]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_local(B(kBarS));
+    };
+    publish_state();
 
-  // ---- final state ----
-  if (p.final_state) {
+    for (int64_t ci = 0; ci < nch; ++ci) {
+      const int st = (int)(ci % kStages);
+      const uint32_t par = (uint32_t)(ci & 1);
+      const unsigned char* stg = smem + st * kStageBytes;
+      wait(B(kBarFull + st), (uint32_t)((ci / kStages) & 1));
+      wait(B(kBarMma1), par);
+      tc_fence_after();
+      if (warp >= 2) {
+        // U_new^T for token t = k - 64 (rows 64.. of D1 hold W S^T)
+        const int t = k - 64;
+        float x[32];
+        tc_ld32(lane_addr + 32 * par, x);
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const int col = kc0 + 8 * nt + 2 * q4;
+        for (int c = 0; c < 4; ++c) {
+          const uint4 u = *reinterpret_cast<const uint4*>(stg + kSU + utile_off(t, 8 * c));
+          const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int64_t off = sbase + (int64_t)(vrow + 8 * hf) * kHeadDim + col;
+          for (int e = 0; e < 4; ++e) {
+            const float2 uv = unpack_f16(uw[e]);
+            const int j = 8 * c + 2 * e;
+            *reinterpret_cast<__half*>(smem + kSUn + kmaj_off(j, t, 32)) = __float2half_rn(uv.x - x[j]);
+            *reinterpret_cast<__half*>(smem + kSUn + kmaj_off(j + 1, t, 32)) =
+                __float2half_rn(uv.y - x[j + 1]);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_local(B(kBarUn));
+      }
+      wait(B(kBarMma23), par);
+      tc_fence_after();
+      {
+        // S[:, k] = gamma_C[k] S[:, k] + delta; publish for the next chunk
+        float d[32];
+        tc_ld32(lane_addr + 64, d);
+        const float gk = reinterpret_cast<const float*>(stg + kSGc)[k];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) s[j] = gk * s[j] + d[j];
+        __syncwarp();
+        if (lane == 0) mbar_arrive_local(B(kBarEmpty + st));  // U tile and gamma_C read
+        publish_state();
+      }
+      if (warp < 2) {
+        // output row t = k: D1 rows 0..63 = q gamma S^T + P U_new
+        const int t = k;
+        const int L = (int)min((int64_t)kChunk, len - ci * kChunk);
+        float o[32];
+        tc_ld32(lane_addr + 32 * par, o);
+        if (t < L) {
+          const int64_t tok = bos + ci * kChunk + t;
+          uint4* dst = reinterpret_cast<uint4*>(p.out + (tok * H + h) * kHeadDim + v0);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            dst[c] = make_uint4(pack_bf16(o[8 * c] * p.scale, o[8 * c + 1] * p.scale),
+                                pack_bf16(o[8 * c + 2] * p.scale, o[8 * c + 3] * p.scale),
+                                pack_bf16(o[8 * c + 4] * p.scale, o[8 * c + 5] * p.scale),
+                                pack_bf16(o[8 * c + 6] * p.scale, o[8 * c + 7] * p.scale));
+        }
+        tc_fence_before();
+      }
+    }
+    // ---- final state ----
+    if (p.final_state) {
+      const int64_t sbase = (n * H + h) * (int64_t)(kHeadDim * kHeadDim);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int64_t off = sbase + (int64_t)(v0 + j) * kHeadDim + k;
         if (p.state_bf16)
-          *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(p.final_state) + off) =
-              pack_bf16(s[nt][2 * hf], s[nt][2 * hf + 1]);
+          reinterpret_cast<__nv_bfloat16*>(p.final_state)[off] = __float2bfloat16_rn(s[j]);
         else
-          *reinterpret_cast<float2*>(reinterpret_cast<float*>(p.final_state) + off) =
-              make_float2(s[nt][2 * hf], s[nt][2 * hf + 1]);
+          reinterpret_cast<float*>(p.final_state)[off] = s[j];
       }
     }
   }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols));
+  cluster_sync();  // no CTA leaves while others may still write into its shared memory
 }
 
 extern "C" int kda_get_status(int clear) {
