@@ -38,8 +38,8 @@ static_assert(kStageBytes % 1024 == 0, "stage bases must stay 1024-aligned");
 constexpr int kSS = kStages * kStageBytes;   // kmaj R=32 (v) K=128 (k): S (B of MMA1)
 constexpr int kSUn = kSS + 8192;              // kmaj R=32 (v) K=64 (t): U_new^T (B of MMA2/3)
 constexpr int kSBar = kSUn + 4096;            // mbarriers
-constexpr int kBarFull = 0, kBarEmpty = 3, kBarCEmpty = 6, kBarMma1 = 9, kBarMma23 = 10,
-              kBarUn = 11, kBarS = 12, kNumBars = 13;
+constexpr int kBarFull = 0, kBarEmpty = 3, kBarCEmpty = 6, kBarMma1 = 9, kBarMma2 = 10,
+              kBarUn = 11, kBarS = 12, kBarMma3 = 13, kNumBars = 14;
 constexpr int kSTmem = kSBar + 8 * kNumBars;  // tensor-memory base address (written by alloc)
 constexpr int kSAbort = kSTmem + 8;
 constexpr int kStateSmem = kSAbort + 8;
@@ -145,7 +145,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
       mbar_init(B(kBarCEmpty + st), kClusterCtas);  // one per CTA of the cluster
     }
     mbar_init(B(kBarMma1), 1);
-    mbar_init(B(kBarMma23), 1);
+    mbar_init(B(kBarMma2), 1);
+    mbar_init(B(kBarMma3), 1);
     mbar_init(B(kBarUn), 2);
     mbar_init(B(kBarS), 4);
     *s_abort = (sb & 1023) ? 1 : 0;  // the swizzled operand images need 1024-byte alignment
@@ -178,10 +179,12 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
     // ---- bulk-copy producer ----
     if (lane == 0) {
       int64_t issued = 0;
+      int st = 0;
+      uint32_t ph_prev = 1;  // phase parity of the previous use of stage st
       for (int64_t ci = 0; ci < nch; ++ci) {
-        const int st = (int)(ci % kStages);
+        if (st == 0) ph_prev ^= 1u;
         if (ci >= kStages) {
-          const uint32_t ph = (uint32_t)(((ci - kStages) / kStages) & 1);
+          const uint32_t ph = ph_prev ^ 1u;
           wait(B(kBarEmpty + st), ph);  // this CTA is done with the stage
 #pragma unroll
           for (int rk = 0; rk < kClusterCtas; ++rk)
@@ -204,6 +207,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
           bulk_g2s_multicast(dst + kSGc, src + kSlotGc, 512u, B(kBarFull + st), 0xF);
         bulk_g2s(dst + kSU, src + kSlotU + vt * 4096, 4096u, B(kBarFull + st));
         issued = ci + 1;
+        st = st + 1 == kStages ? 0 : st + 1;
       }
       if (*s_abort)  // after a timeout: let this CTA's issued copies land before leaving
         for (int64_t c = 0; c < issued; ++c)
@@ -215,34 +219,41 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
       const uint32_t id1 = idesc_f16(128, 32, false);
       const uint32_t id2 = idesc_f16(128, 32, true);
       const uint32_t d3 = tmem + 64;
+      // descriptors of stage 0 / the fixed tiles; the 14-bit address field
+      // (bytes >> 4) takes the stage and k-step offsets by plain addition
+      const uint64_t dA1 = smem_desc(sb + kSA1, 16, 1024), dKh = smem_desc(sb + kSKh, 8192, 1024);
+      const uint64_t dP = smem_desc(sb + kSP, 16, 1024), dS = smem_desc(sb + kSS, 16, 1024);
+      const uint64_t dUn = smem_desc(sb + kSUn, 16, 1024);
+      int st = 0;
+      uint32_t phf = 0;  // phase parity of the full barrier of stage st
       for (int64_t ci = 0; ci < nch; ++ci) {
-        const int st = (int)(ci % kStages);
         const uint32_t par = (uint32_t)(ci & 1);
-        const uint32_t stg = sb + st * kStageBytes;
+        const uint64_t so = (uint64_t)((st * kStageBytes) >> 4);
         const uint32_t d1 = tmem + 32 * par;
-        wait(B(kBarFull + st), (uint32_t)((ci / kStages) & 1));
+        wait(B(kBarFull + st), phf);
         wait(B(kBarS), par);  // S of this chunk published
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          tc_mma(d1, smem_desc(stg + kSA1 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                 smem_desc(sb + kSS + (ks >> 2) * 4096 + (ks & 3) * 32, 16, 1024), id1, ks > 0);
+          tc_mma(d1, dA1 + so + (uint64_t)(((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                 dS + (uint64_t)(((ks >> 2) * 4096 + (ks & 3) * 32) >> 4), id1, ks > 0);
         tc_commit(B(kBarMma1));
         wait(B(kBarUn), par);  // U_new of this chunk published
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          tc_mma(d3, smem_desc(stg + kSKh + ks * 2048, 8192, 1024),
-                 smem_desc(sb + kSUn + ks * 32, 16, 1024), id2, ks > 0);
+          tc_mma(d3, dKh + so + (uint64_t)((ks * 2048) >> 4), dUn + (uint64_t)((ks * 32) >> 4),
+                 id2, ks > 0);
+        tc_commit(B(kBarMma2));  // the state update can start
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          tc_mma(d1, smem_desc(stg + kSP + ks * 32, 16, 1024),
-                 smem_desc(sb + kSUn + ks * 32, 16, 1024), id1, 1);
-        tc_commit(B(kBarMma23));
+          tc_mma(d1, dP + so + (uint64_t)((ks * 32) >> 4), dUn + (uint64_t)((ks * 32) >> 4), id1, 1);
+        tc_commit(B(kBarMma3));
         tc_commit(B(kBarEmpty + st));  // the stage's operands are no longer read by the tensor core
+        if (++st == kStages) { st = 0; phf ^= 1u; }
       }
       if (nch > 0)  // the last products must be complete before tensor memory is freed
-        mbar_wait_bounded(B(kBarMma23), (uint32_t)((nch - 1) & 1));
+        mbar_wait_bounded(B(kBarMma3), (uint32_t)((nch - 1) & 1));
     }
   } else {
     // ---- epilogue warps 0-3: thread = tensor-memory lane (key index / token) ----
@@ -273,11 +284,12 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
     };
     publish_state();
 
+    int st = 0;
+    uint32_t phf = 0;
     for (int64_t ci = 0; ci < nch; ++ci) {
-      const int st = (int)(ci % kStages);
       const uint32_t par = (uint32_t)(ci & 1);
       const unsigned char* stg = smem + st * kStageBytes;
-      wait(B(kBarFull + st), (uint32_t)((ci / kStages) & 1));
+      wait(B(kBarFull + st), phf);
       wait(B(kBarMma1), par);
       tc_fence_after();
       if (warp >= 2) {
@@ -303,7 +315,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
         __syncwarp();
         if (lane == 0) mbar_arrive_local(B(kBarUn));
       }
-      wait(B(kBarMma23), par);
+      wait(B(kBarMma2), par);
       tc_fence_after();
       {
         // S[:, k] = gamma_C[k] S[:, k] + delta; publish for the next chunk
@@ -321,6 +333,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
         const int t = k;
         const int L = (int)min((int64_t)kChunk, len - ci * kChunk);
         float o[32];
+        wait(B(kBarMma3), par);
+        tc_fence_after();
         tc_ld32(lane_addr + 32 * par, o);
         if (t < L) {
           const int64_t tok = bos + ci * kChunk + t;
@@ -334,6 +348,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
         }
         tc_fence_before();
       }
+      if (++st == kStages) { st = 0; phf ^= 1u; }
     }
     // ---- final state ----
     if (p.final_state) {
