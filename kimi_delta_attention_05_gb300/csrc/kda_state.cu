@@ -1,8 +1,8 @@
 // Recurrent stage of the KDA forward pass on the 5th-generation tensor cores
 // (tcgen05, accumulators in tensor memory): one CTA per (sequence, head,
-// 32-wide value tile), walking the chunks of its sequence in order; the four
-// value-tile CTAs of a head form a cluster and share each chunk's operand
-// block by multicast bulk copies.
+// 32-wide value tile), walking the chunks of its sequence in order and
+// bringing each chunk's operand block in with bulk copies, issued in parallel
+// by eight lanes of a producer warp.
 //
 // Per chunk, with S the state (rows = value index, columns = key index) at
 // the chunk start and the intra-chunk quantities of the workspace slot:
@@ -38,17 +38,16 @@ static_assert(kStageBytes % 1024 == 0, "stage bases must stay 1024-aligned");
 constexpr int kSS = kStages * kStageBytes;   // kmaj R=32 (v) K=128 (k): S (B of MMA1)
 constexpr int kSUn = kSS + 8192;              // kmaj R=32 (v) K=64 (t): U_new^T (B of MMA2/3)
 constexpr int kSBar = kSUn + 4096;            // mbarriers
-constexpr int kBarFull = 0, kBarEmpty = 3, kBarCEmpty = 6, kBarMma1 = 9, kBarMma2 = 10,
-              kBarUn = 11, kBarS = 12, kBarMma3 = 13, kNumBars = 14;
+constexpr int kBarFull = 0, kBarEmpty = 3, kBarMma1 = 6, kBarMma2 = 7, kBarUn = 8, kBarS = 9,
+              kBarMma3 = 10, kNumBars = 11;
 constexpr int kSTmem = kSBar + 8 * kNumBars;  // tensor-memory base address (written by alloc)
 constexpr int kSAbort = kSTmem + 8;
 constexpr int kStateSmem = kSAbort + 8;
 constexpr int kVTile = 32;
-constexpr int kClusterCtas = 4;
 constexpr int kPiece = kSP + 8192 - kSA1;    // 57344: the shared block minus gamma_C
-constexpr int kPieceQuarter = kPiece / kClusterCtas;  // 14336
-static_assert(kPieceQuarter % 16 == 0, "bulk copy sizes must be 16-byte multiples");
-constexpr uint32_t kStageTx = kPiece + 512 + 4096;    // bytes landing per stage per CTA
+constexpr int kPieces = 7;                   // copied as 7 pieces of 8 KB, one per lane
+static_assert(kPiece == kPieces * 8192, "piece split");
+constexpr uint32_t kStageTx = kPiece + 512 + 4096;    // bytes landing per stage
 constexpr int kStateThreads = 192;
 constexpr uint32_t kTmemCols = 128;  // D1 (2 x 32 cols), D3 (32 cols)
 
@@ -114,7 +113,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t H = p.H;
   const int64_t unit = blockIdx.x >> 2;
-  const int vt = blockIdx.x & 3;  // == rank in the cluster of four
+  const int vt = blockIdx.x & 3;
   const int v0 = vt * kVTile;
   const int64_t n = unit / H;
   const int h = (int)(unit - n * H);
@@ -142,7 +141,6 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
     for (int st = 0; st < kStages; ++st) {
       mbar_init(B(kBarFull + st), 1);
       mbar_init(B(kBarEmpty + st), 1 + 4);          // MMA commit + four epilogue warps
-      mbar_init(B(kBarCEmpty + st), kClusterCtas);  // one per CTA of the cluster
     }
     mbar_init(B(kBarMma1), 1);
     mbar_init(B(kBarMma2), 1);
@@ -162,7 +160,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
   }
   fence_proxy_async_smem();
   tc_fence_before();
-  cluster_sync();  // every CTA's barriers exist before any multicast lands
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kSTmem);
   if (*s_abort && tid == 0) atomicExch(&g_kda_status, 13);
@@ -176,43 +174,34 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
   };
 
   if (warp == 4) {
-    // ---- bulk-copy producer ----
-    if (lane == 0) {
-      int64_t issued = 0;
-      int st = 0;
-      uint32_t ph_prev = 1;  // phase parity of the previous use of stage st
-      for (int64_t ci = 0; ci < nch; ++ci) {
-        if (st == 0) ph_prev ^= 1u;
-        if (ci >= kStages) {
-          const uint32_t ph = ph_prev ^ 1u;
-          wait(B(kBarEmpty + st), ph);  // this CTA is done with the stage
-#pragma unroll
-          for (int rk = 0; rk < kClusterCtas; ++rk)
-            asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];\n" ::"r"(
-                             mapa_cluster(B(kBarCEmpty + st), rk))
-                         : "memory");
-          if (!*s_abort && !mbar_wait_cluster_bounded(B(kBarCEmpty + st), ph)) {
-            atomicExch(&g_kda_status, 13);
-            *s_abort = 1;
-          }
-        }
-        if (*s_abort) break;
-        const uint32_t dst = sb + st * kStageBytes;
-        const unsigned char* src = slot_ptr(ci);
+    // ---- bulk-copy producer: lane 0 keeps the barrier books, lanes 0..8 copy ----
+    int64_t issued = 0;
+    int st = 0;
+    uint32_t ph_prev = 1;  // phase parity of the previous use of stage st
+    for (int64_t ci = 0; ci < nch; ++ci) {
+      if (st == 0) ph_prev ^= 1u;
+      if (ci >= kStages) wait(B(kBarEmpty + st), ph_prev ^ 1u);  // the stage is free again
+      __syncwarp();
+      if (*s_abort) break;
+      const uint32_t dst = sb + st * kStageBytes;
+      const unsigned char* src = slot_ptr(ci);
+      if (lane == 0) {
         fence_proxy_async_smem();
         mbar_expect_tx(B(kBarFull + st), kStageTx);
-        bulk_g2s_multicast(dst + vt * kPieceQuarter, src + vt * kPieceQuarter, kPieceQuarter,
-                           B(kBarFull + st), 0xF);
-        if (vt == 0)
-          bulk_g2s_multicast(dst + kSGc, src + kSlotGc, 512u, B(kBarFull + st), 0xF);
-        bulk_g2s(dst + kSU, src + kSlotU + vt * 4096, 4096u, B(kBarFull + st));
-        issued = ci + 1;
-        st = st + 1 == kStages ? 0 : st + 1;
       }
-      if (*s_abort)  // after a timeout: let this CTA's issued copies land before leaving
-        for (int64_t c = 0; c < issued; ++c)
-          mbar_wait_bounded(B(kBarFull + (int)(c % kStages)), (uint32_t)((c / kStages) & 1));
+      __syncwarp();
+      if (lane < kPieces)
+        bulk_g2s(dst + lane * 8192, src + lane * 8192, 8192u, B(kBarFull + st));
+      else if (lane == kPieces)
+        bulk_g2s(dst + kSU, src + kSlotU + vt * 4096, 4096u, B(kBarFull + st));
+      else if (lane == kPieces + 1)
+        bulk_g2s(dst + kSGc, src + kSlotGc, 512u, B(kBarFull + st));
+      issued = ci + 1;
+      st = st + 1 == kStages ? 0 : st + 1;
     }
+    if (*s_abort && lane == 0)  // after a timeout: let this CTA's issued copies land before leaving
+      for (int64_t c = 0; c < issued; ++c)
+        mbar_wait_bounded(B(kBarFull + (int)(c % kStages)), (uint32_t)((c / kStages) & 1));
   } else if (warp == 5) {
     // ---- tensor-core issuer ----
     if (lane == 0) {
@@ -368,7 +357,6 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
   tc_fence_after();
   if (warp == 5)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols));
-  cluster_sync();  // no CTA leaves while others may still write into its shared memory
 }
 
 extern "C" int kda_get_status(int clear) {
@@ -388,13 +376,6 @@ void launch_state_kernel(const StateParams& p, cudaStream_t stream) {
   cfg.blockDim = dim3(kStateThreads);
   cfg.dynamicSmemBytes = kStateSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kClusterCtas;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   cudaLaunchKernelEx(&cfg, kda_state_kernel, p);
 }
 
