@@ -51,24 +51,20 @@ constexpr int kCsA16 = kCsV;            // tile64 fp16: A (lower sub-blocks)
 constexpr int kCsAd = kCsV + 8192;      // fp32 [4][16][16]: diagonal sub-blocks of A
 constexpr int kCsX = kCsV + 12288;      // tile64 fp16 [16][64]: inverse of sub-block r at cols 16r..
 // small arrays
-constexpr int kCsD = 81920;      // fp32 [4][128]: exact sub-chunk decay products
-constexpr int kCsXm = 83968;     // fp32 [4][128]: clamped product over tokens 0..7
-constexpr int kCsYm = 86016;     // fp32 [4][128]: clamped product over tokens 8..15
-constexpr int kCsFa = 88064;     // fp32 [6][128]: left factors of the off-diagonal sub-blocks
-constexpr int kCsBeta = 91136;   // fp32 [64]
-constexpr int kCsRq = 91392;     // fp32 [64]: 1 / |q| (or 1)
-constexpr int kCsRk = 91648;     // fp32 [64]: 1 / |k| (or 1)
-constexpr int kCsVt = 91904;     // tile128 [64 t][128 v] fp16: beta V, then U
+constexpr int kCsD = 81920;      // fp32 [8][128]: exact decay products of the 8-token half sub-chunks
+constexpr int kCsXm = 86016;     // fp32 [4][128]: clamped product over tokens 0..7 of a sub-chunk
+constexpr int kCsYm = 88064;     // fp32 [4][128]: clamped product over tokens 8..15
+constexpr int kCsFa = 90112;     // fp32 [6][128]: left factors of the off-diagonal sub-blocks
+constexpr int kCsBeta = 93184;   // fp32 [64]
+constexpr int kCsRq = 93440;     // fp32 [64]: 1 / |q| (or 1)
+constexpr int kCsRk = 93696;     // fp32 [64]: 1 / |k| (or 1)
+constexpr int kCsVt = 93952;     // tile128 [64 t][128 v] fp16: beta V, then U
 constexpr int kChunkSmem = kCsVt + 16384;
 
-__device__ __forceinline__ float sigmoidf_fast(float x) {
-  return __frcp_rn(1.0f + ex2(-x * kLog2e));
-}
-
-// log(1 + e) for e in [0, 1]; a short series where lg2(1 + e) would lose e.
-__device__ __forceinline__ float log1p_small(float e) {
-  if (e < 0.0078125f) return e * (1.0f - e * (0.5f - e * (1.0f / 3.0f)));
-  return lg2(1.0f + e) * 0.69314718055994531f;
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ uint32_t& u32_at(unsigned char* base, uint32_t off) {
@@ -96,15 +92,17 @@ __device__ __forceinline__ void scale_bfrag(uint32_t& b0, uint32_t& b1, uint32_t
   b1 = mul_bf16x2(b1, f89);
 }
 
-__device__ __forceinline__ float gate_decay(float z, float amul, float lb, bool unsafe) {
-  float a;
+// exp(a) for the gate activation a of the pre-activation z (g + dt_bias):
+//   unsafe: a = -amul softplus(z), softplus(z) = max(z, 0) + log(1 + e^-|z|);
+//   safe:   a = lb sigmoid(amul z).
+// Only exp(a) is used, so what matters is the absolute error of a: lg2(1 + e)
+// loses at most ~1e-7 of it when e is tiny, far below what exp(a) resolves.
+__device__ __forceinline__ float gate_decay(float z, float amul_log2e, float lb_log2e, bool unsafe) {
   if (unsafe) {
     const float e = ex2(-fabsf(z) * kLog2e);
-    a = -amul * (fmaxf(z, 0.0f) + log1p_small(e));
-  } else {
-    a = lb * sigmoidf_fast(amul * z);
+    return ex2(-amul_log2e * (fmaxf(z, 0.0f) + lg2(1.0f + e) * 0.69314718055994531f));
   }
-  return ex2(a * kLog2e);
+  return ex2(lb_log2e * rcp_approx(1.0f + ex2(-amul_log2e * z)));
 }
 
 template <bool kUnsafe, bool kL2>
@@ -154,7 +152,7 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
   }
   float* sBeta = reinterpret_cast<float*>(smem + kCsBeta);
   if (tid < kChunk)
-    sBeta[tid] = tid < L ? sigmoidf_fast(bf16_to_f(p.beta[(t0 + tid) * H + h])) : 0.0f;
+    sBeta[tid] = tid < L ? rcp_approx(1.0f + ex2(-bf16_to_f(p.beta[(t0 + tid) * H + h]) * kLog2e)) : 0.0f;
   cp_async_wait<0>();
   __syncthreads();
 
@@ -178,127 +176,148 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
     if (half == 0) (row < 64 ? sRq : sRk)[t] = kL2 ? rsqrtf(ss + 1e-6f) : 1.0f;
   }
 
-  // ---- S2: gate activation, per-token decays d (registers), sub-chunk products ----
-  // thread -> sub-chunk rb, channel pair (c0, c0 + 1)
-  const int rb = tid >> 6;
-  const int c0 = 2 * (tid & 63);
+  // ---- S2: gate activation, per-token decays d (registers), half sub-chunk products ----
+  // thread -> sub-chunk rb, half hf (tokens 8 hf .. 8 hf + 7 of it), channels c0 .. c0 + 3;
+  // a warp covers all 128 channels of one half, so every token row is one access
+  const int cg = tid & 31, hf = (tid >> 5) & 1, rb = tid >> 6;
+  const int c0 = 4 * cg;
+  const int seg = 2 * rb + hf;      // half sub-chunk index 0..7
+  const int tb = 16 * rb + 8 * hf;  // its first token
   float* sD = reinterpret_cast<float*>(smem + kCsD);
   float* sXm = reinterpret_cast<float*>(smem + kCsXm);
   float* sYm = reinterpret_cast<float*>(smem + kCsYm);
   float* sFa = reinterpret_cast<float*>(smem + kCsFa);
-  float d0[kSub], d1[kSub];
+  float d[8][4];
+  float inv[4];  // 1 / (clamped product over this half)
   {
-    const float2 dtb = p.dt_bias ? *reinterpret_cast<const float2*>(p.dt_bias + h * kHeadDim + c0)
-                                 : make_float2(0.f, 0.f);
-    const float amul = p.A_log ? expf(p.A_log[h]) : 1.0f;
-    float D0 = 1.f, D1 = 1.f, xm0 = 1.f, xm1 = 1.f, ym0 = 1.f, ym1 = 1.f;
+    const float4 dtb = p.dt_bias ? *reinterpret_cast<const float4*>(p.dt_bias + h * kHeadDim + c0)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float dtbv[4] = {dtb.x, dtb.y, dtb.z, dtb.w};
+    const float amul_log2e = (p.A_log ? expf(p.A_log[h]) : 1.0f) * kLog2e;
+    const float lb_log2e = p.lower_bound * kLog2e;
+    float D[4] = {1.f, 1.f, 1.f, 1.f}, Dc[4] = {1.f, 1.f, 1.f, 1.f};
 #pragma unroll
-    for (int j = 0; j < kSub; ++j) {
-      const int t = rb * kSub + j;
-      const float2 gz = unpack_bf16(u32_at(smem + kCsG, swz128(t, c0)));
-      float e0 = gate_decay(gz.x + dtb.x, amul, p.lower_bound, kUnsafe);
-      float e1 = gate_decay(gz.y + dtb.y, amul, p.lower_bound, kUnsafe);
-      if (t >= L) { e0 = 1.f; e1 = 1.f; }
-      d0[j] = e0;
-      d1[j] = e1;
-      D0 *= e0;
-      D1 *= e1;
-      if (j < 8) {
-        xm0 *= fmaxf(e0, kDiagDecayFloor);
-        xm1 *= fmaxf(e1, kDiagDecayFloor);
-      } else {
-        ym0 *= fmaxf(e0, kDiagDecayFloor);
-        ym1 *= fmaxf(e1, kDiagDecayFloor);
+    for (int j = 0; j < 8; ++j) {
+      const int t = tb + j;
+      const uint2 graw = *reinterpret_cast<const uint2*>(smem + kCsG + swz128(t, c0));
+      const float2 g01 = unpack_bf16(graw.x), g23 = unpack_bf16(graw.y);
+      const float gz[4] = {g01.x, g01.y, g23.x, g23.y};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float e = gate_decay(gz[c] + dtbv[c], amul_log2e, lb_log2e, kUnsafe);
+        if (t >= L) e = 1.f;
+        d[j][c] = e;
+        D[c] *= e;
+        Dc[c] *= fmaxf(e, kDiagDecayFloor);
       }
     }
-    *reinterpret_cast<float2*>(sD + rb * 128 + c0) = make_float2(D0, D1);
-    *reinterpret_cast<float2*>(sXm + rb * 128 + c0) = make_float2(xm0, xm1);
-    *reinterpret_cast<float2*>(sYm + rb * 128 + c0) = make_float2(ym0, ym1);
+    *reinterpret_cast<float4*>(sD + seg * 128 + c0) = make_float4(D[0], D[1], D[2], D[3]);
+    *reinterpret_cast<float4*>((hf ? sYm : sXm) + rb * 128 + c0) = make_float4(Dc[0], Dc[1], Dc[2], Dc[3]);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) inv[c] = __frcp_rn(Dc[c]);
   }
   __syncthreads();
 
-  // ---- S3: operands (thread = sub-chunk rb, channel pair c0, c0 + 1) ----
+  // ---- S3: operands (same thread mapping) ----
   //  exact, chunk relative:     gamma_j = prod_{s<=j} d_s  -> beta K gamma (smem), q gamma (ws)
   //  exact, chunk-end relative: gamma_C / gamma_j           -> k_hat (ws)
-  //  clamped, midpoint relative: xr_j = e^{lam_j - lam_7}, yr_j = 1 / xr_j -> A / P operands
+  //  clamped, midpoint relative: xr_j = e^{lam_j - lam_7}, yr_j = 1 / xr_j -> A / P operands;
+  //  within the half before the midpoint xr_j = inv * (clamped product up to j), after
+  //  it xr_j = clamped product from token 8 up to j, so each half needs only its own d
   {
-    float pre0 = 1.f, pre1 = 1.f, suf0 = 1.f, suf1 = 1.f;
+    float pre[4] = {1.f, 1.f, 1.f, 1.f}, suf[4] = {1.f, 1.f, 1.f, 1.f};
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      const float2 Ds = *reinterpret_cast<const float2*>(sD + s * 128 + c0);
-      if (s < rb) { pre0 *= Ds.x; pre1 *= Ds.y; }
-      if (s > rb) { suf0 *= Ds.x; suf1 *= Ds.y; }
+    for (int s2 = 0; s2 < 8; ++s2) {
+      const float4 Ds = *reinterpret_cast<const float4*>(sD + s2 * 128 + c0);
+      const float dv[4] = {Ds.x, Ds.y, Ds.z, Ds.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (s2 < seg) pre[c] *= dv[c];
+        if (s2 > seg) suf[c] *= dv[c];
+      }
     }
-    if (rb == 0) {  // left factors of the off-diagonal sub-blocks (r, cb), cb < r
+    if (tid < 32) {  // left factors of the off-diagonal sub-blocks (r, cb), cb < r
 #pragma unroll
       for (int r = 1; r < 4; ++r)
 #pragma unroll
         for (int cb = 0; cb < r; ++cb) {
-          float e0 = sXm[r * 128 + c0], e1 = sXm[r * 128 + c0 + 1];
-          for (int s = cb + 1; s < r; ++s) {
-            e0 *= sXm[s * 128 + c0] * sYm[s * 128 + c0];
-            e1 *= sXm[s * 128 + c0 + 1] * sYm[s * 128 + c0 + 1];
+          float4 e = *reinterpret_cast<const float4*>(sXm + r * 128 + c0);
+          for (int s3 = cb + 1; s3 < r; ++s3) {
+            const float4 xm = *reinterpret_cast<const float4*>(sXm + s3 * 128 + c0);
+            const float4 ym = *reinterpret_cast<const float4*>(sYm + s3 * 128 + c0);
+            e.x *= xm.x * ym.x;
+            e.y *= xm.y * ym.y;
+            e.z *= xm.z * ym.z;
+            e.w *= xm.w * ym.w;
           }
-          const int idx = r * (r - 1) / 2 + cb;
-          *reinterpret_cast<float2*>(sFa + idx * 128 + c0) = make_float2(e0, e1);
+          *reinterpret_cast<float4*>(sFa + (r * (r - 1) / 2 + cb) * 128 + c0) = e;
         }
+      // gamma_C = product over all eight halves
+      *reinterpret_cast<float4*>(ws + kSlotGc + c0 * 4) =
+          make_float4(suf[0] * sD[c0], suf[1] * sD[c0 + 1], suf[2] * sD[c0 + 2], suf[3] * sD[c0 + 3]);
     }
-    const float ixm0 = __frcp_rn(sXm[rb * 128 + c0]), ixm1 = __frcp_rn(sXm[rb * 128 + c0 + 1]);
-    const float iym0 = __frcp_rn(sYm[rb * 128 + c0]), iym1 = __frcp_rn(sYm[rb * 128 + c0 + 1]);
     unsigned char* gQg = ws + kSlotA1;  // rows 0..63 of the [q gamma; W] image
     unsigned char* gKh = ws + kSlotKh;
-    // backward over the sub-chunk (reads the raw k)
+    // backward over the half (reads the raw k)
     {
-      float y0 = suf0, y1 = suf1, yc0 = 1.f, yc1 = 1.f, p70 = 1.f, p71 = 1.f;
+      float y[4] = {suf[0], suf[1], suf[2], suf[3]}, yc[4] = {1.f, 1.f, 1.f, 1.f};
 #pragma unroll
-      for (int j = kSub - 1; j >= 0; --j) {
-        const int t = rb * kSub + j;
+      for (int j = 7; j >= 0; --j) {
+        const int t = tb + j;
         const uint32_t off = swz128(t, c0);
         const float rk = sRk[t];
-        const float2 kr = unpack_bf16(u32_at(smem + kCsK, off));
-        const float k0 = kr.x * rk, k1 = kr.y * rk;
-        const float yr0 = j >= 8 ? yc0 * iym0 : p70;
-        const float yr1 = j >= 8 ? yc1 * iym1 : p71;
-        u32_at(smem + kCsKy, off) = pack_bf16(k0 * yr0, k1 * yr1);
-        u32_at(gKh, kmaj_off(t, c0, 64)) = pack_f16(k0 * y0, k1 * y1);
-        const float dc0 = fmaxf(d0[j], kDiagDecayFloor), dc1 = fmaxf(d1[j], kDiagDecayFloor);
-        y0 *= d0[j];
-        y1 *= d1[j];
-        yc0 *= dc0;
-        yc1 *= dc1;
-        if (j <= 7) { p70 *= dc0; p71 *= dc1; }
+        const uint2 kraw = *reinterpret_cast<const uint2*>(smem + kCsK + off);
+        const float2 k01 = unpack_bf16(kraw.x), k23 = unpack_bf16(kraw.y);
+        const float k[4] = {k01.x * rk, k01.y * rk, k23.x * rk, k23.y * rk};
+        float yr[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) yr[c] = hf ? yc[c] * inv[c] : yc[c];
+        *reinterpret_cast<uint2*>(smem + kCsKy + off) =
+            make_uint2(pack_bf16(k[0] * yr[0], k[1] * yr[1]), pack_bf16(k[2] * yr[2], k[3] * yr[3]));
+        *reinterpret_cast<uint2*>(gKh + kmaj_off(t, c0, 64)) =
+            make_uint2(pack_f16(k[0] * y[0], k[1] * y[1]), pack_f16(k[2] * y[2], k[3] * y[3]));
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          y[c] *= d[j][c];
+          yc[c] *= fmaxf(d[j][c], kDiagDecayFloor);
+        }
       }
     }
-    // forward over the sub-chunk (overwrites raw q, k, g, v)
+    // forward over the half (overwrites raw q, k, g, v)
     {
-      float x0 = pre0, x1 = pre1, xc0 = 1.f, xc1 = 1.f, q80 = 1.f, q81 = 1.f;
+      float x[4] = {pre[0], pre[1], pre[2], pre[3]}, xc[4] = {1.f, 1.f, 1.f, 1.f};
 #pragma unroll
-      for (int j = 0; j < kSub; ++j) {
-        const int t = rb * kSub + j;
+      for (int j = 0; j < 8; ++j) {
+        const int t = tb + j;
         const uint32_t off = swz128(t, c0);
-        const float dc0 = fmaxf(d0[j], kDiagDecayFloor), dc1 = fmaxf(d1[j], kDiagDecayFloor);
-        x0 *= d0[j];
-        x1 *= d1[j];
-        if (j < 8) { xc0 *= dc0; xc1 *= dc1; } else { q80 *= dc0; q81 *= dc1; }
-        const float xr0 = j < 8 ? xc0 * ixm0 : q80;
-        const float xr1 = j < 8 ? xc1 * ixm1 : q81;
-        const float rk = sRk[t], rq = sRq[t], bt = sBeta[t];
-        const float2 kr = unpack_bf16(u32_at(smem + kCsK, off));
-        const float2 qr = unpack_bf16(u32_at(smem + kCsQ, off));
-        const float2 vr = unpack_bf16(u32_at(smem + kCsV, off));
-        const float k0 = kr.x * rk, k1 = kr.y * rk, q0 = qr.x * rq, q1 = qr.y * rq;
-        u32_at(smem + kCsK, off) = pack_bf16(k0 * xr0, k1 * xr1);
-        u32_at(smem + kCsQ, off) = pack_bf16(q0 * xr0, q1 * xr1);
-        u32_at(smem + kCsG, off) = pack_f16(bt * k0 * x0, bt * k1 * x1);
-        u32_at(smem + kCsVt, off) = pack_f16(bt * vr.x, bt * vr.y);
-        u32_at(gQg, kmaj_off(t, c0, 128)) = pack_f16(q0 * x0, q1 * x1);
-      }
-    }
-    if (rb == 0) {
-      float g0 = 1.f, g1 = 1.f;
+        float xr[4];
 #pragma unroll
-      for (int s = 0; s < 4; ++s) { g0 *= sD[s * 128 + c0]; g1 *= sD[s * 128 + c0 + 1]; }
-      *reinterpret_cast<float2*>(reinterpret_cast<float*>(ws + kSlotGc) + c0) = make_float2(g0, g1);
+        for (int c = 0; c < 4; ++c) {
+          x[c] *= d[j][c];
+          xc[c] *= fmaxf(d[j][c], kDiagDecayFloor);
+          xr[c] = hf ? xc[c] : xc[c] * inv[c];
+        }
+        const float rk = sRk[t], rq = sRq[t], bt = sBeta[t];
+        const uint2 kraw = *reinterpret_cast<const uint2*>(smem + kCsK + off);
+        const uint2 qraw = *reinterpret_cast<const uint2*>(smem + kCsQ + off);
+        const uint2 vraw = *reinterpret_cast<const uint2*>(smem + kCsV + off);
+        const float2 k01 = unpack_bf16(kraw.x), k23 = unpack_bf16(kraw.y);
+        const float2 q01 = unpack_bf16(qraw.x), q23 = unpack_bf16(qraw.y);
+        const float2 v01 = unpack_bf16(vraw.x), v23 = unpack_bf16(vraw.y);
+        const float k[4] = {k01.x * rk, k01.y * rk, k23.x * rk, k23.y * rk};
+        const float q[4] = {q01.x * rq, q01.y * rq, q23.x * rq, q23.y * rq};
+        const float v[4] = {v01.x, v01.y, v23.x, v23.y};
+        *reinterpret_cast<uint2*>(smem + kCsK + off) =
+            make_uint2(pack_bf16(k[0] * xr[0], k[1] * xr[1]), pack_bf16(k[2] * xr[2], k[3] * xr[3]));
+        *reinterpret_cast<uint2*>(smem + kCsQ + off) =
+            make_uint2(pack_bf16(q[0] * xr[0], q[1] * xr[1]), pack_bf16(q[2] * xr[2], q[3] * xr[3]));
+        *reinterpret_cast<uint2*>(smem + kCsG + off) =
+            make_uint2(pack_f16(bt * k[0] * x[0], bt * k[1] * x[1]), pack_f16(bt * k[2] * x[2], bt * k[3] * x[3]));
+        *reinterpret_cast<uint2*>(smem + kCsVt + off) =
+            make_uint2(pack_f16(bt * v[0], bt * v[1]), pack_f16(bt * v[2], bt * v[3]));
+        *reinterpret_cast<uint2*>(gQg + kmaj_off(t, c0, 128)) =
+            make_uint2(pack_f16(q[0] * x[0], q[1] * x[1]), pack_f16(q[2] * x[2], q[3] * x[3]));
+      }
     }
   }
   __syncthreads();
