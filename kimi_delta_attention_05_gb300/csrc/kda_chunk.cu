@@ -106,54 +106,84 @@ __device__ __forceinline__ float gate_decay(float z, float amul_log2e, float lb_
 }
 
 template <bool kUnsafe, bool kL2>
-__global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
+__global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_t num_items) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t slot = blockIdx.x;
-  const int h = blockIdx.y;
   const int64_t H = p.H;
-
-  // ---- locate the chunk: sequence n, chunk i, first token t0, length L ----
-  int64_t n, i, bos, seqlen;
-  if (p.cu) {
-    if (slot >= p.chunk_off[p.N]) return;
-    int64_t lo = 0, hi = p.N - 1;  // largest n with chunk_off[n] <= slot
-    while (lo < hi) {
-      int64_t mid = (lo + hi + 1) >> 1;
-      if (p.chunk_off[mid] <= slot) lo = mid; else hi = mid - 1;
-    }
-    n = lo;
-    i = slot - p.chunk_off[n];
-    bos = p.cu[n];
-    seqlen = p.cu[n + 1] - bos;
-  } else {
-    n = slot / p.NT;
-    i = slot - n * p.NT;
-    bos = n * p.T;
-    seqlen = p.T;
-  }
-  const int64_t t0 = bos + i * kChunk;
-  const int L = (int)min((int64_t)kChunk, seqlen - i * kChunk);
-  unsigned char* ws = p.ws + (slot * H + h) * (int64_t)kSlotBytes;
   const uint32_t sbase = smem_u32(smem);
-
-  // ---- S0: stage q, k, g, v into swizzled tiles (rows >= L zero-filled) ----
-  {
-    const uint16_t* src[4] = {p.q, p.k, p.g, p.v};
-    const int dstoff[4] = {kCsQ, kCsK, kCsG, kCsV};
-#pragma unroll 4
-    for (int idx = tid; idx < 4 * 1024; idx += 256) {
-      const int tsr = idx >> 10, row = (idx >> 4) & 63, ch = idx & 15;
-      const bool ok = row < L;
-      const uint16_t* s = ok ? src[tsr] + ((t0 + row) * H + h) * kHeadDim + ch * 8 : src[tsr];
-      cp_async16(sbase + dstoff[tsr] + row * 256 + ((ch ^ (row & 7)) << 4), s, ok ? 16 : 0);
+  // Persistent: CTA b takes items b, b + gridDim.x, ... (item = slot * H + head).
+  // The next item's q, k, g are copied in as soon as the A / P stage has finished
+  // with the q, k and K yr tiles, and its v once the substitution is done with
+  // the A / inverse tiles, so the copies overlap the rest of the current item.
+  if (p.cu) num_items = p.chunk_off[p.N] * H;  // varlen: only the slots in use
+  struct Item {
+    int64_t slot, t0;
+    int h, L;
+  };
+  // ---- locate a chunk: sequence n, chunk i, first token t0, length L ----
+  auto locate = [&](int64_t item) {
+    Item r;
+    r.slot = item / H;
+    r.h = (int)(item - r.slot * H);
+    int64_t n, i, bos, seqlen;
+    if (p.cu) {
+      int64_t lo = 0, hi = p.N - 1;  // largest n with chunk_off[n] <= slot
+      while (lo < hi) {
+        int64_t mid = (lo + hi + 1) >> 1;
+        if (p.chunk_off[mid] <= r.slot) lo = mid; else hi = mid - 1;
+      }
+      n = lo;
+      i = r.slot - p.chunk_off[n];
+      bos = p.cu[n];
+      seqlen = p.cu[n + 1] - bos;
+    } else {
+      n = r.slot / p.NT;
+      i = r.slot - n * p.NT;
+      bos = n * p.T;
+      seqlen = p.T;
     }
-    cp_async_commit();
-  }
+    r.t0 = bos + i * kChunk;
+    r.L = (int)min((int64_t)kChunk, seqlen - i * kChunk);
+    return r;
+  };
+  // stage one [64 x 128] bf16 input tile into a swizzled tile128 (rows >= L zero-filled)
+  auto load_tile = [&](const uint16_t* src, int dst, const Item& it) {
+#pragma unroll 4
+    for (int idx = tid; idx < 1024; idx += 256) {
+      const int row = idx >> 4, ch = idx & 15;
+      const bool ok = row < it.L;
+      const uint16_t* sp = ok ? src + ((it.t0 + row) * H + it.h) * kHeadDim + ch * 8 : src;
+      cp_async16(sbase + dst + row * 256 + ((ch ^ (row & 7)) << 4), sp, ok ? 16 : 0);
+    }
+  };
+  // beta logit of token tid (-inf past the chunk end, so that beta = 0 there)
+  auto load_beta = [&](const Item& it) {
+    return tid < it.L ? bf16_to_f(p.beta[(it.t0 + tid) * H + it.h]) : -INFINITY;
+  };
+  int64_t item = blockIdx.x;
+  if (item >= num_items) return;
+  Item cur = locate(item);
+  // ---- S0 (first item only; later items were prefetched): q, k, g | v ----
+  load_tile(p.q, kCsQ, cur);
+  load_tile(p.k, kCsK, cur);
+  load_tile(p.g, kCsG, cur);
+  cp_async_commit();
+  load_tile(p.v, kCsV, cur);
+  cp_async_commit();
+  float blogit = tid < kChunk ? load_beta(cur) : 0.f;
   float* sBeta = reinterpret_cast<float*>(smem + kCsBeta);
-  if (tid < kChunk)
-    sBeta[tid] = tid < L ? rcp_approx(1.0f + ex2(-bf16_to_f(p.beta[(t0 + tid) * H + h]) * kLog2e)) : 0.0f;
-  cp_async_wait<0>();
+
+  for (int it = 0; item < num_items; item += gridDim.x, ++it) {
+  const int L = cur.L;
+  const int h = cur.h;
+  unsigned char* ws = p.ws + (cur.slot * H + h) * (int64_t)kSlotBytes;
+  const int gt = (it & 1) ? kCsKy : kCsG;  // raw g, then beta K gamma, then W
+  const int yt = (it & 1) ? kCsG : kCsKy;  // bf16 K yr
+  const int64_t next = item + gridDim.x;
+  Item nxt = cur;
+  if (next < num_items) nxt = locate(next);
+  if (tid < kChunk) sBeta[tid] = rcp_approx(1.0f + ex2(-blogit * kLog2e));
+  cp_async_wait<1>();  // q, k, g of this item (v may still be in flight)
   __syncthreads();
 
   // ---- S1: per-token inverse norms of q and k (two threads per row, 64 channels each) ----
@@ -199,7 +229,7 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int t = tb + j;
-      const uint2 graw = *reinterpret_cast<const uint2*>(smem + kCsG + swz128(t, c0));
+      const uint2 graw = *reinterpret_cast<const uint2*>(smem + gt + swz128(t, c0));
       const float2 g01 = unpack_bf16(graw.x), g23 = unpack_bf16(graw.y);
       const float gz[4] = {g01.x, g01.y, g23.x, g23.y};
 #pragma unroll
@@ -272,7 +302,7 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
         float yr[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) yr[c] = hf ? yc[c] * inv[c] : yc[c];
-        *reinterpret_cast<uint2*>(smem + kCsKy + off) =
+        *reinterpret_cast<uint2*>(smem + yt + off) =
             make_uint2(pack_bf16(k[0] * yr[0], k[1] * yr[1]), pack_bf16(k[2] * yr[2], k[3] * yr[3]));
         *reinterpret_cast<uint2*>(gKh + kmaj_off(t, c0, 64)) =
             make_uint2(pack_f16(k[0] * y[0], k[1] * y[1]), pack_f16(k[2] * y[2], k[3] * y[3]));
@@ -283,6 +313,8 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
         }
       }
     }
+    cp_async_wait<0>();  // v of this item
+    __syncthreads();
     // forward over the half (overwrites raw q, k, g, v)
     {
       float x[4] = {pre[0], pre[1], pre[2], pre[3]}, xc[4] = {1.f, 1.f, 1.f, 1.f};
@@ -311,7 +343,7 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
             make_uint2(pack_bf16(k[0] * xr[0], k[1] * xr[1]), pack_bf16(k[2] * xr[2], k[3] * xr[3]));
         *reinterpret_cast<uint2*>(smem + kCsQ + off) =
             make_uint2(pack_bf16(q[0] * xr[0], q[1] * xr[1]), pack_bf16(q[2] * xr[2], q[3] * xr[3]));
-        *reinterpret_cast<uint2*>(smem + kCsG + off) =
+        *reinterpret_cast<uint2*>(smem + gt + off) =
             make_uint2(pack_f16(bt * k[0] * x[0], bt * k[1] * x[1]), pack_f16(bt * k[2] * x[2], bt * k[3] * x[3]));
         *reinterpret_cast<uint2*>(smem + kCsVt + off) =
             make_uint2(pack_f16(bt * v[0], bt * v[1]), pack_f16(bt * v[2], bt * v[3]));
@@ -355,7 +387,7 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
         for (int kk = 0; kk < 8; ++kk) {
           uint32_t a[4], b[4];
           lda_128(a, sbase + (mat ? kCsQ : kCsK), 16 * r, 16 * kk, lane);
-          ldb_nk_128(b, sbase + kCsKy, 16 * cb, 16 * kk, lane);
+          ldb_nk_128(b, sbase + yt, 16 * cb, 16 * kk, lane);
           const int ch = 16 * kk + 2 * q4;
           const float2 fa01 = *reinterpret_cast<const float2*>(sFa + fidx * 128 + ch);
           const float2 fa89 = *reinterpret_cast<const float2*>(sFa + fidx * 128 + ch + 8);
@@ -374,7 +406,7 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
         for (int kk = 0; kk < 8; ++kk) {
           uint32_t a[4], b[4];
           lda_128(a, sbase + (mat ? kCsQ : kCsK), 16 * r, 16 * kk, lane);
-          ldb_nk_128(b, sbase + kCsKy, 16 * cb, 16 * kk, lane);
+          ldb_nk_128(b, sbase + yt, 16 * cb, 16 * kk, lane);
           mma_bf16(acc[0], a, b[0], b[1]);
           mma_bf16(acc[1], a, b[2], b[3]);
         }
@@ -414,6 +446,14 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
     }
   }
   __syncthreads();
+  // q, k, K yr tiles are free: next item's q, k, g (g into this item's K yr tile)
+  if (next < num_items) {
+    load_tile(p.q, kCsQ, nxt);
+    load_tile(p.k, kCsK, nxt);
+    load_tile(p.g, yt, nxt);
+    if (tid < kChunk) blogit = load_beta(nxt);
+  }
+  cp_async_commit();
 
   // ---- S6: X_r = (I + A_rr)^-1 by forward substitution (warp r, lane = column) ----
   if (warp < 4 && lane < 16) {
@@ -437,8 +477,8 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
   //      warp -> 32 columns of B = [beta K gamma | beta V] (warp-private: only __syncwarp)
   {
     const int cbase = 32 * (warp & 3);
-    unsigned char* buf = smem + (warp < 4 ? kCsG : kCsVt);
-    const uint32_t bufa = sbase + (warp < 4 ? kCsG : kCsVt);
+    unsigned char* buf = smem + (warp < 4 ? gt : kCsVt);
+    const uint32_t bufa = sbase + (warp < 4 ? gt : kCsVt);
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       if (r > 0) {
@@ -495,13 +535,16 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
     }
   }
   __syncthreads();
+  // the A / inverse tiles in the raw-v tile are free: next item's v
+  if (next < num_items) load_tile(p.v, kCsV, nxt);
+  cp_async_commit();
 
   // ---- S8: W into rows 64..127 of the [q gamma; W] image, U into the four
   //      per-value-tile images; 16-byte chunks remapped from the tile128 layout ----
 #pragma unroll 4
   for (int idx = tid; idx < 2048; idx += 256) {
     const int m = idx >> 10, t = (idx >> 4) & 63, c = idx & 15;
-    const uint4 val = *reinterpret_cast<const uint4*>(smem + (m ? kCsVt : kCsG) + t * 256 +
+    const uint4 val = *reinterpret_cast<const uint4*>(smem + (m ? kCsVt : gt) + t * 256 +
                                                        ((c ^ (t & 7)) << 4));
     uint32_t dst;
     if (m == 0)
@@ -510,16 +553,24 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p) {
       dst = kSlotU + (c >> 2) * 4096 + utile_off(t, (c & 3) * 8);
     *reinterpret_cast<uint4*>(ws + dst) = val;
   }
+  cur = nxt;
+  }
+  cp_async_wait<0>();
 }
 
 void launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t stream) {
-  const dim3 grid((unsigned)num_slots, (unsigned)p.H);
+  // persistent grid: two CTAs per SM (the shared-memory and register budget), or fewer items
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t items = num_slots * p.H;
+  const unsigned grid = (unsigned)min(items, (int64_t)(2 * (sms > 0 ? sms : 1)));
   if (p.gate_unsafe) {
-    if (p.l2norm) kda_chunk_kernel<true, true><<<grid, 256, kChunkSmem, stream>>>(p);
-    else kda_chunk_kernel<true, false><<<grid, 256, kChunkSmem, stream>>>(p);
+    if (p.l2norm) kda_chunk_kernel<true, true><<<grid, 256, kChunkSmem, stream>>>(p, items);
+    else kda_chunk_kernel<true, false><<<grid, 256, kChunkSmem, stream>>>(p, items);
   } else {
-    if (p.l2norm) kda_chunk_kernel<false, true><<<grid, 256, kChunkSmem, stream>>>(p);
-    else kda_chunk_kernel<false, false><<<grid, 256, kChunkSmem, stream>>>(p);
+    if (p.l2norm) kda_chunk_kernel<false, true><<<grid, 256, kChunkSmem, stream>>>(p, items);
+    else kda_chunk_kernel<false, false><<<grid, 256, kChunkSmem, stream>>>(p, items);
   }
 }
 
