@@ -54,7 +54,10 @@ constexpr int kCsX = kCsV + 12288;      // tile64 fp16 [16][64]: inverse of sub-
 constexpr int kCsD = 81920;      // fp32 [8][128]: exact decay products of the 8-token half sub-chunks
 constexpr int kCsXm = 86016;     // fp32 [4][128]: clamped product over tokens 0..7 of a sub-chunk
 constexpr int kCsYm = 88064;     // fp32 [4][128]: clamped product over tokens 8..15
-constexpr int kCsFa = 90112;     // fp32 [6][128]: left factors of the off-diagonal sub-blocks
+constexpr int kCsFa = 90112;     // bf16x2 [6][64]: left factors of the off-diagonal sub-blocks
+constexpr int kCsYp = 91648;     // bf16x2 [4][64]: right factors (clamped product over tokens 8..15)
+// Packed factor pairs are stored so that the pairs a K step of one mma fragment
+// needs (channels ch, ch+1 and ch+8, ch+9, ch = 16 kk + 2 q4) are adjacent.
 constexpr int kCsBeta = 93184;   // fp32 [64]
 constexpr int kCsRq = 93440;     // fp32 [64]: 1 / |q| (or 1)
 constexpr int kCsRk = 93696;     // fp32 [64]: 1 / |k| (or 1)
@@ -65,6 +68,11 @@ __device__ __forceinline__ float rcp_approx(float x) {
   float y;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Position of channel pair pp (channels 2 pp, 2 pp + 1) in a packed factor row.
+__device__ __forceinline__ int fpair_pos(int pp) {
+  return (pp & ~7) + 2 * (pp & 3) + ((pp >> 2) & 1);
 }
 
 __device__ __forceinline__ uint32_t& u32_at(unsigned char* base, uint32_t off) {
@@ -243,6 +251,11 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
     }
     *reinterpret_cast<float4*>(sD + seg * 128 + c0) = make_float4(D[0], D[1], D[2], D[3]);
     *reinterpret_cast<float4*>((hf ? sYm : sXm) + rb * 128 + c0) = make_float4(Dc[0], Dc[1], Dc[2], Dc[3]);
+    if (hf) {
+      uint32_t* yp = reinterpret_cast<uint32_t*>(smem + kCsYp) + rb * 64;
+      yp[fpair_pos(2 * cg)] = pack_bf16(Dc[0], Dc[1]);
+      yp[fpair_pos(2 * cg + 1)] = pack_bf16(Dc[2], Dc[3]);
+    }
 #pragma unroll
     for (int c = 0; c < 4; ++c) inv[c] = __frcp_rn(Dc[c]);
   }
@@ -280,7 +293,9 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
             e.z *= xm.z * ym.z;
             e.w *= xm.w * ym.w;
           }
-          *reinterpret_cast<float4*>(sFa + (r * (r - 1) / 2 + cb) * 128 + c0) = e;
+          uint32_t* fp = reinterpret_cast<uint32_t*>(sFa) + (r * (r - 1) / 2 + cb) * 64;
+          fp[fpair_pos(2 * cg)] = pack_bf16(e.x, e.y);
+          fp[fpair_pos(2 * cg + 1)] = pack_bf16(e.z, e.w);
         }
       // gamma_C = product over all eight halves
       *reinterpret_cast<float4*>(ws + kSlotGc + c0 * 4) =
@@ -354,79 +369,34 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
   }
   __syncthreads();
 
-  // ---- S4: A (warps 0-3) and P (warps 4-7), row sub-block r, column sub-blocks cb <= r.
-  //      A goes to an fp16 operand tile (plus fp32 diagonal sub-blocks), P to the workspace.
+  // ---- S4: A (beta-scaled strictly lower decayed K K^T: fp16 operand tile plus fp32
+  //      diagonal sub-blocks) and P (lower decayed Q K^T, into the workspace), per
+  //      sub-block pair (r, cb <= r).  One warp computes A and P of a pair together:
+  //      the K yr fragment and its factor are shared, and the K xr and Q xr fragments
+  //      take the same left factor.  Warps 0-5: the off-diagonal pairs
+  //      (1,0) (2,0) (2,1) (3,0) (3,1) (3,2); warps 6, 7: two diagonal pairs each.
   const int g = lane >> 2, q4 = lane & 3;
   float* sAd = reinterpret_cast<float*>(smem + kCsAd);
   {
-    // 20 tiles (A and P, sub-blocks cb <= r); off-diagonal tiles cost ~5x a diagonal one
-    // (operand scaling).  Warp w takes tiles w, w + 8 and w + 16 of this order, so each
-    // warp gets one or two scaled tiles:
-    //   0..11: off-diagonal (A then P, (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)), 12..19: diagonal
     unsigned char* gP = ws + kSlotP;  // kmaj image R=64, K=64
-#pragma unroll 1
-    for (int tile = warp; tile < 20; tile += 8) {
-      int mat, r, cb;
-      if (tile < 12) {
-        mat = tile / 6;
-        const int o = tile % 6;  // (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
-        r = o < 1 ? 1 : (o < 3 ? 2 : 3);
-        cb = o - (r * (r - 1)) / 2;
-      } else {
-        mat = (tile - 12) >> 2;
-        r = cb = (tile - 12) & 3;
-      }
-      float acc[2][4];
-#pragma unroll
-      for (int a = 0; a < 2; ++a)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[a][e] = 0.f;
-      const int fidx = r * (r - 1) / 2 + cb;
-      if (cb < r) {
-#pragma unroll 4
-        for (int kk = 0; kk < 8; ++kk) {
-          uint32_t a[4], b[4];
-          lda_128(a, sbase + (mat ? kCsQ : kCsK), 16 * r, 16 * kk, lane);
-          ldb_nk_128(b, sbase + yt, 16 * cb, 16 * kk, lane);
-          const int ch = 16 * kk + 2 * q4;
-          const float2 fa01 = *reinterpret_cast<const float2*>(sFa + fidx * 128 + ch);
-          const float2 fa89 = *reinterpret_cast<const float2*>(sFa + fidx * 128 + ch + 8);
-          const float2 fb01 = *reinterpret_cast<const float2*>(sYm + cb * 128 + ch);
-          const float2 fb89 = *reinterpret_cast<const float2*>(sYm + cb * 128 + ch + 8);
-          const uint32_t pa01 = pack_bf16(fa01.x, fa01.y), pa89 = pack_bf16(fa89.x, fa89.y);
-          const uint32_t pb01 = pack_bf16(fb01.x, fb01.y), pb89 = pack_bf16(fb89.x, fb89.y);
-          scale_afrag(a, pa01, pa89);
-          scale_bfrag(b[0], b[1], pb01, pb89);
-          scale_bfrag(b[2], b[3], pb01, pb89);
-          mma_bf16(acc[0], a, b[0], b[1]);
-          mma_bf16(acc[1], a, b[2], b[3]);
-        }
-      } else {
-#pragma unroll 4
-        for (int kk = 0; kk < 8; ++kk) {
-          uint32_t a[4], b[4];
-          lda_128(a, sbase + (mat ? kCsQ : kCsK), 16 * r, 16 * kk, lane);
-          ldb_nk_128(b, sbase + yt, 16 * cb, 16 * kk, lane);
-          mma_bf16(acc[0], a, b[0], b[1]);
-          mma_bf16(acc[1], a, b[2], b[3]);
-        }
-      }
+    const uint32_t* fap = reinterpret_cast<const uint32_t*>(sFa);
+    const uint32_t* ybp = reinterpret_cast<const uint32_t*>(smem + kCsYp);
+    auto epilogue = [&](int mat, int r, int cb, const float (&acc)[2][4]) {
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const int row = 16 * r + g + 8 * hf;
+        for (int hh = 0; hh < 2; ++hh) {
+          const int row = 16 * r + g + 8 * hh;
           const int col = 16 * cb + 8 * nt + 2 * q4;
-          const float v0 = acc[nt][2 * hf], v1 = acc[nt][2 * hf + 1];
+          const float v0 = acc[nt][2 * hh], v1 = acc[nt][2 * hh + 1];
           if (mat == 0) {
             const float bt = sBeta[row];
             const float a0 = (cb < r || col < row) ? v0 * bt : 0.f;
             const float a1 = (cb < r || col + 1 < row) ? v1 * bt : 0.f;
             u32_at(smem + kCsA16, swz64(row, col)) = pack_f16(a0, a1);
-            if (cb == r) {
-              sAd[r * 256 + (row - 16 * r) * 16 + (col - 16 * r)] = a0;
-              sAd[r * 256 + (row - 16 * r) * 16 + (col - 16 * r) + 1] = a1;
-            }
+            if (cb == r)
+              *reinterpret_cast<float2*>(sAd + r * 256 + (row - 16 * r) * 16 + (col - 16 * r)) =
+                  make_float2(a0, a1);
           } else {
             const bool k0 = cb < r || col <= row;
             const bool k1 = cb < r || col + 1 <= row;
@@ -434,6 +404,56 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
           }
         }
       }
+    };
+#pragma unroll 1
+    for (int task = 0; task < (warp < 6 ? 1 : 2); ++task) {
+      int r, cb;
+      if (warp < 6) {
+        r = warp < 1 ? 1 : (warp < 3 ? 2 : 3);
+        cb = warp - r * (r - 1) / 2;
+      } else {
+        r = cb = (warp - 6) + 2 * task;
+      }
+      float accA[2][4], accP[2][4];
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) accA[a][e] = accP[a][e] = 0.f;
+      if (cb < r) {
+        const uint32_t* fa = fap + (r * (r - 1) / 2 + cb) * 64 + 2 * q4;
+        const uint32_t* fb = ybp + cb * 64 + 2 * q4;
+#pragma unroll 2
+        for (int kk = 0; kk < 8; ++kk) {
+          uint32_t ak[4], aq[4], b[4];
+          lda_128(ak, sbase + kCsK, 16 * r, 16 * kk, lane);
+          lda_128(aq, sbase + kCsQ, 16 * r, 16 * kk, lane);
+          ldb_nk_128(b, sbase + yt, 16 * cb, 16 * kk, lane);
+          const uint2 pa = *reinterpret_cast<const uint2*>(fa + 8 * kk);
+          const uint2 pb = *reinterpret_cast<const uint2*>(fb + 8 * kk);
+          scale_afrag(ak, pa.x, pa.y);
+          scale_afrag(aq, pa.x, pa.y);
+          scale_bfrag(b[0], b[1], pb.x, pb.y);
+          scale_bfrag(b[2], b[3], pb.x, pb.y);
+          mma_bf16(accA[0], ak, b[0], b[1]);
+          mma_bf16(accA[1], ak, b[2], b[3]);
+          mma_bf16(accP[0], aq, b[0], b[1]);
+          mma_bf16(accP[1], aq, b[2], b[3]);
+        }
+      } else {
+#pragma unroll 2
+        for (int kk = 0; kk < 8; ++kk) {
+          uint32_t ak[4], aq[4], b[4];
+          lda_128(ak, sbase + kCsK, 16 * r, 16 * kk, lane);
+          lda_128(aq, sbase + kCsQ, 16 * r, 16 * kk, lane);
+          ldb_nk_128(b, sbase + yt, 16 * cb, 16 * kk, lane);
+          mma_bf16(accA[0], ak, b[0], b[1]);
+          mma_bf16(accA[1], ak, b[2], b[3]);
+          mma_bf16(accP[0], aq, b[0], b[1]);
+          mma_bf16(accP[1], aq, b[2], b[3]);
+        }
+      }
+      epilogue(0, r, cb, accA);
+      epilogue(1, r, cb, accP);
     }
     // tiles above the diagonal: zero in A (read by the substitution) and in P
     for (int idx = tid; idx < 6 * 128; idx += 256) {
