@@ -101,15 +101,15 @@ __device__ __forceinline__ void scale_bfrag(uint32_t& b0, uint32_t& b1, uint32_t
 }
 
 // exp(a) for the gate activation a of the pre-activation z (g + dt_bias):
-//   unsafe: a = -amul softplus(z), softplus(z) = max(z, 0) + log(1 + e^-|z|);
+//   unsafe: a = -amul softplus(z) = -amul ln(1 + e^z), so exp(a) = 2^(-amul lg2(1 + 2^(z lg2 e)));
+//           for large z, 1 + 2^(.) rounds to 2^(.) and lg2 gives z lg2 e back; past the fp32
+//           range it is +inf and exp(a) = 0, the limit;
 //   safe:   a = lb sigmoid(amul z).
-// Only exp(a) is used, so what matters is the absolute error of a: lg2(1 + e)
-// loses at most ~1e-7 of it when e is tiny, far below what exp(a) resolves.
+// Only exp(a) is used, so what matters is the absolute error of a: lg2(1 + t)
+// loses at most ~1e-7 of it when t is tiny, far below what exp(a) resolves.
+// (amul_log2e = amul lg2 e for the safe gate, amul for the unsafe one.)
 __device__ __forceinline__ float gate_decay(float z, float amul_log2e, float lb_log2e, bool unsafe) {
-  if (unsafe) {
-    const float e = ex2(-fabsf(z) * kLog2e);
-    return ex2(-amul_log2e * (fmaxf(z, 0.0f) + lg2(1.0f + e) * 0.69314718055994531f));
-  }
+  if (unsafe) return ex2(-amul_log2e * lg2(1.0f + ex2(z * kLog2e)));
   return ex2(lb_log2e * rcp_approx(1.0f + ex2(-amul_log2e * z)));
 }
 
@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
     const float4 dtb = p.dt_bias ? *reinterpret_cast<const float4*>(p.dt_bias + h * kHeadDim + c0)
                                  : make_float4(0.f, 0.f, 0.f, 0.f);
     const float dtbv[4] = {dtb.x, dtb.y, dtb.z, dtb.w};
-    const float amul_log2e = (p.A_log ? expf(p.A_log[h]) : 1.0f) * kLog2e;
+    const float amul_log2e = (p.A_log ? expf(p.A_log[h]) : 1.0f) * (kUnsafe ? 1.0f : kLog2e);
     const float lb_log2e = p.lower_bound * kLog2e;
     float D[4] = {1.f, 1.f, 1.f, 1.f}, Dc[4] = {1.f, 1.f, 1.f, 1.f};
 #pragma unroll
@@ -301,6 +301,13 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
       *reinterpret_cast<float4*>(ws + kSlotGc + c0 * 4) =
           make_float4(suf[0] * sD[c0], suf[1] * sD[c0 + 1], suf[2] * sD[c0 + 2], suf[3] * sD[c0 + 3]);
     }
+    // xr takes 1 / (clamped product) in the first half, yr in the second
+    float invx[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      invx[c] = hf ? 1.f : inv[c];
+      inv[c] = hf ? inv[c] : 1.f;
+    }
     unsigned char* gQg = ws + kSlotA1;  // rows 0..63 of the [q gamma; W] image
     unsigned char* gKh = ws + kSlotKh;
     // backward over the half (reads the raw k)
@@ -316,7 +323,7 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
         const float k[4] = {k01.x * rk, k01.y * rk, k23.x * rk, k23.y * rk};
         float yr[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) yr[c] = hf ? yc[c] * inv[c] : yc[c];
+        for (int c = 0; c < 4; ++c) yr[c] = yc[c] * inv[c];  // inv = 1 in the first half
         *reinterpret_cast<uint2*>(smem + yt + off) =
             make_uint2(pack_bf16(k[0] * yr[0], k[1] * yr[1]), pack_bf16(k[2] * yr[2], k[3] * yr[3]));
         *reinterpret_cast<uint2*>(gKh + kmaj_off(t, c0, 64)) =
@@ -342,7 +349,7 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
         for (int c = 0; c < 4; ++c) {
           x[c] *= d[j][c];
           xc[c] *= fmaxf(d[j][c], kDiagDecayFloor);
-          xr[c] = hf ? xc[c] : xc[c] * inv[c];
+          xr[c] = xc[c] * invx[c];  // invx = 1 in the second half
         }
         const float rk = sRk[t], rq = sRq[t], bt = sBeta[t];
         const uint2 kraw = *reinterpret_cast<const uint2*>(smem + kCsK + off);
