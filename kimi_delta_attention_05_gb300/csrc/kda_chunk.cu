@@ -11,8 +11,8 @@
 //     are both <= 1 (fla-kda SKILL.md, "Numerical invariants"; fla-kda skill
 //     page on the midpoint offset),
 //   * [W | U] = (I + A)^-1 Diag(beta) [K gamma | V] by block forward
-//     substitution over the four sub-chunks: 16x16 diagonal inverses by
-//     forward substitution, then Y_r = X_r (B_r - sum_{c<r} A_rc Y_c)
+//     substitution over the four sub-chunks: 16x16 diagonal inverses X_r by
+//     forward substitution, M_rc = -X_r A_rc, then Y_r = X_r B_r + sum_{c<r} M_rc Y_c
 //     (the "solve_tril" triangular block merges and the "wy_fast" WY
 //     recompute of the fla-kda code map, fused),
 //   * q gamma, k gamma_C / gamma and gamma_C for the state stage.
@@ -500,63 +500,65 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
   }
   __syncthreads();
 
-  // ---- S7: [W | U] rows of sub-chunk r = X_r (B_r - sum_{c<r} A_rc Y_c), in place;
-  //      warp -> 32 columns of B = [beta K gamma | beta V] (warp-private: only __syncwarp)
+  // ---- S6b: M_rc = -X_r A_rc for the off-diagonal sub-blocks c < r (warp w < 6 takes
+  //      pair w in the order (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)), written over A_rc ----
+  if (warp < 6) {
+    const int r = warp < 1 ? 1 : (warp < 3 ? 2 : 3);
+    const int c = warp - r * (r - 1) / 2;
+    float acc[2][4];
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[a][e] = 0.f;
+    uint32_t a[4], b[4];
+    lda_64(a, sbase + kCsX, 0, 16 * r, lane);
+    ldb_kn_64(b, sbase + kCsA16, 16 * c, 16 * r, lane);
+    mma_f16(acc[0], a, b[0], b[1]);
+    mma_f16(acc[1], a, b[2], b[3]);
+    __syncwarp();
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+        u32_at(smem + kCsA16, swz64(16 * r + g + 8 * hh, 16 * c + 8 * nt + 2 * q4)) =
+            pack_f16(-acc[nt][2 * hh], -acc[nt][2 * hh + 1]);
+  }
+  __syncthreads();
+
+  // ---- S7: [W | U] rows of sub-chunk r: Y_r = X_r B_r + sum_{c<r} M_rc Y_c, accumulated
+  //      in registers and written over B_r; warp -> 32 columns of B = [beta K gamma | beta V]
+  //      (warp-private: only __syncwarp) ----
   {
     const int cbase = 32 * (warp & 3);
     unsigned char* buf = smem + (warp < 4 ? gt : kCsVt);
     const uint32_t bufa = sbase + (warp < 4 ? gt : kCsVt);
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      if (r > 0) {
-        float acc[4][4];
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[a][e] = 0.f;
-#pragma unroll
-        for (int c = 0; c < r; ++c) {
-          uint32_t a[4];
-          lda_64(a, sbase + kCsA16, 16 * r, 16 * c, lane);
-#pragma unroll
-          for (int np = 0; np < 2; ++np) {
-            uint32_t b[4];
-            ldb_kn_128(b, bufa, cbase + 16 * np, 16 * c, lane);
-            mma_f16(acc[2 * np], a, b[0], b[1]);
-            mma_f16(acc[2 * np + 1], a, b[2], b[3]);
-          }
-        }
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            const uint32_t off = swz128(16 * r + g + 8 * hf, cbase + 8 * nt + 2 * q4);
-            const float2 bv = unpack_f16(u32_at(buf, off));
-            u32_at(buf, off) = pack_f16(bv.x - acc[nt][2 * hf], bv.y - acc[nt][2 * hf + 1]);
-          }
-        __syncwarp();
-      }
       float y[4][4];
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int e = 0; e < 4; ++e) y[a][e] = 0.f;
-      uint32_t a[4];
-      lda_64(a, sbase + kCsX, 0, 16 * r, lane);
 #pragma unroll
-      for (int np = 0; np < 2; ++np) {
-        uint32_t b[4];
-        ldb_kn_128(b, bufa, cbase + 16 * np, 16 * r, lane);
-        mma_f16(y[2 * np], a, b[0], b[1]);
-        mma_f16(y[2 * np + 1], a, b[2], b[3]);
+      for (int c = 0; c <= r; ++c) {
+        uint32_t a[4];
+        if (c == r) lda_64(a, sbase + kCsX, 0, 16 * r, lane);
+        else lda_64(a, sbase + kCsA16, 16 * r, 16 * c, lane);
+#pragma unroll
+        for (int np = 0; np < 2; ++np) {
+          uint32_t b[4];
+          ldb_kn_128(b, bufa, cbase + 16 * np, 16 * c, lane);
+          mma_f16(y[2 * np], a, b[0], b[1]);
+          mma_f16(y[2 * np + 1], a, b[2], b[3]);
+        }
       }
       __syncwarp();
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const uint32_t off = swz128(16 * r + g + 8 * hf, cbase + 8 * nt + 2 * q4);
-          u32_at(buf, off) = pack_f16(y[nt][2 * hf], y[nt][2 * hf + 1]);
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint32_t off = swz128(16 * r + g + 8 * hh, cbase + 8 * nt + 2 * q4);
+          u32_at(buf, off) = pack_f16(y[nt][2 * hh], y[nt][2 * hh + 1]);
         }
       __syncwarp();
     }

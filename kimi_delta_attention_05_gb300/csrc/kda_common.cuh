@@ -167,6 +167,11 @@ __device__ __forceinline__ void ldb_nk_64(uint32_t (&b)[4], uint32_t base, int n
   ldsm_x4(b, base + swz64(n0 + ((mi >> 1) << 3) + (lane & 7), k0 + ((mi & 1) << 3)));
 }
 // Same, from storage [k][n] (n contiguous), via the transposing load.
+__device__ __forceinline__ void ldb_kn_64(uint32_t (&b)[4], uint32_t base, int n0, int k0,
+                                          int lane) {
+  int mi = lane >> 3;
+  ldsm_x4_t(b, base + swz64(k0 + ((mi & 1) << 3) + (lane & 7), n0 + ((mi >> 1) << 3)));
+}
 __device__ __forceinline__ void ldb_kn_128(uint32_t (&b)[4], uint32_t base, int n0, int k0,
                                            int lane) {
   int mi = lane >> 3;
