@@ -279,6 +279,11 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
       const uint32_t par = (uint32_t)(ci & 1);
       const unsigned char* stg = smem + st * kStageBytes;
       wait(B(kBarFull + st), phf);
+      const float gk = reinterpret_cast<const float*>(stg + kSGc)[k];
+      if (warp < 2) {  // gamma_C is all these warps read from the stage
+        __syncwarp();
+        if (lane == 0) mbar_arrive_local(B(kBarEmpty + st));
+      }
       wait(B(kBarMma1), par);
       tc_fence_after();
       if (warp >= 2) {
@@ -302,7 +307,10 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_local(B(kBarUn));
+        if (lane == 0) {
+          mbar_arrive_local(B(kBarUn));
+          mbar_arrive_local(B(kBarEmpty + st));  // U tile read
+        }
       }
       wait(B(kBarMma2), par);
       tc_fence_after();
@@ -310,11 +318,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
         // S[:, k] = gamma_C[k] S[:, k] + delta; publish for the next chunk
         float d[32];
         tc_ld32(lane_addr + 64, d);
-        const float gk = reinterpret_cast<const float*>(stg + kSGc)[k];
 #pragma unroll
         for (int j = 0; j < 32; ++j) s[j] = gk * s[j] + d[j];
-        __syncwarp();
-        if (lane == 0) mbar_arrive_local(B(kBarEmpty + st));  // U tile and gamma_C read
         publish_state();
       }
       if (warp < 2) {
