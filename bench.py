@@ -369,7 +369,8 @@ def workload_config(a, inp, world):
            "chunk": CHUNK, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
            "l2": f"inputs+outputs {total_bytes / 1e6:.0f} MB vs 129 MB L2; no flush"
            if total_bytes > 129e6 else "working set fits L2; no flush (small workload)",
-           "compute": "bf16 I/O; fp16/bf16 mma.sync operands, fp32 accumulate and state"}
+           "compute": "bf16 I/O; intra-chunk mma.sync (bf16 A/P, fp16 WY); state tcgen05 "
+                      "(fp16 operands, fp32 tensor-memory accumulators); fp32 state"}
     return cfg
 
 
