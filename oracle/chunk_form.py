@@ -49,8 +49,8 @@ def _sigmoid(x):
 
 
 def chunk_form(q, k, v, g, beta, *, scale, A_log=None, dt_bias=None, lower_bound=-5.0,
-               gate="safe", qk_l2norm=False, l2_eps=1e-6, initial_state=None, cu_seqlens=None,
-               chunk=64, units=None, keep=False):
+               gate="safe", beta_prob=False, qk_l2norm=False, l2_eps=1e-6, initial_state=None,
+               cu_seqlens=None, chunk=64, units=None, keep=False):
     """Same arguments and return values as ``kda_recurrence``; with
     ``keep=True`` also returns a dict {(n, h): [per-chunk dicts]} holding
     Gamma, A, P, T, W, U, U_new, O, S0 and S_end for every chunk."""
@@ -78,7 +78,7 @@ def chunk_form(q, k, v, g, beta, *, scale, A_log=None, dt_bias=None, lower_bound
         n, h = divmod(int(unit), H)
         S = np.zeros((V, K)) if init is None else init[n, h].copy()
         Ah = None if A_log is None else A_log[h]
-        db = np.zeros(K) if dt_bias is None else dt_bias[h]
+        db = np.zeros(K) if (dt_bias is None or gate == "logspace") else dt_bias[h]
         chunks = []
         for c0 in range(cu[n], cu[n + 1], chunk):
             c1 = min(c0 + chunk, cu[n + 1])
@@ -88,7 +88,7 @@ def chunk_form(q, k, v, g, beta, *, scale, A_log=None, dt_bias=None, lower_bound
                 Qc = Qc / np.sqrt((Qc * Qc).sum(-1, keepdims=True) + l2_eps)
                 Kc = Kc / np.sqrt((Kc * Kc).sum(-1, keepdims=True) + l2_eps)
             a = gate_activation(gf[c0:c1, h] + db, Ah, gate, lower_bound)
-            b = _sigmoid(bf[c0:c1, h])
+            b = bf[c0:c1, h] if beta_prob else _sigmoid(bf[c0:c1, h])
             Gam = np.cumsum(a, axis=0)                       # [L, K]
             diff = Gam[:, None, :] - Gam[None, :, :]         # Gamma_i - Gamma_j
             low = np.tril(np.ones((L, L), dtype=bool))       # j <= i

@@ -19,8 +19,12 @@
  *   o_t   = scale * S q_t                   (read-out after the write)
  *
  * Gate forms (fla-kda SKILL.md, "Gate contracts"; fla-kda skill page):
- *   safe   : a = lower_bound * sigmoid(exp(A_log) * z), A_log omitted -> 1
- *   unsafe : a = -exp(A_log) * softplus(z)
+ *   safe     : a = lower_bound * sigmoid(exp(A_log) * z), A_log omitted -> 1
+ *   unsafe   : a = -exp(A_log) * softplus(z)
+ *   logspace : a = g as given (the caller's log-space decay: chunk_kda without
+ *              the in-kernel gate); dt_bias and A_log are not used
+ * beta is taken as logits (beta = sigmoid(logit)) or, with beta_is_prob, as
+ * beta itself (the "beta activation" mode of the same checklist).
  *
  * Everything is evaluated in double precision from the given inputs (bf16
  * inputs reach this code already widened to float, which is exact).  No
@@ -36,6 +40,7 @@
 
 #define ORACLE_GATE_SAFE 1
 #define ORACLE_GATE_UNSAFE 2
+#define ORACLE_GATE_LOGSPACE 3
 
 /* sigmoid in a form that does not overflow for large |x| */
 static double oracle_sigmoid(double x) {
@@ -54,8 +59,8 @@ static double oracle_softplus(double x) {
  * Run the recurrence for a list of (sequence, head) units.
  *
  * q,k,g : [total_tokens, H, K] float    v : [total_tokens, H, V] float
- * beta  : [total_tokens, H] float (logits)
- * A_log : [H] float or NULL (NULL allowed only with the safe gate)
+ * beta  : [total_tokens, H] float (logits, or beta itself with beta_is_prob)
+ * A_log : [H] float or NULL (NULL allowed only with the safe gate; unused by logspace)
  * dt_bias : [H, K] float or NULL (NULL -> 0)
  * init  : [N, H, V, K] float or NULL (NULL -> zero state)
  * bos   : [N+1] token offsets of the sequences (bos[n]..bos[n+1])
@@ -67,12 +72,14 @@ static double oracle_softplus(double x) {
 int kda_oracle_fwd(const float *q, const float *k, const float *v, const float *g,
                    const float *beta, double scale, const float *A_log,
                    const float *dt_bias, double lower_bound, int gate_mode,
-                   int qk_l2norm, double l2_eps, const float *init, double *out,
-                   double *final_state, const int64_t *bos, int64_t N, int64_t H,
-                   int64_t K, int64_t V, const int64_t *units, int64_t n_units,
+                   int beta_is_prob, int qk_l2norm, double l2_eps, const float *init,
+                   double *out, double *final_state, const int64_t *bos, int64_t N,
+                   int64_t H, int64_t K, int64_t V, const int64_t *units, int64_t n_units,
                    int n_threads) {
   if (!q || !k || !v || !g || !beta || !out || !bos) return -1;
-  if (gate_mode != ORACLE_GATE_SAFE && gate_mode != ORACLE_GATE_UNSAFE) return -1;
+  if (gate_mode != ORACLE_GATE_SAFE && gate_mode != ORACLE_GATE_UNSAFE &&
+      gate_mode != ORACLE_GATE_LOGSPACE)
+    return -1;
   if (gate_mode == ORACLE_GATE_UNSAFE && !A_log) return -1;
   if (K <= 0 || V <= 0 || H <= 0 || N < 0) return -1;
   int64_t total_units = units ? n_units : N * H;
@@ -100,13 +107,13 @@ int kda_oracle_fwd(const float *q, const float *k, const float *v, const float *
         const float *kr = k + (t * H + h) * K;
         const float *vr = v + (t * H + h) * V;
         const float *gr = g + (t * H + h) * K;
-        double b = oracle_sigmoid((double)beta[t * H + h]);
+        double b = beta_is_prob ? (double)beta[t * H + h] : oracle_sigmoid((double)beta[t * H + h]);
         /* gate activation, per key channel */
         for (int64_t c = 0; c < K; ++c) {
           double z = (double)gr[c] + (dt_bias ? (double)dt_bias[h * K + c] : 0.0);
-          double a = (gate_mode == ORACLE_GATE_SAFE)
-                         ? lower_bound * oracle_sigmoid(amul * z)
-                         : -amul * oracle_softplus(z);
+          double a = (gate_mode == ORACLE_GATE_LOGSPACE) ? (double)gr[c]
+                     : (gate_mode == ORACLE_GATE_SAFE) ? lower_bound * oracle_sigmoid(amul * z)
+                                                       : -amul * oracle_softplus(z);
           dec[c] = exp(a);
         }
         /* optional L2 normalisation of q and k */

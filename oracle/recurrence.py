@@ -19,6 +19,7 @@ _lib = None
 
 GATE_SAFE = 1
 GATE_UNSAFE = 2
+GATE_LOGSPACE = 3
 
 
 def build(force: bool = False) -> str:
@@ -37,7 +38,7 @@ def configure(lib):
     lib.kda_oracle_fwd.restype = ctypes.c_int
     lib.kda_oracle_fwd.argtypes = [
         P, P, P, P, P, ctypes.c_double, P, P, ctypes.c_double, ctypes.c_int, ctypes.c_int,
-        ctypes.c_double, P, P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+        ctypes.c_int, ctypes.c_double, P, P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
         ctypes.c_int64, P, ctypes.c_int64, ctypes.c_int]
     lib.kda_oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -74,9 +75,12 @@ def gate_activation(z, A_log_h, gate: str, lower_bound: float):
 
     fla-kda SKILL.md, "Gate contracts": with a lower bound the activation is
     lower_bound * sigmoid(exp(A_log) * z) (A_log omitted -> multiplier one);
-    without one it is -exp(A_log) * softplus(z).
+    without one it is -exp(A_log) * softplus(z).  "logspace" is chunk_kda
+    without the in-kernel gate: z (= g, no bias) is already the log decay.
     """
     z = np.asarray(z, dtype=np.float64)
+    if gate == "logspace":
+        return z
     if gate == "safe":
         m = 1.0 if A_log_h is None else np.exp(np.float64(A_log_h))
         x = m * z
@@ -91,11 +95,13 @@ def gate_activation(z, A_log_h, gate: str, lower_bound: float):
 
 
 def kda_recurrence(q, k, v, g, beta, *, scale, A_log=None, dt_bias=None, lower_bound=-5.0,
-                   gate="safe", qk_l2norm=False, l2_eps=1e-6, initial_state=None,
-                   cu_seqlens=None, units=None, threads=0, want_final=True):
+                   gate="safe", beta_prob=False, qk_l2norm=False, l2_eps=1e-6,
+                   initial_state=None, cu_seqlens=None, units=None, threads=0, want_final=True):
     """fp64 token recurrence.
 
-    q, k, g: [B, T, H, K]; v: [B, T, H, V]; beta: [B, T, H] (logits).
+    q, k, g: [B, T, H, K]; v: [B, T, H, V]; beta: [B, T, H] (logits, or beta
+    itself with ``beta_prob``).  ``gate``: "safe", "unsafe" or "logspace" (g is
+    the log decay; A_log and dt_bias unused).
     With ``cu_seqlens`` ([N+1] int64) B must be 1 and the sequences are the
     packed rows cu[n]..cu[n+1]; otherwise sequence n is batch row n.
     initial_state: [N, H, V, K] or None.  ``units``: optional list of n*H+h
@@ -123,10 +129,11 @@ def kda_recurrence(q, k, v, g, beta, *, scale, A_log=None, dt_bias=None, lower_b
     out = np.full((B, T, H, V), np.nan, dtype=np.float64)
     final = np.full((N, H, V, K), np.nan, dtype=np.float64) if want_final else None
     u = None if units is None else np.ascontiguousarray(np.asarray(units, dtype=np.int64))
-    mode = {"safe": GATE_SAFE, "unsafe": GATE_UNSAFE}[gate]
+    mode = {"safe": GATE_SAFE, "unsafe": GATE_UNSAFE, "logspace": GATE_LOGSPACE}[gate]
     rc = lib.kda_oracle_fwd(
         _ptr(qf), _ptr(kf), _ptr(vf), _ptr(gf), _ptr(bf), float(scale), _ptr(Al), _ptr(db),
-        float(lower_bound), mode, int(bool(qk_l2norm)), float(l2_eps), _ptr(init), _ptr(out),
+        float(lower_bound), mode, int(bool(beta_prob)), int(bool(qk_l2norm)), float(l2_eps),
+        _ptr(init), _ptr(out),
         _ptr(final), _ptr(cu), N, H, K, V, _ptr(u), 0 if u is None else len(u), int(threads))
     if rc != 0:
         raise ValueError("kda_oracle_fwd rejected its arguments")

@@ -27,8 +27,13 @@ MUTATIONS = {
     "dropped A_log multiplier": ("lower_bound * oracle_sigmoid(amul * z)",
                                  "lower_bound * oracle_sigmoid(z)"),
     "dropped dt_bias": ("(dt_bias ? (double)dt_bias[h * K + c] : 0.0)", "0.0"),
-    "beta without sigmoid": ("double b = oracle_sigmoid((double)beta[t * H + h]);",
-                             "double b = (double)beta[t * H + h];"),
+    "beta without sigmoid": (": oracle_sigmoid((double)beta[t * H + h]);",
+                             ": (double)beta[t * H + h];"),
+    "beta-as-probability mode still applies the sigmoid": (
+        "double b = beta_is_prob ? (double)beta[t * H + h] :",
+        "double b = beta_is_prob ? oracle_sigmoid((double)beta[t * H + h]) :"),
+    "log-space gate takes the bias": ("double a = (gate_mode == ORACLE_GATE_LOGSPACE) ? (double)gr[c]",
+                                      "double a = (gate_mode == ORACLE_GATE_LOGSPACE) ? z"),
     "transposed initial state": ("init[(n * H + h) * V * K + i]",
                                  "init[(n * H + h) * V * K + (i % K) * V + i / K]"),
     "l2 norm without sqrt": ("double rq = 1.0 / sqrt(nq + l2_eps)",
@@ -45,6 +50,7 @@ def _pin_suite():
         ("exact rational unsafe", lambda: pins.test_exact_rational_example("unsafe")),
         ("affine safe", lambda: pins.test_affine_map_brute_force(3, 2, 4, "safe")),
         ("affine unsafe", lambda: pins.test_affine_map_brute_force(2, 3, 4, "unsafe")),
+        ("affine logspace, beta given", lambda: pins.test_affine_map_brute_force_modes(3, 2, 4)),
         ("beta zero", lambda: pins.test_beta_zero_closed_form("unsafe")),
         ("gate", pins.test_gate_through_c_recurrence),
         ("fixed point", pins.test_delta_rule_fixed_point),

@@ -171,6 +171,33 @@ def test_affine_map_brute_force(K, V, T, gate):
     np.testing.assert_allclose(fin[0, 0], S, rtol=1e-13, atol=1e-13)
 
 
+@pytest.mark.parametrize("K,V,T", [(3, 2, 4), (2, 3, 3)])
+def test_affine_map_brute_force_modes(K, V, T):
+    """The same brute force for the caller-gated mode (g is the log decay a_t
+    itself; dt_bias and A_log are given but must not be used) with beta given
+    as beta itself (no sigmoid)."""
+    q, k = _rand(1, T, 1, K), _rand(1, T, 1, K)
+    a_in = (-np.abs(_rand(1, T, 1, K))).astype(np.float32)  # log decays <= 0
+    v = _rand(1, T, 1, V)
+    b = np.float32(np.random.default_rng(7).uniform(0.05, 0.95, (1, T, 1)))
+    A_log, dtb, init = np.float32([0.4]), _rand(1, K, std=0.5), _rand(1, 1, V, K)
+    kw = dict(scale=0.7, gate="logspace", beta_prob=True, A_log=A_log, dt_bias=dtb,
+              initial_state=init)
+    out, fin = oracle.kda_recurrence(q, k, v, a_in, b, **kw)
+    S = init[0, 0].astype(np.float64)
+    for t in range(T):
+        bt = np.float64(b[0, t, 0])
+        kt = k[0, t, 0].astype(np.float64)
+        M = np.diag(np.exp(a_in[0, t, 0].astype(np.float64))) @ (np.eye(K) - bt * np.outer(kt, kt))
+        S = S @ M + bt * np.outer(v[0, t, 0].astype(np.float64), kt)
+        np.testing.assert_allclose(out[0, t, 0], 0.7 * S @ q[0, t, 0].astype(np.float64),
+                                   rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(fin[0, 0], S, rtol=1e-13, atol=1e-13)
+    out2, fin2 = oracle.chunk_form(q, k, v, a_in, b, chunk=2, **kw)
+    np.testing.assert_allclose(out2, out, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(fin2, fin, rtol=1e-11, atol=1e-12)
+
+
 # ---------------------------------------------------------------------------
 # I2: beta = 0 -> diagonal-gated linear read-out, closed form
 # ---------------------------------------------------------------------------
