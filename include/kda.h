@@ -36,7 +36,8 @@ extern "C" {
 #define KDA_ERR_NULL_ARG 1        /* a required pointer is NULL */
 #define KDA_ERR_HEAD_DIM 2        /* K or V is not 128 */
 #define KDA_ERR_SHAPE 3           /* negative size, or N inconsistent with B */
-#define KDA_ERR_GATE_FLAGS 4      /* not exactly one of KDA_GATE_SAFE / KDA_GATE_UNSAFE */
+#define KDA_ERR_GATE_FLAGS 4      /* not exactly one of KDA_GATE_SAFE / _UNSAFE / _LOGSPACE,
+                                     or an unknown flag bit */
 #define KDA_ERR_LOWER_BOUND 5     /* safe gate with lower_bound outside [-5, 0) */
 #define KDA_ERR_A_LOG_REQUIRED 6  /* unsafe gate with A_log == NULL */
 #define KDA_ERR_STATE_DTYPE 7     /* state_dtype not KDA_DTYPE_F32 / KDA_DTYPE_BF16 */
@@ -51,6 +52,13 @@ extern "C" {
 #define KDA_GATE_SAFE 0x1u   /* lower_bound * sigmoid(exp(A_log) * (g + dt_bias)) */
 #define KDA_GATE_UNSAFE 0x2u /* -exp(A_log) * softplus(g + dt_bias) */
 #define KDA_QK_L2NORM 0x4u   /* L2-normalise q and k per token inside the kernel */
+/* g already holds the log-space decay a_t (natural log, <= 0 expected; values
+ * are not checked): chunk_kda without the in-kernel gate (fla-kda SKILL.md,
+ * "Gate contracts").  A_log, dt_bias and lower_bound are not used. */
+#define KDA_GATE_LOGSPACE 0x8u
+/* beta already holds beta in [0, 1] (no sigmoid applied): the beta-activation
+ * mode named in the same page's correctness checklist. */
+#define KDA_BETA_PROB 0x10u
 
 /* ---- state dtypes ---- */
 #define KDA_DTYPE_F32 0
@@ -63,7 +71,9 @@ extern "C" {
  * on the given stream, so buffers must stay valid until it completes).
  *
  *  q, k, g : bf16 [B, T, H, 128]      v, out : bf16 [B, T, H, 128]
- *  beta    : bf16 [B, T, H]  (logits; sigmoid applied inside)
+ *  beta    : bf16 [B, T, H]  (logits, sigmoid applied inside; with KDA_BETA_PROB
+ *            beta itself)
+ *  g       : raw gate logits, or with KDA_GATE_LOGSPACE the log decays a_t
  *  out     : written completely for every token of every sequence
  *  A_log   : fp32 [H]       (NULL only with KDA_GATE_SAFE -> multiplier 1)
  *  dt_bias : fp32 [H, 128]  (NULL -> 0)

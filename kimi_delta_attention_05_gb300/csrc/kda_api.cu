@@ -67,9 +67,12 @@ int validate(const kda_fwd_args* a, int64_t* num_slots, size_t* header_bytes) {
   if (!a->q || !a->k || !a->v || !a->g || !a->beta || !a->out) return KDA_ERR_NULL_ARG;
   if (a->K != kHeadDim || a->V != kHeadDim) return KDA_ERR_HEAD_DIM;
   if (a->B < 0 || a->T < 0 || a->H < 0 || a->N < 0 || a->H > 65535) return KDA_ERR_SHAPE;
-  const uint32_t gate = a->flags & (KDA_GATE_SAFE | KDA_GATE_UNSAFE);
-  if (gate != KDA_GATE_SAFE && gate != KDA_GATE_UNSAFE) return KDA_ERR_GATE_FLAGS;
-  if (a->flags & ~(KDA_GATE_SAFE | KDA_GATE_UNSAFE | KDA_QK_L2NORM)) return KDA_ERR_GATE_FLAGS;
+  const uint32_t gate = a->flags & (KDA_GATE_SAFE | KDA_GATE_UNSAFE | KDA_GATE_LOGSPACE);
+  if (gate != KDA_GATE_SAFE && gate != KDA_GATE_UNSAFE && gate != KDA_GATE_LOGSPACE)
+    return KDA_ERR_GATE_FLAGS;
+  if (a->flags & ~(KDA_GATE_SAFE | KDA_GATE_UNSAFE | KDA_GATE_LOGSPACE | KDA_QK_L2NORM |
+                   KDA_BETA_PROB))
+    return KDA_ERR_GATE_FLAGS;
   if (gate == KDA_GATE_SAFE && !(a->lower_bound >= -5.0f && a->lower_bound < 0.0f))
     return KDA_ERR_LOWER_BOUND;
   if (gate == KDA_GATE_UNSAFE && !a->A_log) return KDA_ERR_A_LOG_REQUIRED;
@@ -149,7 +152,9 @@ static int fwd_impl(const kda_fwd_args* a, void* workspace, size_t workspace_byt
     cp.A_log = a->A_log;
     cp.dt_bias = a->dt_bias;
     cp.lower_bound = a->lower_bound;
-    cp.gate_unsafe = (a->flags & KDA_GATE_UNSAFE) ? 1 : 0;
+    cp.gate_mode = (a->flags & KDA_GATE_UNSAFE) ? kGateUnsafe
+                   : (a->flags & KDA_GATE_LOGSPACE) ? kGateLogspace : kGateSafe;
+    cp.beta_prob = (a->flags & KDA_BETA_PROB) ? 1 : 0;
     cp.l2norm = (a->flags & KDA_QK_L2NORM) ? 1 : 0;
     cp.cu = a->cu_seqlens;
     cp.chunk_off = chunk_off;

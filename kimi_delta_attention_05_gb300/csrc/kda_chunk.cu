@@ -104,16 +104,19 @@ __device__ __forceinline__ void scale_bfrag(uint32_t& b0, uint32_t& b1, uint32_t
 //   unsafe: a = -amul softplus(z) = -amul ln(1 + e^z), so exp(a) = 2^(-amul lg2(1 + 2^(z lg2 e)));
 //           for large z, 1 + 2^(.) rounds to 2^(.) and lg2 gives z lg2 e back; past the fp32
 //           range it is +inf and exp(a) = 0, the limit;
-//   safe:   a = lb sigmoid(amul z).
+//   safe:   a = lb sigmoid(amul z);
+//   log-space: z is g itself, already the log decay a.
 // Only exp(a) is used, so what matters is the absolute error of a: lg2(1 + t)
 // loses at most ~1e-7 of it when t is tiny, far below what exp(a) resolves.
 // (amul_log2e = amul lg2 e for the safe gate, amul for the unsafe one.)
-__device__ __forceinline__ float gate_decay(float z, float amul_log2e, float lb_log2e, bool unsafe) {
-  if (unsafe) return ex2(-amul_log2e * lg2(1.0f + ex2(z * kLog2e)));
+template <int kGate>
+__device__ __forceinline__ float gate_decay(float z, float amul_log2e, float lb_log2e) {
+  if (kGate == kGateLogspace) return ex2(z * kLog2e);
+  if (kGate == kGateUnsafe) return ex2(-amul_log2e * lg2(1.0f + ex2(z * kLog2e)));
   return ex2(lb_log2e * rcp_approx(1.0f + ex2(-amul_log2e * z)));
 }
 
-template <bool kUnsafe, bool kL2>
+template <int kGate, bool kL2>
 __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_t num_items) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -164,9 +167,9 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
       cp_async16(sbase + dst + row * 256 + ((ch ^ (row & 7)) << 4), sp, ok ? 16 : 0);
     }
   };
-  // beta logit of token tid (-inf past the chunk end, so that beta = 0 there)
+  // beta input (logit, or beta itself) of token tid; 0 past the chunk end
   auto load_beta = [&](const Item& it) {
-    return tid < it.L ? bf16_to_f(p.beta[(it.t0 + tid) * H + it.h]) : -INFINITY;
+    return tid < it.L ? bf16_to_f(p.beta[(it.t0 + tid) * H + it.h]) : 0.f;
   };
   int64_t item = blockIdx.x;
   if (item >= num_items) return;
@@ -190,7 +193,8 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
   const int64_t next = item + gridDim.x;
   Item nxt = cur;
   if (next < num_items) nxt = locate(next);
-  if (tid < kChunk) sBeta[tid] = rcp_approx(1.0f + ex2(-blogit * kLog2e));
+  if (tid < kChunk)
+    sBeta[tid] = tid >= L ? 0.f : (p.beta_prob ? blogit : rcp_approx(1.0f + ex2(-blogit * kLog2e)));
   cp_async_wait<1>();  // q, k, g of this item (v may still be in flight)
   __syncthreads();
 
@@ -228,10 +232,12 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
   float d[8][4];
   float inv[4];  // 1 / (clamped product over this half)
   {
-    const float4 dtb = p.dt_bias ? *reinterpret_cast<const float4*>(p.dt_bias + h * kHeadDim + c0)
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 dtb = (p.dt_bias && kGate != kGateLogspace)
+                           ? *reinterpret_cast<const float4*>(p.dt_bias + h * kHeadDim + c0)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
     const float dtbv[4] = {dtb.x, dtb.y, dtb.z, dtb.w};
-    const float amul_log2e = (p.A_log ? expf(p.A_log[h]) : 1.0f) * (kUnsafe ? 1.0f : kLog2e);
+    const float amul_log2e = (p.A_log && kGate != kGateLogspace ? expf(p.A_log[h]) : 1.0f) *
+                             (kGate == kGateUnsafe ? 1.0f : kLog2e);
     const float lb_log2e = p.lower_bound * kLog2e;
     float D[4] = {1.f, 1.f, 1.f, 1.f}, Dc[4] = {1.f, 1.f, 1.f, 1.f};
 #pragma unroll
@@ -242,7 +248,7 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
       const float gz[4] = {g01.x, g01.y, g23.x, g23.y};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        float e = gate_decay(gz[c] + dtbv[c], amul_log2e, lb_log2e, kUnsafe);
+        float e = gate_decay<kGate>(gz[c] + dtbv[c], amul_log2e, lb_log2e);
         if (t >= L) e = 1.f;
         d[j][c] = e;
         D[c] *= e;
@@ -587,6 +593,11 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
   cp_async_wait<0>();
 }
 
+template <int kGate, bool kL2>
+static void launch_variant(const ChunkParams& p, unsigned grid, int64_t items, cudaStream_t stream) {
+  kda_chunk_kernel<kGate, kL2><<<grid, 256, kChunkSmem, stream>>>(p, items);
+}
+
 void launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t stream) {
   // persistent grid: two CTAs per SM (the shared-memory and register budget), or fewer items
   int dev = 0, sms = 0;
@@ -594,23 +605,35 @@ void launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t s
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t items = num_slots * p.H;
   const unsigned grid = (unsigned)min(items, (int64_t)(2 * (sms > 0 ? sms : 1)));
-  if (p.gate_unsafe) {
-    if (p.l2norm) kda_chunk_kernel<true, true><<<grid, 256, kChunkSmem, stream>>>(p, items);
-    else kda_chunk_kernel<true, false><<<grid, 256, kChunkSmem, stream>>>(p, items);
-  } else {
-    if (p.l2norm) kda_chunk_kernel<false, true><<<grid, 256, kChunkSmem, stream>>>(p, items);
-    else kda_chunk_kernel<false, false><<<grid, 256, kChunkSmem, stream>>>(p, items);
+  const bool l2 = p.l2norm != 0;
+  switch (p.gate_mode) {
+    case kGateUnsafe:
+      if (l2) launch_variant<kGateUnsafe, true>(p, grid, items, stream);
+      else launch_variant<kGateUnsafe, false>(p, grid, items, stream);
+      break;
+    case kGateLogspace:
+      if (l2) launch_variant<kGateLogspace, true>(p, grid, items, stream);
+      else launch_variant<kGateLogspace, false>(p, grid, items, stream);
+      break;
+    default:
+      if (l2) launch_variant<kGateSafe, true>(p, grid, items, stream);
+      else launch_variant<kGateSafe, false>(p, grid, items, stream);
   }
 }
 
 cudaError_t prepare_chunk_kernel() {
-  cudaError_t e = cudaSuccess;
   const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(kda_chunk_kernel<true, true>, attr, kChunkSmem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(kda_chunk_kernel<true, false>, attr, kChunkSmem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(kda_chunk_kernel<false, true>, attr, kChunkSmem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(kda_chunk_kernel<false, false>, attr, kChunkSmem);
-  return e;
+  const void* fns[] = {(const void*)kda_chunk_kernel<kGateSafe, true>,
+                       (const void*)kda_chunk_kernel<kGateSafe, false>,
+                       (const void*)kda_chunk_kernel<kGateUnsafe, true>,
+                       (const void*)kda_chunk_kernel<kGateUnsafe, false>,
+                       (const void*)kda_chunk_kernel<kGateLogspace, true>,
+                       (const void*)kda_chunk_kernel<kGateLogspace, false>};
+  for (const void* f : fns) {
+    const cudaError_t e = cudaFuncSetAttribute(f, attr, kChunkSmem);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace kda

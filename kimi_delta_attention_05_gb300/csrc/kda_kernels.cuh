@@ -5,13 +5,18 @@
 
 namespace kda {
 
+// Gate forms: lb sigmoid(exp(A_log) z), -exp(A_log) softplus(z), or g given as
+// the log decay (no activation).
+constexpr int kGateSafe = 0, kGateUnsafe = 1, kGateLogspace = 2;
+
 // Intra-chunk stage (one CTA per (chunk slot, head)).
 struct ChunkParams {
   const uint16_t *q, *k, *v, *g, *beta;  // bf16 [tokens, H, 128] / [tokens, H]
   const float* A_log;                     // [H] or nullptr (safe gate only)
   const float* dt_bias;                   // [H, 128] or nullptr
   float lower_bound;
-  int gate_unsafe;                        // 1: -exp(A_log) softplus, 0: lb sigmoid
+  int gate_mode;                          // kGateSafe / kGateUnsafe / kGateLogspace
+  int beta_prob;                          // 1: beta holds beta itself, 0: logits
   int l2norm;
   const int64_t* cu;                      // [N+1] or nullptr (dense)
   const int64_t* chunk_off;               // [N+1] chunk prefix (varlen only)

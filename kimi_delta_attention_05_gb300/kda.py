@@ -16,6 +16,8 @@ from . import _build
 KDA_GATE_SAFE = 0x1
 KDA_GATE_UNSAFE = 0x2
 KDA_QK_L2NORM = 0x4
+KDA_GATE_LOGSPACE = 0x8
+KDA_BETA_PROB = 0x10
 KDA_DTYPE_F32 = 0
 KDA_DTYPE_BF16 = 1
 HEAD_DIM = 128
@@ -86,16 +88,20 @@ def _ptr(t):
 
 def make_args(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_bound=None,
               initial_state=None, final_state=None, cu_seqlens=None, qk_l2norm=False,
-              gate=None) -> kda_fwd_args:
+              gate=None, beta_prob=False) -> kda_fwd_args:
     """Build the C argument block from tensors (no checks beyond shapes;
-    the library validates)."""
+    the library validates).  ``gate``: "safe", "unsafe" or "logspace" (g holds
+    the log decay); default from ``lower_bound``.  ``beta_prob``: beta holds
+    beta itself instead of logits."""
     B, T, H, K = q.shape
     V = v.shape[-1]
     if gate is None:
         gate = "unsafe" if lower_bound is None else "safe"
-    flags = KDA_GATE_SAFE if gate == "safe" else KDA_GATE_UNSAFE
+    flags = {"safe": KDA_GATE_SAFE, "unsafe": KDA_GATE_UNSAFE, "logspace": KDA_GATE_LOGSPACE}[gate]
     if qk_l2norm:
         flags |= KDA_QK_L2NORM
+    if beta_prob:
+        flags |= KDA_BETA_PROB
     N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else B
     st = initial_state if initial_state is not None else final_state
     sd = KDA_DTYPE_BF16 if (st is not None and st.dtype == torch.bfloat16) else KDA_DTYPE_F32
@@ -119,7 +125,7 @@ def workspace_bytes(args: kda_fwd_args) -> int:
 
 def kda_fwd(q, k, v, g, beta, scale, out=None, A_log=None, dt_bias=None, lower_bound=None,
             initial_state=None, final_state=None, cu_seqlens=None, *, qk_l2norm=False,
-            gate=None, workspace=None, stream=None):
+            gate=None, beta_prob=False, workspace=None, stream=None):
     """KDA chunked forward on device tensors; returns ``out``.
 
     Mirrors the flashkda.fwd argument list: q, k, g [B,T,H,128] bf16, v
@@ -133,7 +139,7 @@ def kda_fwd(q, k, v, g, beta, scale, out=None, A_log=None, dt_bias=None, lower_b
     if out is None:
         out = torch.empty_like(v)
     a = make_args(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
-                  final_state, cu_seqlens, qk_l2norm, gate)
+                  final_state, cu_seqlens, qk_l2norm, gate, beta_prob)
     need = int(lib.kda_fwd_workspace_bytes(ctypes.byref(a)))
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)

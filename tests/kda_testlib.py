@@ -43,7 +43,7 @@ def run_gpu(inp, *, final=True, a_log=True, dt_bias=True, stream=None):
     kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], inp["scale"], out,
             d["A_log"] if a_log else None, d["dt_bias"] if dt_bias else None, lb,
             d["initial_state"], fin, d["cu_seqlens"], qk_l2norm=inp["qk_l2norm"],
-            gate=inp["gate"], stream=stream)
+            gate=inp["gate"], beta_prob=inp.get("beta_prob", False), stream=stream)
     torch.cuda.synchronize()
     o = out.float().cpu().numpy().astype(np.float64)
     f = None if fin is None else fin.float().cpu().numpy().astype(np.float64)
@@ -54,7 +54,8 @@ def run_oracle(inp, *, units=None, a_log=True, dt_bias=True):
     return oracle.kda_recurrence(
         inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], scale=inp["scale"],
         A_log=inp["A_log"] if a_log else None, dt_bias=inp["dt_bias"] if dt_bias else None,
-        lower_bound=inp["lower_bound"], gate=inp["gate"], qk_l2norm=inp["qk_l2norm"],
+        lower_bound=inp["lower_bound"], gate=inp["gate"], beta_prob=inp.get("beta_prob", False),
+        qk_l2norm=inp["qk_l2norm"],
         initial_state=inp["initial_state"], cu_seqlens=inp["cu_seqlens"], units=units)
 
 

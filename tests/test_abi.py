@@ -62,7 +62,9 @@ def _call(a, ws=None, nbytes=0):
     (dict(q=None), 1), (dict(out=None), 1), (dict(beta=None), 1),
     (dict(K=64), 2), (dict(V=256), 2),
     (dict(T=-1), 3), (dict(N=3), 3), (dict(H=70000), 3),
-    (dict(flags=0), 4), (dict(flags=3), 4), (dict(flags=1 | 0x100), 4),
+    (dict(flags=0), 4), (dict(flags=3), 4), (dict(flags=1 | 0x100), 4), (dict(flags=1 | 0x20), 4),
+    (dict(flags=K.KDA_GATE_LOGSPACE | K.KDA_GATE_SAFE), 4),
+    (dict(flags=K.KDA_GATE_LOGSPACE | K.KDA_GATE_UNSAFE), 4),
     (dict(lower_bound=0.0), 5), (dict(lower_bound=-5.5), 5), (dict(lower_bound=float("nan")), 5),
     (dict(flags=K.KDA_GATE_UNSAFE, A_log=None), 6),
     (dict(initial_state=FAKE, state_dtype=7), 7),
@@ -73,6 +75,17 @@ def test_invalid_arguments_rejected(over, code):
     a = _valid_args(**over)
     assert _call(a, FAKE, 1 << 40) == code
     assert K.load_library().kda_fwd_workspace_bytes(ctypes.byref(a)) == 0
+
+
+def test_logspace_gate_and_beta_prob_accepted():
+    """The caller-gated mode needs no A_log and ignores lower_bound; beta given
+    as beta itself combines with any gate form."""
+    lib = K.load_library()
+    for flags in (K.KDA_GATE_LOGSPACE, K.KDA_GATE_LOGSPACE | K.KDA_BETA_PROB,
+                  K.KDA_GATE_UNSAFE | K.KDA_BETA_PROB | K.KDA_QK_L2NORM):
+        a = _valid_args(flags=flags, A_log=None if flags & K.KDA_GATE_LOGSPACE else FAKE,
+                        lower_bound=0.0)
+        assert lib.kda_fwd_workspace_bytes(ctypes.byref(a)) > 0
 
 
 def test_workspace_checked_before_launch():

@@ -99,6 +99,31 @@ def test_route_parity_safe_vs_unsafe_on_bounded_gates():
     tl.check_out(ob, ro, "unsafe route")
 
 
+@pytest.mark.parametrize("scale_a", [1.0, 6.0])
+def test_logspace_gate(scale_a):
+    """g given as the log decay itself (no in-kernel gate): a = -|N(0, s)| per
+    channel and token; A_log and dt_bias are passed but must be ignored."""
+    inp = make_inputs(WORKLOADS["dense_batch"], B=2, T=200, H=2, seed=21)
+    gen = torch.Generator().manual_seed(22)
+    a = -(torch.randn(inp["g"].shape, generator=gen) * scale_a).abs()
+    inp = dict(inp, g=a.to(torch.bfloat16), gate="logspace", final_state="f32")
+    _full_check(inp, f"logspace gate s={scale_a}")
+
+
+@pytest.mark.parametrize("gate", ["safe", "unsafe", "logspace"])
+def test_beta_given_as_probability(gate):
+    """beta holds beta itself (no sigmoid in the kernel), values in [0, 1]
+    including the ends."""
+    inp = make_inputs(WORKLOADS["packed_varlen"], lengths=[130, 7, 64, 200], H=2, seed=23)
+    b = torch.sigmoid(inp["beta"].float())
+    b[:, ::17] = 0.0
+    b[:, 5::23] = 1.0
+    inp = dict(inp, beta=b.to(torch.bfloat16), beta_prob=True, gate=gate)
+    if gate == "logspace":
+        inp["g"] = (-(inp["g"].float().abs())).to(torch.bfloat16)
+    _full_check(inp, f"beta given ({gate})")
+
+
 def test_split_chain_on_gpu():
     """Running [0, s) then [s, T) with final -> initial equals one call."""
     inp = make_inputs(WORKLOADS["dense_batch"], B=1, T=300, H=2, seed=16)
