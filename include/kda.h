@@ -131,6 +131,20 @@ int kda_fwd(const kda_fwd_args *args, void *workspace, size_t workspace_bytes, v
 int kda_fwd_profiled(const kda_fwd_args *args, void *workspace, size_t workspace_bytes,
                      void *stream, void *const events[3]);
 
+/*
+ * The same forward pass token by token: the fused_recurrent_kda entry point of
+ * the fla KDA code (fla-kda SKILL.md names chunk_kda and fused_recurrent_kda as
+ * its public entry points).  For decoding, i.e. one or a few tokens per
+ * sequence: each (sequence, head) streams its state from initial_state through
+ * registers to final_state once, with no workspace (none is taken).
+ * Arguments, flags, layouts and error codes as kda_fwd; final_state may be the
+ * same buffer as initial_state (in-place state update).  Asynchronous on
+ * `stream` (cudaStream_t or NULL); returns KDA_ERR_LAUNCH if the launch fails.
+ * Cost grows with the tokens per sequence (a serial loop): prefer kda_fwd for
+ * prefill.
+ */
+int kda_fwd_recurrent(const kda_fwd_args *args, void *stream);
+
 /* Number of kernel launches kda_fwd makes for these arguments (0 if none or
  * if the arguments are invalid). */
 int kda_fwd_launches(const kda_fwd_args *args);

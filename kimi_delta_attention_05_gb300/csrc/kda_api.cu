@@ -197,6 +197,39 @@ extern "C" int kda_fwd_profiled(const kda_fwd_args* a, void* workspace, size_t w
   return fwd_impl(a, workspace, workspace_bytes, stream, events);
 }
 
+extern "C" int kda_fwd_recurrent(const kda_fwd_args* a, void* stream_ptr) {
+  int64_t slots = 0;
+  size_t header = 0;
+  const int rc = validate(a, &slots, &header);
+  if (rc != KDA_OK) return rc;
+  if (a->N == 0 || a->H == 0) return KDA_OK;
+  RecurrentParams rp;
+  rp.q = static_cast<const uint16_t*>(a->q);
+  rp.k = static_cast<const uint16_t*>(a->k);
+  rp.v = static_cast<const uint16_t*>(a->v);
+  rp.g = static_cast<const uint16_t*>(a->g);
+  rp.beta = static_cast<const uint16_t*>(a->beta);
+  rp.out = static_cast<uint16_t*>(a->out);
+  rp.A_log = a->A_log;
+  rp.dt_bias = a->dt_bias;
+  rp.lower_bound = a->lower_bound;
+  rp.scale = a->scale;
+  rp.gate_mode = (a->flags & KDA_GATE_UNSAFE) ? kGateUnsafe
+                 : (a->flags & KDA_GATE_LOGSPACE) ? kGateLogspace : kGateSafe;
+  rp.beta_prob = (a->flags & KDA_BETA_PROB) ? 1 : 0;
+  rp.l2norm = (a->flags & KDA_QK_L2NORM) ? 1 : 0;
+  rp.init = a->initial_state;
+  rp.final_state = a->final_state;
+  rp.state_bf16 = a->state_dtype == KDA_DTYPE_BF16 ? 1 : 0;
+  rp.cu = a->cu_seqlens;
+  rp.N = a->N;
+  rp.T = a->T;
+  rp.H = a->H;
+  launch_recurrent_kernel(rp, reinterpret_cast<cudaStream_t>(stream_ptr));
+  if (cudaGetLastError() != cudaSuccess) return KDA_ERR_LAUNCH;
+  return KDA_OK;
+}
+
 extern "C" int kda_fwd_launches(const kda_fwd_args* a) {
   int64_t slots = 0;
   size_t header = 0;

@@ -38,6 +38,26 @@ struct StateParams {
   const unsigned char* ws;
 };
 
+// Token-by-token path (one CTA per (sequence, head, 32-row value slab)).
+struct RecurrentParams {
+  const uint16_t *q, *k, *v, *g, *beta;  // bf16 [tokens, H, 128] / [tokens, H]
+  uint16_t* out;                          // bf16 [tokens, H, 128]
+  const float* A_log;
+  const float* dt_bias;
+  float lower_bound;
+  float scale;
+  int gate_mode;
+  int beta_prob;
+  int l2norm;
+  const void* init;                       // [N, H, 128, 128] or nullptr
+  void* final_state;                      // [N, H, 128, 128] or nullptr (may equal init)
+  int state_bf16;
+  const int64_t* cu;                      // [N+1] or nullptr (dense)
+  int64_t N, T, H;
+};
+
+void launch_recurrent_kernel(const RecurrentParams& p, cudaStream_t s);
+cudaError_t prepare_recurrent_kernel();
 void launch_chunk_offsets(const int64_t* cu, int64_t N, int64_t* chunk_off, cudaStream_t s);
 void launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t s);
 void launch_state_kernel(const StateParams& p, cudaStream_t s);

@@ -78,6 +78,8 @@ def load_library(build_if_missing: bool = True):
         lib.kda_fwd_launches.argtypes = [ctypes.POINTER(kda_fwd_args)]
         lib.kda_get_status.restype = ctypes.c_int
         lib.kda_get_status.argtypes = [ctypes.c_int]
+        lib.kda_fwd_recurrent.restype = ctypes.c_int
+        lib.kda_fwd_recurrent.argtypes = [ctypes.POINTER(kda_fwd_args), P]
         _lib = lib
     return _lib
 
@@ -146,6 +148,23 @@ def kda_fwd(q, k, v, g, beta, scale, out=None, A_log=None, dt_bias=None, lower_b
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
     rc = lib.kda_fwd(ctypes.byref(a), ctypes.c_void_p(workspace.data_ptr()), need,
                      ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise KdaError(rc, lib.kda_error_string(rc).decode())
+    return out
+
+
+def kda_fwd_recurrent(q, k, v, g, beta, scale, out=None, A_log=None, dt_bias=None,
+                      lower_bound=None, initial_state=None, final_state=None, cu_seqlens=None, *,
+                      qk_l2norm=False, gate=None, beta_prob=False, stream=None):
+    """Token-by-token forward (decoding path, no workspace); same arguments as
+    :func:`kda_fwd`.  ``final_state`` may be ``initial_state`` itself."""
+    lib = load_library()
+    if out is None:
+        out = torch.empty_like(v)
+    a = make_args(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
+                  final_state, cu_seqlens, qk_l2norm, gate, beta_prob)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    rc = lib.kda_fwd_recurrent(ctypes.byref(a), ctypes.c_void_p(s.cuda_stream))
     if rc != 0:
         raise KdaError(rc, lib.kda_error_string(rc).decode())
     return out
