@@ -50,6 +50,7 @@ DEFAULT_STEPS = {"tiny": 2000, "dense_batch": 3000, "long_context": 3000, "packe
 KERNEL_SOURCES = {
     "kda_chunk_kernel": ["kda_chunk.cu", "kda_common.cuh", "kda_kernels.cuh"],
     "kda_state_kernel": ["kda_state.cu", "kda_common.cuh", "kda_kernels.cuh"],
+    "kda_recurrent_kernel": ["kda_recurrent.cu", "kda_common.cuh", "kda_kernels.cuh"],
 }
 
 
@@ -64,6 +65,9 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU work of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--path", choices=["chunked", "recurrent"], default="chunked",
+                   help="recurrent: time the token-by-token (decoding) entry point on the "
+                        "decode workload instead of the chunked path")
     return p.parse_args()
 
 
@@ -374,6 +378,87 @@ def workload_config(a, inp, world):
     return cfg
 
 
+def run_recurrent_line(a, dev):
+    """Decoding steps through kda_fwd_recurrent: the state stays on the device
+    and is updated in place from step to step.  Compulsory bytes per step:
+    the state read and written (fp32, 64 KiB each per (sequence, head)) plus
+    the token inputs and outputs (1282 B per token-head)."""
+    from kimi_delta_attention_05_gb300 import kda as K
+    import ctypes
+    name = "decode" if a.workload == "long_context" else a.workload
+    inp = make_inputs(WORKLOADS[name])
+    d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in inp.items()}
+    state = d["initial_state"]
+    out = torch.empty_like(d["v"])
+    lb = inp["lower_bound"] if inp["gate"] == "safe" else None
+    args = K.make_args(d["q"], d["k"], d["v"], d["g"], d["beta"], inp["scale"], out, d["A_log"],
+                       d["dt_bias"], lb, state, state, d["cu_seqlens"], inp["qk_l2norm"],
+                       inp["gate"])
+    lib = K.load_library()
+    stream = torch.cuda.current_stream(dev)
+    call = lambda: lib.kda_fwd_recurrent(ctypes.byref(args), ctypes.c_void_p(stream.cuda_stream))
+    steps = a.steps or 2000
+    for _ in range(a.warmup):
+        assert call() == 0
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        w0 = time.time()
+        t0.record(stream)
+        for _ in range(steps):
+            call()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        w1 = time.time()
+    ms_step = t0.elapsed_time(t1) / steps
+    th = token_heads(inp)
+    H = inp["q"].shape[2]
+    tokens = th // H
+    units = inp["N"] * H
+    state_bytes = 2 * units * K_DIM * K_DIM * state.element_size()
+    step_bytes = state_bytes + th * (BYTES_IN_PER_TOKEN_HEAD + BYTES_OUT_PER_TOKEN_HEAD)
+    hbm, _, peak_kind = measured_peaks()
+    achieved = step_bytes / (ms_step * 1e-3) / 1e9
+    # end to end: token inputs H2D from pinned memory and outputs D2H each step,
+    # the state resident on the device (a serving loop's traffic)
+    names = ["q", "k", "v", "g", "beta"]
+    host = {n: inp[n].pin_memory() for n in names}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e_steps = max(a.e2e_steps, 1)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        for n in names:
+            d[n].copy_(host[n], non_blocking=True)
+        call()
+        host_out.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e_ms = e0.elapsed_time(e1) / e_steps
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = host_out.numel() * host_out.element_size()
+    cfg = {"workload": name, "B": int(inp["q"].shape[0]), "T": int(inp["q"].shape[1]), "H": int(H),
+           "K": K_DIM, "V": K_DIM, "N": int(inp["N"]), "gate": inp["gate"],
+           "qk_l2norm": bool(inp["qk_l2norm"]), "state": "fp32, updated in place",
+           "path": "token-by-token (kda_fwd_recurrent)", "parallelism": "single GPU",
+           "l2": f"state {state_bytes // 2 / 1e6:.0f} MB > 129 MB L2; no flush"}
+    line = {"metric": "KDA decode tokens/s and % of HBM roofline, 1 GB300", "value": tokens / (ms_step * 1e-3),
+            "unit": "tokens/s", "n_gpus": 1, "steps": steps, "warmup": a.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": cfg,
+            "roofline": {"bound": "hbm", "kernel": "kda_recurrent_kernel", "achieved": achieved,
+                         "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "traffic": recorded_traffic("kda_recurrent_kernel", name),
+                         "algorithmic_bytes_per_launch": step_bytes,
+                         "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"},
+            "gpu_launches": steps, "clocks": clk.summary(w0, w1),
+            "e2e": {"value": tokens / (e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     a = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -407,6 +492,8 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     from kimi_delta_attention_05_gb300 import kda as K
     K.load_library()
+    if a.path == "recurrent":
+        return run_recurrent_line(a, dev) if rank == 0 else 0
     inp = make_inputs(w, seed=w.seed + rank)
     r = run_ours(a, inp, dev, rank, world)
     th = token_heads(inp)

@@ -8,7 +8,7 @@
 //   S' = S Diag(exp(a_t));  S = S' + beta (v - S' k) k^T;  o = scale S q
 // (decay first, delta write with the decayed state, read-out after the write).
 //
-// One CTA per (sequence, head, 32-row value slab), 8 warps x 4 value rows;
+// One CTA per (sequence, head, 64-row value slab), 8 warps x 8 value rows;
 // lane l holds key channels 4l .. 4l+3 of its warp's rows in fp32 registers for
 // the whole sequence, so a row is one 512-byte access and the two dot products
 // per row are warp shuffles.  Rows are independent, so the final state may be
@@ -18,7 +18,8 @@
 
 namespace kda {
 
-constexpr int kRecRows = 32;  // value rows per CTA
+constexpr int kRecWarpRows = 8;                 // value rows per warp
+constexpr int kRecRows = 8 * kRecWarpRows;       // value rows per CTA
 constexpr int kRecThreads = 256;
 
 __device__ __forceinline__ float rcp_fast(float x) {
@@ -62,12 +63,12 @@ __global__ void __launch_bounds__(kRecThreads) kda_recurrent_kernel(RecurrentPar
   const int64_t bos = p.cu ? p.cu[n] : n * p.T;
   const int64_t eos = p.cu ? p.cu[n + 1] : bos + p.T;
   const int c0 = 4 * lane;                        // key channels c0 .. c0 + 3
-  const int r0 = slab * kRecRows + warp * 4;      // value rows r0 .. r0 + 3
+  const int r0 = slab * kRecRows + warp * kRecWarpRows;  // value rows r0 .. r0 + 7
   const int64_t sbase = unit * (int64_t)(kHeadDim * kHeadDim);
 
-  float S[4][4];
+  float S[kRecWarpRows][4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < kRecWarpRows; ++i) {
     const int64_t off = sbase + (int64_t)(r0 + i) * kHeadDim + c0;
     if (!p.init) {
       S[i][0] = S[i][1] = S[i][2] = S[i][3] = 0.f;
@@ -93,11 +94,12 @@ __global__ void __launch_bounds__(kRecThreads) kda_recurrent_kernel(RecurrentPar
 
   for (int64_t t = bos; t < eos; ++t) {
     const int64_t row = t * H + h;
-    float q[4], k[4], g[4], v[4];
+    float q[4], k[4], g[4], v[kRecWarpRows];
     load4_bf16(p.q + row * kHeadDim + c0, q);
     load4_bf16(p.k + row * kHeadDim + c0, k);
     load4_bf16(p.g + row * kHeadDim + c0, g);
-    load4_bf16(p.v + row * kHeadDim + r0, v);
+    load4_bf16(p.v + row * kHeadDim + r0, *reinterpret_cast<float(*)[4]>(v));
+    load4_bf16(p.v + row * kHeadDim + r0 + 4, *reinterpret_cast<float(*)[4]>(v + 4));
     const float braw = bf16_to_f(p.beta[row]);
     const float beta = p.beta_prob ? braw : rcp_fast(1.0f + ex2(-braw * kLog2e));
     if (kL2) {
@@ -113,9 +115,9 @@ __global__ void __launch_bounds__(kRecThreads) kda_recurrent_kernel(RecurrentPar
 #pragma unroll
     for (int c = 0; c < 4; ++c) d[c] = rec_decay<kGate>(g[c] + dtb[c], amul, p.lower_bound);
     // decay, then the prediction S' k of each row
-    float pr[4];
+    float pr[kRecWarpRows];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kRecWarpRows; ++i) {
       pr[i] = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -124,11 +126,11 @@ __global__ void __launch_bounds__(kRecThreads) kda_recurrent_kernel(RecurrentPar
       }
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) pr[i] = warp_sum(pr[i]);
+    for (int i = 0; i < kRecWarpRows; ++i) pr[i] = warp_sum(pr[i]);
     // delta write, then the read-out S q
-    float o[4];
+    float o[kRecWarpRows];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kRecWarpRows; ++i) {
       const float w = beta * (v[i] - pr[i]);
       o[i] = 0.f;
 #pragma unroll
@@ -138,14 +140,15 @@ __global__ void __launch_bounds__(kRecThreads) kda_recurrent_kernel(RecurrentPar
       }
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) o[i] = warp_sum(o[i]);
+    for (int i = 0; i < kRecWarpRows; ++i) o[i] = warp_sum(o[i]);
     if (lane == 0)
-      *reinterpret_cast<uint2*>(p.out + row * kHeadDim + r0) =
-          make_uint2(pack_bf16(o[0] * p.scale, o[1] * p.scale), pack_bf16(o[2] * p.scale, o[3] * p.scale));
+      *reinterpret_cast<uint4*>(p.out + row * kHeadDim + r0) =
+          make_uint4(pack_bf16(o[0] * p.scale, o[1] * p.scale), pack_bf16(o[2] * p.scale, o[3] * p.scale),
+                     pack_bf16(o[4] * p.scale, o[5] * p.scale), pack_bf16(o[6] * p.scale, o[7] * p.scale));
   }
   if (p.final_state) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kRecWarpRows; ++i) {
       const int64_t off = sbase + (int64_t)(r0 + i) * kHeadDim + c0;
       if (p.state_bf16)
         *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.final_state) + off) =

@@ -63,6 +63,10 @@ WORKLOADS = {
     # numerical extremes: wide gate/beta logits, extreme A_log, no L2 norm, bf16 states
     "extremes": Workload("extremes", 2, 32768, 8, "safe", -5.0, False, 0.05, 4.0, 4.0,
                          (0.01, 64.0), "bf16", "bf16"),
+    # decoding step (token-by-token path): 256 sequences x 1 token x 32 heads,
+    # fp32 states carried from call to call (distributions as dense_batch)
+    "decode": Workload("decode", 256, 1, 32, "safe", -5.0, True, 1.0, 1.0, 1.0, (1.0, 16.0),
+                       "f32", "f32"),
 }
 
 # The five workloads in the order they are usually listed.
