@@ -1,8 +1,10 @@
 // Recurrent stage of the KDA forward pass on the 5th-generation tensor cores
 // (tcgen05, accumulators in tensor memory): one CTA per (sequence, head,
-// 32-wide value tile), walking the chunks of its sequence in order and
+// 64-wide value tile), walking the chunks of its sequence in order and
 // bringing each chunk's operand block in with bulk copies, issued in parallel
-// by eight lanes of a producer warp.
+// by nine lanes of a producer warp.  Two CTAs per head (not four of 32
+// columns) because every CTA of a head receives the same 57 KB of chunk
+// operands through its SM's L2 port, the resource that bounds this stage.
 //
 // Per chunk, with S the state (rows = value index, columns = key index) at
 // the chunk start and the intra-chunk quantities of the workspace slot:
@@ -11,14 +13,15 @@
 //                                          the chunk_o stage of the fla code map)
 //   S     = S Diag(gamma_C) + U_new^T K_hat   (chunk_delta_h state update)
 // as three tensor-core products, each issued by one thread:
-//   MMA1: D1 [128 x 32]  = [Q_gamma; W] (128 x 128) . S^T        (rows 64.. = W S^T)
-//   MMA2: D3 [128 x 32]  = K_hat^T (128 x 64)       . U_new       (state delta, row = key)
-//   MMA3: D1[0..63]     += [P; 0]   (128 x 64)       . U_new       (output rows)
-// The state master copy is fp32 in the registers of the four epilogue warps
-// (thread = key index = tensor-memory lane); each chunk it is published as an
-// fp16 operand tile for the next MMA1.  Roles: warps 0-3 epilogue, warp 4 bulk
-// copies, warp 5 tensor-core issue.  Every wait is bounded: a CTA that gives
-// up sets the device status word and stops waiting, so it cannot hang.
+//   MMA1: D1 [128 x 64]  = [Q_gamma; W] (128 x 128) . S^T        (rows 64.. = W S^T)
+//   MMA2: D3 [128 x 64]  = K_hat^T (128 x 64)       . U_new       (state delta, row = key)
+//   MMA3: D1[0..63]     += [P; *]   (128 x 64)       . U_new       (output rows)
+// The state master copy is fp32 in the registers of the eight epilogue warps
+// (warp = tensor-memory lane quarter x 32-column half, thread = key index);
+// each chunk it is published as an fp16 operand tile for the next MMA1.
+// Roles: warps 0-7 epilogue, warp 8 bulk copies, warp 9 tensor-core issue.
+// Every wait is bounded: a CTA that gives up sets the device status word and
+// stops waiting, so it cannot hang.
 #include "kda_common.cuh"
 #include "kda_kernels.cuh"
 
@@ -28,28 +31,41 @@ namespace kda {
 constexpr int kSA1 = 0;          // kmaj R=128 K=128: [q gamma; W]
 constexpr int kSKh = 32768;      // kmaj R=64 (t) K=128 (k): k_hat (MN-major A of MMA2)
 constexpr int kSP = 49152;       // kmaj R=64 K=64: P  (rows 0..63 of the A operand of MMA3)
-constexpr int kSZero = 57344;    // 8 KB of zeros: rows 64..127 of that A operand
-constexpr int kSGc = 65536;      // fp32 [128] gamma_C
-constexpr int kSU = 66048;       // U tile [64 t][32 v] fp16 (utile_off)
-constexpr int kStageBytes = 70656;  // 69 KB
 constexpr int kStages = 3;
-static_assert(kStageBytes % 1024 == 0, "stage bases must stay 1024-aligned");
-// ---- operand tiles written by the epilogue, barriers ----
-constexpr int kSS = kStages * kStageBytes;   // kmaj R=32 (v) K=128 (k): S (B of MMA1)
-constexpr int kSUn = kSS + 8192;              // kmaj R=32 (v) K=64 (t): U_new^T (B of MMA2/3)
-constexpr int kSBar = kSUn + 4096;            // mbarriers
 constexpr int kBarFull = 0, kBarEmpty = 3, kBarMma1 = 6, kBarMma2 = 7, kBarUn = 8, kBarS = 9,
               kBarMma3 = 10, kNumBars = 11;
-constexpr int kSTmem = kSBar + 8 * kNumBars;  // tensor-memory base address (written by alloc)
-constexpr int kSAbort = kSTmem + 8;
-constexpr int kStateSmem = kSAbort + 8;
-constexpr int kVTile = 32;
 constexpr int kPiece = kSP + 8192 - kSA1;    // 57344: the shared block minus gamma_C
 constexpr int kPieces = 7;                   // copied as 7 pieces of 8 KB, one per lane
 static_assert(kPiece == kPieces * 8192, "piece split");
-constexpr uint32_t kStageTx = kPiece + 512 + 4096;    // bytes landing per stage
-constexpr int kStateThreads = 192;
-constexpr uint32_t kTmemCols = 128;  // D1 (2 x 32 cols), D3 (32 cols)
+
+// Layout and roles for a CTA of kVT value columns (32 or 64; 128 / kVT CTAs per
+// head).  Rows 64..127 of MMA3's A operand are the 8 KB after P: zeros with
+// 32 columns; with 64 (where the zeros do not fit) whatever follows P, whose
+// products land in rows of D1 that U_new has already consumed.
+template <int kVT>
+struct StateCfg {
+  static constexpr int kVTile = kVT;
+  static constexpr int kEpiWarps = 4 * (kVT / 32);  // (lane quarter, 32-column group) pairs
+  static constexpr int kProducerWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1;
+  static constexpr int kThreads = 32 * (kEpiWarps + 2);
+  static constexpr bool kZeroPad = kVT == 32;
+  static constexpr int kSZero = 57344;                   // 8 KB of zeros (kZeroPad only)
+  static constexpr int kSGc = kZeroPad ? 65536 : 57344;  // fp32 [128] gamma_C
+  static constexpr int kSU = kSGc + 512;                 // kVT / 32 U tiles [64 t][32 v] fp16
+  static constexpr int kStageBytes = kZeroPad ? 70656 : 66560;
+  static constexpr int kSS = kStages * kStageBytes;      // kmaj R=kVT (v) K=128 (k): S
+  static constexpr int kSUn = kSS + kVT * 256;           // kmaj R=kVT (v) K=64 (t): U_new^T
+  static constexpr int kSBar = kSUn + kVT * 128;         // mbarriers
+  static constexpr int kSTmem = kSBar + 8 * kNumBars;    // tensor-memory base address
+  static constexpr int kSAbort = kSTmem + 8;
+  static constexpr int kSmem = kSAbort + 8;
+  static constexpr uint32_t kStageTx = kPiece + 512 + kVT * 128;  // bytes landing per stage
+  static constexpr uint32_t kTmemCols = kVT == 32 ? 128 : 256;    // D1 x 2 and D3
+  static_assert(kStageBytes % 1024 == 0 && kSS % 1024 == 0 && kSUn % 1024 == 0,
+                "operand images need 1024-byte alignment");
+  static_assert(kSU + kVT * 128 <= kStageBytes, "stage overflow");
+  static_assert(kSmem <= 232448, "exceeds the opt-in shared memory of one CTA");
+};
 
 // Sticky device status: set to KDA_ERR_DEVICE_TIMEOUT (13) by a CTA that gave
 // up waiting; read and cleared by kda_get_status.
@@ -108,13 +124,16 @@ __device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
 }
 
-__global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams p) {
+template <int kVT>
+__global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(StateParams p) {
+  using C = StateCfg<kVT>;
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t H = p.H;
-  const int64_t unit = blockIdx.x >> 2;
-  const int vt = blockIdx.x & 3;
-  const int v0 = vt * kVTile;
+  constexpr int kTiles = kHeadDim / kVT;  // CTAs per head
+  const int64_t unit = blockIdx.x / kTiles;
+  const int vt = (int)(blockIdx.x % kTiles);
+  const int v0 = vt * C::kVTile;
   const int64_t n = unit / H;
   const int h = (int)(unit - n * H);
   int64_t bos, len, slot0;
@@ -129,9 +148,9 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
   }
   const int64_t nch = (len + kChunk - 1) / kChunk;
   const uint32_t sb = smem_u32(smem);
-  const uint32_t bar = sb + kSBar;
+  const uint32_t bar = sb + C::kSBar;
   auto B = [&](int i) { return bar + 8 * i; };
-  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kSAbort);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kSAbort);
   auto slot_ptr = [&](int64_t ci) {
     return p.ws + ((slot0 + ci) * H + h) * (int64_t)kSlotBytes;
   };
@@ -140,29 +159,31 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
   if (tid == 0) {
     for (int st = 0; st < kStages; ++st) {
       mbar_init(B(kBarFull + st), 1);
-      mbar_init(B(kBarEmpty + st), 1 + 4);          // MMA commit + four epilogue warps
+      mbar_init(B(kBarEmpty + st), 1 + C::kEpiWarps);  // MMA commit + the epilogue warps
     }
     mbar_init(B(kBarMma1), 1);
     mbar_init(B(kBarMma2), 1);
     mbar_init(B(kBarMma3), 1);
-    mbar_init(B(kBarUn), 2);
-    mbar_init(B(kBarS), 4);
+    mbar_init(B(kBarUn), C::kEpiWarps / 2);  // the epilogue warps on lanes 64..127
+    mbar_init(B(kBarS), C::kEpiWarps);
     *s_abort = (sb & 1023) ? 1 : 0;  // the swizzled operand images need 1024-byte alignment
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
-  for (int i = tid; i < kStages * 512; i += kStateThreads)
-    reinterpret_cast<uint4*>(smem + (i >> 9) * kStageBytes + kSZero)[i & 511] = make_uint4(0, 0, 0, 0);
-  if (warp == 5) {
+  if (C::kZeroPad)
+    for (int i = tid; i < kStages * 512; i += C::kThreads)
+      reinterpret_cast<uint4*>(smem + (i >> 9) * C::kStageBytes + C::kSZero)[i & 511] =
+          make_uint4(0, 0, 0, 0);
+  if (warp == C::kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
-                     sb + kSTmem),
-                 "r"(kTmemCols));
+                     sb + C::kSTmem),
+                 "r"(C::kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
   }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kSTmem);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::kSTmem);
   if (*s_abort && tid == 0) atomicExch(&g_kda_status, 13);
 
   auto wait = [&](uint32_t b, uint32_t parity) {
@@ -173,7 +194,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
     }
   };
 
-  if (warp == 4) {
+  if (warp == C::kProducerWarp) {
     // ---- bulk-copy producer: lane 0 keeps the barrier books, lanes 0..8 copy ----
     int64_t issued = 0;
     int st = 0;
@@ -183,49 +204,49 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
       if (ci >= kStages) wait(B(kBarEmpty + st), ph_prev ^ 1u);  // the stage is free again
       __syncwarp();
       if (*s_abort) break;
-      const uint32_t dst = sb + st * kStageBytes;
+      const uint32_t dst = sb + st * C::kStageBytes;
       const unsigned char* src = slot_ptr(ci);
       if (lane == 0) {
         fence_proxy_async_smem();
-        mbar_expect_tx(B(kBarFull + st), kStageTx);
+        mbar_expect_tx(B(kBarFull + st), C::kStageTx);
       }
       __syncwarp();
       if (lane < kPieces)
         bulk_g2s(dst + lane * 8192, src + lane * 8192, 8192u, B(kBarFull + st));
-      else if (lane == kPieces)
-        bulk_g2s(dst + kSU, src + kSlotU + vt * 4096, 4096u, B(kBarFull + st));
+      else if (lane == kPieces)  // this CTA's two U tiles, adjacent in the slot
+        bulk_g2s(dst + C::kSU, src + kSlotU + vt * (kVT * 128), kVT * 128u, B(kBarFull + st));
       else if (lane == kPieces + 1)
-        bulk_g2s(dst + kSGc, src + kSlotGc, 512u, B(kBarFull + st));
+        bulk_g2s(dst + C::kSGc, src + kSlotGc, 512u, B(kBarFull + st));
       issued = ci + 1;
       st = st + 1 == kStages ? 0 : st + 1;
     }
     if (*s_abort && lane == 0)  // after a timeout: let this CTA's issued copies land before leaving
       for (int64_t c = 0; c < issued; ++c)
         mbar_wait_bounded(B(kBarFull + (int)(c % kStages)), (uint32_t)((c / kStages) & 1));
-  } else if (warp == 5) {
+  } else if (warp == C::kMmaWarp) {
     // ---- tensor-core issuer ----
     if (lane == 0) {
-      const uint32_t id1 = idesc_f16(128, 32, false);
-      const uint32_t id2 = idesc_f16(128, 32, true);
-      const uint32_t d3 = tmem + 64;
+      const uint32_t id1 = idesc_f16(128, C::kVTile, false);
+      const uint32_t id2 = idesc_f16(128, C::kVTile, true);
+      const uint32_t d3 = tmem + 2 * C::kVTile;
       // descriptors of stage 0 / the fixed tiles; the 14-bit address field
       // (bytes >> 4) takes the stage and k-step offsets by plain addition
       const uint64_t dA1 = smem_desc(sb + kSA1, 16, 1024), dKh = smem_desc(sb + kSKh, 8192, 1024);
-      const uint64_t dP = smem_desc(sb + kSP, 16, 1024), dS = smem_desc(sb + kSS, 16, 1024);
-      const uint64_t dUn = smem_desc(sb + kSUn, 16, 1024);
+      const uint64_t dP = smem_desc(sb + kSP, 16, 1024), dS = smem_desc(sb + C::kSS, 16, 1024);
+      const uint64_t dUn = smem_desc(sb + C::kSUn, 16, 1024);
       int st = 0;
       uint32_t phf = 0;  // phase parity of the full barrier of stage st
       for (int64_t ci = 0; ci < nch; ++ci) {
         const uint32_t par = (uint32_t)(ci & 1);
-        const uint64_t so = (uint64_t)((st * kStageBytes) >> 4);
-        const uint32_t d1 = tmem + 32 * par;
+        const uint64_t so = (uint64_t)((st * C::kStageBytes) >> 4);
+        const uint32_t d1 = tmem + C::kVTile * par;
         wait(B(kBarFull + st), phf);
         wait(B(kBarS), par);  // S of this chunk published
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           tc_mma(d1, dA1 + so + (uint64_t)(((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
-                 dS + (uint64_t)(((ks >> 2) * 4096 + (ks & 3) * 32) >> 4), id1, ks > 0);
+                 dS + (uint64_t)(((ks >> 2) * (C::kVTile * 128) + (ks & 3) * 32) >> 4), id1, ks > 0);
         tc_commit(B(kBarMma1));
         wait(B(kBarUn), par);  // U_new of this chunk published
         tc_fence_after();
@@ -245,17 +266,20 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
         mbar_wait_bounded(B(kBarMma3), (uint32_t)((nch - 1) & 1));
     }
   } else {
-    // ---- epilogue warps 0-3: thread = tensor-memory lane (key index / token) ----
-    const int k = tid;  // 0..127
-    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-    float s[32];  // S[v0 + j][k], j = 0..31
+    // ---- epilogue warps 0-7: warp = (lane quarter q, column half hc); thread =
+    //      tensor-memory lane (key index / token), 32 of the CTA's 64 value columns ----
+    const int q = warp & 3, hc = warp >> 2;
+    const int k = q * 32 + lane;  // 0..127
+    const int vc = v0 + 32 * hc;  // first value column of this warp
+    const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16) + 32 * hc;
+    float s[32];  // S[vc + j][k], j = 0..31
     {
       const int64_t sbase = (n * H + h) * (int64_t)(kHeadDim * kHeadDim);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         float x = 0.f;
         if (p.init) {
-          const int64_t off = sbase + (int64_t)(v0 + j) * kHeadDim + k;
+          const int64_t off = sbase + (int64_t)(vc + j) * kHeadDim + k;
           x = p.state_bf16 ? bf16_to_f(reinterpret_cast<const uint16_t*>(p.init)[off])
                            : reinterpret_cast<const float*>(p.init)[off];
         }
@@ -265,7 +289,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
     auto publish_state = [&]() {
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        *reinterpret_cast<__half*>(smem + kSS + kmaj_off(j, k, 32)) = __float2half_rn(s[j]);
+        *reinterpret_cast<__half*>(smem + C::kSS + kmaj_off(32 * hc + j, k, C::kVTile)) =
+            __float2half_rn(s[j]);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -277,30 +302,31 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
     uint32_t phf = 0;
     for (int64_t ci = 0; ci < nch; ++ci) {
       const uint32_t par = (uint32_t)(ci & 1);
-      const unsigned char* stg = smem + st * kStageBytes;
+      const unsigned char* stg = smem + st * C::kStageBytes;
       wait(B(kBarFull + st), phf);
-      const float gk = reinterpret_cast<const float*>(stg + kSGc)[k];
-      if (warp < 2) {  // gamma_C is all these warps read from the stage
+      const float gk = reinterpret_cast<const float*>(stg + C::kSGc)[k];
+      if (q < 2) {  // gamma_C is all these warps read from the stage
         __syncwarp();
         if (lane == 0) mbar_arrive_local(B(kBarEmpty + st));
       }
       wait(B(kBarMma1), par);
       tc_fence_after();
-      if (warp >= 2) {
+      if (q >= 2) {
         // U_new^T for token t = k - 64 (rows 64.. of D1 hold W S^T)
         const int t = k - 64;
         float x[32];
-        tc_ld32(lane_addr + 32 * par, x);
+        tc_ld32(lane_addr + C::kVTile * par, x);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const uint4 u = *reinterpret_cast<const uint4*>(stg + kSU + utile_off(t, 8 * c));
+          const uint4 u = *reinterpret_cast<const uint4*>(stg + C::kSU + hc * 4096 + utile_off(t, 8 * c));
           const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 uv = unpack_f16(uw[e]);
             const int j = 8 * c + 2 * e;
-            *reinterpret_cast<__half*>(smem + kSUn + kmaj_off(j, t, 32)) = __float2half_rn(uv.x - x[j]);
-            *reinterpret_cast<__half*>(smem + kSUn + kmaj_off(j + 1, t, 32)) =
+            *reinterpret_cast<__half*>(smem + C::kSUn + kmaj_off(32 * hc + j, t, C::kVTile)) =
+                __float2half_rn(uv.x - x[j]);
+            *reinterpret_cast<__half*>(smem + C::kSUn + kmaj_off(32 * hc + j + 1, t, C::kVTile)) =
                 __float2half_rn(uv.y - x[j + 1]);
           }
         }
@@ -317,22 +343,22 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
       {
         // S[:, k] = gamma_C[k] S[:, k] + delta; publish for the next chunk
         float d[32];
-        tc_ld32(lane_addr + 64, d);
+        tc_ld32(lane_addr + 2 * C::kVTile, d);
 #pragma unroll
         for (int j = 0; j < 32; ++j) s[j] = gk * s[j] + d[j];
         publish_state();
       }
-      if (warp < 2) {
+      if (q < 2) {
         // output row t = k: D1 rows 0..63 = q gamma S^T + P U_new
         const int t = k;
         const int L = (int)min((int64_t)kChunk, len - ci * kChunk);
         float o[32];
         wait(B(kBarMma3), par);
         tc_fence_after();
-        tc_ld32(lane_addr + 32 * par, o);
+        tc_ld32(lane_addr + C::kVTile * par, o);
         if (t < L) {
           const int64_t tok = bos + ci * kChunk + t;
-          uint4* dst = reinterpret_cast<uint4*>(p.out + (tok * H + h) * kHeadDim + v0);
+          uint4* dst = reinterpret_cast<uint4*>(p.out + (tok * H + h) * kHeadDim + vc);
 #pragma unroll
           for (int c = 0; c < 4; ++c)
             dst[c] = make_uint4(pack_bf16(o[8 * c] * p.scale, o[8 * c + 1] * p.scale),
@@ -349,7 +375,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
       const int64_t sbase = (n * H + h) * (int64_t)(kHeadDim * kHeadDim);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const int64_t off = sbase + (int64_t)(v0 + j) * kHeadDim + k;
+        const int64_t off = sbase + (int64_t)(vc + j) * kHeadDim + k;
         if (p.state_bf16)
           reinterpret_cast<__nv_bfloat16*>(p.final_state)[off] = __float2bfloat16_rn(s[j]);
         else
@@ -360,8 +386,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) kda_state_kernel(StateParams
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTmemCols));
+  if (warp == C::kMmaWarp)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(C::kTmemCols));
 }
 
 extern "C" int kda_get_status(int clear) {
@@ -374,19 +400,34 @@ extern "C" int kda_get_status(int clear) {
   return v;
 }
 
-void launch_state_kernel(const StateParams& p, cudaStream_t stream) {
-  const int64_t blocks = p.N * p.H * (kHeadDim / kVTile);
+template <int kVT>
+static void launch_state_variant(const StateParams& p, cudaStream_t stream) {
+  using C = StateCfg<kVT>;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)blocks);
-  cfg.blockDim = dim3(kStateThreads);
-  cfg.dynamicSmemBytes = kStateSmem;
+  cfg.gridDim = dim3((unsigned)(p.N * p.H * (kHeadDim / kVT)));
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = stream;
-  cudaLaunchKernelEx(&cfg, kda_state_kernel, p);
+  cudaLaunchKernelEx(&cfg, kda_state_kernel<kVT>, p);
+}
+
+// 32-column CTAs (four per head) give the shortest chunk period; 64-column
+// CTAs (two per head) halve the bytes all CTAs of a head pull through their SM
+// ports per chunk.  So: four per head while they fit on the GPU at once (one
+// CTA per SM), two per head once they would run in more than one wave.
+void launch_state_kernel(const StateParams& p, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (p.N * p.H * (kHeadDim / 32) <= (int64_t)sms) launch_state_variant<32>(p, stream);
+  else launch_state_variant<64>(p, stream);
 }
 
 cudaError_t prepare_state_kernel() {
-  return cudaFuncSetAttribute(kda_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kStateSmem);
+  const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  cudaError_t e = cudaFuncSetAttribute(kda_state_kernel<32>, attr, StateCfg<32>::kSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kda_state_kernel<64>, attr, StateCfg<64>::kSmem);
+  return e;
 }
 
 }  // namespace kda

@@ -124,6 +124,14 @@ def test_beta_given_as_probability(gate):
     _full_check(inp, f"beta given ({gate})")
 
 
+def test_many_units_two_ctas_per_head():
+    """More (sequence, head) units than four 32-column CTAs per head can run at
+    once (B*H*4 > SM count): the state stage runs two 64-column CTAs per head."""
+    inp = make_inputs(WORKLOADS["dense_batch"], B=8, T=100, H=8, seed=24)
+    assert inp["q"].shape[0] * inp["q"].shape[2] * 4 > torch.cuda.get_device_properties(0).multi_processor_count
+    _full_check(inp, "two CTAs per head")
+
+
 def test_split_chain_on_gpu():
     """Running [0, s) then [s, T) with final -> initial equals one call."""
     inp = make_inputs(WORKLOADS["dense_batch"], B=1, T=300, H=2, seed=16)
