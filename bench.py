@@ -202,6 +202,30 @@ def device_call(inp, dev):
     return d, out, fin, args, ws
 
 
+# ---------------------------------------------------------------------------
+# multi-rank host logic (also exercised with the gloo backend on CPU by the tests)
+# ---------------------------------------------------------------------------
+
+def rank_inputs(w, rank):
+    """Every rank runs its own copy of the workload, seeded seed + rank."""
+    return make_inputs(w, seed=w.seed + rank)
+
+
+def max_over_ranks(ms, world, device="cpu"):
+    """The timed region's duration is the slowest rank's (all ranks call this)."""
+    if world <= 1:
+        return float(ms)
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(tokens_per_rank, world, ms_step):
+    """tokens/s over all ranks (weak scaling: every rank does the same work)."""
+    return tokens_per_rank * world / (ms_step * 1e-3)
+
+
 def run_ours(a, inp, dev, rank, world):
     from kimi_delta_attention_05_gb300 import kda as K
     import torch.distributed as dist
@@ -238,10 +262,7 @@ def run_ours(a, inp, dev, rank, world):
     ms = t_start.elapsed_time(t_end)
     chunk_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)]
     state_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(steps)]
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     return dict(ms=ms, steps=steps, chunk_ms=statistics.mean(chunk_ms),
                 state_ms=statistics.mean(state_ms), launches=launches_per_step * steps,
                 clocks=clk.summary(w0, w1))
@@ -494,13 +515,13 @@ def main():
     K.load_library()
     if a.path == "recurrent":
         return run_recurrent_line(a, dev) if rank == 0 else 0
-    inp = make_inputs(w, seed=w.seed + rank)
+    inp = rank_inputs(w, rank)
     r = run_ours(a, inp, dev, rank, world)
     th = token_heads(inp)
     H = inp["q"].shape[2]
     tokens = th // H
     ms_step = r["ms"] / r["steps"]
-    value = tokens * world / (ms_step * 1e-3)
+    value = whole_job_value(tokens, world, ms_step)
     hbm, bf16, peak_kind = measured_peaks()
     sio = state_io_bytes(inp)
     chunk_bytes = th * BYTES_IN_PER_TOKEN_HEAD
