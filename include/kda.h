@@ -184,6 +184,17 @@ int kda_fwd_noalloc(const kda_fwd_args *args, void *stream);
  */
 int kda_get_status(int clear);
 
+/*
+ * Self-test of the failure path (no counterpart in the pages): launches one
+ * block on `stream` that waits, with the same bounded mbarrier wait the state
+ * kernel uses, on a barrier phase that nothing completes; after `cycles` SM
+ * cycles (1 .. 2^31) it gives up, sets the device status word to
+ * KDA_ERR_DEVICE_TIMEOUT exactly as a real timeout does, and returns.  The
+ * context stays usable.  Returns KDA_OK, KDA_ERR_SHAPE for a cycle count out
+ * of range, or KDA_ERR_LAUNCH.
+ */
+int kda_selftest_wait_timeout(long long cycles, void *stream);
+
 /* Human-readable text of a status code (static storage). */
 const char *kda_error_string(int code);
 

@@ -197,11 +197,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 // Wait for the phase with the given parity to complete; gives up (returns
-// false) after about 2^31 SM cycles instead of spinning forever.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t addr, uint32_t parity) {
+// false) after `limit` SM cycles (default 2^31, about one second) instead of
+// spinning forever.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t addr, uint32_t parity,
+                                                  long long limit = 1LL << 31) {
   const long long t0 = clock64();
   while (!mbar_try_wait(addr, parity))
-    if (clock64() - t0 > (1LL << 31)) return false;
+    if (clock64() - t0 > limit) return false;
   return true;
 }
 // Flat global -> shared copy by the bulk-copy engine, completing `bytes`

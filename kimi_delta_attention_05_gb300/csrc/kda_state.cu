@@ -390,6 +390,25 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(C::kTmemCols));
 }
 
+// One block waits on an mbarrier phase that nothing completes, with the same
+// bounded wait and status word as the state kernel's waits, and returns.
+__global__ void kda_wait_selftest_kernel(long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait_bounded(smem_u32(&bar), 0u, limit))
+    atomicExch(&g_kda_status, 13);
+}
+
+extern "C" int kda_selftest_wait_timeout(long long cycles, void* stream) {
+  if (cycles <= 0 || cycles > (1LL << 31)) return 3;  // KDA_ERR_SHAPE
+  kda_wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(cycles);
+  return cudaGetLastError() == cudaSuccess ? 0 : 11;  // KDA_OK / KDA_ERR_LAUNCH
+}
+
 extern "C" int kda_get_status(int clear) {
   int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_kda_status, sizeof(int)) != cudaSuccess) return -1;

@@ -78,6 +78,8 @@ def load_library(build_if_missing: bool = True):
         lib.kda_fwd_launches.argtypes = [ctypes.POINTER(kda_fwd_args)]
         lib.kda_get_status.restype = ctypes.c_int
         lib.kda_get_status.argtypes = [ctypes.c_int]
+        lib.kda_selftest_wait_timeout.restype = ctypes.c_int
+        lib.kda_selftest_wait_timeout.argtypes = [ctypes.c_longlong, P]
         lib.kda_fwd_recurrent.restype = ctypes.c_int
         lib.kda_fwd_recurrent.argtypes = [ctypes.POINTER(kda_fwd_args), P]
         _lib = lib

@@ -88,6 +88,12 @@ def test_logspace_gate_and_beta_prob_accepted():
         assert lib.kda_fwd_workspace_bytes(ctypes.byref(a)) > 0
 
 
+def test_wait_selftest_rejects_bad_limits_before_launch():
+    lib = K.load_library()
+    assert lib.kda_selftest_wait_timeout(0, None) == 3
+    assert lib.kda_selftest_wait_timeout(1 << 40, None) == 3
+
+
 def test_workspace_checked_before_launch():
     a = _valid_args()
     need = K.load_library().kda_fwd_workspace_bytes(ctypes.byref(a))
