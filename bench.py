@@ -9,8 +9,9 @@ inputs resident in HBM.  Prints ONE JSON line (rank 0):
   tflops     algorithmic TFLOP/s (132,693 flop per token-head)
   roofline   dominant kernel: its algorithmic bytes / its average duration,
              against the measured HBM copy bandwidth; plus the whole path
-  e2e        same metric through the public API with pinned host buffers,
-             host->device inputs and device->host outputs inside the timing
+  e2e        same metric through the C-ABI host-buffer call (kda_fwd_host) on
+             pinned host buffers: host->device inputs and device->host
+             outputs inside the timing, pipelined with the kernels
   cpu_baseline  the fp64 oracle on a bounded sample, on the host cores
 
 ``--impl reference`` times the oracle itself as the reference arm.
@@ -269,8 +270,11 @@ def run_ours(a, inp, dev, rank, world):
 
 
 def run_e2e(a, inp, dev):
-    """Public API with pinned host buffers; H2D inputs and D2H outputs timed."""
-    from kimi_delta_attention_05_gb300 import kda_fwd
+    """The public C-ABI call on HOST buffers (kda_fwd_host): every step copies
+    the inputs from pinned host memory and the output (and final state) back
+    inside the timed region; the library pipelines those copies with its
+    kernels.  Returns (ms per step, H2D bytes, D2H bytes per step)."""
+    from kimi_delta_attention_05_gb300.kda import host_device_bytes, kda_fwd_host_args_call, make_args
     host = {k: (v.pin_memory() if torch.is_tensor(v) else v) for k, v in inp.items()}
     names = ["q", "k", "v", "g", "beta", "A_log", "dt_bias", "initial_state", "cu_seqlens"]
     h2d = sum(host[n].numel() * host[n].element_size() for n in names if host[n] is not None)
@@ -283,17 +287,13 @@ def run_e2e(a, inp, dev):
         (inp["N"], H, K_DIM, K_DIM), dtype=fin_dt).pin_memory()
     d2h = out_host.numel() * 2 + (0 if fin_host is None else fin_host.numel() * fin_host.element_size())
     lb = inp["lower_bound"] if inp["gate"] == "safe" else None
+    args = make_args(host["q"], host["k"], host["v"], host["g"], host["beta"], inp["scale"],
+                     out_host, host["A_log"], host["dt_bias"], lb, host["initial_state"], fin_host,
+                     host["cu_seqlens"], inp["qk_l2norm"], inp["gate"])
+    dbuf = torch.empty(max(host_device_bytes(args), 1), dtype=torch.uint8, device=dev)
 
     def step():
-        d = {n: (host[n].to(dev, non_blocking=True) if host[n] is not None else None) for n in names}
-        fin = None if fin_dt is None else torch.empty((inp["N"], H, K_DIM, K_DIM), dtype=fin_dt,
-                                                      device=dev)
-        out = kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], inp["scale"], None, d["A_log"],
-                      d["dt_bias"], lb, d["initial_state"], fin, d["cu_seqlens"],
-                      qk_l2norm=inp["qk_l2norm"], gate=inp["gate"])
-        out_host.copy_(out, non_blocking=True)
-        if fin is not None:
-            fin_host.copy_(fin, non_blocking=True)
+        kda_fwd_host_args_call(args, dbuf, stream)
 
     for _ in range(3):
         step()

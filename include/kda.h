@@ -75,6 +75,8 @@ extern "C" {
  *            beta itself)
  *  g       : raw gate logits, or with KDA_GATE_LOGSPACE the log decays a_t
  *  out     : written completely for every token of every sequence
+ *  q, k, v, g, beta, out may be NULL when B * T == 0 (no tokens: only the
+ *            final state, equal to the initial state, is written)
  *  A_log   : fp32 [H]       (NULL only with KDA_GATE_SAFE -> multiplier 1)
  *  dt_bias : fp32 [H, 128]  (NULL -> 0)
  *  initial_state, final_state : [N, H, 128(V), 128(K)] in state_dtype, or
@@ -174,6 +176,45 @@ int kda_fwd_launches(const kda_fwd_args *args);
  */
 #define KDA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 int kda_fwd_noalloc(const kda_fwd_args *args, void *stream);
+
+/*
+ * The forward pass end to end on HOST buffers: copy the inputs to the device,
+ * run the same two stages as kda_fwd, copy the output (and final state) back.
+ * No counterpart in the pages, whose entry point takes device tensors; this
+ * is the call for callers whose data sit in host memory.  The transfers of one
+ * call are pipelined with its kernels: dense inputs are cut along the token
+ * axis into at most 64 pieces of whole 64-token chunks (about 32 MiB of
+ * inputs each; the recurrent state passes from piece to piece in fp32 inside
+ * device_buffer, so the result is that of kda_fwd on the same inputs), packed
+ * inputs into groups of whole sequences; the copy in of piece p + 1, the
+ * kernels of piece p and the copy back of piece p - 1 overlap.
+ *
+ *  - Arguments: as kda_fwd, except that every pointer in `args` (q, k, v, g,
+ *    beta, out, A_log, dt_bias, initial_state, final_state, cu_seqlens) is
+ *    host memory.  Page-locked memory (cudaHostAlloc / cudaHostRegister) is
+ *    needed for the copies to be asynchronous and overlap; pageable memory
+ *    gives the same results with the copies serialised.  cu_seqlens is read
+ *    on the host and checked: cu[0] == 0, non-decreasing, cu[N] == T, else
+ *    KDA_ERR_SHAPE.
+ *  - device_buffer: caller-owned device memory of at least
+ *    kda_fwd_host_device_bytes(args) bytes, 256-byte aligned, holding the
+ *    device copies, the output, the carried state and the workspace; garbage
+ *    afterwards.  Calls sharing it must be ordered.
+ *  - Ordering: the call starts after the work already on `stream`
+ *    (cudaStream_t or NULL) and `stream` waits for its last copy back, so
+ *    `out` and `final_state` hold the results once `stream` has reached that
+ *    point (e.g. after cudaStreamSynchronize(stream)).  The host buffers
+ *    must stay valid until then.
+ *  - Resources: on first use per device the library creates two non-blocking
+ *    copy streams (one per direction) and 130 events, kept until the process
+ *    exits; concurrent
+ *    calls on one device enqueue one after another (a mutex).
+ *  - Errors: as kda_fwd (checked before anything is enqueued); KDA_ERR_WORKSPACE
+ *    for a missing, misaligned or short device_buffer; KDA_ERR_LAUNCH if a copy
+ *    or launch fails to enqueue.
+ */
+size_t kda_fwd_host_device_bytes(const kda_fwd_args *args);
+int kda_fwd_host(const kda_fwd_args *args, void *device_buffer, size_t device_bytes, void *stream);
 
 /*
  * Device-side status of the kernels on the current device: KDA_OK, or

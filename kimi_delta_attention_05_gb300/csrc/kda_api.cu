@@ -60,11 +60,15 @@ bool aligned(const void* p, uintptr_t a) { return p == nullptr || (((uintptr_t)p
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+}  // namespace
+
 // Validates everything that can be checked on the host.  Returns KDA_OK or an
 // error code; fills the slot count (chunk capacity) on success.
 int validate(const kda_fwd_args* a, int64_t* num_slots, size_t* header_bytes) {
   if (!a) return KDA_ERR_NULL_ARG;
-  if (!a->q || !a->k || !a->v || !a->g || !a->beta || !a->out) return KDA_ERR_NULL_ARG;
+  const bool no_tokens = a->B == 0 || a->T == 0;  // token tensors may then be NULL (empty)
+  if (!no_tokens && (!a->q || !a->k || !a->v || !a->g || !a->beta || !a->out))
+    return KDA_ERR_NULL_ARG;
   if (a->K != kHeadDim || a->V != kHeadDim) return KDA_ERR_HEAD_DIM;
   if (a->B < 0 || a->T < 0 || a->H < 0 || a->N < 0 || a->H > 65535) return KDA_ERR_SHAPE;
   const uint32_t gate = a->flags & (KDA_GATE_SAFE | KDA_GATE_UNSAFE | KDA_GATE_LOGSPACE);
@@ -99,7 +103,6 @@ int validate(const kda_fwd_args* a, int64_t* num_slots, size_t* header_bytes) {
   return KDA_OK;
 }
 
-}  // namespace
 }  // namespace kda
 
 using namespace kda;
@@ -111,8 +114,8 @@ extern "C" size_t kda_fwd_workspace_bytes(const kda_fwd_args* args) {
   return header + (size_t)slots * (size_t)args->H * (size_t)kSlotBytes;
 }
 
-static int fwd_impl(const kda_fwd_args* a, void* workspace, size_t workspace_bytes,
-                    void* stream_ptr, void* const* events) {
+int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_bytes,
+                    cudaStream_t stream, void* const* events, int init_bf16, int final_bf16) {
   int64_t slots = 0;
   size_t header = 0;
   int rc = validate(a, &slots, &header);
@@ -121,8 +124,6 @@ static int fwd_impl(const kda_fwd_args* a, void* workspace, size_t workspace_byt
   const size_t need = header + (size_t)slots * (size_t)a->H * (size_t)kSlotBytes;
   if (need > 0 && (!workspace || !aligned(workspace, 256) || workspace_bytes < need))
     return KDA_ERR_WORKSPACE;
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
-
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_LAUNCH;
   if (dev >= 0 && dev < kMaxDevices && g_prepared[dev].load() == 0) {
@@ -171,7 +172,9 @@ static int fwd_impl(const kda_fwd_args* a, void* workspace, size_t workspace_byt
   sp.out = static_cast<uint16_t*>(a->out);
   sp.init = a->initial_state;
   sp.final_state = a->final_state;
-  sp.state_bf16 = a->state_dtype == KDA_DTYPE_BF16 ? 1 : 0;
+  const int sb16 = a->state_dtype == KDA_DTYPE_BF16 ? 1 : 0;
+  sp.init_bf16 = init_bf16 >= 0 ? init_bf16 : sb16;
+  sp.final_bf16 = final_bf16 >= 0 ? final_bf16 : sb16;
   sp.scale = a->scale;
   sp.cu = a->cu_seqlens;
   sp.chunk_off = chunk_off;
@@ -189,12 +192,14 @@ static int fwd_impl(const kda_fwd_args* a, void* workspace, size_t workspace_byt
 
 extern "C" int kda_fwd(const kda_fwd_args* a, void* workspace, size_t workspace_bytes,
                        void* stream) {
-  return fwd_impl(a, workspace, workspace_bytes, stream, nullptr);
+  return fwd_device(a, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream), nullptr,
+                    -1, -1);
 }
 
 extern "C" int kda_fwd_profiled(const kda_fwd_args* a, void* workspace, size_t workspace_bytes,
                                 void* stream, void* const events[3]) {
-  return fwd_impl(a, workspace, workspace_bytes, stream, events);
+  return fwd_device(a, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream), events,
+                    -1, -1);
 }
 
 extern "C" int kda_fwd_recurrent(const kda_fwd_args* a, void* stream_ptr) {

@@ -1,7 +1,10 @@
 // Kernel parameter blocks and launch entry points shared by the host API.
 #pragma once
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
+
+struct kda_fwd_args;
 
 namespace kda {
 
@@ -30,7 +33,7 @@ struct StateParams {
   uint16_t* out;                          // bf16 [tokens, H, 128]
   const void* init;                       // [N, H, 128, 128] or nullptr
   void* final_state;                      // [N, H, 128, 128] or nullptr
-  int state_bf16;
+  int init_bf16, final_bf16;              // state dtypes (1: bf16, 0: fp32)
   float scale;
   const int64_t* cu;
   const int64_t* chunk_off;
@@ -55,6 +58,18 @@ struct RecurrentParams {
   const int64_t* cu;                      // [N+1] or nullptr (dense)
   int64_t N, T, H;
 };
+
+// Host-side argument checks of kda_fwd (KDA_OK or an error code); on success
+// the workspace slot count and the varlen header bytes.
+int validate(const kda_fwd_args* args, int64_t* num_slots, size_t* header_bytes);
+
+// Validate and enqueue one chunked forward pass on device buffers (the body
+// of kda_fwd).  init_bf16 / final_bf16 >= 0 override the state dtype of the
+// initial / final state separately (the host-buffer entry point carries the
+// state between pieces in fp32 whatever the caller's dtype); -1 keeps
+// args->state_dtype.
+int fwd_device(const kda_fwd_args* args, void* workspace, size_t workspace_bytes,
+               cudaStream_t stream, void* const* events, int init_bf16, int final_bf16);
 
 void launch_recurrent_kernel(const RecurrentParams& p, cudaStream_t s);
 cudaError_t prepare_recurrent_kernel();

@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
         float x = 0.f;
         if (p.init) {
           const int64_t off = sbase + (int64_t)(vc + j) * kHeadDim + k;
-          x = p.state_bf16 ? bf16_to_f(reinterpret_cast<const uint16_t*>(p.init)[off])
+          x = p.init_bf16 ? bf16_to_f(reinterpret_cast<const uint16_t*>(p.init)[off])
                            : reinterpret_cast<const float*>(p.init)[off];
         }
         s[j] = x;
@@ -376,7 +376,7 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const int64_t off = sbase + (int64_t)(vc + j) * kHeadDim + k;
-        if (p.state_bf16)
+        if (p.final_bf16)
           reinterpret_cast<__nv_bfloat16*>(p.final_state)[off] = __float2bfloat16_rn(s[j]);
         else
           reinterpret_cast<float*>(p.final_state)[off] = s[j];

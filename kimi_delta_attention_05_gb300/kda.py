@@ -80,6 +80,10 @@ def load_library(build_if_missing: bool = True):
         lib.kda_get_status.argtypes = [ctypes.c_int]
         lib.kda_selftest_wait_timeout.restype = ctypes.c_int
         lib.kda_selftest_wait_timeout.argtypes = [ctypes.c_longlong, P]
+        lib.kda_fwd_host.restype = ctypes.c_int
+        lib.kda_fwd_host.argtypes = [ctypes.POINTER(kda_fwd_args), P, ctypes.c_size_t, P]
+        lib.kda_fwd_host_device_bytes.restype = ctypes.c_size_t
+        lib.kda_fwd_host_device_bytes.argtypes = [ctypes.POINTER(kda_fwd_args)]
         lib.kda_fwd_recurrent.restype = ctypes.c_int
         lib.kda_fwd_recurrent.argtypes = [ctypes.POINTER(kda_fwd_args), P]
         _lib = lib
@@ -189,17 +193,46 @@ def kda_fwd_args_call(args: kda_fwd_args, workspace, stream, events=None) -> Non
         raise KdaError(rc, lib.kda_error_string(rc).decode())
 
 
-def kda_fwd_host(inputs: dict, *, stream=None, device="cuda"):
-    """End-to-end call on host (CPU, ideally pinned) tensors: copy inputs to
-    the device, run kda_fwd, copy the output (and final state) back."""
-    dev = torch.device(device)
-    d = {k: (v.to(dev, non_blocking=True) if torch.is_tensor(v) else v) for k, v in inputs.items()}
-    fin = None
-    if inputs.get("final_state_dtype") is not None:
-        fin = torch.empty((inputs["N"], d["q"].shape[2], HEAD_DIM, HEAD_DIM),
-                          dtype=inputs["final_state_dtype"], device=dev)
-    out = kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], None, d.get("A_log"),
-                  d.get("dt_bias"), d.get("lower_bound"), d.get("initial_state"), fin,
-                  d.get("cu_seqlens"), qk_l2norm=d.get("qk_l2norm", False), gate=d.get("gate"),
-                  stream=stream)
-    return out.to("cpu", non_blocking=True), (None if fin is None else fin.to("cpu", non_blocking=True))
+def kda_fwd_host(q, k, v, g, beta, scale, out=None, A_log=None, dt_bias=None, lower_bound=None,
+                 initial_state=None, final_state=None, cu_seqlens=None, *, qk_l2norm=False,
+                 gate=None, beta_prob=False, device_buffer=None, stream=None, device=None):
+    """End-to-end forward on HOST (CPU) tensors through ``kda_fwd_host``: the
+    library copies the inputs in, runs the path and copies ``out`` (and
+    ``final_state``) back, pipelining the copies with the kernels.  Tensors
+    should be pinned (``.pin_memory()``) for the copies to overlap.  Same
+    arguments as :func:`kda_fwd`, all on the CPU; ``device_buffer`` is an
+    optional uint8 CUDA tensor of at least :func:`host_device_bytes` bytes.
+    Asynchronous on ``stream``: synchronise it before reading the results.
+    Returns ``out``."""
+    lib = load_library()
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    if out is None:
+        out = torch.empty(v.shape, dtype=v.dtype, pin_memory=v.is_pinned())
+    a = make_args(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
+                  final_state, cu_seqlens, qk_l2norm, gate, beta_prob)
+    need = int(lib.kda_fwd_host_device_bytes(ctypes.byref(a)))
+    if device_buffer is None or device_buffer.numel() < need:
+        device_buffer = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    rc = lib.kda_fwd_host(ctypes.byref(a), ctypes.c_void_p(device_buffer.data_ptr()), need,
+                          ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise KdaError(rc, lib.kda_error_string(rc).decode())
+    return out
+
+
+def host_device_bytes(args: kda_fwd_args) -> int:
+    """Device buffer bytes kda_fwd_host needs for an argument block of host
+    pointers (0 for an invalid one)."""
+    return int(load_library().kda_fwd_host_device_bytes(ctypes.byref(args)))
+
+
+def kda_fwd_host_args_call(args: kda_fwd_args, device_buffer, stream) -> None:
+    """kda_fwd_host on a prepared argument block of host pointers (keeps
+    Python marshalling out of a timed loop)."""
+    lib = load_library()
+    need = int(lib.kda_fwd_host_device_bytes(ctypes.byref(args)))
+    rc = lib.kda_fwd_host(ctypes.byref(args), ctypes.c_void_p(device_buffer.data_ptr()), need,
+                          ctypes.c_void_p(stream.cuda_stream))
+    if rc != 0:
+        raise KdaError(rc, lib.kda_error_string(rc).decode())

@@ -115,3 +115,75 @@ def test_error_strings():
         assert lib.kda_error_string(c)
     assert b"unknown" in lib.kda_error_string(99)
     assert lib.kda_version() >= 100
+
+
+# ---- kda_fwd_host: argument checks and device-buffer size (no GPU touched) ----
+
+def _host_call(a, buf=None, nbytes=0):
+    return K.load_library().kda_fwd_host(ctypes.byref(a), buf, nbytes, None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), 1), (dict(K=64), 2), (dict(N=3), 3), (dict(flags=0), 4),
+    (dict(lower_bound=0.0), 5), (dict(flags=K.KDA_GATE_UNSAFE, A_log=None), 6),
+    (dict(initial_state=FAKE, state_dtype=7), 7), (dict(cu_seqlens=FAKE, B=2), 8),
+    (dict(q=FAKE + 2), 9),
+])
+def test_host_entry_rejects_like_kda_fwd(over, code):
+    a = _valid_args(**over)
+    assert _host_call(a, FAKE, 1 << 40) == code
+    assert K.load_library().kda_fwd_host_device_bytes(ctypes.byref(a)) == 0
+
+
+def test_host_device_bytes_dense_single_piece():
+    """B=2, T=100, H=4, no states: device copies of q, k, v, g, out, beta,
+    A_log, dt_bias and one piece's workspace, each region 256-byte aligned."""
+    a = _valid_args()
+    need = K.load_library().kda_fwd_host_device_bytes(ctypes.byref(a))
+    rows = 2 * 100
+    qlike = rows * 4 * 256
+    assert need == 5 * qlike + 1792 + 256 + 2048 + 2 * 2 * 4 * 74240
+    assert _host_call(a, None, need) == 10
+    assert _host_call(a, FAKE, need - 1) == 10
+    assert _host_call(a, FAKE + 16, need) == 10
+
+
+def test_host_device_bytes_dense_pieces_carry_state():
+    """Past 32 MiB of inputs a dense call is cut into token-range pieces: the
+    workspace is one piece's and an fp32 state carry appears."""
+    import numpy as np
+    a = _valid_args(B=1, N=1, T=16384, H=4)
+    need = K.load_library().kda_fwd_host_device_bytes(ctypes.byref(a))
+    qlike = 16384 * 4 * 256
+    beta = 16384 * 4 * 2
+    carry = 1 * 4 * 128 * 128 * 4
+    ws = 1 * (5504 // 64) * 4 * 74240  # three pieces of at most 5504 tokens
+    assert need == 5 * qlike + beta + 256 + 2048 + carry + ws
+    assert np.int64(need) > 0
+
+
+def test_host_cu_seqlens_checked_on_host():
+    import numpy as np
+    lib = K.load_library()
+    for bad in ([0, 10, 5, 100], [0, 10, 50, 99], [1, 10, 50, 100]):
+        cu = np.array(bad, dtype=np.int64)
+        a = _valid_args(B=1, T=100, N=3, cu_seqlens=cu.ctypes.data)
+        assert _host_call(a, FAKE, 1 << 40) == 3
+        assert lib.kda_fwd_host_device_bytes(ctypes.byref(a)) == 0
+    cu = np.array([0, 10, 10, 100], dtype=np.int64)
+    a = _valid_args(B=1, T=100, N=3, cu_seqlens=cu.ctypes.data)
+    need = lib.kda_fwd_host_device_bytes(ctypes.byref(a))
+    qlike = 100 * 4 * 256
+    ws = 256 + (2 + 3) * 4 * 74240  # one group of all three sequences
+    assert need == 5 * qlike + 1024 + 256 + 2048 + 256 + ws
+
+
+def test_no_tokens_allows_null_token_tensors():
+    """B * T == 0: the token tensors may be NULL (empty torch tensors have no
+    storage); with tokens they may not."""
+    lib = K.load_library()
+    empty = dict(q=None, k=None, v=None, g=None, beta=None, out=None, T=0)
+    a = _valid_args(**empty)
+    assert lib.kda_fwd_host_device_bytes(ctypes.byref(a)) == 256 + 2048  # A_log, dt_bias
+    assert _host_call(a, None, 0) == 10  # past the argument checks: wants its buffer
+    assert _host_call(_valid_args(q=None), None, 0) == 1
