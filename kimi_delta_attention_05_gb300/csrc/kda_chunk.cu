@@ -100,6 +100,48 @@ __device__ __forceinline__ void scale_bfrag(uint32_t& b0, uint32_t& b1, uint32_t
   b1 = mul_bf16x2(b1, f89);
 }
 
+// Pairs of fp32 values in one 64-bit register for the packed f32x2 arithmetic
+// of sm_100-class SMs: one instruction per pair, each lane rounded exactly as
+// the scalar instruction would (round to nearest, no flush), so results are
+// bit-identical to the scalar form.  Channel pairs (c, c + 1) travel together.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 f2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2u(f32x2 v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// The two bf16 values of a 32-bit word (low half first) as fp32.
+__device__ __forceinline__ f32x2 bf2_to_f2(uint32_t w) {
+  return f2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+__device__ __forceinline__ uint32_t pack_bf16_2(f32x2 v) {
+  const float2 x = f2u(v);
+  return pack_bf16(x.x, x.y);
+}
+__device__ __forceinline__ uint32_t pack_f16_2(f32x2 v) {
+  const float2 x = f2u(v);
+  return pack_f16(x.x, x.y);
+}
+__device__ __forceinline__ f32x2 max2_floor(f32x2 v) {
+  const float2 x = f2u(v);
+  return f2(fmaxf(x.x, kDiagDecayFloor), fmaxf(x.y, kDiagDecayFloor));
+}
+
 // exp(a) for the gate activation a of the pre-activation z (g + dt_bias):
 //   unsafe: a = -amul softplus(z) = -amul ln(1 + e^z), so exp(a) = 2^(-amul lg2(1 + 2^(z lg2 e)));
 //           for large z, 1 + 2^(.) rounds to 2^(.) and lg2 gives z lg2 e back; past the fp32
@@ -109,11 +151,23 @@ __device__ __forceinline__ void scale_bfrag(uint32_t& b0, uint32_t& b1, uint32_t
 // Only exp(a) is used, so what matters is the absolute error of a: lg2(1 + t)
 // loses at most ~1e-7 of it when t is tiny, far below what exp(a) resolves.
 // (amul_log2e = amul lg2 e for the safe gate, amul for the unsafe one.)
+// (Evaluated on a channel pair, lane by lane.)
 template <int kGate>
-__device__ __forceinline__ float gate_decay(float z, float amul_log2e, float lb_log2e) {
-  if (kGate == kGateLogspace) return ex2(z * kLog2e);
-  if (kGate == kGateUnsafe) return ex2(-amul_log2e * lg2(1.0f + ex2(z * kLog2e)));
-  return ex2(lb_log2e * rcp_approx(1.0f + ex2(-amul_log2e * z)));
+__device__ __forceinline__ f32x2 gate_decay2(f32x2 z, float amul_log2e, float lb_log2e) {
+  if (kGate == kGateLogspace) {
+    const float2 a = f2u(mul2(z, f2(kLog2e, kLog2e)));
+    return f2(ex2(a.x), ex2(a.y));
+  }
+  if (kGate == kGateUnsafe) {
+    const float2 a = f2u(mul2(z, f2(kLog2e, kLog2e)));
+    const float2 b = f2u(add2(f2(1.0f, 1.0f), f2(ex2(a.x), ex2(a.y))));
+    const float2 c = f2u(mul2(f2(-amul_log2e, -amul_log2e), f2(lg2(b.x), lg2(b.y))));
+    return f2(ex2(c.x), ex2(c.y));
+  }
+  const float2 a = f2u(mul2(f2(-amul_log2e, -amul_log2e), z));
+  const float2 b = f2u(add2(f2(1.0f, 1.0f), f2(ex2(a.x), ex2(a.y))));
+  const float2 c = f2u(mul2(f2(lb_log2e, lb_log2e), f2(rcp_approx(b.x), rcp_approx(b.y))));
+  return f2(ex2(c.x), ex2(c.y));
 }
 
 template <int kGate, bool kL2>
@@ -229,41 +283,45 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
   float* sXm = reinterpret_cast<float*>(smem + kCsXm);
   float* sYm = reinterpret_cast<float*>(smem + kCsYm);
   float* sFa = reinterpret_cast<float*>(smem + kCsFa);
-  float d[8][4];
+  // decays of channel pairs (c0, c0 + 1), (c0 + 2, c0 + 3) in f32x2 registers
+  f32x2 d2[8][2];
   float inv[4];  // 1 / (clamped product over this half)
+  const f32x2 one2 = f2(1.0f, 1.0f);
   {
     const float4 dtb = (p.dt_bias && kGate != kGateLogspace)
                            ? *reinterpret_cast<const float4*>(p.dt_bias + h * kHeadDim + c0)
                            : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float dtbv[4] = {dtb.x, dtb.y, dtb.z, dtb.w};
+    const f32x2 dtb2[2] = {f2(dtb.x, dtb.y), f2(dtb.z, dtb.w)};
     const float amul_log2e = (p.A_log && kGate != kGateLogspace ? expf(p.A_log[h]) : 1.0f) *
                              (kGate == kGateUnsafe ? 1.0f : kLog2e);
     const float lb_log2e = p.lower_bound * kLog2e;
-    float D[4] = {1.f, 1.f, 1.f, 1.f}, Dc[4] = {1.f, 1.f, 1.f, 1.f};
+    f32x2 D2[2] = {one2, one2}, Dc2[2] = {one2, one2};
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int t = tb + j;
       const uint2 graw = *reinterpret_cast<const uint2*>(smem + gt + swz128(t, c0));
-      const float2 g01 = unpack_bf16(graw.x), g23 = unpack_bf16(graw.y);
-      const float gz[4] = {g01.x, g01.y, g23.x, g23.y};
+      const uint32_t gw[2] = {graw.x, graw.y};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float e = gate_decay<kGate>(gz[c] + dtbv[c], amul_log2e, lb_log2e);
-        if (t >= L) e = 1.f;
-        d[j][c] = e;
-        D[c] *= e;
-        Dc[c] *= fmaxf(e, kDiagDecayFloor);
+      for (int pp = 0; pp < 2; ++pp) {
+        f32x2 e = gate_decay2<kGate>(add2(bf2_to_f2(gw[pp]), dtb2[pp]), amul_log2e, lb_log2e);
+        if (t >= L) e = one2;
+        d2[j][pp] = e;
+        D2[pp] = mul2(D2[pp], e);
+        Dc2[pp] = mul2(Dc2[pp], max2_floor(e));
       }
     }
-    *reinterpret_cast<float4*>(sD + seg * 128 + c0) = make_float4(D[0], D[1], D[2], D[3]);
-    *reinterpret_cast<float4*>((hf ? sYm : sXm) + rb * 128 + c0) = make_float4(Dc[0], Dc[1], Dc[2], Dc[3]);
+    const float2 Da = f2u(D2[0]), Db = f2u(D2[1]), Dca = f2u(Dc2[0]), Dcb = f2u(Dc2[1]);
+    *reinterpret_cast<float4*>(sD + seg * 128 + c0) = make_float4(Da.x, Da.y, Db.x, Db.y);
+    *reinterpret_cast<float4*>((hf ? sYm : sXm) + rb * 128 + c0) = make_float4(Dca.x, Dca.y, Dcb.x, Dcb.y);
     if (hf) {
       uint32_t* yp = reinterpret_cast<uint32_t*>(smem + kCsYp) + rb * 64;
-      yp[fpair_pos(2 * cg)] = pack_bf16(Dc[0], Dc[1]);
-      yp[fpair_pos(2 * cg + 1)] = pack_bf16(Dc[2], Dc[3]);
+      yp[fpair_pos(2 * cg)] = pack_bf16(Dca.x, Dca.y);
+      yp[fpair_pos(2 * cg + 1)] = pack_bf16(Dcb.x, Dcb.y);
     }
-#pragma unroll
-    for (int c = 0; c < 4; ++c) inv[c] = __frcp_rn(Dc[c]);
+    inv[0] = __frcp_rn(Dca.x);
+    inv[1] = __frcp_rn(Dca.y);
+    inv[2] = __frcp_rn(Dcb.x);
+    inv[3] = __frcp_rn(Dcb.y);
   }
   __syncthreads();
 
@@ -274,15 +332,15 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
   //  within the half before the midpoint xr_j = inv * (clamped product up to j), after
   //  it xr_j = clamped product from token 8 up to j, so each half needs only its own d
   {
-    float pre[4] = {1.f, 1.f, 1.f, 1.f}, suf[4] = {1.f, 1.f, 1.f, 1.f};
+    f32x2 pre2[2] = {one2, one2}, suf2[2] = {one2, one2};
 #pragma unroll
     for (int s2 = 0; s2 < 8; ++s2) {
       const float4 Ds = *reinterpret_cast<const float4*>(sD + s2 * 128 + c0);
-      const float dv[4] = {Ds.x, Ds.y, Ds.z, Ds.w};
+      const f32x2 dv2[2] = {f2(Ds.x, Ds.y), f2(Ds.z, Ds.w)};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (s2 < seg) pre[c] *= dv[c];
-        if (s2 > seg) suf[c] *= dv[c];
+      for (int pp = 0; pp < 2; ++pp) {
+        if (s2 < seg) pre2[pp] = mul2(pre2[pp], dv2[pp]);
+        if (s2 > seg) suf2[pp] = mul2(suf2[pp], dv2[pp]);
       }
     }
     if (tid < 32) {  // left factors of the off-diagonal sub-blocks (r, cb), cb < r
@@ -304,40 +362,35 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
           fp[fpair_pos(2 * cg + 1)] = pack_bf16(e.z, e.w);
         }
       // gamma_C = product over all eight halves
+      const float2 sa = f2u(suf2[0]), sb = f2u(suf2[1]);
       *reinterpret_cast<float4*>(ws + kSlotGc + c0 * 4) =
-          make_float4(suf[0] * sD[c0], suf[1] * sD[c0 + 1], suf[2] * sD[c0 + 2], suf[3] * sD[c0 + 3]);
+          make_float4(sa.x * sD[c0], sa.y * sD[c0 + 1], sb.x * sD[c0 + 2], sb.y * sD[c0 + 3]);
     }
     // xr takes 1 / (clamped product) in the first half, yr in the second
-    float invx[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      invx[c] = hf ? 1.f : inv[c];
-      inv[c] = hf ? inv[c] : 1.f;
-    }
+    const f32x2 invx2[2] = {hf ? one2 : f2(inv[0], inv[1]), hf ? one2 : f2(inv[2], inv[3])};
+    const f32x2 inv2[2] = {hf ? f2(inv[0], inv[1]) : one2, hf ? f2(inv[2], inv[3]) : one2};
     unsigned char* gQg = ws + kSlotA1;  // rows 0..63 of the [q gamma; W] image
     unsigned char* gKh = ws + kSlotKh;
     // backward over the half (reads the raw k)
     {
-      float y[4] = {suf[0], suf[1], suf[2], suf[3]}, yc[4] = {1.f, 1.f, 1.f, 1.f};
+      f32x2 y2[2] = {suf2[0], suf2[1]}, yc2[2] = {one2, one2};
 #pragma unroll
       for (int j = 7; j >= 0; --j) {
         const int t = tb + j;
         const uint32_t off = swz128(t, c0);
         const float rk = sRk[t];
+        const f32x2 rk2 = f2(rk, rk);
         const uint2 kraw = *reinterpret_cast<const uint2*>(smem + kCsK + off);
-        const float2 k01 = unpack_bf16(kraw.x), k23 = unpack_bf16(kraw.y);
-        const float k[4] = {k01.x * rk, k01.y * rk, k23.x * rk, k23.y * rk};
-        float yr[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) yr[c] = yc[c] * inv[c];  // inv = 1 in the first half
+        const f32x2 k2[2] = {mul2(bf2_to_f2(kraw.x), rk2), mul2(bf2_to_f2(kraw.y), rk2)};
+        const f32x2 yr2[2] = {mul2(yc2[0], inv2[0]), mul2(yc2[1], inv2[1])};  // inv = 1 in the first half
         *reinterpret_cast<uint2*>(smem + yt + off) =
-            make_uint2(pack_bf16(k[0] * yr[0], k[1] * yr[1]), pack_bf16(k[2] * yr[2], k[3] * yr[3]));
+            make_uint2(pack_bf16_2(mul2(k2[0], yr2[0])), pack_bf16_2(mul2(k2[1], yr2[1])));
         *reinterpret_cast<uint2*>(gKh + kmaj_off(t, c0, 64)) =
-            make_uint2(pack_f16(k[0] * y[0], k[1] * y[1]), pack_f16(k[2] * y[2], k[3] * y[3]));
+            make_uint2(pack_f16_2(mul2(k2[0], y2[0])), pack_f16_2(mul2(k2[1], y2[1])));
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          y[c] *= d[j][c];
-          yc[c] *= fmaxf(d[j][c], kDiagDecayFloor);
+        for (int pp = 0; pp < 2; ++pp) {
+          y2[pp] = mul2(y2[pp], d2[j][pp]);
+          yc2[pp] = mul2(yc2[pp], max2_floor(d2[j][pp]));
         }
       }
     }
@@ -345,38 +398,36 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
     __syncthreads();
     // forward over the half (overwrites raw q, k, g, v)
     {
-      float x[4] = {pre[0], pre[1], pre[2], pre[3]}, xc[4] = {1.f, 1.f, 1.f, 1.f};
+      f32x2 x2[2] = {pre2[0], pre2[1]}, xc2[2] = {one2, one2};
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int t = tb + j;
         const uint32_t off = swz128(t, c0);
-        float xr[4];
+        f32x2 xr2[2];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          x[c] *= d[j][c];
-          xc[c] *= fmaxf(d[j][c], kDiagDecayFloor);
-          xr[c] = xc[c] * invx[c];  // invx = 1 in the second half
+        for (int pp = 0; pp < 2; ++pp) {
+          x2[pp] = mul2(x2[pp], d2[j][pp]);
+          xc2[pp] = mul2(xc2[pp], max2_floor(d2[j][pp]));
+          xr2[pp] = mul2(xc2[pp], invx2[pp]);  // invx = 1 in the second half
         }
         const float rk = sRk[t], rq = sRq[t], bt = sBeta[t];
+        const f32x2 rk2 = f2(rk, rk), rq2 = f2(rq, rq), bt2 = f2(bt, bt);
         const uint2 kraw = *reinterpret_cast<const uint2*>(smem + kCsK + off);
         const uint2 qraw = *reinterpret_cast<const uint2*>(smem + kCsQ + off);
         const uint2 vraw = *reinterpret_cast<const uint2*>(smem + kCsV + off);
-        const float2 k01 = unpack_bf16(kraw.x), k23 = unpack_bf16(kraw.y);
-        const float2 q01 = unpack_bf16(qraw.x), q23 = unpack_bf16(qraw.y);
-        const float2 v01 = unpack_bf16(vraw.x), v23 = unpack_bf16(vraw.y);
-        const float k[4] = {k01.x * rk, k01.y * rk, k23.x * rk, k23.y * rk};
-        const float q[4] = {q01.x * rq, q01.y * rq, q23.x * rq, q23.y * rq};
-        const float v[4] = {v01.x, v01.y, v23.x, v23.y};
+        const f32x2 k2[2] = {mul2(bf2_to_f2(kraw.x), rk2), mul2(bf2_to_f2(kraw.y), rk2)};
+        const f32x2 q2[2] = {mul2(bf2_to_f2(qraw.x), rq2), mul2(bf2_to_f2(qraw.y), rq2)};
+        const f32x2 v2[2] = {bf2_to_f2(vraw.x), bf2_to_f2(vraw.y)};
         *reinterpret_cast<uint2*>(smem + kCsK + off) =
-            make_uint2(pack_bf16(k[0] * xr[0], k[1] * xr[1]), pack_bf16(k[2] * xr[2], k[3] * xr[3]));
+            make_uint2(pack_bf16_2(mul2(k2[0], xr2[0])), pack_bf16_2(mul2(k2[1], xr2[1])));
         *reinterpret_cast<uint2*>(smem + kCsQ + off) =
-            make_uint2(pack_bf16(q[0] * xr[0], q[1] * xr[1]), pack_bf16(q[2] * xr[2], q[3] * xr[3]));
+            make_uint2(pack_bf16_2(mul2(q2[0], xr2[0])), pack_bf16_2(mul2(q2[1], xr2[1])));
         *reinterpret_cast<uint2*>(smem + gt + off) =
-            make_uint2(pack_f16(bt * k[0] * x[0], bt * k[1] * x[1]), pack_f16(bt * k[2] * x[2], bt * k[3] * x[3]));
+            make_uint2(pack_f16_2(mul2(mul2(bt2, k2[0]), x2[0])), pack_f16_2(mul2(mul2(bt2, k2[1]), x2[1])));
         *reinterpret_cast<uint2*>(smem + kCsVt + off) =
-            make_uint2(pack_f16(bt * v[0], bt * v[1]), pack_f16(bt * v[2], bt * v[3]));
+            make_uint2(pack_f16_2(mul2(bt2, v2[0])), pack_f16_2(mul2(bt2, v2[1])));
         *reinterpret_cast<uint2*>(gQg + kmaj_off(t, c0, 128)) =
-            make_uint2(pack_f16(q[0] * x[0], q[1] * x[1]), pack_f16(q[2] * x[2], q[3] * x[3]));
+            make_uint2(pack_f16_2(mul2(q2[0], x2[0])), pack_f16_2(mul2(q2[1], x2[1])));
       }
     }
   }
