@@ -53,14 +53,27 @@ struct StateCfg {
   static constexpr int kSGc = kZeroPad ? 65536 : 57344;  // fp32 [128] gamma_C
   static constexpr int kSU = kSGc + 512;                 // kVT / 32 U tiles [64 t][32 v] fp16
   static constexpr int kStageBytes = kZeroPad ? 70656 : 66560;
-  static constexpr int kSS = kStages * kStageBytes;      // kmaj R=kVT (v) K=128 (k): S
-  static constexpr int kSUn = kSS + kVT * 256;           // kmaj R=kVT (v) K=64 (t): U_new^T
+  static constexpr int kSS = kStages * kStageBytes;      // MN-major [128 k][kVT v] fp16: S
+  static constexpr int kSUn = kSS + kVT * 256;           // MN-major [64 t][kVT v] fp16: U_new
   static constexpr int kSBar = kSUn + kVT * 128;         // mbarriers
   static constexpr int kSTmem = kSBar + 8 * kNumBars;    // tensor-memory base address
   static constexpr int kSAbort = kSTmem + 8;
-  static constexpr int kSmem = kSAbort + 8;
+  // 1 KB of slack after the last word: an operand read formed from any of the
+  // descriptors above, under any swizzle mode, stays inside the allocation.
+  static constexpr int kSmem = kSAbort + 8 + 1024;
   static constexpr uint32_t kStageTx = kPiece + 512 + kVT * 128;  // bytes landing per stage
   static constexpr uint32_t kTmemCols = kVT == 32 ? 128 : 256;    // D1 x 2 and D3
+  // The fp16 B operands S (N = v, K = k) and U_new (N = v, K = t) are stored
+  // MN-major: one row of the CTA's kVT values per k (or t), so a thread that
+  // holds a row writes it with 16-byte stores.  64 columns fill a 128-byte
+  // swizzle atom, 32 columns a 64-byte one.
+  static constexpr int kRowB = 2 * kVT;                    // bytes per row
+  static constexpr uint32_t kBLayout = kVT == 64 ? 2u : 4u;  // descriptor: 128- / 64-byte swizzle
+  static constexpr uint32_t kBSbo = 8 * kRowB;              // next group of 8 rows
+  // byte offset of 16-byte chunk `chunk` (values 8 chunk .. 8 chunk + 7) of row `row`
+  __device__ static uint32_t boff(int row, int chunk) {
+    return (uint32_t)(row * kRowB + ((chunk ^ (kVT == 64 ? (row & 7) : ((row >> 1) & 3))) << 4));
+  }
   static_assert(kStageBytes % 1024 == 0 && kSS % 1024 == 0 && kSUn % 1024 == 0,
                 "operand images need 1024-byte alignment");
   static_assert(kSU + kVT * 128 <= kStageBytes, "stage overflow");
@@ -72,20 +85,21 @@ struct StateCfg {
 __device__ int g_kda_status = 0;
 
 // ---- tcgen05 helpers ----
-// Shared-memory matrix descriptor: 128-byte swizzle, given leading / stride
-// byte offsets.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+// Shared-memory matrix descriptor: given leading / stride byte offsets and
+// swizzle layout (2: 128-byte, 4: 64-byte).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t layout = 2) {
   uint64_t d = (uint64_t)((addr >> 4) & 0x3FFF);
   d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
   d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
   d |= (uint64_t)1 << 46;  // descriptor version
-  d |= (uint64_t)2 << 61;  // 128-byte swizzle
+  d |= (uint64_t)layout << 61;
   return d;
 }
-// Instruction descriptor: fp16 x fp16 -> fp32, M x N, A K-major or MN-major, B K-major.
-__device__ __forceinline__ uint32_t idesc_f16(int m, int n, bool a_mn_major) {
-  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((uint32_t)(n >> 3) << 17) |
-         ((uint32_t)(m >> 4) << 24);
+// Instruction descriptor: fp16 x fp16 -> fp32, M x N, each operand K-major or MN-major.
+__device__ __forceinline__ uint32_t idesc_f16(int m, int n, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                        uint32_t accumulate) {
@@ -226,14 +240,16 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
   } else if (warp == C::kMmaWarp) {
     // ---- tensor-core issuer ----
     if (lane == 0) {
-      const uint32_t id1 = idesc_f16(128, C::kVTile, false);
-      const uint32_t id2 = idesc_f16(128, C::kVTile, true);
+      const uint32_t id1 = idesc_f16(128, C::kVTile, false, true);
+      const uint32_t id2 = idesc_f16(128, C::kVTile, true, true);
       const uint32_t d3 = tmem + 2 * C::kVTile;
       // descriptors of stage 0 / the fixed tiles; the 14-bit address field
       // (bytes >> 4) takes the stage and k-step offsets by plain addition
       const uint64_t dA1 = smem_desc(sb + kSA1, 16, 1024), dKh = smem_desc(sb + kSKh, 8192, 1024);
-      const uint64_t dP = smem_desc(sb + kSP, 16, 1024), dS = smem_desc(sb + C::kSS, 16, 1024);
-      const uint64_t dUn = smem_desc(sb + C::kSUn, 16, 1024);
+      const uint64_t dP = smem_desc(sb + kSP, 16, 1024);
+      const uint64_t dS = smem_desc(sb + C::kSS, 16, C::kBSbo, C::kBLayout);
+      const uint64_t dUn = smem_desc(sb + C::kSUn, 16, C::kBSbo, C::kBLayout);
+      constexpr uint32_t kStepB = 16 * C::kRowB;  // one K step (16 rows) of an MN-major B
       int st = 0;
       uint32_t phf = 0;  // phase parity of the full barrier of stage st
       for (int64_t ci = 0; ci < nch; ++ci) {
@@ -246,18 +262,18 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           tc_mma(d1, dA1 + so + (uint64_t)(((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
-                 dS + (uint64_t)(((ks >> 2) * (C::kVTile * 128) + (ks & 3) * 32) >> 4), id1, ks > 0);
+                 dS + (uint64_t)((ks * kStepB) >> 4), id1, ks > 0);
         tc_commit(B(kBarMma1));
         wait(B(kBarUn), par);  // U_new of this chunk published
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          tc_mma(d3, dKh + so + (uint64_t)((ks * 2048) >> 4), dUn + (uint64_t)((ks * 32) >> 4),
+          tc_mma(d3, dKh + so + (uint64_t)((ks * 2048) >> 4), dUn + (uint64_t)((ks * kStepB) >> 4),
                  id2, ks > 0);
         tc_commit(B(kBarMma2));  // the state update can start
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          tc_mma(d1, dP + so + (uint64_t)((ks * 32) >> 4), dUn + (uint64_t)((ks * 32) >> 4), id1, 1);
+          tc_mma(d1, dP + so + (uint64_t)((ks * 32) >> 4), dUn + (uint64_t)((ks * kStepB) >> 4), id1, 1);
         tc_commit(B(kBarMma3));
         tc_commit(B(kBarEmpty + st));  // the stage's operands are no longer read by the tensor core
         if (++st == kStages) { st = 0; phf ^= 1u; }
@@ -286,11 +302,12 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
         s[j] = x;
       }
     }
-    auto publish_state = [&]() {
+    auto publish_state = [&]() {  // row k of S^T: this warp's 32 values, four 16-byte chunks
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        *reinterpret_cast<__half*>(smem + C::kSS + kmaj_off(32 * hc + j, k, C::kVTile)) =
-            __float2half_rn(s[j]);
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(smem + C::kSS + C::boff(k, 4 * hc + c)) =
+            make_uint4(pack_f16(s[8 * c], s[8 * c + 1]), pack_f16(s[8 * c + 2], s[8 * c + 3]),
+                       pack_f16(s[8 * c + 4], s[8 * c + 5]), pack_f16(s[8 * c + 6], s[8 * c + 7]));
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -317,18 +334,18 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
         float x[32];
         tc_ld32(lane_addr + C::kVTile * par, x);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 4; ++c) {  // row t of U_new: this warp's 32 values
           const uint4 u = *reinterpret_cast<const uint4*>(stg + C::kSU + hc * 4096 + utile_off(t, 8 * c));
           const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+          uint32_t un[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 uv = unpack_f16(uw[e]);
             const int j = 8 * c + 2 * e;
-            *reinterpret_cast<__half*>(smem + C::kSUn + kmaj_off(32 * hc + j, t, C::kVTile)) =
-                __float2half_rn(uv.x - x[j]);
-            *reinterpret_cast<__half*>(smem + C::kSUn + kmaj_off(32 * hc + j + 1, t, C::kVTile)) =
-                __float2half_rn(uv.y - x[j + 1]);
+            un[e] = pack_f16(uv.x - x[j], uv.y - x[j + 1]);
           }
+          *reinterpret_cast<uint4*>(smem + C::kSUn + C::boff(t, 4 * hc + c)) =
+              make_uint4(un[0], un[1], un[2], un[3]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
