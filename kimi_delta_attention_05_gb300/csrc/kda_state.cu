@@ -326,23 +326,35 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
         __syncwarp();
         if (lane == 0) mbar_arrive_local(B(kBarEmpty + st));
       }
+      // U warps: this token's U row comes in before MMA1 completes (it landed with the stage)
+      const int t = k - 64;  // token of this tensor-memory lane in rows 64.. of D1
+      float uf[32];
+      if (q >= 2) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 u = *reinterpret_cast<const uint4*>(stg + C::kSU + hc * 4096 + utile_off(t, 8 * c));
+          const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 uv = unpack_f16(uw[e]);
+            uf[8 * c + 2 * e] = uv.x;
+            uf[8 * c + 2 * e + 1] = uv.y;
+          }
+        }
+      }
       wait(B(kBarMma1), par);
       tc_fence_after();
       if (q >= 2) {
-        // U_new^T for token t = k - 64 (rows 64.. of D1 hold W S^T)
-        const int t = k - 64;
+        // U_new for token t: U - (W S^T)[t, :] (rows 64.. of D1)
         float x[32];
         tc_ld32(lane_addr + C::kVTile * par, x);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {  // row t of U_new: this warp's 32 values
-          const uint4 u = *reinterpret_cast<const uint4*>(stg + C::kSU + hc * 4096 + utile_off(t, 8 * c));
-          const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
           uint32_t un[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float2 uv = unpack_f16(uw[e]);
             const int j = 8 * c + 2 * e;
-            un[e] = pack_f16(uv.x - x[j], uv.y - x[j + 1]);
+            un[e] = pack_f16(uf[j] - x[j], uf[j + 1] - x[j + 1]);
           }
           *reinterpret_cast<uint4*>(smem + C::kSUn + C::boff(t, 4 * hc + c)) =
               make_uint4(un[0], un[1], un[2], un[3]);
