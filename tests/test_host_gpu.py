@@ -122,3 +122,36 @@ def test_device_bytes_cover_the_device_path():
                   inp["A_log"], inp["dt_bias"], None, None, None, None, qk_l2norm=True,
                   gate="unsafe")
     assert host_device_bytes(a) >= 5 * inp["q"].numel() * 2
+
+
+@pytest.mark.parametrize("gate,beta_prob", [("logspace", True), ("unsafe", False)])
+def test_flags_through_host_entry(gate, beta_prob):
+    """Caller-gated g and beta given as beta, through the host-buffer entry:
+    identical to kda_fwd on the same inputs, and within the oracle tolerance."""
+    inp = make_inputs(WORKLOADS["dense_batch"], B=2, T=700, H=4, seed=67)
+    inp["gate"] = gate
+    if gate == "logspace":
+        inp["g"] = (-(inp["g"].float().abs())).to(torch.bfloat16)
+    if beta_prob:
+        inp["beta"] = torch.sigmoid(inp["beta"].float()).to(torch.bfloat16)
+        inp["beta_prob"] = True
+    o_h, f_h = _run_host(inp)
+    o_d, f_d = tl.run_gpu(inp)
+    assert np.array_equal(o_h, o_d) and np.array_equal(f_h, f_d)
+    ro, rf = tl.run_oracle(inp)
+    tl.check_out(o_h, ro, f"host {gate}")
+    tl.check_state(f_h, rf, f"host {gate}")
+
+
+def test_packed_bf16_states_through_host_entry():
+    """Packed sequences with bf16 initial and final states (per-group slices of
+    the state tensors)."""
+    rng = np.random.default_rng(68)
+    lengths = [int(x) for x in rng.integers(1, 5000, size=12)]
+    inp = make_inputs(WORKLOADS["packed_varlen"], lengths=lengths, H=8, seed=68)
+    inp["initial_state"] = inp["initial_state"].to(torch.bfloat16)
+    inp["final_state"] = "bf16"
+    o_h, f_h = _run_host(inp)
+    ro, rf = tl.run_oracle(inp)
+    tl.check_out(o_h, ro, "host packed bf16")
+    tl.check_state(f_h, rf, "host packed bf16")
