@@ -186,9 +186,12 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
     int h, L;
   };
   // ---- locate a chunk: sequence n, chunk i, first token t0, length L ----
+  // (32-bit divisions whenever the item count allows: 64-bit ones are long
+  // instruction sequences, run by every thread once per item)
+  const bool idx32 = num_items <= 0xffffffffLL;
   auto locate = [&](int64_t item) {
     Item r;
-    r.slot = item / H;
+    r.slot = idx32 ? (int64_t)((uint32_t)item / (uint32_t)H) : item / H;
     r.h = (int)(item - r.slot * H);
     int64_t n, i, bos, seqlen;
     if (p.cu) {
@@ -202,7 +205,7 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
       bos = p.cu[n];
       seqlen = p.cu[n + 1] - bos;
     } else {
-      n = r.slot / p.NT;
+      n = idx32 ? (int64_t)((uint32_t)r.slot / (uint32_t)p.NT) : r.slot / p.NT;
       i = r.slot - n * p.NT;
       bos = n * p.T;
       seqlen = p.T;
