@@ -59,6 +59,10 @@ extern "C" {
 /* beta already holds beta in [0, 1] (no sigmoid applied): the beta-activation
  * mode named in the same page's correctness checklist. */
 #define KDA_BETA_PROB 0x10u
+/* g is fp32 [B, T, H, 128] instead of bf16, with any gate form; meant for the
+ * caller-gated mode, whose log decays the pages pass in fp32 (fla-kda SKILL.md,
+ * "Gate contracts": chunk_kda with use_gate_in_kernel=False). */
+#define KDA_G_FP32 0x20u
 
 /* ---- state dtypes ---- */
 #define KDA_DTYPE_F32 0
@@ -71,6 +75,7 @@ extern "C" {
  * on the given stream, so buffers must stay valid until it completes).
  *
  *  q, k, g : bf16 [B, T, H, 128]      v, out : bf16 [B, T, H, 128]
+ *            (g fp32 with KDA_G_FP32)
  *  beta    : bf16 [B, T, H]  (logits, sigmoid applied inside; with KDA_BETA_PROB
  *            beta itself)
  *  g       : raw gate logits, or with KDA_GATE_LOGSPACE the log decays a_t

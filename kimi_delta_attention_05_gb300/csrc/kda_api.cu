@@ -75,7 +75,7 @@ int validate(const kda_fwd_args* a, int64_t* num_slots, size_t* header_bytes) {
   if (gate != KDA_GATE_SAFE && gate != KDA_GATE_UNSAFE && gate != KDA_GATE_LOGSPACE)
     return KDA_ERR_GATE_FLAGS;
   if (a->flags & ~(KDA_GATE_SAFE | KDA_GATE_UNSAFE | KDA_GATE_LOGSPACE | KDA_QK_L2NORM |
-                   KDA_BETA_PROB))
+                   KDA_BETA_PROB | KDA_G_FP32))
     return KDA_ERR_GATE_FLAGS;
   if (gate == KDA_GATE_SAFE && !(a->lower_bound >= -5.0f && a->lower_bound < 0.0f))
     return KDA_ERR_LOWER_BOUND;
@@ -157,6 +157,7 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
                    : (a->flags & KDA_GATE_LOGSPACE) ? kGateLogspace : kGateSafe;
     cp.beta_prob = (a->flags & KDA_BETA_PROB) ? 1 : 0;
     cp.l2norm = (a->flags & KDA_QK_L2NORM) ? 1 : 0;
+    cp.g32 = (a->flags & KDA_G_FP32) ? static_cast<const float*>(a->g) : nullptr;
     cp.cu = a->cu_seqlens;
     cp.chunk_off = chunk_off;
     cp.N = a->N;
@@ -223,6 +224,7 @@ extern "C" int kda_fwd_recurrent(const kda_fwd_args* a, void* stream_ptr) {
                  : (a->flags & KDA_GATE_LOGSPACE) ? kGateLogspace : kGateSafe;
   rp.beta_prob = (a->flags & KDA_BETA_PROB) ? 1 : 0;
   rp.l2norm = (a->flags & KDA_QK_L2NORM) ? 1 : 0;
+  rp.g32 = (a->flags & KDA_G_FP32) ? static_cast<const float*>(a->g) : nullptr;
   rp.init = a->initial_state;
   rp.final_state = a->final_state;
   rp.state_bf16 = a->state_dtype == KDA_DTYPE_BF16 ? 1 : 0;

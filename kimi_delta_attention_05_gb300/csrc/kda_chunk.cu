@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
   // ---- S0 (first item only; later items were prefetched): q, k, g | v ----
   load_tile(p.q, kCsQ, cur);
   load_tile(p.k, kCsK, cur);
-  load_tile(p.g, kCsG, cur);
+  if (!p.g32) load_tile(p.g, kCsG, cur);  // fp32 g is read in the gate stage itself
   cp_async_commit();
   load_tile(p.v, kCsV, cur);
   cp_async_commit();
@@ -299,18 +299,38 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
                              (kGate == kGateUnsafe ? 1.0f : kLog2e);
     const float lb_log2e = p.lower_bound * kLog2e;
     f32x2 D2[2] = {one2, one2}, Dc2[2] = {one2, one2};
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    // decay of token tb + j from its gate input pair values
+    auto gate_token = [&](int j, f32x2 g01, f32x2 g23) {
       const int t = tb + j;
-      const uint2 graw = *reinterpret_cast<const uint2*>(smem + gt + swz128(t, c0));
-      const uint32_t gw[2] = {graw.x, graw.y};
+      const f32x2 gz[2] = {g01, g23};
 #pragma unroll
       for (int pp = 0; pp < 2; ++pp) {
-        f32x2 e = gate_decay2<kGate>(add2(bf2_to_f2(gw[pp]), dtb2[pp]), amul_log2e, lb_log2e);
+        f32x2 e = gate_decay2<kGate>(add2(gz[pp], dtb2[pp]), amul_log2e, lb_log2e);
         if (t >= L) e = one2;
         d2[j][pp] = e;
         D2[pp] = mul2(D2[pp], e);
         Dc2[pp] = mul2(Dc2[pp], max2_floor(e));
+      }
+    };
+    if (p.g32) {  // fp32 g straight from global memory, four tokens' loads in flight at a time
+#pragma unroll
+      for (int j0 = 0; j0 < 8; j0 += 4) {
+        float4 gv[4];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int t = tb + j0 + jj;
+          gv[jj] = t < L ? __ldg(reinterpret_cast<const float4*>(p.g32 + ((cur.t0 + t) * H + h) * kHeadDim + c0))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+          gate_token(j0 + jj, f2(gv[jj].x, gv[jj].y), f2(gv[jj].z, gv[jj].w));
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint2 graw = *reinterpret_cast<const uint2*>(smem + gt + swz128(tb + j, c0));
+        gate_token(j, bf2_to_f2(graw.x), bf2_to_f2(graw.y));
       }
     }
     const float2 Da = f2u(D2[0]), Db = f2u(D2[1]), Dca = f2u(Dc2[0]), Dcb = f2u(Dc2[1]);
@@ -537,7 +557,7 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
   if (next < num_items) {
     load_tile(p.q, kCsQ, nxt);
     load_tile(p.k, kCsK, nxt);
-    load_tile(p.g, yt, nxt);
+    if (!p.g32) load_tile(p.g, yt, nxt);
     if (tid < kChunk) blogit = load_beta(nxt);
   }
   cp_async_commit();

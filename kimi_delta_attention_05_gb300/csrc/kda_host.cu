@@ -72,7 +72,8 @@ int make_plan(const kda_fwd_args* a, Plan* pl) {
       if (cu[n + 1] < cu[n]) return KDA_ERR_SHAPE;
   }
   if (N == 0 || H == 0) return KDA_OK;  // nothing to move or compute
-  const int64_t th_bytes = H * (4 * kRowBytes + 2);  // q, k, v, g rows and beta per token
+  const int64_t g_row = (a->flags & KDA_G_FP32) ? 2 * kRowBytes : kRowBytes;  // bytes of one g row
+  const int64_t th_bytes = H * (3 * kRowBytes + g_row + 2);  // q, k, v, g rows and beta per token
   const int64_t total_in = B * T * th_bytes;
   const int64_t target = std::max(kPieceInputBytes, cdiv(total_in, kMaxPieces));
   size_t ws_max = 0;
@@ -114,7 +115,7 @@ int make_plan(const kda_fwd_args* a, Plan* pl) {
   pl->q = take(rows * H * kRowBytes);
   pl->k = take(rows * H * kRowBytes);
   pl->v = take(rows * H * kRowBytes);
-  pl->g = take(rows * H * kRowBytes);
+  pl->g = take(rows * H * g_row);
   pl->beta = take(rows * H * 2);
   pl->out = take(rows * H * kRowBytes);
   pl->alog = take(a->A_log ? H * 4 : 0);
@@ -184,6 +185,8 @@ extern "C" int kda_fwd_host(const kda_fwd_args* a, void* device_buffer, size_t d
   unsigned char* d = static_cast<unsigned char*>(device_buffer);
   const int64_t B = a->B, T = a->T, H = a->H, N = a->N;
   const int64_t row = H * kRowBytes, brow = H * 2;  // bytes per token: q-like, beta
+  // bytes per token of q, k, v, g (g fp32 with KDA_G_FP32)
+  const int64_t rows_b[4] = {row, row, row, (a->flags & KDA_G_FP32) ? 2 * row : row};
   const size_t esz = a->state_dtype == KDA_DTYPE_BF16 ? 2 : 4;
   const size_t unit_state = (size_t)(H * kStateElems) * esz;  // one sequence's state
   const unsigned char* hq[4] = {static_cast<const unsigned char*>(a->q),
@@ -238,14 +241,14 @@ extern "C" int kda_fwd_host(const kda_fwd_args* a, void* device_buffer, size_t d
       // piece block [B, span, H, 128] at row B * t0 of the device copies
       const size_t r0 = (size_t)(B * pc.t0);
       for (int i = 0; i < 4; ++i)
-        copy_rows(d + dq[i] + r0 * row, span * row, hq[i] + pc.t0 * row, T * row, span * row, B,
-                  cudaMemcpyHostToDevice, hs);
+        copy_rows(d + dq[i] + r0 * rows_b[i], span * rows_b[i], hq[i] + pc.t0 * rows_b[i],
+                  T * rows_b[i], span * rows_b[i], B, cudaMemcpyHostToDevice, hs);
       copy_rows(d + pl.beta + r0 * brow, span * brow, hbeta + pc.t0 * brow, T * brow, span * brow,
                 B, cudaMemcpyHostToDevice, hs);
       sub.q = d + pl.q + r0 * row;
       sub.k = d + pl.k + r0 * row;
       sub.v = d + pl.v + r0 * row;
-      sub.g = d + pl.g + r0 * row;
+      sub.g = d + pl.g + r0 * rows_b[3];
       sub.beta = d + pl.beta + r0 * brow;
       sub.out = d + pl.out + r0 * row;
       sub.T = span;
@@ -257,7 +260,8 @@ extern "C" int kda_fwd_host(const kda_fwd_args* a, void* device_buffer, size_t d
       if (!last) final_bf16 = 0;
     } else {
       // sequences n0 .. n1 - 1: token rows t0 .. t1 - 1 of the packed tensors
-      for (int i = 0; i < 4; ++i) h2d(dq[i] + pc.t0 * row, hq[i] + pc.t0 * row, span * row, hs);
+      for (int i = 0; i < 4; ++i)
+        h2d(dq[i] + pc.t0 * rows_b[i], hq[i] + pc.t0 * rows_b[i], span * rows_b[i], hs);
       h2d(pl.beta + pc.t0 * brow, hbeta + pc.t0 * brow, span * brow, hs);
       sub.q = d + pl.q;  // cu_seqlens of the group index the full packed copies
       sub.k = d + pl.k;

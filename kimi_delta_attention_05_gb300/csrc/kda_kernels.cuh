@@ -15,6 +15,7 @@ constexpr int kGateSafe = 0, kGateUnsafe = 1, kGateLogspace = 2;
 // Intra-chunk stage (one CTA per (chunk slot, head)).
 struct ChunkParams {
   const uint16_t *q, *k, *v, *g, *beta;  // bf16 [tokens, H, 128] / [tokens, H]
+  const float* g32;                       // g as fp32 [tokens, H, 128], or nullptr (bf16 g)
   const float* A_log;                     // [H] or nullptr (safe gate only)
   const float* dt_bias;                   // [H, 128] or nullptr
   float lower_bound;
@@ -44,6 +45,7 @@ struct StateParams {
 // Token-by-token path (one CTA per (sequence, head, 32-row value slab)).
 struct RecurrentParams {
   const uint16_t *q, *k, *v, *g, *beta;  // bf16 [tokens, H, 128] / [tokens, H]
+  const float* g32;                       // g as fp32 [tokens, H, 128], or nullptr (bf16 g)
   uint16_t* out;                          // bf16 [tokens, H, 128]
   const float* A_log;
   const float* dt_bias;

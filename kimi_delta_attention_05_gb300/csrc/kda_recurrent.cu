@@ -97,7 +97,15 @@ __global__ void __launch_bounds__(kRecThreads) kda_recurrent_kernel(RecurrentPar
     float q[4], k[4], g[4], v[kRecWarpRows];
     load4_bf16(p.q + row * kHeadDim + c0, q);
     load4_bf16(p.k + row * kHeadDim + c0, k);
-    load4_bf16(p.g + row * kHeadDim + c0, g);
+    if (p.g32) {
+      const float4 x = *reinterpret_cast<const float4*>(p.g32 + row * kHeadDim + c0);
+      g[0] = x.x;
+      g[1] = x.y;
+      g[2] = x.z;
+      g[3] = x.w;
+    } else {
+      load4_bf16(p.g + row * kHeadDim + c0, g);
+    }
     load4_bf16(p.v + row * kHeadDim + r0, *reinterpret_cast<float(*)[4]>(v));
     load4_bf16(p.v + row * kHeadDim + r0 + 4, *reinterpret_cast<float(*)[4]>(v + 4));
     const float braw = bf16_to_f(p.beta[row]);

@@ -18,6 +18,7 @@ KDA_GATE_UNSAFE = 0x2
 KDA_QK_L2NORM = 0x4
 KDA_GATE_LOGSPACE = 0x8
 KDA_BETA_PROB = 0x10
+KDA_G_FP32 = 0x20
 KDA_DTYPE_F32 = 0
 KDA_DTYPE_BF16 = 1
 HEAD_DIM = 128
@@ -100,7 +101,7 @@ def make_args(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_boun
     """Build the C argument block from tensors (no checks beyond shapes;
     the library validates).  ``gate``: "safe", "unsafe" or "logspace" (g holds
     the log decay); default from ``lower_bound``.  ``beta_prob``: beta holds
-    beta itself instead of logits."""
+    beta itself instead of logits.  A float32 ``g`` sets KDA_G_FP32."""
     B, T, H, K = q.shape
     V = v.shape[-1]
     if gate is None:
@@ -110,6 +111,8 @@ def make_args(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_boun
         flags |= KDA_QK_L2NORM
     if beta_prob:
         flags |= KDA_BETA_PROB
+    if g is not None and g.dtype == torch.float32:
+        flags |= KDA_G_FP32
     N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else B
     st = initial_state if initial_state is not None else final_state
     sd = KDA_DTYPE_BF16 if (st is not None and st.dtype == torch.bfloat16) else KDA_DTYPE_F32

@@ -62,7 +62,7 @@ def _call(a, ws=None, nbytes=0):
     (dict(q=None), 1), (dict(out=None), 1), (dict(beta=None), 1),
     (dict(K=64), 2), (dict(V=256), 2),
     (dict(T=-1), 3), (dict(N=3), 3), (dict(H=70000), 3),
-    (dict(flags=0), 4), (dict(flags=3), 4), (dict(flags=1 | 0x100), 4), (dict(flags=1 | 0x20), 4),
+    (dict(flags=0), 4), (dict(flags=3), 4), (dict(flags=1 | 0x100), 4), (dict(flags=1 | 0x40), 4),
     (dict(flags=K.KDA_GATE_LOGSPACE | K.KDA_GATE_SAFE), 4),
     (dict(flags=K.KDA_GATE_LOGSPACE | K.KDA_GATE_UNSAFE), 4),
     (dict(lower_bound=0.0), 5), (dict(lower_bound=-5.5), 5), (dict(lower_bound=float("nan")), 5),
@@ -82,7 +82,8 @@ def test_logspace_gate_and_beta_prob_accepted():
     as beta itself combines with any gate form."""
     lib = K.load_library()
     for flags in (K.KDA_GATE_LOGSPACE, K.KDA_GATE_LOGSPACE | K.KDA_BETA_PROB,
-                  K.KDA_GATE_UNSAFE | K.KDA_BETA_PROB | K.KDA_QK_L2NORM):
+                  K.KDA_GATE_UNSAFE | K.KDA_BETA_PROB | K.KDA_QK_L2NORM,
+                  K.KDA_GATE_LOGSPACE | K.KDA_G_FP32, K.KDA_GATE_UNSAFE | K.KDA_G_FP32):
         a = _valid_args(flags=flags, A_log=None if flags & K.KDA_GATE_LOGSPACE else FAKE,
                         lower_bound=0.0)
         assert lib.kda_fwd_workspace_bytes(ctypes.byref(a)) > 0
@@ -187,3 +188,12 @@ def test_no_tokens_allows_null_token_tensors():
     assert lib.kda_fwd_host_device_bytes(ctypes.byref(a)) == 256 + 2048  # A_log, dt_bias
     assert _host_call(a, None, 0) == 10  # past the argument checks: wants its buffer
     assert _host_call(_valid_args(q=None), None, 0) == 1
+
+
+def test_fp32_g_doubles_the_g_region_of_the_host_buffer():
+    lib = K.load_library()
+    a16 = _valid_args()
+    a32 = _valid_args(flags=K.KDA_GATE_SAFE | K.KDA_QK_L2NORM | K.KDA_G_FP32)
+    d16 = lib.kda_fwd_host_device_bytes(ctypes.byref(a16))
+    d32 = lib.kda_fwd_host_device_bytes(ctypes.byref(a32))
+    assert d32 - d16 == 2 * 100 * 4 * 256  # B * T * H rows of 256 more bytes

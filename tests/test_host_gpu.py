@@ -155,3 +155,21 @@ def test_packed_bf16_states_through_host_entry():
     ro, rf = tl.run_oracle(inp)
     tl.check_out(o_h, ro, "host packed bf16")
     tl.check_state(f_h, rf, "host packed bf16")
+
+
+def test_g_in_fp32_through_host_entry():
+    """fp32 log decays through the host-buffer entry: dense pieces (2-D copies of
+    512-byte g rows) and packed groups."""
+    gen = torch.Generator().manual_seed(69)
+    inp = make_inputs(WORKLOADS["dense_batch"], B=2, T=8192, H=4, seed=69)
+    inp.update(g=-(torch.randn(inp["g"].shape, generator=gen)).abs(), gate="logspace")
+    o_h, f_h = _run_host(inp)
+    o_d, f_d = tl.run_gpu(inp)
+    assert np.array_equal(o_h, o_d) and np.array_equal(f_h, f_d)
+    lengths = [3000, 17, 5000, 64, 2500]
+    inp = make_inputs(WORKLOADS["packed_varlen"], lengths=lengths, H=4, seed=70)
+    inp.update(g=-(torch.randn(inp["g"].shape, generator=gen)).abs(), gate="logspace")
+    o_h, f_h = _run_host(inp)
+    ro, rf = tl.run_oracle(inp)
+    tl.check_out(o_h, ro, "host fp32 g packed")
+    tl.check_state(f_h, rf, "host fp32 g packed")

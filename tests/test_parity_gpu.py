@@ -110,6 +110,22 @@ def test_logspace_gate(scale_a):
     _full_check(inp, f"logspace gate s={scale_a}")
 
 
+@pytest.mark.parametrize("gate", ["logspace", "safe", "unsafe"])
+def test_g_in_fp32(gate):
+    """g passed in fp32 (KDA_G_FP32): log decays with full fp32 resolution in the
+    caller-gated mode, raw logits in fp32 with the in-kernel gates; ragged
+    chunks and packed sequences."""
+    inp = make_inputs(WORKLOADS["packed_varlen"], lengths=[300, 1, 64, 129], H=3, seed=24)
+    gen = torch.Generator().manual_seed(25)
+    if gate == "logspace":
+        g = -(torch.randn(inp["g"].shape, generator=gen) * 1.5).abs() - 1e-3 * torch.rand(inp["g"].shape, generator=gen)
+    else:
+        g = torch.randn(inp["g"].shape, generator=gen) * 2.0
+    assert g.dtype == torch.float32 and not torch.equal(g, g.to(torch.bfloat16).float())
+    inp = dict(inp, g=g, gate=gate)
+    _full_check(inp, f"fp32 g ({gate})")
+
+
 @pytest.mark.parametrize("gate", ["safe", "unsafe", "logspace"])
 def test_beta_given_as_probability(gate):
     """beta holds beta itself (no sigmoid in the kernel), values in [0, 1]

@@ -70,6 +70,17 @@ def test_multi_token_modes(gate, beta_prob, l2):
     _check(inp, f"recurrent {gate} beta_prob={beta_prob} l2={l2}")
 
 
+@pytest.mark.parametrize("gate", ["logspace", "unsafe"])
+def test_g_in_fp32(gate):
+    inp = make_inputs(WORKLOADS["decode"], B=8, T=3, H=4, seed=36)
+    gen = torch.Generator().manual_seed(37)
+    g = torch.randn(inp["g"].shape, generator=gen) * 2.0
+    if gate == "logspace":
+        g = -g.abs()
+    inp.update(g=g, gate=gate)
+    _check(inp, f"recurrent fp32 g ({gate})")
+
+
 def test_varlen_with_empty_sequences_in_place_state():
     """Packed sequences (two empty), the final state written over the initial
     state buffer."""
