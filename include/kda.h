@@ -47,6 +47,7 @@ extern "C" {
 #define KDA_ERR_LAUNCH 11         /* a CUDA launch failed (cudaGetLastError) */
 #define KDA_ERR_NOALLOC_LIMIT 12  /* kda_fwd_noalloc: problem needs more scratch than built in */
 #define KDA_ERR_DEVICE_TIMEOUT 13 /* (device status) a kernel gave up waiting for its operands */
+#define KDA_ERR_BAD_SEQLENS 14    /* (device status) cu_seqlens values inconsistent (see kda_fwd_args) */
 
 /* ---- flags ---- */
 #define KDA_GATE_SAFE 0x1u   /* lower_bound * sigmoid(exp(A_log) * (g + dt_bias)) */
@@ -88,8 +89,14 @@ extern "C" {
  *            NULL (initial NULL -> zero state; final NULL -> not written).
  *            bf16 final states are rounded to nearest-even from fp32.
  *  cu_seqlens : int64 [N+1] device array or NULL.  With it B must be 1, T is
- *            the packed token total, cu[0] = 0, non-decreasing, cu[N] = T
- *            (the values are the caller's duty; they are not read on the host).
+ *            the packed token total, cu[0] = 0, non-decreasing, cu[N] = T.
+ *            The values are not read on the host; the kernels check them and
+ *            any violation sets the device status to KDA_ERR_BAD_SEQLENS.
+ *            Then kda_fwd (and kda_fwd_noalloc) process no sequence at all
+ *            (out untouched, every final state = its initial state), since
+ *            overlapping sequences could need more workspace than was sized;
+ *            kda_fwd_recurrent skips only the sequences whose bounds leave
+ *            [0, T] or decrease.
  *            Without it N must equal B and sequence n is batch row n.
  *  All sizes are int64; tensor pointers must be 16-byte aligned.
  */
@@ -222,11 +229,13 @@ size_t kda_fwd_host_device_bytes(const kda_fwd_args *args);
 int kda_fwd_host(const kda_fwd_args *args, void *device_buffer, size_t device_bytes, void *stream);
 
 /*
- * Device-side status of the kernels on the current device: KDA_OK, or
+ * Device-side status of the kernels on the current device: KDA_OK,
  * KDA_ERR_DEVICE_TIMEOUT if a CTA gave up waiting (bounded wait, about a
  * second of SM cycles) for its asynchronous operand copies and returned
- * without finishing its work.  Sticky until read with clear != 0.  Reads
- * device memory synchronously; returns -1 if that read fails.
+ * without finishing its work, or KDA_ERR_BAD_SEQLENS if a call's cu_seqlens
+ * values were inconsistent (the offending sequences were skipped).  Sticky
+ * until read with clear != 0 (the last code set wins).  Reads device memory
+ * synchronously; returns -1 if that read fails.
  */
 int kda_get_status(int clear);
 

@@ -10,17 +10,33 @@
 namespace kda {
 
 // Exclusive prefix of per-sequence chunk counts ceil(L_n / 64), one block.
+// First pass: check 0 = cu[0] <= cu[1] <= ... <= cu[N] = T.  Any violation
+// sets the status word and gives every sequence zero chunks: with bounds that
+// decrease somewhere, sequences can overlap and need more chunk slots than the
+// workspace holds, so the chunked path then touches no token row and no slot
+// (final states are still written, equal to the initial states).
 __global__ void __launch_bounds__(1024) kda_chunk_offsets_kernel(const int64_t* cu, int64_t N,
-                                                                  int64_t* chunk_off) {
+                                                                  int64_t T, int64_t* chunk_off,
+                                                                  int* status) {
   __shared__ int64_t warp_sums[32];
   __shared__ int64_t carry;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) { carry = 0; chunk_off[0] = 0; }
+  int bad = 0;
+  for (int64_t n = tid; n <= N; n += 1024) {
+    const int64_t c = cu[n];
+    bad |= (n == 0 && c != 0) || (n == N && c != T) || (n > 0 && c < cu[n - 1]) || c < 0 || c > T;
+  }
+  const bool any_bad = __syncthreads_or(bad) != 0;
+  if (tid == 0) {
+    carry = 0;
+    chunk_off[0] = 0;
+    if (any_bad && status) atomicExch(status, 14);
+  }
   __syncthreads();
   for (int64_t base = 0; base < N; base += 1024) {
     const int64_t n = base + tid;
     int64_t cnt = 0;
-    if (n < N) cnt = (cu[n + 1] - cu[n] + kChunk - 1) / kChunk;
+    if (n < N && !any_bad) cnt = (cu[n + 1] - cu[n] + kChunk - 1) / kChunk;
     int64_t x = cnt;  // inclusive warp scan
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -47,8 +63,9 @@ __global__ void __launch_bounds__(1024) kda_chunk_offsets_kernel(const int64_t* 
   }
 }
 
-void launch_chunk_offsets(const int64_t* cu, int64_t N, int64_t* chunk_off, cudaStream_t s) {
-  kda_chunk_offsets_kernel<<<1, 1024, 0, s>>>(cu, N, chunk_off);
+void launch_chunk_offsets(const int64_t* cu, int64_t N, int64_t T, int64_t* chunk_off, int* status,
+                          cudaStream_t s) {
+  kda_chunk_offsets_kernel<<<1, 1024, 0, s>>>(cu, N, T, chunk_off, status);
 }
 
 namespace {
@@ -141,7 +158,8 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
     if (events && events[i]) cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), stream);
   };
   mark(0);
-  if (a->cu_seqlens) launch_chunk_offsets(a->cu_seqlens, a->N, chunk_off, stream);
+  if (a->cu_seqlens)
+    launch_chunk_offsets(a->cu_seqlens, a->N, a->T, chunk_off, status_device_ptr(), stream);
 
   if (slots > 0) {
     ChunkParams cp;
@@ -232,6 +250,7 @@ extern "C" int kda_fwd_recurrent(const kda_fwd_args* a, void* stream_ptr) {
   rp.N = a->N;
   rp.T = a->T;
   rp.H = a->H;
+  rp.status = a->cu_seqlens ? status_device_ptr() : nullptr;
   launch_recurrent_kernel(rp, reinterpret_cast<cudaStream_t>(stream_ptr));
   if (cudaGetLastError() != cudaSuccess) return KDA_ERR_LAUNCH;
   return KDA_OK;
@@ -260,6 +279,9 @@ extern "C" const char* kda_error_string(int code) {
     case KDA_ERR_LAUNCH: return "CUDA launch failed";
     case KDA_ERR_DEVICE_TIMEOUT:
       return "a kernel gave up waiting for its operand copies (device status)";
+    case KDA_ERR_BAD_SEQLENS:
+      return "cu_seqlens is not 0 = cu[0] <= ... <= cu[N] = T; the call skipped the sequences "
+             "(device status)";
     case KDA_ERR_NOALLOC_LIMIT:
       return "problem needs more scratch than kda_fwd_noalloc's built-in buffer holds";
     default: return "unknown status code";

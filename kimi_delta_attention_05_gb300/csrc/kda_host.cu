@@ -52,7 +52,7 @@ struct Piece {
 struct Plan {
   bool varlen = false;
   std::vector<Piece> pieces;
-  size_t q = 0, k = 0, v = 0, g = 0, beta = 0, out = 0, alog = 0, dtb = 0, cu = 0, init = 0,
+  size_t q = 0, k = 0, v = 0, g = 0, beta = 0, out = 0, alog = 0, dtb = 0, cu = 0, cur = 0, init = 0,
          fin = 0, carry = 0, ws = 0, ws_bytes = 0, total = 0;
 };
 
@@ -121,6 +121,7 @@ int make_plan(const kda_fwd_args* a, Plan* pl) {
   pl->alog = take(a->A_log ? H * 4 : 0);
   pl->dtb = take(a->dt_bias ? H * kHeadDim * 4 : 0);
   pl->cu = take(cu ? (size_t)(N + 1) * 8 : 0);
+  pl->cur = take(cu ? (size_t)(N + pl->pieces.size()) * 8 : 0);  // each group's cu, from 0
   pl->init = take(a->initial_state ? state_bytes : 0);
   pl->fin = take(a->final_state ? state_bytes : 0);
   pl->carry = take(!cu && pl->pieces.size() > 1 ? (size_t)(N * H * kStateElems) * 4 : 0);
@@ -128,6 +129,18 @@ int make_plan(const kda_fwd_args* a, Plan* pl) {
   pl->ws_bytes = ws_max;
   pl->total = off;
   return KDA_OK;
+}
+
+// Each packed group's cu_seqlens rebased to its first token: group i's N_i + 1
+// entries at out + off[i] are cu[n0[i] + j] - cu[n0[i]].
+struct RebaseTable {
+  int64_t n0[kMaxPieces], n1[kMaxPieces], off[kMaxPieces];
+  int count;
+};
+__global__ void kda_rebase_cu_kernel(const int64_t* cu, int64_t* out, RebaseTable tab) {
+  for (int gi = blockIdx.x; gi < tab.count; gi += gridDim.x)
+    for (int64_t j = threadIdx.x; j <= tab.n1[gi] - tab.n0[gi]; j += blockDim.x)
+      out[tab.off[gi] + j] = cu[tab.n0[gi] + j] - cu[tab.n0[gi]];
 }
 
 // Per-device copy streams and events, made on first use and kept until exit.
@@ -225,7 +238,22 @@ extern "C" int kda_fwd_host(const kda_fwd_args* a, void* device_buffer, size_t d
   // the per-call inputs go first, on the stream that also carries piece 0
   if (a->A_log) h2d(pl.alog, a->A_log, (size_t)H * 4, c.h2d[0]);
   if (a->dt_bias) h2d(pl.dtb, a->dt_bias, (size_t)H * kHeadDim * 4, c.h2d[0]);
-  if (a->cu_seqlens) h2d(pl.cu, a->cu_seqlens, (size_t)(N + 1) * 8, c.h2d[0]);
+  std::vector<int64_t> cu_off(pl.pieces.size(), 0);  // packed groups: where their cu starts
+  if (a->cu_seqlens) {
+    h2d(pl.cu, a->cu_seqlens, (size_t)(N + 1) * 8, c.h2d[0]);
+    RebaseTable tab;
+    tab.count = (int)pl.pieces.size();
+    int64_t off = 0;
+    for (int i = 0; i < tab.count; ++i) {
+      tab.n0[i] = pl.pieces[i].n0;
+      tab.n1[i] = pl.pieces[i].n1;
+      tab.off[i] = cu_off[i] = off;
+      off += pl.pieces[i].n1 - pl.pieces[i].n0 + 1;
+    }
+    kda_rebase_cu_kernel<<<tab.count, 256, 0, c.h2d[0]>>>(
+        reinterpret_cast<const int64_t*>(d + pl.cu), reinterpret_cast<int64_t*>(d + pl.cur), tab);
+    chk(cudaGetLastError());
+  }
   if (a->initial_state) h2d(pl.init, a->initial_state, (size_t)N * unit_state, c.h2d[0]);
 
   const int np = (int)pl.pieces.size();
@@ -263,13 +291,14 @@ extern "C" int kda_fwd_host(const kda_fwd_args* a, void* device_buffer, size_t d
       for (int i = 0; i < 4; ++i)
         h2d(dq[i] + pc.t0 * rows_b[i], hq[i] + pc.t0 * rows_b[i], span * rows_b[i], hs);
       h2d(pl.beta + pc.t0 * brow, hbeta + pc.t0 * brow, span * brow, hs);
-      sub.q = d + pl.q;  // cu_seqlens of the group index the full packed copies
-      sub.k = d + pl.k;
-      sub.v = d + pl.v;
-      sub.g = d + pl.g;
-      sub.beta = d + pl.beta;
-      sub.out = d + pl.out;
-      sub.cu_seqlens = reinterpret_cast<const int64_t*>(d + pl.cu) + pc.n0;
+      // the group as a packed call of its own: tensors from its first row, cu from 0
+      sub.q = d + pl.q + pc.t0 * rows_b[0];
+      sub.k = d + pl.k + pc.t0 * rows_b[1];
+      sub.v = d + pl.v + pc.t0 * rows_b[2];
+      sub.g = d + pl.g + pc.t0 * rows_b[3];
+      sub.beta = d + pl.beta + pc.t0 * brow;
+      sub.out = d + pl.out + pc.t0 * row;
+      sub.cu_seqlens = reinterpret_cast<const int64_t*>(d + pl.cur) + cu_off[p];
       sub.N = pc.n1 - pc.n0;
       sub.T = span;
       sub.initial_state = a->initial_state ? d + pl.init + pc.n0 * unit_state : nullptr;

@@ -59,6 +59,7 @@ struct RecurrentParams {
   int state_bf16;
   const int64_t* cu;                      // [N+1] or nullptr (dense)
   int64_t N, T, H;
+  int* status;                            // device status word (bad cu_seqlens)
 };
 
 // Host-side argument checks of kda_fwd (KDA_OK or an error code); on success
@@ -75,7 +76,13 @@ int fwd_device(const kda_fwd_args* args, void* workspace, size_t workspace_bytes
 
 void launch_recurrent_kernel(const RecurrentParams& p, cudaStream_t s);
 cudaError_t prepare_recurrent_kernel();
-void launch_chunk_offsets(const int64_t* cu, int64_t N, int64_t* chunk_off, cudaStream_t s);
+// Chunk prefix of packed sequences, checking 0 = cu[0] <= cu[1] <= ... <= cu[N] = T:
+// a sequence whose bounds leave [0, T] or decrease gets no chunks, and any
+// violation sets *status to 14 (KDA_ERR_BAD_SEQLENS).
+void launch_chunk_offsets(const int64_t* cu, int64_t N, int64_t T, int64_t* chunk_off, int* status,
+                          cudaStream_t s);
+// Device address of the library's sticky status word on the current device.
+int* status_device_ptr();
 void launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t s);
 void launch_state_kernel(const StateParams& p, cudaStream_t s);
 cudaError_t prepare_chunk_kernel();

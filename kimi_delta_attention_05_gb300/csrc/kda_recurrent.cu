@@ -61,7 +61,13 @@ __global__ void __launch_bounds__(kRecThreads) kda_recurrent_kernel(RecurrentPar
   const int64_t n = unit / H;
   const int h = (int)(unit - n * H);
   const int64_t bos = p.cu ? p.cu[n] : n * p.T;
-  const int64_t eos = p.cu ? p.cu[n + 1] : bos + p.T;
+  int64_t eos = p.cu ? p.cu[n + 1] : bos + p.T;
+  if (p.cu) {  // bounds checked on the device: a sequence outside [0, T] is skipped
+    const bool inside = bos >= 0 && eos >= bos && eos <= p.T;
+    const bool bad = !inside || (n == 0 && bos != 0) || (n == p.N - 1 && eos != p.T);
+    if (bad && threadIdx.x == 0 && p.status) atomicExch(p.status, 14);
+    if (!inside) eos = bos;
+  }
   const int c0 = 4 * lane;                        // key channels c0 .. c0 + 3
   const int r0 = slab * kRecRows + warp * kRecWarpRows;  // value rows r0 .. r0 + 7
   const int64_t sbase = unit * (int64_t)(kHeadDim * kHeadDim);

@@ -22,6 +22,8 @@
 // Roles: warps 0-7 epilogue, warp 8 bulk copies, warp 9 tensor-core issue.
 // Every wait is bounded: a CTA that gives up sets the device status word and
 // stops waiting, so it cannot hang.
+#include <atomic>
+
 #include "kda_common.cuh"
 #include "kda_kernels.cuh"
 
@@ -151,16 +153,18 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
   const int64_t n = unit / H;
   const int h = (int)(unit - n * H);
   int64_t bos, len, slot0;
-  if (p.cu) {
+  int64_t nch;
+  if (p.cu) {  // chunk count from the checked scan: 0 for a sequence with bad bounds
     bos = p.cu[n];
     len = p.cu[n + 1] - bos;
     slot0 = p.chunk_off[n];
+    nch = p.chunk_off[n + 1] - slot0;
   } else {
     bos = n * p.T;
     len = p.T;
     slot0 = n * p.NT;
+    nch = (len + kChunk - 1) / kChunk;
   }
-  const int64_t nch = (len + kChunk - 1) / kChunk;
   const uint32_t sb = smem_u32(smem);
   const uint32_t bar = sb + C::kSBar;
   auto B = [&](int i) { return bar + 8 * i; };
@@ -436,6 +440,20 @@ extern "C" int kda_selftest_wait_timeout(long long cycles, void* stream) {
   if (cycles <= 0 || cycles > (1LL << 31)) return 3;  // KDA_ERR_SHAPE
   kda_wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(cycles);
   return cudaGetLastError() == cudaSuccess ? 0 : 11;  // KDA_OK / KDA_ERR_LAUNCH
+}
+
+int* status_device_ptr() {
+  static std::atomic<int*> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  int* p = cache[dev].load();
+  if (!p) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_kda_status) != cudaSuccess) return nullptr;
+    p = static_cast<int*>(a);
+    cache[dev].store(p);
+  }
+  return p;
 }
 
 extern "C" int kda_get_status(int clear) {
