@@ -1,6 +1,8 @@
 // Host side of libkda: argument validation, workspace layout, launches.
 // Declared in include/kda.h.
+#include <algorithm>
 #include <atomic>
+#include <mutex>
 #include <cmath>
 
 #include "../../include/kda.h"
@@ -124,26 +126,87 @@ int validate(const kda_fwd_args* a, int64_t* num_slots, size_t* header_bytes) {
 
 using namespace kda;
 
+#ifndef KDA_PIPE_RANGES
+#define KDA_PIPE_RANGES 4
+#endif
+static_assert(KDA_PIPE_RANGES >= 1 && KDA_PIPE_RANGES <= 8, "pipeline ranges");
+
+namespace {
+
+int device_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+// Token ranges a dense pass is cut into (every range of every sequence, whole
+// chunks), so that the state stage of range r, on a high-priority stream,
+// overlaps the intra-chunk stage of range r + 1 on the SMs it leaves free.  It
+// pays when the state stage occupies at most half the SMs (few sequence-heads:
+// four 32-column CTAs per head) and the sequences are long; otherwise 1.
+int pipeline_ranges(const kda_fwd_args* a, int sms) {
+  if (a->cu_seqlens || sms <= 0) return 1;
+  const int64_t state_ctas = a->N * a->H * (kHeadDim / 32);
+  if (state_ctas == 0 || 2 * state_ctas > sms) return 1;
+  if (ceil_div(a->T, kChunk) < 32) return 1;
+  return KDA_PIPE_RANGES;
+}
+
+size_t carry_bytes(const kda_fwd_args* a) { return (size_t)(a->N * a->H) * kHeadDim * kHeadDim * 4; }
+
+// Per-device stream (greatest priority) and events of the pipelined pass.
+struct PipeCtx {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t state_stream = nullptr;
+  cudaEvent_t start = nullptr, end = nullptr, chunked[KDA_PIPE_RANGES] = {};
+};
+PipeCtx g_pipe[kMaxDevices];
+
+bool make_pipe_ctx(PipeCtx& c) {
+  if (c.ready) return true;
+  int lo = 0, hi = 0;
+  if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) return false;
+  if (cudaStreamCreateWithPriority(&c.state_stream, cudaStreamNonBlocking, hi) != cudaSuccess) return false;
+  const unsigned ef = cudaEventDisableTiming;
+  if (cudaEventCreateWithFlags(&c.start, ef) != cudaSuccess) return false;
+  if (cudaEventCreateWithFlags(&c.end, ef) != cudaSuccess) return false;
+  for (auto& e : c.chunked)
+    if (cudaEventCreateWithFlags(&e, ef) != cudaSuccess) return false;
+  c.ready = true;
+  return true;
+}
+
+}  // namespace
+
 extern "C" size_t kda_fwd_workspace_bytes(const kda_fwd_args* args) {
   int64_t slots = 0;
   size_t header = 0;
   if (validate(args, &slots, &header) != KDA_OK) return 0;
-  return header + (size_t)slots * (size_t)args->H * (size_t)kSlotBytes;
+  const size_t ws = header + (size_t)slots * (size_t)args->H * (size_t)kSlotBytes;
+  return ws + (pipeline_ranges(args, device_sms()) > 1 ? carry_bytes(args) : 0);
 }
 
 int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_bytes,
-                    cudaStream_t stream, void* const* events, int init_bf16, int final_bf16) {
+                    cudaStream_t stream, void* const* events, int init_bf16, int final_bf16,
+                    bool allow_pipeline) {
   int64_t slots = 0;
   size_t header = 0;
   int rc = validate(a, &slots, &header);
   if (rc != KDA_OK) return rc;
   if (a->N == 0 || a->H == 0) return KDA_OK;
-  const size_t need = header + (size_t)slots * (size_t)a->H * (size_t)kSlotBytes;
+  const int ranges = allow_pipeline ? pipeline_ranges(a, device_sms()) : 1;
+  const size_t slot_bytes = (size_t)slots * (size_t)a->H * (size_t)kSlotBytes;
+  const size_t need = header + slot_bytes + (ranges > 1 ? carry_bytes(a) : 0);
   if (need > 0 && (!workspace || !aligned(workspace, 256) || workspace_bytes < need))
     return KDA_ERR_WORKSPACE;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_LAUNCH;
-  if (dev >= 0 && dev < kMaxDevices && g_prepared[dev].load() == 0) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KDA_ERR_LAUNCH;
+  if (g_prepared[dev].load() == 0) {
     if (prepare_chunk_kernel() != cudaSuccess || prepare_state_kernel() != cudaSuccess)
       return KDA_ERR_LAUNCH;
     g_prepared[dev].store(1);
@@ -152,22 +215,28 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
   unsigned char* ws = reinterpret_cast<unsigned char*>(workspace);
   int64_t* chunk_off = a->cu_seqlens ? reinterpret_cast<int64_t*>(ws) : nullptr;
   unsigned char* slots_base = ws + header;
-  const int64_t NT = ceil_div(a->T, kChunk);
+  void* carry = ws + header + slot_bytes;
+  const int sb16 = a->state_dtype == KDA_DTYPE_BF16 ? 1 : 0;
+  const int ib16 = init_bf16 >= 0 ? init_bf16 : sb16, fb16 = final_bf16 >= 0 ? final_bf16 : sb16;
 
   auto mark = [&](int i) {
     if (events && events[i]) cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), stream);
   };
-  mark(0);
-  if (a->cu_seqlens)
-    launch_chunk_offsets(a->cu_seqlens, a->N, a->T, chunk_off, status_device_ptr(), stream);
-
-  if (slots > 0) {
+  // The two stages over token range [t0, t0 + span) of every sequence (dense), or
+  // over the whole call (packed); the range's chunks take their own workspace slots.
+  auto launch_chunks = [&](int64_t t0, int64_t span, unsigned char* ws_r, cudaStream_t s,
+                           int busy_sms) {
+    const int64_t nt = ceil_div(span, kChunk);
+    const int64_t nslots = a->cu_seqlens ? slots : a->B * nt;
+    if (nslots == 0) return;
+    const int64_t r0 = t0 * a->H * kHeadDim;  // element offset of the range's first row
     ChunkParams cp;
-    cp.q = static_cast<const uint16_t*>(a->q);
-    cp.k = static_cast<const uint16_t*>(a->k);
-    cp.v = static_cast<const uint16_t*>(a->v);
-    cp.g = static_cast<const uint16_t*>(a->g);
-    cp.beta = static_cast<const uint16_t*>(a->beta);
+    cp.q = static_cast<const uint16_t*>(a->q) + r0;
+    cp.k = static_cast<const uint16_t*>(a->k) + r0;
+    cp.v = static_cast<const uint16_t*>(a->v) + r0;
+    cp.g = static_cast<const uint16_t*>(a->g) + r0;
+    cp.g32 = (a->flags & KDA_G_FP32) ? static_cast<const float*>(a->g) + r0 : nullptr;
+    cp.beta = static_cast<const uint16_t*>(a->beta) + t0 * a->H;
     cp.A_log = a->A_log;
     cp.dt_bias = a->dt_bias;
     cp.lower_bound = a->lower_bound;
@@ -175,36 +244,73 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
                    : (a->flags & KDA_GATE_LOGSPACE) ? kGateLogspace : kGateSafe;
     cp.beta_prob = (a->flags & KDA_BETA_PROB) ? 1 : 0;
     cp.l2norm = (a->flags & KDA_QK_L2NORM) ? 1 : 0;
-    cp.g32 = (a->flags & KDA_G_FP32) ? static_cast<const float*>(a->g) : nullptr;
     cp.cu = a->cu_seqlens;
     cp.chunk_off = chunk_off;
     cp.N = a->N;
-    cp.T = a->T;
+    cp.T = span;
     cp.H = a->H;
-    cp.NT = NT;
-    cp.ws = slots_base;
-    launch_chunk_kernel(cp, slots, stream);
+    cp.NT = nt;
+    cp.ld = a->T;
+    cp.ws = ws_r;
+    launch_chunk_kernel(cp, nslots, s, busy_sms);
+  };
+  auto launch_state = [&](int64_t t0, int64_t span, unsigned char* ws_r, const void* init,
+                          void* fin, int ib, int fb, cudaStream_t s) {
+    const int64_t r0 = t0 * a->H * kHeadDim;
+    StateParams sp;
+    sp.out = static_cast<uint16_t*>(a->out) + (a->out ? r0 : 0);
+    sp.init = init;
+    sp.final_state = fin;
+    sp.init_bf16 = ib;
+    sp.final_bf16 = fb;
+    sp.scale = a->scale;
+    sp.cu = a->cu_seqlens;
+    sp.chunk_off = chunk_off;
+    sp.N = a->N;
+    sp.T = span;
+    sp.H = a->H;
+    sp.NT = ceil_div(span, kChunk);
+    sp.ld = a->T;
+    sp.ws = ws_r;
+    launch_state_kernel(sp, s);
+  };
+
+  if (ranges == 1) {
+    mark(0);
+    if (a->cu_seqlens)
+      launch_chunk_offsets(a->cu_seqlens, a->N, a->T, chunk_off, status_device_ptr(), stream);
+    launch_chunks(0, a->T, slots_base, stream, 0);
+    mark(1);
+    launch_state(0, a->T, slots_base, a->initial_state, a->final_state, ib16, fb16, stream);
+    mark(2);
+  } else {
+    // chunk stage of range r on the caller's stream, state stage on the
+    // high-priority stream after it; the fp32 state passes from range to range
+    PipeCtx& c = g_pipe[dev];
+    std::lock_guard<std::mutex> lock(c.mu);
+    if (!make_pipe_ctx(c)) return KDA_ERR_LAUNCH;
+    const int64_t span = ceil_div(ceil_div(a->T, kChunk), ranges) * kChunk;
+    mark(0);
+    cudaEventRecord(c.start, stream);
+    cudaStreamWaitEvent(c.state_stream, c.start, 0);
+    unsigned char* ws_r = slots_base;
+    int r = 0;
+    for (int64_t t0 = 0; t0 < a->T; t0 += span, ++r) {
+      const int64_t len = std::min(span, a->T - t0);
+      const bool first = t0 == 0, last = t0 + len == a->T;
+      // from the second range on, the previous range's state stage holds four SMs per head
+      launch_chunks(t0, len, ws_r, stream, first ? 0 : (int)(a->N * a->H * (kHeadDim / 32)));
+      cudaEventRecord(c.chunked[r], stream);
+      cudaStreamWaitEvent(c.state_stream, c.chunked[r], 0);
+      launch_state(t0, len, ws_r, first ? a->initial_state : carry, last ? a->final_state : carry,
+                   first ? ib16 : 0, last ? fb16 : 0, c.state_stream);
+      ws_r += (size_t)(a->B * ceil_div(len, kChunk) * a->H) * kSlotBytes;
+    }
+    mark(1);
+    cudaEventRecord(c.end, c.state_stream);
+    cudaStreamWaitEvent(stream, c.end, 0);
+    mark(2);
   }
-
-  mark(1);
-  StateParams sp;
-  sp.out = static_cast<uint16_t*>(a->out);
-  sp.init = a->initial_state;
-  sp.final_state = a->final_state;
-  const int sb16 = a->state_dtype == KDA_DTYPE_BF16 ? 1 : 0;
-  sp.init_bf16 = init_bf16 >= 0 ? init_bf16 : sb16;
-  sp.final_bf16 = final_bf16 >= 0 ? final_bf16 : sb16;
-  sp.scale = a->scale;
-  sp.cu = a->cu_seqlens;
-  sp.chunk_off = chunk_off;
-  sp.N = a->N;
-  sp.T = a->T;
-  sp.H = a->H;
-  sp.NT = NT;
-  sp.ws = slots_base;
-  launch_state_kernel(sp, stream);
-  mark(2);
-
   if (cudaGetLastError() != cudaSuccess) return KDA_ERR_LAUNCH;
   return KDA_OK;
 }
@@ -212,13 +318,13 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
 extern "C" int kda_fwd(const kda_fwd_args* a, void* workspace, size_t workspace_bytes,
                        void* stream) {
   return fwd_device(a, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream), nullptr,
-                    -1, -1);
+                    -1, -1, true);
 }
 
 extern "C" int kda_fwd_profiled(const kda_fwd_args* a, void* workspace, size_t workspace_bytes,
                                 void* stream, void* const events[3]) {
   return fwd_device(a, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream), events,
-                    -1, -1);
+                    -1, -1, true);
 }
 
 extern "C" int kda_fwd_recurrent(const kda_fwd_args* a, void* stream_ptr) {

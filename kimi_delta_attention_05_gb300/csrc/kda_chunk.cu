@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
     } else {
       n = idx32 ? (int64_t)((uint32_t)r.slot / (uint32_t)p.NT) : r.slot / p.NT;
       i = r.slot - n * p.NT;
-      bos = n * p.T;
+      bos = n * p.ld;
       seqlen = p.T;
     }
     r.t0 = bos + i * kChunk;
@@ -672,13 +672,16 @@ static void launch_variant(const ChunkParams& p, unsigned grid, int64_t items, c
   kda_chunk_kernel<kGate, kL2><<<grid, 256, kChunkSmem, stream>>>(p, items);
 }
 
-void launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t stream) {
-  // persistent grid: two CTAs per SM (the shared-memory and register budget), or fewer items
+void launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t stream,
+                         int busy_sms) {
+  // persistent grid: two CTAs per SM (the shared-memory and register budget) on
+  // the SMs another kernel does not hold, or fewer items
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t items = num_slots * p.H;
-  const unsigned grid = (unsigned)min(items, (int64_t)(2 * (sms > 0 ? sms : 1)));
+  const int free_sms = sms - busy_sms > 0 ? sms - busy_sms : 1;
+  const unsigned grid = (unsigned)min(items, (int64_t)(2 * free_sms));
   const bool l2 = p.l2norm != 0;
   switch (p.gate_mode) {
     case kGateUnsafe:

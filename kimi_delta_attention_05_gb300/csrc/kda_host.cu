@@ -307,7 +307,7 @@ extern "C" int kda_fwd_host(const kda_fwd_args* a, void* device_buffer, size_t d
     chk(cudaEventRecord(c.loaded[p], hs));
     if (!ok) break;
     chk(cudaStreamWaitEvent(st, c.loaded[p], 0));
-    rc = fwd_device(&sub, d + pl.ws, pl.ws_bytes, st, nullptr, init_bf16, final_bf16);
+    rc = fwd_device(&sub, d + pl.ws, pl.ws_bytes, st, nullptr, init_bf16, final_bf16, false);
     if (rc != KDA_OK) break;
     chk(cudaEventRecord(c.computed[p], st));
     chk(cudaStreamWaitEvent(c.d2h, c.computed[p], 0));

@@ -26,6 +26,7 @@ struct ChunkParams {
   const int64_t* chunk_off;               // [N+1] chunk prefix (varlen only)
   int64_t N, T, H;
   int64_t NT;                             // chunks per row (dense)
+  int64_t ld;                             // dense: rows from one sequence's start to the next (>= T)
   unsigned char* ws;                      // first workspace slot
 };
 
@@ -39,6 +40,7 @@ struct StateParams {
   const int64_t* cu;
   const int64_t* chunk_off;
   int64_t N, T, H, NT;
+  int64_t ld;                             // dense: rows from one sequence's start to the next (>= T)
   const unsigned char* ws;
 };
 
@@ -70,9 +72,12 @@ int validate(const kda_fwd_args* args, int64_t* num_slots, size_t* header_bytes)
 // of kda_fwd).  init_bf16 / final_bf16 >= 0 override the state dtype of the
 // initial / final state separately (the host-buffer entry point carries the
 // state between pieces in fp32 whatever the caller's dtype); -1 keeps
-// args->state_dtype.
+// args->state_dtype.  allow_pipeline: the two stages of consecutive token
+// ranges may overlap on two streams (needs the larger workspace that
+// kda_fwd_workspace_bytes reports for such calls).
 int fwd_device(const kda_fwd_args* args, void* workspace, size_t workspace_bytes,
-               cudaStream_t stream, void* const* events, int init_bf16, int final_bf16);
+               cudaStream_t stream, void* const* events, int init_bf16, int final_bf16,
+               bool allow_pipeline);
 
 void launch_recurrent_kernel(const RecurrentParams& p, cudaStream_t s);
 cudaError_t prepare_recurrent_kernel();
@@ -83,7 +88,8 @@ void launch_chunk_offsets(const int64_t* cu, int64_t N, int64_t T, int64_t* chun
                           cudaStream_t s);
 // Device address of the library's sticky status word on the current device.
 int* status_device_ptr();
-void launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t s);
+// busy_sms: SMs held by a kernel running alongside (the persistent grid covers the rest)
+void launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t s, int busy_sms = 0);
 void launch_state_kernel(const StateParams& p, cudaStream_t s);
 cudaError_t prepare_chunk_kernel();
 cudaError_t prepare_state_kernel();

@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
     slot0 = p.chunk_off[n];
     nch = p.chunk_off[n + 1] - slot0;
   } else {
-    bos = n * p.T;
+    bos = n * p.ld;
     len = p.T;
     slot0 = n * p.NT;
     nch = (len + kChunk - 1) / kChunk;

@@ -173,3 +173,20 @@ def test_g_in_fp32_through_host_entry():
     ro, rf = tl.run_oracle(inp)
     tl.check_out(o_h, ro, "host fp32 g packed")
     tl.check_state(f_h, rf, "host fp32 g packed")
+
+
+@pytest.mark.parametrize("gate,B,T,H", [("unsafe", 1, 4096, 4), ("safe", 2, 3000, 2)])
+def test_stage_pipeline_is_bit_exact(gate, B, T, H):
+    """Few sequence-heads and long sequences: kda_fwd overlaps the state stage
+    of one token range with the intra-chunk stage of the next on two streams,
+    carrying the state in fp32.  The host entry runs the same single-piece
+    problem without that overlap: the results are identical."""
+    inp = make_inputs(WORKLOADS["dense_batch"], B=B, T=T, H=H, seed=71)
+    inp.update(gate=gate)
+    assert B * T * H * 1026 < PIECE_BYTES  # one piece on the host path
+    o_h, f_h = _run_host(inp)
+    o_d, f_d = tl.run_gpu(inp)
+    assert np.array_equal(o_h, o_d) and np.array_equal(f_h, f_d)
+    ro, rf = tl.run_oracle(inp)
+    tl.check_out(o_d, ro, "pipelined stages")
+    tl.check_state(f_d, rf, "pipelined stages")
