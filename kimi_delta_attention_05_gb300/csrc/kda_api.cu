@@ -146,12 +146,14 @@ int device_sms() {
 // Token ranges a dense pass is cut into (every range of every sequence, whole
 // chunks), so that the state stage of range r, on a high-priority stream,
 // overlaps the intra-chunk stage of range r + 1 on the SMs it leaves free.  It
-// pays when the state stage occupies at most half the SMs (few sequence-heads:
-// four 32-column CTAs per head) and the sequences are long; otherwise 1.
+// pays when the state stage, in four 32-column CTAs per head, fits in half the
+// SMs (few sequence-heads) and the sequences are long; otherwise 1.  (With the
+// 64-column shape, which would admit 32 heads, it measured within run-to-run
+// noise: 0.314 -> 0.309 ms on B1 T8192 H32.)
 int pipeline_ranges(const kda_fwd_args* a, int sms) {
   if (a->cu_seqlens || sms <= 0) return 1;
-  const int64_t state_ctas = a->N * a->H * (kHeadDim / 32);
-  if (state_ctas == 0 || 2 * state_ctas > sms) return 1;
+  const int64_t units = a->N * a->H;
+  if (units == 0 || 2 * units * 4 > sms) return 1;
   if (ceil_div(a->T, kChunk) < 32) return 1;
   return KDA_PIPE_RANGES;
 }
@@ -272,7 +274,7 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
     sp.NT = ceil_div(span, kChunk);
     sp.ld = a->T;
     sp.ws = ws_r;
-    launch_state_kernel(sp, s);
+    launch_state_kernel(sp, s, ranges > 1 ? device_sms() / 2 : 0);
   };
 
   if (ranges == 1) {
@@ -298,8 +300,9 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
     for (int64_t t0 = 0; t0 < a->T; t0 += span, ++r) {
       const int64_t len = std::min(span, a->T - t0);
       const bool first = t0 == 0, last = t0 + len == a->T;
-      // from the second range on, the previous range's state stage holds four SMs per head
-      launch_chunks(t0, len, ws_r, stream, first ? 0 : (int)(a->N * a->H * (kHeadDim / 32)));
+      // from the second range on, the previous range's state stage holds its SMs
+      const int state_ctas = (int)(a->N * a->H) * state_tiles(a->N * a->H, device_sms() / 2);
+      launch_chunks(t0, len, ws_r, stream, first ? 0 : state_ctas);
       cudaEventRecord(c.chunked[r], stream);
       cudaStreamWaitEvent(c.state_stream, c.chunked[r], 0);
       launch_state(t0, len, ws_r, first ? a->initial_state : carry, last ? a->final_state : carry,

@@ -90,7 +90,11 @@ void launch_chunk_offsets(const int64_t* cu, int64_t N, int64_t T, int64_t* chun
 int* status_device_ptr();
 // busy_sms: SMs held by a kernel running alongside (the persistent grid covers the rest)
 void launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t s, int busy_sms = 0);
-void launch_state_kernel(const StateParams& p, cudaStream_t s);
+// max_ctas: at most this many CTAs at once (0: the SM count) picks the
+// 32-column shape (four CTAs per head) if they fit, else the 64-column one
+void launch_state_kernel(const StateParams& p, cudaStream_t s, int max_ctas = 0);
+// CTAs per head the state stage uses for `units` (sequence, head) pairs under max_ctas
+int state_tiles(int64_t units, int max_ctas);
 cudaError_t prepare_chunk_kernel();
 cudaError_t prepare_state_kernel();
 

@@ -481,13 +481,16 @@ static void launch_state_variant(const StateParams& p, cudaStream_t stream) {
 // CTAs (two per head) halve the bytes all CTAs of a head pull through their SM
 // ports per chunk.  So: four per head while they fit on the GPU at once (one
 // CTA per SM), two per head once they would run in more than one wave.
-void launch_state_kernel(const StateParams& p, cudaStream_t stream) {
+void launch_state_kernel(const StateParams& p, cudaStream_t stream, int max_ctas) {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (p.N * p.H * (kHeadDim / 32) <= (int64_t)sms) launch_state_variant<32>(p, stream);
+  const int64_t budget = max_ctas > 0 && max_ctas < sms ? max_ctas : sms;
+  if (state_tiles(p.N * p.H, (int)budget) == 4) launch_state_variant<32>(p, stream);
   else launch_state_variant<64>(p, stream);
 }
+
+int state_tiles(int64_t units, int max_ctas) { return units * 4 <= max_ctas ? 4 : 2; }
 
 cudaError_t prepare_state_kernel() {
   const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
