@@ -147,14 +147,17 @@ def kda_fwd(q, k, v, g, beta, scale, out=None, A_log=None, dt_bias=None, lower_b
     optional pre-allocated uint8 device tensor; ``stream`` a torch stream.
     """
     lib = load_library()
-    if out is None:
-        out = torch.empty_like(v)
-    a = make_args(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
-                  final_state, cu_seqlens, qk_l2norm, gate, beta_prob)
-    need = int(lib.kda_fwd_workspace_bytes(ctypes.byref(a)))
-    if workspace is None or workspace.numel() < need:
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    # buffers made here are allocated on the stream that uses them, so the
+    # caching allocator does not hand them out again while that stream runs
+    with torch.cuda.stream(s):
+        if out is None:
+            out = torch.empty_like(v)
+        a = make_args(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
+                      final_state, cu_seqlens, qk_l2norm, gate, beta_prob)
+        need = int(lib.kda_fwd_workspace_bytes(ctypes.byref(a)))
+        if workspace is None or workspace.numel() < need:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     rc = lib.kda_fwd(ctypes.byref(a), ctypes.c_void_p(workspace.data_ptr()), need,
                      ctypes.c_void_p(s.cuda_stream))
     if rc != 0:
@@ -168,11 +171,12 @@ def kda_fwd_recurrent(q, k, v, g, beta, scale, out=None, A_log=None, dt_bias=Non
     """Token-by-token forward (decoding path, no workspace); same arguments as
     :func:`kda_fwd`.  ``final_state`` may be ``initial_state`` itself."""
     lib = load_library()
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
     if out is None:
-        out = torch.empty_like(v)
+        with torch.cuda.stream(s):
+            out = torch.empty_like(v)
     a = make_args(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
                   final_state, cu_seqlens, qk_l2norm, gate, beta_prob)
-    s = stream if stream is not None else torch.cuda.current_stream(q.device)
     rc = lib.kda_fwd_recurrent(ctypes.byref(a), ctypes.c_void_p(s.cuda_stream))
     if rc != 0:
         raise KdaError(rc, lib.kda_error_string(rc).decode())
@@ -214,9 +218,10 @@ def kda_fwd_host(q, k, v, g, beta, scale, out=None, A_log=None, dt_bias=None, lo
     a = make_args(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state,
                   final_state, cu_seqlens, qk_l2norm, gate, beta_prob)
     need = int(lib.kda_fwd_host_device_bytes(ctypes.byref(a)))
-    if device_buffer is None or device_buffer.numel() < need:
-        device_buffer = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
+    if device_buffer is None or device_buffer.numel() < need:
+        with torch.cuda.stream(s):  # allocated on the stream that uses it
+            device_buffer = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     rc = lib.kda_fwd_host(ctypes.byref(a), ctypes.c_void_p(device_buffer.data_ptr()), need,
                           ctypes.c_void_p(s.cuda_stream))
     if rc != 0:

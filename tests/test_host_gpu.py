@@ -190,3 +190,35 @@ def test_stage_pipeline_is_bit_exact(gate, B, T, H):
     ro, rf = tl.run_oracle(inp)
     tl.check_out(o_d, ro, "pipelined stages")
     tl.check_state(f_d, rf, "pipelined stages")
+
+
+def test_stage_pipeline_two_streams_at_once():
+    """Two pipelined calls issued on two streams without ordering between them
+    (they share the library's state stream and events): each result equals the
+    same call run alone."""
+    cases = [make_inputs(WORKLOADS["long_context"], T=4096, H=4, seed=72),
+             make_inputs(WORKLOADS["extremes"], B=1, T=6000, H=3, seed=73)]
+    alone = [tl.run_gpu(inp) for inp in cases]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    devs, outs, fins = [], [], []
+    for inp in cases:
+        d = tl.to_device(inp)
+        devs.append(d)
+        outs.append(torch.full_like(d["v"], float("nan")))
+        fdt = inp.get("final_state")
+        fins.append(None if fdt is None else torch.full(
+            (inp["N"], d["q"].shape[2], 128, 128), float("nan"), device="cuda",
+            dtype=torch.bfloat16 if fdt == "bf16" else torch.float32))
+    torch.cuda.synchronize()
+    from kimi_delta_attention_05_gb300 import kda_fwd
+    for rep in range(3):
+        for inp, d, out, fin, s in zip(cases, devs, outs, fins, streams):
+            lb = inp["lower_bound"] if inp["gate"] == "safe" else None
+            kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], inp["scale"], out, d["A_log"],
+                    d["dt_bias"], lb, d["initial_state"], fin, d["cu_seqlens"],
+                    qk_l2norm=inp["qk_l2norm"], gate=inp["gate"], stream=s)
+    torch.cuda.synchronize()
+    for (o_ref, f_ref), out, fin in zip(alone, outs, fins):
+        assert np.array_equal(out.float().cpu().numpy().astype(np.float64), o_ref)
+        if fin is not None:
+            assert np.array_equal(fin.float().cpu().numpy().astype(np.float64), f_ref)
