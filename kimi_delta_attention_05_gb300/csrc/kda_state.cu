@@ -1,10 +1,11 @@
 // Recurrent stage of the KDA forward pass on the 5th-generation tensor cores
-// (tcgen05, accumulators in tensor memory): one CTA per (sequence, head,
-// 64-wide value tile), walking the chunks of its sequence in order and
+// (tcgen05, accumulators in tensor memory): one CTA per (sequence, head, value
+// tile of 32 or 64 columns), walking the chunks of its sequence in order and
 // bringing each chunk's operand block in with bulk copies, issued in parallel
-// by nine lanes of a producer warp.  Two CTAs per head (not four of 32
-// columns) because every CTA of a head receives the same 57 KB of chunk
-// operands through its SM's L2 port, the resource that bounds this stage.
+// by nine lanes of a producer warp.  Four 32-column CTAs per head while they
+// all fit on the GPU at once (shortest chunk period), else two 64-column ones
+// (every CTA of a head receives the same 57 KB of chunk operands through its
+// SM's L2 port, so fewer CTAs per head move fewer bytes).
 //
 // Per chunk, with S the state (rows = value index, columns = key index) at
 // the chunk start and the intra-chunk quantities of the workspace slot:
@@ -12,16 +13,20 @@
 //   O     = scale (Q_gamma S^T + P U_new)  (inter + intra read-out, fused as in
 //                                          the chunk_o stage of the fla code map)
 //   S     = S Diag(gamma_C) + U_new^T K_hat   (chunk_delta_h state update)
-// as three tensor-core products, each issued by one thread:
-//   MMA1: D1 [128 x 64]  = [Q_gamma; W] (128 x 128) . S^T        (rows 64.. = W S^T)
-//   MMA2: D3 [128 x 64]  = K_hat^T (128 x 64)       . U_new       (state delta, row = key)
+// as three tensor-core products, each issued by one thread (widths for a
+// tile of kVT value columns):
+//   MMA1: D1 [128 x kVT] = [Q_gamma; W] (128 x 128) . S^T        (rows 64.. = W S^T)
+//   MMA2: D3 [128 x kVT] = K_hat^T (128 x 64)       . U_new       (state delta, row = key)
 //   MMA3: D1[0..63]     += [P; *]   (128 x 64)       . U_new       (output rows)
-// The state master copy is fp32 in the registers of the eight epilogue warps
-// (warp = tensor-memory lane quarter x 32-column half, thread = key index);
+// The state master copy is fp32 in the registers of the epilogue warps
+// (warp = tensor-memory lane quarter x 32-column group, thread = key index);
 // each chunk it is published as an fp16 operand tile for the next MMA1.
-// Roles: warps 0-7 epilogue, warp 8 bulk copies, warp 9 tensor-core issue.
-// Every wait is bounded: a CTA that gives up sets the device status word and
-// stops waiting, so it cannot hang.
+// Roles: epilogue warps, then one bulk-copy warp, then the tensor-core warp.
+// Waits on mbarriers (copies landed, products complete) are bounded: a CTA that
+// gives up sets the device status word and stops waiting.  The two epilogue ->
+// tensor-core hand-offs use named barriers, which every participating warp
+// passes exactly once per chunk (plus once for the initial state) whatever
+// happens, so they always complete.
 #include <atomic>
 
 #include "kda_common.cuh"
@@ -34,8 +39,10 @@ constexpr int kSA1 = 0;          // kmaj R=128 K=128: [q gamma; W]
 constexpr int kSKh = 32768;      // kmaj R=64 (t) K=128 (k): k_hat (MN-major A of MMA2)
 constexpr int kSP = 49152;       // kmaj R=64 K=64: P  (rows 0..63 of the A operand of MMA3)
 constexpr int kStages = 3;
-constexpr int kBarFull = 0, kBarEmpty = 3, kBarMma1 = 6, kBarMma2 = 7, kBarUn = 8, kBarS = 9,
-              kBarMma3 = 10, kNumBars = 11;
+// (U_new and S are published to the tensor-core warp through hardware named
+// barriers, below: an mbarrier hand-off measured ~230-430 cycles, a named one
+// ~120.)
+constexpr int kBarFull = 0, kBarEmpty = 3, kBarMma1 = 6, kBarMma2 = 7, kBarMma3 = 8, kNumBars = 9;
 constexpr int kPiece = kSP + 8192 - kSA1;    // 57344: the shared block minus gamma_C
 constexpr int kPieces = 7;                   // copied as 7 pieces of 8 KB, one per lane
 static_assert(kPiece == kPieces * 8192, "piece split");
@@ -65,6 +72,8 @@ struct StateCfg {
   static constexpr int kSmem = kSAbort + 8 + 1024;
   static constexpr uint32_t kStageTx = kPiece + 512 + kVT * 128;  // bytes landing per stage
   static constexpr uint32_t kTmemCols = kVT == 32 ? 128 : 256;    // D1 x 2 and D3
+  static constexpr int kNbSCount = 32 * (kEpiWarps + 1);       // S published: epilogue + MMA warp
+  static constexpr int kNbUnCount = 32 * (kEpiWarps / 2 + 1);  // U_new published: lanes 64.. + MMA warp
   // The fp16 B operands S (N = v, K = k) and U_new (N = v, K = t) are stored
   // MN-major: one row of the CTA's kVT values per k (or t), so a thread that
   // holds a row writes it with 16-byte stores.  64 columns fill a 128-byte
@@ -136,6 +145,16 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
+// Hardware named barriers (ids 1, 2; 0 is __syncthreads): the publishing warps
+// arrive, the tensor-core warp (all 32 lanes) waits.  Every participant passes
+// each barrier the same number of times, whatever happens (no early exits).
+constexpr int kNbS = 1, kNbUn = 2;
+__device__ __forceinline__ void named_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 __device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
 }
@@ -182,8 +201,6 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
     mbar_init(B(kBarMma1), 1);
     mbar_init(B(kBarMma2), 1);
     mbar_init(B(kBarMma3), 1);
-    mbar_init(B(kBarUn), C::kEpiWarps / 2);  // the epilogue warps on lanes 64..127
-    mbar_init(B(kBarS), C::kEpiWarps);
     *s_abort = (sb & 1023) ? 1 : 0;  // the swizzled operand images need 1024-byte alignment
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
@@ -242,8 +259,9 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
       for (int64_t c = 0; c < issued; ++c)
         mbar_wait_bounded(B(kBarFull + (int)(c % kStages)), (uint32_t)((c / kStages) & 1));
   } else if (warp == C::kMmaWarp) {
-    // ---- tensor-core issuer ----
-    if (lane == 0) {
+    // ---- tensor-core issuer: the whole warp keeps step with the named barriers,
+    //      lane 0 issues ----
+    {
       const uint32_t id1 = idesc_f16(128, C::kVTile, false, true);
       const uint32_t id2 = idesc_f16(128, C::kVTile, true, true);
       const uint32_t d3 = tmem + 2 * C::kVTile;
@@ -261,28 +279,35 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
         const uint64_t so = (uint64_t)((st * C::kStageBytes) >> 4);
         const uint32_t d1 = tmem + C::kVTile * par;
         wait(B(kBarFull + st), phf);
-        wait(B(kBarS), par);  // S of this chunk published
+        named_sync(kNbS, C::kNbSCount);  // S of this chunk published
         tc_fence_after();
+        if (lane == 0) {
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          tc_mma(d1, dA1 + so + (uint64_t)(((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
-                 dS + (uint64_t)((ks * kStepB) >> 4), id1, ks > 0);
-        tc_commit(B(kBarMma1));
-        wait(B(kBarUn), par);  // U_new of this chunk published
+          for (int ks = 0; ks < 8; ++ks)
+            tc_mma(d1, dA1 + so + (uint64_t)(((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                   dS + (uint64_t)((ks * kStepB) >> 4), id1, ks > 0);
+          tc_commit(B(kBarMma1));
+        }
+        __syncwarp();
+        named_sync(kNbUn, C::kNbUnCount);  // U_new of this chunk published
         tc_fence_after();
+        if (lane == 0) {
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          tc_mma(d3, dKh + so + (uint64_t)((ks * 2048) >> 4), dUn + (uint64_t)((ks * kStepB) >> 4),
-                 id2, ks > 0);
-        tc_commit(B(kBarMma2));  // the state update can start
+          for (int ks = 0; ks < 4; ++ks)
+            tc_mma(d3, dKh + so + (uint64_t)((ks * 2048) >> 4), dUn + (uint64_t)((ks * kStepB) >> 4),
+                   id2, ks > 0);
+          tc_commit(B(kBarMma2));  // the state update can start
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          tc_mma(d1, dP + so + (uint64_t)((ks * 32) >> 4), dUn + (uint64_t)((ks * kStepB) >> 4), id1, 1);
-        tc_commit(B(kBarMma3));
-        tc_commit(B(kBarEmpty + st));  // the stage's operands are no longer read by the tensor core
+          for (int ks = 0; ks < 4; ++ks)
+            tc_mma(d1, dP + so + (uint64_t)((ks * 32) >> 4), dUn + (uint64_t)((ks * kStepB) >> 4), id1, 1);
+          tc_commit(B(kBarMma3));
+          tc_commit(B(kBarEmpty + st));  // the stage's operands are no longer read by the tensor core
+        }
+        __syncwarp();
         if (++st == kStages) { st = 0; phf ^= 1u; }
       }
-      if (nch > 0)  // the last products must be complete before tensor memory is freed
+      named_sync(kNbS, C::kNbSCount);  // the state published after the last chunk (no product uses it)
+      if (lane == 0 && nch > 0)  // the last products must be complete before tensor memory is freed
         mbar_wait_bounded(B(kBarMma3), (uint32_t)((nch - 1) & 1));
     }
   } else {
@@ -315,7 +340,7 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_local(B(kBarS));
+      named_arrive(kNbS, C::kNbSCount);
     };
     publish_state();
 
@@ -366,10 +391,8 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive_local(B(kBarUn));
-          mbar_arrive_local(B(kBarEmpty + st));  // U tile read
-        }
+        named_arrive(kNbUn, C::kNbUnCount);
+        if (lane == 0) mbar_arrive_local(B(kBarEmpty + st));  // U tile read
       }
       wait(B(kBarMma2), par);
       tc_fence_after();
