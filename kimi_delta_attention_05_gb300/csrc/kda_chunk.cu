@@ -100,31 +100,6 @@ __device__ __forceinline__ void scale_bfrag(uint32_t& b0, uint32_t& b1, uint32_t
   b1 = mul_bf16x2(b1, f89);
 }
 
-// Pairs of fp32 values in one 64-bit register for the packed f32x2 arithmetic
-// of sm_100-class SMs: one instruction per pair, each lane rounded exactly as
-// the scalar instruction would (round to nearest, no flush), so results are
-// bit-identical to the scalar form.  Channel pairs (c, c + 1) travel together.
-typedef unsigned long long f32x2;
-__device__ __forceinline__ f32x2 f2(float lo, float hi) {
-  f32x2 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ float2 f2u(f32x2 v) {
-  float2 r;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
-  return r;
-}
-__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
-  f32x2 d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
-  f32x2 d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
 // The two bf16 values of a 32-bit word (low half first) as fp32.
 __device__ __forceinline__ f32x2 bf2_to_f2(uint32_t w) {
   return f2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));

@@ -178,6 +178,42 @@ __device__ __forceinline__ void ldb_kn_128(uint32_t (&b)[4], uint32_t base, int 
   ldsm_x4_t(b, base + swz128(k0 + ((mi & 1) << 3) + (lane & 7), n0 + ((mi >> 1) << 3)));
 }
 
+// Pairs of fp32 values in one 64-bit register for the packed f32x2 arithmetic
+// of sm_100-class SMs: one instruction per pair, each lane rounded exactly as
+// the scalar instruction would (round to nearest, no flush), so results are
+// bit-identical to the scalar form.  Channel pairs (c, c + 1) travel together.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 f2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2u(f32x2 v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// a * b + c with one rounding per lane (as the scalar fused multiply-add)
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
 // ---- mbarrier + bulk-copy (TMA engine) primitives ----
 __device__ __forceinline__ void mbar_init(uint32_t addr, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(addr), "r"(count) : "memory");
