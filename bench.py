@@ -263,9 +263,11 @@ def run_ours(a, inp, dev, rank, world):
     ms = t_start.elapsed_time(t_end)
     chunk_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)]
     state_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(steps)]
+    call_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(steps)]  # one call, event to event
     ms = max_over_ranks(ms, world, dev)
     return dict(ms=ms, steps=steps, chunk_ms=statistics.mean(chunk_ms),
                 state_ms=statistics.mean(state_ms), launches=launches_per_step * steps,
+                call_median_ms=statistics.median(call_ms), call_min_ms=min(call_ms),
                 clocks=clk.summary(w0, w1))
 
 
@@ -548,6 +550,8 @@ def main():
                      "path": {"achieved": path_gbs, "frac": path_gbs / hbm,
                               "roofline_ms": roof_t * 1e3, "frac_of_roofline": roof_t * 1e3 / ms_step}},
         "stages_ms": {"kda_chunk_kernel": r["chunk_ms"], "kda_state_kernel": r["state_ms"]},
+        "call_ms": {"median": r["call_median_ms"], "min": r["call_min_ms"],
+                    "note": "per call, from the event before its first launch to the one after its last"},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }
