@@ -292,9 +292,11 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
     std::lock_guard<std::mutex> lock(c.mu);
     if (!make_pipe_ctx(c)) return KDA_ERR_LAUNCH;
     const int64_t span = ceil_div(ceil_div(a->T, kChunk), ranges) * kChunk;
+    bool ok = true;
+    auto chk = [&](cudaError_t e) { ok = ok && e == cudaSuccess; };
     mark(0);
-    cudaEventRecord(c.start, stream);
-    cudaStreamWaitEvent(c.state_stream, c.start, 0);
+    chk(cudaEventRecord(c.start, stream));
+    chk(cudaStreamWaitEvent(c.state_stream, c.start, 0));
     unsigned char* ws_r = slots_base;
     int r = 0;
     for (int64_t t0 = 0; t0 < a->T; t0 += span, ++r) {
@@ -303,16 +305,17 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
       // from the second range on, the previous range's state stage holds its SMs
       const int state_ctas = (int)(a->N * a->H) * state_tiles(a->N * a->H, device_sms() / 2);
       launch_chunks(t0, len, ws_r, stream, first ? 0 : state_ctas);
-      cudaEventRecord(c.chunked[r], stream);
-      cudaStreamWaitEvent(c.state_stream, c.chunked[r], 0);
+      chk(cudaEventRecord(c.chunked[r], stream));
+      chk(cudaStreamWaitEvent(c.state_stream, c.chunked[r], 0));
       launch_state(t0, len, ws_r, first ? a->initial_state : carry, last ? a->final_state : carry,
                    first ? ib16 : 0, last ? fb16 : 0, c.state_stream);
       ws_r += (size_t)(a->B * ceil_div(len, kChunk) * a->H) * kSlotBytes;
     }
     mark(1);
-    cudaEventRecord(c.end, c.state_stream);
-    cudaStreamWaitEvent(stream, c.end, 0);
+    chk(cudaEventRecord(c.end, c.state_stream));
+    chk(cudaStreamWaitEvent(stream, c.end, 0));
     mark(2);
+    if (!ok) return KDA_ERR_LAUNCH;
   }
   if (cudaGetLastError() != cudaSuccess) return KDA_ERR_LAUNCH;
   return KDA_OK;
