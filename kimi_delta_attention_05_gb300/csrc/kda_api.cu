@@ -143,17 +143,23 @@ int device_sms() {
   return sms;
 }
 
+// CTAs the state stage may hold while the intra-chunk stage of the next token
+// range runs beside it: half the SMs, in four 32-column CTAs per head; 0: no
+// overlap.  Measured on B1 T8192 H32, where they do not fit: with 64-column
+// CTAs (64 SMs) 0.314 -> 0.309 ms, within run-to-run noise; with one
+// 128-column CTA per head (32 SMs, 120 left to the intra-chunk stage; 16
+// epilogue warps per SM) 0.305 -> 0.365 ms, its chunk period being about
+// twice as long.
+int pipe_state_budget(int64_t units, int sms) { return units * 4 * 2 <= sms ? sms / 2 : 0; }
+
 // Token ranges a dense pass is cut into (every range of every sequence, whole
 // chunks), so that the state stage of range r, on a high-priority stream,
-// overlaps the intra-chunk stage of range r + 1 on the SMs it leaves free.  It
-// pays when the state stage, in four 32-column CTAs per head, fits in half the
-// SMs (few sequence-heads) and the sequences are long; otherwise 1.  (With the
-// 64-column shape, which would admit 32 heads, it measured within run-to-run
-// noise: 0.314 -> 0.309 ms on B1 T8192 H32.)
+// overlaps the intra-chunk stage of range r + 1 on the SMs it leaves free:
+// for few sequence-heads (above) and long sequences; otherwise 1.
 int pipeline_ranges(const kda_fwd_args* a, int sms) {
   if (a->cu_seqlens || sms <= 0) return 1;
   const int64_t units = a->N * a->H;
-  if (units == 0 || 2 * units * 4 > sms) return 1;
+  if (units == 0 || pipe_state_budget(units, sms) == 0) return 1;
   if (ceil_div(a->T, kChunk) < 32) return 1;
   return KDA_PIPE_RANGES;
 }
@@ -274,7 +280,7 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
     sp.NT = ceil_div(span, kChunk);
     sp.ld = a->T;
     sp.ws = ws_r;
-    launch_state_kernel(sp, s, ranges > 1 ? device_sms() / 2 : 0);
+    launch_state_kernel(sp, s, ranges > 1 ? pipe_state_budget(a->N * a->H, device_sms()) : 0);
   };
 
   if (ranges == 1) {
@@ -303,7 +309,8 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
       const int64_t len = std::min(span, a->T - t0);
       const bool first = t0 == 0, last = t0 + len == a->T;
       // from the second range on, the previous range's state stage holds its SMs
-      const int state_ctas = (int)(a->N * a->H) * state_tiles(a->N * a->H, device_sms() / 2);
+      const int budget = pipe_state_budget(a->N * a->H, device_sms());
+      const int state_ctas = (int)(a->N * a->H) * state_tiles(a->N * a->H, budget);
       launch_chunks(t0, len, ws_r, stream, first ? 0 : state_ctas);
       chk(cudaEventRecord(c.chunked[r], stream));
       chk(cudaStreamWaitEvent(c.state_stream, c.chunked[r], 0));

@@ -47,22 +47,26 @@ constexpr int kPiece = kSP + 8192 - kSA1;    // 57344: the shared block minus ga
 constexpr int kPieces = 7;                   // copied as 7 pieces of 8 KB, one per lane
 static_assert(kPiece == kPieces * 8192, "piece split");
 
-// Layout and roles for a CTA of kVT value columns (32 or 64; 128 / kVT CTAs per
-// head).  Rows 64..127 of MMA3's A operand are the 8 KB after P: zeros with
-// 32 columns; with 64 (where the zeros do not fit) whatever follows P, whose
-// products land in rows of D1 that U_new has already consumed.
+// Layout and roles for a CTA of kVT value columns (32, 64 or 128; 128 / kVT
+// CTAs per head).  Rows 64..127 of MMA3's A operand are the 8 KB after P:
+// zeros with 32 columns; otherwise (where the zeros do not fit) whatever
+// follows P, whose products land in rows of D1 that U_new has already consumed.
+// (The layout also admits 128 columns, one head per SM: two stages of 73 KB
+// and all 512 tensor-memory columns; its chunk period measured about twice
+// the 32-column one, so no launch uses it.)
 template <int kVT>
 struct StateCfg {
   static constexpr int kVTile = kVT;
   static constexpr int kEpiWarps = 4 * (kVT / 32);  // (lane quarter, 32-column group) pairs
   static constexpr int kProducerWarp = kEpiWarps, kMmaWarp = kEpiWarps + 1;
   static constexpr int kThreads = 32 * (kEpiWarps + 2);
+  static constexpr int kStg = kVT == 128 ? 2 : kStages;  // chunk stages in flight
   static constexpr bool kZeroPad = kVT == 32;
   static constexpr int kSZero = 57344;                   // 8 KB of zeros (kZeroPad only)
   static constexpr int kSGc = kZeroPad ? 65536 : 57344;  // fp32 [128] gamma_C
   static constexpr int kSU = kSGc + 512;                 // kVT / 32 U tiles [64 t][32 v] fp16
-  static constexpr int kStageBytes = kZeroPad ? 70656 : 66560;
-  static constexpr int kSS = kStages * kStageBytes;      // MN-major [128 k][kVT v] fp16: S
+  static constexpr int kStageBytes = (kSU + kVT * 128 + 1023) / 1024 * 1024;
+  static constexpr int kSS = kStg * kStageBytes;         // MN-major [128 k][kVT v] fp16: S
   static constexpr int kSUn = kSS + kVT * 256;           // MN-major [64 t][kVT v] fp16: U_new
   static constexpr int kSBar = kSUn + kVT * 128;         // mbarriers
   static constexpr int kSTmem = kSBar + 8 * kNumBars;    // tensor-memory base address
@@ -71,24 +75,31 @@ struct StateCfg {
   // descriptors above, under any swizzle mode, stays inside the allocation.
   static constexpr int kSmem = kSAbort + 8 + 1024;
   static constexpr uint32_t kStageTx = kPiece + 512 + kVT * 128;  // bytes landing per stage
-  static constexpr uint32_t kTmemCols = kVT == 32 ? 128 : 256;    // D1 x 2 and D3
+  static constexpr uint32_t kTmemCols = kVT == 32 ? 128 : (kVT == 64 ? 256 : 512);  // D1 x 2, D3
   static constexpr int kNbSCount = 32 * (kEpiWarps + 1);       // S published: epilogue + MMA warp
   static constexpr int kNbUnCount = 32 * (kEpiWarps / 2 + 1);  // U_new published: lanes 64.. + MMA warp
   // The fp16 B operands S (N = v, K = k) and U_new (N = v, K = t) are stored
-  // MN-major: one row of the CTA's kVT values per k (or t), so a thread that
-  // holds a row writes it with 16-byte stores.  64 columns fill a 128-byte
-  // swizzle atom, 32 columns a 64-byte one.
-  static constexpr int kRowB = 2 * kVT;                    // bytes per row
-  static constexpr uint32_t kBLayout = kVT == 64 ? 2u : 4u;  // descriptor: 128- / 64-byte swizzle
-  static constexpr uint32_t kBSbo = 8 * kRowB;              // next group of 8 rows
-  // byte offset of 16-byte chunk `chunk` (values 8 chunk .. 8 chunk + 7) of row `row`
-  __device__ static uint32_t boff(int row, int chunk) {
-    return (uint32_t)(row * kRowB + ((chunk ^ (kVT == 64 ? (row & 7) : ((row >> 1) & 3))) << 4));
+  // MN-major: one row of values per k (or t), so a thread that holds a row
+  // writes it with 16-byte stores.  A row of a column block is one swizzle
+  // atom wide: 64 columns (128-byte swizzle) or 32 (64-byte); 128 columns are
+  // two 64-column blocks, the second `rows` rows after the first (the
+  // descriptor's leading byte offset).
+  static constexpr int kBlkCols = kVT < 64 ? kVT : 64;
+  static constexpr int kRowB = 2 * kBlkCols;                 // bytes per row of a column block
+  static constexpr uint32_t kBLayout = kVT == 32 ? 4u : 2u;  // descriptor: 64- / 128-byte swizzle
+  static constexpr uint32_t kBSbo = 8 * kRowB;               // next group of 8 rows
+  // byte offset of 16-byte chunk `chunk` (values 8 chunk .. 8 chunk + 7) of row `row` in a
+  // tile of `rows` rows
+  __device__ static uint32_t boff(int row, int chunk, int rows) {
+    const int blk = chunk / (kBlkCols / 8), c = chunk % (kBlkCols / 8);
+    return (uint32_t)(blk * rows * kRowB + row * kRowB +
+                      ((c ^ (kVT == 32 ? ((row >> 1) & 3) : (row & 7))) << 4));
   }
   static_assert(kStageBytes % 1024 == 0 && kSS % 1024 == 0 && kSUn % 1024 == 0,
                 "operand images need 1024-byte alignment");
   static_assert(kSU + kVT * 128 <= kStageBytes, "stage overflow");
   static_assert(kSmem <= 232448, "exceeds the opt-in shared memory of one CTA");
+  static_assert(kStg <= kStages, "barrier slots");
 };
 
 // Sticky device status: set to KDA_ERR_DEVICE_TIMEOUT (13) by a CTA that gave
@@ -194,7 +205,7 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
 
   // ---- set-up: barriers, zero tiles, tensor memory ----
   if (tid == 0) {
-    for (int st = 0; st < kStages; ++st) {
+    for (int st = 0; st < C::kStg; ++st) {
       mbar_init(B(kBarFull + st), 1);
       mbar_init(B(kBarEmpty + st), 1 + C::kEpiWarps);  // MMA commit + the epilogue warps
     }
@@ -205,7 +216,7 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (C::kZeroPad)
-    for (int i = tid; i < kStages * 512; i += C::kThreads)
+    for (int i = tid; i < C::kStg * 512; i += C::kThreads)
       reinterpret_cast<uint4*>(smem + (i >> 9) * C::kStageBytes + C::kSZero)[i & 511] =
           make_uint4(0, 0, 0, 0);
   if (warp == C::kMmaWarp) {
@@ -236,7 +247,7 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
     uint32_t ph_prev = 1;  // phase parity of the previous use of stage st
     for (int64_t ci = 0; ci < nch; ++ci) {
       if (st == 0) ph_prev ^= 1u;
-      if (ci >= kStages) wait(B(kBarEmpty + st), ph_prev ^ 1u);  // the stage is free again
+      if (ci >= C::kStg) wait(B(kBarEmpty + st), ph_prev ^ 1u);  // the stage is free again
       __syncwarp();
       if (*s_abort) break;
       const uint32_t dst = sb + st * C::kStageBytes;
@@ -253,11 +264,11 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
       else if (lane == kPieces + 1)
         bulk_g2s(dst + C::kSGc, src + kSlotGc, 512u, B(kBarFull + st));
       issued = ci + 1;
-      st = st + 1 == kStages ? 0 : st + 1;
+      st = st + 1 == C::kStg ? 0 : st + 1;
     }
     if (*s_abort && lane == 0)  // after a timeout: let this CTA's issued copies land before leaving
       for (int64_t c = 0; c < issued; ++c)
-        mbar_wait_bounded(B(kBarFull + (int)(c % kStages)), (uint32_t)((c / kStages) & 1));
+        mbar_wait_bounded(B(kBarFull + (int)(c % C::kStg)), (uint32_t)((c / C::kStg) & 1));
   } else if (warp == C::kMmaWarp) {
     // ---- tensor-core issuer: the whole warp keeps step with the named barriers,
     //      lane 0 issues ----
@@ -269,8 +280,8 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
       // (bytes >> 4) takes the stage and k-step offsets by plain addition
       const uint64_t dA1 = smem_desc(sb + kSA1, 16, 1024), dKh = smem_desc(sb + kSKh, 8192, 1024);
       const uint64_t dP = smem_desc(sb + kSP, 16, 1024);
-      const uint64_t dS = smem_desc(sb + C::kSS, 16, C::kBSbo, C::kBLayout);
-      const uint64_t dUn = smem_desc(sb + C::kSUn, 16, C::kBSbo, C::kBLayout);
+      const uint64_t dS = smem_desc(sb + C::kSS, 128 * C::kRowB, C::kBSbo, C::kBLayout);
+      const uint64_t dUn = smem_desc(sb + C::kSUn, 64 * C::kRowB, C::kBSbo, C::kBLayout);
       constexpr uint32_t kStepB = 16 * C::kRowB;  // one K step (16 rows) of an MN-major B
       int st = 0;
       uint32_t phf = 0;  // phase parity of the full barrier of stage st
@@ -304,7 +315,7 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
           tc_commit(B(kBarEmpty + st));  // the stage's operands are no longer read by the tensor core
         }
         __syncwarp();
-        if (++st == kStages) { st = 0; phf ^= 1u; }
+        if (++st == C::kStg) { st = 0; phf ^= 1u; }
       }
       named_sync(kNbS, C::kNbSCount);  // the state published after the last chunk (no product uses it)
       if (lane == 0 && nch > 0)  // the last products must be complete before tensor memory is freed
@@ -334,7 +345,7 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
     auto publish_state = [&]() {  // row k of S^T: this warp's 32 values, four 16-byte chunks
 #pragma unroll
       for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4*>(smem + C::kSS + C::boff(k, 4 * hc + c)) =
+        *reinterpret_cast<uint4*>(smem + C::kSS + C::boff(k, 4 * hc + c, 128)) =
             make_uint4(pack_f16(s[8 * c], s[8 * c + 1]), pack_f16(s[8 * c + 2], s[8 * c + 3]),
                        pack_f16(s[8 * c + 4], s[8 * c + 5]), pack_f16(s[8 * c + 6], s[8 * c + 7]));
       fence_proxy_async_smem();
@@ -355,10 +366,11 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
         __syncwarp();
         if (lane == 0) mbar_arrive_local(B(kBarEmpty + st));
       }
-      // U warps: this token's U row comes in before MMA1 completes (it landed with the stage)
+      // U warps: this token's U row comes in before MMA1 completes (it landed with
+      // the stage); the 128-column shape loads it after, within its register budget
       const int t = k - 64;  // token of this tensor-memory lane in rows 64.. of D1
       float uf[32];
-      if (q >= 2) {
+      auto load_u = [&]() {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const uint4 u = *reinterpret_cast<const uint4*>(stg + C::kSU + hc * 4096 + utile_off(t, 8 * c));
@@ -370,10 +382,12 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
             uf[8 * c + 2 * e + 1] = uv.y;
           }
         }
-      }
+      };
+      if (q >= 2 && kVT < 128) load_u();
       wait(B(kBarMma1), par);
       tc_fence_after();
       if (q >= 2) {
+        if (kVT == 128) load_u();
         // U_new for token t: U - (W S^T)[t, :] (rows 64.. of D1)
         float x[32];
         tc_ld32(lane_addr + C::kVTile * par, x);
@@ -385,7 +399,7 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
             const int j = 8 * c + 2 * e;
             un[e] = pack_f16(uf[j] - x[j], uf[j + 1] - x[j + 1]);
           }
-          *reinterpret_cast<uint4*>(smem + C::kSUn + C::boff(t, 4 * hc + c)) =
+          *reinterpret_cast<uint4*>(smem + C::kSUn + C::boff(t, 4 * hc + c, 64)) =
               make_uint4(un[0], un[1], un[2], un[3]);
         }
         fence_proxy_async_smem();
@@ -424,7 +438,7 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
         }
         tc_fence_before();
       }
-      if (++st == kStages) { st = 0; phf ^= 1u; }
+      if (++st == C::kStg) { st = 0; phf ^= 1u; }
     }
     // ---- final state ----
     if (p.final_state) {
@@ -513,6 +527,7 @@ void launch_state_kernel(const StateParams& p, cudaStream_t stream, int max_ctas
   else launch_state_variant<64>(p, stream);
 }
 
+// 32-column CTAs (shortest chunk period) if all fit under max_ctas, else 64-column ones.
 int state_tiles(int64_t units, int max_ctas) { return units * 4 <= max_ctas ? 4 : 2; }
 
 cudaError_t prepare_state_kernel() {
