@@ -120,8 +120,13 @@ typedef struct kda_fwd_args {
  * Device scratch (bytes) that kda_fwd needs for these arguments: per-chunk
  * intermediates of the WY form (W, U, gated queries, end-decayed keys, the
  * intra-chunk read-out matrix and the chunk decay) plus the chunk index of
- * packed sequences.  Depends only on sizes and on whether cu_seqlens is
- * given.  Returns 0 for argument sets that kda_fwd would reject.
+ * packed sequences.  For a dense call with few sequence-heads (N*H*8 at most
+ * the current device's SM count) and at least 32 chunks per sequence, kda_fwd
+ * splits the pass into token ranges whose intra-chunk and state stages
+ * overlap on two streams; the fp32 state carried from range to range adds
+ * N*H*64 KiB.  Depends on sizes, on whether cu_seqlens is given and on the
+ * current device; size the workspace on the device that runs the call.
+ * Returns 0 for argument sets that kda_fwd would reject.
  */
 size_t kda_fwd_workspace_bytes(const kda_fwd_args *args);
 
@@ -159,8 +164,10 @@ int kda_fwd_profiled(const kda_fwd_args *args, void *workspace, size_t workspace
  */
 int kda_fwd_recurrent(const kda_fwd_args *args, void *stream);
 
-/* Number of kernel launches kda_fwd makes for these arguments (0 if none or
- * if the arguments are invalid). */
+/* Number of kernel launches kda_fwd makes for these arguments on the current
+ * device (0 if none or if the arguments are invalid): 2 or 3 for one pass,
+ * 2 per token range when the pass is split into token ranges (see
+ * kda_fwd_workspace_bytes). */
 int kda_fwd_launches(const kda_fwd_args *args);
 
 /*

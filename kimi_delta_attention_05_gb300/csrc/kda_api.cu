@@ -379,6 +379,11 @@ extern "C" int kda_fwd_launches(const kda_fwd_args* a) {
   int64_t slots = 0;
   size_t header = 0;
   if (validate(a, &slots, &header) != KDA_OK || a->N == 0 || a->H == 0) return 0;
+  const int ranges = pipeline_ranges(a, device_sms());
+  if (ranges > 1) {  // one chunk and one state launch per token range
+    const int64_t span = ceil_div(ceil_div(a->T, kChunk), ranges) * kChunk;
+    return (int)(2 * ceil_div(a->T, span));
+  }
   return 1 + (slots > 0 ? 1 : 0) + (a->cu_seqlens ? 1 : 0);
 }
 
