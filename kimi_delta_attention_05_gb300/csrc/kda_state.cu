@@ -13,8 +13,8 @@
 //   O     = scale (Q_gamma S^T + P U_new)  (inter + intra read-out, fused as in
 //                                          the chunk_o stage of the fla code map)
 //   S     = S Diag(gamma_C) + U_new^T K_hat   (chunk_delta_h state update)
-// as three tensor-core products, each issued by one thread (widths for a
-// tile of kVT value columns):
+// as three tensor-core products, each issued by one elected lane of the
+// tensor-core warp (widths for a tile of kVT value columns):
 //   MMA1: D1 [128 x kVT] = [Q_gamma; W] (128 x 128) . S^T        (rows 64.. = W S^T)
 //   MMA2: D3 [128 x kVT] = K_hat^T (128 x 64)       . U_new       (state delta, row = key)
 //   MMA3: D1[0..63]     += [P; *]   (128 x 64)       . U_new       (output rows)
@@ -123,15 +123,20 @@ __device__ __forceinline__ uint32_t idesc_f16(int m, int n, bool a_mn_major, boo
   return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
          ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
+// Issued by a whole converged warp: elect.sync picks the one lane that issues.
+// All lanes hold the same (warp-uniform) operands, so the descriptors stay in
+// uniform registers; a branch on one lane instead costs ~50 cycles per issue
+// (measured: 8 products 407 -> 192 cycles of issue), which the chain pays.
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                        uint32_t accumulate) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "{\n .reg .pred p, e;\n elect.sync _|e, 0xffffffff;\n setp.ne.u32 p, %4, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 __device__ __forceinline__ void tc_commit(uint32_t mbar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(mbar)
+  asm volatile("{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+               " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(mbar)
                : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
@@ -270,8 +275,8 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
       for (int64_t c = 0; c < issued; ++c)
         mbar_wait_bounded(B(kBarFull + (int)(c % C::kStg)), (uint32_t)((c / C::kStg) & 1));
   } else if (warp == C::kMmaWarp) {
-    // ---- tensor-core issuer: the whole warp keeps step with the named barriers,
-    //      lane 0 issues ----
+    // ---- tensor-core issuer: the whole warp keeps step with the named barriers
+    //      and runs the issue loops; one elected lane issues ----
     {
       const uint32_t id1 = idesc_f16(128, C::kVTile, false, true);
       const uint32_t id2 = idesc_f16(128, C::kVTile, true, true);
@@ -292,29 +297,23 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
         wait(B(kBarFull + st), phf);
         named_sync(kNbS, C::kNbSCount);  // S of this chunk published
         tc_fence_after();
-        if (lane == 0) {
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            tc_mma(d1, dA1 + so + (uint64_t)(((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
-                   dS + (uint64_t)((ks * kStepB) >> 4), id1, ks > 0);
-          tc_commit(B(kBarMma1));
-        }
-        __syncwarp();
+        for (int ks = 0; ks < 8; ++ks)
+          tc_mma(d1, dA1 + so + (uint64_t)(((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                 dS + (uint64_t)((ks * kStepB) >> 4), id1, ks > 0);
+        tc_commit(B(kBarMma1));
         named_sync(kNbUn, C::kNbUnCount);  // U_new of this chunk published
         tc_fence_after();
-        if (lane == 0) {
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            tc_mma(d3, dKh + so + (uint64_t)((ks * 2048) >> 4), dUn + (uint64_t)((ks * kStepB) >> 4),
-                   id2, ks > 0);
-          tc_commit(B(kBarMma2));  // the state update can start
+        for (int ks = 0; ks < 4; ++ks)
+          tc_mma(d3, dKh + so + (uint64_t)((ks * 2048) >> 4), dUn + (uint64_t)((ks * kStepB) >> 4),
+                 id2, ks > 0);
+        tc_commit(B(kBarMma2));  // the state update can start
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            tc_mma(d1, dP + so + (uint64_t)((ks * 32) >> 4), dUn + (uint64_t)((ks * kStepB) >> 4), id1, 1);
-          tc_commit(B(kBarMma3));
-          tc_commit(B(kBarEmpty + st));  // the stage's operands are no longer read by the tensor core
-        }
-        __syncwarp();
+        for (int ks = 0; ks < 4; ++ks)
+          tc_mma(d1, dP + so + (uint64_t)((ks * 32) >> 4), dUn + (uint64_t)((ks * kStepB) >> 4), id1, 1);
+        tc_commit(B(kBarMma3));
+        tc_commit(B(kBarEmpty + st));  // the stage's operands are no longer read by the tensor core
         if (++st == C::kStg) { st = 0; phf ^= 1u; }
       }
       named_sync(kNbS, C::kNbSCount);  // the state published after the last chunk (no product uses it)
