@@ -199,6 +199,16 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
       cp_async16(sbase + dst + row * 256 + ((ch ^ (row & 7)) << 4), sp, ok ? 16 : 0);
     }
   };
+  // the same by the threads [first, first + count) only
+  auto load_tile_part = [&](const uint16_t* src, int dst, const Item& it, int first, int count) {
+#pragma unroll 4
+    for (int idx = tid - first; idx < 1024; idx += count) {
+      const int row = idx >> 4, ch = idx & 15;
+      const bool ok = row < it.L;
+      const uint16_t* sp = ok ? src + ((it.t0 + row) * H + it.h) * kHeadDim + ch * 8 : src;
+      cp_async16(sbase + dst + row * 256 + ((ch ^ (row & 7)) << 4), sp, ok ? 16 : 0);
+    }
+  };
   // beta input (logit, or beta itself) of token tid; 0 past the chunk end
   auto load_beta = [&](const Item& it) {
     return tid < it.L ? bf16_to_f(p.beta[(it.t0 + tid) * H + it.h]) : 0.f;
@@ -529,10 +539,12 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
   }
   __syncthreads();
   // q, k, K yr tiles are free: next item's q, k, g (g into this item's K yr tile)
-  if (next < num_items) {
-    load_tile(p.q, kCsQ, nxt);
-    load_tile(p.k, kCsK, nxt);
-    if (!p.g32) load_tile(p.g, yt, nxt);
+  if (next < num_items) {  // by warps 4-7, idle in the substitution below
+    if (warp >= 4) {
+      load_tile_part(p.q, kCsQ, nxt, 128, 128);
+      load_tile_part(p.k, kCsK, nxt, 128, 128);
+      if (!p.g32) load_tile_part(p.g, yt, nxt, 128, 128);
+    }
     if (tid < kChunk) blogit = load_beta(nxt);
   }
   cp_async_commit();

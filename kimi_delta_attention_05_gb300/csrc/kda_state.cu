@@ -295,6 +295,7 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
         const uint64_t so = (uint64_t)((st * C::kStageBytes) >> 4);
         const uint32_t d1 = tmem + C::kVTile * par;
         wait(B(kBarFull + st), phf);
+        __syncwarp();  // bar.sync is warp-aligned: reconverge after the per-lane wait
         named_sync(kNbS, C::kNbSCount);  // S of this chunk published
         tc_fence_after();
 #pragma unroll
@@ -383,7 +384,10 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
         }
       };
       if (q >= 2 && kVT < 128) load_u();
-      wait(B(kBarMma1), par);
+      // only the U_new warps read MMA1's result now; the output rows wait for
+      // MMA3 below (every suspending wait adds wake-up latency: 115 -> 110 us
+      // on T=8192 H=32 without this one in the output warps)
+      if (q >= 2) wait(B(kBarMma1), par);
       tc_fence_after();
       if (q >= 2) {
         if (kVT == 128) load_u();
