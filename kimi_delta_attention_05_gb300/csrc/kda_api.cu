@@ -227,6 +227,7 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
   const int sb16 = a->state_dtype == KDA_DTYPE_BF16 ? 1 : 0;
   const int ib16 = init_bf16 >= 0 ? init_bf16 : sb16, fb16 = final_bf16 >= 0 ? final_bf16 : sb16;
 
+  bool maps_ok = true;  // the chunk stage's tensor maps could be made
   auto mark = [&](int i) {
     if (events && events[i]) cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), stream);
   };
@@ -260,7 +261,8 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
     cp.NT = nt;
     cp.ld = a->T;
     cp.ws = ws_r;
-    launch_chunk_kernel(cp, nslots, s, busy_sms);
+    cp.status = status_device_ptr();
+    if (!launch_chunk_kernel(cp, nslots, s, busy_sms)) maps_ok = false;
   };
   auto launch_state = [&](int64_t t0, int64_t span, unsigned char* ws_r, const void* init,
                           void* fin, int ib, int fb, cudaStream_t s) {
@@ -324,7 +326,7 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
     mark(2);
     if (!ok) return KDA_ERR_LAUNCH;
   }
-  if (cudaGetLastError() != cudaSuccess) return KDA_ERR_LAUNCH;
+  if (!maps_ok || cudaGetLastError() != cudaSuccess) return KDA_ERR_LAUNCH;
   return KDA_OK;
 }
 

@@ -31,10 +31,21 @@
 // Precision: the A / P operands are bf16 (they need its exponent range); the
 // diagonal inverses are fp32; everything else is fp16 (11-bit significand)
 // with fp32 accumulation.
+#include <cuda.h>  // CUtensorMap (the encoder is reached through the runtime's entry-point query)
+
+#include <cstring>
+#include <mutex>
+
 #include "kda_common.cuh"
 #include "kda_kernels.cuh"
 
 namespace kda {
+
+// Tensor maps of the bf16 inputs [rows, H, 128]: 64 x 64 boxes (64 rows of one
+// head, 64 channels) with the 128-byte swizzle, rows past the view zero-filled.
+struct ChunkMaps {
+  CUtensorMap q, k, v, g;
+};
 
 // exp(-10): floor of the per-token decay inside the A / P operands.
 constexpr float kDiagDecayFloor = 4.5399929762484854e-05f;
@@ -62,7 +73,11 @@ constexpr int kCsBeta = 93184;   // fp32 [64]
 constexpr int kCsRq = 93440;     // fp32 [64]: 1 / |q| (or 1)
 constexpr int kCsRk = 93696;     // fp32 [64]: 1 / |k| (or 1)
 constexpr int kCsVt = 93952;     // tile128 [64 t][128 v] fp16: beta V, then U
-constexpr int kChunkSmem = kCsVt + 16384;
+constexpr int kCsBar = kCsVt + 16384;  // two mbarriers: q/k/g tiles, v tile
+constexpr int kChunkSmem = kCsBar + 16;
+static_assert(kCsQ % 1024 == 0 && kCsK % 1024 == 0 && kCsKy % 1024 == 0 && kCsG % 1024 == 0 &&
+                  kCsV % 1024 == 0,
+              "tensor-copy destinations with the 128-byte swizzle need 1024-byte alignment");
 
 __device__ __forceinline__ float rcp_approx(float x) {
   float y;
@@ -146,8 +161,9 @@ __device__ __forceinline__ f32x2 gate_decay2(f32x2 z, float amul_log2e, float lb
 }
 
 template <int kGate, bool kL2>
-__global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_t num_items) {
-  extern __shared__ __align__(128) unsigned char smem[];
+__global__ void __launch_bounds__(256, 2)
+    kda_chunk_kernel(ChunkParams p, int64_t num_items, const __grid_constant__ ChunkMaps maps) {
+  extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t H = p.H;
   const uint32_t sbase = smem_u32(smem);
@@ -155,6 +171,7 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
   // The next item's q, k, g are copied in as soon as the A / P stage has finished
   // with the q, k and K yr tiles, and its v once the substitution is done with
   // the A / inverse tiles, so the copies overlap the rest of the current item.
+  // Each tile is two tensor copies issued by one thread onto an mbarrier.
   if (p.cu) num_items = p.chunk_off[p.N] * H;  // varlen: only the slots in use
   struct Item {
     int64_t slot, t0;
@@ -189,25 +206,40 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
     r.L = (int)min((int64_t)kChunk, seqlen - i * kChunk);
     return r;
   };
-  // stage one [64 x 128] bf16 input tile into a swizzled tile128 (rows >= L zero-filled)
-  auto load_tile = [&](const uint16_t* src, int dst, const Item& it) {
-#pragma unroll 4
-    for (int idx = tid; idx < 1024; idx += 256) {
-      const int row = idx >> 4, ch = idx & 15;
-      const bool ok = row < it.L;
-      const uint16_t* sp = ok ? src + ((it.t0 + row) * H + it.h) * kHeadDim + ch * 8 : src;
-      cp_async16(sbase + dst + row * 256 + ((ch ^ (row & 7)) << 4), sp, ok ? 16 : 0);
+  const uint32_t bar_qkg = sbase + kCsBar, bar_v = sbase + kCsBar + 8;
+  // one thread: the q, k (and bf16 g) tiles of an item, two 64-column boxes each
+  auto copy_qkg = [&](const Item& it, int gdst) {
+    fence_proxy_async_smem();  // the tiles were last read by the generic proxy
+    mbar_expect_tx(bar_qkg, (p.g32 ? 2u : 3u) * 16384u);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      tma_load_3d(sbase + kCsQ + hh * 8192, &maps.q, 64 * hh, it.h, (int)it.t0, bar_qkg);
+      tma_load_3d(sbase + kCsK + hh * 8192, &maps.k, 64 * hh, it.h, (int)it.t0, bar_qkg);
+      if (!p.g32) tma_load_3d(sbase + gdst + hh * 8192, &maps.g, 64 * hh, it.h, (int)it.t0, bar_qkg);
     }
   };
-  // the same by the threads [first, first + count) only
-  auto load_tile_part = [&](const uint16_t* src, int dst, const Item& it, int first, int count) {
-#pragma unroll 4
-    for (int idx = tid - first; idx < 1024; idx += count) {
-      const int row = idx >> 4, ch = idx & 15;
-      const bool ok = row < it.L;
-      const uint16_t* sp = ok ? src + ((it.t0 + row) * H + it.h) * kHeadDim + ch * 8 : src;
-      cp_async16(sbase + dst + row * 256 + ((ch ^ (row & 7)) << 4), sp, ok ? 16 : 0);
+  auto copy_v = [&](const Item& it) {
+    fence_proxy_async_smem();
+    mbar_expect_tx(bar_v, 16384u);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+      tma_load_3d(sbase + kCsV + hh * 8192, &maps.v, 64 * hh, it.h, (int)it.t0, bar_v);
+  };
+  // every thread: bounded wait for a tile phase; a wait that gives up sets the
+  // status word, and the item goes on with whatever the tiles hold
+  bool gave_up = false;
+  auto wait_tiles = [&](uint32_t bar, uint32_t parity) {
+    if (!gave_up && !mbar_wait_bounded(bar, parity)) {
+      gave_up = true;
+      atomicExch(p.status, 13);
     }
+  };
+  // rows L..63 of a tile copied past a short chunk's end (the next sequence's
+  // rows, or zeros past the view) are cleared: the stages below expect zeros
+  auto zero_tail = [&](int tile, int L) {
+    for (int idx = tid; idx < (kChunk - L) * 16; idx += 256)
+      *reinterpret_cast<uint4*>(smem + tile + swz128(L + (idx >> 4), 8 * (idx & 15))) =
+          make_uint4(0u, 0u, 0u, 0u);
   };
   // beta input (logit, or beta itself) of token tid; 0 past the chunk end
   auto load_beta = [&](const Item& it) {
@@ -216,17 +248,23 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
   int64_t item = blockIdx.x;
   if (item >= num_items) return;
   Item cur = locate(item);
+  if (tid == 0) {
+    mbar_init(bar_qkg, 1);
+    mbar_init(bar_v, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
   // ---- S0 (first item only; later items were prefetched): q, k, g | v ----
-  load_tile(p.q, kCsQ, cur);
-  load_tile(p.k, kCsK, cur);
-  if (!p.g32) load_tile(p.g, kCsG, cur);  // fp32 g is read in the gate stage itself
-  cp_async_commit();
-  load_tile(p.v, kCsV, cur);
-  cp_async_commit();
+  // (fp32 g is read in the gate stage itself)
+  if (tid == 0) {
+    copy_qkg(cur, kCsG);
+    copy_v(cur);
+  }
   float blogit = tid < kChunk ? load_beta(cur) : 0.f;
   float* sBeta = reinterpret_cast<float*>(smem + kCsBeta);
 
-  for (int it = 0; item < num_items; item += gridDim.x, ++it) {
+  int it = 0;
+  for (; item < num_items; item += gridDim.x, ++it) {
   const int L = cur.L;
   const int h = cur.h;
   unsigned char* ws = p.ws + (cur.slot * H + h) * (int64_t)kSlotBytes;
@@ -237,7 +275,12 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
   if (next < num_items) nxt = locate(next);
   if (tid < kChunk)
     sBeta[tid] = tid >= L ? 0.f : (p.beta_prob ? blogit : rcp_approx(1.0f + ex2(-blogit * kLog2e)));
-  cp_async_wait<1>();  // q, k, g of this item (v may still be in flight)
+  wait_tiles(bar_qkg, (uint32_t)(it & 1));  // q, k, g of this item (v may still be in flight)
+  if (L < kChunk) {
+    zero_tail(kCsQ, L);
+    zero_tail(kCsK, L);
+    if (!p.g32) zero_tail(gt, L);
+  }
   __syncthreads();
 
   // ---- S1: per-token inverse norms of q and k (two threads per row, 64 channels each) ----
@@ -251,7 +294,7 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
       const unsigned char* tile = smem + (row < 64 ? kCsQ : kCsK);
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const uint4 v = *reinterpret_cast<const uint4*>(tile + t * 256 + (((8 * half + c) ^ (t & 7)) << 4));
+        const uint4 v = *reinterpret_cast<const uint4*>(tile + half * 8192 + t * 128 + ((c ^ (t & 7)) << 4));
         const float2 a = unpack_bf16(v.x), b = unpack_bf16(v.y), e = unpack_bf16(v.z), f = unpack_bf16(v.w);
         ss += a.x * a.x + a.y * a.y + b.x * b.x + b.y * b.y + e.x * e.x + e.y * e.y + f.x * f.x + f.y * f.y;
       }
@@ -402,7 +445,8 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
         }
       }
     }
-    cp_async_wait<0>();  // v of this item
+    wait_tiles(bar_v, (uint32_t)(it & 1));  // v of this item
+    if (L < kChunk) zero_tail(kCsV, L);
     __syncthreads();
     // forward over the half (overwrites raw q, k, g, v)
     {
@@ -539,15 +583,10 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
   }
   __syncthreads();
   // q, k, K yr tiles are free: next item's q, k, g (g into this item's K yr tile)
-  if (next < num_items) {  // by warps 4-7, idle in the substitution below
-    if (warp >= 4) {
-      load_tile_part(p.q, kCsQ, nxt, 128, 128);
-      load_tile_part(p.k, kCsK, nxt, 128, 128);
-      if (!p.g32) load_tile_part(p.g, yt, nxt, 128, 128);
-    }
+  if (next < num_items) {
+    if (tid == 128) copy_qkg(nxt, yt);  // warp 4: idle in the substitution below
     if (tid < kChunk) blogit = load_beta(nxt);
   }
-  cp_async_commit();
 
   // ---- S6: X_r = (I + A_rr)^-1 by forward substitution (warp r, lane = column) ----
   if (warp < 4 && lane < 16) {
@@ -632,16 +671,14 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
   }
   __syncthreads();
   // the A / inverse tiles in the raw-v tile are free: next item's v
-  if (next < num_items) load_tile(p.v, kCsV, nxt);
-  cp_async_commit();
+  if (next < num_items && tid == 0) copy_v(nxt);
 
   // ---- S8: W into rows 64..127 of the [q gamma; W] image, U into the four
   //      per-value-tile images; 16-byte chunks remapped from the tile128 layout ----
 #pragma unroll 4
   for (int idx = tid; idx < 2048; idx += 256) {
     const int m = idx >> 10, t = (idx >> 4) & 63, c = idx & 15;
-    const uint4 val = *reinterpret_cast<const uint4*>(smem + (m ? kCsVt : gt) + t * 256 +
-                                                       ((c ^ (t & 7)) << 4));
+    const uint4 val = *reinterpret_cast<const uint4*>(smem + (m ? kCsVt : gt) + swz128(t, 8 * c));
     uint32_t dst;
     if (m == 0)
       dst = kSlotA1 + (c >> 3) * 16384 + (64 + t) * 128 + (((c & 7) ^ (t & 7)) << 4);
@@ -651,16 +688,61 @@ __global__ void __launch_bounds__(256, 2) kda_chunk_kernel(ChunkParams p, int64_
   }
   cur = nxt;
   }
-  cp_async_wait<0>();
+  if (gave_up) {  // let this CTA's last copies land (bounded) before it exits
+    mbar_wait_bounded(bar_qkg, (uint32_t)((it - 1) & 1));
+    mbar_wait_bounded(bar_v, (uint32_t)((it - 1) & 1));
+  }
 }
 
 template <int kGate, bool kL2>
-static void launch_variant(const ChunkParams& p, unsigned grid, int64_t items, cudaStream_t stream) {
-  kda_chunk_kernel<kGate, kL2><<<grid, 256, kChunkSmem, stream>>>(p, items);
+static void launch_variant(const ChunkParams& p, unsigned grid, int64_t items, const ChunkMaps& maps,
+                           cudaStream_t stream) {
+  kda_chunk_kernel<kGate, kL2><<<grid, 256, kChunkSmem, stream>>>(p, items, maps);
 }
 
-void launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t stream,
+namespace {
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link against
+// the driver library)
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiled encoder() {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(f);
+  });
+  return fn;
+}
+// [rows, H, 128] bf16 at `base` (rows of H * 256 bytes), 64 x 64 boxes
+bool encode_input_map(CUtensorMap* m, const void* base, int64_t H, int64_t rows) {
+  const EncodeTiled fn = encoder();
+  if (!fn || rows < 1 || rows > INT32_MAX) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)H, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)(H * kHeadDim * 2)};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)kChunk};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estride,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
+bool launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t stream,
                          int busy_sms) {
+  // the rows the kernel may touch from the row pointers: every sequence's
+  // range (dense), or the packed tokens
+  const int64_t rows = p.cu ? p.T : (p.N - 1) * p.ld + p.T;
+  ChunkMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  if (!encode_input_map(&maps.q, p.q, p.H, rows) || !encode_input_map(&maps.k, p.k, p.H, rows) ||
+      !encode_input_map(&maps.v, p.v, p.H, rows) || (!p.g32 && !encode_input_map(&maps.g, p.g, p.H, rows)))
+    return false;
   // persistent grid: two CTAs per SM (the shared-memory and register budget) on
   // the SMs another kernel does not hold, or fewer items
   int dev = 0, sms = 0;
@@ -672,17 +754,18 @@ void launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t s
   const bool l2 = p.l2norm != 0;
   switch (p.gate_mode) {
     case kGateUnsafe:
-      if (l2) launch_variant<kGateUnsafe, true>(p, grid, items, stream);
-      else launch_variant<kGateUnsafe, false>(p, grid, items, stream);
+      if (l2) launch_variant<kGateUnsafe, true>(p, grid, items, maps, stream);
+      else launch_variant<kGateUnsafe, false>(p, grid, items, maps, stream);
       break;
     case kGateLogspace:
-      if (l2) launch_variant<kGateLogspace, true>(p, grid, items, stream);
-      else launch_variant<kGateLogspace, false>(p, grid, items, stream);
+      if (l2) launch_variant<kGateLogspace, true>(p, grid, items, maps, stream);
+      else launch_variant<kGateLogspace, false>(p, grid, items, maps, stream);
       break;
     default:
-      if (l2) launch_variant<kGateSafe, true>(p, grid, items, stream);
-      else launch_variant<kGateSafe, false>(p, grid, items, stream);
+      if (l2) launch_variant<kGateSafe, true>(p, grid, items, maps, stream);
+      else launch_variant<kGateSafe, false>(p, grid, items, maps, stream);
   }
+  return true;
 }
 
 cudaError_t prepare_chunk_kernel() {

@@ -56,8 +56,13 @@ __device__ __forceinline__ uint32_t utile_off(int t, int v) {
 }
 
 // ---- swizzled shared-memory addressing ----
+// A 64-row tile of 128 16-bit columns is two 8 KB halves (columns 0..63, 64..127),
+// each [64 rows][128 bytes] with the 16-byte chunks of a row permuted by row % 8:
+// the image a tensor copy with the 128-byte swizzle writes for a 64 x 64 box
+// (at a 1024-byte aligned address), and conflict-free for 8-row matrix loads.
 __device__ __forceinline__ uint32_t swz128(int row, int col) {  // byte offset
-  return (uint32_t)(row * 256 + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1));
+  return (uint32_t)((col >> 6) * 8192 + row * 128 + (((((col >> 3) & 7) ^ (row & 7))) << 4) +
+                    ((col & 7) << 1));
 }
 __device__ __forceinline__ uint32_t swz64(int row, int col) {
   return (uint32_t)(row * 128 + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1));
@@ -249,6 +254,18 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(mbar)
+      : "memory");
+}
+
+// Tensor copy of one box of a 3-D tensor map (coordinates innermost first)
+// into shared memory, completing its bytes on the mbarrier.  `map` is the
+// generic address of a CUtensorMap kernel parameter (__grid_constant__).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, int x, int y, int z,
+                                            uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(mbar)
       : "memory");
 }
 

@@ -28,6 +28,7 @@ struct ChunkParams {
   int64_t NT;                             // chunks per row (dense)
   int64_t ld;                             // dense: rows from one sequence's start to the next (>= T)
   unsigned char* ws;                      // first workspace slot
+  int* status;                            // device status word (bounded waits that give up)
 };
 
 // Recurrent stage (one CTA per (sequence, head, 64-wide value tile)).
@@ -88,8 +89,9 @@ void launch_chunk_offsets(const int64_t* cu, int64_t N, int64_t T, int64_t* chun
                           cudaStream_t s);
 // Device address of the library's sticky status word on the current device.
 int* status_device_ptr();
-// busy_sms: SMs held by a kernel running alongside (the persistent grid covers the rest)
-void launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t s, int busy_sms = 0);
+// busy_sms: SMs held by a kernel running alongside (the persistent grid covers the rest).
+// false if the inputs' tensor maps cannot be made (nothing launched).
+bool launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t s, int busy_sms = 0);
 // max_ctas: at most this many CTAs at once (0: the SM count) picks the
 // 32-column shape (four CTAs per head) if they fit, else the 64-column one
 void launch_state_kernel(const StateParams& p, cudaStream_t s, int max_ctas = 0);
