@@ -591,13 +591,19 @@ __global__ void __launch_bounds__(256, 2)
   // ---- S6: X_r = (I + A_rr)^-1 by forward substitution (warp r, lane = column) ----
   if (warp < 4 && lane < 16) {
     const int j = lane;
-    const float* Ad = sAd + warp * 256;
+    const float4* Ad4 = reinterpret_cast<const float4*>(sAd + warp * 256);  // rows of 16 floats
     float x[kSub];
 #pragma unroll
     for (int ii = 0; ii < kSub; ++ii) {
       float acc = 0.f;
 #pragma unroll
-      for (int s = 0; s < ii; ++s) acc += Ad[ii * 16 + s] * x[s];
+      for (int s4 = 0; 4 * s4 < ii; ++s4) {  // row ii, four entries per 16-byte load
+        const float4 a = Ad4[ii * 4 + s4];
+        const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (4 * s4 + c < ii) acc += av[c] * x[4 * s4 + c];
+      }
       x[ii] = (ii == j) ? 1.f : (ii < j ? 0.f : -acc);
     }
 #pragma unroll
@@ -669,25 +675,34 @@ __global__ void __launch_bounds__(256, 2)
       __syncwarp();
     }
   }
+  fence_proxy_async_smem();  // W (rows of gt) is read next by bulk copies
   __syncthreads();
   // the A / inverse tiles in the raw-v tile are free: next item's v
   if (next < num_items && tid == 0) copy_v(nxt);
+  // W: each 64-column half of the tile is byte for byte the half of rows 64..127
+  // of the [q gamma; W] image (same 128-byte rows, same row % 8 chunk order)
+  if (tid == 32) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+      asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], 8192;\n" ::"l"(ws + kSlotA1 + hh * 16384 + 64 * 128),
+                   "r"(sbase + gt + hh * 8192) : "memory");
+    asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+  }
 
   // ---- S8: W into rows 64..127 of the [q gamma; W] image, U into the four
   //      per-value-tile images; 16-byte chunks remapped from the tile128 layout ----
 #pragma unroll 4
-  for (int idx = tid; idx < 2048; idx += 256) {
-    const int m = idx >> 10, t = (idx >> 4) & 63, c = idx & 15;
-    const uint4 val = *reinterpret_cast<const uint4*>(smem + (m ? kCsVt : gt) + swz128(t, 8 * c));
-    uint32_t dst;
-    if (m == 0)
-      dst = kSlotA1 + (c >> 3) * 16384 + (64 + t) * 128 + (((c & 7) ^ (t & 7)) << 4);
-    else
-      dst = kSlotU + (c >> 2) * 4096 + utile_off(t, (c & 3) * 8);
-    *reinterpret_cast<uint4*>(ws + dst) = val;
+  for (int idx = tid; idx < 1024; idx += 256) {
+    const int t = (idx >> 4) & 63, c = idx & 15;
+    const uint4 val = *reinterpret_cast<const uint4*>(smem + kCsVt + swz128(t, 8 * c));
+    *reinterpret_cast<uint4*>(ws + kSlotU + (c >> 2) * 4096 + utile_off(t, (c & 3) * 8)) = val;
   }
+  if (tid == 32)  // the W copies have read gt before the next item writes it
+    asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
   cur = nxt;
   }
+  if (tid == 32)  // the W stores complete before the CTA exits
+    asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
   if (gave_up) {  // let this CTA's last copies land (bounded) before it exits
     mbar_wait_bounded(bar_qkg, (uint32_t)((it - 1) & 1));
     mbar_wait_bounded(bar_v, (uint32_t)((it - 1) & 1));
