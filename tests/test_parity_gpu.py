@@ -44,6 +44,26 @@ def test_varlen_edge_lengths():
     _full_check(inp, "varlen")
 
 
+def test_short_chunk_isolated_from_next_sequence():
+    """A chunk cut short by its sequence's end uses no value of the rows after
+    it, although its tiles are copied as whole 64-row boxes: the next
+    sequence's keys are 1e30 (they overflow fp16 operands), yet the first
+    sequence's outputs and final state match the oracle."""
+    inp = make_inputs(WORKLOADS["packed_varlen"], lengths=[5, 64], H=2, seed=21)
+    inp["qk_l2norm"] = False  # raw keys: small for the first sequence, huge after it
+    inp["q"] = (inp["q"].float() * 0.05).to(torch.bfloat16)
+    k = inp["k"].float() * 0.05
+    k[:, 5:] = 1e30
+    inp["k"] = k.to(torch.bfloat16)
+    o, f = tl.run_gpu(inp)
+    first = dict(inp, q=inp["q"][:, :5], k=inp["k"][:, :5], v=inp["v"][:, :5], g=inp["g"][:, :5],
+                 beta=inp["beta"][:, :5], cu_seqlens=torch.tensor([0, 5], dtype=torch.int64), N=1,
+                 initial_state=inp["initial_state"][:1])
+    ro, rf = tl.run_oracle(first)
+    tl.check_out(o[:, :5], ro, "first sequence")
+    tl.check_state(f[:1], rf, "first sequence")
+
+
 def test_extremes_reduced():
     inp = make_inputs(WORKLOADS["extremes"], B=2, T=333, H=2, seed=3)
     _full_check(inp, "extremes")
