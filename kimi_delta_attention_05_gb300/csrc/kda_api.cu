@@ -127,7 +127,7 @@ int validate(const kda_fwd_args* a, int64_t* num_slots, size_t* header_bytes) {
 using namespace kda;
 
 #ifndef KDA_PIPE_RANGES
-#define KDA_PIPE_RANGES 4
+#define KDA_PIPE_RANGES 6
 #endif
 static_assert(KDA_PIPE_RANGES >= 1 && KDA_PIPE_RANGES <= 8, "pipeline ranges");
 
@@ -155,12 +155,17 @@ int pipe_state_budget(int64_t units, int sms) { return units * 4 * 2 <= sms ? sm
 // Token ranges a dense pass is cut into (every range of every sequence, whole
 // chunks), so that the state stage of range r, on a high-priority stream,
 // overlaps the intra-chunk stage of range r + 1 on the SMs it leaves free:
-// for few sequence-heads (above) and long sequences; otherwise 1.
+// for few sequence-heads (above) and sequences of at least 256 chunks;
+// otherwise 1.  Measured, ms per call by ranges 1 / 3 / 4 / 6 / 8: B2 T32768 H8
+// 0.699 / 0.651 / 0.612 / 0.580 / 0.608, the same with H4 0.563 / 0.534 /
+// 0.517 / 0.513 / 0.528; with 128 chunks per sequence (T8192, H16 or H8) no
+// range count beats one pass (H8: 0.155 against 0.162 at 4 ranges).
+constexpr int64_t kPipeMinChunks = 256;
 int pipeline_ranges(const kda_fwd_args* a, int sms) {
   if (a->cu_seqlens || sms <= 0) return 1;
   const int64_t units = a->N * a->H;
   if (units == 0 || pipe_state_budget(units, sms) == 0) return 1;
-  if (ceil_div(a->T, kChunk) < 32) return 1;
+  if (ceil_div(a->T, kChunk) < kPipeMinChunks) return 1;
   return KDA_PIPE_RANGES;
 }
 

@@ -6,6 +6,8 @@ to piece in fp32, which must leave every bit of the result as kda_fwd gives
 it; packed inputs are split between sequences.  Both are also checked against
 the fp64 oracle with the usual tolerances (tests/kda_testlib.py).
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -175,15 +177,21 @@ def test_g_in_fp32_through_host_entry():
     tl.check_state(f_h, rf, "host fp32 g packed")
 
 
-@pytest.mark.parametrize("gate,B,T,H", [("unsafe", 1, 4096, 4), ("safe", 2, 3000, 2)])
+@pytest.mark.parametrize("gate,B,T,H", [("unsafe", 1, 16384, 4), ("safe", 2, 16500, 2)])
 def test_stage_pipeline_is_bit_exact(gate, B, T, H):
-    """Few sequence-heads and long sequences: kda_fwd overlaps the state stage
-    of one token range with the intra-chunk stage of the next on two streams,
-    carrying the state in fp32.  The host entry runs the same single-piece
-    problem without that overlap: the results are identical."""
+    """Few sequence-heads and sequences of at least 256 chunks: kda_fwd
+    overlaps the state stage of one token range with the intra-chunk stage of
+    the next on two streams, carrying the state in fp32.  The host entry runs
+    the same problem without that overlap (its token pieces carry the state
+    in fp32 at other chunk boundaries): the results are identical."""
     inp = make_inputs(WORKLOADS["dense_batch"], B=B, T=T, H=H, seed=71)
     inp.update(gate=gate)
-    assert B * T * H * 1026 < PIECE_BYTES  # one piece on the host path
+    d = tl.to_device(inp)
+    a = make_args(d["q"], d["k"], d["v"], d["g"], d["beta"], inp["scale"], torch.empty_like(d["v"]),
+                  d["A_log"], d["dt_bias"], inp["lower_bound"] if gate == "safe" else None,
+                  d["initial_state"], None, None, inp["qk_l2norm"], gate)
+    from kimi_delta_attention_05_gb300 import kda as K
+    assert K.load_library().kda_fwd_launches(ctypes.byref(a)) == 12  # 6 token ranges x 2 stages
     o_h, f_h = _run_host(inp)
     o_d, f_d = tl.run_gpu(inp)
     assert np.array_equal(o_h, o_d) and np.array_equal(f_h, f_d)
@@ -196,8 +204,8 @@ def test_stage_pipeline_two_streams_at_once():
     """Two pipelined calls issued on two streams without ordering between them
     (they share the library's state stream and events): each result equals the
     same call run alone."""
-    cases = [make_inputs(WORKLOADS["long_context"], T=4096, H=4, seed=72),
-             make_inputs(WORKLOADS["extremes"], B=1, T=6000, H=3, seed=73)]
+    cases = [make_inputs(WORKLOADS["long_context"], T=16384, H=4, seed=72),
+             make_inputs(WORKLOADS["extremes"], B=1, T=16500, H=3, seed=73)]
     alone = [tl.run_gpu(inp) for inp in cases]
     streams = [torch.cuda.Stream(), torch.cuda.Stream()]
     devs, outs, fins = [], [], []
