@@ -135,8 +135,15 @@ size_t kda_fwd_workspace_bytes(const kda_fwd_args *args);
  * stream).  `workspace` is caller-owned device memory of at least
  * kda_fwd_workspace_bytes(args) bytes, 256-byte aligned; its contents need no
  * initialisation and are garbage afterwards.  Calls that share a workspace
- * must be ordered on the device.  Returns KDA_OK or an error code; on error
- * nothing is launched and nothing is written.
+ * must be ordered on the device.  Returns KDA_OK or an error code; on an
+ * argument error nothing is launched and nothing is written; KDA_ERR_LAUNCH
+ * (a failed launch, event or tensor-map set-up) may follow launches already
+ * made by the same call.  The call only enqueues work, so it may be captured
+ * into a CUDA graph: the tensor maps of the inputs travel with the launch as
+ * parameters, and when the two stages overlap on the library's second stream
+ * that stream joins the capture through events recorded on `stream` (tested
+ * bit-identical to eager calls).  The first call on a device, which sets up
+ * kernel attributes and that stream, is best made outside a capture.
  */
 int kda_fwd(const kda_fwd_args *args, void *workspace, size_t workspace_bytes, void *stream);
 

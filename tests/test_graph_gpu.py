@@ -1,0 +1,64 @@
+"""CUDA graph capture of kda_fwd.
+
+A call captured into a CUDA graph replays to the same bits as the call run
+eagerly: for a one-pass shape, a packed (cu_seqlens) shape with its chunk-index
+scan, and a shape whose two stages overlap across token ranges, where the state
+stage runs on the library's second stream (joined into the capture through
+events).  The tensor maps of the intra-chunk stage are kernel parameters, so
+they are captured by value with the launch.
+"""
+import pytest
+import torch
+
+from kimi_delta_attention_05_gb300 import kda_fwd
+from kimi_delta_attention_05_gb300.workloads import WORKLOADS, make_inputs
+from tests import kda_testlib as tl
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    ("one pass", "long_context", dict(T=1000, H=4, seed=90)),
+    ("packed", "packed_varlen", dict(lengths=[70, 1, 300, 64], H=2, seed=91)),
+    ("overlapped token ranges", "long_context", dict(T=16384, H=4, seed=92)),
+]
+
+
+def _call(inp, d, out, fin):
+    lb = inp["lower_bound"] if inp["gate"] == "safe" else None
+    return kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], inp["scale"], out, d["A_log"],
+                   d["dt_bias"], lb, d["initial_state"], fin, d["cu_seqlens"],
+                   qk_l2norm=inp["qk_l2norm"], gate=inp["gate"])
+
+
+@pytest.mark.parametrize("tag,workload,kw", CASES, ids=[c[0] for c in CASES])
+def test_captured_call_replays_bit_identical(tag, workload, kw):
+    inp = make_inputs(WORKLOADS[workload], **kw)
+    inp["final_state"] = "f32"
+    d = tl.to_device(inp)
+    H = d["q"].shape[2]
+
+    def fresh():
+        return (torch.full_like(d["v"], float("nan")),
+                torch.full((inp["N"], H, 128, 128), float("nan"), device="cuda"))
+
+    out_e, fin_e = fresh()
+    _call(inp, d, out_e, fin_e)  # eager; also makes the library's per-device set-up
+    torch.cuda.synchronize()
+
+    out_g, fin_g = fresh()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        _call(inp, d, out_g, fin_g)  # warm-up on the capturing stream's kind of stream
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        _call(inp, d, out_g, fin_g)
+    for _ in range(3):
+        out_g.fill_(float("nan"))
+        fin_g.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out_g.view(torch.int16), out_e.view(torch.int16)), tag
+        assert torch.equal(fin_g, fin_e), tag
