@@ -51,6 +51,8 @@ struct ChunkMaps {
 constexpr float kDiagDecayFloor = 4.5399929762484854e-05f;
 
 // ---- shared-memory map (bytes) ----
+// A "tile128" is 64 rows x 128 16-bit columns in two 8 KB halves, addressed by
+// swz128 (the tensor-copy image of two 64 x 64 boxes with the 128-byte swizzle).
 // phase 1 (until the A / P products are done)
 constexpr int kCsQ = 0;          // tile128: raw q, then bf16 q_hat * xr
 constexpr int kCsK = 16384;      // tile128: raw k, then bf16 k_hat * xr
@@ -697,8 +699,8 @@ __global__ void __launch_bounds__(256, 2)
     asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
   }
 
-  // ---- S8: W into rows 64..127 of the [q gamma; W] image, U into the four
-  //      per-value-tile images; 16-byte chunks remapped from the tile128 layout ----
+  // ---- S8: U into the four per-value-tile images, 16-byte chunks remapped from
+  //      the tile128 layout (W went out above by bulk copies) ----
 #pragma unroll 4
   for (int idx = tid; idx < 1024; idx += 256) {
     const int t = (idx >> 4) & 63, c = idx & 15;
