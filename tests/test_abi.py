@@ -110,6 +110,19 @@ def test_workspace_varlen_size():
     assert need == 256 + (16 + 5) * 4 * 74240
 
 
+def test_launch_count():
+    """kda_fwd_launches: the chunk and state kernels (2), plus the chunk-index
+    scan with cu_seqlens (3), only the state kernel with no tokens (1), none for
+    argument sets kda_fwd rejects (0).  These sequences are far too short for
+    the token-range split, so the counts hold with or without a device."""
+    lib = K.load_library()
+    assert lib.kda_fwd_launches(ctypes.byref(_valid_args())) == 2
+    assert lib.kda_fwd_launches(ctypes.byref(_valid_args(B=1, T=1000, N=5, cu_seqlens=FAKE))) == 3
+    assert lib.kda_fwd_launches(ctypes.byref(_valid_args(T=0))) == 1
+    assert lib.kda_fwd_launches(ctypes.byref(_valid_args(K=64))) == 0
+    assert lib.kda_fwd_launches(ctypes.byref(_valid_args(flags=0))) == 0
+
+
 def test_error_strings():
     lib = K.load_library()
     for c in range(12):
