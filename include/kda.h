@@ -121,8 +121,8 @@ typedef struct kda_fwd_args {
  * intermediates of the WY form (W, U, gated queries, end-decayed keys, the
  * intra-chunk read-out matrix and the chunk decay) plus the chunk index of
  * packed sequences.  For a dense call with few sequence-heads (N*H*8 at most
- * the current device's SM count) and at least 32 chunks per sequence, kda_fwd
- * splits the pass into token ranges whose intra-chunk and state stages
+ * the current device's SM count) and at least 256 chunks per sequence,
+ * kda_fwd splits the pass into token ranges whose intra-chunk and state stages
  * overlap on two streams; the fp32 state carried from range to range adds
  * N*H*64 KiB.  Depends on sizes, on whether cu_seqlens is given and on the
  * current device; size the workspace on the device that runs the call.
@@ -142,8 +142,14 @@ size_t kda_fwd_workspace_bytes(const kda_fwd_args *args);
  * into a CUDA graph: the tensor maps of the inputs travel with the launch as
  * parameters, and when the two stages overlap on the library's second stream
  * that stream joins the capture through events recorded on `stream` (tested
- * bit-identical to eager calls).  The first call on a device, which sets up
- * kernel attributes and that stream, is best made outside a capture.
+ * bit-identical to eager calls).  The second stream belongs to `stream` alone:
+ * the library keeps one per caller stream (for up to 64 caller streams per
+ * device; calls from further streams run in one pass, with the same results),
+ * so a capture open on one caller stream takes in no other caller's work.
+ * The first call on a device, and the first overlapped call on a caller
+ * stream, which set up kernel attributes and that stream, are best made
+ * outside a capture.  The per-device and per-stream set-up is kept for the
+ * life of the process: do not use the library across cudaDeviceReset.
  */
 int kda_fwd(const kda_fwd_args *args, void *workspace, size_t workspace_bytes, void *stream);
 
@@ -193,7 +199,8 @@ int kda_fwd_launches(const kda_fwd_args *args);
  *    T * H <= 28,864 token-heads for dense inputs).
  *  - Set-up: the first call on a device looks up the buffer's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is kept for the life of the
+ *    process: do not use the library across cudaDeviceReset.
  *  - Sharing: every call on a device uses the same buffer, which keeps the
  *    previous call's contents.  Nothing in it needs to start at zero, but
  *    calls that can overlap on the GPU (different streams, no ordering) race
@@ -243,23 +250,36 @@ size_t kda_fwd_host_device_bytes(const kda_fwd_args *args);
 int kda_fwd_host(const kda_fwd_args *args, void *device_buffer, size_t device_bytes, void *stream);
 
 /*
- * Device-side status of the kernels on the current device: KDA_OK,
- * KDA_ERR_DEVICE_TIMEOUT if a CTA gave up waiting (bounded wait, about a
- * second of SM cycles) for its asynchronous operand copies and returned
- * without finishing its work, or KDA_ERR_BAD_SEQLENS if a call's cu_seqlens
- * values were inconsistent (the offending sequences were skipped).  Sticky
- * until read with clear != 0 (the last code set wins).  Reads device memory
- * synchronously; returns -1 if that read fails.
+ * Device-side status of the forward calls enqueued on `stream` (a cudaStream_t;
+ * NULL = legacy default stream), the kda_get_status(cudaStream_t) of the
+ * boundary: KDA_OK, KDA_ERR_DEVICE_TIMEOUT if a CTA of such a call gave up
+ * waiting (bounded wait, about a second of SM cycles) for its asynchronous
+ * operand copies and returned without finishing its work, or
+ * KDA_ERR_BAD_SEQLENS if a call's cu_seqlens values were inconsistent.
+ *
+ *  - One status word per (device, stream): every kernel of a call reports into
+ *    the word of the stream the call was enqueued on (also the stages that run
+ *    on the library's second stream), so calls on different streams never see,
+ *    overwrite or clear each other's codes.  The words come from a table of
+ *    1023 slots built into the library; a stream takes a slot on its first
+ *    call and keeps it, and the streams beyond the 1023rd distinct handle on a
+ *    device share one further slot.  Two host threads using the per-thread
+ *    default stream handle (cudaStreamPerThread) share a word.
+ *  - Sticky until read: the call synchronises `stream`, returns its word as it
+ *    stands after all work enqueued on it so far (the last code set wins) and
+ *    clears it.  Returns -1 if the read fails or `stream` is being captured
+ *    into a CUDA graph (a captured call reports into the word of the stream it
+ *    was captured on, whatever stream replays the graph).
  */
-int kda_get_status(int clear);
+int kda_get_status(void *stream);
 
 /*
  * Self-test of the failure path (no counterpart in the pages): launches one
  * block on `stream` that waits, with the same bounded mbarrier wait the state
  * kernel uses, on a barrier phase that nothing completes; after `cycles` SM
  * cycles (1 .. 2^31) it gives up, sets the device status word to
- * KDA_ERR_DEVICE_TIMEOUT exactly as a real timeout does, and returns.  The
- * context stays usable.  Returns KDA_OK, KDA_ERR_SHAPE for a cycle count out
+ * KDA_ERR_DEVICE_TIMEOUT in the status word of `stream` exactly as a real
+ * timeout does, and returns.  The context stays usable.  Returns KDA_OK, KDA_ERR_SHAPE for a cycle count out
  * of range, or KDA_ERR_LAUNCH.
  */
 int kda_selftest_wait_timeout(long long cycles, void *stream);

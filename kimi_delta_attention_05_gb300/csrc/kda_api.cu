@@ -2,8 +2,10 @@
 // Declared in include/kda.h.
 #include <algorithm>
 #include <atomic>
-#include <mutex>
 #include <cmath>
+#include <memory>
+#include <mutex>
+#include <unordered_map>
 
 #include "../../include/kda.h"
 #include "kda_common.cuh"
@@ -171,14 +173,25 @@ int pipeline_ranges(const kda_fwd_args* a, int sms) {
 
 size_t carry_bytes(const kda_fwd_args* a) { return (size_t)(a->N * a->H) * kHeadDim * kHeadDim * 4; }
 
-// Per-device stream (greatest priority) and events of the pipelined pass.
+// Second stream (greatest priority) and events of the pipelined pass, one set
+// per caller stream: the state stages of a call run on its caller's own
+// second stream, so calls from different caller streams never share one (a
+// capture open on one caller stream cannot take in another caller's work, and
+// unrelated callers do not queue behind each other).
 struct PipeCtx {
   std::mutex mu;
   bool ready = false;
   cudaStream_t state_stream = nullptr;
   cudaEvent_t start = nullptr, end = nullptr, chunked[KDA_PIPE_RANGES] = {};
 };
-PipeCtx g_pipe[kMaxDevices];
+// At most this many caller streams per device get a second stream (kept until
+// the process exits); calls from further streams run in one pass.
+constexpr size_t kMaxPipeStreams = 64;
+struct PipeTable {
+  std::mutex mu;
+  std::unordered_map<uintptr_t, std::unique_ptr<PipeCtx>> ctx;
+};
+PipeTable g_pipes[kMaxDevices];
 
 bool make_pipe_ctx(PipeCtx& c) {
   if (c.ready) return true;
@@ -192,6 +205,18 @@ bool make_pipe_ctx(PipeCtx& c) {
     if (cudaEventCreateWithFlags(&e, ef) != cudaSuccess) return false;
   c.ready = true;
   return true;
+}
+
+// The pipelined-pass context of caller stream `s` on device `dev`, made on
+// first use; nullptr once the table is full.
+PipeCtx* pipe_ctx(int dev, cudaStream_t s) {
+  PipeTable& t = g_pipes[dev];
+  std::lock_guard<std::mutex> lock(t.mu);
+  const uintptr_t key = s == cudaStreamLegacy ? (uintptr_t)0 : reinterpret_cast<uintptr_t>(s);
+  auto it = t.ctx.find(key);
+  if (it != t.ctx.end()) return it->second.get();
+  if (t.ctx.size() >= kMaxPipeStreams) return nullptr;
+  return t.ctx.emplace(key, std::make_unique<PipeCtx>()).first->second.get();
 }
 
 }  // namespace
@@ -212,7 +237,7 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
   int rc = validate(a, &slots, &header);
   if (rc != KDA_OK) return rc;
   if (a->N == 0 || a->H == 0) return KDA_OK;
-  const int ranges = allow_pipeline ? pipeline_ranges(a, device_sms()) : 1;
+  int ranges = allow_pipeline ? pipeline_ranges(a, device_sms()) : 1;
   const size_t slot_bytes = (size_t)slots * (size_t)a->H * (size_t)kSlotBytes;
   const size_t need = header + slot_bytes + (ranges > 1 ? carry_bytes(a) : 0);
   if (need > 0 && (!workspace || !aligned(workspace, 256) || workspace_bytes < need))
@@ -224,6 +249,11 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
       return KDA_ERR_LAUNCH;
     g_prepared[dev].store(1);
   }
+  // every kernel of this call reports into the status word of the caller's stream
+  int* status = status_slot(stream);
+  if (!status) return KDA_ERR_LAUNCH;
+  PipeCtx* pipe = ranges > 1 ? pipe_ctx(dev, stream) : nullptr;
+  if (!pipe) ranges = 1;  // (workspace sized for the pipelined pass is large enough for one pass)
 
   unsigned char* ws = reinterpret_cast<unsigned char*>(workspace);
   int64_t* chunk_off = a->cu_seqlens ? reinterpret_cast<int64_t*>(ws) : nullptr;
@@ -266,7 +296,7 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
     cp.NT = nt;
     cp.ld = a->T;
     cp.ws = ws_r;
-    cp.status = status_device_ptr();
+    cp.status = status;
     if (!launch_chunk_kernel(cp, nslots, s, busy_sms)) maps_ok = false;
   };
   auto launch_state = [&](int64_t t0, int64_t span, unsigned char* ws_r, const void* init,
@@ -287,13 +317,14 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
     sp.NT = ceil_div(span, kChunk);
     sp.ld = a->T;
     sp.ws = ws_r;
+    sp.status = status;
     launch_state_kernel(sp, s, ranges > 1 ? pipe_state_budget(a->N * a->H, device_sms()) : 0);
   };
 
   if (ranges == 1) {
     mark(0);
     if (a->cu_seqlens)
-      launch_chunk_offsets(a->cu_seqlens, a->N, a->T, chunk_off, status_device_ptr(), stream);
+      launch_chunk_offsets(a->cu_seqlens, a->N, a->T, chunk_off, status, stream);
     launch_chunks(0, a->T, slots_base, stream, 0);
     mark(1);
     launch_state(0, a->T, slots_base, a->initial_state, a->final_state, ib16, fb16, stream);
@@ -301,7 +332,7 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
   } else {
     // chunk stage of range r on the caller's stream, state stage on the
     // high-priority stream after it; the fp32 state passes from range to range
-    PipeCtx& c = g_pipe[dev];
+    PipeCtx& c = *pipe;
     std::lock_guard<std::mutex> lock(c.mu);
     if (!make_pipe_ctx(c)) return KDA_ERR_LAUNCH;
     const int64_t span = ceil_div(ceil_div(a->T, kChunk), ranges) * kChunk;
@@ -376,7 +407,8 @@ extern "C" int kda_fwd_recurrent(const kda_fwd_args* a, void* stream_ptr) {
   rp.N = a->N;
   rp.T = a->T;
   rp.H = a->H;
-  rp.status = a->cu_seqlens ? status_device_ptr() : nullptr;
+  rp.status = a->cu_seqlens ? status_slot(reinterpret_cast<cudaStream_t>(stream_ptr)) : nullptr;
+  if (a->cu_seqlens && !rp.status) return KDA_ERR_LAUNCH;
   launch_recurrent_kernel(rp, reinterpret_cast<cudaStream_t>(stream_ptr));
   if (cudaGetLastError() != cudaSuccess) return KDA_ERR_LAUNCH;
   return KDA_OK;

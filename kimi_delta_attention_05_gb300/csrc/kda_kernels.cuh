@@ -44,6 +44,7 @@ struct StateParams {
   int64_t N, T, H, NT;
   int64_t ld;                             // dense: rows from one sequence's start to the next (>= T)
   const unsigned char* ws;
+  int* status;                            // status word of the caller's stream (waits that give up)
 };
 
 // Token-by-token path (one CTA per (sequence, head, 32-row value slab)).
@@ -88,8 +89,9 @@ cudaError_t prepare_recurrent_kernel();
 // violation sets *status to 14 (KDA_ERR_BAD_SEQLENS).
 void launch_chunk_offsets(const int64_t* cu, int64_t N, int64_t T, int64_t* chunk_off, int* status,
                           cudaStream_t s);
-// Device address of the library's sticky status word on the current device.
-int* status_device_ptr();
+// Device address of the status word of stream `s` on the current device (a
+// slot of the library's table, assigned on the stream's first use), or nullptr.
+int* status_slot(cudaStream_t s);
 // busy_sms: SMs held by a kernel running alongside (the persistent grid covers the rest).
 // false if the inputs' tensor maps cannot be made (nothing launched).
 bool launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t s, int busy_sms = 0);

@@ -27,8 +27,6 @@
 // tensor-core hand-offs use named barriers, which every participating warp
 // passes exactly once per chunk (plus once for the initial state) whatever
 // happens, so they always complete.
-#include <atomic>
-
 #include "kda_common.cuh"
 #include "kda_kernels.cuh"
 
@@ -101,10 +99,6 @@ struct StateCfg {
   static_assert(kSmem <= 232448, "exceeds the opt-in shared memory of one CTA");
   static_assert(kStg <= kStages, "barrier slots");
 };
-
-// Sticky device status: set to KDA_ERR_DEVICE_TIMEOUT (13) by a CTA that gave
-// up waiting; read and cleared by kda_get_status.
-__device__ int g_kda_status = 0;
 
 // ---- tcgen05 helpers ----
 // Shared-memory matrix descriptor: given leading / stride byte offsets and
@@ -235,12 +229,12 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::kSTmem);
-  if (*s_abort && tid == 0) atomicExch(&g_kda_status, 13);
+  if (*s_abort && tid == 0) atomicExch(p.status, 13);
 
   auto wait = [&](uint32_t b, uint32_t parity) {
     if (*s_abort) return;
     if (!mbar_wait_bounded(b, parity)) {
-      atomicExch(&g_kda_status, 13);
+      atomicExch(p.status, 13);
       *s_abort = 1;
     }
   };
@@ -461,49 +455,6 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
   tc_fence_after();
   if (warp == C::kMmaWarp)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(C::kTmemCols));
-}
-
-// One block waits on an mbarrier phase that nothing completes, with the same
-// bounded wait and status word as the state kernel's waits, and returns.
-__global__ void kda_wait_selftest_kernel(long long limit) {
-  __shared__ __align__(8) uint64_t bar;
-  if (threadIdx.x == 0) {
-    mbar_init(smem_u32(&bar), 1);
-    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-  }
-  __syncthreads();
-  if (threadIdx.x == 0 && !mbar_wait_bounded(smem_u32(&bar), 0u, limit))
-    atomicExch(&g_kda_status, 13);
-}
-
-extern "C" int kda_selftest_wait_timeout(long long cycles, void* stream) {
-  if (cycles <= 0 || cycles > (1LL << 31)) return 3;  // KDA_ERR_SHAPE
-  kda_wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(cycles);
-  return cudaGetLastError() == cudaSuccess ? 0 : 11;  // KDA_OK / KDA_ERR_LAUNCH
-}
-
-int* status_device_ptr() {
-  static std::atomic<int*> cache[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  int* p = cache[dev].load();
-  if (!p) {
-    void* a = nullptr;
-    if (cudaGetSymbolAddress(&a, g_kda_status) != cudaSuccess) return nullptr;
-    p = static_cast<int*>(a);
-    cache[dev].store(p);
-  }
-  return p;
-}
-
-extern "C" int kda_get_status(int clear) {
-  int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_kda_status, sizeof(int)) != cudaSuccess) return -1;
-  if (clear && v != 0) {
-    const int z = 0;
-    if (cudaMemcpyToSymbol(g_kda_status, &z, sizeof(int)) != cudaSuccess) return -1;
-  }
-  return v;
 }
 
 template <int kVT>

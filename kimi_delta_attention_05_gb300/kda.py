@@ -78,7 +78,7 @@ def load_library(build_if_missing: bool = True):
         lib.kda_fwd_launches.restype = ctypes.c_int
         lib.kda_fwd_launches.argtypes = [ctypes.POINTER(kda_fwd_args)]
         lib.kda_get_status.restype = ctypes.c_int
-        lib.kda_get_status.argtypes = [ctypes.c_int]
+        lib.kda_get_status.argtypes = [P]
         lib.kda_selftest_wait_timeout.restype = ctypes.c_int
         lib.kda_selftest_wait_timeout.argtypes = [ctypes.c_longlong, P]
         lib.kda_fwd_host.restype = ctypes.c_int
@@ -128,6 +128,15 @@ def make_args(q, k, v, g, beta, scale, out, A_log=None, dt_bias=None, lower_boun
     a.B, a.T, a.H, a.N, a.K, a.V = B, T, H, N, K, V
     a.flags = flags
     return a
+
+
+def get_status(stream=None) -> int:
+    """Read and clear the device status word of ``stream`` (a torch stream;
+    default: the current stream): 0, KDA_ERR_DEVICE_TIMEOUT (13) or
+    KDA_ERR_BAD_SEQLENS (14) for the calls enqueued on it; -1 if it cannot be
+    read.  Synchronises the stream."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(load_library().kda_get_status(ctypes.c_void_p(s.cuda_stream)))
 
 
 def workspace_bytes(args: kda_fwd_args) -> int:

@@ -27,3 +27,21 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Print the parity margins the full-size GPU tests recorded."""
+    try:
+        from tests import kda_testlib as tl
+    except Exception:
+        return
+    if not tl.MARGINS:
+        return
+    tr = terminalreporter
+    tr.section("KDA parity margins (full-size workloads, every unit, against the fp64 oracle)")
+    tr.write_line(f"bounds: out rel-RMS <= {tl.OUT_RMS:g}, out max-abs <= {tl.OUT_MAXABS:g} max|ref|, "
+                  f"final-state rel-RMS <= {tl.STATE_RMS:g}")
+    for tag, r, m, w, st in tl.MARGINS:
+        sts = "-" if st is None else f"{st:.3e}"
+        tr.write_line(f"{tag:<28} out rel-RMS {r:.3e}  max-abs/max|ref| {m:.3e}  "
+                      f"worst unit rel-RMS {w:.3e}  state rel-RMS {sts}")

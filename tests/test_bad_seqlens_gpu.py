@@ -38,8 +38,8 @@ def _call(cu_vals, T_declared, recurrent=False, H=2, seed=80):
     a = K.make_args(d["q"], d["k"], d["v"], d["g"], d["beta"], inp["scale"], out, d["A_log"],
                     d["dt_bias"], inp["lower_bound"], init, final, cu, qk_l2norm=True, gate="safe")
     a.T = T_declared
-    assert lib.kda_get_status(1) >= 0  # clear
     stream = torch.cuda.current_stream()
+    assert K.get_status(stream) >= 0  # clear
     if recurrent:
         rc = lib.kda_fwd_recurrent(ctypes.byref(a), ctypes.c_void_p(stream.cuda_stream))
     else:
@@ -49,7 +49,7 @@ def _call(cu_vals, T_declared, recurrent=False, H=2, seed=80):
                          ctypes.c_void_p(stream.cuda_stream))
     assert rc == 0
     torch.cuda.synchronize()
-    status = lib.kda_get_status(1)
+    status = K.get_status(stream)
     return out, final, init, status
 
 
@@ -78,7 +78,7 @@ def test_valid_call_after_a_bad_one_is_clean():
     _call([0, 300, 100, 400], 400)
     inp = make_inputs(WORKLOADS["packed_varlen"], lengths=[130, 0, 70], H=2, seed=81)
     o, f = tl.run_gpu(inp)
-    assert K.load_library().kda_get_status(1) == 0
+    assert K.get_status() == 0
     ro, rf = tl.run_oracle(inp)
     tl.check_out(o, ro, "after bad call")
     tl.check_state(f, rf, "after bad call")

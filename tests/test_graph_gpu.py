@@ -62,3 +62,52 @@ def test_captured_call_replays_bit_identical(tag, workload, kw):
         torch.cuda.synchronize()
         assert torch.equal(out_g.view(torch.int16), out_e.view(torch.int16)), tag
         assert torch.equal(fin_g, fin_e), tag
+
+
+def test_eager_call_while_another_stream_captures():
+    """A capture of an overlapped call stays open on stream X while an eager
+    overlapped call runs on stream Y.  Each caller stream has its own second
+    stream for the state stages, so Y's work neither joins X's capture nor
+    fails; both results equal the eager reference bit for bit."""
+    from kimi_delta_attention_05_gb300 import kda as K
+    inp = make_inputs(WORKLOADS["long_context"], T=16384, H=4, seed=93)
+    inp["final_state"] = "f32"
+    d = tl.to_device(inp)
+    H = d["q"].shape[2]
+
+    def buffers():
+        out = torch.full_like(d["v"], float("nan"))
+        fin = torch.full((inp["N"], H, 128, 128), float("nan"), device="cuda")
+        args = K.make_args(d["q"], d["k"], d["v"], d["g"], d["beta"], inp["scale"], out,
+                           d["A_log"], d["dt_bias"], None, None, fin, None, inp["qk_l2norm"],
+                           inp["gate"])
+        ws = torch.empty(K.workspace_bytes(args), dtype=torch.uint8, device="cuda")
+        return out, fin, args, ws
+
+    lib = K.load_library()
+    import ctypes
+    out_r, fin_r, args_r, ws_r = buffers()
+    assert lib.kda_fwd_launches(ctypes.byref(args_r)) > 3  # the overlapped pass
+    K.kda_fwd_args_call(args_r, ws_r, torch.cuda.current_stream())
+    sx, sy = torch.cuda.Stream(), torch.cuda.Stream()
+    out_x, fin_x, args_x, ws_x = buffers()
+    out_y, fin_y, args_y, ws_y = buffers()
+    torch.cuda.synchronize()
+    K.kda_fwd_args_call(args_x, ws_x, sx)  # per-stream set-up outside the capture
+    K.kda_fwd_args_call(args_y, ws_y, sy)
+    torch.cuda.synchronize()
+    for t in (out_x, fin_x, out_y, fin_y):
+        t.fill_(float("nan"))
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=sx, capture_error_mode="relaxed"):
+        K.kda_fwd_args_call(args_x, ws_x, sx)
+        K.kda_fwd_args_call(args_y, ws_y, sy)  # eager, on another stream, capture still open
+    torch.cuda.synchronize()
+    assert torch.equal(out_y.view(torch.int16), out_r.view(torch.int16))
+    assert torch.equal(fin_y, fin_r)
+    assert torch.isnan(out_x.float()).all()  # captured, not run yet
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out_x.view(torch.int16), out_r.view(torch.int16))
+    assert torch.equal(fin_x, fin_r)

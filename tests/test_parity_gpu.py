@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 import torch
 
-from kimi_delta_attention_05_gb300.workloads import WORKLOADS, make_inputs
+from kimi_delta_attention_05_gb300.workloads import WORKLOAD_ORDER, WORKLOADS, make_inputs
 from tests import kda_testlib as tl
 
 pytestmark = pytest.mark.gpu
@@ -219,18 +219,39 @@ def test_empty_sequences_write_initial_state():
     tl.check_out(o, ro, "with empty sequences")
 
 
-# ---- full-size workloads: sampled units against the oracle ----
+def test_fp16_operand_range_large_values():
+    """The state path's fp16 operands (U, U_new, the state, q gamma, W) hold
+    values up to 65,504.  Values and states in the thousands, no L2 norm
+    (keys ~ N(0, 0.05) as the extremes workload): still within tolerance."""
+    inp = make_inputs(WORKLOADS["extremes"], B=1, T=500, H=2, seed=31)
+    gen = torch.Generator().manual_seed(32)
+    inp["v"] = (torch.randn(inp["v"].shape, generator=gen) * 4000.0).to(torch.bfloat16)
+    inp["initial_state"] = torch.randn((1, 2, 128, 128), generator=gen) * 4000.0
+    inp["final_state"] = "f32"
+    assert float(inp["v"].float().abs().max()) > 15000
+    _full_check(inp, "values and state ~4000")
 
-@pytest.mark.parametrize("name,units", [
-    ("dense_batch", [0, 17, 63]),
-    ("long_context", [0, 13, 31]),
-    ("packed_varlen", [0, 5 * 16 + 3, 63 * 16 + 15]),
-    ("extremes", [0, 15]),
-])
-def test_full_size_sampled(name, units):
+
+# ---- full-size workloads: every (sequence, head) unit against the oracle ----
+
+def _worst_unit_rms(inp, o, ro):
+    H = inp["q"].shape[2]
+    worst = 0.0
+    for (b, t0, t1, h) in tl.unit_rows(inp, range(inp["N"] * H)):
+        if t1 > t0:
+            worst = max(worst, tl.rel_rms(o[b, t0:t1, h], ro[b, t0:t1, h]))
+    return worst
+
+
+@pytest.mark.parametrize("name", WORKLOAD_ORDER)
+def test_full_size_every_unit(name):
+    """Each workload at its full size, in the launch configuration the
+    benchmark times, compared element by element on every (sequence, head)
+    unit; the margins are recorded and printed at the end of the session."""
     inp = make_inputs(WORKLOADS[name])
     o, f = tl.run_gpu(inp)
-    assert np.isfinite(o).all()
-    if f is not None:
-        assert np.isfinite(f).all()
-    tl.compare_units(inp, o, f, units, name)
+    ro, rf = tl.run_oracle(inp)
+    r, m = tl.check_out(o, ro, name)
+    st = tl.check_state(f, rf, name) if f is not None else None
+    ratio = m / float(np.abs(ro).max())
+    tl.record_margin(name, r, ratio, _worst_unit_rms(inp, o, ro), st)

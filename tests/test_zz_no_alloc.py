@@ -76,3 +76,42 @@ def test_noalloc_rejects_problems_beyond_its_buffer():
     rc = _lib().kda_fwd_noalloc(ctypes.byref(a), None)
     assert rc == KDA_ERR_NOALLOC_LIMIT
     assert b"built-in" in _lib().kda_error_string(rc)
+
+
+def test_noalloc_overlapped_pass_and_allocates_nothing():
+    """A shape that takes the overlapped two-stream pass (one sequence-head,
+    256 chunks: six token ranges, twelve launches) puts its fp32 carry inside
+    the built-in buffer too.  After one warm-up call (which loads the kernels
+    and makes the stream's set-up), further calls change neither torch's
+    allocation count nor the device's free memory."""
+    inp = make_inputs(WORKLOADS["long_context"], B=1, T=16384, H=1, seed=43)
+    inp["final_state"] = "f32"
+    d = tl.to_device(inp)
+    out = torch.full_like(d["v"], float("nan"))
+    fin = torch.full((1, 1, 128, 128), float("nan"), device="cuda")
+    args = K.make_args(d["q"], d["k"], d["v"], d["g"], d["beta"], inp["scale"], out, d["A_log"],
+                       d["dt_bias"], None, None, fin, None, inp["qk_l2norm"], inp["gate"])
+    lib = _lib()
+    assert lib.kda_fwd_launches(ctypes.byref(args)) == 12
+    assert 0 < K.workspace_bytes(args) <= 32 * 1024 * 1024
+    stream = torch.cuda.current_stream()
+    assert lib.kda_fwd_noalloc(ctypes.byref(args), ctypes.c_void_p(stream.cuda_stream)) == 0
+    torch.cuda.synchronize()
+    alloc0 = torch.cuda.memory_allocated()
+    free0, _ = torch.cuda.mem_get_info()
+    out.fill_(float("nan"))
+    fin.fill_(float("nan"))
+    torch.cuda.synchronize()
+    for _ in range(2):
+        assert lib.kda_fwd_noalloc(ctypes.byref(args), ctypes.c_void_p(stream.cuda_stream)) == 0
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated() == alloc0
+    assert torch.cuda.mem_get_info()[0] == free0
+    o = out.double().cpu().numpy()
+    f = fin.double().cpu().numpy()
+    o_ref, f_ref = _run(inp, use_noalloc=False)
+    np.testing.assert_array_equal(o, o_ref)
+    np.testing.assert_array_equal(f, f_ref)
+    ro, rf = tl.run_oracle(inp)
+    tl.check_out(o, ro, "noalloc overlapped vs oracle")
+    tl.check_state(f, rf, "noalloc overlapped vs oracle")
