@@ -49,8 +49,8 @@ BYTES_OUT_PER_TOKEN_HEAD = 2 * K_DIM
 DEFAULT_STEPS = {"tiny": 2000, "dense_batch": 3000, "long_context": 3000, "packed_varlen": 500,
                  "extremes": 1000}
 KERNEL_SOURCES = {
-    "kda_chunk_kernel": ["kda_chunk.cu", "kda_common.cuh", "kda_kernels.cuh"],
-    "kda_state_kernel": ["kda_state.cu", "kda_common.cuh", "kda_kernels.cuh"],
+    "kda_chunk_kernel": ["kda_chunk.cu", "kda_common.cuh", "kda_kernels.cuh", "kda_tc.cuh"],
+    "kda_state_kernel": ["kda_state.cu", "kda_common.cuh", "kda_kernels.cuh", "kda_tc.cuh"],
     "kda_recurrent_kernel": ["kda_recurrent.cu", "kda_common.cuh", "kda_kernels.cuh"],
 }
 

@@ -29,7 +29,6 @@ struct ChunkParams {
   int64_t ld;                             // dense: rows from one sequence's start to the next (>= T)
   unsigned char* ws;                      // first workspace slot
   int* status;                            // device status word (bounded waits that give up)
-  int second_wave;                        // first block of the second CTA per SM (set by the launch)
 };
 
 // Recurrent stage (one CTA per (sequence, head, 64-wide value tile)).

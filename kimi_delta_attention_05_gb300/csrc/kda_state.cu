@@ -29,6 +29,7 @@
 // happens, so they always complete.
 #include "kda_common.cuh"
 #include "kda_kernels.cuh"
+#include "kda_tc.cuh"
 
 namespace kda {
 
@@ -100,61 +101,6 @@ struct StateCfg {
   static_assert(kStg <= kStages, "barrier slots");
 };
 
-// ---- tcgen05 helpers ----
-// Shared-memory matrix descriptor: given leading / stride byte offsets and
-// swizzle layout (2: 128-byte, 4: 64-byte).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
-                                              uint32_t layout = 2) {
-  uint64_t d = (uint64_t)((addr >> 4) & 0x3FFF);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
-  d |= (uint64_t)1 << 46;  // descriptor version
-  d |= (uint64_t)layout << 61;
-  return d;
-}
-// Instruction descriptor: fp16 x fp16 -> fp32, M x N, each operand K-major or MN-major.
-__device__ __forceinline__ uint32_t idesc_f16(int m, int n, bool a_mn_major, bool b_mn_major) {
-  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
-         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
-}
-// Issued by a whole converged warp: elect.sync picks the one lane that issues.
-// All lanes hold the same (warp-uniform) operands, so the descriptors stay in
-// uniform registers; a branch on one lane instead costs ~50 cycles per issue
-// (measured: 8 products 407 -> 192 cycles of issue), which the chain pays.
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p, e;\n elect.sync _|e, 0xffffffff;\n setp.ne.u32 p, %4, 0;\n"
-      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
-}
-__device__ __forceinline__ void tc_commit(uint32_t mbar) {
-  asm volatile("{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
-               " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(mbar)
-               : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
-}
-// 32 consecutive fp32 columns of this thread's tensor-memory lane.
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
-        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
-        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-}
 // Hardware named barriers (ids 1, 2; 0 is __syncthreads): the publishing warps
 // arrive, the tensor-core warp (all 32 lanes) waits.  Every participant passes
 // each barrier the same number of times, whatever happens (no early exits).
