@@ -250,6 +250,55 @@ size_t kda_fwd_host_device_bytes(const kda_fwd_args *args);
 int kda_fwd_host(const kda_fwd_args *args, void *device_buffer, size_t device_bytes, void *stream);
 
 /*
+ * Backward pass: the gradients of L = <out, dout> + <final_state, dfinal_state>
+ * with respect to every input of the forward call (the "chunk_bwd" stage of the
+ * fla-kda code map, SKILL.md "Code map"; the pages' FlashKDA entry point itself
+ * is forward-only).  Computed in fp32 from the bf16 inputs, token by token:
+ * the forward recurrence is replayed from state checkpoints taken every 16
+ * tokens (workspace), and the reverse recurrence runs per value row of the
+ * state.  All gradients are fp32.
+ *
+ *  fwd            : the forward call's arguments (out and final_state unused;
+ *                   every layout, flag and check as kda_fwd)
+ *  dout           : bf16 [B, T, H, 128], dL/d out
+ *  dfinal_state   : fp32 [N, H, 128, 128] or NULL (no final-state term)
+ *  dq, dk, dv, dg : fp32 [B, T, H, 128], written completely (dg with respect to
+ *                   the raw g: logits, or the log decays with KDA_GATE_LOGSPACE)
+ *  dbeta          : fp32 [B, T, H] with respect to the raw beta (logits, or beta
+ *                   itself with KDA_BETA_PROB)
+ *  dA_log         : fp32 [H] or NULL; not written with KDA_GATE_LOGSPACE
+ *  ddt_bias       : fp32 [H, 128] or NULL; not written with KDA_GATE_LOGSPACE
+ *  dinitial_state : fp32 [N, H, 128, 128] or NULL
+ * dA_log and ddt_bias are sums over tokens accumulated with float atomics (the
+ * order, and so the last bits, may differ from run to run); every other
+ * gradient is deterministic.  With cu_seqlens, a sequence whose bounds are
+ * inconsistent is skipped (zero token gradients, dinitial_state = dfinal_state)
+ * and the stream's status word reads KDA_ERR_BAD_SEQLENS.
+ */
+typedef struct kda_bwd_args {
+  kda_fwd_args fwd;
+  const void *dout;
+  const float *dfinal_state;
+  float *dq, *dk, *dv, *dg;
+  float *dbeta;
+  float *dA_log;
+  float *ddt_bias;
+  float *dinitial_state;
+} kda_bwd_args;
+
+/* Device scratch for kda_bwd (state checkpoints, H * (B*T / 16 + N + 1) *
+ * 64 KiB, and per-token-head records, B*T*H*1540 bytes); 0 if the forward
+ * arguments are invalid. */
+size_t kda_bwd_workspace_bytes(const kda_bwd_args *args);
+
+/* Enqueue the backward pass on `stream`.  Workspace as for kda_fwd (caller
+ * owned, 256-byte aligned, at least kda_bwd_workspace_bytes).  Returns KDA_OK
+ * or an error code before any launch (the kda_fwd checks; dout and the token
+ * gradients must be given when B * T > 0; 16-byte alignment of the float
+ * tensors), or KDA_ERR_LAUNCH. */
+int kda_bwd(const kda_bwd_args *args, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Device-side status of the forward calls enqueued on `stream` (a cudaStream_t;
  * NULL = legacy default stream), the kda_get_status(cudaStream_t) of the
  * boundary: KDA_OK, KDA_ERR_DEVICE_TIMEOUT if a CTA of such a call gave up

@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libkda.so")
 SOURCES = ["kda_api.cu", "kda_chunk.cu", "kda_state.cu", "kda_recurrent.cu", "kda_noalloc.cu",
-           "kda_host.cu", "kda_status.cu"]
+           "kda_host.cu", "kda_status.cu", "kda_bwd.cu"]
 HEADERS = ["kda_common.cuh", "kda_kernels.cuh", "kda_tc.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -155,8 +155,8 @@ int device_sms() {
 int pipe_state_budget(int64_t units, int sms) { return units * 4 * 2 <= sms ? sms / 2 : 0; }
 
 // Token ranges a dense pass is cut into (every range of every sequence, whole
-// chunks), so that the state stage of range r, on a high-priority stream,
-// overlaps the intra-chunk stage of range r + 1 on the SMs it leaves free:
+// chunks), so that the state stage of range r, on a second stream, overlaps
+// the intra-chunk stage of range r + 1 on the SMs it leaves free:
 // for few sequence-heads (above) and sequences of at least 256 chunks;
 // otherwise 1.  Measured, ms per call by ranges 1 / 3 / 4 / 6 / 8: B2 T32768 H8
 // 0.699 / 0.651 / 0.612 / 0.580 / 0.608, the same with H4 0.563 / 0.534 /
@@ -173,8 +173,37 @@ int pipeline_ranges(const kda_fwd_args* a, int sms) {
 
 size_t carry_bytes(const kda_fwd_args* a) { return (size_t)(a->N * a->H) * kHeadDim * kHeadDim * 4; }
 
-// Second stream (greatest priority) and events of the pipelined pass, one set
-// per caller stream: the state stages of a call run on its caller's own
+// Sequence split inside one GPU (dense calls with very few sequence-heads):
+// the state stage's chain over C chunks is cut into G segments.  The state
+// after a segment is affine in the state before it, S_end = S_start M + R,
+// with M the state the recurrence reaches from the identity with U taken as
+// zero and R the state it reaches from zero.  One launch runs segment 0 as
+// usual beside the R and M runs of segments 1 .. G-1 (2G - 1 runs of C / G
+// chunks at once), a small kernel chains S_{g+1} = S_g M_g + R_g, and a second
+// launch runs segments 1 .. G-1 from their S_g with the outputs: 2C / G chunk
+// periods instead of C.  Used when all 2G - 1 runs (four 32-column CTAs per
+// sequence-head each) fit on the GPU at once for some G >= 3, with at least
+// 64 chunks per segment.
+#ifndef KDA_SPLIT_SEGMENTS
+#define KDA_SPLIT_SEGMENTS 0  // > 0: always this many segments (measurement builds)
+#endif
+constexpr int kSplitMaxSegments = (kMaxStateJobs + 1) / 2;  // 2G - 1 runs in one launch
+constexpr int64_t kSplitMinChunks = 64;
+static_assert(KDA_SPLIT_SEGMENTS <= kSplitMaxSegments, "split segments");
+int split_segments(const kda_fwd_args* a, int sms) {
+  if (a->cu_seqlens || sms <= 0) return 1;
+  const int64_t units = a->N * a->H, nch = ceil_div(a->T, kChunk);
+  if (units == 0) return 1;
+  if (KDA_SPLIT_SEGMENTS > 0) return nch >= KDA_SPLIT_SEGMENTS ? KDA_SPLIT_SEGMENTS : 1;
+  for (int g = kSplitMaxSegments; g >= 3; --g)
+    if ((2 * g - 1) * units * 4 <= sms && nch >= g * kSplitMinChunks) return g;
+  return 1;
+}
+// fp32 [units][128][128] buffers of a split pass: X (segment 0's final state),
+// R_g and M_g for g = 1 .. G-1, S_g for g = 2 .. G-1.
+size_t split_bytes(const kda_fwd_args* a, int G) { return G > 1 ? (size_t)(3 * G - 3) * carry_bytes(a) : 0; }
+
+// Second stream and events of the pipelined pass, one set per caller stream: the state stages of a call run on its caller's own
 // second stream, so calls from different caller streams never share one (a
 // capture open on one caller stream cannot take in another caller's work, and
 // unrelated callers do not queue behind each other).
@@ -193,11 +222,12 @@ struct PipeTable {
 };
 PipeTable g_pipes[kMaxDevices];
 
+// The second stream has the default priority: a stream of greater priority may
+// preempt running CTAs of the intra-chunk stage, which hold tensor-memory
+// columns, while the state stage's CTAs wait to allocate theirs.
 bool make_pipe_ctx(PipeCtx& c) {
   if (c.ready) return true;
-  int lo = 0, hi = 0;
-  if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) return false;
-  if (cudaStreamCreateWithPriority(&c.state_stream, cudaStreamNonBlocking, hi) != cudaSuccess) return false;
+  if (cudaStreamCreateWithFlags(&c.state_stream, cudaStreamNonBlocking) != cudaSuccess) return false;
   const unsigned ef = cudaEventDisableTiming;
   if (cudaEventCreateWithFlags(&c.start, ef) != cudaSuccess) return false;
   if (cudaEventCreateWithFlags(&c.end, ef) != cudaSuccess) return false;
@@ -226,7 +256,10 @@ extern "C" size_t kda_fwd_workspace_bytes(const kda_fwd_args* args) {
   size_t header = 0;
   if (validate(args, &slots, &header) != KDA_OK) return 0;
   const size_t ws = header + (size_t)slots * (size_t)args->H * (size_t)kSlotBytes;
-  return ws + (pipeline_ranges(args, device_sms()) > 1 ? carry_bytes(args) : 0);
+  const int sms = device_sms();
+  const int G = split_segments(args, sms);
+  if (G > 1) return ws + split_bytes(args, G);
+  return ws + (pipeline_ranges(args, sms) > 1 ? carry_bytes(args) : 0);
 }
 
 int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_bytes,
@@ -237,9 +270,10 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
   int rc = validate(a, &slots, &header);
   if (rc != KDA_OK) return rc;
   if (a->N == 0 || a->H == 0) return KDA_OK;
-  int ranges = allow_pipeline ? pipeline_ranges(a, device_sms()) : 1;
+  const int G = allow_pipeline ? split_segments(a, device_sms()) : 1;
+  int ranges = allow_pipeline && G == 1 ? pipeline_ranges(a, device_sms()) : 1;
   const size_t slot_bytes = (size_t)slots * (size_t)a->H * (size_t)kSlotBytes;
-  const size_t need = header + slot_bytes + (ranges > 1 ? carry_bytes(a) : 0);
+  const size_t need = header + slot_bytes + (G > 1 ? split_bytes(a, G) : (ranges > 1 ? carry_bytes(a) : 0));
   if (need > 0 && (!workspace || !aligned(workspace, 256) || workspace_bytes < need))
     return KDA_ERR_WORKSPACE;
   int dev = 0;
@@ -303,6 +337,7 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
                           void* fin, int ib, int fb, cudaStream_t s) {
     const int64_t r0 = t0 * a->H * kHeadDim;
     StateParams sp;
+    sp.njobs = 0;
     sp.out = static_cast<uint16_t*>(a->out) + (a->out ? r0 : 0);
     sp.init = init;
     sp.final_state = fin;
@@ -320,8 +355,66 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
     sp.status = status;
     launch_state_kernel(sp, s, ranges > 1 ? pipe_state_budget(a->N * a->H, device_sms()) : 0);
   };
+  // The split pass (see split_segments): runs of the state stage as jobs of one launch.
+  auto launch_split = [&]() {
+    const int64_t units = a->N * a->H;
+    const int64_t nch = ceil_div(a->T, kChunk), segc = ceil_div(nch, G);
+    const size_t mat = (size_t)units * kHeadDim * kHeadDim;  // floats per buffer
+    float* X = reinterpret_cast<float*>(ws + header + slot_bytes);
+    float* R = X + mat;
+    float* M = R + (size_t)(G - 1) * mat;
+    float* S = M + (size_t)(G - 1) * mat;
+    StateParams sp;
+    sp.out = static_cast<uint16_t*>(a->out);
+    sp.init = nullptr;
+    sp.final_state = nullptr;
+    sp.init_bf16 = sp.final_bf16 = 0;
+    sp.scale = a->scale;
+    sp.cu = nullptr;
+    sp.chunk_off = nullptr;
+    sp.N = a->N;
+    sp.T = a->T;
+    sp.H = a->H;
+    sp.NT = nch;
+    sp.ld = a->T;
+    sp.ws = slots_base;
+    sp.status = status;
+    auto job = [&](int64_t seg, const void* init, int kind, int ib, void* fin, int fb, int u_zero,
+                   int write_out) {
+      StateJob j;
+      j.c0 = seg * segc;
+      j.c1 = (seg + 1) * segc;
+      j.init = init;
+      j.init_kind = kind;
+      j.init_bf16 = ib;
+      j.fin = fin;
+      j.fin_bf16 = fb;
+      j.u_zero = u_zero;
+      j.write_out = write_out;
+      return j;
+    };
+    sp.njobs = 2 * G - 1;  // segment 0 as usual; R and M of the others
+    sp.jobs[0] = job(0, a->initial_state, a->initial_state ? 1 : 0, ib16, X, 0, 0, 1);
+    for (int g = 1; g < G; ++g) {
+      sp.jobs[2 * g - 1] = job(g, nullptr, 0, 0, R + (size_t)(g - 1) * mat, 0, 0, 0);
+      sp.jobs[2 * g] = job(g, nullptr, 2, 0, M + (size_t)(g - 1) * mat, 0, 1, 0);
+    }
+    launch_state_kernel(sp, stream, 0);
+    launch_split_combine(X, R, M, S, units, G, stream);
+    sp.njobs = G - 1;  // segments 1 .. G-1 from their true initial states, with the outputs
+    for (int g = 1; g < G; ++g)
+      sp.jobs[g - 1] = job(g, g == 1 ? X : S + (size_t)(g - 2) * mat, 1, 0,
+                           g == G - 1 ? a->final_state : nullptr, fb16, 0, 1);
+    launch_state_kernel(sp, stream, 0);
+  };
 
-  if (ranges == 1) {
+  if (G > 1) {
+    mark(0);
+    launch_chunks(0, a->T, slots_base, stream, 0);
+    mark(1);
+    launch_split();
+    mark(2);
+  } else if (ranges == 1) {
     mark(0);
     if (a->cu_seqlens)
       launch_chunk_offsets(a->cu_seqlens, a->N, a->T, chunk_off, status, stream);
@@ -331,7 +424,7 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
     mark(2);
   } else {
     // chunk stage of range r on the caller's stream, state stage on the
-    // high-priority stream after it; the fp32 state passes from range to range
+    // second stream after it; the fp32 state passes from range to range
     PipeCtx& c = *pipe;
     std::lock_guard<std::mutex> lock(c.mu);
     if (!make_pipe_ctx(c)) return KDA_ERR_LAUNCH;
@@ -418,6 +511,7 @@ extern "C" int kda_fwd_launches(const kda_fwd_args* a) {
   int64_t slots = 0;
   size_t header = 0;
   if (validate(a, &slots, &header) != KDA_OK || a->N == 0 || a->H == 0) return 0;
+  if (split_segments(a, device_sms()) > 1) return 4;  // chunk, state, combine, state
   const int ranges = pipeline_ranges(a, device_sms());
   if (ranges > 1) {  // one chunk and one state launch per token range
     const int64_t span = ceil_div(ceil_div(a->T, kChunk), ranges) * kChunk;

@@ -80,12 +80,6 @@ constexpr int kRhsV = kRhs + 16384;
 // (1,0) (2,0) (2,1) (3,0) (3,1) (3,2).
 constexpr int kKc = 65536;
 constexpr int kKcHalf = 160 * 128;
-// Scratch between the gate and operand stages: the decay products of each
-// 8-token half sub-chunk go into the g-tile rows of that half (1 KB from byte
-// 128 t0 of half 0), which only the warp that owns the half reads, and only
-// before it writes them: exact product fp32 [128] first, then the clamped one.
-__device__ __forceinline__ int cs_exact(int seg) { return kRhs + seg * 1024; }
-__device__ __forceinline__ int cs_clamped(int seg) { return kRhs + seg * 1024 + 512; }
 // Scratch inside the column-operand region after the A / P products (the
 // column operands are dead):
 constexpr int kT = kKc;              // kmaj [64][64] fp16: T = (I + A)^-1; its copy follows at +8 KB
@@ -93,10 +87,16 @@ constexpr int kAd = kKc + 20480;     // fp32 [4][16][16]: diagonal sub-blocks of
 constexpr int kA16 = kKc + 24576;    // [64][64] fp16 (swz64): off-diagonal sub-blocks of A, then M_rc
 // small arrays
 constexpr int kSm = kKc + 2 * kKcHalf;  // 106496
-constexpr int kCsBeta = kSm + 1536;     // fp32 [64]
-constexpr int kCsRq = kSm + 1792;       // fp32 [64]: 1 / |q| (or 1)
-constexpr int kCsRk = kSm + 2048;       // fp32 [64]: 1 / |k| (or 1)
-constexpr int kCsBar = kSm + 2304;      // mbarriers: q/k tiles, g/v tiles, tensor-core commits
+// decay products of the eight 8-token half sub-chunks, fp32 [8][2][128]: the
+// exact product, then the clamped one (written by the gate stage, read by the
+// operand stage; no other stage touches them)
+constexpr int kCsDec = kSm;
+__device__ __forceinline__ int cs_exact(int seg) { return kCsDec + seg * 1024; }
+__device__ __forceinline__ int cs_clamped(int seg) { return kCsDec + seg * 1024 + 512; }
+constexpr int kCsBeta = kSm + 8192;     // fp32 [64]
+constexpr int kCsRq = kCsBeta + 256;    // fp32 [64]: 1 / |q| (or 1)
+constexpr int kCsRk = kCsBeta + 512;    // fp32 [64]: 1 / |k| (or 1)
+constexpr int kCsBar = kCsBeta + 768;   // mbarriers: q/k tiles, g/v tiles, tensor-core commits
 constexpr int kCsTmem = kCsBar + 24;    // tensor-memory base address
 constexpr int kChunkSmem = kCsTmem + 8;
 static_assert(kRo % 1024 == 0 && kRhs % 1024 == 0 && kKc % 1024 == 0 && (kKc + kKcHalf) % 1024 == 0,
@@ -200,6 +200,25 @@ __device__ __forceinline__ void store_tblock(unsigned char* smem, const float (&
       u32_at(smem + kT, off) = v;
       u32_at(smem + kT + 8192, off) = v;
     }
+}
+
+// Row sub-chunk R of T: M_Rc = -X_R A_Rc for c < R into m0.. (fp16 A fragments),
+// then T_R,R-1 = M_R,R-1 X_R-1, stored.
+template <int R>
+__device__ __forceinline__ void t_first(unsigned char* smem, uint32_t sbase, uint32_t (&m0)[4],
+                                        uint32_t (&m1)[4], uint32_t (&m2)[4], int lane) {
+  uint32_t xa[4];
+  lda_64(xa, sbase + kT, 16 * R, 16 * R, lane);  // X_R
+  uint32_t(*ms[3])[4] = {&m0, &m1, &m2};
+#pragma unroll
+  for (int c = 0; c < R; ++c) {
+    float acc[2][4] = {};
+    mma16_kn(acc, xa, sbase + kA16, 16 * c, 16 * R, lane);  // X_R A_Rc
+    cfrag_to_afrag(acc, *ms[c], -1.f);
+  }
+  float t[2][4] = {};
+  mma16_kn(t, *ms[R - 1], sbase + kT, 16 * (R - 1), 16 * (R - 1), lane);  // M_R,R-1 X_R-1
+  store_tblock(smem, t, 16 * R, 16 * (R - 1), lane);
 }
 
 template <int kGate, bool kL2>
@@ -323,6 +342,16 @@ __global__ void __launch_bounds__(256, 2)
     copy_gv(cur);
   }
   float blogit = tid < kChunk ? load_beta(cur) : 0.f;
+  // per-head gate inputs of this thread's four channels (loaded one item ahead)
+  const int c0g = 4 * (tid & 31);
+  auto load_dtb = [&](const Item& it) {
+    return (p.dt_bias && kGate != kGateLogspace)
+               ? *reinterpret_cast<const float4*>(p.dt_bias + it.h * kHeadDim + c0g)
+               : make_float4(0.f, 0.f, 0.f, 0.f);
+  };
+  auto load_alog = [&](const Item& it) { return (p.A_log && kGate != kGateLogspace) ? p.A_log[it.h] : 0.f; };
+  float4 dtb_next = load_dtb(cur);
+  float alog_next = load_alog(cur);
   float* sBeta = reinterpret_cast<float*>(smem + kCsBeta);
   float* sRq = reinterpret_cast<float*>(smem + kCsRq);
   float* sRk = reinterpret_cast<float*>(smem + kCsRk);
@@ -347,6 +376,12 @@ __global__ void __launch_bounds__(256, 2)
   const int64_t next = item + gridDim.x;
   Item nxt = cur;
   if (next < num_items) nxt = locate(next);
+  const float4 dtb = dtb_next;
+  const float alog = alog_next;
+  if (next < num_items) {
+    dtb_next = load_dtb(nxt);
+    alog_next = load_alog(nxt);
+  }
   if (tid < kChunk)
     sBeta[tid] = tid >= L ? 0.f : (p.beta_prob ? blogit : rcp_approx(1.0f + ex2(-blogit * kLog2e)));
   wait_bar(bar_qk, (uint32_t)(it & 1));
@@ -378,11 +413,8 @@ __global__ void __launch_bounds__(256, 2)
   float inv[4];    // 1 / (clamped product over this half)
   const f32x2 one2 = f2(1.0f, 1.0f);
   {
-    const float4 dtb = (p.dt_bias && kGate != kGateLogspace)
-                           ? *reinterpret_cast<const float4*>(p.dt_bias + h * kHeadDim + c0)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
     const f32x2 dtb2[2] = {f2(dtb.x, dtb.y), f2(dtb.z, dtb.w)};
-    const float amul_log2e = (p.A_log && kGate != kGateLogspace ? expf(p.A_log[h]) : 1.0f) *
+    const float amul_log2e = (p.A_log && kGate != kGateLogspace ? expf(alog) : 1.0f) *
                              (kGate == kGateUnsafe ? 1.0f : kLog2e);
     const float lb_log2e = p.lower_bound * kLog2e;
     f32x2 D2[2] = {one2, one2}, Dc2[2] = {one2, one2};
@@ -420,13 +452,13 @@ __global__ void __launch_bounds__(256, 2)
       }
     }
     const float2 Da = f2u(D2[0]), Db = f2u(D2[1]), Dca = f2u(Dc2[0]), Dcb = f2u(Dc2[1]);
-    __syncwarp();  // the whole warp has read its g rows before they take the products
     *reinterpret_cast<float4*>(smem + cs_exact(seg) + c0 * 4) = make_float4(Da.x, Da.y, Db.x, Db.y);
     *reinterpret_cast<float4*>(smem + cs_clamped(seg) + c0 * 4) = make_float4(Dca.x, Dca.y, Dcb.x, Dcb.y);
-    inv[0] = __frcp_rn(Dca.x);
-    inv[1] = __frcp_rn(Dca.y);
-    inv[2] = __frcp_rn(Dcb.x);
-    inv[3] = __frcp_rn(Dcb.y);
+    // (an approximate reciprocal: it only scales the bf16 A / P operands)
+    inv[0] = rcp_approx(Dca.x);
+    inv[1] = rcp_approx(Dca.y);
+    inv[2] = rcp_approx(Dcb.x);
+    inv[3] = rcp_approx(Dcb.y);
   }
   // norms from the diagonal of the Gram product: lane l of warp w < 4 holds row 32 w + l
   if (kL2) {
@@ -551,8 +583,10 @@ __global__ void __launch_bounds__(256, 2)
       }
     }
   }
-  __syncthreads();
-  // forward over the half (overwrites raw q, k, g, v)
+  // forward over the half (overwrites raw q, k, g, v).  No barrier: from the
+  // gate stage on, every thread reads and writes only its own elements of the
+  // q, k, g and v tiles.
+
   {
     unsigned char* gQg = ws + kSlotA1;  // rows 0..63 of the [q gamma; W] image
     f32x2 x2[2] = {pre2[0], pre2[1]}, xc2[2] = {one2, one2};
@@ -682,11 +716,11 @@ __global__ void __launch_bounds__(256, 2)
   tc_fence_before();
   __syncthreads();
 
-  // ---- X_r = (I + A_rr)^-1 by forward substitution (warp r, lane = column) into the
-  //      diagonal blocks of T ----
-  if (warp < 4 && lane < 16) {
-    const int j = lane;
-    const float4* Ad4 = reinterpret_cast<const float4*>(smem + kAd + warp * 1024);  // rows of 16 floats
+  // ---- X_r = (I + A_rr)^-1 by forward substitution (warp w: sub-chunks 2 w and
+  //      2 w + 1 in lanes 0-15 and 16-31, lane = column) into the diagonal blocks of T ----
+  if (warp < 2) {
+    const int j = lane & 15, rx = 2 * warp + (lane >> 4);
+    const float4* Ad4 = reinterpret_cast<const float4*>(smem + kAd + rx * 1024);  // rows of 16 floats
     float x[kSub];
 #pragma unroll
     for (int ii = 0; ii < kSub; ++ii) {
@@ -704,7 +738,7 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
     for (int ii = 0; ii < kSub; ++ii) {
       const __half xv = __float2half_rn(x[ii]);
-      const uint32_t off = swz64(16 * warp + ii, 16 * warp + j);
+      const uint32_t off = swz64(16 * rx + ii, 16 * rx + j);
       *reinterpret_cast<__half*>(smem + kT + off) = xv;
       *reinterpret_cast<__half*>(smem + kT + 8192 + off) = xv;
     }
@@ -712,39 +746,25 @@ __global__ void __launch_bounds__(256, 2)
   __syncthreads();
   // ---- off-diagonal blocks of T: T_rc = sum_{m=c}^{r-1} M_rm T_mc, M_rm = -X_r A_rm.
   //      Warp r - 1 forms M_r0 .. M_r,r-1 in registers, then T_r,r-1; the deeper
-  //      blocks follow after the blocks they read are stored ----
-  uint32_t aM[3][4];
-  if (warp < 3) {
-    const int r = warp + 1;
-    uint32_t xa[4];
-    lda_64(xa, sbase + kT, 16 * r, 16 * r, lane);  // X_r
-#pragma unroll
-    for (int c = 0; c < 3; ++c) {
-      if (c < r) {
-        float acc[2][4] = {};
-        mma16_kn(acc, xa, sbase + kA16, 16 * c, 16 * r, lane);  // X_r A_rc
-        cfrag_to_afrag(acc, aM[c], -1.f);
-      }
-    }
-    float t[2][4] = {};
-    uint32_t am[4] = {aM[r - 1][0], aM[r - 1][1], aM[r - 1][2], aM[r - 1][3]};
-    mma16_kn(t, am, sbase + kT, 16 * (r - 1), 16 * (r - 1), lane);  // M_r,r-1 X_r-1
-    store_tblock(smem, t, 16 * r, 16 * (r - 1), lane);
-  }
+  //      blocks follow once the blocks they read are stored ----
+  uint32_t aM0[4], aM1[4], aM2[4];
+  if (warp == 0) t_first<1>(smem, sbase, aM0, aM1, aM2, lane);
+  else if (warp == 1) t_first<2>(smem, sbase, aM0, aM1, aM2, lane);
+  else if (warp == 2) t_first<3>(smem, sbase, aM0, aM1, aM2, lane);
   __syncthreads();
   if (warp == 1 || warp == 2) {  // T_20 (warp 1), T_31 (warp 2)
     const int r = warp + 1, c = r - 2;
     float t[2][4] = {};
-    mma16_kn(t, aM[c], sbase + kT, 16 * c, 16 * c, lane);            // M_rc X_c
-    mma16_kn(t, aM[c + 1], sbase + kT, 16 * c, 16 * (c + 1), lane);  // M_r,c+1 T_c+1,c
+    mma16_kn(t, warp == 1 ? aM0 : aM1, sbase + kT, 16 * c, 16 * c, lane);            // M_rc X_c
+    mma16_kn(t, warp == 1 ? aM1 : aM2, sbase + kT, 16 * c, 16 * (c + 1), lane);      // M_r,c+1 T_c+1,c
     store_tblock(smem, t, 16 * r, 16 * c, lane);
   }
   __syncthreads();
   if (warp == 2) {  // T_30
     float t[2][4] = {};
-    mma16_kn(t, aM[0], sbase + kT, 0, 0, lane);
-    mma16_kn(t, aM[1], sbase + kT, 0, 16, lane);
-    mma16_kn(t, aM[2], sbase + kT, 0, 32, lane);
+    mma16_kn(t, aM0, sbase + kT, 0, 0, lane);
+    mma16_kn(t, aM1, sbase + kT, 0, 16, lane);
+    mma16_kn(t, aM2, sbase + kT, 0, 32, lane);
     store_tblock(smem, t, 48, 0, lane);
   }
   fence_proxy_async_smem();  // T is read by the tensor core next

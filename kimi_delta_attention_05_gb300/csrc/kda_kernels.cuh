@@ -31,7 +31,22 @@ struct ChunkParams {
   int* status;                            // device status word (bounded waits that give up)
 };
 
-// Recurrent stage (one CTA per (sequence, head, 64-wide value tile)).
+// One run of the recurrent stage over a chunk range of every sequence (dense
+// calls only): initial state zero (kind 0), from a tensor (1) or the identity
+// (2, which with U taken as zero makes the final state the range's transition
+// matrix: S_end = S_start M + R is affine in S_start); final state written to
+// `fin` if not null; outputs of the range written or not.
+struct StateJob {
+  int64_t c0, c1;       // chunk range [c0, c1) (clamped to each sequence's chunks)
+  const void* init;     // [N, H, 128, 128] (kind 1)
+  void* fin;            // [N, H, 128, 128] or nullptr
+  int init_kind, init_bf16, fin_bf16;
+  int u_zero;           // 1: U taken as zero
+  int write_out;        // 1: write the range's outputs
+};
+constexpr int kMaxStateJobs = 16;
+
+// Recurrent stage (one CTA per (sequence, head, value tile) and job).
 struct StateParams {
   uint16_t* out;                          // bf16 [tokens, H, 128]
   const void* init;                       // [N, H, 128, 128] or nullptr
@@ -44,6 +59,8 @@ struct StateParams {
   int64_t ld;                             // dense: rows from one sequence's start to the next (>= T)
   const unsigned char* ws;
   int* status;                            // status word of the caller's stream (waits that give up)
+  int njobs;                              // 0: one run over every chunk with init / final_state
+  StateJob jobs[kMaxStateJobs];           // else blockIdx.y selects one of njobs runs
 };
 
 // Token-by-token path (one CTA per (sequence, head, 32-row value slab)).
@@ -65,6 +82,32 @@ struct RecurrentParams {
   int64_t N, T, H;
   int* status;                            // device status word (bad cu_seqlens)
 };
+
+// Backward pass (token-recurrent, see kda_bwd.cu).
+struct BwdParams {
+  const uint16_t *q, *k, *v, *g, *beta, *dout;  // bf16 inputs and dL/d out
+  const float* g32;                             // g as fp32, or nullptr
+  const float* A_log;
+  const float* dt_bias;
+  float lower_bound, scale;
+  int gate_mode, beta_prob, l2norm;
+  const void* init;                             // [N, H, 128, 128] or nullptr
+  int init_bf16;
+  const float* dfinal;                          // [N, H, 128, 128] fp32 or nullptr
+  const int64_t* cu;
+  int64_t N, T, H;
+  int64_t rows;                                 // packed token rows (B * T)
+  int64_t nslots;                               // checkpoint slots per head
+  int* status;
+  float* ckpt;                                  // [H][nslots][128][128]
+  float* rec;                                   // [rows][H][3 * 128 + 1]
+  float *dq, *dk, *dv, *dg, *dbeta;             // fp32 gradients
+  float *dA_log, *ddt_bias, *dinit;             // fp32, each may be nullptr
+};
+void launch_bwd(const BwdParams& p, cudaStream_t s);
+cudaError_t prepare_bwd();
+int64_t bwd_slots(int64_t rows, int64_t N);
+int bwd_record_floats();
 
 // Host-side argument checks of kda_fwd (KDA_OK or an error code); on success
 // the workspace slot count and the varlen header bytes.
@@ -97,6 +140,11 @@ bool launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t s
 // max_ctas: at most this many CTAs at once (0: the SM count) picks the
 // 32-column shape (four CTAs per head) if they fit, else the 64-column one
 void launch_state_kernel(const StateParams& p, cudaStream_t s, int max_ctas = 0);
+// Chains the segment transitions of a split pass for `units` (sequence, head)
+// pairs: S_1 = X, S_{g+1} = S_g M_g + R_g for g = 1 .. G - 2, into S (S_2 .. S_{G-1});
+// all fp32 [units][128][128], R and M indexed g - 1.
+void launch_split_combine(const float* X, const float* R, const float* M, float* S, int64_t units,
+                          int G, cudaStream_t s);
 // CTAs per head the state stage uses for `units` (sequence, head) pairs under max_ctas
 int state_tiles(int64_t units, int max_ctas);
 cudaError_t prepare_chunk_kernel();

@@ -115,8 +115,12 @@ __device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
 }
 
-template <int kVT>
-__global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(StateParams p) {
+// kJobs: the CTA runs the job blockIdx.y of p.jobs (a chunk range with its own
+// initial / final state, U possibly taken as zero, outputs possibly not
+// written); without it, the ordinary run over every chunk.
+template <int kVT, bool kJobs>
+__global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1)
+    kda_state_kernel(const __grid_constant__ StateParams p) {
   using C = StateCfg<kVT>;
   extern __shared__ __align__(1024) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -140,6 +144,18 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
     slot0 = n * p.NT;
     nch = (len + kChunk - 1) / kChunk;
   }
+  // this CTA's run: a chunk range with its own initial and final state (job
+  // fields other than the range and the two flags are read where they are used)
+  const StateJob* job = kJobs ? &p.jobs[blockIdx.y] : nullptr;
+  int64_t c_begin = 0, c_end = nch;
+  bool u_zero = false, write_out = true;
+  if (kJobs) {
+    c_begin = min(job->c0, nch);
+    c_end = min(job->c1, nch);
+    u_zero = job->u_zero != 0;
+    write_out = job->write_out != 0;
+  }
+  const int64_t ncj = c_end > c_begin ? c_end - c_begin : 0;  // chunks this CTA walks
   const uint32_t sb = smem_u32(smem);
   const uint32_t bar = sb + C::kSBar;
   auto B = [&](int i) { return bar + 8 * i; };
@@ -190,9 +206,10 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
     int64_t issued = 0;
     int st = 0;
     uint32_t ph_prev = 1;  // phase parity of the previous use of stage st
-    for (int64_t ci = 0; ci < nch; ++ci) {
+    for (int64_t it = 0; it < ncj; ++it) {
+      const int64_t ci = c_begin + it;
       if (st == 0) ph_prev ^= 1u;
-      if (ci >= C::kStg) wait(B(kBarEmpty + st), ph_prev ^ 1u);  // the stage is free again
+      if (it >= C::kStg) wait(B(kBarEmpty + st), ph_prev ^ 1u);  // the stage is free again
       __syncwarp();
       if (*s_abort) break;
       const uint32_t dst = sb + st * C::kStageBytes;
@@ -208,7 +225,7 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
         bulk_g2s(dst + C::kSU, src + kSlotU + vt * (kVT * 128), kVT * 128u, B(kBarFull + st));
       else if (lane == kPieces + 1)
         bulk_g2s(dst + C::kSGc, src + kSlotGc, 512u, B(kBarFull + st));
-      issued = ci + 1;
+      issued = it + 1;
       st = st + 1 == C::kStg ? 0 : st + 1;
     }
     if (*s_abort && lane == 0)  // after a timeout: let this CTA's issued copies land before leaving
@@ -230,8 +247,8 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
       constexpr uint32_t kStepB = 16 * C::kRowB;  // one K step (16 rows) of an MN-major B
       int st = 0;
       uint32_t phf = 0;  // phase parity of the full barrier of stage st
-      for (int64_t ci = 0; ci < nch; ++ci) {
-        const uint32_t par = (uint32_t)(ci & 1);
+      for (int64_t it = 0; it < ncj; ++it) {
+        const uint32_t par = (uint32_t)(it & 1);
         const uint64_t so = (uint64_t)((st * C::kStageBytes) >> 4);
         const uint32_t d1 = tmem + C::kVTile * par;
         wait(B(kBarFull + st), phf);
@@ -258,8 +275,8 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
         if (++st == C::kStg) { st = 0; phf ^= 1u; }
       }
       named_sync(kNbS, C::kNbSCount);  // the state published after the last chunk (no product uses it)
-      if (lane == 0 && nch > 0)  // the last products must be complete before tensor memory is freed
-        mbar_wait_bounded(B(kBarMma3), (uint32_t)((nch - 1) & 1));
+      if (lane == 0 && ncj > 0)  // the last products must be complete before tensor memory is freed
+        mbar_wait_bounded(B(kBarMma3), (uint32_t)((ncj - 1) & 1));
     }
   } else {
     // ---- epilogue warps 0-7: warp = (lane quarter q, column half hc); thread =
@@ -271,13 +288,18 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
     float s[32];  // S[vc + j][k], j = 0..31
     {
       const int64_t sbase = (n * H + h) * (int64_t)(kHeadDim * kHeadDim);
+      const void* init = kJobs ? job->init : p.init;
+      const int init_kind = kJobs ? job->init_kind : (p.init ? 1 : 0);
+      const int init_bf16 = kJobs ? job->init_bf16 : p.init_bf16;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         float x = 0.f;
-        if (p.init) {
+        if (init_kind == 1) {
           const int64_t off = sbase + (int64_t)(vc + j) * kHeadDim + k;
-          x = p.init_bf16 ? bf16_to_f(reinterpret_cast<const uint16_t*>(p.init)[off])
-                           : reinterpret_cast<const float*>(p.init)[off];
+          x = init_bf16 ? bf16_to_f(reinterpret_cast<const uint16_t*>(init)[off])
+                        : reinterpret_cast<const float*>(init)[off];
+        } else if (init_kind == 2) {
+          x = (vc + j == k) ? 1.f : 0.f;
         }
         s[j] = x;
       }
@@ -297,8 +319,9 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
 
     int st = 0;
     uint32_t phf = 0;
-    for (int64_t ci = 0; ci < nch; ++ci) {
-      const uint32_t par = (uint32_t)(ci & 1);
+    for (int64_t it = 0; it < ncj; ++it) {
+      const int64_t ci = c_begin + it;
+      const uint32_t par = (uint32_t)(it & 1);
       const unsigned char* stg = smem + st * C::kStageBytes;
       wait(B(kBarFull + st), phf);
       const float gk = reinterpret_cast<const float*>(stg + C::kSGc)[k];
@@ -323,14 +346,19 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
           }
         }
       };
-      if (q >= 2 && kVT < 128) load_u();
+      if (kJobs && u_zero) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) uf[j] = 0.f;
+      } else if (q >= 2 && kVT < 128) {
+        load_u();
+      }
       // only the U_new warps read MMA1's result now; the output rows wait for
       // MMA3 below (every suspending wait adds wake-up latency: 115 -> 110 us
       // on T=8192 H=32 without this one in the output warps)
       if (q >= 2) wait(B(kBarMma1), par);
       tc_fence_after();
       if (q >= 2) {
-        if (kVT == 128) load_u();
+        if (kVT == 128 && !(kJobs && u_zero)) load_u();
         // U_new for token t: U - (W S^T)[t, :] (rows 64.. of D1)
         float x[32];
         tc_ld32(lane_addr + C::kVTile * par, x);
@@ -369,7 +397,7 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
         wait(B(kBarMma3), par);
         tc_fence_after();
         tc_ld32(lane_addr + C::kVTile * par, o);
-        if (t < L) {
+        if ((!kJobs || write_out) && t < L) {
           const int64_t tok = bos + ci * kChunk + t;
           uint4* dst = reinterpret_cast<uint4*>(p.out + (tok * H + h) * kHeadDim + vc);
 #pragma unroll
@@ -384,15 +412,17 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1) kda_state_kernel(S
       if (++st == C::kStg) { st = 0; phf ^= 1u; }
     }
     // ---- final state ----
-    if (p.final_state) {
+    void* fin = kJobs ? job->fin : p.final_state;
+    const int fin_bf16 = kJobs ? job->fin_bf16 : p.final_bf16;
+    if (fin) {
       const int64_t sbase = (n * H + h) * (int64_t)(kHeadDim * kHeadDim);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const int64_t off = sbase + (int64_t)(vc + j) * kHeadDim + k;
-        if (p.final_bf16)
-          reinterpret_cast<__nv_bfloat16*>(p.final_state)[off] = __float2bfloat16_rn(s[j]);
+        if (fin_bf16)
+          reinterpret_cast<__nv_bfloat16*>(fin)[off] = __float2bfloat16_rn(s[j]);
         else
-          reinterpret_cast<float*>(p.final_state)[off] = s[j];
+          reinterpret_cast<float*>(fin)[off] = s[j];
       }
     }
   }
@@ -407,11 +437,12 @@ template <int kVT>
 static void launch_state_variant(const StateParams& p, cudaStream_t stream) {
   using C = StateCfg<kVT>;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(p.N * p.H * (kHeadDim / kVT)));
+  cfg.gridDim = dim3((unsigned)(p.N * p.H * (kHeadDim / kVT)), (unsigned)(p.njobs > 0 ? p.njobs : 1));
   cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = stream;
-  cudaLaunchKernelEx(&cfg, kda_state_kernel<kVT>, p);
+  if (p.njobs > 0) cudaLaunchKernelEx(&cfg, kda_state_kernel<kVT, true>, p);
+  else cudaLaunchKernelEx(&cfg, kda_state_kernel<kVT, false>, p);
 }
 
 // 32-column CTAs (four per head) give the shortest chunk period; 64-column
@@ -423,17 +454,63 @@ void launch_state_kernel(const StateParams& p, cudaStream_t stream, int max_ctas
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t budget = max_ctas > 0 && max_ctas < sms ? max_ctas : sms;
-  if (state_tiles(p.N * p.H, (int)budget) == 4) launch_state_variant<32>(p, stream);
+  const int64_t runs = p.N * p.H * (p.njobs > 0 ? p.njobs : 1);
+  if (state_tiles(runs, (int)budget) == 4) launch_state_variant<32>(p, stream);
   else launch_state_variant<64>(p, stream);
 }
 
 // 32-column CTAs (shortest chunk period) if all fit under max_ctas, else 64-column ones.
 int state_tiles(int64_t units, int max_ctas) { return units * 4 <= max_ctas ? 4 : 2; }
 
+// S_{g+1} = S_g M_g + R_g, fp32.  CTA (unit, row block) owns rows 16 rb .. 16 rb + 15
+// of every S_g: a row of S_{g+1} needs only the same row of S_g, so the CTAs
+// of a unit never wait for one another.  Thread = column c, rows 8 hr .. 8 hr + 7
+// of the block; M is read column by column from global memory (L2), the rows
+// of S_g from shared memory.
+__global__ void __launch_bounds__(256) kda_split_combine_kernel(const float* X, const float* R,
+                                                                const float* M, float* S,
+                                                                int64_t units, int G) {
+  __shared__ float rows[16][kHeadDim];
+  const int64_t u = blockIdx.x;
+  const int rb = blockIdx.y, c = threadIdx.x & 127, hr = threadIdx.x >> 7;
+  constexpr int64_t kMat = (int64_t)kHeadDim * kHeadDim;
+  for (int i = threadIdx.x; i < 16 * kHeadDim; i += 256)
+    rows[i / kHeadDim][i % kHeadDim] = X[u * kMat + (16 * rb + i / kHeadDim) * kHeadDim + i % kHeadDim];
+  __syncthreads();
+  for (int g = 1; g + 1 < G; ++g) {
+    const float* Mg = M + ((int64_t)(g - 1) * units + u) * kMat;
+    const float* Rg = R + ((int64_t)(g - 1) * units + u) * kMat;
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = Rg[(16 * rb + 8 * hr + i) * kHeadDim + c];
+    for (int kk = 0; kk < kHeadDim; ++kk) {
+      const float m = Mg[kk * kHeadDim + c];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(rows[8 * hr + i][kk], m, acc[i]);
+    }
+    __syncthreads();  // every thread has read rows of S_g
+    float* Sg = S + ((int64_t)(g - 1) * units + u) * kMat;  // S_{g+1}
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      rows[8 * hr + i][c] = acc[i];
+      Sg[(16 * rb + 8 * hr + i) * kHeadDim + c] = acc[i];
+    }
+    __syncthreads();
+  }
+}
+
+void launch_split_combine(const float* X, const float* R, const float* M, float* S, int64_t units,
+                          int G, cudaStream_t s) {
+  if (G < 3 || units == 0) return;
+  kda_split_combine_kernel<<<dim3((unsigned)units, 8), 256, 0, s>>>(X, R, M, S, units, G);
+}
+
 cudaError_t prepare_state_kernel() {
   const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  cudaError_t e = cudaFuncSetAttribute(kda_state_kernel<32>, attr, StateCfg<32>::kSmem);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(kda_state_kernel<64>, attr, StateCfg<64>::kSmem);
+  cudaError_t e = cudaFuncSetAttribute(kda_state_kernel<32, false>, attr, StateCfg<32>::kSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kda_state_kernel<64, false>, attr, StateCfg<64>::kSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kda_state_kernel<32, true>, attr, StateCfg<32>::kSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kda_state_kernel<64, true>, attr, StateCfg<64>::kSmem);
   return e;
 }
 

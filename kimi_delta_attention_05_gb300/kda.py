@@ -47,6 +47,16 @@ class kda_fwd_args(ctypes.Structure):
     ]
 
 
+class kda_bwd_args(ctypes.Structure):
+    _fields_ = [
+        ("fwd", kda_fwd_args),
+        ("dout", ctypes.c_void_p), ("dfinal_state", ctypes.c_void_p),
+        ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p),
+        ("dg", ctypes.c_void_p), ("dbeta", ctypes.c_void_p), ("dA_log", ctypes.c_void_p),
+        ("ddt_bias", ctypes.c_void_p), ("dinitial_state", ctypes.c_void_p),
+    ]
+
+
 _lib = None
 
 
@@ -87,6 +97,10 @@ def load_library(build_if_missing: bool = True):
         lib.kda_fwd_host_device_bytes.argtypes = [ctypes.POINTER(kda_fwd_args)]
         lib.kda_fwd_recurrent.restype = ctypes.c_int
         lib.kda_fwd_recurrent.argtypes = [ctypes.POINTER(kda_fwd_args), P]
+        lib.kda_bwd.restype = ctypes.c_int
+        lib.kda_bwd.argtypes = [ctypes.POINTER(kda_bwd_args), P, ctypes.c_size_t, P]
+        lib.kda_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.kda_bwd_workspace_bytes.argtypes = [ctypes.POINTER(kda_bwd_args)]
         _lib = lib
     return _lib
 
@@ -253,3 +267,42 @@ def kda_fwd_host_args_call(args: kda_fwd_args, device_buffer, stream) -> None:
                           ctypes.c_void_p(stream.cuda_stream))
     if rc != 0:
         raise KdaError(rc, lib.kda_error_string(rc).decode())
+
+
+def kda_bwd(q, k, v, g, beta, scale, dout, A_log=None, dt_bias=None, lower_bound=None,
+            initial_state=None, dfinal_state=None, cu_seqlens=None, *, qk_l2norm=False,
+            gate=None, beta_prob=False, workspace=None, stream=None):
+    """Backward pass through ``kda_bwd``: gradients of <out, dout> +
+    <final_state, dfinal_state> for the forward call with these arguments
+    (same conventions as :func:`kda_fwd`).  Returns a dict of fp32 device
+    tensors: q, k, v, g, beta, A_log (None unless A_log given and the gate is
+    not logspace), dt_bias (likewise), initial_state (None unless given)."""
+    lib = load_library()
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    gate_name = gate if gate is not None else ("unsafe" if lower_bound is None else "safe")
+    with torch.cuda.stream(s):
+        f32 = dict(dtype=torch.float32, device=q.device)
+        grads = {"q": torch.empty(q.shape, **f32), "k": torch.empty(k.shape, **f32),
+                 "v": torch.empty(v.shape, **f32), "g": torch.empty(g.shape, **f32),
+                 "beta": torch.empty(beta.shape, **f32)}
+        gate_params = gate_name != "logspace"
+        grads["A_log"] = torch.empty(A_log.shape, **f32) if (A_log is not None and gate_params) else None
+        grads["dt_bias"] = torch.empty(dt_bias.shape, **f32) if (dt_bias is not None and gate_params) else None
+        grads["initial_state"] = torch.empty(initial_state.shape, **f32) if initial_state is not None else None
+        a = kda_bwd_args()
+        a.fwd = make_args(q, k, v, g, beta, scale, None, A_log, dt_bias, lower_bound, initial_state,
+                          None, cu_seqlens, qk_l2norm, gate, beta_prob)
+        a.dout = _ptr(dout)
+        a.dfinal_state = _ptr(dfinal_state)
+        a.dq, a.dk, a.dv, a.dg = _ptr(grads["q"]), _ptr(grads["k"]), _ptr(grads["v"]), _ptr(grads["g"])
+        a.dbeta = _ptr(grads["beta"])
+        a.dA_log, a.ddt_bias = _ptr(grads["A_log"]), _ptr(grads["dt_bias"])
+        a.dinitial_state = _ptr(grads["initial_state"])
+        need = int(lib.kda_bwd_workspace_bytes(ctypes.byref(a)))
+        if workspace is None or workspace.numel() < need:
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    rc = lib.kda_bwd(ctypes.byref(a), ctypes.c_void_p(workspace.data_ptr()), need,
+                     ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise KdaError(rc, lib.kda_error_string(rc).decode())
+    return grads

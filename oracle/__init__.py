@@ -15,8 +15,13 @@ Two independent fp64 implementations live here:
   per-chunk intermediates (cumulative decay, A, T, W, U, P, per-chunk states)
   for debugging the GPU stages one by one.
 
-Parity status: both functions are pinned (see ``tests/test_oracle_pins.py``
-and ``tests/test_oracle_mutations.py``).
+and, for the backward pass, :func:`kda_backward`: fp64 gradients by autograd
+over a plain torch restatement of the same token recurrence
+(``backward.py``).
+
+Parity status: every function is pinned (see ``tests/test_oracle_pins.py``,
+``tests/test_oracle_mutations.py`` and ``tests/test_backward_oracle.py``).
 """
 from .recurrence import build, kda_recurrence, gate_activation, max_threads  # noqa: F401
 from .chunk_form import chunk_form  # noqa: F401
+from .backward import kda_backward, kda_forward_torch  # noqa: F401

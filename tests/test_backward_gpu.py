@@ -1,0 +1,112 @@
+"""GPU backward pass (kda_bwd) against the fp64 backward oracle.
+
+Every gradient (q, k, v, g, beta, A_log, dt_bias, initial state) element by
+element on small cases: every gate form, beta given or as logits, with and
+without the L2 norm, fp32 and bf16 initial states, a final-state gradient,
+packed sequences including empty ones, ragged lengths across the 16-token
+checkpoint blocks.  Tolerance (fp32 arithmetic from bf16 inputs; the
+recomputed states are bit-identical to the checkpoint pass): rel-RMS <= 1e-3
+and max-abs <= 1e-2 max|ref| for every gradient tensor.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kimi_delta_attention_05_gb300 import kda as K
+from kimi_delta_attention_05_gb300.workloads import WORKLOADS, make_inputs
+from tests import kda_testlib as tl
+
+pytestmark = pytest.mark.gpu
+
+GRAD_RMS = 1e-3
+GRAD_MAXABS = 1e-2
+
+
+def _check(name, x, ref):
+    assert x.shape == ref.shape, (name, x.shape, ref.shape)
+    assert np.isfinite(x).all(), name
+    r = tl.rel_rms(x, ref)
+    m = float(np.abs(x - ref).max()) if ref.size else 0.0
+    bound = GRAD_MAXABS * float(np.abs(ref).max()) if ref.size else 0.0
+    assert r <= GRAD_RMS, f"{name}: rel-RMS {r:.3e}"
+    assert m <= bound + 1e-30, f"{name}: max-abs {m:.3e} > {bound:.3e}"
+    return r
+
+
+def _run(inp, dfinal=True, tag=""):
+    gen = torch.Generator().manual_seed(123)
+    dout = (torch.randn(inp["v"].shape, generator=gen) * 0.5).to(torch.bfloat16)
+    H = inp["q"].shape[2]
+    dfin = torch.randn((inp["N"], H, 128, 128), generator=gen) * 0.1 if dfinal else None
+    d = tl.to_device(inp)
+    lb = inp["lower_bound"] if inp["gate"] == "safe" else None
+    grads = K.kda_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], inp["scale"], dout.cuda(), d["A_log"],
+                      d["dt_bias"], lb, d["initial_state"], None if dfin is None else dfin.cuda(),
+                      d["cu_seqlens"], qk_l2norm=inp["qk_l2norm"], gate=inp["gate"],
+                      beta_prob=inp.get("beta_prob", False))
+    torch.cuda.synchronize()
+    ref = oracle.kda_backward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], dout.double().numpy(),
+                              scale=inp["scale"], A_log=inp["A_log"], dt_bias=inp["dt_bias"],
+                              lower_bound=inp["lower_bound"], gate=inp["gate"],
+                              beta_prob=inp.get("beta_prob", False), qk_l2norm=inp["qk_l2norm"],
+                              initial_state=inp["initial_state"],
+                              dfinal=None if dfin is None else dfin.double().numpy(),
+                              cu_seqlens=inp["cu_seqlens"])
+    errs = {}
+    for name in ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "initial_state"):
+        if ref[name] is None:
+            assert grads.get(name) is None, name
+            continue
+        errs[name] = _check(f"{tag} d{name}", grads[name].double().cpu().numpy(), ref[name])
+    return errs
+
+
+@pytest.mark.parametrize("T", [1, 15, 16, 17, 64, 130])
+def test_backward_dense_safe(T):
+    inp = make_inputs(WORKLOADS["dense_batch"], B=2, T=T, H=2, seed=200 + T)
+    _run(inp, tag=f"safe T={T}")
+
+
+def test_backward_unsafe_no_states():
+    inp = make_inputs(WORKLOADS["long_context"], T=150, H=2, seed=210)
+    _run(inp, dfinal=False, tag="unsafe")
+
+
+def test_backward_unsafe_final_only():
+    inp = make_inputs(WORKLOADS["long_context"], T=70, H=3, seed=211)
+    _run(inp, dfinal=True, tag="unsafe dfinal")
+
+
+def test_backward_extremes_bf16_state_no_l2():
+    inp = make_inputs(WORKLOADS["extremes"], B=1, T=120, H=2, seed=212)
+    _run(inp, tag="extremes")
+
+
+def test_backward_logspace_beta_given():
+    inp = make_inputs(WORKLOADS["dense_batch"], B=1, T=90, H=2, seed=213)
+    gen = torch.Generator().manual_seed(214)
+    inp["g"] = (-(torch.randn(inp["g"].shape, generator=gen)).abs()).to(torch.bfloat16)
+    inp["beta"] = torch.sigmoid(inp["beta"].float()).to(torch.bfloat16)
+    inp.update(gate="logspace", beta_prob=True)
+    _run(inp, tag="logspace")
+
+
+def test_backward_packed_with_empty_sequences():
+    inp = make_inputs(WORKLOADS["packed_varlen"], lengths=[17, 0, 1, 40, 16], H=2, seed=215)
+    _run(inp, tag="packed")
+
+
+def test_backward_safe_without_a_log():
+    inp = make_inputs(WORKLOADS["dense_batch"], B=1, T=33, H=2, seed=216)
+    inp["A_log"] = None
+    _run(inp, tag="no A_log")
+
+
+def test_backward_rejects_bad_arguments():
+    lib = K.load_library()
+    a = K.kda_bwd_args()
+    assert lib.kda_bwd(None, None, 0, None) == 1
+    assert lib.kda_bwd_workspace_bytes(None) == 0
+    import ctypes
+    assert lib.kda_bwd(ctypes.byref(a), None, 0, None) != 0  # K = V = 0, flags 0

@@ -55,9 +55,9 @@ def _pieces_dense(inp):
 
 
 def test_dense_long_sequence_split_is_bit_exact():
-    """One long sequence in three token-range pieces: identical to kda_fwd."""
-    inp = make_inputs(WORKLOADS["long_context"], T=16384, H=4, seed=61)
-    assert _pieces_dense(inp) == 3
+    """One long sequence (eight heads) in token-range pieces: identical to kda_fwd."""
+    inp = make_inputs(WORKLOADS["long_context"], T=16384, H=8, seed=61)
+    assert _pieces_dense(inp) >= 2
     o_h, _ = _run_host(inp)
     o_d, _ = tl.run_gpu(inp)
     assert np.array_equal(o_h, o_d)
@@ -177,7 +177,7 @@ def test_g_in_fp32_through_host_entry():
     tl.check_state(f_h, rf, "host fp32 g packed")
 
 
-@pytest.mark.parametrize("gate,B,T,H", [("unsafe", 1, 16384, 4), ("safe", 2, 16500, 2)])
+@pytest.mark.parametrize("gate,B,T,H", [("unsafe", 1, 16384, 8), ("safe", 2, 16500, 4)])
 def test_stage_pipeline_is_bit_exact(gate, B, T, H):
     """Few sequence-heads and sequences of at least 256 chunks: kda_fwd
     overlaps the state stage of one token range with the intra-chunk stage of
@@ -202,10 +202,10 @@ def test_stage_pipeline_is_bit_exact(gate, B, T, H):
 
 def test_stage_pipeline_two_streams_at_once():
     """Two pipelined calls issued on two streams without ordering between them
-    (they share the library's state stream and events): each result equals the
-    same call run alone."""
-    cases = [make_inputs(WORKLOADS["long_context"], T=16384, H=4, seed=72),
-             make_inputs(WORKLOADS["extremes"], B=1, T=16500, H=3, seed=73)]
+    (each caller stream has its own second stream and events): each result
+    equals the same call run alone."""
+    cases = [make_inputs(WORKLOADS["long_context"], T=16384, H=8, seed=72),
+             make_inputs(WORKLOADS["extremes"], B=1, T=16500, H=8, seed=73)]
     alone = [tl.run_gpu(inp) for inp in cases]
     streams = [torch.cuda.Stream(), torch.cuda.Stream()]
     devs, outs, fins = [], [], []
