@@ -287,7 +287,7 @@ typedef struct kda_bwd_args {
 } kda_bwd_args;
 
 /* Device scratch for kda_bwd (state checkpoints, H * (B*T / 16 + N + 1) *
- * 64 KiB, and per-token-head records, B*T*H*1540 bytes); 0 if the forward
+ * 64 KiB, and per-token-head records, B*T*H*1552 bytes); 0 if the forward
  * arguments are invalid. */
 size_t kda_bwd_workspace_bytes(const kda_bwd_args *args);
 

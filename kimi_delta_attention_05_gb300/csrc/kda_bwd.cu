@@ -41,7 +41,11 @@ namespace kda {
 constexpr int kBwdBlock = 16;                  // tokens per checkpoint
 constexpr int kBwdWarps = 16;                  // x 8 value rows = 128
 constexpr int kBwdThreads = 32 * kBwdWarps;
-constexpr int kBwdRec = 3 * kHeadDim + 1;      // record: dq_hat, dk_hat, dD (128 each), dbeta
+// record of a token-head: dq_hat, dk_hat, dD (128 each), dbeta, padded to a
+// multiple of four floats so that every 128-float part starts 16-byte aligned
+// (the parts are read and written as float4)
+constexpr int kBwdRec = 3 * kHeadDim + 4;
+constexpr int kBwdRecBeta = 3 * kHeadDim;      // index of dbeta in a record
 
 __device__ __forceinline__ float rcp_fast_b(float x) {
   float y;
@@ -204,6 +208,7 @@ __global__ void __launch_bounds__(kBwdThreads) kda_bwd_ckpt_kernel(BwdParams p) 
 // [16], and the per-warp terms of one token's record [16 warps][kBwdRec]
 constexpr int kBwdSmK = 0, kBwdSmQ = 16 * 128, kBwdSmD = 32 * 128, kBwdSmV = 48 * 128, kBwdSmO = 64 * 128;
 constexpr int kBwdSmB = 80 * 128, kBwdSmR = 80 * 128 + 16;
+static_assert(kBwdSmR % 4 == 0 && kBwdRec % 4 == 0, "float4 access to the record rows");
 constexpr int kBwdSmem = (kBwdSmR + kBwdWarps * kBwdRec) * 4;
 
 template <int kGate, bool kL2>
@@ -348,9 +353,9 @@ __global__ void __launch_bounds__(kBwdThreads) kda_bwd_kernel(BwdParams p) {
       *reinterpret_cast<float4*>(rw + c0) = make_float4(gq[0], gq[1], gq[2], gq[3]);
       *reinterpret_cast<float4*>(rw + kHeadDim + c0) = make_float4(gk[0], gk[1], gk[2], gk[3]);
       *reinterpret_cast<float4*>(rw + 2 * kHeadDim + c0) = make_float4(gD[0], gD[1], gD[2], gD[3]);
-      if (lane == 0) rw[3 * kHeadDim] = gb;
+      if (lane == 0) rw[kBwdRecBeta] = gb;
       __syncthreads();
-      if (threadIdx.x < kBwdRec) {
+      if (threadIdx.x <= kBwdRecBeta) {
         float s = 0.f;
         for (int w = 0; w < kBwdWarps; ++w) s += sm[kBwdSmR + w * kBwdRec + threadIdx.x];
         p.rec[row * kBwdRec + threadIdx.x] = s;
@@ -451,7 +456,7 @@ __global__ void __launch_bounds__(256) kda_bwd_finalize_kernel(BwdParams p) {
     *reinterpret_cast<float4*>(p.dg + row * kHeadDim + c0) = make_float4(dg[0], dg[1], dg[2], dg[3]);
     if (lane == 0) {
       const float braw = bf16_to_f(p.beta[row]);
-      float db = rec[3 * kHeadDim];
+      float db = rec[kBwdRecBeta];
       if (!p.beta_prob) {
         const float bt = 1.0f / (1.0f + expf(-braw));
         db *= bt * (1.0f - bt);
