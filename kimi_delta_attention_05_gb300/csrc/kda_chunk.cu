@@ -647,7 +647,8 @@ __global__ void __launch_bounds__(256, 2)
   }
   // ---- A / P epilogue: lane = row of [K xr; Q xr]; rows 0..63 give A (beta-scaled,
   //      strictly lower), rows 64..127 P (lower).  Warps w and w + 4 share a lane
-  //      quarter: w < 4 the diagonal sub-block, w >= 4 the off-diagonal part ----
+  //      quarter: w < 4 the diagonal sub-block (and, for sub-chunks 2 and 3, the
+  //      first two off-diagonal pieces), w >= 4 the other off-diagonal pieces ----
   {
     const int qd = warp & 3, hw = warp >> 2;
     const int row = 32 * qd + lane;
@@ -679,27 +680,28 @@ __global__ void __launch_bounds__(256, 2)
         for (int c = 2 * r + 2; c < 8; ++c)
           *reinterpret_cast<uint4*>(gP + kmaj_off(i, 8 * c, 64)) = make_uint4(0u, 0u, 0u, 0u);
       }
-    } else {
-      // off-diagonal columns 0 .. 16 r - 1 of row i sit at tensor-memory columns
-      // 64 + 8 r (r - 1) + j; taken in 16-column pieces (column, sub-chunk, first j):
-      // quarters of sub-chunks 0, 1: (64, 1, 0); of sub-chunks 2, 3: (80, 2, 0) (96, 2, 16)
-      // (112, 3, 0) (128, 3, 16) (144, 3, 32)
-      const int npieces = (qd & 1) ? 5 : 1;
-      for (int pc = 0; pc < npieces; ++pc) {
-        const int col = (qd & 1) ? 80 + 16 * pc : 64;
-        const int blk = (qd & 1) ? (pc < 2 ? 2 : 3) : 1;
-        const int j0 = (qd & 1) ? 16 * (pc < 2 ? pc : pc - 2) : 0;
-        float a[16];
-        tc_ld16(lane_base + col, a);
-        if (r == blk) {
-          const float s = (isA ? bt : 1.f) * kOffScaleInv;
+    }
+    // off-diagonal columns 0 .. 16 r - 1 of row i sit at tensor-memory columns
+    // 64 + 8 r (r - 1) + j; taken in 16-column pieces (column, sub-chunk, first j):
+    // quarters of sub-chunks 0, 1: (64, 1, 0); of sub-chunks 2, 3: (80, 2, 0) (96, 2, 16)
+    // (112, 3, 0) (128, 3, 16) (144, 3, 32).  Sub-chunk 2's two pieces go to the warp
+    // that did the diagonal part.
+    const int pc0 = (qd & 1) ? (hw == 0 ? 0 : 2) : 0;
+    const int pc1 = (qd & 1) ? (hw == 0 ? 2 : 5) : (hw == 0 ? 0 : 1);
+    for (int pc = pc0; pc < pc1; ++pc) {
+      const int col = (qd & 1) ? 80 + 16 * pc : 64;
+      const int blk = (qd & 1) ? (pc < 2 ? 2 : 3) : 1;
+      const int j0 = (qd & 1) ? 16 * (pc < 2 ? pc : pc - 2) : 0;
+      float a[16];
+      tc_ld16(lane_base + col, a);
+      if (r == blk) {
+        const float sc = (isA ? bt : 1.f) * kOffScaleInv;
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const uint4 val = make_uint4(pack_f16(s * a[8 * c], s * a[8 * c + 1]), pack_f16(s * a[8 * c + 2], s * a[8 * c + 3]),
-                                         pack_f16(s * a[8 * c + 4], s * a[8 * c + 5]), pack_f16(s * a[8 * c + 6], s * a[8 * c + 7]));
-            if (isA) *reinterpret_cast<uint4*>(smem + kA16 + swz64(i, j0 + 8 * c)) = val;
-            else *reinterpret_cast<uint4*>(gP + kmaj_off(i, j0 + 8 * c, 64)) = val;
-          }
+        for (int c = 0; c < 2; ++c) {
+          const uint4 val = make_uint4(pack_f16(sc * a[8 * c], sc * a[8 * c + 1]), pack_f16(sc * a[8 * c + 2], sc * a[8 * c + 3]),
+                                       pack_f16(sc * a[8 * c + 4], sc * a[8 * c + 5]), pack_f16(sc * a[8 * c + 6], sc * a[8 * c + 7]));
+          if (isA) *reinterpret_cast<uint4*>(smem + kA16 + swz64(i, j0 + 8 * c)) = val;
+          else *reinterpret_cast<uint4*>(gP + kmaj_off(i, j0 + 8 * c, 64)) = val;
         }
       }
     }
@@ -724,16 +726,16 @@ __global__ void __launch_bounds__(256, 2)
     float x[kSub];
 #pragma unroll
     for (int ii = 0; ii < kSub; ++ii) {
-      float acc = 0.f;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};  // four partial sums: a short dependency chain
 #pragma unroll
       for (int s4 = 0; 4 * s4 < ii; ++s4) {  // row ii, four entries per 16-byte load
         const float4 a = Ad4[ii * 4 + s4];
         const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-          if (4 * s4 + c < ii) acc += av[c] * x[4 * s4 + c];
+          if (4 * s4 + c < ii) acc[c] += av[c] * x[4 * s4 + c];
       }
-      x[ii] = (ii == j) ? 1.f : (ii < j ? 0.f : -acc);
+      x[ii] = (ii == j) ? 1.f : (ii < j ? 0.f : -((acc[0] + acc[1]) + (acc[2] + acc[3])));
     }
 #pragma unroll
     for (int ii = 0; ii < kSub; ++ii) {

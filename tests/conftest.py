@@ -35,9 +35,14 @@ def pytest_terminal_summary(terminalreporter, exitstatus, config):
         from tests import kda_testlib as tl
     except Exception:
         return
+    tr = terminalreporter
+    if tl.GRAD_MARGINS:
+        tr.section("KDA backward margins (rel-RMS of each gradient against the fp64 autograd oracle)")
+        tr.write_line("bound: rel-RMS <= 1e-3 and max-abs <= 1e-2 max|ref| per gradient")
+        for tag, errs in tl.GRAD_MARGINS:
+            tr.write_line(f"{tag:<22} " + "  ".join(f"d{k} {v:.1e}" for k, v in errs.items()))
     if not tl.MARGINS:
         return
-    tr = terminalreporter
     tr.section("KDA parity margins (full-size workloads, every unit, against the fp64 oracle)")
     tr.write_line(f"bounds: out rel-RMS <= {tl.OUT_RMS:g}, out max-abs <= {tl.OUT_MAXABS:g} max|ref|, "
                   f"final-state rel-RMS <= {tl.STATE_RMS:g}")

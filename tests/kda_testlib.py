@@ -93,6 +93,14 @@ def record_margin(tag, out_rms, out_maxabs_ratio, worst_unit_rms, state_rms):
     MARGINS.append((tag, out_rms, out_maxabs_ratio, worst_unit_rms, state_rms))
 
 
+# Gradient errors of the backward-pass tests: (tag, {input name: rel-RMS}).
+GRAD_MARGINS = []
+
+
+def record_grad_margin(tag, errs):
+    GRAD_MARGINS.append((tag, dict(errs)))
+
+
 def unit_rows(inp, units):
     """Token rows [(b, t0, t1, h)] covered by (n*H + h) units."""
     H = inp["q"].shape[2]

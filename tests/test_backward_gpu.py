@@ -59,6 +59,7 @@ def _run(inp, dfinal=True, tag=""):
             assert grads.get(name) is None, name
             continue
         errs[name] = _check(f"{tag} d{name}", grads[name].double().cpu().numpy(), ref[name])
+    tl.record_grad_margin(tag, errs)
     return errs
 
 
