@@ -120,12 +120,13 @@ typedef struct kda_fwd_args {
  * Device scratch (bytes) that kda_fwd needs for these arguments: per-chunk
  * intermediates of the WY form (W, U, gated queries, end-decayed keys, the
  * intra-chunk read-out matrix and the chunk decay) plus the chunk index of
- * packed sequences.  For a dense call with few sequence-heads (N*H*8 at most
- * the current device's SM count) and at least 256 chunks per sequence,
- * kda_fwd splits the pass into token ranges whose intra-chunk and state stages
- * overlap on two streams; the fp32 state carried from range to range adds
- * N*H*64 KiB.  Depends on sizes, on whether cu_seqlens is given and on the
- * current device; size the workspace on the device that runs the call.
+ * packed sequences.  For a dense call with very few sequence-heads (N*H at
+ * most 7 on 152 SMs: all 2G - 1 runs of four CTAs each fit on the GPU at once
+ * for some G >= 3) and at least 64 chunks per segment, kda_fwd cuts the state
+ * stage's chain into G segments (the sequence split): the fp32 transition
+ * buffers add (3G - 3) * N*H*64 KiB.  Depends on sizes, on whether cu_seqlens
+ * is given and on the current device; size the workspace on the device that
+ * runs the call.
  * Returns 0 for argument sets that kda_fwd would reject.
  */
 size_t kda_fwd_workspace_bytes(const kda_fwd_args *args);
@@ -140,16 +141,11 @@ size_t kda_fwd_workspace_bytes(const kda_fwd_args *args);
  * (a failed launch, event or tensor-map set-up) may follow launches already
  * made by the same call.  The call only enqueues work, so it may be captured
  * into a CUDA graph: the tensor maps of the inputs travel with the launch as
- * parameters, and when the two stages overlap on the library's second stream
- * that stream joins the capture through events recorded on `stream` (tested
- * bit-identical to eager calls).  The second stream belongs to `stream` alone:
- * the library keeps one per caller stream (for up to 64 caller streams per
- * device; calls from further streams run in one pass, with the same results),
- * so a capture open on one caller stream takes in no other caller's work.
- * The first call on a device, and the first overlapped call on a caller
- * stream, which set up kernel attributes and that stream, are best made
- * outside a capture.  The per-device and per-stream set-up is kept for the
- * life of the process: do not use the library across cudaDeviceReset.
+ * parameters (tested bit-identical to eager calls).  Every kernel of a call
+ * runs on `stream`, one after another.  The first call on a device, which sets
+ * up kernel attributes, is best made outside a capture.  The per-device set-up
+ * is kept for the life of the process: do not use the library across
+ * cudaDeviceReset.
  */
 int kda_fwd(const kda_fwd_args *args, void *workspace, size_t workspace_bytes, void *stream);
 
@@ -178,8 +174,8 @@ int kda_fwd_profiled(const kda_fwd_args *args, void *workspace, size_t workspace
 int kda_fwd_recurrent(const kda_fwd_args *args, void *stream);
 
 /* Number of kernel launches kda_fwd makes for these arguments on the current
- * device (0 if none or if the arguments are invalid): 2 or 3 for one pass,
- * 2 per token range when the pass is split into token ranges (see
+ * device (0 if none or if the arguments are invalid): 2 or 3 for one pass
+ * (3 with cu_seqlens: the chunk index scan), 4 for the sequence split (see
  * kda_fwd_workspace_bytes). */
 int kda_fwd_launches(const kda_fwd_args *args);
 
@@ -307,12 +303,11 @@ int kda_bwd(const kda_bwd_args *args, void *workspace, size_t workspace_bytes, v
  * KDA_ERR_BAD_SEQLENS if a call's cu_seqlens values were inconsistent.
  *
  *  - One status word per (device, stream): every kernel of a call reports into
- *    the word of the stream the call was enqueued on (also the stages that run
- *    on the library's second stream), so calls on different streams never see,
- *    overwrite or clear each other's codes.  The words come from a table of
- *    1023 slots built into the library; a stream takes a slot on its first
- *    call and keeps it, and the streams beyond the 1023rd distinct handle on a
- *    device share one further slot.  Two host threads using the per-thread
+ *    the word of the stream the call was enqueued on, so calls on different
+ *    streams never see, overwrite or clear each other's codes.  The words come
+ *    from a table of 1023 slots built into the library; a stream takes a slot
+ *    on its first call and keeps it, and the streams beyond the 1023rd
+ *    distinct handle on a device share one further slot.  Two host threads using the per-thread
  *    default stream handle (cudaStreamPerThread) share a word.
  *  - Sticky until read: the call synchronises `stream`, returns its word as it
  *    stands after all work enqueued on it so far (the last code set wins) and

@@ -3,9 +3,6 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
-#include <memory>
-#include <mutex>
-#include <unordered_map>
 
 #include "../../include/kda.h"
 #include "kda_common.cuh"
@@ -128,11 +125,6 @@ int validate(const kda_fwd_args* a, int64_t* num_slots, size_t* header_bytes) {
 
 using namespace kda;
 
-#ifndef KDA_PIPE_RANGES
-#define KDA_PIPE_RANGES 6
-#endif
-static_assert(KDA_PIPE_RANGES >= 1 && KDA_PIPE_RANGES <= 8, "pipeline ranges");
-
 namespace {
 
 int device_sms() {
@@ -145,33 +137,8 @@ int device_sms() {
   return sms;
 }
 
-// CTAs the state stage may hold while the intra-chunk stage of the next token
-// range runs beside it: half the SMs, in four 32-column CTAs per head; 0: no
-// overlap.  Measured on B1 T8192 H32, where they do not fit: with 64-column
-// CTAs (64 SMs) 0.314 -> 0.309 ms, within run-to-run noise; with one
-// 128-column CTA per head (32 SMs, 120 left to the intra-chunk stage; 16
-// epilogue warps per SM) 0.305 -> 0.365 ms, its chunk period being about
-// twice as long.
-int pipe_state_budget(int64_t units, int sms) { return units * 4 * 2 <= sms ? sms / 2 : 0; }
-
-// Token ranges a dense pass is cut into (every range of every sequence, whole
-// chunks), so that the state stage of range r, on a second stream, overlaps
-// the intra-chunk stage of range r + 1 on the SMs it leaves free:
-// for few sequence-heads (above) and sequences of at least 256 chunks;
-// otherwise 1.  Measured, ms per call by ranges 1 / 3 / 4 / 6 / 8: B2 T32768 H8
-// 0.699 / 0.651 / 0.612 / 0.580 / 0.608, the same with H4 0.563 / 0.534 /
-// 0.517 / 0.513 / 0.528; with 128 chunks per sequence (T8192, H16 or H8) no
-// range count beats one pass (H8: 0.155 against 0.162 at 4 ranges).
-constexpr int64_t kPipeMinChunks = 256;
-int pipeline_ranges(const kda_fwd_args* a, int sms) {
-  if (a->cu_seqlens || sms <= 0) return 1;
-  const int64_t units = a->N * a->H;
-  if (units == 0 || pipe_state_budget(units, sms) == 0) return 1;
-  if (ceil_div(a->T, kChunk) < kPipeMinChunks) return 1;
-  return KDA_PIPE_RANGES;
-}
-
-size_t carry_bytes(const kda_fwd_args* a) { return (size_t)(a->N * a->H) * kHeadDim * kHeadDim * 4; }
+// bytes of one fp32 [N * H][128][128] state buffer
+size_t state_mat_bytes(const kda_fwd_args* a) { return (size_t)(a->N * a->H) * kHeadDim * kHeadDim * 4; }
 
 // Sequence split inside one GPU (dense calls with very few sequence-heads):
 // the state stage's chain over C chunks is cut into G segments.  The state
@@ -201,53 +168,7 @@ int split_segments(const kda_fwd_args* a, int sms) {
 }
 // fp32 [units][128][128] buffers of a split pass: X (segment 0's final state),
 // R_g and M_g for g = 1 .. G-1, S_g for g = 2 .. G-1.
-size_t split_bytes(const kda_fwd_args* a, int G) { return G > 1 ? (size_t)(3 * G - 3) * carry_bytes(a) : 0; }
-
-// Second stream and events of the pipelined pass, one set per caller stream: the state stages of a call run on its caller's own
-// second stream, so calls from different caller streams never share one (a
-// capture open on one caller stream cannot take in another caller's work, and
-// unrelated callers do not queue behind each other).
-struct PipeCtx {
-  std::mutex mu;
-  bool ready = false;
-  cudaStream_t state_stream = nullptr;
-  cudaEvent_t start = nullptr, end = nullptr, chunked[KDA_PIPE_RANGES] = {};
-};
-// At most this many caller streams per device get a second stream (kept until
-// the process exits); calls from further streams run in one pass.
-constexpr size_t kMaxPipeStreams = 64;
-struct PipeTable {
-  std::mutex mu;
-  std::unordered_map<uintptr_t, std::unique_ptr<PipeCtx>> ctx;
-};
-PipeTable g_pipes[kMaxDevices];
-
-// The second stream has the default priority: a stream of greater priority may
-// preempt running CTAs of the intra-chunk stage, which hold tensor-memory
-// columns, while the state stage's CTAs wait to allocate theirs.
-bool make_pipe_ctx(PipeCtx& c) {
-  if (c.ready) return true;
-  if (cudaStreamCreateWithFlags(&c.state_stream, cudaStreamNonBlocking) != cudaSuccess) return false;
-  const unsigned ef = cudaEventDisableTiming;
-  if (cudaEventCreateWithFlags(&c.start, ef) != cudaSuccess) return false;
-  if (cudaEventCreateWithFlags(&c.end, ef) != cudaSuccess) return false;
-  for (auto& e : c.chunked)
-    if (cudaEventCreateWithFlags(&e, ef) != cudaSuccess) return false;
-  c.ready = true;
-  return true;
-}
-
-// The pipelined-pass context of caller stream `s` on device `dev`, made on
-// first use; nullptr once the table is full.
-PipeCtx* pipe_ctx(int dev, cudaStream_t s) {
-  PipeTable& t = g_pipes[dev];
-  std::lock_guard<std::mutex> lock(t.mu);
-  const uintptr_t key = s == cudaStreamLegacy ? (uintptr_t)0 : reinterpret_cast<uintptr_t>(s);
-  auto it = t.ctx.find(key);
-  if (it != t.ctx.end()) return it->second.get();
-  if (t.ctx.size() >= kMaxPipeStreams) return nullptr;
-  return t.ctx.emplace(key, std::make_unique<PipeCtx>()).first->second.get();
-}
+size_t split_bytes(const kda_fwd_args* a, int G) { return G > 1 ? (size_t)(3 * G - 3) * state_mat_bytes(a) : 0; }
 
 }  // namespace
 
@@ -257,23 +178,20 @@ extern "C" size_t kda_fwd_workspace_bytes(const kda_fwd_args* args) {
   if (validate(args, &slots, &header) != KDA_OK) return 0;
   const size_t ws = header + (size_t)slots * (size_t)args->H * (size_t)kSlotBytes;
   const int sms = device_sms();
-  const int G = split_segments(args, sms);
-  if (G > 1) return ws + split_bytes(args, G);
-  return ws + (pipeline_ranges(args, sms) > 1 ? carry_bytes(args) : 0);
+  return ws + split_bytes(args, split_segments(args, sms));
 }
 
 int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_bytes,
                     cudaStream_t stream, void* const* events, int init_bf16, int final_bf16,
-                    bool allow_pipeline) {
+                    bool allow_split) {
   int64_t slots = 0;
   size_t header = 0;
   int rc = validate(a, &slots, &header);
   if (rc != KDA_OK) return rc;
   if (a->N == 0 || a->H == 0) return KDA_OK;
-  const int G = allow_pipeline ? split_segments(a, device_sms()) : 1;
-  int ranges = allow_pipeline && G == 1 ? pipeline_ranges(a, device_sms()) : 1;
+  const int G = allow_split ? split_segments(a, device_sms()) : 1;
   const size_t slot_bytes = (size_t)slots * (size_t)a->H * (size_t)kSlotBytes;
-  const size_t need = header + slot_bytes + (G > 1 ? split_bytes(a, G) : (ranges > 1 ? carry_bytes(a) : 0));
+  const size_t need = header + slot_bytes + split_bytes(a, G);
   if (need > 0 && (!workspace || !aligned(workspace, 256) || workspace_bytes < need))
     return KDA_ERR_WORKSPACE;
   int dev = 0;
@@ -286,13 +204,10 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
   // every kernel of this call reports into the status word of the caller's stream
   int* status = status_slot(stream);
   if (!status) return KDA_ERR_LAUNCH;
-  PipeCtx* pipe = ranges > 1 ? pipe_ctx(dev, stream) : nullptr;
-  if (!pipe) ranges = 1;  // (workspace sized for the pipelined pass is large enough for one pass)
 
   unsigned char* ws = reinterpret_cast<unsigned char*>(workspace);
   int64_t* chunk_off = a->cu_seqlens ? reinterpret_cast<int64_t*>(ws) : nullptr;
   unsigned char* slots_base = ws + header;
-  void* carry = ws + header + slot_bytes;
   const int sb16 = a->state_dtype == KDA_DTYPE_BF16 ? 1 : 0;
   const int ib16 = init_bf16 >= 0 ? init_bf16 : sb16, fb16 = final_bf16 >= 0 ? final_bf16 : sb16;
 
@@ -300,21 +215,16 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
   auto mark = [&](int i) {
     if (events && events[i]) cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), stream);
   };
-  // The two stages over token range [t0, t0 + span) of every sequence (dense), or
-  // over the whole call (packed); the range's chunks take their own workspace slots.
-  auto launch_chunks = [&](int64_t t0, int64_t span, unsigned char* ws_r, cudaStream_t s,
-                           int busy_sms) {
-    const int64_t nt = ceil_div(span, kChunk);
-    const int64_t nslots = a->cu_seqlens ? slots : a->B * nt;
-    if (nslots == 0) return;
-    const int64_t r0 = t0 * a->H * kHeadDim;  // element offset of the range's first row
+  // The intra-chunk stage over the whole call: every chunk takes its own workspace slot.
+  auto launch_chunks = [&]() {
+    if (slots == 0) return;
     ChunkParams cp;
-    cp.q = static_cast<const uint16_t*>(a->q) + r0;
-    cp.k = static_cast<const uint16_t*>(a->k) + r0;
-    cp.v = static_cast<const uint16_t*>(a->v) + r0;
-    cp.g = static_cast<const uint16_t*>(a->g) + r0;
-    cp.g32 = (a->flags & KDA_G_FP32) ? static_cast<const float*>(a->g) + r0 : nullptr;
-    cp.beta = static_cast<const uint16_t*>(a->beta) + t0 * a->H;
+    cp.q = static_cast<const uint16_t*>(a->q);
+    cp.k = static_cast<const uint16_t*>(a->k);
+    cp.v = static_cast<const uint16_t*>(a->v);
+    cp.g = static_cast<const uint16_t*>(a->g);
+    cp.g32 = (a->flags & KDA_G_FP32) ? static_cast<const float*>(a->g) : nullptr;
+    cp.beta = static_cast<const uint16_t*>(a->beta);
     cp.A_log = a->A_log;
     cp.dt_bias = a->dt_bias;
     cp.lower_bound = a->lower_bound;
@@ -325,20 +235,18 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
     cp.cu = a->cu_seqlens;
     cp.chunk_off = chunk_off;
     cp.N = a->N;
-    cp.T = span;
+    cp.T = a->T;
     cp.H = a->H;
-    cp.NT = nt;
+    cp.NT = ceil_div(a->T, kChunk);
     cp.ld = a->T;
-    cp.ws = ws_r;
+    cp.ws = slots_base;
     cp.status = status;
-    if (!launch_chunk_kernel(cp, nslots, s, busy_sms)) maps_ok = false;
+    if (!launch_chunk_kernel(cp, slots, stream)) maps_ok = false;
   };
-  auto launch_state = [&](int64_t t0, int64_t span, unsigned char* ws_r, const void* init,
-                          void* fin, int ib, int fb, cudaStream_t s) {
-    const int64_t r0 = t0 * a->H * kHeadDim;
+  auto launch_state = [&](const void* init, void* fin, int ib, int fb) {
     StateParams sp;
     sp.njobs = 0;
-    sp.out = static_cast<uint16_t*>(a->out) + (a->out ? r0 : 0);
+    sp.out = static_cast<uint16_t*>(a->out);
     sp.init = init;
     sp.final_state = fin;
     sp.init_bf16 = ib;
@@ -347,13 +255,13 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
     sp.cu = a->cu_seqlens;
     sp.chunk_off = chunk_off;
     sp.N = a->N;
-    sp.T = span;
+    sp.T = a->T;
     sp.H = a->H;
-    sp.NT = ceil_div(span, kChunk);
+    sp.NT = ceil_div(a->T, kChunk);
     sp.ld = a->T;
-    sp.ws = ws_r;
+    sp.ws = slots_base;
     sp.status = status;
-    launch_state_kernel(sp, s, ranges > 1 ? pipe_state_budget(a->N * a->H, device_sms()) : 0);
+    launch_state_kernel(sp, stream);
   };
   // The split pass (see split_segments): runs of the state stage as jobs of one launch.
   auto launch_split = [&]() {
@@ -399,62 +307,22 @@ int kda::fwd_device(const kda_fwd_args* a, void* workspace, size_t workspace_byt
       sp.jobs[2 * g - 1] = job(g, nullptr, 0, 0, R + (size_t)(g - 1) * mat, 0, 0, 0);
       sp.jobs[2 * g] = job(g, nullptr, 2, 0, M + (size_t)(g - 1) * mat, 0, 1, 0);
     }
-    launch_state_kernel(sp, stream, 0);
+    launch_state_kernel(sp, stream);
     launch_split_combine(X, R, M, S, units, G, stream);
     sp.njobs = G - 1;  // segments 1 .. G-1 from their true initial states, with the outputs
     for (int g = 1; g < G; ++g)
       sp.jobs[g - 1] = job(g, g == 1 ? X : S + (size_t)(g - 2) * mat, 1, 0,
                            g == G - 1 ? a->final_state : nullptr, fb16, 0, 1);
-    launch_state_kernel(sp, stream, 0);
+    launch_state_kernel(sp, stream);
   };
 
-  if (G > 1) {
-    mark(0);
-    launch_chunks(0, a->T, slots_base, stream, 0);
-    mark(1);
-    launch_split();
-    mark(2);
-  } else if (ranges == 1) {
-    mark(0);
-    if (a->cu_seqlens)
-      launch_chunk_offsets(a->cu_seqlens, a->N, a->T, chunk_off, status, stream);
-    launch_chunks(0, a->T, slots_base, stream, 0);
-    mark(1);
-    launch_state(0, a->T, slots_base, a->initial_state, a->final_state, ib16, fb16, stream);
-    mark(2);
-  } else {
-    // chunk stage of range r on the caller's stream, state stage on the
-    // second stream after it; the fp32 state passes from range to range
-    PipeCtx& c = *pipe;
-    std::lock_guard<std::mutex> lock(c.mu);
-    if (!make_pipe_ctx(c)) return KDA_ERR_LAUNCH;
-    const int64_t span = ceil_div(ceil_div(a->T, kChunk), ranges) * kChunk;
-    bool ok = true;
-    auto chk = [&](cudaError_t e) { ok = ok && e == cudaSuccess; };
-    mark(0);
-    chk(cudaEventRecord(c.start, stream));
-    chk(cudaStreamWaitEvent(c.state_stream, c.start, 0));
-    unsigned char* ws_r = slots_base;
-    int r = 0;
-    for (int64_t t0 = 0; t0 < a->T; t0 += span, ++r) {
-      const int64_t len = std::min(span, a->T - t0);
-      const bool first = t0 == 0, last = t0 + len == a->T;
-      // from the second range on, the previous range's state stage holds its SMs
-      const int budget = pipe_state_budget(a->N * a->H, device_sms());
-      const int state_ctas = (int)(a->N * a->H) * state_tiles(a->N * a->H, budget);
-      launch_chunks(t0, len, ws_r, stream, first ? 0 : state_ctas);
-      chk(cudaEventRecord(c.chunked[r], stream));
-      chk(cudaStreamWaitEvent(c.state_stream, c.chunked[r], 0));
-      launch_state(t0, len, ws_r, first ? a->initial_state : carry, last ? a->final_state : carry,
-                   first ? ib16 : 0, last ? fb16 : 0, c.state_stream);
-      ws_r += (size_t)(a->B * ceil_div(len, kChunk) * a->H) * kSlotBytes;
-    }
-    mark(1);
-    chk(cudaEventRecord(c.end, c.state_stream));
-    chk(cudaStreamWaitEvent(stream, c.end, 0));
-    mark(2);
-    if (!ok) return KDA_ERR_LAUNCH;
-  }
+  mark(0);
+  if (a->cu_seqlens) launch_chunk_offsets(a->cu_seqlens, a->N, a->T, chunk_off, status, stream);
+  launch_chunks();
+  mark(1);
+  if (G > 1) launch_split();
+  else launch_state(a->initial_state, a->final_state, ib16, fb16);
+  mark(2);
   if (!maps_ok || cudaGetLastError() != cudaSuccess) return KDA_ERR_LAUNCH;
   return KDA_OK;
 }
@@ -512,11 +380,6 @@ extern "C" int kda_fwd_launches(const kda_fwd_args* a) {
   size_t header = 0;
   if (validate(a, &slots, &header) != KDA_OK || a->N == 0 || a->H == 0) return 0;
   if (split_segments(a, device_sms()) > 1) return 4;  // chunk, state, combine, state
-  const int ranges = pipeline_ranges(a, device_sms());
-  if (ranges > 1) {  // one chunk and one state launch per token range
-    const int64_t span = ceil_div(ceil_div(a->T, kChunk), ranges) * kChunk;
-    return (int)(2 * ceil_div(a->T, span));
-  }
   return 1 + (slots > 0 ? 1 : 0) + (a->cu_seqlens ? 1 : 0);
 }
 

@@ -861,8 +861,7 @@ bool encode_input_map(CUtensorMap* m, const void* base, int64_t H, int64_t rows)
 }
 }  // namespace
 
-bool launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t stream,
-                         int busy_sms) {
+bool launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t stream) {
   // the rows the kernel may touch from the row pointers: every sequence's
   // range (dense), or the packed tokens
   const int64_t rows = p.cu ? p.T : (p.N - 1) * p.ld + p.T;
@@ -872,13 +871,12 @@ bool launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t s
       !encode_input_map(&maps.v, p.v, p.H, rows) || (!p.g32 && !encode_input_map(&maps.g, p.g, p.H, rows)))
     return false;
   // persistent grid: two CTAs per SM (shared memory, registers and tensor-memory
-  // columns all allow two) on the SMs another kernel does not hold, or fewer items
+  // columns all allow two), or fewer items
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t items = num_slots * p.H;
-  const int free_sms = sms - busy_sms > 0 ? sms - busy_sms : 1;
-  const unsigned grid = (unsigned)min(items, (int64_t)(2 * free_sms));
+  const unsigned grid = (unsigned)min(items, (int64_t)(2 * (sms > 0 ? sms : 1)));
   const bool l2 = p.l2norm != 0;
   switch (p.gate_mode) {
     case kGateUnsafe:

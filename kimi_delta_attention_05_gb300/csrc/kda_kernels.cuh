@@ -134,19 +134,17 @@ void launch_chunk_offsets(const int64_t* cu, int64_t N, int64_t T, int64_t* chun
 // Device address of the status word of stream `s` on the current device (a
 // slot of the library's table, assigned on the stream's first use), or nullptr.
 int* status_slot(cudaStream_t s);
-// busy_sms: SMs held by a kernel running alongside (the persistent grid covers the rest).
-// false if the inputs' tensor maps cannot be made (nothing launched).
-bool launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t s, int busy_sms = 0);
-// max_ctas: at most this many CTAs at once (0: the SM count) picks the
-// 32-column shape (four CTAs per head) if they fit, else the 64-column one
-void launch_state_kernel(const StateParams& p, cudaStream_t s, int max_ctas = 0);
+// Persistent grid of two CTAs per SM (or fewer items); false if the inputs'
+// tensor maps cannot be made (nothing launched).
+bool launch_chunk_kernel(const ChunkParams& p, int64_t num_slots, cudaStream_t s);
+// The 32-column shape (four CTAs per head) if all CTAs fit on the GPU at once
+// (one per SM), else the 64-column one.
+void launch_state_kernel(const StateParams& p, cudaStream_t s);
 // Chains the segment transitions of a split pass for `units` (sequence, head)
 // pairs: S_1 = X, S_{g+1} = S_g M_g + R_g for g = 1 .. G - 2, into S (S_2 .. S_{G-1});
 // all fp32 [units][128][128], R and M indexed g - 1.
 void launch_split_combine(const float* X, const float* R, const float* M, float* S, int64_t units,
                           int G, cudaStream_t s);
-// CTAs per head the state stage uses for `units` (sequence, head) pairs under max_ctas
-int state_tiles(int64_t units, int max_ctas);
 cudaError_t prepare_chunk_kernel();
 cudaError_t prepare_state_kernel();
 

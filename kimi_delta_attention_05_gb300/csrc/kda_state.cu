@@ -228,8 +228,12 @@ __global__ void __launch_bounds__(StateCfg<kVT>::kThreads, 1)
       issued = it + 1;
       st = st + 1 == C::kStg ? 0 : st + 1;
     }
-    if (*s_abort && lane == 0)  // after a timeout: let this CTA's issued copies land before leaving
-      for (int64_t c = 0; c < issued; ++c)
+    // After a timeout: let the copies still in flight land before leaving.  Only
+    // the last kStg can be: an earlier copy's stage was reused, so its own full
+    // phase completed before the reuse was issued (and waiting on its parity
+    // again could alias a later phase and spend the whole limit).
+    if (*s_abort && lane == 0)
+      for (int64_t c = issued > C::kStg ? issued - C::kStg : 0; c < issued; ++c)
         mbar_wait_bounded(B(kBarFull + (int)(c % C::kStg)), (uint32_t)((c / C::kStg) & 1));
   } else if (warp == C::kMmaWarp) {
     // ---- tensor-core issuer: the whole warp keeps step with the named barriers
@@ -449,18 +453,14 @@ static void launch_state_variant(const StateParams& p, cudaStream_t stream) {
 // CTAs (two per head) halve the bytes all CTAs of a head pull through their SM
 // ports per chunk.  So: four per head while they fit on the GPU at once (one
 // CTA per SM), two per head once they would run in more than one wave.
-void launch_state_kernel(const StateParams& p, cudaStream_t stream, int max_ctas) {
+void launch_state_kernel(const StateParams& p, cudaStream_t stream) {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t budget = max_ctas > 0 && max_ctas < sms ? max_ctas : sms;
   const int64_t runs = p.N * p.H * (p.njobs > 0 ? p.njobs : 1);
-  if (state_tiles(runs, (int)budget) == 4) launch_state_variant<32>(p, stream);
+  if (runs * 4 <= sms) launch_state_variant<32>(p, stream);
   else launch_state_variant<64>(p, stream);
 }
-
-// 32-column CTAs (shortest chunk period) if all fit under max_ctas, else 64-column ones.
-int state_tiles(int64_t units, int max_ctas) { return units * 4 <= max_ctas ? 4 : 2; }
 
 // S_{g+1} = S_g M_g + R_g, fp32.  CTA (unit, row block) owns rows 16 rb .. 16 rb + 15
 // of every S_g: a row of S_{g+1} needs only the same row of S_g, so the CTAs

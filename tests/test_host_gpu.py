@@ -178,12 +178,11 @@ def test_g_in_fp32_through_host_entry():
 
 
 @pytest.mark.parametrize("gate,B,T,H", [("unsafe", 1, 16384, 8), ("safe", 2, 16500, 4)])
-def test_stage_pipeline_is_bit_exact(gate, B, T, H):
-    """Few sequence-heads and sequences of at least 256 chunks: kda_fwd
-    overlaps the state stage of one token range with the intra-chunk stage of
-    the next on two streams, carrying the state in fp32.  The host entry runs
-    the same problem without that overlap (its token pieces carry the state
-    in fp32 at other chunk boundaries): the results are identical."""
+def test_host_pieces_match_one_pass(gate, B, T, H):
+    """Few sequence-heads and sequences of at least 256 chunks: the host entry
+    cuts the tokens into pieces whose state passes from piece to piece in
+    fp32; kda_fwd runs the same problem in one pass, its state never leaving
+    fp32 between chunks either: the results are identical."""
     inp = make_inputs(WORKLOADS["dense_batch"], B=B, T=T, H=H, seed=71)
     inp.update(gate=gate)
     d = tl.to_device(inp)
@@ -191,19 +190,18 @@ def test_stage_pipeline_is_bit_exact(gate, B, T, H):
                   d["A_log"], d["dt_bias"], inp["lower_bound"] if gate == "safe" else None,
                   d["initial_state"], None, None, inp["qk_l2norm"], gate)
     from kimi_delta_attention_05_gb300 import kda as K
-    assert K.load_library().kda_fwd_launches(ctypes.byref(a)) == 12  # 6 token ranges x 2 stages
+    assert K.load_library().kda_fwd_launches(ctypes.byref(a)) == 2  # one pass
     o_h, f_h = _run_host(inp)
     o_d, f_d = tl.run_gpu(inp)
     assert np.array_equal(o_h, o_d) and np.array_equal(f_h, f_d)
     ro, rf = tl.run_oracle(inp)
-    tl.check_out(o_d, ro, "pipelined stages")
-    tl.check_state(f_d, rf, "pipelined stages")
+    tl.check_out(o_d, ro, "one pass, 256 chunks")
+    tl.check_state(f_d, rf, "one pass, 256 chunks")
 
 
-def test_stage_pipeline_two_streams_at_once():
-    """Two pipelined calls issued on two streams without ordering between them
-    (each caller stream has its own second stream and events): each result
-    equals the same call run alone."""
+def test_two_streams_at_once():
+    """Two calls issued on two streams without ordering between them: each
+    result equals the same call run alone."""
     cases = [make_inputs(WORKLOADS["long_context"], T=16384, H=8, seed=72),
              make_inputs(WORKLOADS["extremes"], B=1, T=16500, H=8, seed=73)]
     alone = [tl.run_gpu(inp) for inp in cases]
