@@ -91,6 +91,11 @@ constexpr int kSm = kKc + 2 * kKcHalf;  // 106496
 // exact product, then the clamped one (written by the gate stage, read by the
 // operand stage; no other stage touches them)
 constexpr int kCsDec = kSm;
+// While the A / P product of an item runs (the decay products are dead), the
+// next item's per-head gate inputs and beta inputs are staged here: fp32
+// dt_bias [128], beta [64], A_log; read at the next item's start, before the
+// gate stage writes the decay products.
+constexpr int kStg = kCsDec;
 __device__ __forceinline__ int cs_exact(int seg) { return kCsDec + seg * 1024; }
 __device__ __forceinline__ int cs_clamped(int seg) { return kCsDec + seg * 1024 + 512; }
 constexpr int kCsBeta = kSm + 8192;     // fp32 [64]
@@ -299,11 +304,12 @@ __global__ void __launch_bounds__(256, 2)
     tc_fence_after();
   };
   // rows L..63 copied past a short chunk's end (the next sequence's rows, or
-  // zeros past the view) are cleared: the stages below expect zeros
-  auto zero_tails = [&](int L) {
+  // zeros past the view) are cleared: the stages below expect zeros.  Tiles
+  // 0, 1: k and q; 2, 3: g and v.
+  auto zero_tails = [&](int L, int tile0) {
     const int n = (kChunk - L) * 16;  // 16-byte chunks per tile
-    for (int idx = tid; idx < 4 * n; idx += 256) {
-      const int tile = idx / n, e = idx - tile * n;
+    for (int idx = tid; idx < 2 * n; idx += 256) {
+      const int tile = tile0 + (idx >= n), e = idx - (idx >= n ? n : 0);
       const int t = L + (e >> 4), c = 8 * (e & 15);
       uint32_t off;
       if (tile == 0) off = kRo + kmaj_off(t, c, 128);
@@ -313,14 +319,59 @@ __global__ void __launch_bounds__(256, 2)
       *reinterpret_cast<uint4*>(smem + off) = make_uint4(0u, 0u, 0u, 0u);
     }
   };
-  // beta input (logit, or beta itself) of token tid; 0 past the chunk end
-  auto load_beta = [&](const Item& it) {
-    return tid < it.L ? bf16_to_f(p.beta[(it.t0 + tid) * H + it.h]) : 0.f;
-  };
-
   int64_t item = blockIdx.x;
   if (item >= num_items) return;
   Item cur = locate(item);
+  float* sBeta = reinterpret_cast<float*>(smem + kCsBeta);
+  float* sRq = reinterpret_cast<float*>(smem + kCsRq);
+  float* sRk = reinterpret_cast<float*>(smem + kCsRk);
+  float* sStg = reinterpret_cast<float*>(smem + kStg);
+  // an item's per-head gate inputs and beta inputs into the staging area, by
+  // threads 64.. (u = tid - 64: dt_bias u < 32, A_log u = 32, beta 64 <= u < 128)
+  auto stage_scalars = [&](const Item& x) {
+    const int u = tid - 64;
+    if (u >= 0 && u < 32)
+      *reinterpret_cast<float4*>(sStg + 4 * u) =
+          (p.dt_bias && kGate != kGateLogspace)
+              ? __ldg(reinterpret_cast<const float4*>(p.dt_bias + x.h * kHeadDim) + u)
+              : make_float4(0.f, 0.f, 0.f, 0.f);
+    else if (u == 32)
+      sStg[192] = (p.A_log && kGate != kGateLogspace) ? __ldg(p.A_log + x.h) : 0.f;
+    else if (u >= 64 && u < 64 + kChunk)
+      sStg[128 + u - 64] = u - 64 < x.L ? bf16_to_f(p.beta[(x.t0 + u - 64) * H + x.h]) : 0.f;
+  };
+  // An item's q and k rows once their copy has landed (parity of its phase):
+  // rows past its end cleared, then the reciprocal norms 1 / sqrt(|x|^2 + eps)
+  // (1 without the L2 norm) into sRk / sRq: two threads per row, 64 channels
+  // each, fp32 sums of the bf16 squares (16-byte chunks taken in swizzled
+  // order, so the eight rows of a group read eight different bank groups).
+  auto prep_rows = [&](const Item& x, uint32_t parity) {
+    wait_bar(bar_qk, parity);
+    if (x.L < kChunk) zero_tails(x.L, 0);
+    if (kL2) {
+      __syncthreads();  // the cleared rows are read below
+      const int row = tid >> 1, hh = tid & 1;
+      const unsigned char* src = smem + kRo + hh * 16384 + row * 128;
+      float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 w = *reinterpret_cast<const uint4*>(src + 16 * (c ^ (row & 7)));
+        const uint32_t ws4[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = f2u(bf2_to_f2(ws4[e]));
+          acc.x = fmaf(f.x, f.x, acc.x);
+          acc.y = fmaf(f.y, f.y, acc.y);
+        }
+      }
+      float ss = acc.x + acc.y;
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      if (hh == 0) (row < 64 ? sRk : sRq)[row & 63] = rsqrtf(ss + 1e-6f);
+    } else if (tid < 128) {
+      (tid < 64 ? sRk : sRq)[tid & 63] = 1.0f;
+    }
+  };
+  stage_scalars(cur);
   if (tid == 0) {
     mbar_init(bar_qk, 1);
     mbar_init(bar_gv, 1);
@@ -341,20 +392,7 @@ __global__ void __launch_bounds__(256, 2)
     copy_qk(cur);
     copy_gv(cur);
   }
-  float blogit = tid < kChunk ? load_beta(cur) : 0.f;
-  // per-head gate inputs of this thread's four channels (loaded one item ahead)
-  const int c0g = 4 * (tid & 31);
-  auto load_dtb = [&](const Item& it) {
-    return (p.dt_bias && kGate != kGateLogspace)
-               ? *reinterpret_cast<const float4*>(p.dt_bias + it.h * kHeadDim + c0g)
-               : make_float4(0.f, 0.f, 0.f, 0.f);
-  };
-  auto load_alog = [&](const Item& it) { return (p.A_log && kGate != kGateLogspace) ? p.A_log[it.h] : 0.f; };
-  float4 dtb_next = load_dtb(cur);
-  float alog_next = load_alog(cur);
-  float* sBeta = reinterpret_cast<float*>(smem + kCsBeta);
-  float* sRq = reinterpret_cast<float*>(smem + kCsRq);
-  float* sRk = reinterpret_cast<float*>(smem + kCsRk);
+  prep_rows(cur, 0u);
   // exact product of half s2, clamped products of the first (Xm) and second
   // (Ym) half of sub-chunk r, channels c .. c + 3
   auto ld_exact = [&](int s2, int c) { return *reinterpret_cast<const float4*>(smem + cs_exact(s2) + c * 4); };
@@ -374,33 +412,20 @@ __global__ void __launch_bounds__(256, 2)
   const int h = cur.h;
   unsigned char* ws = p.ws + (cur.slot * H + h) * (int64_t)kSlotBytes;
   const int64_t next = item + gridDim.x;
-  Item nxt = cur;
-  if (next < num_items) nxt = locate(next);
-  const float4 dtb = dtb_next;
-  const float alog = alog_next;
-  if (next < num_items) {
-    dtb_next = load_dtb(nxt);
-    alog_next = load_alog(nxt);
+  Item nxt = cur;  // located while the A / P product runs
+  // this item's staged per-head gate inputs (this thread's four channels) and beta
+  const float4 dtb = *reinterpret_cast<const float4*>(sStg + 4 * (tid & 31));
+  const float alog = sStg[192];
+  if (tid < kChunk) {
+    const float bl = sStg[128 + tid];
+    sBeta[tid] = tid >= L ? 0.f : (p.beta_prob ? bl : rcp_approx(1.0f + ex2(-bl * kLog2e)));
   }
-  if (tid < kChunk)
-    sBeta[tid] = tid >= L ? 0.f : (p.beta_prob ? blogit : rcp_approx(1.0f + ex2(-blogit * kLog2e)));
-  wait_bar(bar_qk, (uint32_t)(it & 1));
+  wait_bar(bar_qk, (uint32_t)(it & 1));  // (also waited on, and rows prepared, one item ahead)
   wait_bar(bar_gv, (uint32_t)(it & 1));
-  if (L < kChunk) zero_tails(L);
-  fence_proxy_async_smem();  // the zeroed rows are read by the tensor core next
+  if (L < kChunk) zero_tails(L, 2);
+  fence_proxy_async_smem();  // the zeroed rows are read by the tensor core later
   tc_fence_before();
   __syncthreads();
-  // ---- squared norms: diagonal of [k; q] [k; q]^T (tensor memory columns 0..127) ----
-  if (kL2 && warp == 0) {
-    tc_fence_after();
-    const uint32_t id = idesc_bf16(128, 128, false, false);
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const uint64_t o = (uint64_t)(((ks >> 2) * 16384 + (ks & 3) * 32) >> 4);
-      tc_mma(tmem, dRo + o, dRo + o, id, ks > 0);
-    }
-    tc_commit(bar_mma);
-  }
 
   // ---- gate activation, per-token decays d (registers), half sub-chunk products ----
   // thread -> sub-chunk rb, half hf (tokens 8 hf .. 8 hf + 7 of it), channels c0 .. c0 + 3;
@@ -460,24 +485,7 @@ __global__ void __launch_bounds__(256, 2)
     inv[2] = rcp_approx(Dcb.x);
     inv[3] = rcp_approx(Dcb.y);
   }
-  // norms from the diagonal of the Gram product: lane l of warp w < 4 holds row 32 w + l
-  if (kL2) {
-    wait_mma();
-    if (warp < 4) {
-      float v[32];
-      tc_ld32(tmem + ((uint32_t)(32 * warp) << 16) + 32 * warp, v);
-      float ss = 0.f;
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j == lane) ss = v[j];
-      const int row = 32 * warp + lane;
-      (row < 64 ? sRk : sRq)[row & 63] = rsqrtf(ss + 1e-6f);
-    }
-    tc_fence_before();
-  } else if (tid < 128) {
-    (tid < 64 ? sRk : sRq)[tid & 63] = 1.0f;
-  }
-  __syncthreads();
+  __syncthreads();  // the half products are read by every warp below
 
   // ---- operands ----
   //  exact, chunk relative:     gamma_j = prod_{s<=j} d_s  -> beta K gamma (rhs), q gamma (ws)
@@ -639,12 +647,10 @@ __global__ void __launch_bounds__(256, 2)
     }
     tc_commit(bar_mma);
   }
+  if (next < num_items) nxt = locate(next);  // while the tensor core runs
   wait_mma();
   // q, k tiles are free: the next item's q, k
-  if (next < num_items) {
-    if (tid == 0) copy_qk(nxt);
-    if (tid < kChunk) blogit = load_beta(nxt);
-  }
+  if (next < num_items && tid == 0) copy_qk(nxt);
   // ---- A / P epilogue: lane = row of [K xr; Q xr]; rows 0..63 give A (beta-scaled,
   //      strictly lower), rows 64..127 P (lower).  Warps w and w + 4 share a lane
   //      quarter: w < 4 the diagonal sub-block (and, for sub-chunks 2 and 3, the
@@ -671,14 +677,12 @@ __global__ void __launch_bounds__(256, 2)
 #pragma unroll
         for (int c = 0; c < 4; ++c) ad[c] = make_float4(e[4 * c], e[4 * c + 1], e[4 * c + 2], e[4 * c + 3]);
       } else {
-        // P columns 16 r .. 16 r + 15, then zeros up to column 63
+        // P columns 16 r .. 16 r + 15 (the zeros right of them are written above)
 #pragma unroll
         for (int c = 0; c < 2; ++c)
           *reinterpret_cast<uint4*>(gP + kmaj_off(i, 16 * r + 8 * c, 64)) =
               make_uint4(pack_f16(e[8 * c], e[8 * c + 1]), pack_f16(e[8 * c + 2], e[8 * c + 3]),
                          pack_f16(e[8 * c + 4], e[8 * c + 5]), pack_f16(e[8 * c + 6], e[8 * c + 7]));
-        for (int c = 2 * r + 2; c < 8; ++c)
-          *reinterpret_cast<uint4*>(gP + kmaj_off(i, 8 * c, 64)) = make_uint4(0u, 0u, 0u, 0u);
       }
     }
     // off-diagonal columns 0 .. 16 r - 1 of row i sit at tensor-memory columns
@@ -744,6 +748,16 @@ __global__ void __launch_bounds__(256, 2)
       *reinterpret_cast<__half*>(smem + kT + off) = xv;
       *reinterpret_cast<__half*>(smem + kT + 8192 + off) = xv;
     }
+  } else {
+    // the other warps meanwhile: the next item's scalars into the staging area
+    // (the decay products are dead), and the columns of P right of each row's
+    // sub-chunk, which are zero
+    if (next < num_items) stage_scalars(nxt);
+    if (tid >= 192) {
+      const int i = tid - 192, r = i >> 4;
+      for (int c = 2 * r + 2; c < 8; ++c)
+        *reinterpret_cast<uint4*>(ws + kSlotP + kmaj_off(i, 8 * c, 64)) = make_uint4(0u, 0u, 0u, 0u);
+    }
   }
   __syncthreads();
   // ---- off-diagonal blocks of T: T_rc = sum_{m=c}^{r-1} M_rm T_mc, M_rm = -X_r A_rm.
@@ -782,6 +796,9 @@ __global__ void __launch_bounds__(256, 2)
       tc_mma(tmem, dT + (uint64_t)((ks * 32) >> 4), dRhs + (uint64_t)((ks * 2048) >> 4), id, ks > 0);
     tc_commit(bar_mma);
   }
+  // while the tensor core runs: the next item's q, k rows and norms (its copy
+  // went out after the A / P product; this item's norms are no longer read)
+  if (next < num_items) prep_rows(nxt, (uint32_t)((it + 1) & 1));
   wait_mma();
   // the right-hand-side tiles are free: the next item's g and v
   if (next < num_items && tid == 0) copy_gv(nxt);
