@@ -175,14 +175,6 @@ __device__ __forceinline__ f32x2 gate_decay2(f32x2 z, float amul_log2e, float lb
   return f2(ex2(c.x), ex2(c.y));
 }
 
-// C fragments of a 16 x 16 product (two n8 tiles) as the A fragment of the next
-// product (fp16), negated if asked.
-__device__ __forceinline__ void cfrag_to_afrag(const float (&c)[2][4], uint32_t (&a)[4], float sgn) {
-  a[0] = pack_f16(sgn * c[0][0], sgn * c[0][1]);
-  a[1] = pack_f16(sgn * c[0][2], sgn * c[0][3]);
-  a[2] = pack_f16(sgn * c[1][0], sgn * c[1][1]);
-  a[3] = pack_f16(sgn * c[1][2], sgn * c[1][3]);
-}
 // 16 x 16 product accumulated into c: A fragment a times B = block (k0.., n0..)
 // of a [k][n] fp16 tile (swz64 layout).
 __device__ __forceinline__ void mma16_kn(float (&c)[2][4], const uint32_t (&a)[4], uint32_t bbase,
@@ -207,23 +199,16 @@ __device__ __forceinline__ void store_tblock(unsigned char* smem, const float (&
     }
 }
 
-// Row sub-chunk R of T: M_Rc = -X_R A_Rc for c < R into m0.. (fp16 A fragments),
-// then T_R,R-1 = M_R,R-1 X_R-1, stored.
-template <int R>
-__device__ __forceinline__ void t_first(unsigned char* smem, uint32_t sbase, uint32_t (&m0)[4],
-                                        uint32_t (&m1)[4], uint32_t (&m2)[4], int lane) {
-  uint32_t xa[4];
-  lda_64(xa, sbase + kT, 16 * R, 16 * R, lane);  // X_R
-  uint32_t(*ms[3])[4] = {&m0, &m1, &m2};
+// Store -C (a 16 x 16 block in C fragments) as fp16 at (r0, c0) of the kA16 tile.
+__device__ __forceinline__ void store_mblock(unsigned char* smem, const float (&c)[2][4], int r0,
+                                             int c0, int lane) {
+  const int g = lane >> 2, q4 = lane & 3;
 #pragma unroll
-  for (int c = 0; c < R; ++c) {
-    float acc[2][4] = {};
-    mma16_kn(acc, xa, sbase + kA16, 16 * c, 16 * R, lane);  // X_R A_Rc
-    cfrag_to_afrag(acc, *ms[c], -1.f);
-  }
-  float t[2][4] = {};
-  mma16_kn(t, *ms[R - 1], sbase + kT, 16 * (R - 1), 16 * (R - 1), lane);  // M_R,R-1 X_R-1
-  store_tblock(smem, t, 16 * R, 16 * (R - 1), lane);
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+      u32_at(smem + kA16, swz64(r0 + g + 8 * hh, c0 + 8 * nt + 2 * q4)) =
+          pack_f16(-c[nt][2 * hh], -c[nt][2 * hh + 1]);
 }
 
 template <int kGate, bool kL2>
@@ -398,7 +383,6 @@ __global__ void __launch_bounds__(256, 2)
   auto ld_exact = [&](int s2, int c) { return *reinterpret_cast<const float4*>(smem + cs_exact(s2) + c * 4); };
   auto ld_xm = [&](int r, int c) { return *reinterpret_cast<const float4*>(smem + cs_clamped(2 * r) + c * 4); };
   auto ld_ym = [&](int r, int c) { return *reinterpret_cast<const float4*>(smem + cs_clamped(2 * r + 1) + c * 4); };
-  const int g4 = lane >> 2, q4 = lane & 3;  // mma.sync fragment coordinates
   // tensor-core operand descriptors (the 14-bit address field takes the
   // k-step offsets by plain addition)
   const uint64_t dRo = smem_desc(sbase + kRo, 16, 1024);
@@ -420,7 +404,7 @@ __global__ void __launch_bounds__(256, 2)
     const float bl = sStg[128 + tid];
     sBeta[tid] = tid >= L ? 0.f : (p.beta_prob ? bl : rcp_approx(1.0f + ex2(-bl * kLog2e)));
   }
-  wait_bar(bar_qk, (uint32_t)(it & 1));  // (also waited on, and rows prepared, one item ahead)
+  // (this item's q, k copy was waited on, and its rows prepared, one item ahead)
   wait_bar(bar_gv, (uint32_t)(it & 1));
   if (L < kChunk) zero_tails(L, 2);
   fence_proxy_async_smem();  // the zeroed rows are read by the tensor core later
@@ -761,27 +745,49 @@ __global__ void __launch_bounds__(256, 2)
   }
   __syncthreads();
   // ---- off-diagonal blocks of T: T_rc = sum_{m=c}^{r-1} M_rm T_mc, M_rm = -X_r A_rm.
-  //      Warp r - 1 forms M_r0 .. M_r,r-1 in registers, then T_r,r-1; the deeper
-  //      blocks follow once the blocks they read are stored ----
-  uint32_t aM0[4], aM1[4], aM2[4];
-  if (warp == 0) t_first<1>(smem, sbase, aM0, aM1, aM2, lane);
-  else if (warp == 1) t_first<2>(smem, sbase, aM0, aM1, aM2, lane);
-  else if (warp == 2) t_first<3>(smem, sbase, aM0, aM1, aM2, lane);
-  __syncthreads();
-  if (warp == 1 || warp == 2) {  // T_20 (warp 1), T_31 (warp 2)
-    const int r = warp + 1, c = r - 2;
-    float t[2][4] = {};
-    mma16_kn(t, warp == 1 ? aM0 : aM1, sbase + kT, 16 * c, 16 * c, lane);            // M_rc X_c
-    mma16_kn(t, warp == 1 ? aM1 : aM2, sbase + kT, 16 * c, 16 * (c + 1), lane);      // M_r,c+1 T_c+1,c
-    store_tblock(smem, t, 16 * r, 16 * c, lane);
+  //      Level 0: six warps form one M_rc each (fp16, over A_rc in place).  Level 1:
+  //      T_10, T_21, T_32 = M_r,r-1 X_r-1, while three warps start the sums of T_20,
+  //      T_31 and T_30 (fp32 fragments in registers).  Levels 2 and 3 add the terms
+  //      whose T blocks the previous level stored.  Every block keeps one accumulator
+  //      fed in the order m = c .. r - 1. ----
+  if (warp < 6) {
+    const int r = warp < 1 ? 1 : (warp < 3 ? 2 : 3), c = warp - (r * (r - 1)) / 2;
+    uint32_t xa[4];
+    lda_64(xa, sbase + kT, 16 * r, 16 * r, lane);  // X_r
+    float acc[2][4] = {};
+    mma16_kn(acc, xa, sbase + kA16, 16 * c, 16 * r, lane);  // X_r A_rc
+    store_mblock(smem, acc, 16 * r, 16 * c, lane);
   }
   __syncthreads();
-  if (warp == 2) {  // T_30
-    float t[2][4] = {};
-    mma16_kn(t, aM0, sbase + kT, 0, 0, lane);
-    mma16_kn(t, aM1, sbase + kT, 0, 16, lane);
-    mma16_kn(t, aM2, sbase + kT, 0, 32, lane);
-    store_tblock(smem, t, 48, 0, lane);
+  float tacc[2][4] = {};  // warp 3: T_20, warp 4: T_31, warp 5: T_30 (partial sums)
+  if (warp < 6) {
+    uint32_t am[4];
+    if (warp < 3) {  // T_r,r-1 = M_r,r-1 X_r-1, r = warp + 1
+      const int r = warp + 1;
+      lda_64(am, sbase + kA16, 16 * r, 16 * (r - 1), lane);
+      float t[2][4] = {};
+      mma16_kn(t, am, sbase + kT, 16 * (r - 1), 16 * (r - 1), lane);
+      store_tblock(smem, t, 16 * r, 16 * (r - 1), lane);
+    } else {  // first terms: M_20 X_0, M_31 X_1, M_30 X_0
+      const int r = warp == 4 ? 3 : (warp == 3 ? 2 : 3), c = warp == 4 ? 1 : 0;
+      lda_64(am, sbase + kA16, 16 * r, 16 * c, lane);
+      mma16_kn(tacc, am, sbase + kT, 16 * c, 16 * c, lane);
+    }
+  }
+  __syncthreads();
+  if (warp >= 3 && warp < 6) {  // + M_21 T_10 (T_20), M_32 T_21 (T_31), M_31 T_10 (T_30)
+    const int r = warp == 3 ? 2 : 3, m = warp == 4 ? 2 : 1, c = warp == 4 ? 1 : 0;
+    uint32_t am[4];
+    lda_64(am, sbase + kA16, 16 * r, 16 * m, lane);
+    mma16_kn(tacc, am, sbase + kT, 16 * c, 16 * m, lane);
+    if (warp < 5) store_tblock(smem, tacc, 16 * r, 16 * c, lane);
+  }
+  __syncthreads();
+  if (warp == 5) {  // T_30 += M_32 T_20
+    uint32_t am[4];
+    lda_64(am, sbase + kA16, 48, 32, lane);
+    mma16_kn(tacc, am, sbase + kT, 0, 32, lane);
+    store_tblock(smem, tacc, 48, 0, lane);
   }
   fence_proxy_async_smem();  // T is read by the tensor core next
   tc_fence_before();
