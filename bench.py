@@ -47,7 +47,7 @@ FLOP_PER_TOKEN_HEAD = 6 * K_DIM * K_DIM + 2 * CHUNK * K_DIM + (CHUNK + 1) * 2 * 
 BYTES_IN_PER_TOKEN_HEAD = 4 * 2 * K_DIM + 2
 BYTES_OUT_PER_TOKEN_HEAD = 2 * K_DIM
 DEFAULT_STEPS = {"tiny": 2000, "dense_batch": 3000, "long_context": 3000, "packed_varlen": 500,
-                 "extremes": 1000}
+                 "extremes": 1000, "long_sequence": 1000}
 KERNEL_SOURCES = {
     "kda_chunk_kernel": ["kda_chunk.cu", "kda_common.cuh", "kda_kernels.cuh", "kda_tc.cuh"],
     "kda_state_kernel": ["kda_state.cu", "kda_common.cuh", "kda_kernels.cuh", "kda_tc.cuh"],
@@ -66,9 +66,10 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU work of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--path", choices=["chunked", "recurrent"], default="chunked",
+    p.add_argument("--path", choices=["chunked", "recurrent", "backward"], default="chunked",
                    help="recurrent: time the token-by-token (decoding) entry point on the "
-                        "decode workload instead of the chunked path")
+                        "decode workload instead of the chunked path; backward: time kda_bwd "
+                        "(gradients of every input) on the workload")
     return p.parse_args()
 
 
@@ -500,6 +501,111 @@ def run_recurrent_line(a, dev):
     return 0
 
 
+# backward bytes per token-head: q, k, v, g, dout (bf16) and beta in; dq, dk,
+# dv, dg (fp32) and dbeta (fp32) out
+BWD_BYTES_PER_TOKEN_HEAD = 5 * 2 * K_DIM + 2 + 4 * 4 * K_DIM + 4
+
+
+def run_backward_line(a, dev):
+    """kda_bwd on the workload: gradients of <out, dout> (+ <final, dfinal>
+    when the workload has a final state) with respect to every input.  Each
+    call is timed by its own events (kda_bwd_profiled: checkpoint, reverse and
+    finalize launches), with an untimed L2 flush between calls."""
+    from kimi_delta_attention_05_gb300 import kda as K
+    w = WORKLOADS[a.workload]
+    inp = make_inputs(w)
+    gen = torch.Generator().manual_seed(w.seed + 1000)
+    dout_h = torch.randn(inp["v"].shape, generator=gen).to(torch.bfloat16)
+    H = inp["q"].shape[2]
+    dfin_h = (torch.randn((inp["N"], H, K_DIM, K_DIM), generator=gen)
+              if inp["final_state"] is not None else None)
+    d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in inp.items()}
+    dout = dout_h.to(dev)
+    dfin = dfin_h.to(dev) if dfin_h is not None else None
+    lb = inp["lower_bound"] if inp["gate"] == "safe" else None
+    args, grads = K.make_bwd_args(d["q"], d["k"], d["v"], d["g"], d["beta"], inp["scale"], dout,
+                                  d["A_log"], d["dt_bias"], lb, d["initial_state"], dfin,
+                                  d["cu_seqlens"], qk_l2norm=inp["qk_l2norm"], gate=inp["gate"])
+    ws = torch.empty(max(K.bwd_workspace_bytes(args), 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    steps = a.steps or 20
+    flush = L2Flush(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for quad in ev:
+        for e in quad:
+            e.record(stream)
+    for _ in range(a.warmup):
+        flush()
+        K.kda_bwd_args_call(args, ws, stream)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        w0 = time.time()
+        for i in range(steps):
+            flush()
+            K.kda_bwd_args_call(args, ws, stream, events=[e.cuda_event for e in ev[i]])
+        torch.cuda.synchronize(dev)
+        w1 = time.time()
+    stage = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps))
+             for j, name in enumerate(["kda_bwd_ckpt_kernel", "kda_bwd_kernel", "kda_bwd_finalize_kernel"])}
+    ms_step = statistics.mean(ev[i][0].elapsed_time(ev[i][3]) for i in range(steps))
+    th = token_heads(inp)
+    tokens = th // H
+    units = inp["N"] * H
+    st_bytes = 0
+    if inp["initial_state"] is not None:
+        st_bytes += 2 * units * K_DIM * K_DIM * inp["initial_state"].element_size() + units * K_DIM * K_DIM * 4
+    if dfin is not None:
+        st_bytes += units * K_DIM * K_DIM * 4
+    step_bytes = th * BWD_BYTES_PER_TOKEN_HEAD + st_bytes
+    hbm, _, peak_kind = measured_peaks()
+    achieved = step_bytes / (ms_step * 1e-3) / 1e9
+    # end to end: inputs and dout in from pinned host memory, token gradients
+    # back, around the same call
+    names = ["q", "k", "v", "g", "beta"]
+    host = {n: inp[n].pin_memory() for n in names}
+    host_dout = dout_h.pin_memory()
+    host_g = {n: torch.empty(grads[n].shape, dtype=torch.float32).pin_memory()
+              for n in ["q", "k", "v", "g", "beta"]}
+    e_steps = max(min(a.e2e_steps, 10), 1)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        for n in names:
+            d[n].copy_(host[n], non_blocking=True)
+        dout.copy_(host_dout, non_blocking=True)
+        K.kda_bwd_args_call(args, ws, stream)
+        for n, t in host_g.items():
+            t.copy_(grads[n], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e_ms = e0.elapsed_time(e1) / e_steps
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names) + host_dout.numel() * 2
+    d2h = sum(t.numel() * 4 for t in host_g.values())
+    cfg = {"workload": a.workload, "B": int(inp["q"].shape[0]), "T": int(inp["q"].shape[1]),
+           "H": int(H), "K": K_DIM, "V": K_DIM, "N": int(inp["N"]), "gate": inp["gate"],
+           "qk_l2norm": bool(inp["qk_l2norm"]), "initial_state": w.init_state,
+           "dfinal_state": "fp32" if dfin is not None else None,
+           "path": "backward (kda_bwd): token-recurrent, fp32, state checkpoints every 16 tokens",
+           "parallelism": "single GPU",
+           "l2": "untimed L2 flush between calls (256 MB written, another 256 MB read); each call "
+                 "timed by its own CUDA events"}
+    dom = max(stage, key=stage.get)
+    line = {"metric": "KDA bwd tokens/s and % of HBM roofline, 1 GB300", "value": tokens / (ms_step * 1e-3),
+            "unit": "tokens/s", "n_gpus": 1, "steps": steps, "warmup": a.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": cfg,
+            "roofline": {"bound": "hbm", "kernel": "kda_bwd (three launches)", "achieved": achieved,
+                         "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                         "algorithmic_bytes_per_launch": step_bytes, "dominant_launch": dom,
+                         "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"},
+            "stages_ms": stage, "gpu_launches": 3 * steps, "clocks": clk.summary(w0, w1),
+            "e2e": {"value": tokens / (e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     a = parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -535,6 +641,8 @@ def main():
     K.load_library()
     if a.path == "recurrent":
         return run_recurrent_line(a, dev) if rank == 0 else 0
+    if a.path == "backward":
+        return run_backward_line(a, dev) if rank == 0 else 0
     inp = rank_inputs(w, rank)
     r = run_ours(a, inp, dev, rank, world)
     th = token_heads(inp)
@@ -573,6 +681,9 @@ def main():
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }
+    lpc = r["launches"] // r["steps"]
+    line["config"]["state_pass"] = ("sequence split: segment runs, transition chain, re-runs "
+                                    "(4 launches per call)" if lpc == 4 else f"one pass ({lpc} launches per call)")
     if rank == 0:
         e_ms, h2d, d2h = run_e2e(a, inp, dev)
         line["e2e"] = {"value": tokens * world / (e_ms * 1e-3), "unit": "tokens/s",

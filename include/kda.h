@@ -295,6 +295,17 @@ size_t kda_bwd_workspace_bytes(const kda_bwd_args *args);
 int kda_bwd(const kda_bwd_args *args, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * kda_bwd, additionally recording four caller-created CUDA events
+ * (cudaEvent_t, each may be NULL) on `stream`: events[0] before the first
+ * operation, events[1] after the checkpoint launch (forward replay storing the
+ * state every 16 tokens), events[2] after the reverse launch, events[3] after
+ * the finalize launch.  For measurement only; the computation is identical to
+ * kda_bwd.
+ */
+int kda_bwd_profiled(const kda_bwd_args *args, void *workspace, size_t workspace_bytes,
+                     void *stream, void *const events[4]);
+
+/*
  * Device-side status of the forward calls enqueued on `stream` (a cudaStream_t;
  * NULL = legacy default stream), the kda_get_status(cudaStream_t) of the
  * boundary: KDA_OK, KDA_ERR_DEVICE_TIMEOUT if a CTA of such a call gave up

@@ -472,31 +472,41 @@ __global__ void __launch_bounds__(256) kda_bwd_finalize_kernel(BwdParams p) {
 }
 
 template <int kGate, bool kL2>
-static void launch_bwd_variant(const BwdParams& p, cudaStream_t s) {
+static void launch_bwd_variant(const BwdParams& p, cudaStream_t s, void* const* ev) {
+  auto mark = [&](int i) {
+    if (ev && ev[i]) cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[i]), s);
+  };
   const unsigned units = (unsigned)(p.N * p.H);
   kda_bwd_ckpt_kernel<kGate, kL2><<<units, kBwdThreads, 0, s>>>(p);
+  mark(1);
   kda_bwd_kernel<kGate, kL2><<<units, kBwdThreads, kBwdSmem, s>>>(p);
+  mark(2);
   const int64_t warps = (p.rows + kFinRun - 1) / kFinRun * p.H;
   if (warps > 0) kda_bwd_finalize_kernel<kGate, kL2><<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(p);
+  mark(3);
 }
 
-void launch_bwd(const BwdParams& p, cudaStream_t s) {
+// ev: optional events (cudaEvent_t, each may be null) recorded after the
+// checkpoint, reverse and finalize launches (entries 1, 2, 3).
+static void launch_bwd_events(const BwdParams& p, cudaStream_t s, void* const* ev) {
   if (p.N * p.H == 0) return;
   const bool l2 = p.l2norm != 0;
   switch (p.gate_mode) {
     case kGateUnsafe:
-      if (l2) launch_bwd_variant<kGateUnsafe, true>(p, s);
-      else launch_bwd_variant<kGateUnsafe, false>(p, s);
+      if (l2) launch_bwd_variant<kGateUnsafe, true>(p, s, ev);
+      else launch_bwd_variant<kGateUnsafe, false>(p, s, ev);
       break;
     case kGateLogspace:
-      if (l2) launch_bwd_variant<kGateLogspace, true>(p, s);
-      else launch_bwd_variant<kGateLogspace, false>(p, s);
+      if (l2) launch_bwd_variant<kGateLogspace, true>(p, s, ev);
+      else launch_bwd_variant<kGateLogspace, false>(p, s, ev);
       break;
     default:
-      if (l2) launch_bwd_variant<kGateSafe, true>(p, s);
-      else launch_bwd_variant<kGateSafe, false>(p, s);
+      if (l2) launch_bwd_variant<kGateSafe, true>(p, s, ev);
+      else launch_bwd_variant<kGateSafe, false>(p, s, ev);
   }
 }
+
+void launch_bwd(const BwdParams& p, cudaStream_t s) { launch_bwd_events(p, s, nullptr); }
 
 cudaError_t prepare_bwd() {
   const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
@@ -546,7 +556,9 @@ extern "C" size_t kda_bwd_workspace_bytes(const kda_bwd_args* a) {
   return round256(ckpt) + round256(rec);
 }
 
-extern "C" int kda_bwd(const kda_bwd_args* a, void* workspace, size_t workspace_bytes, void* stream_ptr) {
+namespace {
+int bwd_device(const kda_bwd_args* a, void* workspace, size_t workspace_bytes, void* stream_ptr,
+               void* const* events) {
   if (!a) return KDA_ERR_NULL_ARG;
   const kda_fwd_args& f = a->fwd;
   int64_t slots = 0;
@@ -572,6 +584,7 @@ extern "C" int kda_bwd(const kda_bwd_args* a, void* workspace, size_t workspace_
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream_ptr);
   int* status = status_slot(s);
   if (!status) return KDA_ERR_LAUNCH;
+  if (events && events[0]) cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[0]), s);
   const int64_t H = f.H;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   const size_t ckpt_bytes = round256((size_t)H * (size_t)bwd_slots(rows, f.N) * kHeadDim * kHeadDim * sizeof(float));
@@ -623,7 +636,17 @@ extern "C" int kda_bwd(const kda_bwd_args* a, void* workspace, size_t workspace_
   p.dA_log = gate != KDA_GATE_LOGSPACE ? a->dA_log : nullptr;
   p.ddt_bias = gate != KDA_GATE_LOGSPACE ? a->ddt_bias : nullptr;
   p.dinit = a->dinitial_state;
-  launch_bwd(p, s);
+  launch_bwd_events(p, s, events);
   if (!ok || cudaGetLastError() != cudaSuccess) return KDA_ERR_LAUNCH;
   return KDA_OK;
+}
+}  // namespace
+
+extern "C" int kda_bwd(const kda_bwd_args* a, void* workspace, size_t workspace_bytes, void* stream_ptr) {
+  return bwd_device(a, workspace, workspace_bytes, stream_ptr, nullptr);
+}
+
+extern "C" int kda_bwd_profiled(const kda_bwd_args* a, void* workspace, size_t workspace_bytes,
+                                void* stream_ptr, void* const events[4]) {
+  return bwd_device(a, workspace, workspace_bytes, stream_ptr, events);
 }

@@ -101,6 +101,9 @@ def load_library(build_if_missing: bool = True):
         lib.kda_bwd.argtypes = [ctypes.POINTER(kda_bwd_args), P, ctypes.c_size_t, P]
         lib.kda_bwd_workspace_bytes.restype = ctypes.c_size_t
         lib.kda_bwd_workspace_bytes.argtypes = [ctypes.POINTER(kda_bwd_args)]
+        lib.kda_bwd_profiled.restype = ctypes.c_int
+        lib.kda_bwd_profiled.argtypes = [ctypes.POINTER(kda_bwd_args), P, ctypes.c_size_t, P,
+                                         ctypes.POINTER(ctypes.c_void_p)]
         _lib = lib
     return _lib
 
@@ -269,6 +272,51 @@ def kda_fwd_host_args_call(args: kda_fwd_args, device_buffer, stream) -> None:
         raise KdaError(rc, lib.kda_error_string(rc).decode())
 
 
+def make_bwd_args(q, k, v, g, beta, scale, dout, A_log=None, dt_bias=None, lower_bound=None,
+                  initial_state=None, dfinal_state=None, cu_seqlens=None, *, qk_l2norm=False,
+                  gate=None, beta_prob=False):
+    """The argument block of ``kda_bwd`` and freshly allocated fp32 gradient
+    tensors (same conventions as :func:`kda_bwd`): returns (args, grads)."""
+    gate_name = gate if gate is not None else ("unsafe" if lower_bound is None else "safe")
+    f32 = dict(dtype=torch.float32, device=q.device)
+    grads = {"q": torch.empty(q.shape, **f32), "k": torch.empty(k.shape, **f32),
+             "v": torch.empty(v.shape, **f32), "g": torch.empty(g.shape, **f32),
+             "beta": torch.empty(beta.shape, **f32)}
+    gate_params = gate_name != "logspace"
+    grads["A_log"] = torch.empty(A_log.shape, **f32) if (A_log is not None and gate_params) else None
+    grads["dt_bias"] = torch.empty(dt_bias.shape, **f32) if (dt_bias is not None and gate_params) else None
+    grads["initial_state"] = torch.empty(initial_state.shape, **f32) if initial_state is not None else None
+    a = kda_bwd_args()
+    a.fwd = make_args(q, k, v, g, beta, scale, None, A_log, dt_bias, lower_bound, initial_state,
+                      None, cu_seqlens, qk_l2norm, gate, beta_prob)
+    a.dout = _ptr(dout)
+    a.dfinal_state = _ptr(dfinal_state)
+    a.dq, a.dk, a.dv, a.dg = _ptr(grads["q"]), _ptr(grads["k"]), _ptr(grads["v"]), _ptr(grads["g"])
+    a.dbeta = _ptr(grads["beta"])
+    a.dA_log, a.ddt_bias = _ptr(grads["A_log"]), _ptr(grads["dt_bias"])
+    a.dinitial_state = _ptr(grads["initial_state"])
+    return a, grads
+
+
+def bwd_workspace_bytes(args: kda_bwd_args) -> int:
+    return int(load_library().kda_bwd_workspace_bytes(ctypes.byref(args)))
+
+
+def kda_bwd_args_call(args: kda_bwd_args, workspace, stream, events=None) -> None:
+    """Call ``kda_bwd`` on a prepared argument block (``events``: optional four
+    raw cudaEvent_t handles for ``kda_bwd_profiled``)."""
+    lib = load_library()
+    need = int(lib.kda_bwd_workspace_bytes(ctypes.byref(args)))
+    wptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else None
+    if events is None:
+        rc = lib.kda_bwd(ctypes.byref(args), wptr, need, ctypes.c_void_p(stream.cuda_stream))
+    else:
+        arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e) if e else None for e in events])
+        rc = lib.kda_bwd_profiled(ctypes.byref(args), wptr, need, ctypes.c_void_p(stream.cuda_stream), arr)
+    if rc != 0:
+        raise KdaError(rc, lib.kda_error_string(rc).decode())
+
+
 def kda_bwd(q, k, v, g, beta, scale, dout, A_log=None, dt_bias=None, lower_bound=None,
             initial_state=None, dfinal_state=None, cu_seqlens=None, *, qk_l2norm=False,
             gate=None, beta_prob=False, workspace=None, stream=None):
@@ -277,32 +325,13 @@ def kda_bwd(q, k, v, g, beta, scale, dout, A_log=None, dt_bias=None, lower_bound
     (same conventions as :func:`kda_fwd`).  Returns a dict of fp32 device
     tensors: q, k, v, g, beta, A_log (None unless A_log given and the gate is
     not logspace), dt_bias (likewise), initial_state (None unless given)."""
-    lib = load_library()
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
-    gate_name = gate if gate is not None else ("unsafe" if lower_bound is None else "safe")
     with torch.cuda.stream(s):
-        f32 = dict(dtype=torch.float32, device=q.device)
-        grads = {"q": torch.empty(q.shape, **f32), "k": torch.empty(k.shape, **f32),
-                 "v": torch.empty(v.shape, **f32), "g": torch.empty(g.shape, **f32),
-                 "beta": torch.empty(beta.shape, **f32)}
-        gate_params = gate_name != "logspace"
-        grads["A_log"] = torch.empty(A_log.shape, **f32) if (A_log is not None and gate_params) else None
-        grads["dt_bias"] = torch.empty(dt_bias.shape, **f32) if (dt_bias is not None and gate_params) else None
-        grads["initial_state"] = torch.empty(initial_state.shape, **f32) if initial_state is not None else None
-        a = kda_bwd_args()
-        a.fwd = make_args(q, k, v, g, beta, scale, None, A_log, dt_bias, lower_bound, initial_state,
-                          None, cu_seqlens, qk_l2norm, gate, beta_prob)
-        a.dout = _ptr(dout)
-        a.dfinal_state = _ptr(dfinal_state)
-        a.dq, a.dk, a.dv, a.dg = _ptr(grads["q"]), _ptr(grads["k"]), _ptr(grads["v"]), _ptr(grads["g"])
-        a.dbeta = _ptr(grads["beta"])
-        a.dA_log, a.ddt_bias = _ptr(grads["A_log"]), _ptr(grads["dt_bias"])
-        a.dinitial_state = _ptr(grads["initial_state"])
-        need = int(lib.kda_bwd_workspace_bytes(ctypes.byref(a)))
+        a, grads = make_bwd_args(q, k, v, g, beta, scale, dout, A_log, dt_bias, lower_bound,
+                                 initial_state, dfinal_state, cu_seqlens, qk_l2norm=qk_l2norm,
+                                 gate=gate, beta_prob=beta_prob)
+        need = bwd_workspace_bytes(a)
         if workspace is None or workspace.numel() < need:
             workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    rc = lib.kda_bwd(ctypes.byref(a), ctypes.c_void_p(workspace.data_ptr()), need,
-                     ctypes.c_void_p(s.cuda_stream))
-    if rc != 0:
-        raise KdaError(rc, lib.kda_error_string(rc).decode())
+    kda_bwd_args_call(a, workspace, s)
     return grads

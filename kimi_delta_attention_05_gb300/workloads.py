@@ -60,6 +60,11 @@ WORKLOADS = {
     # 64 packed sequences, lengths U{1..4096}, per-sequence fp32 states
     "packed_varlen": Workload("packed_varlen", 1, 0, 16, "safe", -5.0, True, 1.0, 1.0, 1.0,
                               (1.0, 16.0), "f32", "f32", n_seqs=64, max_len=4096),
+    # one long sequence with few heads (distributions as long_context, fp32 final
+    # state): few sequence-heads for the GPU, so the state stage's chain is cut
+    # into segments (the sequence split)
+    "long_sequence": Workload("long_sequence", 1, 65536, 4, "unsafe", -5.0, True, 1.0, 1.0, 1.0,
+                              (1.0, 16.0), None, "f32"),
     # numerical extremes: wide gate/beta logits, extreme A_log, no L2 norm, bf16 states
     "extremes": Workload("extremes", 2, 32768, 8, "safe", -5.0, False, 0.05, 4.0, 4.0,
                          (0.01, 64.0), "bf16", "bf16"),
@@ -69,8 +74,8 @@ WORKLOADS = {
                        "f32", "f32"),
 }
 
-# The five workloads in the order they are usually listed.
-WORKLOAD_ORDER = ["tiny", "dense_batch", "long_context", "packed_varlen", "extremes"]
+# The chunked-path workloads in the order they are usually listed.
+WORKLOAD_ORDER = ["tiny", "dense_batch", "long_context", "packed_varlen", "extremes", "long_sequence"]
 
 
 def make_inputs(w: Workload, *, seed: int | None = None, lengths=None, T: int | None = None,
