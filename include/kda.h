@@ -250,7 +250,7 @@ int kda_fwd_host(const kda_fwd_args *args, void *device_buffer, size_t device_by
  * with respect to every input of the forward call (the "chunk_bwd" stage of the
  * fla-kda code map, SKILL.md "Code map"; the pages' FlashKDA entry point itself
  * is forward-only).  Computed in fp32 from the bf16 inputs, token by token:
- * the forward recurrence is replayed from state checkpoints taken every 16
+ * the forward recurrence is replayed from state checkpoints taken every 8
  * tokens (workspace), and the reverse recurrence runs per value row of the
  * state.  All gradients are fp32.
  *
@@ -282,9 +282,11 @@ typedef struct kda_bwd_args {
   float *dinitial_state;
 } kda_bwd_args;
 
-/* Device scratch for kda_bwd (state checkpoints, H * (B*T / 16 + N + 1) *
- * 64 KiB, and per-token-head records, B*T*H*1552 bytes); 0 if the forward
- * arguments are invalid. */
+/* Device scratch for kda_bwd (state checkpoints, H * (B*T / 8 + N + 1) *
+ * 64 KiB, and per-token-head records, R * B*T*H*1552 bytes, where R = 1, 2,
+ * 4, 8 or 16 value-row blocks per (sequence, head): the largest that keeps
+ * N*H*R within twice the current device's SM count); 0 if the forward
+ * arguments are invalid.  Size it on the device that runs the call. */
 size_t kda_bwd_workspace_bytes(const kda_bwd_args *args);
 
 /* Enqueue the backward pass on `stream`.  Workspace as for kda_fwd (caller
@@ -298,7 +300,7 @@ int kda_bwd(const kda_bwd_args *args, void *workspace, size_t workspace_bytes, v
  * kda_bwd, additionally recording four caller-created CUDA events
  * (cudaEvent_t, each may be NULL) on `stream`: events[0] before the first
  * operation, events[1] after the checkpoint launch (forward replay storing the
- * state every 16 tokens), events[2] after the reverse launch, events[3] after
+ * state every 8 tokens), events[2] after the reverse launch, events[3] after
  * the finalize launch.  For measurement only; the computation is identical to
  * kda_bwd.
  */

@@ -16,20 +16,22 @@
 // and dL/d(initial state) is ds after the first token.  dq, dk, dD and dbeta
 // are sums over the 128 rows.
 //
-// Three launches:
-//  1. checkpoints: the forward recurrence, storing the state (fp32) at the start
-//     of every 16-token block;
-//  2. reverse walk: one CTA per (sequence, head), 16 warps x 8 value rows, lane =
-//     4 key channels.  Per block (last to first) the block's k, q (normalised),
+// The 128 value rows of a (sequence, head) are split over R CTAs ("row
+// blocks", R a power of two chosen per call so that the grid covers the GPU:
+// 16 / R warps of 8 value rows each, lane = 4 key channels).  Three launches:
+//  1. checkpoints: the forward recurrence of the CTA's rows, a block of kBwdBlock
+//     tokens at a time (the block's normalised k, D, beta and v staged in shared memory),
+//     storing the state (fp32) at the start of every block;
+//  2. reverse walk: per block (last to first) the block's k, q (normalised),
 //     D, beta, v and dout are staged in shared memory; for each token, last to
 //     first, the state before it is recomputed from the block's checkpoint with
 //     the same step (bit-identical to pass 1), the reverse step is applied, and
 //     the per-row terms of dq, dk, dD, dbeta are summed over the CTA's rows in
-//     shared memory into a per-token-head record;
-//  3. finalize, one warp per (run of 64 packed token rows, head): the L2-norm,
-//     gate and sigmoid derivatives turn the records into dq, dk, dg, dbeta, and
-//     the sums over tokens give dA_log and dt_bias (float atomics, one per
-//     channel per run).
+//     shared memory into the row block's part of a per-token-head record;
+//  3. finalize, one warp per (run of 64 packed token rows, head): the R parts
+//     of each record are summed in row-block order, and the L2-norm, gate and
+//     sigmoid derivatives turn them into dq, dk, dg, dbeta; the sums over tokens
+//     give dA_log and dt_bias (float atomics, one per channel per run).
 #include <atomic>
 
 #include "../../include/kda.h"
@@ -38,7 +40,7 @@
 
 namespace kda {
 
-constexpr int kBwdBlock = 16;                  // tokens per checkpoint
+constexpr int kBwdBlock = 8;                   // tokens per checkpoint
 constexpr int kBwdWarps = 16;                  // x 8 value rows = 128
 constexpr int kBwdThreads = 32 * kBwdWarps;
 // record of a token-head: dq_hat, dk_hat, dD (128 each), dbeta, padded to a
@@ -160,14 +162,18 @@ __device__ __forceinline__ void seq_bounds(const BwdParams& p, int64_t n, int64_
 
 // ---- pass 1: checkpoints ----
 template <int kGate, bool kL2>
-__global__ void __launch_bounds__(kBwdThreads) kda_bwd_ckpt_kernel(BwdParams p) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t unit = blockIdx.x, H = p.H;
+__global__ void __launch_bounds__(kBwdThreads) kda_bwd_ckpt_kernel(BwdParams p, int rsplit) {
+  __shared__ float sk[kBwdBlock][kHeadDim], sd[kBwdBlock][kHeadDim], sv[kBwdBlock][kHeadDim];
+  __shared__ float sb[kBwdBlock];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int64_t H = p.H;
+  const int64_t unit = blockIdx.x / rsplit;
+  const int rb = (int)(blockIdx.x - unit * rsplit);
   const int64_t n = unit / H;
   const int h = (int)(unit - n * H);
   int64_t bos, eos;
   seq_bounds(p, n, bos, eos);
-  const int c0 = 4 * lane, r0 = 8 * warp;
+  const int c0 = 4 * lane, r0 = 8 * (warp + nw * rb);
   const int64_t sbase = unit * (int64_t)(kHeadDim * kHeadDim);
   const GateC gc = gate_consts(p, h, c0);
   float S[8][4];
@@ -187,40 +193,62 @@ __global__ void __launch_bounds__(kBwdThreads) kda_bwd_ckpt_kernel(BwdParams p) 
     }
   }
   float* ck = p.ckpt + (h * p.nslots + bos / kBwdBlock + n) * (int64_t)(kHeadDim * kHeadDim);
-  for (int64_t t = bos; t < eos; ++t) {
-    if ((t - bos) % kBwdBlock == 0) {
-      float* dst = ck + ((t - bos) / kBwdBlock) * (int64_t)(kHeadDim * kHeadDim);
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        *reinterpret_cast<float4*>(dst + (r0 + i) * kHeadDim + c0) = make_float4(S[i][0], S[i][1], S[i][2], S[i][3]);
+  const int64_t nblk = (eos - bos + kBwdBlock - 1) / kBwdBlock;
+  for (int64_t blk = 0; blk < nblk; ++blk) {
+    const int64_t t_lo = bos + blk * kBwdBlock;
+    const int nt = (int)min((int64_t)kBwdBlock, eos - t_lo);
+    __syncthreads();  // the previous block's staging is no longer read
+    for (int j = warp; j < nt; j += nw) {  // warp w stages tokens w, w + nw, ...
+      const int64_t row = (t_lo + j) * H + h;
+      float k[4], q[4], D[4], beta, vv[4];
+      token_inputs<kGate, kL2>(p, row, c0, gc, k, q, D, beta);
+      load4(p.v + row * kHeadDim + c0, vv);
+      *reinterpret_cast<float4*>(&sk[j][c0]) = make_float4(k[0], k[1], k[2], k[3]);
+      *reinterpret_cast<float4*>(&sd[j][c0]) = make_float4(D[0], D[1], D[2], D[3]);
+      *reinterpret_cast<float4*>(&sv[j][c0]) = make_float4(vv[0], vv[1], vv[2], vv[3]);
+      if (lane == 0) sb[j] = beta;
     }
-    const int64_t row = t * H + h;
-    float k[4], q[4], D[4], beta, v[8];
-    token_inputs<kGate, kL2>(p, row, c0, gc, k, q, D, beta);
-    load4(p.v + row * kHeadDim + r0, *reinterpret_cast<float(*)[4]>(v));
-    load4(p.v + row * kHeadDim + r0 + 4, *reinterpret_cast<float(*)[4]>(v + 4));
-    fwd_step(S, k, D, beta, v);
+    __syncthreads();
+    float* dst = ck + blk * (int64_t)(kHeadDim * kHeadDim);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      *reinterpret_cast<float4*>(dst + (r0 + i) * kHeadDim + c0) = make_float4(S[i][0], S[i][1], S[i][2], S[i][3]);
+    for (int j = 0; j < nt; ++j) {
+      const float4 kk = *reinterpret_cast<const float4*>(&sk[j][c0]);
+      const float4 dd = *reinterpret_cast<const float4*>(&sd[j][c0]);
+      const float k[4] = {kk.x, kk.y, kk.z, kk.w}, D[4] = {dd.x, dd.y, dd.z, dd.w};
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = sv[j][r0 + i];
+      fwd_step(S, k, D, sb[j], v);
+    }
   }
 }
 
 // ---- pass 2: reverse walk ----
-// shared memory per block of tokens: k, q, D, v, dout [16][128] fp32 each, beta
-// [16], and the per-warp terms of one token's record [16 warps][kBwdRec]
-constexpr int kBwdSmK = 0, kBwdSmQ = 16 * 128, kBwdSmD = 32 * 128, kBwdSmV = 48 * 128, kBwdSmO = 64 * 128;
-constexpr int kBwdSmB = 80 * 128, kBwdSmR = 80 * 128 + 16;
+// shared memory per block of tokens: k, q, D, v, dout [kBwdBlock][128] fp32
+// each, beta [kBwdBlock], and the per-warp terms of one token's record [warps][kBwdRec]
+constexpr int kBwdSmK = 0, kBwdSmQ = kBwdBlock * 128, kBwdSmD = 2 * kBwdBlock * 128;
+constexpr int kBwdSmV = 3 * kBwdBlock * 128, kBwdSmO = 4 * kBwdBlock * 128;
+constexpr int kBwdSmB = 5 * kBwdBlock * 128, kBwdSmR = kBwdSmB + kBwdBlock;
 static_assert(kBwdSmR % 4 == 0 && kBwdRec % 4 == 0, "float4 access to the record rows");
+// (with 16 / R warps per CTA, only their record rows are used)
 constexpr int kBwdSmem = (kBwdSmR + kBwdWarps * kBwdRec) * 4;
+__host__ __device__ constexpr int bwd_smem_bytes(int warps) { return (kBwdSmR + warps * kBwdRec) * 4; }
 
 template <int kGate, bool kL2>
-__global__ void __launch_bounds__(kBwdThreads) kda_bwd_kernel(BwdParams p) {
+__global__ void __launch_bounds__(kBwdThreads) kda_bwd_kernel(BwdParams p, int rsplit) {
   extern __shared__ float sm[];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t unit = blockIdx.x, H = p.H;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int64_t H = p.H;
+  const int64_t unit = blockIdx.x / rsplit;
+  const int rb = (int)(blockIdx.x - unit * rsplit);
   const int64_t n = unit / H;
   const int h = (int)(unit - n * H);
   int64_t bos, eos;
   seq_bounds(p, n, bos, eos);
-  const int c0 = 4 * lane, r0 = 8 * warp;
+  const int c0 = 4 * lane, r0 = 8 * (warp + nw * rb);
+  float* rec = p.rec + (int64_t)rb * p.rows * H * kBwdRec;  // this row block's record parts
   const int64_t sbase = unit * (int64_t)(kHeadDim * kHeadDim);
   const GateC gc = gate_consts(p, h, c0);
   float ds[8][4];  // dL / d(state row) after the current token
@@ -243,19 +271,19 @@ __global__ void __launch_bounds__(kBwdThreads) kda_bwd_kernel(BwdParams p) {
     const int64_t t_lo = bos + blk * kBwdBlock;
     const int nt = (int)min((int64_t)kBwdBlock, eos - t_lo);
     __syncthreads();  // the previous block's staging is no longer read
-    if (warp < nt) {  // warp w stages token t_lo + w
-      const int64_t row = (t_lo + warp) * H + h;
+    for (int j = warp; j < nt; j += nw) {  // warp w stages tokens w, w + nw, ...
+      const int64_t row = (t_lo + j) * H + h;
       float k[4], q[4], D[4], beta;
       token_inputs<kGate, kL2>(p, row, c0, gc, k, q, D, beta);
       float dov[4], vv[4];
       load4(p.v + row * kHeadDim + c0, vv);
       load4(p.dout + row * kHeadDim + c0, dov);
-      *reinterpret_cast<float4*>(sm + kBwdSmK + warp * 128 + c0) = make_float4(k[0], k[1], k[2], k[3]);
-      *reinterpret_cast<float4*>(sm + kBwdSmQ + warp * 128 + c0) = make_float4(q[0], q[1], q[2], q[3]);
-      *reinterpret_cast<float4*>(sm + kBwdSmD + warp * 128 + c0) = make_float4(D[0], D[1], D[2], D[3]);
-      *reinterpret_cast<float4*>(sm + kBwdSmV + warp * 128 + c0) = make_float4(vv[0], vv[1], vv[2], vv[3]);
-      *reinterpret_cast<float4*>(sm + kBwdSmO + warp * 128 + c0) = make_float4(dov[0], dov[1], dov[2], dov[3]);
-      if (lane == 0) sm[kBwdSmB + warp] = beta;
+      *reinterpret_cast<float4*>(sm + kBwdSmK + j * 128 + c0) = make_float4(k[0], k[1], k[2], k[3]);
+      *reinterpret_cast<float4*>(sm + kBwdSmQ + j * 128 + c0) = make_float4(q[0], q[1], q[2], q[3]);
+      *reinterpret_cast<float4*>(sm + kBwdSmD + j * 128 + c0) = make_float4(D[0], D[1], D[2], D[3]);
+      *reinterpret_cast<float4*>(sm + kBwdSmV + j * 128 + c0) = make_float4(vv[0], vv[1], vv[2], vv[3]);
+      *reinterpret_cast<float4*>(sm + kBwdSmO + j * 128 + c0) = make_float4(dov[0], dov[1], dov[2], dov[3]);
+      if (lane == 0) sm[kBwdSmB + j] = beta;
     }
     __syncthreads();
     float S0[8][4];
@@ -348,17 +376,17 @@ __global__ void __launch_bounds__(kBwdThreads) kda_bwd_kernel(BwdParams p) {
         *reinterpret_cast<float4*>(p.dv + row * kHeadDim + r0) = make_float4(duv[0], duv[1], duv[2], duv[3]);
       else if (lane == 1)
         *reinterpret_cast<float4*>(p.dv + row * kHeadDim + r0 + 4) = make_float4(duv[4], duv[5], duv[6], duv[7]);
-      // the token's record: this warp's terms, then the sum over the 16 warps
+      // the token's record: this warp's terms, then the sum over the CTA's warps
       float* rw = sm + kBwdSmR + warp * kBwdRec;
       *reinterpret_cast<float4*>(rw + c0) = make_float4(gq[0], gq[1], gq[2], gq[3]);
       *reinterpret_cast<float4*>(rw + kHeadDim + c0) = make_float4(gk[0], gk[1], gk[2], gk[3]);
       *reinterpret_cast<float4*>(rw + 2 * kHeadDim + c0) = make_float4(gD[0], gD[1], gD[2], gD[3]);
       if (lane == 0) rw[kBwdRecBeta] = gb;
       __syncthreads();
-      if (threadIdx.x <= kBwdRecBeta) {
+      for (int e = threadIdx.x; e <= kBwdRecBeta; e += blockDim.x) {
         float s = 0.f;
-        for (int w = 0; w < kBwdWarps; ++w) s += sm[kBwdSmR + w * kBwdRec + threadIdx.x];
-        p.rec[row * kBwdRec + threadIdx.x] = s;
+        for (int w = 0; w < nw; ++w) s += sm[kBwdSmR + w * kBwdRec + e];
+        rec[row * kBwdRec + e] = s;
       }
       __syncthreads();
     }
@@ -377,7 +405,7 @@ __global__ void __launch_bounds__(kBwdThreads) kda_bwd_kernel(BwdParams p) {
 constexpr int kFinRun = 64;
 
 template <int kGate, bool kL2>
-__global__ void __launch_bounds__(256) kda_bwd_finalize_kernel(BwdParams p) {
+__global__ void __launch_bounds__(256) kda_bwd_finalize_kernel(BwdParams p, int rsplit) {
   const int lane = threadIdx.x & 31;
   const int64_t H = p.H, rows = p.rows;
   const int64_t runs = (rows + kFinRun - 1) / kFinRun;
@@ -391,7 +419,20 @@ __global__ void __launch_bounds__(256) kda_bwd_finalize_kernel(BwdParams p) {
   float acc_dtb[4] = {0.f, 0.f, 0.f, 0.f}, acc_alog = 0.f;
   for (int64_t t = t0; t < t1; ++t) {
     const int64_t row = t * H + h;
-    const float* rec = p.rec + row * kBwdRec;
+    // the record: its R row-block parts summed in order
+    const int64_t part = p.rows * H * kBwdRec;
+    float4 gq4 = make_float4(0.f, 0.f, 0.f, 0.f), gk4 = gq4, gD4 = gq4;
+    float recb = 0.f;
+    for (int r = 0; r < rsplit; ++r) {
+      const float* rp = p.rec + r * part + row * kBwdRec;
+      const float4 a = *reinterpret_cast<const float4*>(rp + c0);
+      const float4 b = *reinterpret_cast<const float4*>(rp + kHeadDim + c0);
+      const float4 c = *reinterpret_cast<const float4*>(rp + 2 * kHeadDim + c0);
+      gq4 = make_float4(gq4.x + a.x, gq4.y + a.y, gq4.z + a.z, gq4.w + a.w);
+      gk4 = make_float4(gk4.x + b.x, gk4.y + b.y, gk4.z + b.z, gk4.w + b.w);
+      gD4 = make_float4(gD4.x + c.x, gD4.y + c.y, gD4.z + c.z, gD4.w + c.w);
+      if (lane == 0) recb += rp[kBwdRecBeta];
+    }
     float q[4], k[4], g[4];
     load4(p.q + row * kHeadDim + c0, q);
     load4(p.k + row * kHeadDim + c0, k);
@@ -401,9 +442,6 @@ __global__ void __launch_bounds__(256) kda_bwd_finalize_kernel(BwdParams p) {
     } else {
       load4(p.g + row * kHeadDim + c0, g);
     }
-    const float4 gq4 = *reinterpret_cast<const float4*>(rec + c0);
-    const float4 gk4 = *reinterpret_cast<const float4*>(rec + kHeadDim + c0);
-    const float4 gD4 = *reinterpret_cast<const float4*>(rec + 2 * kHeadDim + c0);
     const float gq[4] = {gq4.x, gq4.y, gq4.z, gq4.w}, gk[4] = {gk4.x, gk4.y, gk4.z, gk4.w};
     const float gD[4] = {gD4.x, gD4.y, gD4.z, gD4.w};
     float dq[4], dk[4];
@@ -456,7 +494,7 @@ __global__ void __launch_bounds__(256) kda_bwd_finalize_kernel(BwdParams p) {
     *reinterpret_cast<float4*>(p.dg + row * kHeadDim + c0) = make_float4(dg[0], dg[1], dg[2], dg[3]);
     if (lane == 0) {
       const float braw = bf16_to_f(p.beta[row]);
-      float db = rec[kBwdRecBeta];
+      float db = recb;
       if (!p.beta_prob) {
         const float bt = 1.0f / (1.0f + expf(-braw));
         db *= bt * (1.0f - bt);
@@ -472,41 +510,56 @@ __global__ void __launch_bounds__(256) kda_bwd_finalize_kernel(BwdParams p) {
 }
 
 template <int kGate, bool kL2>
-static void launch_bwd_variant(const BwdParams& p, cudaStream_t s, void* const* ev) {
+static void launch_bwd_variant(const BwdParams& p, int rsplit, cudaStream_t s, void* const* ev) {
   auto mark = [&](int i) {
     if (ev && ev[i]) cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[i]), s);
   };
-  const unsigned units = (unsigned)(p.N * p.H);
-  kda_bwd_ckpt_kernel<kGate, kL2><<<units, kBwdThreads, 0, s>>>(p);
+  const unsigned ctas = (unsigned)(p.N * p.H * rsplit);
+  const int warps_per_cta = kBwdWarps / rsplit;
+  kda_bwd_ckpt_kernel<kGate, kL2><<<ctas, 32 * warps_per_cta, 0, s>>>(p, rsplit);
   mark(1);
-  kda_bwd_kernel<kGate, kL2><<<units, kBwdThreads, kBwdSmem, s>>>(p);
+  kda_bwd_kernel<kGate, kL2><<<ctas, 32 * warps_per_cta, bwd_smem_bytes(warps_per_cta), s>>>(p, rsplit);
   mark(2);
   const int64_t warps = (p.rows + kFinRun - 1) / kFinRun * p.H;
-  if (warps > 0) kda_bwd_finalize_kernel<kGate, kL2><<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(p);
+  if (warps > 0) kda_bwd_finalize_kernel<kGate, kL2><<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(p, rsplit);
   mark(3);
 }
 
 // ev: optional events (cudaEvent_t, each may be null) recorded after the
 // checkpoint, reverse and finalize launches (entries 1, 2, 3).
-static void launch_bwd_events(const BwdParams& p, cudaStream_t s, void* const* ev) {
+static void launch_bwd_events(const BwdParams& p, int rsplit, cudaStream_t s, void* const* ev) {
   if (p.N * p.H == 0) return;
   const bool l2 = p.l2norm != 0;
   switch (p.gate_mode) {
     case kGateUnsafe:
-      if (l2) launch_bwd_variant<kGateUnsafe, true>(p, s, ev);
-      else launch_bwd_variant<kGateUnsafe, false>(p, s, ev);
+      if (l2) launch_bwd_variant<kGateUnsafe, true>(p, rsplit, s, ev);
+      else launch_bwd_variant<kGateUnsafe, false>(p, rsplit, s, ev);
       break;
     case kGateLogspace:
-      if (l2) launch_bwd_variant<kGateLogspace, true>(p, s, ev);
-      else launch_bwd_variant<kGateLogspace, false>(p, s, ev);
+      if (l2) launch_bwd_variant<kGateLogspace, true>(p, rsplit, s, ev);
+      else launch_bwd_variant<kGateLogspace, false>(p, rsplit, s, ev);
       break;
     default:
-      if (l2) launch_bwd_variant<kGateSafe, true>(p, s, ev);
-      else launch_bwd_variant<kGateSafe, false>(p, s, ev);
+      if (l2) launch_bwd_variant<kGateSafe, true>(p, rsplit, s, ev);
+      else launch_bwd_variant<kGateSafe, false>(p, rsplit, s, ev);
   }
 }
 
-void launch_bwd(const BwdParams& p, cudaStream_t s) { launch_bwd_events(p, s, nullptr); }
+// Row blocks per (sequence, head): the largest power of two up to 16 that keeps
+// the CTAs of a launch within two per SM (1 when the units alone fill the GPU,
+// and on the host without a device).
+static int bwd_row_split(int64_t units) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 1;
+  }
+  int r = 1;
+  while (r < kBwdWarps && units * (2 * r) <= 2 * (int64_t)sms) r *= 2;
+  return r;
+}
+
+void launch_bwd(const BwdParams& p, cudaStream_t s) { launch_bwd_events(p, bwd_row_split(p.N * p.H), s, nullptr); }
 
 cudaError_t prepare_bwd() {
   const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
@@ -521,8 +574,9 @@ cudaError_t prepare_bwd() {
   return cudaSuccess;
 }
 
-// Checkpoint slots per head: sequence n (rows bos .. eos) uses slots bos / 16 + n
-// + b for its blocks b, which never collide: rows / 16 + N + 1 cover them all.
+// Checkpoint slots per head: sequence n (rows bos .. eos) uses slots
+// bos / kBwdBlock + n + b for its blocks b, which never collide:
+// rows / kBwdBlock + N + 1 cover them all.
 int64_t bwd_slots(int64_t rows, int64_t N) { return rows / kBwdBlock + N + 1; }
 int bwd_record_floats() { return kBwdRec; }
 
@@ -552,7 +606,8 @@ extern "C" size_t kda_bwd_workspace_bytes(const kda_bwd_args* a) {
   if (validate_bwd(a, &slots, &header) != KDA_OK) return 0;
   const int64_t rows = a->fwd.B * a->fwd.T, H = a->fwd.H, N = a->fwd.N;
   const size_t ckpt = (size_t)H * (size_t)bwd_slots(rows, N) * kHeadDim * kHeadDim * sizeof(float);
-  const size_t rec = (size_t)rows * (size_t)H * (size_t)bwd_record_floats() * sizeof(float);
+  const size_t rec = (size_t)rows * (size_t)H * (size_t)bwd_record_floats() * sizeof(float) *
+                     (size_t)bwd_row_split(N * H);
   return round256(ckpt) + round256(rec);
 }
 
@@ -588,7 +643,9 @@ int bwd_device(const kda_bwd_args* a, void* workspace, size_t workspace_bytes, v
   const int64_t H = f.H;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   const size_t ckpt_bytes = round256((size_t)H * (size_t)bwd_slots(rows, f.N) * kHeadDim * kHeadDim * sizeof(float));
-  const size_t rec_bytes = (size_t)rows * (size_t)H * (size_t)bwd_record_floats() * sizeof(float);
+  const int rsplit = bwd_row_split(f.N * H);
+  const size_t rec_bytes =
+      (size_t)rows * (size_t)H * (size_t)bwd_record_floats() * sizeof(float) * (size_t)rsplit;
   const uint32_t gate = f.flags & (KDA_GATE_SAFE | KDA_GATE_UNSAFE | KDA_GATE_LOGSPACE);
   bool ok = true;
   auto chk = [&](cudaError_t e) { ok = ok && e == cudaSuccess; };
@@ -636,7 +693,7 @@ int bwd_device(const kda_bwd_args* a, void* workspace, size_t workspace_bytes, v
   p.dA_log = gate != KDA_GATE_LOGSPACE ? a->dA_log : nullptr;
   p.ddt_bias = gate != KDA_GATE_LOGSPACE ? a->ddt_bias : nullptr;
   p.dinit = a->dinitial_state;
-  launch_bwd_events(p, s, events);
+  launch_bwd_events(p, rsplit, s, events);
   if (!ok || cudaGetLastError() != cudaSuccess) return KDA_ERR_LAUNCH;
   return KDA_OK;
 }

@@ -63,7 +63,7 @@ def _run(inp, dfinal=True, tag=""):
     return errs
 
 
-@pytest.mark.parametrize("T", [1, 15, 16, 17, 64, 130])
+@pytest.mark.parametrize("T", [1, 7, 8, 9, 15, 16, 17, 64, 130])
 def test_backward_dense_safe(T):
     inp = make_inputs(WORKLOADS["dense_batch"], B=2, T=T, H=2, seed=200 + T)
     _run(inp, tag=f"safe T={T}")
