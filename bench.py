@@ -586,7 +586,7 @@ def run_backward_line(a, dev):
            "H": int(H), "K": K_DIM, "V": K_DIM, "N": int(inp["N"]), "gate": inp["gate"],
            "qk_l2norm": bool(inp["qk_l2norm"]), "initial_state": w.init_state,
            "dfinal_state": "fp32" if dfin is not None else None,
-           "path": "backward (kda_bwd): token-recurrent, fp32, state checkpoints every 16 tokens",
+           "path": "backward (kda_bwd): token-recurrent, fp32, value rows over up to 16 CTAs per sequence-head, state checkpoints every 8 tokens",
            "parallelism": "single GPU",
            "l2": "untimed L2 flush between calls (256 MB written, another 256 MB read); each call "
                  "timed by its own CUDA events"}
