@@ -234,9 +234,18 @@ constexpr int kBwdSmB = 5 * kBwdBlock * 128, kBwdSmR = kBwdSmB + kBwdBlock;
 static_assert(kBwdSmR % 4 == 0 && kBwdRec % 4 == 0, "float4 access to the record rows");
 // (with 16 / R warps per CTA, only their record rows are used)
 constexpr int kBwdSmem = (kBwdSmR + kBwdWarps * kBwdRec) * 4;
-__host__ __device__ constexpr int bwd_smem_bytes(int warps) { return (kBwdSmR + warps * kBwdRec) * 4; }
+__host__ __device__ constexpr int bwd_smem_bytes(int warps, bool store = false) {
+  return (kBwdSmR + warps * kBwdRec + (store ? kBwdBlock * 8 * warps * kHeadDim : 0)) * 4;
+}
+constexpr int kBwdStoreWarps = 2;  // CTAs up to this many warps keep the block's states
+constexpr int kBwdSmemStore = bwd_smem_bytes(kBwdStoreWarps, true);
 
-template <int kGate, bool kL2>
+// kStore (CTAs of at most 2 warps): the states before the block's tokens are
+// computed once, going forward from the checkpoint, and kept in shared memory
+// after the record rows ([kBwdBlock][8 rows per warp x warps][128] fp32, each
+// thread reading back only what it wrote); otherwise each token's state is
+// replayed from the checkpoint.  Both give the same bits.
+template <int kGate, bool kL2, bool kStore>
 __global__ void __launch_bounds__(kBwdThreads) kda_bwd_kernel(BwdParams p, int rsplit) {
   extern __shared__ float sm[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -298,14 +307,44 @@ __global__ void __launch_bounds__(kBwdThreads) kda_bwd_kernel(BwdParams p, int r
         S0[i][3] = x.w;
       }
     }
+    float* sst = sm + kBwdSmR + nw * kBwdRec;  // stored states (kStore)
+    if (kStore) {
+      for (int j = 0; j < nt; ++j) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          *reinterpret_cast<float4*>(sst + (j * 8 * nw + 8 * warp + i) * kHeadDim + c0) =
+              make_float4(S0[i][0], S0[i][1], S0[i][2], S0[i][3]);
+        if (j + 1 < nt) {
+          float k[4], D[4], v[8];
+          const float4 kk = *reinterpret_cast<const float4*>(sm + kBwdSmK + j * 128 + c0);
+          const float4 dd = *reinterpret_cast<const float4*>(sm + kBwdSmD + j * 128 + c0);
+          k[0] = kk.x; k[1] = kk.y; k[2] = kk.z; k[3] = kk.w;
+          D[0] = dd.x; D[1] = dd.y; D[2] = dd.z; D[3] = dd.w;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[i] = sm[kBwdSmV + j * 128 + r0 + i];
+          fwd_step(S0, k, D, sm[kBwdSmB + j], v);
+        }
+      }
+    }
     for (int j = nt - 1; j >= 0; --j) {
-      // state before token j of the block: replay tokens 0 .. j-1 from the checkpoint
+      // state before token j of the block: stored, or replayed from the checkpoint
       float S[8][4];
+      if (kStore) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < 8; ++i) {
+          const float4 x = *reinterpret_cast<const float4*>(sst + (j * 8 * nw + 8 * warp + i) * kHeadDim + c0);
+          S[i][0] = x.x;
+          S[i][1] = x.y;
+          S[i][2] = x.z;
+          S[i][3] = x.w;
+        }
+      } else {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) S[i][c] = S0[i][c];
-      for (int jj = 0; jj < j; ++jj) {
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) S[i][c] = S0[i][c];
+      }
+      for (int jj = 0; jj < (kStore ? 0 : j); ++jj) {
         float k[4], D[4], v[8];
         const float4 kk = *reinterpret_cast<const float4*>(sm + kBwdSmK + jj * 128 + c0);
         const float4 dd = *reinterpret_cast<const float4*>(sm + kBwdSmD + jj * 128 + c0);
@@ -518,7 +557,10 @@ static void launch_bwd_variant(const BwdParams& p, int rsplit, cudaStream_t s, v
   const int warps_per_cta = kBwdWarps / rsplit;
   kda_bwd_ckpt_kernel<kGate, kL2><<<ctas, 32 * warps_per_cta, 0, s>>>(p, rsplit);
   mark(1);
-  kda_bwd_kernel<kGate, kL2><<<ctas, 32 * warps_per_cta, bwd_smem_bytes(warps_per_cta), s>>>(p, rsplit);
+  if (warps_per_cta <= kBwdStoreWarps)
+    kda_bwd_kernel<kGate, kL2, true><<<ctas, 32 * warps_per_cta, bwd_smem_bytes(warps_per_cta, true), s>>>(p, rsplit);
+  else
+    kda_bwd_kernel<kGate, kL2, false><<<ctas, 32 * warps_per_cta, bwd_smem_bytes(warps_per_cta), s>>>(p, rsplit);
   mark(2);
   const int64_t warps = (p.rows + kFinRun - 1) / kFinRun * p.H;
   if (warps > 0) kda_bwd_finalize_kernel<kGate, kL2><<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(p, rsplit);
@@ -563,12 +605,24 @@ void launch_bwd(const BwdParams& p, cudaStream_t s) { launch_bwd_events(p, bwd_r
 
 cudaError_t prepare_bwd() {
   const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  const void* fns[] = {(const void*)kda_bwd_kernel<kGateSafe, true>, (const void*)kda_bwd_kernel<kGateSafe, false>,
-                       (const void*)kda_bwd_kernel<kGateUnsafe, true>, (const void*)kda_bwd_kernel<kGateUnsafe, false>,
-                       (const void*)kda_bwd_kernel<kGateLogspace, true>,
-                       (const void*)kda_bwd_kernel<kGateLogspace, false>};
+  const void* fns[] = {(const void*)kda_bwd_kernel<kGateSafe, true, false>,
+                       (const void*)kda_bwd_kernel<kGateSafe, false, false>,
+                       (const void*)kda_bwd_kernel<kGateUnsafe, true, false>,
+                       (const void*)kda_bwd_kernel<kGateUnsafe, false, false>,
+                       (const void*)kda_bwd_kernel<kGateLogspace, true, false>,
+                       (const void*)kda_bwd_kernel<kGateLogspace, false, false>};
+  const void* fns_store[] = {(const void*)kda_bwd_kernel<kGateSafe, true, true>,
+                             (const void*)kda_bwd_kernel<kGateSafe, false, true>,
+                             (const void*)kda_bwd_kernel<kGateUnsafe, true, true>,
+                             (const void*)kda_bwd_kernel<kGateUnsafe, false, true>,
+                             (const void*)kda_bwd_kernel<kGateLogspace, true, true>,
+                             (const void*)kda_bwd_kernel<kGateLogspace, false, true>};
   for (const void* f : fns) {
     const cudaError_t e = cudaFuncSetAttribute(f, attr, kBwdSmem);
+    if (e != cudaSuccess) return e;
+  }
+  for (const void* f : fns_store) {
+    const cudaError_t e = cudaFuncSetAttribute(f, attr, kBwdSmemStore);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
