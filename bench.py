@@ -414,7 +414,7 @@ def workload_config(a, inp, world):
            "l2": f"inputs+outputs {total_bytes / 1e6:.0f} MB vs 129 MB L2; untimed L2 flush "
                  "between calls (256 MB written, another 256 MB read); each call timed by "
                  "its own CUDA events",
-           "compute": "bf16 I/O; intra-chunk tcgen05 (bf16 q/k Gram and A/P, fp16 WY; fp32 "
+           "compute": "bf16 I/O; intra-chunk tcgen05 (bf16 A/P, fp16 WY; fp32 "
                       "tensor-memory accumulators) with 16x16 T blocks on mma.sync; state tcgen05 "
                       "(fp16 operands, fp32 tensor-memory accumulators); fp32 state"}
     return cfg

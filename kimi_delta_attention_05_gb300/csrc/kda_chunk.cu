@@ -7,8 +7,8 @@
 // recurrent state and stores it in the workspace slot of (chunk, head):
 //   * the gate activation and the in-chunk cumulative decay (the "gate.py"
 //     stage of the fla-kda code map: gate activation + cumulative decay),
-//   * optional q/k L2 normalisation: the squared norms are the diagonal of the
-//     Gram matrix [k; q][k; q]^T, one tensor-core product,
+//   * optional q/k L2 normalisation: fp32 sums of the bf16 squares on the CUDA
+//     cores, taken for the next item while the current item's WY product runs,
 //   * A (beta-scaled strictly-lower decayed K K^T) and P (lower decayed Q K^T)
 //     from 16-token sub-chunks (fla-kda SKILL.md, "Numerical invariants"; fla-kda
 //     skill page on the midpoint offset): rows carry exp(Gamma_i - Gamma_m), m the

@@ -92,9 +92,6 @@ __device__ __forceinline__ float2 unpack_f16(uint32_t u) {
   __half2 v = *reinterpret_cast<__half2*>(&u);
   return __half22float2(v);
 }
-__device__ __forceinline__ float f16_to_f(uint16_t u) {
-  return __half2float(__ushort_as_half(u));
-}
 
 // ---- hardware approximations (single MUFU instructions) ----
 __device__ __forceinline__ float ex2(float x) {
@@ -108,17 +105,8 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
-// ---- tensor-core and data-movement primitives ----
-__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Same shape with fp16 operands (11-bit significand, same issue rate).
+// ---- warp-level tensor-core products (the 16 x 16 blocks of T) ----
+// D += A B, m16n8k16, fp16 operands (11-bit significand), fp32 accumulation.
 __device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
                                         uint32_t b1) {
   asm volatile(
@@ -139,48 +127,18 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
                : "r"(addr));
 }
 
-// 16-byte async copy global -> shared; src_bytes = 0 writes zeros.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
-               "r"(src_bytes));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
-}
-
-// A fragment (16x16) of a swizzled tile128 / tile64 at (row0, col0).
-__device__ __forceinline__ void lda_128(uint32_t (&a)[4], uint32_t base, int row0, int col0,
-                                        int lane) {
-  ldsm_x4(a, base + swz128(row0 + (lane & 15), col0 + ((lane >> 4) << 3)));
-}
+// A fragment (16x16) of a 64-column swizzled tile (swz64) at (row0, col0).
 __device__ __forceinline__ void lda_64(uint32_t (&a)[4], uint32_t base, int row0, int col0,
                                        int lane) {
   ldsm_x4(a, base + swz64(row0 + (lane & 15), col0 + ((lane >> 4) << 3)));
 }
-// B fragments for two n8 tiles (n0, n0+8) x k16 at k0, from storage [n][k]
-// (k contiguous).  b[0..1] -> tile n0, b[2..3] -> tile n0+8.
-__device__ __forceinline__ void ldb_nk_128(uint32_t (&b)[4], uint32_t base, int n0, int k0,
-                                           int lane) {
-  int mi = lane >> 3;
-  ldsm_x4(b, base + swz128(n0 + ((mi >> 1) << 3) + (lane & 7), k0 + ((mi & 1) << 3)));
-}
-__device__ __forceinline__ void ldb_nk_64(uint32_t (&b)[4], uint32_t base, int n0, int k0,
-                                          int lane) {
-  int mi = lane >> 3;
-  ldsm_x4(b, base + swz64(n0 + ((mi >> 1) << 3) + (lane & 7), k0 + ((mi & 1) << 3)));
-}
-// Same, from storage [k][n] (n contiguous), via the transposing load.
+// B fragments for two n8 tiles (n0, n0+8) x k16 at k0, from a swz64 tile stored
+// [k][n] (n contiguous), via the transposing load: b[0..1] -> tile n0,
+// b[2..3] -> tile n0+8.
 __device__ __forceinline__ void ldb_kn_64(uint32_t (&b)[4], uint32_t base, int n0, int k0,
                                           int lane) {
   int mi = lane >> 3;
   ldsm_x4_t(b, base + swz64(k0 + ((mi & 1) << 3) + (lane & 7), n0 + ((mi >> 1) << 3)));
-}
-__device__ __forceinline__ void ldb_kn_128(uint32_t (&b)[4], uint32_t base, int n0, int k0,
-                                           int lane) {
-  int mi = lane >> 3;
-  ldsm_x4_t(b, base + swz128(k0 + ((mi & 1) << 3) + (lane & 7), n0 + ((mi >> 1) << 3)));
 }
 
 // Pairs of fp32 values in one 64-bit register for the packed f32x2 arithmetic
@@ -208,17 +166,7 @@ __device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
-  f32x2 d;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-// a * b + c with one rounding per lane (as the scalar fused multiply-add)
-__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
-  f32x2 d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
+
 // ---- mbarrier + bulk-copy (TMA engine) primitives ----
 __device__ __forceinline__ void mbar_init(uint32_t addr, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(addr), "r"(count) : "memory");

@@ -2,13 +2,12 @@
 //
 // A kernel of a forward call that gives up a bounded wait, or that finds the
 // cu_seqlens values inconsistent, records a code in the status word of the
-// stream the call was enqueued on (the caller's stream: also when a stage runs
-// on the library's second stream, it reports into the caller's word).  So two
-// calls in flight on different streams cannot read, overwrite or clear each
-// other's codes.  The words live in a fixed table compiled into the library;
-// a stream gets a slot on its first call and keeps it.  Slot 0 is shared by
-// the streams that arrive after the table is full (more than kStatusSlots - 1
-// distinct stream handles on one device).
+// stream the call was enqueued on (every kernel of a call runs on that
+// stream).  So two calls in flight on different streams cannot read,
+// overwrite or clear each other's codes.  The words live in a fixed table
+// compiled into the library; a stream gets a slot on its first call and keeps
+// it.  Slot 0 is shared by the streams that arrive after the table is full
+// (more than kStatusSlots - 1 distinct stream handles on one device).
 #include <mutex>
 #include <unordered_map>
 
