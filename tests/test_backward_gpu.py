@@ -3,10 +3,12 @@
 Every gradient (q, k, v, g, beta, A_log, dt_bias, initial state) element by
 element on small cases: every gate form, beta given or as logits, with and
 without the L2 norm, fp32 and bf16 initial states, a final-state gradient,
-packed sequences including empty ones, ragged lengths across the 16-token
-checkpoint blocks.  Tolerance (fp32 arithmetic from bf16 inputs; the
-recomputed states are bit-identical to the checkpoint pass): rel-RMS <= 1e-3
-and max-abs <= 1e-2 max|ref| for every gradient tensor.
+packed sequences including empty ones, ragged lengths across the 8-token
+checkpoint blocks, and every split of the value rows over CTAs (1 to 16 row
+blocks per sequence-head, stored or replayed block states).  Tolerance (fp32
+arithmetic from bf16 inputs; the recomputed states are bit-identical to the
+checkpoint pass): rel-RMS <= 1e-3 and max-abs <= 1e-2 max|ref| for every
+gradient tensor.
 """
 import numpy as np
 import pytest
@@ -111,3 +113,33 @@ def test_backward_rejects_bad_arguments():
     assert lib.kda_bwd_workspace_bytes(None) == 0
     import ctypes
     assert lib.kda_bwd(ctypes.byref(a), None, 0, None) != 0  # K = V = 0, flags 0
+
+
+def _row_blocks(units):
+    """Row blocks per sequence-head the library picks on this device: the
+    largest power of two up to 16 with units * R within twice the SM count."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    r = 1
+    while r < 16 and units * 2 * r <= 2 * sms:
+        r *= 2
+    return r
+
+
+@pytest.mark.parametrize("H", [24, 48, 96, 160])
+def test_backward_every_row_split(H):
+    """Enough sequence-heads for each row split the library uses on this GPU
+    (on 152 SMs: 8 blocks of two warps with the block states kept in shared
+    memory, as on long_context; 4, 2 and 1 blocks replaying them), checked
+    against the oracle; the workspace holds one record part per row block."""
+    inp = make_inputs(WORKLOADS["dense_batch"], B=1, T=40, H=H, seed=220 + H)
+    r = _row_blocks(H)
+    d = tl.to_device(inp)
+    a, _ = K.make_bwd_args(d["q"], d["k"], d["v"], d["g"], d["beta"], inp["scale"],
+                           torch.empty_like(d["v"]), d["A_log"], d["dt_bias"], inp["lower_bound"],
+                           d["initial_state"], None, None, qk_l2norm=True, gate="safe")
+    rows = 40
+    ckpt = H * (rows // 8 + 1 + 1) * 128 * 128 * 4
+    rec = r * rows * H * (3 * 128 + 4) * 4
+    rup = lambda x: (x + 255) // 256 * 256
+    assert K.bwd_workspace_bytes(a) == rup(ckpt) + rup(rec)
+    _run(inp, tag=f"row blocks {r} (H={H})")
