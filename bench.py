@@ -509,8 +509,9 @@ BWD_BYTES_PER_TOKEN_HEAD = 5 * 2 * K_DIM + 2 + 4 * 4 * K_DIM + 4
 def run_backward_line(a, dev):
     """kda_bwd on the workload: gradients of <out, dout> (+ <final, dfinal>
     when the workload has a final state) with respect to every input.  Each
-    call is timed by its own events (kda_bwd_profiled: checkpoint, reverse and
-    finalize launches), with an untimed L2 flush between calls."""
+    call is timed by its own events (kda_bwd_profiled: prep and forward state
+    pass, reverse state pass, chunk gradients and finalize), with an untimed L2
+    flush between calls."""
     from kimi_delta_attention_05_gb300 import kda as K
     w = WORKLOADS[a.workload]
     inp = make_inputs(w)
@@ -546,7 +547,8 @@ def run_backward_line(a, dev):
         torch.cuda.synchronize(dev)
         w1 = time.time()
     stage = {name: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(steps))
-             for j, name in enumerate(["kda_bwd_ckpt_kernel", "kda_bwd_kernel", "kda_bwd_finalize_kernel"])}
+             for j, name in enumerate(["prep + forward state pass", "reverse state pass",
+                                       "gradient products + chunk gradients + finalize"])}
     ms_step = statistics.mean(ev[i][0].elapsed_time(ev[i][3]) for i in range(steps))
     th = token_heads(inp)
     tokens = th // H
@@ -586,20 +588,26 @@ def run_backward_line(a, dev):
            "H": int(H), "K": K_DIM, "V": K_DIM, "N": int(inp["N"]), "gate": inp["gate"],
            "qk_l2norm": bool(inp["qk_l2norm"]), "initial_state": w.init_state,
            "dfinal_state": "fp32" if dfin is not None else None,
-           "path": "backward (kda_bwd): token-recurrent, fp32, value rows over up to 16 CTAs per sequence-head, state checkpoints every 8 tokens",
+           "path": "backward (kda_bwd): chunked WY form in fp32 on the CUDA cores; per 64-token chunk "
+                   "recompute, forward and reverse state passes (16 value rows per CTA), gradient "
+                   "products and chunk gradients",
            "parallelism": "single GPU",
            "l2": "untimed L2 flush between calls (256 MB written, another 256 MB read); each call "
                  "timed by its own CUDA events"}
     dom = max(stage, key=stage.get)
+    # prep, forward pass, reverse pass, products, gradients; finalize with gate
+    # parameters; the chunk prefix with packed sequences
+    launches = 5 + (1 if (grads["A_log"] is not None or grads["dt_bias"] is not None) else 0) \
+        + (1 if inp["cu_seqlens"] is not None else 0)
     line = {"metric": "KDA bwd tokens/s and % of HBM roofline, 1 GB300", "value": tokens / (ms_step * 1e-3),
             "unit": "tokens/s", "n_gpus": 1, "steps": steps, "warmup": a.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "config": cfg,
-            "roofline": {"bound": "hbm", "kernel": "kda_bwd (three launches)", "achieved": achieved,
+            "roofline": {"bound": "hbm", "kernel": f"kda_bwd ({launches} launches)", "achieved": achieved,
                          "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
                          "algorithmic_bytes_per_launch": step_bytes, "dominant_launch": dom,
                          "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"},
-            "stages_ms": stage, "gpu_launches": 3 * steps, "clocks": clk.summary(w0, w1),
+            "stages_ms": stage, "gpu_launches": launches * steps, "clocks": clk.summary(w0, w1),
             "e2e": {"value": tokens / (e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}}
     print(json.dumps(line), flush=True)

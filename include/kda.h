@@ -249,10 +249,12 @@ int kda_fwd_host(const kda_fwd_args *args, void *device_buffer, size_t device_by
  * Backward pass: the gradients of L = <out, dout> + <final_state, dfinal_state>
  * with respect to every input of the forward call (the "chunk_bwd" stage of the
  * fla-kda code map, SKILL.md "Code map"; the pages' FlashKDA entry point itself
- * is forward-only).  Computed in fp32 from the bf16 inputs, token by token:
- * the forward recurrence is replayed from state checkpoints taken every 8
- * tokens (workspace), and the reverse recurrence runs per value row of the
- * state.  All gradients are fp32.
+ * is forward-only).  Computed in fp32 from the bf16 inputs in chunked (WY / UT)
+ * form over 64-token chunks: the chunk quantities of the forward are recomputed
+ * per chunk, a forward pass over the chunks stores the state before each chunk,
+ * a reverse pass stores the state gradient after each chunk, and every chunk's
+ * input gradients are then formed independently (workspace).  All gradients are
+ * fp32.
  *
  *  fwd            : the forward call's arguments (out and final_state unused;
  *                   every layout, flag and check as kda_fwd)
@@ -265,11 +267,11 @@ int kda_fwd_host(const kda_fwd_args *args, void *device_buffer, size_t device_by
  *  dA_log         : fp32 [H] or NULL; not written with KDA_GATE_LOGSPACE
  *  ddt_bias       : fp32 [H, 128] or NULL; not written with KDA_GATE_LOGSPACE
  *  dinitial_state : fp32 [N, H, 128, 128] or NULL
- * dA_log and ddt_bias are sums over tokens accumulated with float atomics (the
- * order, and so the last bits, may differ from run to run); every other
- * gradient is deterministic.  With cu_seqlens, a sequence whose bounds are
- * inconsistent is skipped (zero token gradients, dinitial_state = dfinal_state)
- * and the stream's status word reads KDA_ERR_BAD_SEQLENS.
+ * dA_log and ddt_bias are sums over tokens taken per chunk and then over the
+ * chunks in order; every gradient is deterministic.  dA_log reads 0 for the safe
+ * gate without A_log.  With cu_seqlens whose bounds are inconsistent, no chunk
+ * is processed (zero token gradients, dinitial_state = dfinal_state) and the
+ * stream's status word reads KDA_ERR_BAD_SEQLENS.
  */
 typedef struct kda_bwd_args {
   kda_fwd_args fwd;
@@ -282,11 +284,11 @@ typedef struct kda_bwd_args {
   float *dinitial_state;
 } kda_bwd_args;
 
-/* Device scratch for kda_bwd (state checkpoints, H * (B*T / 8 + N + 1) *
- * 64 KiB, and per-token-head records, R * B*T*H*1552 bytes, where R = 1, 2,
- * 4, 8 or 16 value-row blocks per (sequence, head): the largest that keeps
- * N*H*R within twice the current device's SM count); 0 if the forward
- * arguments are invalid.  Size it on the device that runs the call. */
+/* Device scratch for kda_bwd: one 395,008-byte item per (chunk slot, head),
+ * holding the chunk's recomputed quantities, the state before the chunk and the
+ * state gradient after it (fp32), for B * ceil(T / 64) chunk slots, or
+ * ceil(T / 64) + N with cu_seqlens after a 256-byte-rounded header of
+ * (N + 1) int64 chunk offsets; 0 if the forward arguments are invalid. */
 size_t kda_bwd_workspace_bytes(const kda_bwd_args *args);
 
 /* Enqueue the backward pass on `stream`.  Workspace as for kda_fwd (caller
@@ -299,10 +301,9 @@ int kda_bwd(const kda_bwd_args *args, void *workspace, size_t workspace_bytes, v
 /*
  * kda_bwd, additionally recording four caller-created CUDA events
  * (cudaEvent_t, each may be NULL) on `stream`: events[0] before the first
- * operation, events[1] after the checkpoint launch (forward replay storing the
- * state every 8 tokens), events[2] after the reverse launch, events[3] after
- * the finalize launch.  For measurement only; the computation is identical to
- * kda_bwd.
+ * operation, events[1] after the recompute and forward state pass launches,
+ * events[2] after the reverse state pass, events[3] after the chunk gradient
+ * launches.  For measurement only; the computation is identical to kda_bwd.
  */
 int kda_bwd_profiled(const kda_bwd_args *args, void *workspace, size_t workspace_bytes,
                      void *stream, void *const events[4]);

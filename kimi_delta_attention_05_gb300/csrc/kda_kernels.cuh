@@ -83,32 +83,6 @@ struct RecurrentParams {
   int* status;                            // device status word (bad cu_seqlens)
 };
 
-// Backward pass (token-recurrent, see kda_bwd.cu).
-struct BwdParams {
-  const uint16_t *q, *k, *v, *g, *beta, *dout;  // bf16 inputs and dL/d out
-  const float* g32;                             // g as fp32, or nullptr
-  const float* A_log;
-  const float* dt_bias;
-  float lower_bound, scale;
-  int gate_mode, beta_prob, l2norm;
-  const void* init;                             // [N, H, 128, 128] or nullptr
-  int init_bf16;
-  const float* dfinal;                          // [N, H, 128, 128] fp32 or nullptr
-  const int64_t* cu;
-  int64_t N, T, H;
-  int64_t rows;                                 // packed token rows (B * T)
-  int64_t nslots;                               // checkpoint slots per head
-  int* status;
-  float* ckpt;                                  // [H][nslots][128][128]
-  float* rec;                                   // [rows][H][3 * 128 + 1]
-  float *dq, *dk, *dv, *dg, *dbeta;             // fp32 gradients
-  float *dA_log, *ddt_bias, *dinit;             // fp32, each may be nullptr
-};
-void launch_bwd(const BwdParams& p, cudaStream_t s);
-cudaError_t prepare_bwd();
-int64_t bwd_slots(int64_t rows, int64_t N);
-int bwd_record_floats();
-
 // Host-side argument checks of kda_fwd (KDA_OK or an error code); on success
 // the workspace slot count and the varlen header bytes.
 int validate(const kda_fwd_args* args, int64_t* num_slots, size_t* header_bytes);
@@ -117,12 +91,12 @@ int validate(const kda_fwd_args* args, int64_t* num_slots, size_t* header_bytes)
 // of kda_fwd).  init_bf16 / final_bf16 >= 0 override the state dtype of the
 // initial / final state separately (the host-buffer entry point carries the
 // state between pieces in fp32 whatever the caller's dtype); -1 keeps
-// args->state_dtype.  allow_pipeline: the two stages of consecutive token
-// ranges may overlap on two streams (needs the larger workspace that
-// kda_fwd_workspace_bytes reports for such calls).
+// args->state_dtype.  allow_split: the recurrent stage may run as a split
+// pass over sequence segments when the policy picks one (needs the larger
+// workspace that kda_fwd_workspace_bytes reports for such calls).
 int fwd_device(const kda_fwd_args* args, void* workspace, size_t workspace_bytes,
                cudaStream_t stream, void* const* events, int init_bf16, int final_bf16,
-               bool allow_pipeline);
+               bool allow_split);
 
 void launch_recurrent_kernel(const RecurrentParams& p, cudaStream_t s);
 cudaError_t prepare_recurrent_kernel();

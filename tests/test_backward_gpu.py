@@ -3,12 +3,10 @@
 Every gradient (q, k, v, g, beta, A_log, dt_bias, initial state) element by
 element on small cases: every gate form, beta given or as logits, with and
 without the L2 norm, fp32 and bf16 initial states, a final-state gradient,
-packed sequences including empty ones, ragged lengths across the 8-token
-checkpoint blocks, and every split of the value rows over CTAs (1 to 16 row
-blocks per sequence-head, stored or replayed block states).  Tolerance (fp32
-arithmetic from bf16 inputs; the recomputed states are bit-identical to the
-checkpoint pass): rel-RMS <= 1e-3 and max-abs <= 1e-2 max|ref| for every
-gradient tensor.
+packed sequences including empty ones, ragged lengths across the
+64-token chunks and their 16-token blocks, and many heads.  Tolerance (fp32
+arithmetic from bf16 inputs): rel-RMS <= 1e-3 and max-abs <= 1e-2 max|ref| for
+every gradient tensor.
 """
 import numpy as np
 import pytest
@@ -115,31 +113,29 @@ def test_backward_rejects_bad_arguments():
     assert lib.kda_bwd(ctypes.byref(a), None, 0, None) != 0  # K = V = 0, flags 0
 
 
-def _row_blocks(units):
-    """Row blocks per sequence-head the library picks on this device: the
-    largest power of two up to 16 with units * R within twice the SM count."""
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    r = 1
-    while r < 16 and units * 2 * r <= 2 * sms:
-        r *= 2
-    return r
+ITEM_BYTES = 395008  # workspace per (64-token chunk slot, head)
 
 
-@pytest.mark.parametrize("H", [24, 48, 96, 160])
-def test_backward_every_row_split(H):
-    """Enough sequence-heads for each row split the library uses on this GPU
-    (on 152 SMs: 8 blocks of two warps with the block states kept in shared
-    memory, as on long_context; 4, 2 and 1 blocks replaying them), checked
-    against the oracle; the workspace holds one record part per row block."""
-    inp = make_inputs(WORKLOADS["dense_batch"], B=1, T=40, H=H, seed=220 + H)
-    r = _row_blocks(H)
+@pytest.mark.parametrize("H", [24, 160])
+def test_backward_many_heads(H):
+    """Many (chunk, head) items per launch, checked against the oracle; the
+    workspace is one item per chunk slot and head."""
+    inp = make_inputs(WORKLOADS["dense_batch"], B=1, T=70, H=H, seed=220 + H)
     d = tl.to_device(inp)
     a, _ = K.make_bwd_args(d["q"], d["k"], d["v"], d["g"], d["beta"], inp["scale"],
                            torch.empty_like(d["v"]), d["A_log"], d["dt_bias"], inp["lower_bound"],
                            d["initial_state"], None, None, qk_l2norm=True, gate="safe")
-    rows = 40
-    ckpt = H * (rows // 8 + 1 + 1) * 128 * 128 * 4
-    rec = r * rows * H * (3 * 128 + 4) * 4
-    rup = lambda x: (x + 255) // 256 * 256
-    assert K.bwd_workspace_bytes(a) == rup(ckpt) + rup(rec)
-    _run(inp, tag=f"row blocks {r} (H={H})")
+    assert K.bwd_workspace_bytes(a) == 2 * H * ITEM_BYTES
+    _run(inp, tag=f"H={H}")
+
+
+def test_backward_packed_workspace():
+    """Packed sequences: a 256-byte header for the chunk prefix, then one item
+    per chunk slot (ceil(T / 64) + N slots) and head."""
+    inp = make_inputs(WORKLOADS["packed_varlen"], lengths=[17, 0, 1, 40, 16], H=2, seed=230)
+    d = tl.to_device(inp)
+    a, _ = K.make_bwd_args(d["q"], d["k"], d["v"], d["g"], d["beta"], inp["scale"],
+                           torch.empty_like(d["v"]), d["A_log"], d["dt_bias"], inp["lower_bound"],
+                           d["initial_state"], None, d["cu_seqlens"], qk_l2norm=True, gate="safe")
+    T, N = 74, 5
+    assert K.bwd_workspace_bytes(a) == 256 + ((T + 63) // 64 + N) * 2 * ITEM_BYTES
