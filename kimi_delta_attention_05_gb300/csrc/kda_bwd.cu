@@ -30,7 +30,7 @@
 // Launches:
 //  1. prep, one CTA per (chunk, head): Gamma, G, P, Minv, W, U, Khat, Qg, Kg, gC
 //     into the chunk's workspace item;
-//  2. forward state pass, one CTA per (sequence, head, 16 value rows): walks the
+//  2. forward state pass, one CTA per (sequence, head, 32 value rows): walks the
 //     chunks, storing S before each chunk and Unew (value rows are independent);
 //  3. reverse state pass, same grid, chunks last to first from dfinal: stores
 //     dS_C and dU of each chunk, then dinitial;
@@ -73,8 +73,6 @@ constexpr int kC = kChunk;    // 64 tokens per chunk
 constexpr int kD = kHeadDim;  // 128
 constexpr int kLd = 132;      // row stride (floats) of [64][128] shared arrays (bank spread)
 constexpr int kLs = 68;       // row stride of [64][64] shared arrays
-constexpr int kVb = 16;       // value rows per CTA of the state passes
-constexpr int kRowBlocks = kD / kVb;
 
 // Workspace item of a (chunk slot, head), fp32 blocks (row-major):
 constexpr int kItemW = 0;         // W [64][128]; dKg after the reverse pass
@@ -96,8 +94,6 @@ constexpr int kItemFloats = 98752;  // 395,008 bytes, a multiple of 256
 static_assert(kItemPart + kD + 1 <= kItemFloats && kItemFloats % 64 == 0, "item layout");
 
 constexpr int kStage = 16 * (kLs + kLd);  // GEMM staging floats
-constexpr int kPrepFloats = 3 * kC * kLd + 3 * kC * kLs + 80 * kLd + kStage + kC;
-constexpr int kGradFloats = 3 * kC * kLd + 2 * kC * kLs + 80 * kLd + kStage + 16 * kD + 4 * kC;
 constexpr int kProdFloats = kC * kLd + kStage;
 
 __device__ __forceinline__ float warp_sum(float x) {
@@ -114,6 +110,40 @@ __device__ __forceinline__ void load4(const uint16_t* p, float (&x)[4]) {
   x[3] = b.y;
 }
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+// packed pairs of fp32 (low word = first element) and the paired FMA, two
+// IEEE fused multiply-adds per instruction
+typedef unsigned long long f2_t;
+__device__ __forceinline__ f2_t pk2(float a, float b) {
+  f2_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 up2(f2_t r) {
+  float2 f;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(r));
+  return f;
+}
+__device__ __forceinline__ f2_t fma2(f2_t a, f2_t b, f2_t c) {
+  f2_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ ulonglong2 ld2x2(const float* p) { return *reinterpret_cast<const ulonglong2*>(p); }
+__device__ __forceinline__ void ld8(const float* p, float (&x)[8]) {  // p 16-byte aligned
+  const float4 a = ld4(p), b = ld4(p + 4);
+  x[0] = a.x;
+  x[1] = a.y;
+  x[2] = a.z;
+  x[3] = a.w;
+  x[4] = b.x;
+  x[5] = b.y;
+  x[6] = b.z;
+  x[7] = b.w;
+}
+// e^x of a decay exponent (x <= 0 up to rounding): the hardware exponential,
+// relative error a few 1e-7 plus |x| 2^-24 from the base change, far inside
+// the gradients' tolerance
+__device__ __forceinline__ float dexp(float x) { return __expf(x); }
 __device__ __forceinline__ void st4(float* p, float a, float b, float c, float d) {
   *reinterpret_cast<float4*>(p) = make_float4(a, b, c, d);
 }
@@ -146,11 +176,28 @@ __device__ __forceinline__ float gate_a(int mode, float z, float amul, float lb,
 __device__ __forceinline__ float gate_mul(const BwdParams& p, int h) {
   return (p.A_log && p.gate_mode != kGateLogspace) ? expf(p.A_log[h]) : 1.f;
 }
-// z = g + dt_bias (logspace: g) of element (row, c)
-__device__ __forceinline__ float gate_z(const BwdParams& p, int64_t row, int h, int c) {
-  const float g = p.g32 ? p.g32[row * kD + c] : bf16_to_f(p.g[row * kD + c]);
-  if (p.gate_mode == kGateLogspace || !p.dt_bias) return g;
-  return g + p.dt_bias[h * kD + c];
+// z of elements (row, c0 .. c0 + 7), c0 a multiple of 8
+__device__ __forceinline__ void gate_z8(const BwdParams& p, int64_t row, int h, int c0, float (&z)[8]) {
+  if (p.g32) {
+    ld8(p.g32 + row * kD + c0, z);
+  } else {
+    const uint4 r = *reinterpret_cast<const uint4*>(p.g + row * kD + c0);
+    const float2 a = unpack_bf16(r.x), b = unpack_bf16(r.y), c = unpack_bf16(r.z), d = unpack_bf16(r.w);
+    z[0] = a.x;
+    z[1] = a.y;
+    z[2] = b.x;
+    z[3] = b.y;
+    z[4] = c.x;
+    z[5] = c.y;
+    z[6] = d.x;
+    z[7] = d.y;
+  }
+  if (p.gate_mode != kGateLogspace && p.dt_bias) {
+    float d[8];
+    ld8(p.dt_bias + h * kD + c0, d);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) z[j] += d[j];
+  }
 }
 
 // Token range of a chunk slot: rows t0 .. t0 + L - 1 of sequence n.  False for
@@ -194,29 +241,37 @@ __device__ __forceinline__ void seq_chunks(const BwdParams& p, int64_t n, int64_
 
 // The chunk's rows of k and q (L2-normalised if asked) into Kh, Qh [64][kLd],
 // beta into vb, the norm factors 1 / sqrt(|x|^2 + eps) into rq, rk (if given);
-// rows >= L are zero.  One warp per row, lane = 4 channels.
+// rows >= L are zero.  One warp per row, lane = 4 channels; kNT threads.
+template <int kNT>
 __device__ void load_rows(const BwdParams& p, const ChunkLoc& cl, int h, float* Kh, float* Qh,
                           float* vb, float* rq, float* rk) {
+  constexpr int kNW = kNT / 32, kRows = kC / kNW;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int t = warp; t < kC; t += 8) {
-    float q[4] = {0.f, 0.f, 0.f, 0.f}, k[4] = {0.f, 0.f, 0.f, 0.f};
-    float b = 0.f;
-    if (t < cl.L) {
-      const int64_t row = (cl.t0 + t) * p.H + h;
-      load4(p.q + row * kD + 4 * lane, q);
-      load4(p.k + row * kD + 4 * lane, k);
-      const float braw = bf16_to_f(p.beta[row]);
-      b = p.beta_prob ? braw : 1.f / (1.f + expf(-braw));
+  float q[kRows][4], k[kRows][4], braw[kRows];
+#pragma unroll
+  for (int i = 0; i < kRows; ++i) {  // every load of the warp's rows before any use (rows
+    const int t = min(warp + kNW * i, cl.L - 1);  // past the chunk re-read its last row)
+    const int64_t row = (cl.t0 + t) * p.H + h;
+    load4(p.q + row * kD + 4 * lane, q[i]);
+    load4(p.k + row * kD + 4 * lane, k[i]);
+    braw[i] = bf16_to_f(p.beta[row]);
+  }
+#pragma unroll
+  for (int i = 0; i < kRows; ++i) {
+    const int t = warp + kNW * i;
+    if (t >= cl.L) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) q[i][c] = k[i][c] = 0.f;
     }
     float sq = 1.f, sk = 1.f;
     if (p.l2norm) {
-      sq = rsqrtf(warp_sum(q[0] * q[0] + q[1] * q[1] + q[2] * q[2] + q[3] * q[3]) + 1e-6f);
-      sk = rsqrtf(warp_sum(k[0] * k[0] + k[1] * k[1] + k[2] * k[2] + k[3] * k[3]) + 1e-6f);
+      sq = rsqrtf(warp_sum(q[i][0] * q[i][0] + q[i][1] * q[i][1] + q[i][2] * q[i][2] + q[i][3] * q[i][3]) + 1e-6f);
+      sk = rsqrtf(warp_sum(k[i][0] * k[i][0] + k[i][1] * k[i][1] + k[i][2] * k[i][2] + k[i][3] * k[i][3]) + 1e-6f);
     }
-    st4(Qh + t * kLd + 4 * lane, q[0] * sq, q[1] * sq, q[2] * sq, q[3] * sq);
-    st4(Kh + t * kLd + 4 * lane, k[0] * sk, k[1] * sk, k[2] * sk, k[3] * sk);
+    st4(Qh + t * kLd + 4 * lane, q[i][0] * sq, q[i][1] * sq, q[i][2] * sq, q[i][3] * sq);
+    st4(Kh + t * kLd + 4 * lane, k[i][0] * sk, k[i][1] * sk, k[i][2] * sk, k[i][3] * sk);
     if (lane == 0) {
-      vb[t] = b;
+      vb[t] = t < cl.L ? (p.beta_prob ? braw[i] : 1.f / (1.f + expf(-braw[i]))) : 0.f;
       if (rq) rq[t] = sq;
       if (rk) rk[t] = sk;
     }
@@ -224,25 +279,39 @@ __device__ void load_rows(const BwdParams& p, const ChunkLoc& cl, int h, float* 
 }
 
 // Gamma [64][kLd]: the in-chunk cumulative sums of the activated gate (a = 0 on
-// rows >= L).  Ends with a barrier.
+// rows >= L).  kNT threads: thread = (channel, group of 64 / (kNT / 128)
+// consecutive tokens); each group then adds the totals of the groups before it.
+// Ends with a barrier.
+template <int kNT>
 __device__ void gate_cumsum(const BwdParams& p, const ChunkLoc& cl, int h, float* Gm) {
+  constexpr int kG = kNT / kD, kN = kC / kG;
+  const int c = threadIdx.x & (kD - 1), grp = threadIdx.x >> 7;
   const float amul = gate_mul(p, h);
-  for (int e = threadIdx.x; e < kC * kD; e += blockDim.x) {
-    const int t = e >> 7, c = e & (kD - 1);
-    float a = 0.f;
-    if (t < cl.L) {
-      float d1, d2;
-      a = gate_a(p.gate_mode, gate_z(p, (cl.t0 + t) * p.H + h, h, c), amul, p.lower_bound, d1, d2);
-    }
-    Gm[t * kLd + c] = a;
+  const float dtb = (p.gate_mode != kGateLogspace && p.dt_bias) ? p.dt_bias[h * kD + c] : 0.f;
+  float z[kN];
+  const int64_t e0 = (cl.t0 * p.H + h) * kD + c, ld = p.H * kD;
+  if (p.g32) {  // every load first (rows past the chunk re-read its last row)
+#pragma unroll
+    for (int i = 0; i < kN; ++i) z[i] = p.g32[e0 + min(kN * grp + i, cl.L - 1) * ld];
+  } else {
+#pragma unroll
+    for (int i = 0; i < kN; ++i) z[i] = bf16_to_f(p.g[e0 + min(kN * grp + i, cl.L - 1) * ld]);
+  }
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < kN; ++i) {
+    const int t = kN * grp + i;
+    float d1, d2;
+    if (t < cl.L) acc += gate_a(p.gate_mode, z[i] + dtb, amul, p.lower_bound, d1, d2);
+    Gm[t * kLd + c] = acc;
   }
   __syncthreads();
-  if (threadIdx.x < kD) {
-    float acc = 0.f;
-    for (int t = 0; t < kC; ++t) {
-      acc += Gm[t * kLd + threadIdx.x];
-      Gm[t * kLd + threadIdx.x] = acc;
-    }
+  float base = 0.f;
+  for (int g = 0; g < grp; ++g) base += Gm[(kN * g + kN - 1) * kLd + c];
+  __syncthreads();
+  if (grp) {
+#pragma unroll 8
+    for (int i = 0; i < kN; ++i) Gm[(kN * grp + i) * kLd + c] += base;
   }
   __syncthreads();
 }
@@ -275,60 +344,84 @@ __device__ __forceinline__ float opd_at(const Opd& o, int r, int c) {
 // 64 + 4 tx + j - 4 (j >= 4, BN = 128).  Staged through `stage` in
 // 16-deep slices; begins and ends with a barrier.
 
+// 256 threads of the CTA (local index lt) take part; every thread of the CTA
+// must call it (it holds the CTA's barriers), with active = false for the others.
 template <int BN, bool kAT, bool kBT>
-__device__ void gemm64(float (&acc)[4][BN / 16], const Opd& a, const Opd& b, int kd, float* stage) {
+__device__ void gemm64(float (&acc)[4][BN / 16], const Opd& a, const Opd& b, int kd, float* stage,
+                       int lt, bool active) {
   constexpr int kBs = BN + 4;
   float* As = stage;             // [16][kLs]: As[k][m]
   float* Bs = stage + 16 * kLs;  // [16][kBs]: Bs[k][n]
-  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-  for (int k0 = 0; k0 < kd; k0 += 16) {
-    __syncthreads();
+  const int tid = lt, ty = tid >> 4, tx = tid & 15;
+  float ra[4], rb[BN / 16];
+  auto fetch = [&](int k0) {  // the slice's operands into registers
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int e = tid + 256 * i;
-      if (kAT) {
-        const int m = e & 63, k = e >> 6;
-        As[k * kLs + m] = opd_at(a, k0 + k, m);
-      } else {
-        const int k = e & 15, m = e >> 4;
-        As[k * kLs + m] = opd_at(a, m, k0 + k);
-      }
+      ra[i] = kAT ? opd_at(a, k0 + (e >> 6), e & 63) : opd_at(a, e >> 4, k0 + (e & 15));
     }
 #pragma unroll
     for (int i = 0; i < BN / 16; ++i) {
       const int e = tid + 256 * i;
-      if (kBT) {
-        const int k = e & 15, n = e >> 4;
-        Bs[k * kBs + n] = opd_at(b, n, k0 + k);
-      } else {
-        const int n = e % BN, k = e / BN;
-        Bs[k * kBs + n] = opd_at(b, k0 + k, n);
-      }
+      rb[i] = kBT ? opd_at(b, e >> 4, k0 + (e & 15)) : opd_at(b, k0 + e / BN, e % BN);
+    }
+  };
+  __syncthreads();  // operands written to shared memory before the call are complete
+  f2_t c2[4][BN / 32];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < BN / 32; ++j) c2[i][j] = pk2(acc[i][2 * j], acc[i][2 * j + 1]);
+  if (active) fetch(0);
+  for (int k0 = 0; k0 < kd; k0 += 16) {
+    __syncthreads();  // the previous slice is consumed
+    if (!active) {
+      __syncthreads();
+      continue;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = tid + 256 * i;
+      if (kAT) As[(e >> 6) * kLs + (e & 63)] = ra[i];
+      else As[(e & 15) * kLs + (e >> 4)] = ra[i];
+    }
+#pragma unroll
+    for (int i = 0; i < BN / 16; ++i) {
+      const int e = tid + 256 * i;
+      if (kBT) Bs[(e & 15) * kBs + (e >> 4)] = rb[i];
+      else Bs[(e / BN) * kBs + e % BN] = rb[i];
     }
     __syncthreads();
+    if (k0 + 16 < kd) fetch(k0 + 16);  // in flight during this slice's products
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) {
       const float4 av = ld4(As + kk * kLs + 4 * ty);
       const float ar[4] = {av.x, av.y, av.z, av.w};
-      float br[BN / 16];
-      const float4 b0 = ld4(Bs + kk * kBs + 4 * tx);
+      f2_t br[BN / 32];
+      const ulonglong2 b0 = ld2x2(Bs + kk * kBs + 4 * tx);
       br[0] = b0.x;
       br[1] = b0.y;
-      br[2] = b0.z;
-      br[3] = b0.w;
       if constexpr (BN == 128) {
-        const float4 b1 = ld4(Bs + kk * kBs + 64 + 4 * tx);
-        br[4] = b1.x;
-        br[5] = b1.y;
-        br[6] = b1.z;
-        br[7] = b1.w;
+        const ulonglong2 b1 = ld2x2(Bs + kk * kBs + 64 + 4 * tx);
+        br[2] = b1.x;
+        br[3] = b1.y;
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 4; ++i) {
+        const f2_t a2 = pk2(ar[i], ar[i]);
 #pragma unroll
-        for (int j = 0; j < BN / 16; ++j) acc[i][j] = fmaf(ar[i], br[j], acc[i][j]);
+        for (int j = 0; j < BN / 32; ++j) c2[i][j] = fma2(a2, br[j], c2[i][j]);
+      }
     }
   }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < BN / 32; ++j) {
+      const float2 v = up2(c2[i][j]);
+      acc[i][2 * j] = v.x;
+      acc[i][2 * j + 1] = v.y;
+    }
   __syncthreads();
 }
 
@@ -341,7 +434,10 @@ __device__ __forceinline__ void zero_acc(float (&acc)[4][N]) {
 }
 
 // ==== 1. prep ====
-__global__ void __launch_bounds__(256, 1) kda_bwd_prep_kernel(BwdParams p) {
+constexpr int kPT = 512;  // threads of the prep and chunk-gradient kernels
+constexpr int kPrepFloats = 3 * kC * kLd + 3 * kC * kLs + 80 * kLd + 2 * kStage + kC;
+
+__global__ void __launch_bounds__(kPT, 1) kda_bwd_prep_kernel(BwdParams p) {
   extern __shared__ __align__(16) float sm[];
   float* Kh = sm;
   float* Qh = Kh + kC * kLd;
@@ -349,42 +445,41 @@ __global__ void __launch_bounds__(256, 1) kda_bwd_prep_kernel(BwdParams p) {
   float* Gs = Gm + kC * kLd;  // G, then T
   float* Ps = Gs + kC * kLs;
   float* Mi = Ps + kC * kLs;
-  float* X = Mi + kC * kLs;   // [80][kLd]: Lk, Lq, R; then Kg
-  float* stage = X + 80 * kLd;
-  float* vb = stage + kStage;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float* X = Mi + kC * kLs;   // [80][kLd]: Lk, Lq, R; the inverse's block sums; then Kg
+  float* stage = X + 80 * kLd;  // two GEMM staging areas
+  float* vb = stage + 2 * kStage;
+  const int tid = threadIdx.x;
   const int64_t item = blockIdx.x, slot = item / p.H;
   const int h = (int)(item - slot * p.H);
   ChunkLoc cl;
   if (!locate(p, slot, cl)) return;
   float* it = p.ws + item * (int64_t)kItemFloats;
 
-  load_rows(p, cl, h, Kh, Qh, vb, nullptr, nullptr);
+  load_rows<kPT>(p, cl, h, Kh, Qh, vb, nullptr, nullptr);
   __syncthreads();
-  gate_cumsum(p, cl, h, Gm);
+  gate_cumsum<kPT>(p, cl, h, Gm);
 
-  // G and P inside the 16-token diagonal blocks, pair by pair: one warp per pair
-  for (int e = warp; e < 4 * 136; e += 8) {
+  // G and P inside the 16-token diagonal blocks, pair by pair: one thread per pair
+  for (int e = tid; e < 4 * 136; e += kPT) {
     const int blk = e / 136, r = e - blk * 136;
     int ii = 0;
     while ((ii + 1) * (ii + 2) / 2 <= r) ++ii;
     const int jj = r - ii * (ii + 1) / 2;
     const int i = 16 * blk + ii, j = 16 * blk + jj;
-    const float4 gi = ld4(Gm + i * kLd + 4 * lane), gj = ld4(Gm + j * kLd + 4 * lane);
-    const float4 ki = ld4(Kh + i * kLd + 4 * lane), kj = ld4(Kh + j * kLd + 4 * lane);
-    const float4 qi = ld4(Qh + i * kLd + 4 * lane);
-    const float f0 = expf(gi.x - gj.x), f1 = expf(gi.y - gj.y), f2 = expf(gi.z - gj.z), f3 = expf(gi.w - gj.w);
-    float sg = ki.x * kj.x * f0 + ki.y * kj.y * f1 + ki.z * kj.z * f2 + ki.w * kj.w * f3;
-    float sp = qi.x * kj.x * f0 + qi.y * kj.y * f1 + qi.z * kj.z * f2 + qi.w * kj.w * f3;
-    sg = warp_sum(sg);
-    sp = warp_sum(sp);
-    if (lane == 0) {
-      Gs[i * kLs + j] = j < i ? sg : 0.f;
-      Ps[i * kLs + j] = sp;
+    float sg = 0.f, sp = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < kD; c += 4) {
+      const float4 gi = ld4(Gm + i * kLd + c), gj = ld4(Gm + j * kLd + c);
+      const float4 ki = ld4(Kh + i * kLd + c), kj = ld4(Kh + j * kLd + c), qi = ld4(Qh + i * kLd + c);
+      const float f0 = dexp(gi.x - gj.x) * kj.x, f1 = dexp(gi.y - gj.y) * kj.y;
+      const float f2 = dexp(gi.z - gj.z) * kj.z, f3 = dexp(gi.w - gj.w) * kj.w;
+      sg += ki.x * f0 + ki.y * f1 + ki.z * f2 + ki.w * f3;
+      sp += qi.x * f0 + qi.y * f1 + qi.z * f2 + qi.w * f3;
     }
+    Gs[i * kLs + j] = j < i ? sg : 0.f;
+    Ps[i * kLs + j] = sp;
   }
-  // zero the upper triangles and the off-diagonal blocks' upper parts
-  for (int e = tid; e < kC * kC; e += 256) {
+  for (int e = tid; e < kC * kC; e += kPT) {  // upper triangles
     const int i = e >> 6, j = e & 63;
     if (j > i) {
       Gs[i * kLs + j] = 0.f;
@@ -399,25 +494,25 @@ __global__ void __launch_bounds__(256, 1) kda_bwd_prep_kernel(BwdParams p) {
     float* Lq = X + 16 * kLd;
     float* R = X + 32 * kLd;
     __syncthreads();
-    for (int e = tid; e < (32 + r) * 32; e += 256) {
+    for (int e = tid; e < (32 + r) * 32; e += kPT) {
       const int row = e >> 5, c = 4 * (e & 31);
       const float4 gr = ld4(Gm + r * kLd + c);
       if (row < 32) {  // Lk / Lq rows of block I
         const int ii = row & 15, i = r + ii;
         const float4 gi = ld4(Gm + i * kLd + c);
-        const float l0 = expf(gi.x - gr.x), l1 = expf(gi.y - gr.y), l2 = expf(gi.z - gr.z), l3 = expf(gi.w - gr.w);
+        const float l0 = dexp(gi.x - gr.x), l1 = dexp(gi.y - gr.y), l2 = dexp(gi.z - gr.z), l3 = dexp(gi.w - gr.w);
         const float4 x = ld4((row < 16 ? Kh : Qh) + i * kLd + c);
         st4((row < 16 ? Lk : Lq) + ii * kLd + c, x.x * l0, x.y * l1, x.z * l2, x.w * l3);
       } else {
         const int j = row - 32;
         const float4 gj = ld4(Gm + j * kLd + c);
         const float4 x = ld4(Kh + j * kLd + c);
-        st4(R + j * kLd + c, x.x * expf(gr.x - gj.x), x.y * expf(gr.y - gj.y), x.z * expf(gr.z - gj.z),
-            x.w * expf(gr.w - gj.w));
+        st4(R + j * kLd + c, x.x * dexp(gr.x - gj.x), x.y * dexp(gr.y - gj.y), x.z * dexp(gr.z - gj.z),
+            x.w * dexp(gr.w - gj.w));
       }
     }
     __syncthreads();
-    for (int e = tid; e < 16 * r; e += 256) {
+    for (int e = tid; e < 16 * r; e += kPT) {
       const int ii = e / r, j = e - ii * r;
       float sg = 0.f, sp = 0.f;
 #pragma unroll 4
@@ -431,96 +526,202 @@ __global__ void __launch_bounds__(256, 1) kda_bwd_prep_kernel(BwdParams p) {
     }
   }
   __syncthreads();
-  // Minv = (I + Diag(beta) G)^-1 by forward substitution: four lanes per column
-  {
-    const int col = warp * 8 + (lane >> 2), l = lane & 3;
-    for (int i = 0; i < kC; ++i) {
-      float s = 0.f;
-      for (int m = col + l; m < i; m += 4) s = fmaf(Gs[i * kLs + m], Mi[m * kLs + col], s);
-      s += __shfl_xor_sync(0xffffffffu, s, 1);
-      s += __shfl_xor_sync(0xffffffffu, s, 2);
-      if (l == 0) Mi[i * kLs + col] = i < col ? 0.f : (i == col ? 1.f : -vb[i] * s);
-      __syncwarp();
+  // Minv = (I + A)^-1, A = Diag(beta) G strictly lower, by 16 x 16 blocks: the
+  // diagonal blocks' inverses by forward substitution (one thread per column, in
+  // registers), then block row I left of the diagonal, nearest blocks first:
+  // Minv_IJ = -Minv_II sum_{J <= K < I} A_IK Minv_KJ.
+  if (tid < kC) {
+    const int b = tid >> 4, j = tid & 15, o = 16 * b;
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float acc = 0.f;
+#pragma unroll
+      for (int m = 0; m < i; ++m) acc = fmaf(Gs[(o + i) * kLs + o + m], x[m], acc);
+      x[i] = (i == j ? 1.f : 0.f) - vb[o + i] * acc;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) Mi[(o + i) * kLs + o + j] = x[i];
+  } else {
+    for (int e = tid - kC; e < kC * kC; e += kPT - kC) {  // above the diagonal blocks
+      const int i = e >> 6, j = e & 63;
+      if ((j >> 4) > (i >> 4)) Mi[i * kLs + j] = 0.f;
+    }
+  }
+#pragma unroll 1
+  for (int d = 1; d < 4; ++d) {  // block distance I - J
+    float* Tm = X;               // [pairs][16][16]: sum_K A_IK Minv_KJ
+    const int pairs = 4 - d;
+    __syncthreads();
+    for (int e = tid; e < pairs * 256; e += kPT) {
+      const int J = e >> 8, I = J + d, r = (e >> 4) & 15, c = e & 15;
+      float acc = 0.f;
+      for (int col = 16 * J; col < 16 * I; ++col) acc = fmaf(Gs[(16 * I + r) * kLs + col], Mi[col * kLs + 16 * J + c], acc);
+      Tm[e] = vb[16 * I + r] * acc;
+    }
+    __syncthreads();
+    for (int e = tid; e < pairs * 256; e += kPT) {
+      const int J = e >> 8, I = J + d, r = (e >> 4) & 15, c = e & 15;
+      float acc = 0.f;
+#pragma unroll
+      for (int m = 0; m < 16; ++m) acc = fmaf(Mi[(16 * I + r) * kLs + 16 * I + m], Tm[(J << 8) + m * 16 + c], acc);
+      Mi[(16 * I + r) * kLs + 16 * J + c] = -acc;
     }
   }
   __syncthreads();
   // write G, P, Minv, gC, Qg, Khat, Kg; T = Minv Diag(beta) over G; Kg into X
-  for (int e = tid; e < kC * kC; e += 256) {
+  for (int e = tid; e < kC * kC; e += kPT) {
     const int i = e >> 6, j = e & 63;
     it[kItemG + e] = Gs[i * kLs + j];
     it[kItemP + e] = Ps[i * kLs + j];
     it[kItemMi + e] = Mi[i * kLs + j];
   }
   __syncthreads();
-  for (int e = tid; e < kC * kC; e += 256) {
+  for (int e = tid; e < kC * kC; e += kPT) {
     const int i = e >> 6, j = e & 63;
     Gs[i * kLs + j] = Mi[i * kLs + j] * vb[j];
   }
-  for (int e = tid; e < kC * 32; e += 256) {
+  for (int e = tid; e < kC * 32; e += kPT) {
     const int t = e >> 5, c = 4 * (e & 31);
     const float4 gt = ld4(Gm + t * kLd + c), gl = ld4(Gm + (kC - 1) * kLd + c);
     const float4 kx = ld4(Kh + t * kLd + c), qx = ld4(Qh + t * kLd + c);
-    const float e0 = expf(gt.x), e1 = expf(gt.y), e2 = expf(gt.z), e3 = expf(gt.w);
+    const float e0 = dexp(gt.x), e1 = dexp(gt.y), e2 = dexp(gt.z), e3 = dexp(gt.w);
     st4(it + kItemQg + t * kD + c, qx.x * e0, qx.y * e1, qx.z * e2, qx.w * e3);
     st4(it + kItemKg + t * kD + c, kx.x * e0, kx.y * e1, kx.z * e2, kx.w * e3);
     st4(X + t * kLd + c, kx.x * e0, kx.y * e1, kx.z * e2, kx.w * e3);
-    st4(it + kItemKh + t * kD + c, kx.x * expf(gl.x - gt.x), kx.y * expf(gl.y - gt.y), kx.z * expf(gl.z - gt.z),
-        kx.w * expf(gl.w - gt.w));
+    st4(it + kItemKh + t * kD + c, kx.x * dexp(gl.x - gt.x), kx.y * dexp(gl.y - gt.y), kx.z * dexp(gl.z - gt.z),
+        kx.w * dexp(gl.w - gt.w));
   }
-  if (tid < kD) it[kItemGC + tid] = expf(Gm[(kC - 1) * kLd + tid]);
-  // W = T Kg, U = T V
-  const int ty = tid >> 4, tx = tid & 15;
+  if (tid < kD) it[kItemGC + tid] = dexp(Gm[(kC - 1) * kLd + tid]);
+  __syncthreads();  // Qh no longer read: V (fp32, rows >= L zero) takes its place
   {
-    float acc[4][8];
-    zero_acc(acc);
-    gemm64<128, false, false>(acc, opd(Gs, kLs, kC), opd(X, kLd, kC), kC, stage);
+    const int lane = tid & 31, warp = tid >> 5;
+    float v4[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      load4(p.v + ((cl.t0 + min(warp + 16 * i, cl.L - 1)) * p.H + h) * kD + 4 * lane, v4[i]);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      float* dst = it + kItemW + (4 * ty + i) * kD;
-      st4(dst + 4 * tx, acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-      st4(dst + 64 + 4 * tx, acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+      const int t = warp + 16 * i;
+      const float z = t < cl.L ? 1.f : 0.f;
+      st4(Qh + t * kLd + 4 * lane, z * v4[i][0], z * v4[i][1], z * v4[i][2], z * v4[i][3]);
     }
   }
+  // W = T Kg (threads 0-255) and U = T V (threads 256-511) side by side
   {
+    const int half = tid >> 8, lt = tid & 255, ty = lt >> 4, tx = lt & 15;
+    const Opd B = opd(half ? Qh : X, kLd, kC);
     float acc[4][8];
     zero_acc(acc);
-    gemm64<128, false, false>(acc, opd(Gs, kLs, kC), opd(p.v + (cl.t0 * p.H + h) * kD, p.H * kD, cl.L, 1), kC,
-                              stage);
+    gemm64<128, false, false>(acc, opd(Gs, kLs, kC), B, kC, stage + half * kStage, lt, true);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      float* dst = it + kItemU + (4 * ty + i) * kD;
+      float* dst = it + (half ? kItemU : kItemW) + (4 * ty + i) * kD;
       st4(dst + 4 * tx, acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
       st4(dst + 64 + 4 * tx, acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
     }
   }
 }
 
+// ---- asynchronous 16-byte copies (global -> shared), per-thread groups ----
+__device__ __forceinline__ void cp16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+// L2 prefetch of `bytes` (a multiple of 16) from a 16-byte aligned address
+__device__ __forceinline__ void l2_prefetch(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
+}
+// rows x 128 fp32 (contiguous in the item) into a [rows][kLd] shared array
+__device__ __forceinline__ void cp_rows128(float* dst, const float* src, int rows, int tid, int nthr) {
+  for (int e = tid; e < rows * 32; e += nthr) cp16(dst + (e >> 5) * kLd + 4 * (e & 31), src + 4 * e);
+}
+
+// Channel quad k (0..15) of half h of a 128-channel row: 16-channel groups
+// alternate between the halves, so that eight lanes reading rows r .. r + 3 of
+// a [..][kLd] array hit eight different bank quads.
+__device__ __forceinline__ int cq(int k, int h) { return 32 * (k >> 2) + 16 * h + 4 * (k & 3); }
+
+// Channels of a product-2 thread: quads c1 = 4 chp(co) and c2 = 64 + c1, chp
+// placing the two co of a quarter-warp four quads apart (with the four token
+// rows of the quarter, eight different bank quads).
+__device__ __forceinline__ int chp(int co) { return ((co >> 1) & 3) + 4 * (co & 1) + 8 * (co >> 3); }
+
+constexpr int kSt = 512;                  // threads of the state passes
+constexpr int kSv = 32;                   // value rows per CTA
+constexpr int kSBlocks = kD / kSv;        // CTAs per (sequence, head)
+constexpr int kSu = kSv + 4;              // row stride of [64][kSv] shared arrays
+constexpr int kFwdFloats = 2 * kC * kLd + kC * kSv + kSv * kLd + kC * kSu + kD;
+constexpr int kRevFloats = 3 * kC * kLd + kC * kLs + kSv * kLd + 2 * kC * kSu + kC * kSv / 2 + kD;
+
 // ==== 2. forward state pass ====
-// CTA = (sequence, head, 16 value rows v0 ..).  Product 1 (Unew = U - W S^T,
-// 64 x 16 over 128 channels): lane = (2 tokens, 4 value rows, channel half),
-// halves combined by a shuffle.  Product 2 (S = S Diag(gC) + Unew^T Khat, 16 x
-// 128 over 64 tokens): thread = (4 value rows, 8 channels, token quarter),
-// quarters combined by shuffles; every quarter keeps the full result.
-__global__ void __launch_bounds__(256) kda_bwd_fwd_state_kernel(BwdParams p) {
-  __shared__ __align__(16) float Ss[kVb * kLd];
-  __shared__ __align__(16) float Un[kC * kVb];
+// CTA = (sequence, head, 32 value rows v0 ..), 512 threads; S of the CTA's rows
+// in registers (product-2 ownership) and shared memory.  Per chunk, W and the
+// CTA's U columns arrive (cp.async) while the previous chunk's product 2 runs,
+// Khat and gC while product 1 runs.  Product 1 (Unew = U - W S^T, 64 x 32 over
+// 128 channels): thread = (2 tokens, 4 value rows, channel half), halves added
+// by a shuffle.  Product 2 (S = S Diag(gC) + Unew^T Khat, 32 x 128 over 64
+// tokens): thread = (4 value rows, channel quads c1 and c1 + 64, tokens t = 4 i + quarter),
+// quarters added by shuffles; every quarter keeps the full result.  Product 1's
+// value rows are v = pv + 8 i (i < 4): rows 8 apart keep its shared-memory
+// reads of S free of bank conflicts.
+__global__ void __launch_bounds__(kSt, 1) kda_bwd_fwd_state_kernel(BwdParams p) {
+  extern __shared__ __align__(16) float sm[];
+  float* Wb = sm;                 // W [64][kLd]
+  float* Kb = Wb + kC * kLd;      // Khat [64][kLd]
+  float* Ub = Kb + kC * kLd;      // U columns [64][kSv]
+  float* Ss = Ub + kC * kSv;      // S [kSv][kLd]
+  float* Un = Ss + kSv * kLd;     // Unew [64][kSu]
+  float* gc = Un + kC * kSu;      // gC [128]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t unit = blockIdx.x / kRowBlocks;
-  const int v0 = kVb * (int)(blockIdx.x - unit * kRowBlocks);
+  const int64_t unit = blockIdx.x / kSBlocks;
+  const int v0 = kSv * (int)(blockIdx.x - unit * kSBlocks);
   const int64_t n = unit / p.H;
   const int h = (int)(unit - n * p.H);
-  // product-2 ownership
-  const int tq = lane & 3, co = ((warp & 1) << 3) | (lane >> 2), vq = warp >> 1;
+  const int tq = lane & 3, co = ((warp & 1) << 3) | (lane >> 2), vq = warp >> 1;  // product 2
+  const int c1 = 4 * chp(co), c2 = c1 + 64;
+  const int ch = tid & 1, pv = (tid >> 1) & 7, pt = 2 * (tid >> 4);               // product 1
+  int64_t first, count;
+  seq_chunks(p, n, first, count);
+  auto item = [&](int64_t ci) { return p.ws + ((first + ci) * p.H + h) * (int64_t)kItemFloats; };
+  auto issue_w = [&](int64_t ci) {  // W and U columns of chunk ci; the chunk after it into L2
+    if (ci + 1 < count && tid == 0) {
+      const float* nx = item(ci + 1);
+      l2_prefetch(nx + kItemW, 3 * kC * kD * 4);  // W, U, Khat
+      l2_prefetch(nx + kItemGC, kD * 4);
+    }
+    if (ci < count) {
+      const float* it = item(ci);
+      cp_rows128(Wb, it + kItemW, kC, tid, kSt);
+      for (int e = tid; e < kC * kSv / 4; e += kSt)
+        cp16(Ub + 4 * e, it + kItemU + (e / (kSv / 4)) * kD + v0 + 4 * (e % (kSv / 4)));
+    }
+    cp_commit();
+  };
+  auto issue_k = [&](int64_t ci) {  // Khat and gC of chunk ci
+    if (ci < count) {
+      const float* it = item(ci);
+      cp_rows128(Kb, it + kItemKh, kC, tid, kSt);
+      if (tid < kD / 4) cp16(gc + 4 * tid, it + kItemGC + 4 * tid);
+    }
+    cp_commit();
+  };
+  issue_w(0);
+  issue_k(0);
   float s[4][8];
   {
-    const int64_t base = (unit * kD + v0 + 4 * vq) * kD + 8 * co;
+    const int64_t base = (unit * kD + v0 + 4 * vq) * kD;
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         float x = 0.f;
         if (p.init) {
-          const int64_t e = base + (int64_t)i * kD + j;
+          const int64_t e = base + (int64_t)i * kD + (j < 4 ? c1 + j : c2 + j - 4);
           x = p.init_bf16 ? bf16_to_f(static_cast<const uint16_t*>(p.init)[e])
                           : static_cast<const float*>(p.init)[e];
         }
@@ -530,35 +731,46 @@ __global__ void __launch_bounds__(256) kda_bwd_fwd_state_kernel(BwdParams p) {
   if (tq == 0)
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      st4(Ss + (4 * vq + i) * kLd + 8 * co, s[i][0], s[i][1], s[i][2], s[i][3]);
-      st4(Ss + (4 * vq + i) * kLd + 8 * co + 4, s[i][4], s[i][5], s[i][6], s[i][7]);
+      st4(Ss + (4 * vq + i) * kLd + c1, s[i][0], s[i][1], s[i][2], s[i][3]);
+      st4(Ss + (4 * vq + i) * kLd + c2, s[i][4], s[i][5], s[i][6], s[i][7]);
     }
-  // product-1 ownership
-  const int ch = lane & 1, pv = (lane >> 1) & 3, pt = 8 * warp + 2 * (lane >> 3);
-  int64_t first, count;
-  seq_chunks(p, n, first, count);
   for (int64_t ci = 0; ci < count; ++ci) {
-    float* it = p.ws + ((first + ci) * p.H + h) * (int64_t)kItemFloats;
-    __syncthreads();  // Ss holds S before this chunk
+    float* it = item(ci);
+    cp_wait<1>();     // W, U of this chunk
+    __syncthreads();  // ... for every thread; Ss holds S before this chunk
     if (tq == 0)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        float* d = it + kItemS0 + (v0 + 4 * vq + i) * kD + 8 * co;
+        float* d = it + kItemS0 + (v0 + 4 * vq + i) * kD + c1;
         st4(d, s[i][0], s[i][1], s[i][2], s[i][3]);
-        st4(d + 4, s[i][4], s[i][5], s[i][6], s[i][7]);
+        st4(d + 64, s[i][4], s[i][5], s[i][6], s[i][7]);
       }
     {
-      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      const float* W0 = it + kItemW + pt * kD;
-#pragma unroll 4
-      for (int c = 64 * ch; c < 64 * ch + 64; c += 4) {
-        const float4 w0 = ld4(W0 + c), w1 = ld4(W0 + kD + c);
+      float acc[2][4];
+      {
+        f2_t a2[2][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 sv = ld4(Ss + (4 * pv + i) * kLd + c);
-          acc[0][i] += w0.x * sv.x + w0.y * sv.y + w0.z * sv.z + w0.w * sv.w;
-          acc[1][i] += w1.x * sv.x + w1.y * sv.y + w1.z * sv.z + w1.w * sv.w;
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) a2[r][i] = 0ull;
+#pragma unroll 4
+        for (int k = 0; k < 16; ++k) {
+          const int c = cq(k, ch);
+          const ulonglong2 w0 = ld2x2(Wb + pt * kLd + c), w1 = ld2x2(Wb + (pt + 1) * kLd + c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const ulonglong2 sv = ld2x2(Ss + (pv + 8 * i) * kLd + c);
+            a2[0][i] = fma2(w0.y, sv.y, fma2(w0.x, sv.x, a2[0][i]));
+            a2[1][i] = fma2(w1.y, sv.y, fma2(w1.x, sv.x, a2[1][i]));
+          }
         }
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 v = up2(a2[r][i]);
+            acc[r][i] = v.x + v.y;
+          }
       }
 #pragma unroll
       for (int r = 0; r < 2; ++r)
@@ -566,127 +778,205 @@ __global__ void __launch_bounds__(256) kda_bwd_fwd_state_kernel(BwdParams p) {
         for (int i = 0; i < 4; ++i) acc[r][i] += __shfl_xor_sync(0xffffffffu, acc[r][i], 1);
       if (ch == 0) {
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          float* u = it + kItemU + (pt + r) * kD + v0 + 4 * pv;
-          const float4 uu = ld4(u);
-          const float n0 = uu.x - acc[r][0], n1 = uu.y - acc[r][1], n2 = uu.z - acc[r][2], n3 = uu.w - acc[r][3];
-          st4(u, n0, n1, n2, n3);
-          st4(Un + (pt + r) * kVb + 4 * pv, n0, n1, n2, n3);
-        }
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int v = pv + 8 * i;
+            const float un = Ub[(pt + r) * kSv + v] - acc[r][i];
+            it[kItemU + (pt + r) * kD + v0 + v] = un;
+            Un[(pt + r) * kSu + v] = un;
+          }
       }
     }
-    __syncthreads();  // Unew complete; Ss no longer read
+    __syncthreads();  // Unew complete; Wb, Ub, Ss free
+    issue_w(ci + 1);
+    cp_wait<1>();     // Khat, gC of this chunk
+    __syncthreads();
     {
       float acc[4][8];
-      zero_acc(acc);
-      const float* K0 = it + kItemKh + 8 * co;
+      {
+        f2_t a2[4][4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) a2[a][j] = 0ull;
 #pragma unroll 4
-      for (int t = 16 * tq; t < 16 * tq + 16; ++t) {
-        const float4 u = ld4(Un + t * kVb + 4 * vq);
-        const float4 k0 = ld4(K0 + t * kD), k1 = ld4(K0 + t * kD + 4);
-        const float ur[4] = {u.x, u.y, u.z, u.w}, kr[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+        for (int i = 0; i < 16; ++i) {
+          const int t = 4 * i + tq;
+          const float4 u = ld4(Un + t * kSu + 4 * vq);
+          const ulonglong2 k0 = ld2x2(Kb + t * kLd + c1), k1 = ld2x2(Kb + t * kLd + c2);
+          const float ur[4] = {u.x, u.y, u.z, u.w};
+          const f2_t kr[4] = {k0.x, k0.y, k1.x, k1.y};
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+          for (int a = 0; a < 4; ++a) {
+            const f2_t uu = pk2(ur[a], ur[a]);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(ur[i], kr[j], acc[i][j]);
+            for (int j = 0; j < 4; ++j) a2[a][j] = fma2(uu, kr[j], a2[a][j]);
+          }
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 v = up2(a2[a][j]);
+            acc[a][2 * j] = v.x;
+            acc[a][2 * j + 1] = v.y;
+          }
       }
-      const float4 g0 = ld4(it + kItemGC + 8 * co), g1 = ld4(it + kItemGC + 8 * co + 4);
+      const float4 g0 = ld4(gc + c1), g1 = ld4(gc + c2);
       const float gr[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          float x = acc[i][j];
+          float x = acc[a][j];
           x += __shfl_xor_sync(0xffffffffu, x, 1);
           x += __shfl_xor_sync(0xffffffffu, x, 2);
-          s[i][j] = fmaf(s[i][j], gr[j], x);
+          s[a][j] = fmaf(s[a][j], gr[j], x);
         }
       if (tq == 0)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          st4(Ss + (4 * vq + i) * kLd + 8 * co, s[i][0], s[i][1], s[i][2], s[i][3]);
-          st4(Ss + (4 * vq + i) * kLd + 8 * co + 4, s[i][4], s[i][5], s[i][6], s[i][7]);
+        for (int a = 0; a < 4; ++a) {
+          st4(Ss + (4 * vq + a) * kLd + c1, s[a][0], s[a][1], s[a][2], s[a][3]);
+          st4(Ss + (4 * vq + a) * kLd + c2, s[a][4], s[a][5], s[a][6], s[a][7]);
         }
     }
+    __syncthreads();  // Kb, gc, Un free
+    issue_k(ci + 1);
   }
+  cp_wait<0>();
 }
 
 // ==== 3. reverse state pass ====
-// Same grid and ownership as the forward pass.  Product A (dU = scale P^T dO +
-// Khat dS^T, 64 x 16): lane = (2 tokens, 4 value rows, half of the 64 tokens j
-// and of the 128 channels).  Product B (dS = dS Diag(gC) + scale dO^T Qg -
-// dU^T W, 16 x 128 over 64 tokens).
-__global__ void __launch_bounds__(256) kda_bwd_rev_state_kernel(BwdParams p) {
-  __shared__ __align__(16) float Ds[kVb * kLd];
-  __shared__ __align__(16) float Os[kC * kVb];   // scale dO, this CTA's value columns
-  __shared__ __align__(16) float Us[kC * kVb];   // dU
+// Same grid, threads and ownership as the forward pass, chunks last to first.
+// Per chunk, Khat, P, the CTA's dout columns and gC arrive while the previous
+// chunk's product B runs, Qg and W while product A runs.  Product A (dU =
+// scale P^T dO + Khat dS^T, 64 x 32): thread = (2 tokens, 4 value rows, half of
+// the 128 channels and of the 64 tokens j, by parity).  Product B (dS = dS Diag(gC) +
+// scale dO^T Qg - dU^T W, 32 x 128 over 64 tokens).
+__global__ void __launch_bounds__(kSt, 1) kda_bwd_rev_state_kernel(BwdParams p) {
+  extern __shared__ __align__(16) float sm[];
+  float* Kb = sm;                 // Khat [64][kLd]
+  float* Qb = Kb + kC * kLd;      // Qg
+  float* Wb = Qb + kC * kLd;      // W
+  float* Pb = Wb + kC * kLd;      // P [64][kLs]
+  float* Ds = Pb + kC * kLs;      // dS [kSv][kLd]
+  float* Os = Ds + kSv * kLd;     // scale dO [64][kSu]
+  float* Us = Os + kC * kSu;      // dU [64][kSu]
+  uint16_t* Ob = reinterpret_cast<uint16_t*>(Us + kC * kSu);  // dO bf16 [64][kSv]
+  float* gc = Us + kC * kSu + kC * kSv / 2;                      // gC [128]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t unit = blockIdx.x / kRowBlocks;
-  const int v0 = kVb * (int)(blockIdx.x - unit * kRowBlocks);
+  const int64_t unit = blockIdx.x / kSBlocks;
+  const int v0 = kSv * (int)(blockIdx.x - unit * kSBlocks);
   const int64_t n = unit / p.H;
   const int h = (int)(unit - n * p.H);
   const int tq = lane & 3, co = ((warp & 1) << 3) | (lane >> 2), vq = warp >> 1;
+  const int c1 = 4 * chp(co), c2 = c1 + 64;
+  const int ch = tid & 1, pv = (tid >> 1) & 7, pt = 2 * (tid >> 4);
+  int64_t first, count;
+  seq_chunks(p, n, first, count);
+  const int64_t bos = p.cu ? p.cu[n] : n * p.T, eos = p.cu ? p.cu[n + 1] : (n + 1) * p.T;
+  auto item = [&](int64_t ci) { return p.ws + ((first + ci) * p.H + h) * (int64_t)kItemFloats; };
+  auto chunk_len = [&](int64_t ci) { return (int)min((int64_t)kC, eos - bos - ci * kC); };
+  auto issue_a = [&](int64_t ci) {  // Khat, P, dout columns, gC of chunk ci; the chunk before it into L2
+    if (ci >= 1 && tid == 0) {
+      const float* nx = item(ci - 1);
+      l2_prefetch(nx + kItemW, kC * kD * 4);
+      l2_prefetch(nx + kItemKh, 2 * kC * kD * 4);  // Khat, Qg
+      l2_prefetch(nx + kItemP, kC * kC * 4);
+      l2_prefetch(nx + kItemGC, kD * 4);
+    }
+    if (ci >= 0) {
+      const float* it = item(ci);
+      cp_rows128(Kb, it + kItemKh, kC, tid, kSt);
+      for (int e = tid; e < kC * 16; e += kSt) cp16(Pb + (e >> 4) * kLs + 4 * (e & 15), it + kItemP + 4 * e);
+      const int L = chunk_len(ci);
+      for (int e = tid; e < L * (kSv / 8); e += kSt) {
+        const int t = e / (kSv / 8), q = e % (kSv / 8);
+        cp16(Ob + t * kSv + 8 * q, p.dout + ((bos + ci * kC + t) * p.H + h) * kD + v0 + 8 * q);
+      }
+      if (tid < kD / 4) cp16(gc + 4 * tid, it + kItemGC + 4 * tid);
+    }
+    cp_commit();
+  };
+  auto issue_b = [&](int64_t ci) {  // Qg and W of chunk ci
+    if (ci >= 0) {
+      const float* it = item(ci);
+      cp_rows128(Qb, it + kItemQg, kC, tid, kSt);
+      cp_rows128(Wb, it + kItemW, kC, tid, kSt);
+    }
+    cp_commit();
+  };
+  issue_a(count - 1);
+  issue_b(count - 1);
   float s[4][8];
   {
-    const int64_t base = (unit * kD + v0 + 4 * vq) * kD + 8 * co;
+    const int64_t base = (unit * kD + v0 + 4 * vq) * kD;
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) s[i][j] = p.dfinal ? p.dfinal[base + (int64_t)i * kD + j] : 0.f;
+      for (int j = 0; j < 8; ++j)
+        s[i][j] = p.dfinal ? p.dfinal[base + (int64_t)i * kD + (j < 4 ? c1 + j : c2 + j - 4)] : 0.f;
   }
   if (tq == 0)
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      st4(Ds + (4 * vq + i) * kLd + 8 * co, s[i][0], s[i][1], s[i][2], s[i][3]);
-      st4(Ds + (4 * vq + i) * kLd + 8 * co + 4, s[i][4], s[i][5], s[i][6], s[i][7]);
+      st4(Ds + (4 * vq + i) * kLd + c1, s[i][0], s[i][1], s[i][2], s[i][3]);
+      st4(Ds + (4 * vq + i) * kLd + c2, s[i][4], s[i][5], s[i][6], s[i][7]);
     }
-  const int ch = lane & 1, pv = (lane >> 1) & 3, pt = 8 * warp + 2 * (lane >> 3);
-  int64_t first, count;
-  seq_chunks(p, n, first, count);
   for (int64_t ci = count - 1; ci >= 0; --ci) {
-    const int64_t slot = first + ci;
-    float* it = p.ws + (slot * p.H + h) * (int64_t)kItemFloats;
-    const int64_t t0 = p.cu ? p.cu[n] + ci * kC : n * p.T + ci * kC;
-    const int L = (int)min((int64_t)kC, (p.cu ? p.cu[n + 1] : (n + 1) * p.T) - t0);
-    __syncthreads();  // Ds holds dS_C; Os, Us free
-    for (int e = tid; e < kC * kVb; e += 256) {
-      const int t = e >> 4, v = e & 15;
-      Os[e] = t < L ? p.scale * bf16_to_f(p.dout[((t0 + t) * p.H + h) * kD + v0 + v]) : 0.f;
+    float* it = item(ci);
+    const int L = chunk_len(ci);
+    cp_wait<1>();     // Khat, P, dout, gC of this chunk
+    __syncthreads();  // ... for every thread; Ds holds dS_C
+    for (int e = tid; e < kC * kSv; e += kSt) {
+      const int t = e / kSv, v = e % kSv;
+      Os[t * kSu + v] = t < L ? p.scale * bf16_to_f(Ob[e]) : 0.f;
     }
     if (tq == 0)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        float* d = it + kItemDS + (v0 + 4 * vq + i) * kD + 8 * co;
+        float* d = it + kItemDS + (v0 + 4 * vq + i) * kD + c1;
         st4(d, s[i][0], s[i][1], s[i][2], s[i][3]);
-        st4(d + 4, s[i][4], s[i][5], s[i][6], s[i][7]);
+        st4(d + 64, s[i][4], s[i][5], s[i][6], s[i][7]);
       }
     __syncthreads();
     {
-      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      const float* K0 = it + kItemKh + pt * kD;
+      float acc[2][4];
+      {
+        f2_t a2[2][4];
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) a2[r][i] = 0ull;
 #pragma unroll 4
-      for (int c = 64 * ch; c < 64 * ch + 64; c += 4) {
-        const float4 k0 = ld4(K0 + c), k1 = ld4(K0 + kD + c);
+        for (int k = 0; k < 16; ++k) {
+          const int c = cq(k, ch);
+          const ulonglong2 k0 = ld2x2(Kb + pt * kLd + c), k1 = ld2x2(Kb + (pt + 1) * kLd + c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const ulonglong2 d = ld2x2(Ds + (pv + 8 * i) * kLd + c);
+            a2[0][i] = fma2(k0.y, d.y, fma2(k0.x, d.x, a2[0][i]));
+            a2[1][i] = fma2(k1.y, d.y, fma2(k1.x, d.x, a2[1][i]));
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 v = up2(a2[r][i]);
+            acc[r][i] = v.x + v.y;
+          }
+      }
+#pragma unroll 4
+      for (int j = ch; j < kC; j += 2) {  // tokens split by parity: the halves' rows sit on different banks
+        const float2 pj = *reinterpret_cast<const float2*>(Pb + j * kLs + pt);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float4 d = ld4(Ds + (4 * pv + i) * kLd + c);
-          acc[0][i] += k0.x * d.x + k0.y * d.y + k0.z * d.z + k0.w * d.w;
-          acc[1][i] += k1.x * d.x + k1.y * d.y + k1.z * d.z + k1.w * d.w;
+          const float o = Os[j * kSu + pv + 8 * i];
+          acc[0][i] = fmaf(pj.x, o, acc[0][i]);
+          acc[1][i] = fmaf(pj.y, o, acc[1][i]);
         }
-      }
-      const float* P0 = it + kItemP + pt;
-#pragma unroll 4
-      for (int j = 32 * ch; j < 32 * ch + 32; ++j) {
-        const float2 pj = *reinterpret_cast<const float2*>(P0 + j * kC);
-        const float4 o = ld4(Os + j * kVb + 4 * pv);
-        acc[0][0] += pj.x * o.x;
-        acc[0][1] += pj.x * o.y;
-        acc[0][2] += pj.x * o.z;
-        acc[0][3] += pj.x * o.w;
-        acc[1][0] += pj.y * o.x;
-        acc[1][1] += pj.y * o.y;
-        acc[1][2] += pj.y * o.z;
-        acc[1][3] += pj.y * o.w;
       }
 #pragma unroll
       for (int r = 0; r < 2; ++r)
@@ -694,62 +984,86 @@ __global__ void __launch_bounds__(256) kda_bwd_rev_state_kernel(BwdParams p) {
         for (int i = 0; i < 4; ++i) acc[r][i] += __shfl_xor_sync(0xffffffffu, acc[r][i], 1);
       if (ch == 0) {
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          st4(it + kItemDU + (pt + r) * kD + v0 + 4 * pv, acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-          st4(Us + (pt + r) * kVb + 4 * pv, acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-        }
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int v = pv + 8 * i;
+            it[kItemDU + (pt + r) * kD + v0 + v] = acc[r][i];
+            Us[(pt + r) * kSu + v] = acc[r][i];
+          }
       }
     }
+    __syncthreads();  // dU complete; Kb, Pb, Ob, Ds free
+    const float4 g0 = ld4(gc + c1), g1 = ld4(gc + c2);
+    __syncthreads();  // gc read by every thread before it is replaced
+    issue_a(ci - 1);
+    cp_wait<1>();     // Qg, W of this chunk
     __syncthreads();
     {
       float acc[4][8];
-      zero_acc(acc);
-      const float* Q0 = it + kItemQg + 8 * co;
-      const float* W0 = it + kItemW + 8 * co;
+      {
+        f2_t a2[4][4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) a2[a][j] = 0ull;
 #pragma unroll 2
-      for (int t = 16 * tq; t < 16 * tq + 16; ++t) {
-        const float4 o = ld4(Os + t * kVb + 4 * vq), u = ld4(Us + t * kVb + 4 * vq);
-        const float4 q0 = ld4(Q0 + t * kD), q1 = ld4(Q0 + t * kD + 4);
-        const float4 w0 = ld4(W0 + t * kD), w1 = ld4(W0 + t * kD + 4);
-        const float orr[4] = {o.x, o.y, o.z, o.w}, ur[4] = {u.x, u.y, u.z, u.w};
-        const float qr[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-        const float wr[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        for (int i = 0; i < 16; ++i) {
+          const int t = 4 * i + tq;
+          const float4 o = ld4(Os + t * kSu + 4 * vq), u = ld4(Us + t * kSu + 4 * vq);
+          const ulonglong2 q0 = ld2x2(Qb + t * kLd + c1), q1 = ld2x2(Qb + t * kLd + c2);
+          const ulonglong2 w0 = ld2x2(Wb + t * kLd + c1), w1 = ld2x2(Wb + t * kLd + c2);
+          const float orr[4] = {o.x, o.y, o.z, o.w}, ur[4] = {u.x, u.y, u.z, u.w};
+          const f2_t qr[4] = {q0.x, q0.y, q1.x, q1.y}, wr[4] = {w0.x, w0.y, w1.x, w1.y};
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+          for (int a = 0; a < 4; ++a) {
+            const f2_t oo = pk2(orr[a], orr[a]), uu = pk2(-ur[a], -ur[a]);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(orr[i], qr[j], fmaf(-ur[i], wr[j], acc[i][j]));
+            for (int j = 0; j < 4; ++j) a2[a][j] = fma2(oo, qr[j], fma2(uu, wr[j], a2[a][j]));
+          }
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 v = up2(a2[a][j]);
+            acc[a][2 * j] = v.x;
+            acc[a][2 * j + 1] = v.y;
+          }
       }
-      const float4 g0 = ld4(it + kItemGC + 8 * co), g1 = ld4(it + kItemGC + 8 * co + 4);
       const float gr[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          float x = acc[i][j];
+          float x = acc[a][j];
           x += __shfl_xor_sync(0xffffffffu, x, 1);
           x += __shfl_xor_sync(0xffffffffu, x, 2);
-          s[i][j] = fmaf(s[i][j], gr[j], x);
+          s[a][j] = fmaf(s[a][j], gr[j], x);
         }
       if (tq == 0)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          st4(Ds + (4 * vq + i) * kLd + 8 * co, s[i][0], s[i][1], s[i][2], s[i][3]);
-          st4(Ds + (4 * vq + i) * kLd + 8 * co + 4, s[i][4], s[i][5], s[i][6], s[i][7]);
+        for (int a = 0; a < 4; ++a) {
+          st4(Ds + (4 * vq + a) * kLd + c1, s[a][0], s[a][1], s[a][2], s[a][3]);
+          st4(Ds + (4 * vq + a) * kLd + c2, s[a][4], s[a][5], s[a][6], s[a][7]);
         }
     }
+    __syncthreads();  // Qb, Wb, Os, Us free
+    issue_b(ci - 1);
   }
+  cp_wait<0>();
   if (p.dinit && tq == 0) {
-    const int64_t base = (unit * kD + v0 + 4 * vq) * kD + 8 * co;
+    const int64_t base = (unit * kD + v0 + 4 * vq) * kD;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      st4(p.dinit + base + (int64_t)i * kD, s[i][0], s[i][1], s[i][2], s[i][3]);
-      st4(p.dinit + base + (int64_t)i * kD + 4, s[i][4], s[i][5], s[i][6], s[i][7]);
+      st4(p.dinit + base + (int64_t)i * kD + c1, s[i][0], s[i][1], s[i][2], s[i][3]);
+      st4(p.dinit + base + (int64_t)i * kD + c2, s[i][4], s[i][5], s[i][6], s[i][7]);
     }
   }
 }
 
 // ==== 4. gradient products ====
-__global__ void __launch_bounds__(256) kda_bwd_prod_kernel(BwdParams p) {
+__global__ void __launch_bounds__(256, 2) kda_bwd_prod_kernel(BwdParams p) {
   extern __shared__ __align__(16) float sm[];
   float* dWs = sm;  // [64][kLd]
   float* stage = dWs + kC * kLd;
@@ -776,11 +1090,11 @@ __global__ void __launch_bounds__(256) kda_bwd_prod_kernel(BwdParams p) {
   float acc[4][8];
   // dQg = scale dO S (over Qg, no longer read)
   zero_acc(acc);
-  gemm64<128, false, false>(acc, dO, S0, kD, stage);
+  gemm64<128, false, false>(acc, dO, S0, kD, stage, tid, true);
   store128(it + kItemQg, acc, p.scale);
   // dW = -dU S (shared memory)
   zero_acc(acc);
-  gemm64<128, false, false>(acc, dU, S0, kD, stage);
+  gemm64<128, false, false>(acc, dU, S0, kD, stage, tid, true);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     float* d = dWs + (4 * ty + i) * kLd;
@@ -789,19 +1103,27 @@ __global__ void __launch_bounds__(256) kda_bwd_prod_kernel(BwdParams p) {
   }
   // dKhat = Unew dS_C
   zero_acc(acc);
-  gemm64<128, false, false>(acc, Un, dS, kD, stage);
+  gemm64<128, false, false>(acc, Un, dS, kD, stage, tid, true);
   store128(it + kItemKh, acc, 1.f);
-  // dgC = colsum(S . dS_C)
-  if (tid < kD) {
-    float x = 0.f;
-    for (int v = 0; v < kD; ++v) x = fmaf(it[kItemS0 + v * kD + tid], it[kItemDS + v * kD + tid], x);
-    it[kItemDGC + tid] = x;
+  // dgC = colsum(S . dS_C): two threads per channel, halves added through
+  // shared memory (the staging area, free between products)
+  {
+    const int c = tid & (kD - 1), v0 = 64 * (tid >> 7);
+    float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+    for (int v = v0; v < v0 + 64; v += 8)
+#pragma unroll
+      for (int u = 0; u < 8; ++u) x[u] = fmaf(it[kItemS0 + (v + u) * kD + c], it[kItemDS + (v + u) * kD + c], x[u]);
+    const float y = ((x[0] + x[1]) + (x[2] + x[3])) + ((x[4] + x[5]) + (x[6] + x[7]));
+    if (tid >= kD) stage[c] = y;
+    __syncthreads();
+    if (tid < kD) it[kItemDGC + c] = y + stage[c];
   }
   // dP = scale dO Unew^T (s <= t)
   {
     float a2[4][4];
     zero_acc(a2);
-    gemm64<64, false, true>(a2, dO, Un, kD, stage);
+    gemm64<64, false, true>(a2, dO, Un, kD, stage, tid, true);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int t = 4 * ty + i;
@@ -815,8 +1137,8 @@ __global__ void __launch_bounds__(256) kda_bwd_prod_kernel(BwdParams p) {
   {
     float a2[4][4];
     zero_acc(a2);
-    gemm64<64, false, true>(a2, dU, Vv, kD, stage);
-    gemm64<64, false, true>(a2, opd(dWs, kLd, kC), Kg, kD, stage);
+    gemm64<64, false, true>(a2, dU, Vv, kD, stage, tid, true);
+    gemm64<64, false, true>(a2, opd(dWs, kLd, kC), Kg, kD, stage, tid, true);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int t = 4 * ty + i;
@@ -840,7 +1162,7 @@ __global__ void __launch_bounds__(256) kda_bwd_prod_kernel(BwdParams p) {
   }
   // dv = Diag(beta) Minv^T dU
   zero_acc(acc);
-  gemm64<128, true, false>(acc, Mi, dU, kC, stage);
+  gemm64<128, true, false>(acc, Mi, dU, kC, stage, tid, true);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int t = 4 * ty + i;
@@ -852,7 +1174,7 @@ __global__ void __launch_bounds__(256) kda_bwd_prod_kernel(BwdParams p) {
   }
   // dKg = Diag(beta) Minv^T dW (over W, no longer read)
   zero_acc(acc);
-  gemm64<128, true, false>(acc, Mi, opd(dWs, kLd, kC), kC, stage);
+  gemm64<128, true, false>(acc, Mi, opd(dWs, kLd, kC), kC, stage, tid, true);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     float* d = it + kItemW + (4 * ty + i) * kD;
@@ -862,9 +1184,35 @@ __global__ void __launch_bounds__(256) kda_bwd_prod_kernel(BwdParams p) {
 }
 
 // ==== 5. chunk gradients ====
-// Thread (ty = tid / 16, tx = tid % 16) accumulates dq_hat, dk_hat and dGamma
-// of rows 16 m + ty (m = 0..3), channels 8 tx .. 8 tx + 7, in registers.
-__global__ void __launch_bounds__(256, 1) kda_bwd_grad_kernel(BwdParams p) {
+// 512 threads: thread (hf = tid / 256, ty = (tid % 256) / 16, tx = tid % 16)
+// accumulates dq_hat, dk_hat and dGamma of rows 16 m + ty (m = 0..3), channels
+// cb = 64 hf + 4 tx .. cb + 3, in registers.
+constexpr int kGradFloats = 3 * kC * kLd + 2 * kC * kLs + 80 * kLd + kStage + 16 * kD + 4 * kC + 4 * kC;
+
+// g + dt_bias (logspace: g) of elements (row, c0 .. c0 + 3), c0 a multiple of 4
+__device__ __forceinline__ float4 gate_z4(const BwdParams& p, int64_t row, int h, int c0) {
+  float4 z;
+  if (p.g32) {
+    z = ld4(p.g32 + row * kD + c0);
+  } else {
+    const uint2 r = *reinterpret_cast<const uint2*>(p.g + row * kD + c0);
+    const float2 a = unpack_bf16(r.x), b = unpack_bf16(r.y);
+    z = make_float4(a.x, a.y, b.x, b.y);
+  }
+  if (p.gate_mode != kGateLogspace && p.dt_bias) {
+    const float4 d = ld4(p.dt_bias + h * kD + c0);
+    z = make_float4(z.x + d.x, z.y + d.y, z.z + d.z, z.w + d.w);
+  }
+  return z;
+}
+__device__ __forceinline__ void f4a(float4 v, float (&x)[4]) {
+  x[0] = v.x;
+  x[1] = v.y;
+  x[2] = v.z;
+  x[3] = v.w;
+}
+
+__global__ void __launch_bounds__(kPT, 1) kda_bwd_grad_kernel(BwdParams p) {
   extern __shared__ __align__(16) float sm[];
   float* Kh = sm;
   float* Qh = Kh + kC * kLd;
@@ -878,110 +1226,129 @@ __global__ void __launch_bounds__(256, 1) kda_bwd_grad_kernel(BwdParams p) {
   float* rq = vb + kC;
   float* rk = rq + kC;
   float* dbv = rk + kC;
-  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  float* xs = dbv + kC;          // [2 halves][2][64]: row sums of the norm terms
+  const int tid = threadIdx.x, hf = tid >> 8, lt = tid & 255, ty = lt >> 4, tx = lt & 15;
+  const int cb = 64 * hf + 4 * tx;
   const int64_t item = blockIdx.x, slot = item / p.H;
   const int h = (int)(item - slot * p.H);
   ChunkLoc cl;
   if (!locate(p, slot, cl)) return;
   float* it = p.ws + item * (int64_t)kItemFloats;
 
-  load_rows(p, cl, h, Kh, Qh, vb, rq, rk);
+  load_rows<kPT>(p, cl, h, Kh, Qh, vb, rq, rk);
   __syncthreads();
-  gate_cumsum(p, cl, h, Gm);
+  gate_cumsum<kPT>(p, cl, h, Gm);
 
-  // ---- dM = -Minv^T (dT Diag(beta)) Minv^T, dA, dG, dbeta ----
+  // ---- dM = -Minv^T (dT Diag(beta)) Minv^T, dA, dG, dbeta (threads 0-255) ----
   {
-    float* Xa = X;             // dT Diag(beta) [64][kLs]
-    float* Xb = X + kC * kLs;  // Minv^T dT Diag(beta)
-    for (int e = tid; e < kC * kC; e += 256) {
+    float* Mi = dGs;            // Minv [64][kLs] until dG replaces it
+    float* Xa = X;              // dT
+    float* Xb = X + kC * kLs;   // (Minv^T dT) Diag(beta)
+#pragma unroll 4
+    for (int e = tid; e < kC * kC; e += kPT) {
       const int i = e >> 6, j = e & 63;
-      Xa[i * kLs + j] = it[kItemDT + e] * vb[j];
+      Xa[i * kLs + j] = it[kItemDT + e];
+      Mi[i * kLs + j] = it[kItemMi + e];
       dPs[i * kLs + j] = it[kItemP + e];
     }
-    if (tid < kC) {  // (Minv^T dT)_tt
-      float x = 0.f;
-      for (int j = tid; j < kC; ++j) x = fmaf(it[kItemMi + j * kC + tid], it[kItemDT + j * kC + tid], x);
-      dbv[tid] = x;
-    }
+    const bool act = hf == 0;
     float a2[4][4];
     zero_acc(a2);
-    gemm64<64, true, false>(a2, opd(it + kItemMi, kC, kC), opd(Xa, kLs, kC), kC, stage);
+    gemm64<64, true, false>(a2, opd(Mi, kLs, kC), opd(Xa, kLs, kC), kC, stage, lt, act);
+    if (act) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) st4(Xb + (4 * ty + i) * kLs + 4 * tx, a2[i][0], a2[i][1], a2[i][2], a2[i][3]);
-    zero_acc(a2);
-    gemm64<64, false, true>(a2, opd(Xb, kLs, kC), opd(it + kItemMi, kC, kC), kC, stage);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int t = 4 * ty + i;
-      float d[4], gsum = 0.f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int s = 4 * tx + j;
-        const float dA = s < t ? -a2[i][j] : 0.f;
-        gsum = fmaf(dA, it[kItemG + t * kC + s], gsum);
-        d[j] = vb[t] * dA;
+      for (int i = 0; i < 4; ++i) {
+        if (ty == tx) dbv[4 * ty + i] = a2[i][i];  // (Minv^T dT)_tt
+        st4(Xb + (4 * ty + i) * kLs + 4 * tx, a2[i][0] * vb[4 * tx], a2[i][1] * vb[4 * tx + 1],
+            a2[i][2] * vb[4 * tx + 2], a2[i][3] * vb[4 * tx + 3]);
       }
-      st4(dGs + t * kLs + 4 * tx, d[0], d[1], d[2], d[3]);
+    }
+    zero_acc(a2);
+    gemm64<64, false, true>(a2, opd(Xb, kLs, kC), opd(Mi, kLs, kC), kC, stage, lt, act);
+    if (act) {
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) gsum += __shfl_xor_sync(0xffffffffu, gsum, o);
-      if (tx == 0) dbv[t] += gsum;
+      for (int i = 0; i < 4; ++i) {
+        const int t = 4 * ty + i;
+        float gv[4];
+        f4a(ld4(it + kItemG + t * kC + 4 * tx), gv);
+        float d[4], gsum = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int s = 4 * tx + j;
+          const float dA = s < t ? -a2[i][j] : 0.f;
+          gsum = fmaf(dA, gv[j], gsum);
+          d[j] = vb[t] * dA;
+        }
+        st4(dGs + t * kLs + 4 * tx, d[0], d[1], d[2], d[3]);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) gsum += __shfl_xor_sync(0xffffffffu, gsum, o);
+        if (tx == 0) dbv[t] += gsum;
+      }
     }
   }
   __syncthreads();
 
-  float aQ[4][8], aK[4][8], aG[4][8];
+  float aQ[4][4], aK[4][4], aG[4][4];
   // ---- the scalings: Qg = q e^Gamma, Kg = k e^Gamma, Khat = k e^{Gamma_C - Gamma} ----
   {
-    float cs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float cs[4] = {0.f, 0.f, 0.f, 0.f};
+    float4 gq[4], gk[4], gh[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {  // every load first
+      const int o = (16 * m + ty) * kD + cb;
+      gq[m] = ld4(it + kItemQg + o);
+      gk[m] = ld4(it + kItemW + o);
+      gh[m] = ld4(it + kItemKh + o);
+    }
+    float glv[4];
+    f4a(ld4(Gm + (kC - 1) * kLd + cb), glv);
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const int t = 16 * m + ty;
+      float dqv[4], dkv[4], dhv[4], gtv[4], qhv[4], khv[4];
+      f4a(gq[m], dqv);
+      f4a(gk[m], dkv);
+      f4a(gh[m], dhv);
+      f4a(ld4(Gm + t * kLd + cb), gtv);
+      f4a(ld4(Qh + t * kLd + cb), qhv);
+      f4a(ld4(Kh + t * kLd + cb), khv);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int c = 8 * tx + j;
-        const float gt = Gm[t * kLd + c], e = expf(gt), ec = expf(Gm[(kC - 1) * kLd + c] - gt);
-        const float qh = Qh[t * kLd + c], kh = Kh[t * kLd + c];
-        const float dqg = it[kItemQg + t * kD + c], dkg = it[kItemW + t * kD + c], dkh = it[kItemKh + t * kD + c];
-        aQ[m][j] = dqg * e;
-        aK[m][j] = dkg * e + dkh * ec;
-        aG[m][j] = dqg * qh * e + dkg * kh * e - dkh * kh * ec;
-        cs[j] += dkh * kh * ec;
+      for (int j = 0; j < 4; ++j) {
+        const float e = dexp(gtv[j]), ec = dexp(glv[j] - gtv[j]);
+        aQ[m][j] = dqv[j] * e;
+        aK[m][j] = dkv[j] * e + dhv[j] * ec;
+        aG[m][j] = dqv[j] * qhv[j] * e + dkv[j] * khv[j] * e - dhv[j] * khv[j] * ec;
+        cs[j] += dhv[j] * khv[j] * ec;
       }
     }
-    st4(part + ty * kD + 8 * tx, cs[0], cs[1], cs[2], cs[3]);
-    st4(part + ty * kD + 8 * tx + 4, cs[4], cs[5], cs[6], cs[7]);
+    st4(part + ty * kD + cb, cs[0], cs[1], cs[2], cs[3]);
   }
   // ---- G and P inside the diagonal blocks, pair by pair ----
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
     const int t = 16 * m + ty;
-    float gt[8], kt[8], qt[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      gt[j] = Gm[t * kLd + 8 * tx + j];
-      kt[j] = Kh[t * kLd + 8 * tx + j];
-      qt[j] = Qh[t * kLd + 8 * tx + j];
-    }
+    float gt[4], kt[4], qt[4];
+    f4a(ld4(Gm + t * kLd + cb), gt);
+    f4a(ld4(Kh + t * kLd + cb), kt);
+    f4a(ld4(Qh + t * kLd + cb), qt);
     const float dpd = dPs[t * kLs + t];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < 4; ++j) {
       aQ[m][j] = fmaf(dpd, kt[j], aQ[m][j]);
       aK[m][j] = fmaf(dpd, qt[j], aK[m][j]);
     }
+#pragma unroll 4
     for (int s = 16 * m; s < 16 * m + 16; ++s) {
       if (s == t) continue;
-      float gs[8], ks[8], qs[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        gs[j] = Gm[s * kLd + 8 * tx + j];
-        ks[j] = Kh[s * kLd + 8 * tx + j];
-        qs[j] = Qh[s * kLd + 8 * tx + j];
-      }
+      float gs[4], ks[4], qs[4];
+      f4a(ld4(Gm + s * kLd + cb), gs);
+      f4a(ld4(Kh + s * kLd + cb), ks);
+      f4a(ld4(Qh + s * kLd + cb), qs);
       if (s < t) {  // t takes the role of the later token
         const float dg = dGs[t * kLs + s], dp = dPs[t * kLs + s];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float f = expf(gt[j] - gs[j]) * ks[j];
+        for (int j = 0; j < 4; ++j) {
+          const float f = dexp(gt[j] - gs[j]) * ks[j];
           aK[m][j] = fmaf(dg, f, aK[m][j]);
           aQ[m][j] = fmaf(dp, f, aQ[m][j]);
           aG[m][j] = fmaf(dg * kt[j] + dp * qt[j], f, aG[m][j]);
@@ -989,9 +1356,9 @@ __global__ void __launch_bounds__(256, 1) kda_bwd_grad_kernel(BwdParams p) {
       } else {  // t is the earlier token
         const float dg = dGs[s * kLs + t], dp = dPs[s * kLs + t];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float w = (dg * ks[j] + dp * qs[j]) * expf(gs[j] - gt[j]);
-          aK[m][j] = fmaf(w, 1.f, aK[m][j]);
+        for (int j = 0; j < 4; ++j) {
+          const float w = (dg * ks[j] + dp * qs[j]) * dexp(gs[j] - gt[j]);
+          aK[m][j] += w;
           aG[m][j] = fmaf(-w, kt[j], aG[m][j]);
         }
       }
@@ -1005,81 +1372,104 @@ __global__ void __launch_bounds__(256, 1) kda_bwd_grad_kernel(BwdParams p) {
     float* Lq = X + 16 * kLd;
     float* R = X + 32 * kLd;
     __syncthreads();
-    for (int e = tid; e < (32 + r) * 32; e += 256) {
+    for (int e = tid; e < (32 + r) * 32; e += kPT) {
       const int row = e >> 5, c = 4 * (e & 31);
       const float4 gr = ld4(Gm + r * kLd + c);
       if (row < 32) {
         const int ii = row & 15, i = r + ii;
         const float4 gi = ld4(Gm + i * kLd + c);
         const float4 x = ld4((row < 16 ? Kh : Qh) + i * kLd + c);
-        st4((row < 16 ? Lk : Lq) + ii * kLd + c, x.x * expf(gi.x - gr.x), x.y * expf(gi.y - gr.y),
-            x.z * expf(gi.z - gr.z), x.w * expf(gi.w - gr.w));
+        st4((row < 16 ? Lk : Lq) + ii * kLd + c, x.x * dexp(gi.x - gr.x), x.y * dexp(gi.y - gr.y),
+            x.z * dexp(gi.z - gr.z), x.w * dexp(gi.w - gr.w));
       } else {
         const int j = row - 32;
         const float4 gj = ld4(Gm + j * kLd + c);
         const float4 x = ld4(Kh + j * kLd + c);
-        st4(R + j * kLd + c, x.x * expf(gr.x - gj.x), x.y * expf(gr.y - gj.y), x.z * expf(gr.z - gj.z),
-            x.w * expf(gr.w - gj.w));
+        st4(R + j * kLd + c, x.x * dexp(gr.x - gj.x), x.y * dexp(gr.y - gj.y), x.z * dexp(gr.z - gj.z),
+            x.w * dexp(gr.w - gj.w));
       }
     }
     __syncthreads();
     {  // rows of block I (t = r + ty): X_G = dG R, X_P = dP R over s < r
       const int t = r + ty;
-      float xg[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, xp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float xg[4] = {0.f, 0.f, 0.f, 0.f}, xp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
       for (int s = 0; s < r; ++s) {
         const float dg = dGs[t * kLs + s], dp = dPs[t * kLs + s];
-        const float4 r0 = ld4(R + s * kLd + 8 * tx), r1 = ld4(R + s * kLd + 8 * tx + 4);
-        const float rr[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+        float rr[4];
+        f4a(ld4(R + s * kLd + cb), rr);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 4; ++j) {
           xg[j] = fmaf(dg, rr[j], xg[j]);
           xp[j] = fmaf(dp, rr[j], xp[j]);
         }
       }
+      float gtv[4], grv[4], ktv[4], qtv[4];
+      f4a(ld4(Gm + t * kLd + cb), gtv);
+      f4a(ld4(Gm + r * kLd + cb), grv);
+      f4a(ld4(Kh + t * kLd + cb), ktv);
+      f4a(ld4(Qh + t * kLd + cb), qtv);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int c = 8 * tx + j;
-        const float l = expf(Gm[t * kLd + c] - Gm[r * kLd + c]);
+      for (int j = 0; j < 4; ++j) {
+        const float l = dexp(gtv[j] - grv[j]);
         aK[I][j] = fmaf(l, xg[j], aK[I][j]);
         aQ[I][j] = fmaf(l, xp[j], aQ[I][j]);
-        aG[I][j] = fmaf(l, Kh[t * kLd + c] * xg[j] + Qh[t * kLd + c] * xp[j], aG[I][j]);
+        aG[I][j] = fmaf(l, ktv[j] * xg[j] + qtv[j] * xp[j], aG[I][j]);
       }
     }
 #pragma unroll
     for (int m = 0; m < I; ++m) {  // rows s = 16 m + ty < r: Y = dG^T Lk + dP^T Lq over block I
       const int s = 16 * m + ty;
-      float y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
       for (int ii = 0; ii < 16; ++ii) {
         const float dg = dGs[(r + ii) * kLs + s], dp = dPs[(r + ii) * kLs + s];
-        const float4 k0 = ld4(Lk + ii * kLd + 8 * tx), k1 = ld4(Lk + ii * kLd + 8 * tx + 4);
-        const float4 q0 = ld4(Lq + ii * kLd + 8 * tx), q1 = ld4(Lq + ii * kLd + 8 * tx + 4);
-        const float kr[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
-        const float qr[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        float kr[4], qr[4];
+        f4a(ld4(Lk + ii * kLd + cb), kr);
+        f4a(ld4(Lq + ii * kLd + cb), qr);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) y[j] = fmaf(dg, kr[j], fmaf(dp, qr[j], y[j]));
+        for (int j = 0; j < 4; ++j) y[j] = fmaf(dg, kr[j], fmaf(dp, qr[j], y[j]));
       }
+      float rrv[4], grv[4], gsv[4];
+      f4a(ld4(R + s * kLd + cb), rrv);  // k_s e^{Gamma_r - Gamma_s}
+      f4a(ld4(Gm + r * kLd + cb), grv);
+      f4a(ld4(Gm + s * kLd + cb), gsv);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int c = 8 * tx + j;
-        const float rr = R[s * kLd + c];                       // k_s e^{Gamma_r - Gamma_s}
-        const float e = expf(Gm[r * kLd + c] - Gm[s * kLd + c]);
-        aK[m][j] = fmaf(e, y[j], aK[m][j]);
-        aG[m][j] = fmaf(-rr, y[j], aG[m][j]);
+      for (int j = 0; j < 4; ++j) {
+        aK[m][j] = fmaf(dexp(grv[j] - gsv[j]), y[j], aK[m][j]);
+        aG[m][j] = fmaf(-rrv[j], y[j], aG[m][j]);
       }
     }
   }
   __syncthreads();
-  // ---- dGamma -> da by the reverse cumulative sum ----
+  // ---- dGamma -> da by the reverse cumulative sum; row sums of the norm terms ----
   float* Dg = X;  // [64][kLd]
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
-    float* d = Dg + (16 * m + ty) * kLd + 8 * tx;
-    st4(d, aG[m][0], aG[m][1], aG[m][2], aG[m][3]);
-    st4(d + 4, aG[m][4], aG[m][5], aG[m][6], aG[m][7]);
+    const int t = 16 * m + ty;
+    st4(Dg + t * kLd + cb, aG[m][0], aG[m][1], aG[m][2], aG[m][3]);
+    float qv[4], kv[4];
+    f4a(ld4(Qh + t * kLd + cb), qv);
+    f4a(ld4(Kh + t * kLd + cb), kv);
+    float xq = 0.f, xk = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      xq = fmaf(qv[j], aQ[m][j], xq);
+      xk = fmaf(kv[j], aK[m][j], xk);
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) {
+      xq += __shfl_xor_sync(0xffffffffu, xq, o);
+      xk += __shfl_xor_sync(0xffffffffu, xk, o);
+    }
+    if (tx == 0) {
+      xs[(hf * 2) * kC + t] = xq;
+      xs[(hf * 2 + 1) * kC + t] = xk;
+    }
   }
   __syncthreads();
   if (tid < kD) {
-    float x = it[kItemDGC + tid] * expf(Gm[(kC - 1) * kLd + tid]);
+    float x = it[kItemDGC + tid] * dexp(Gm[(kC - 1) * kLd + tid]);
     for (int y = 0; y < 16; ++y) x += part[y * kD + tid];
     float acc = Dg[(kC - 1) * kLd + tid] + x;
     Dg[(kC - 1) * kLd + tid] = acc;
@@ -1091,51 +1481,41 @@ __global__ void __launch_bounds__(256, 1) kda_bwd_grad_kernel(BwdParams p) {
   __syncthreads();
   // ---- outputs ----
   const float amul = gate_mul(p, h);
-  float pdt[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, pal = 0.f;
+  float pdt[4] = {0.f, 0.f, 0.f, 0.f}, pal = 0.f;
+  float4 zall[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m)  // every load first (rows past the chunk re-read its last row)
+    zall[m] = gate_z4(p, (cl.t0 + min(16 * m + ty, cl.L - 1)) * p.H + h, h, cb);
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
     const int t = 16 * m + ty;
-    const bool live = t < cl.L;
-    const int64_t row = (cl.t0 + (live ? t : 0)) * p.H + h;
-    float xq = 0.f, xk = 0.f;
+    if (t >= cl.L) continue;
+    const int64_t row = (cl.t0 + t) * p.H + h;
+    float qv[4], kv[4], dav[4], zv[4];
+    f4a(ld4(Qh + t * kLd + cb), qv);
+    f4a(ld4(Kh + t * kLd + cb), kv);
+    f4a(ld4(Dg + t * kLd + cb), dav);
+    f4a(zall[m], zv);
+    const float xq = xs[t] + xs[2 * kC + t], xk = xs[kC + t] + xs[3 * kC + t];
+    float dq[4], dk[4], dz[4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      xq = fmaf(Qh[t * kLd + 8 * tx + j], aQ[m][j], xq);
-      xk = fmaf(Kh[t * kLd + 8 * tx + j], aK[m][j], xk);
-    }
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) {
-      xq += __shfl_xor_sync(0xffffffffu, xq, o);
-      xk += __shfl_xor_sync(0xffffffffu, xk, o);
-    }
-    if (!live) continue;
-    float dq[8], dk[8], dz[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int c = 8 * tx + j;
+    for (int j = 0; j < 4; ++j) {
       if (p.l2norm) {
-        dq[j] = rq[t] * (aQ[m][j] - Qh[t * kLd + c] * xq);
-        dk[j] = rk[t] * (aK[m][j] - Kh[t * kLd + c] * xk);
+        dq[j] = rq[t] * (aQ[m][j] - qv[j] * xq);
+        dk[j] = rk[t] * (aK[m][j] - kv[j] * xk);
       } else {
         dq[j] = aQ[m][j];
         dk[j] = aK[m][j];
       }
       float dadz, dadA;
-      gate_a(p.gate_mode, gate_z(p, row, h, c), amul, p.lower_bound, dadz, dadA);
-      const float da = Dg[t * kLd + c];
-      dz[j] = da * dadz;
+      gate_a(p.gate_mode, zv[j], amul, p.lower_bound, dadz, dadA);
+      dz[j] = dav[j] * dadz;
       pdt[j] += dz[j];
-      pal = fmaf(da, dadA, pal);
+      pal = fmaf(dav[j], dadA, pal);
     }
-    float* o = p.dq + row * kD + 8 * tx;
-    st4(o, dq[0], dq[1], dq[2], dq[3]);
-    st4(o + 4, dq[4], dq[5], dq[6], dq[7]);
-    o = p.dk + row * kD + 8 * tx;
-    st4(o, dk[0], dk[1], dk[2], dk[3]);
-    st4(o + 4, dk[4], dk[5], dk[6], dk[7]);
-    o = p.dg + row * kD + 8 * tx;
-    st4(o, dz[0], dz[1], dz[2], dz[3]);
-    st4(o + 4, dz[4], dz[5], dz[6], dz[7]);
+    st4(p.dq + row * kD + cb, dq[0], dq[1], dq[2], dq[3]);
+    st4(p.dk + row * kD + cb, dk[0], dk[1], dk[2], dk[3]);
+    st4(p.dg + row * kD + cb, dz[0], dz[1], dz[2], dz[3]);
   }
   if (tid < cl.L) {
     float db = dbv[tid];
@@ -1144,8 +1524,7 @@ __global__ void __launch_bounds__(256, 1) kda_bwd_grad_kernel(BwdParams p) {
   }
   // the chunk's parts of dt_bias and A_log, summed in a fixed order
   __syncthreads();
-  st4(part + ty * kD + 8 * tx, pdt[0], pdt[1], pdt[2], pdt[3]);
-  st4(part + ty * kD + 8 * tx + 4, pdt[4], pdt[5], pdt[6], pdt[7]);
+  st4(part + ty * kD + cb, pdt[0], pdt[1], pdt[2], pdt[3]);
   pal = warp_sum(pal);
   if ((tid & 31) == 0) X[tid >> 5] = pal;
   __syncthreads();
@@ -1156,7 +1535,7 @@ __global__ void __launch_bounds__(256, 1) kda_bwd_grad_kernel(BwdParams p) {
   }
   if (tid == kD) {
     float x = 0.f;
-    for (int w = 0; w < 8; ++w) x += X[w];
+    for (int w = 0; w < kPT / 32; ++w) x += X[w];
     it[kItemPart + kD] = x;
   }
 }
@@ -1185,15 +1564,15 @@ static void launch_bwd(const BwdParams& p, cudaStream_t s, void* const* ev) {
     if (ev && ev[i]) cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[i]), s);
   };
   const unsigned items = (unsigned)(p.nslots * p.H);
-  const unsigned units = (unsigned)(p.N * p.H * kRowBlocks);
-  if (items) kda_bwd_prep_kernel<<<items, 256, kPrepFloats * 4, s>>>(p);
-  kda_bwd_fwd_state_kernel<<<units, 256, 0, s>>>(p);
+  const unsigned units = (unsigned)(p.N * p.H * kSBlocks);
+  if (items) kda_bwd_prep_kernel<<<items, kPT, kPrepFloats * 4, s>>>(p);
+  kda_bwd_fwd_state_kernel<<<units, kSt, kFwdFloats * 4, s>>>(p);
   mark(1);
-  kda_bwd_rev_state_kernel<<<units, 256, 0, s>>>(p);
+  kda_bwd_rev_state_kernel<<<units, kSt, kRevFloats * 4, s>>>(p);
   mark(2);
   if (items) {
     kda_bwd_prod_kernel<<<items, 256, kProdFloats * 4, s>>>(p);
-    kda_bwd_grad_kernel<<<items, 256, kGradFloats * 4, s>>>(p);
+    kda_bwd_grad_kernel<<<items, kPT, kGradFloats * 4, s>>>(p);
   }
   if (p.gate_mode != kGateLogspace && (p.dA_log || p.ddt_bias))
     kda_bwd_finalize_kernel<<<(unsigned)p.H, kD + 32, 0, s>>>(p);
@@ -1205,6 +1584,8 @@ static cudaError_t prepare_bwd() {
   cudaError_t e = cudaFuncSetAttribute((const void*)kda_bwd_prep_kernel, attr, kPrepFloats * 4);
   if (e == cudaSuccess) e = cudaFuncSetAttribute((const void*)kda_bwd_prod_kernel, attr, kProdFloats * 4);
   if (e == cudaSuccess) e = cudaFuncSetAttribute((const void*)kda_bwd_grad_kernel, attr, kGradFloats * 4);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute((const void*)kda_bwd_fwd_state_kernel, attr, kFwdFloats * 4);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute((const void*)kda_bwd_rev_state_kernel, attr, kRevFloats * 4);
   return e;
 }
 
