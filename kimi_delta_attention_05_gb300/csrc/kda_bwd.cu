@@ -318,7 +318,7 @@ __device__ void gate_cumsum(const BwdParams& p, const ChunkLoc& cl, int h, float
 
 // ---- fp32 block GEMM (256 threads) ----
 // Operand view: element (r, c) = p[r * ld + c] (fp32, or bf16 if b16); rows
-// r >= rows read as zero.
+// r >= rows read as zero.  Row starts and ld are multiples of 4 elements.
 struct Opd {
   const void* p;
   int64_t ld;
@@ -332,46 +332,49 @@ __device__ __forceinline__ Opd opd(const void* p, int64_t ld, int rows, int b16 
   o.b16 = b16;
   return o;
 }
-__device__ __forceinline__ float opd_at(const Opd& o, int r, int c) {
-  if (r >= o.rows) return 0.f;
+// elements (r, c .. c + 3), c a multiple of 4
+__device__ __forceinline__ float4 opd4(const Opd& o, int r, int c) {
+  if (r >= o.rows) return make_float4(0.f, 0.f, 0.f, 0.f);
   const int64_t i = (int64_t)r * o.ld + c;
-  return o.b16 ? bf16_to_f(static_cast<const uint16_t*>(o.p)[i]) : static_cast<const float*>(o.p)[i];
+  if (o.b16) {
+    const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(o.p) + i);
+    const float2 a = unpack_bf16(u.x), b = unpack_bf16(u.y);
+    return make_float4(a.x, a.y, b.x, b.y);
+  }
+  return ld4(static_cast<const float*>(o.p) + i);
 }
 
 // acc[4][BN / 16] += A (64 x kd) B (kd x BN), with A(m, k) = kAT ? a(k, m) : a(m, k)
 // and B(k, n) = kBT ? b(n, k) : b(k, n); kd a multiple of 16.  Thread (ty =
-// tid / 16, tx = tid % 16) owns rows 4 ty + i and columns 4 tx + j (j < 4) and
-// 64 + 4 tx + j - 4 (j >= 4, BN = 128).  Staged through `stage` in
-// 16-deep slices; begins and ends with a barrier.
-
-// 256 threads of the CTA (local index lt) take part; every thread of the CTA
-// must call it (it holds the CTA's barriers), with active = false for the others.
+// lt / 16, tx = lt % 16) owns rows 4 ty + i and columns 4 tx + j (j < 4) and
+// 64 + 4 tx + j - 4 (j >= 4, BN = 128).  Staged through `stage` in 16-deep
+// slices read as 4-element vectors (the next slice in registers while this one
+// is multiplied); begins and ends with a barrier.  256 threads of the CTA
+// (local index lt) take part; every thread of the CTA must call it (it holds
+// the CTA's barriers), with active = false for the others.
 template <int BN, bool kAT, bool kBT>
 __device__ void gemm64(float (&acc)[4][BN / 16], const Opd& a, const Opd& b, int kd, float* stage,
                        int lt, bool active) {
   constexpr int kBs = BN + 4;
+  constexpr int kNB = BN / 64;   // B vectors per thread and slice
   float* As = stage;             // [16][kLs]: As[k][m]
   float* Bs = stage + 16 * kLs;  // [16][kBs]: Bs[k][n]
-  const int tid = lt, ty = tid >> 4, tx = tid & 15;
-  float ra[4], rb[BN / 16];
-  auto fetch = [&](int k0) {  // the slice's operands into registers
+  const int ty = lt >> 4, tx = lt & 15;
+  float4 ra, rb[kNB];
+  auto fetch = [&](int k0) {  // the slice's operands into registers, one vector each
+    ra = kAT ? opd4(a, k0 + (lt >> 4), 4 * (lt & 15)) : opd4(a, lt >> 2, k0 + 4 * (lt & 3));
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int e = tid + 256 * i;
-      ra[i] = kAT ? opd_at(a, k0 + (e >> 6), e & 63) : opd_at(a, e >> 4, k0 + (e & 15));
-    }
-#pragma unroll
-    for (int i = 0; i < BN / 16; ++i) {
-      const int e = tid + 256 * i;
-      rb[i] = kBT ? opd_at(b, e >> 4, k0 + (e & 15)) : opd_at(b, k0 + e / BN, e % BN);
+    for (int i = 0; i < kNB; ++i) {
+      const int e = lt + 256 * i;
+      rb[i] = kBT ? opd4(b, e >> 2, k0 + 4 * (e & 3)) : opd4(b, k0 + e / (BN / 4), 4 * (e % (BN / 4)));
     }
   };
-  __syncthreads();  // operands written to shared memory before the call are complete
   f2_t c2[4][BN / 32];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < BN / 32; ++j) c2[i][j] = pk2(acc[i][2 * j], acc[i][2 * j + 1]);
+  __syncthreads();  // operands written to shared memory before the call are complete
   if (active) fetch(0);
   for (int k0 = 0; k0 < kd; k0 += 16) {
     __syncthreads();  // the previous slice is consumed
@@ -379,17 +382,27 @@ __device__ void gemm64(float (&acc)[4][BN / 16], const Opd& a, const Opd& b, int
       __syncthreads();
       continue;
     }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int e = tid + 256 * i;
-      if (kAT) As[(e >> 6) * kLs + (e & 63)] = ra[i];
-      else As[(e & 15) * kLs + (e >> 4)] = ra[i];
+    if (kAT) {
+      st4(As + (lt >> 4) * kLs + 4 * (lt & 15), ra.x, ra.y, ra.z, ra.w);
+    } else {
+      const int m = lt >> 2, k = 4 * (lt & 3);
+      As[k * kLs + m] = ra.x;
+      As[(k + 1) * kLs + m] = ra.y;
+      As[(k + 2) * kLs + m] = ra.z;
+      As[(k + 3) * kLs + m] = ra.w;
     }
 #pragma unroll
-    for (int i = 0; i < BN / 16; ++i) {
-      const int e = tid + 256 * i;
-      if (kBT) Bs[(e & 15) * kBs + (e >> 4)] = rb[i];
-      else Bs[(e / BN) * kBs + e % BN] = rb[i];
+    for (int i = 0; i < kNB; ++i) {
+      const int e = lt + 256 * i;
+      if (kBT) {
+        const int n = e >> 2, k = 4 * (e & 3);
+        Bs[k * kBs + n] = rb[i].x;
+        Bs[(k + 1) * kBs + n] = rb[i].y;
+        Bs[(k + 2) * kBs + n] = rb[i].z;
+        Bs[(k + 3) * kBs + n] = rb[i].w;
+      } else {
+        st4(Bs + (e / (BN / 4)) * kBs + 4 * (e % (BN / 4)), rb[i].x, rb[i].y, rb[i].z, rb[i].w);
+      }
     }
     __syncthreads();
     if (k0 + 16 < kd) fetch(k0 + 16);  // in flight during this slice's products
@@ -632,10 +645,6 @@ template <int N>
 __device__ __forceinline__ void cp_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
-// L2 prefetch of `bytes` (a multiple of 16) from a 16-byte aligned address
-__device__ __forceinline__ void l2_prefetch(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
-}
 // rows x 128 fp32 (contiguous in the item) into a [rows][kLd] shared array
 __device__ __forceinline__ void cp_rows128(float* dst, const float* src, int rows, int tid, int nthr) {
   for (int e = tid; e < rows * 32; e += nthr) cp16(dst + (e >> 5) * kLd + 4 * (e & 31), src + 4 * e);
@@ -688,12 +697,7 @@ __global__ void __launch_bounds__(kSt, 1) kda_bwd_fwd_state_kernel(BwdParams p) 
   int64_t first, count;
   seq_chunks(p, n, first, count);
   auto item = [&](int64_t ci) { return p.ws + ((first + ci) * p.H + h) * (int64_t)kItemFloats; };
-  auto issue_w = [&](int64_t ci) {  // W and U columns of chunk ci; the chunk after it into L2
-    if (ci + 1 < count && tid == 0) {
-      const float* nx = item(ci + 1);
-      l2_prefetch(nx + kItemW, 3 * kC * kD * 4);  // W, U, Khat
-      l2_prefetch(nx + kItemGC, kD * 4);
-    }
+  auto issue_w = [&](int64_t ci) {  // W and U columns of chunk ci
     if (ci < count) {
       const float* it = item(ci);
       cp_rows128(Wb, it + kItemW, kC, tid, kSt);
@@ -878,14 +882,7 @@ __global__ void __launch_bounds__(kSt, 1) kda_bwd_rev_state_kernel(BwdParams p) 
   const int64_t bos = p.cu ? p.cu[n] : n * p.T, eos = p.cu ? p.cu[n + 1] : (n + 1) * p.T;
   auto item = [&](int64_t ci) { return p.ws + ((first + ci) * p.H + h) * (int64_t)kItemFloats; };
   auto chunk_len = [&](int64_t ci) { return (int)min((int64_t)kC, eos - bos - ci * kC); };
-  auto issue_a = [&](int64_t ci) {  // Khat, P, dout columns, gC of chunk ci; the chunk before it into L2
-    if (ci >= 1 && tid == 0) {
-      const float* nx = item(ci - 1);
-      l2_prefetch(nx + kItemW, kC * kD * 4);
-      l2_prefetch(nx + kItemKh, 2 * kC * kD * 4);  // Khat, Qg
-      l2_prefetch(nx + kItemP, kC * kC * 4);
-      l2_prefetch(nx + kItemGC, kD * 4);
-    }
+  auto issue_a = [&](int64_t ci) {  // Khat, P, dout columns, gC of chunk ci
     if (ci >= 0) {
       const float* it = item(ci);
       cp_rows128(Kb, it + kItemKh, kC, tid, kSt);
