@@ -1231,6 +1231,15 @@ __global__ void __launch_bounds__(kPT, 1) kda_bwd_grad_kernel(BwdParams p) {
   ChunkLoc cl;
   if (!locate(p, slot, cl)) return;
   float* it = p.ws + item * (int64_t)kItemFloats;
+  // dT, Minv and P into shared memory (Minv where dG goes later, dT at the
+  // start of the scratch area) while the rows load and the gate runs
+  for (int e = tid; e < kC * 16; e += kPT) {
+    const int i = e >> 4, c = 4 * (e & 15);
+    cp16(X + i * kLs + c, it + kItemDT + 4 * e);
+    cp16(dGs + i * kLs + c, it + kItemMi + 4 * e);
+    cp16(dPs + i * kLs + c, it + kItemP + 4 * e);
+  }
+  cp_commit();
 
   load_rows<kPT>(p, cl, h, Kh, Qh, vb, rq, rk);
   __syncthreads();
@@ -1241,13 +1250,7 @@ __global__ void __launch_bounds__(kPT, 1) kda_bwd_grad_kernel(BwdParams p) {
     float* Mi = dGs;            // Minv [64][kLs] until dG replaces it
     float* Xa = X;              // dT
     float* Xb = X + kC * kLs;   // (Minv^T dT) Diag(beta)
-#pragma unroll 4
-    for (int e = tid; e < kC * kC; e += kPT) {
-      const int i = e >> 6, j = e & 63;
-      Xa[i * kLs + j] = it[kItemDT + e];
-      Mi[i * kLs + j] = it[kItemMi + e];
-      dPs[i * kLs + j] = it[kItemP + e];
-    }
+    cp_wait<0>();               // (made visible by the barrier the product begins with)
     const bool act = hf == 0;
     float a2[4][4];
     zero_acc(a2);
