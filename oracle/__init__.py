@@ -17,7 +17,9 @@ Two independent fp64 implementations live here:
 
 and, for the backward pass, :func:`kda_backward`: fp64 gradients by autograd
 over a plain torch restatement of the same token recurrence
-(``backward.py``).
+(``backward.py``), and :func:`chunk_backward`: the same gradients derived by
+hand through the chunk algebra (``chunk_backward.py``), pinned to the autograd
+oracle and exposing per-chunk gradient intermediates.
 
 Parity status: every function is pinned (see ``tests/test_oracle_pins.py``,
 ``tests/test_oracle_mutations.py`` and ``tests/test_backward_oracle.py``).
@@ -25,3 +27,4 @@ Parity status: every function is pinned (see ``tests/test_oracle_pins.py``,
 from .recurrence import build, kda_recurrence, gate_activation, max_threads  # noqa: F401
 from .chunk_form import chunk_form  # noqa: F401
 from .backward import kda_backward, kda_forward_torch  # noqa: F401
+from .chunk_backward import chunk_backward  # noqa: F401

@@ -166,3 +166,45 @@ def test_initial_state_gradient_is_the_transition_product():
     expected = np.zeros((3, 4))
     expected[1] = M[:, 2]  # S_T[1, 2] = sum_j S0[1, j] M[j, 2]
     np.testing.assert_allclose(gr["initial_state"][0, 0], expected, rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", MODES, ids=[m["gate"] + ("_l2" if m["qk_l2norm"] else "") for m in MODES])
+@pytest.mark.parametrize("chunk", [4, 5, 64])
+def test_chunk_backward_equals_autograd(mode, chunk):
+    """The hand-derived chunked backward (oracle/chunk_backward.py) gives the
+    autograd gradients of the token recurrence, for every input: chunk sizes
+    that cut the sequences into several full and partial chunks, and one
+    larger than every sequence; dense with states and a final-state gradient,
+    and packed with an empty sequence."""
+    gen = torch.Generator().manual_seed(7)
+    for kw in (dict(B=2, T=13, H=2, K=6, V=5, seed=11), dict(lengths=[7, 0, 1, 12], H=2, K=6, V=5, seed=12)):
+        inp = _prep(_inputs(**kw), mode)
+        B, T = inp["q"].shape[:2]
+        dout = torch.randn((B, T, 2, 5), generator=gen, dtype=torch.float64).numpy()
+        dfin = torch.randn((inp["N"], 2, 5, 6), generator=gen, dtype=torch.float64).numpy()
+        args = dict(scale=0.4, A_log=inp["A_log"], dt_bias=inp["dt_bias"], lower_bound=mode["lower_bound"],
+                    gate=mode["gate"], beta_prob=mode["beta_prob"], qk_l2norm=mode["qk_l2norm"],
+                    initial_state=inp["initial_state"], dfinal=dfin, cu_seqlens=inp["cu_seqlens"])
+        ref = oracle.kda_backward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], dout, **args)
+        got = oracle.chunk_backward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], dout, chunk=chunk, **args)
+        for name in ("q", "k", "v", "g", "beta", "A_log", "dt_bias", "initial_state"):
+            if ref[name] is None:
+                assert got[name] is None, name
+                continue
+            scale_ = max(np.abs(ref[name]).max(), 1e-300)
+            assert np.abs(got[name] - ref[name]).max() <= 1e-10 * scale_, (name, chunk)
+
+
+def test_chunk_backward_intermediates():
+    """The kept per-chunk dS_end values chain as the reverse recurrence
+    dS_prev = scale dO^T Qg + dS Diag(gC) - dU^T W implies: the first chunk's
+    incoming dS is the next chunk's ... down to dfinal for the last chunk."""
+    inp = _inputs(B=1, T=11, H=1, K=4, V=3, seed=21)
+    dout = np.ones((1, 11, 1, 3))
+    dfin = np.full((1, 1, 3, 4), 0.25)
+    got = oracle.chunk_backward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], dout, scale=1.0,
+                                A_log=inp["A_log"], dt_bias=inp["dt_bias"], initial_state=inp["initial_state"],
+                                dfinal=dfin, chunk=4, keep=True)
+    chunks = got["chunks"][(0, 0)]
+    assert len(chunks) == 3 and chunks[0]["dP"].shape == (4, 4) and chunks[-1]["dP"].shape == (3, 3)
+    np.testing.assert_array_equal(chunks[-1]["dS_end"], dfin[0, 0])
