@@ -82,6 +82,17 @@ def measured_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+def sm_max_mhz():
+    """Maximum SM clock: MEASURED_PEAKS.json's record, else the part's 2070 MHz."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("sm_max_mhz"):
+            return float(d["sm_max_mhz"])
+    return 2070.0
+
+
 def kernel_source_hash(kernel):
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel]:
@@ -461,6 +472,18 @@ def run_recurrent_line(a, dev):
     step_bytes = state_bytes + th * (BYTES_IN_PER_TOKEN_HEAD + BYTES_OUT_PER_TOKEN_HEAD)
     hbm, _, peak_kind = measured_peaks()
     achieved = step_bytes / (ms_step * 1e-3) / 1e9
+    # fp32 arithmetic against the CUDA cores' peak (SM count x 128 FMA lanes x 2
+    # flop x the maximum SM clock): the launches issue fp32 multiply-adds
+    if inp["cu_seqlens"] is not None:
+        cu = inp["cu_seqlens"].tolist()
+        chunks = sum((cu[i + 1] - cu[i] + 63) // 64 for i in range(len(cu) - 1))
+    else:
+        chunks = int(inp["q"].shape[0]) * ((int(inp["q"].shape[1]) + 63) // 64)
+    fma_item = bwd_fma_per_chunk_head()
+    flops = 2.0 * fma_item * chunks * H
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = sm_max_mhz()
+    fp32_peak = sms * 128 * 2 * mhz * 1e6 / 1e12
     # end to end: token inputs H2D from pinned memory and outputs D2H each step,
     # the state resident on the device (a serving loop's traffic)
     names = ["q", "k", "v", "g", "beta"]
@@ -504,6 +527,22 @@ def run_recurrent_line(a, dev):
 # backward bytes per token-head: q, k, v, g, dout (bf16) and beta in; dq, dk,
 # dv, dg (fp32) and dbeta (fp32) out
 BWD_BYTES_PER_TOKEN_HEAD = 5 * 2 * K_DIM + 2 + 4 * 4 * K_DIM + 4
+
+
+def bwd_fma_per_chunk_head(C=64, D=K_DIM):
+    """fp32 multiply-adds of the chunked backward per (64-token chunk, head),
+    as it is formulated (dense C x C factors, padded chunks): recompute, the two
+    state chains, the gradient products and the chunk gradients."""
+    prep = (4 * 136 * D * 2                                  # G, P inside the 16-token blocks
+            + sum(16 * 16 * i * D * 2 for i in (1, 2, 3))    # G, P left of the diagonal blocks
+            + 4 * 16 * 120 + sum((4 - d) * 256 * (16 * d + 16) for d in (1, 2, 3))  # (I+A)^-1
+            + 2 * C * C * D)                                 # W, U
+    fwd = 2 * C * D * D                                      # U - W S^T, U_new^T Khat
+    rev = C * D * (D + C) + 2 * D * D * C                    # dU; dS
+    prod = 3 * C * D * D + 2 * C * C * D + C * C * D + 2 * C * D * C + D * D  # dQg dW dKhat; dT; dP; dV dKg; dgC
+    grad = (2 * C ** 3 + 4 * 16 * 15 * D * 4                  # dM; pairwise inside the blocks
+            + 2 * sum(16 * 16 * i * D * 2 for i in (1, 2, 3)) + C * D * 6)  # left of the blocks; scalings
+    return prep + fwd + rev + prod + grad
 
 
 def run_backward_line(a, dev):
@@ -561,6 +600,18 @@ def run_backward_line(a, dev):
     step_bytes = th * BWD_BYTES_PER_TOKEN_HEAD + st_bytes
     hbm, _, peak_kind = measured_peaks()
     achieved = step_bytes / (ms_step * 1e-3) / 1e9
+    # fp32 arithmetic against the CUDA cores' peak (SM count x 128 FMA lanes x 2
+    # flop x the maximum SM clock): the launches issue fp32 multiply-adds
+    if inp["cu_seqlens"] is not None:
+        cu = inp["cu_seqlens"].tolist()
+        chunks = sum((cu[i + 1] - cu[i] + 63) // 64 for i in range(len(cu) - 1))
+    else:
+        chunks = int(inp["q"].shape[0]) * ((int(inp["q"].shape[1]) + 63) // 64)
+    fma_item = bwd_fma_per_chunk_head()
+    flops = 2.0 * fma_item * chunks * H
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = sm_max_mhz()
+    fp32_peak = sms * 128 * 2 * mhz * 1e6 / 1e12
     # end to end: inputs and dout in from pinned host memory, token gradients
     # back, around the same call
     names = ["q", "k", "v", "g", "beta"]
@@ -603,10 +654,15 @@ def run_backward_line(a, dev):
             "unit": "tokens/s", "n_gpus": 1, "steps": steps, "warmup": a.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic", "config": cfg,
-            "roofline": {"bound": "hbm", "kernel": f"kda_bwd ({launches} launches)", "achieved": achieved,
-                         "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
-                         "algorithmic_bytes_per_launch": step_bytes, "dominant_launch": dom,
-                         "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"},
+            "roofline": {"bound": "alu", "kernel": f"kda_bwd ({launches} launches)",
+                         "achieved": flops / (ms_step * 1e-3) / 1e12, "peak": fp32_peak, "unit": "TFLOP/s",
+                         "frac": flops / (ms_step * 1e-3) / 1e12 / fp32_peak, "traffic": None,
+                         "fp32_fma_per_chunk_head": fma_item, "chunk_heads": chunks * H,
+                         "dominant_launch": dom,
+                         "peak_source": f"{sms} SMs x 128 fp32 FMA lanes x 2 flop x {mhz:.0f} MHz (unit counts, maximum clock)",
+                         "hbm": {"achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                                 "algorithmic_bytes_per_call": step_bytes,
+                                 "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})"}},
             "stages_ms": stage, "gpu_launches": launches * steps, "clocks": clk.summary(w0, w1),
             "e2e": {"value": tokens / (e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}}
