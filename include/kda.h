@@ -284,7 +284,7 @@ typedef struct kda_bwd_args {
   float *dinitial_state;
 } kda_bwd_args;
 
-/* Device scratch for kda_bwd: one 395,008-byte item per (chunk slot, head),
+/* Device scratch for kda_bwd: one 559,872-byte item per (chunk slot, head),
  * holding the chunk's recomputed quantities, the state before the chunk and the
  * state gradient after it (fp32), for B * ceil(T / 64) chunk slots, or
  * ceil(T / 64) + N with cu_seqlens after a 256-byte-rounded header of

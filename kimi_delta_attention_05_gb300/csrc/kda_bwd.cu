@@ -90,8 +90,15 @@ constexpr int kItemDT = 94208;    // dT [64][64]
 constexpr int kItemGC = 98304;    // gC [128]
 constexpr int kItemDGC = 98432;   // dgC [128]
 constexpr int kItemPart = 98560;  // parts of ddt_bias [128] and dA_log [1]
-constexpr int kItemFloats = 98752;  // 395,008 bytes, a multiple of 256
-static_assert(kItemPart + kD + 1 <= kItemFloats && kItemFloats % 64 == 0, "item layout");
+constexpr int kItemQh = 98752;    // q (L2-normalised if asked) [64][128]
+constexpr int kItemKn = 106944;   // k (L2-normalised if asked) [64][128]
+constexpr int kItemGm = 115136;   // Gamma [64][128]
+constexpr int kItemDz = 123328;   // da/dz of the gate [64][128]
+constexpr int kItemDa = 131520;   // da/dA_log of the gate [64][128]
+constexpr int kItemVec = 139712;  // beta [64], norm factors of q [64] and k [64]
+constexpr int kItemFloats = 139968;  // 559,872 bytes, a multiple of 256
+static_assert(kItemPart + kD + 1 <= kItemQh && kItemVec + 3 * kC <= kItemFloats && kItemFloats % 64 == 0,
+              "item layout");
 
 constexpr int kStage = 16 * (kLs + kLd);  // GEMM staging floats
 constexpr int kProdFloats = kC * kLd + kStage;
@@ -129,17 +136,6 @@ __device__ __forceinline__ f2_t fma2(f2_t a, f2_t b, f2_t c) {
   return d;
 }
 __device__ __forceinline__ ulonglong2 ld2x2(const float* p) { return *reinterpret_cast<const ulonglong2*>(p); }
-__device__ __forceinline__ void ld8(const float* p, float (&x)[8]) {  // p 16-byte aligned
-  const float4 a = ld4(p), b = ld4(p + 4);
-  x[0] = a.x;
-  x[1] = a.y;
-  x[2] = a.z;
-  x[3] = a.w;
-  x[4] = b.x;
-  x[5] = b.y;
-  x[6] = b.z;
-  x[7] = b.w;
-}
 // e^x of a decay exponent (x <= 0 up to rounding): the hardware exponential,
 // relative error a few 1e-7 plus |x| 2^-24 from the base change, far inside
 // the gradients' tolerance
@@ -176,30 +172,6 @@ __device__ __forceinline__ float gate_a(int mode, float z, float amul, float lb,
 __device__ __forceinline__ float gate_mul(const BwdParams& p, int h) {
   return (p.A_log && p.gate_mode != kGateLogspace) ? expf(p.A_log[h]) : 1.f;
 }
-// z of elements (row, c0 .. c0 + 7), c0 a multiple of 8
-__device__ __forceinline__ void gate_z8(const BwdParams& p, int64_t row, int h, int c0, float (&z)[8]) {
-  if (p.g32) {
-    ld8(p.g32 + row * kD + c0, z);
-  } else {
-    const uint4 r = *reinterpret_cast<const uint4*>(p.g + row * kD + c0);
-    const float2 a = unpack_bf16(r.x), b = unpack_bf16(r.y), c = unpack_bf16(r.z), d = unpack_bf16(r.w);
-    z[0] = a.x;
-    z[1] = a.y;
-    z[2] = b.x;
-    z[3] = b.y;
-    z[4] = c.x;
-    z[5] = c.y;
-    z[6] = d.x;
-    z[7] = d.y;
-  }
-  if (p.gate_mode != kGateLogspace && p.dt_bias) {
-    float d[8];
-    ld8(p.dt_bias + h * kD + c0, d);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) z[j] += d[j];
-  }
-}
-
 // Token range of a chunk slot: rows t0 .. t0 + L - 1 of sequence n.  False for
 // a slot past the last chunk (varlen workspaces are sized for the worst case).
 struct ChunkLoc {
@@ -281,9 +253,11 @@ __device__ void load_rows(const BwdParams& p, const ChunkLoc& cl, int h, float* 
 // Gamma [64][kLd]: the in-chunk cumulative sums of the activated gate (a = 0 on
 // rows >= L).  kNT threads: thread = (channel, group of 64 / (kNT / 128)
 // consecutive tokens); each group then adds the totals of the groups before it.
-// Ends with a barrier.
+// The gate's derivatives da/dz and da/dA_log go to dz_out, da_out ([64][128],
+// zero on rows >= L).  Ends with a barrier.
 template <int kNT>
-__device__ void gate_cumsum(const BwdParams& p, const ChunkLoc& cl, int h, float* Gm) {
+__device__ void gate_cumsum(const BwdParams& p, const ChunkLoc& cl, int h, float* Gm, float* dz_out,
+                            float* da_out) {
   constexpr int kG = kNT / kD, kN = kC / kG;
   const int c = threadIdx.x & (kD - 1), grp = threadIdx.x >> 7;
   const float amul = gate_mul(p, h);
@@ -301,9 +275,11 @@ __device__ void gate_cumsum(const BwdParams& p, const ChunkLoc& cl, int h, float
 #pragma unroll
   for (int i = 0; i < kN; ++i) {
     const int t = kN * grp + i;
-    float d1, d2;
+    float d1 = 0.f, d2 = 0.f;
     if (t < cl.L) acc += gate_a(p.gate_mode, z[i] + dtb, amul, p.lower_bound, d1, d2);
     Gm[t * kLd + c] = acc;
+    dz_out[t * kD + c] = t < cl.L ? d1 : 0.f;
+    da_out[t * kD + c] = t < cl.L ? d2 : 0.f;
   }
   __syncthreads();
   float base = 0.f;
@@ -448,7 +424,7 @@ __device__ __forceinline__ void zero_acc(float (&acc)[4][N]) {
 
 // ==== 1. prep ====
 constexpr int kPT = 512;  // threads of the prep and chunk-gradient kernels
-constexpr int kPrepFloats = 3 * kC * kLd + 3 * kC * kLs + 80 * kLd + 2 * kStage + kC;
+constexpr int kPrepFloats = 3 * kC * kLd + 3 * kC * kLs + 80 * kLd + 2 * kStage + 3 * kC;
 
 __global__ void __launch_bounds__(kPT, 1) kda_bwd_prep_kernel(BwdParams p) {
   extern __shared__ __align__(16) float sm[];
@@ -468,9 +444,17 @@ __global__ void __launch_bounds__(kPT, 1) kda_bwd_prep_kernel(BwdParams p) {
   if (!locate(p, slot, cl)) return;
   float* it = p.ws + item * (int64_t)kItemFloats;
 
-  load_rows<kPT>(p, cl, h, Kh, Qh, vb, nullptr, nullptr);
+  load_rows<kPT>(p, cl, h, Kh, Qh, vb, vb + kC, vb + 2 * kC);
   __syncthreads();
-  gate_cumsum<kPT>(p, cl, h, Gm);
+  gate_cumsum<kPT>(p, cl, h, Gm, it + kItemDz, it + kItemDa);
+  // normalised q, k, Gamma, beta and the norm factors, for the chunk-gradient kernel
+  for (int e = tid; e < kC * 32; e += kPT) {
+    const int t = e >> 5, c = 4 * (e & 31);
+    *reinterpret_cast<float4*>(it + kItemQh + t * kD + c) = ld4(Qh + t * kLd + c);
+    *reinterpret_cast<float4*>(it + kItemKn + t * kD + c) = ld4(Kh + t * kLd + c);
+    *reinterpret_cast<float4*>(it + kItemGm + t * kD + c) = ld4(Gm + t * kLd + c);
+  }
+  if (tid < 3 * kC) it[kItemVec + tid] = vb[tid];
 
   // G and P inside the 16-token diagonal blocks, pair by pair: one thread per pair
   for (int e = tid; e < 4 * 136; e += kPT) {
@@ -1186,22 +1170,6 @@ __global__ void __launch_bounds__(256, 2) kda_bwd_prod_kernel(BwdParams p) {
 // cb = 64 hf + 4 tx .. cb + 3, in registers.
 constexpr int kGradFloats = 3 * kC * kLd + 2 * kC * kLs + 80 * kLd + kStage + 16 * kD + 4 * kC + 4 * kC;
 
-// g + dt_bias (logspace: g) of elements (row, c0 .. c0 + 3), c0 a multiple of 4
-__device__ __forceinline__ float4 gate_z4(const BwdParams& p, int64_t row, int h, int c0) {
-  float4 z;
-  if (p.g32) {
-    z = ld4(p.g32 + row * kD + c0);
-  } else {
-    const uint2 r = *reinterpret_cast<const uint2*>(p.g + row * kD + c0);
-    const float2 a = unpack_bf16(r.x), b = unpack_bf16(r.y);
-    z = make_float4(a.x, a.y, b.x, b.y);
-  }
-  if (p.gate_mode != kGateLogspace && p.dt_bias) {
-    const float4 d = ld4(p.dt_bias + h * kD + c0);
-    z = make_float4(z.x + d.x, z.y + d.y, z.z + d.z, z.w + d.w);
-  }
-  return z;
-}
 __device__ __forceinline__ void f4a(float4 v, float (&x)[4]) {
   x[0] = v.x;
   x[1] = v.y;
@@ -1231,26 +1199,31 @@ __global__ void __launch_bounds__(kPT, 1) kda_bwd_grad_kernel(BwdParams p) {
   ChunkLoc cl;
   if (!locate(p, slot, cl)) return;
   float* it = p.ws + item * (int64_t)kItemFloats;
-  // dT, Minv and P into shared memory (Minv where dG goes later, dT at the
-  // start of the scratch area) while the rows load and the gate runs
+  // the chunk's rows as the recompute left them (normalised k, q, Gamma; beta
+  // and the norm factors), dT, Minv and P (Minv where dG goes later, dT at the
+  // start of the scratch area), into shared memory
+  for (int e = tid; e < kC * 32; e += kPT) {
+    const int t = e >> 5, c = 4 * (e & 31);
+    cp16(Kh + t * kLd + c, it + kItemKn + 4 * e);
+    cp16(Qh + t * kLd + c, it + kItemQh + 4 * e);
+    cp16(Gm + t * kLd + c, it + kItemGm + 4 * e);
+  }
   for (int e = tid; e < kC * 16; e += kPT) {
     const int i = e >> 4, c = 4 * (e & 15);
     cp16(X + i * kLs + c, it + kItemDT + 4 * e);
     cp16(dGs + i * kLs + c, it + kItemMi + 4 * e);
     cp16(dPs + i * kLs + c, it + kItemP + 4 * e);
   }
+  if (tid < 3 * kC / 4) cp16(vb + 4 * tid, it + kItemVec + 4 * tid);  // vb, rq, rk contiguous
   cp_commit();
-
-  load_rows<kPT>(p, cl, h, Kh, Qh, vb, rq, rk);
-  __syncthreads();
-  gate_cumsum<kPT>(p, cl, h, Gm);
 
   // ---- dM = -Minv^T (dT Diag(beta)) Minv^T, dA, dG, dbeta (threads 0-255) ----
   {
     float* Mi = dGs;            // Minv [64][kLs] until dG replaces it
     float* Xa = X;              // dT
     float* Xb = X + kC * kLs;   // (Minv^T dT) Diag(beta)
-    cp_wait<0>();               // (made visible by the barrier the product begins with)
+    cp_wait<0>();
+    __syncthreads();
     const bool act = hf == 0;
     float a2[4][4];
     zero_acc(a2);
@@ -1480,22 +1453,24 @@ __global__ void __launch_bounds__(kPT, 1) kda_bwd_grad_kernel(BwdParams p) {
   }
   __syncthreads();
   // ---- outputs ----
-  const float amul = gate_mul(p, h);
   float pdt[4] = {0.f, 0.f, 0.f, 0.f}, pal = 0.f;
-  float4 zall[4];
+  float4 dzall[4], daall[4];
 #pragma unroll
-  for (int m = 0; m < 4; ++m)  // every load first (rows past the chunk re-read its last row)
-    zall[m] = gate_z4(p, (cl.t0 + min(16 * m + ty, cl.L - 1)) * p.H + h, h, cb);
+  for (int m = 0; m < 4; ++m) {  // every load first: the gate's derivatives from the recompute
+    dzall[m] = ld4(it + kItemDz + (16 * m + ty) * kD + cb);
+    daall[m] = ld4(it + kItemDa + (16 * m + ty) * kD + cb);
+  }
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
     const int t = 16 * m + ty;
     if (t >= cl.L) continue;
     const int64_t row = (cl.t0 + t) * p.H + h;
-    float qv[4], kv[4], dav[4], zv[4];
+    float qv[4], kv[4], dav[4], dzv[4], dAv[4];
     f4a(ld4(Qh + t * kLd + cb), qv);
     f4a(ld4(Kh + t * kLd + cb), kv);
     f4a(ld4(Dg + t * kLd + cb), dav);
-    f4a(zall[m], zv);
+    f4a(dzall[m], dzv);
+    f4a(daall[m], dAv);
     const float xq = xs[t] + xs[2 * kC + t], xk = xs[kC + t] + xs[3 * kC + t];
     float dq[4], dk[4], dz[4];
 #pragma unroll
@@ -1507,11 +1482,9 @@ __global__ void __launch_bounds__(kPT, 1) kda_bwd_grad_kernel(BwdParams p) {
         dq[j] = aQ[m][j];
         dk[j] = aK[m][j];
       }
-      float dadz, dadA;
-      gate_a(p.gate_mode, zv[j], amul, p.lower_bound, dadz, dadA);
-      dz[j] = dav[j] * dadz;
+      dz[j] = dav[j] * dzv[j];
       pdt[j] += dz[j];
-      pal = fmaf(dav[j], dadA, pal);
+      pal = fmaf(dav[j], dAv[j], pal);
     }
     st4(p.dq + row * kD + cb, dq[0], dq[1], dq[2], dq[3]);
     st4(p.dk + row * kD + cb, dk[0], dk[1], dk[2], dk[3]);

@@ -113,7 +113,7 @@ def test_backward_rejects_bad_arguments():
     assert lib.kda_bwd(ctypes.byref(a), None, 0, None) != 0  # K = V = 0, flags 0
 
 
-ITEM_BYTES = 395008  # workspace per (64-token chunk slot, head)
+ITEM_BYTES = 559872  # workspace per (64-token chunk slot, head)
 
 
 @pytest.mark.parametrize("H", [24, 160])
