@@ -1261,41 +1261,17 @@ __global__ void __launch_bounds__(kPT, 1) kda_bwd_grad_kernel(BwdParams p) {
   }
   __syncthreads();
 
+  // The pairwise sums G and P contribute, per row t and channel c, three sums:
+  //   xi = sum_{s<t} dG_ts k_s F_ts     (t the later token of a G term)
+  //   xp = sum_{s<=t} dP_ts k_s F_ts    (t the later token of a P term)
+  //   yj = sum_{i>t} (dG_it k_i + dP_it q_i) F_it   (t the earlier token; i = t for P)
+  // giving dk += xi + yj, dq += xp and dGamma += k xi + q xp - k yj.  Registers:
+  // aK = xi, aQ = xp, aG = yj until the scalings below combine them.
   float aQ[4][4], aK[4][4], aG[4][4];
-  // ---- the scalings: Qg = q e^Gamma, Kg = k e^Gamma, Khat = k e^{Gamma_C - Gamma} ----
-  {
-    float cs[4] = {0.f, 0.f, 0.f, 0.f};
-    float4 gq[4], gk[4], gh[4];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {  // every load first
-      const int o = (16 * m + ty) * kD + cb;
-      gq[m] = ld4(it + kItemQg + o);
-      gk[m] = ld4(it + kItemW + o);
-      gh[m] = ld4(it + kItemKh + o);
-    }
-    float glv[4];
-    f4a(ld4(Gm + (kC - 1) * kLd + cb), glv);
+  for (int m = 0; m < 4; ++m)
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const int t = 16 * m + ty;
-      float dqv[4], dkv[4], dhv[4], gtv[4], qhv[4], khv[4];
-      f4a(gq[m], dqv);
-      f4a(gk[m], dkv);
-      f4a(gh[m], dhv);
-      f4a(ld4(Gm + t * kLd + cb), gtv);
-      f4a(ld4(Qh + t * kLd + cb), qhv);
-      f4a(ld4(Kh + t * kLd + cb), khv);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float e = dexp(gtv[j]), ec = dexp(glv[j] - gtv[j]);
-        aQ[m][j] = dqv[j] * e;
-        aK[m][j] = dkv[j] * e + dhv[j] * ec;
-        aG[m][j] = dqv[j] * qhv[j] * e + dkv[j] * khv[j] * e - dhv[j] * khv[j] * ec;
-        cs[j] += dhv[j] * khv[j] * ec;
-      }
-    }
-    st4(part + ty * kD + cb, cs[0], cs[1], cs[2], cs[3]);
-  }
+    for (int j = 0; j < 4; ++j) aQ[m][j] = aK[m][j] = aG[m][j] = 0.f;
   // ---- G and P inside the diagonal blocks, pair by pair ----
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
@@ -1307,16 +1283,15 @@ __global__ void __launch_bounds__(kPT, 1) kda_bwd_grad_kernel(BwdParams p) {
     const float dpd = dPs[t * kLs + t];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      aQ[m][j] = fmaf(dpd, kt[j], aQ[m][j]);
-      aK[m][j] = fmaf(dpd, qt[j], aK[m][j]);
+      aQ[m][j] = dpd * kt[j];
+      aG[m][j] = dpd * qt[j];
     }
 #pragma unroll 4
     for (int s = 16 * m; s < 16 * m + 16; ++s) {
       if (s == t) continue;
-      float gs[4], ks[4], qs[4];
+      float gs[4], ks[4];
       f4a(ld4(Gm + s * kLd + cb), gs);
       f4a(ld4(Kh + s * kLd + cb), ks);
-      f4a(ld4(Qh + s * kLd + cb), qs);
       if (s < t) {  // t takes the role of the later token
         const float dg = dGs[t * kLs + s], dp = dPs[t * kLs + s];
 #pragma unroll
@@ -1324,16 +1299,13 @@ __global__ void __launch_bounds__(kPT, 1) kda_bwd_grad_kernel(BwdParams p) {
           const float f = dexp(gt[j] - gs[j]) * ks[j];
           aK[m][j] = fmaf(dg, f, aK[m][j]);
           aQ[m][j] = fmaf(dp, f, aQ[m][j]);
-          aG[m][j] = fmaf(dg * kt[j] + dp * qt[j], f, aG[m][j]);
         }
       } else {  // t is the earlier token
         const float dg = dGs[s * kLs + t], dp = dPs[s * kLs + t];
+        float qs[4];
+        f4a(ld4(Qh + s * kLd + cb), qs);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float w = (dg * ks[j] + dp * qs[j]) * dexp(gs[j] - gt[j]);
-          aK[m][j] += w;
-          aG[m][j] = fmaf(-w, kt[j], aG[m][j]);
-        }
+        for (int j = 0; j < 4; ++j) aG[m][j] = fmaf(fmaf(dg, ks[j], dp * qs[j]), dexp(gs[j] - gt[j]), aG[m][j]);
       }
     }
   }
@@ -1363,7 +1335,7 @@ __global__ void __launch_bounds__(kPT, 1) kda_bwd_grad_kernel(BwdParams p) {
       }
     }
     __syncthreads();
-    {  // rows of block I (t = r + ty): X_G = dG R, X_P = dP R over s < r
+    {  // rows of block I (t = r + ty): xi += l (dG R), xp += l (dP R) over s < r, l = e^{Gamma_t - Gamma_r}
       const int t = r + ty;
       float xg[4] = {0.f, 0.f, 0.f, 0.f}, xp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
@@ -1377,21 +1349,18 @@ __global__ void __launch_bounds__(kPT, 1) kda_bwd_grad_kernel(BwdParams p) {
           xp[j] = fmaf(dp, rr[j], xp[j]);
         }
       }
-      float gtv[4], grv[4], ktv[4], qtv[4];
+      float gtv[4], grv[4];
       f4a(ld4(Gm + t * kLd + cb), gtv);
       f4a(ld4(Gm + r * kLd + cb), grv);
-      f4a(ld4(Kh + t * kLd + cb), ktv);
-      f4a(ld4(Qh + t * kLd + cb), qtv);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const float l = dexp(gtv[j] - grv[j]);
         aK[I][j] = fmaf(l, xg[j], aK[I][j]);
         aQ[I][j] = fmaf(l, xp[j], aQ[I][j]);
-        aG[I][j] = fmaf(l, ktv[j] * xg[j] + qtv[j] * xp[j], aG[I][j]);
       }
     }
 #pragma unroll
-    for (int m = 0; m < I; ++m) {  // rows s = 16 m + ty < r: Y = dG^T Lk + dP^T Lq over block I
+    for (int m = 0; m < I; ++m) {  // rows s = 16 m + ty < r: yj += e^{Gamma_r - Gamma_s} (dG^T Lk + dP^T Lq)
       const int s = 16 * m + ty;
       float y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
@@ -1403,16 +1372,49 @@ __global__ void __launch_bounds__(kPT, 1) kda_bwd_grad_kernel(BwdParams p) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) y[j] = fmaf(dg, kr[j], fmaf(dp, qr[j], y[j]));
       }
-      float rrv[4], grv[4], gsv[4];
-      f4a(ld4(R + s * kLd + cb), rrv);  // k_s e^{Gamma_r - Gamma_s}
+      float grv[4], gsv[4];
       f4a(ld4(Gm + r * kLd + cb), grv);
       f4a(ld4(Gm + s * kLd + cb), gsv);
 #pragma unroll
+      for (int j = 0; j < 4; ++j) aG[m][j] = fmaf(dexp(grv[j] - gsv[j]), y[j], aG[m][j]);
+    }
+  }
+  // ---- the scalings Qg = q e^Gamma, Kg = k e^Gamma, Khat = k e^{Gamma_C - Gamma}, and the
+  // combination of the pairwise sums ----
+  {
+    float cs[4] = {0.f, 0.f, 0.f, 0.f};
+    float4 gq[4], gk[4], gh[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {  // every load first
+      const int o = (16 * m + ty) * kD + cb;
+      gq[m] = ld4(it + kItemQg + o);
+      gk[m] = ld4(it + kItemW + o);
+      gh[m] = ld4(it + kItemKh + o);
+    }
+    float glv[4];
+    f4a(ld4(Gm + (kC - 1) * kLd + cb), glv);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int t = 16 * m + ty;
+      float dqv[4], dkv[4], dhv[4], gtv[4], qhv[4], khv[4];
+      f4a(gq[m], dqv);
+      f4a(gk[m], dkv);
+      f4a(gh[m], dhv);
+      f4a(ld4(Gm + t * kLd + cb), gtv);
+      f4a(ld4(Qh + t * kLd + cb), qhv);
+      f4a(ld4(Kh + t * kLd + cb), khv);
+#pragma unroll
       for (int j = 0; j < 4; ++j) {
-        aK[m][j] = fmaf(dexp(grv[j] - gsv[j]), y[j], aK[m][j]);
-        aG[m][j] = fmaf(-rrv[j], y[j], aG[m][j]);
+        const float e = dexp(gtv[j]), ec = dexp(glv[j] - gtv[j]);
+        const float xi = aK[m][j], xp = aQ[m][j], yj = aG[m][j];
+        aQ[m][j] = xp + dqv[j] * e;
+        aK[m][j] = xi + yj + dkv[j] * e + dhv[j] * ec;
+        aG[m][j] = khv[j] * (xi - yj) + qhv[j] * xp + dqv[j] * qhv[j] * e + dkv[j] * khv[j] * e -
+                   dhv[j] * khv[j] * ec;
+        cs[j] += dhv[j] * khv[j] * ec;
       }
     }
+    st4(part + ty * kD + cb, cs[0], cs[1], cs[2], cs[3]);
   }
   __syncthreads();
   // ---- dGamma -> da by the reverse cumulative sum; row sums of the norm terms ----
