@@ -139,3 +139,51 @@ def test_backward_packed_workspace():
                            d["initial_state"], None, d["cu_seqlens"], qk_l2norm=True, gate="safe")
     T, N = 74, 5
     assert K.bwd_workspace_bytes(a) == 256 + ((T + 63) // 64 + N) * 2 * ITEM_BYTES
+
+
+def _head_slice(inp, h, dout, dfin):
+    """Inputs of head h alone (heads are independent), for the oracle."""
+    s3 = lambda x: None if x is None else x[:, :, h:h + 1]
+    st = lambda x: None if x is None else x[:, h:h + 1]
+    return dict(q=s3(inp["q"]), k=s3(inp["k"]), v=s3(inp["v"]), g=s3(inp["g"]), beta=inp["beta"][:, :, h:h + 1],
+                dout=dout[:, :, h:h + 1], A_log=inp["A_log"][h:h + 1], dt_bias=inp["dt_bias"][h:h + 1],
+                initial_state=st(inp["initial_state"]), dfinal=None if dfin is None else st(dfin),
+                cu_seqlens=inp["cu_seqlens"])
+
+
+@pytest.mark.parametrize("workload,heads", [("long_context", (0, 29)), ("dense_batch", (5,))])
+def test_backward_full_size_sampled(workload, heads):
+    """The full-size workload through kda_bwd (every chunk of every head, the
+    launch configuration the benchmark times), checked against the chunked fp64
+    oracle on sampled heads: every token gradient of the head, its dA_log and
+    dt_bias sums and (with states) its initial-state gradient."""
+    inp = make_inputs(WORKLOADS[workload])
+    gen = torch.Generator().manual_seed(77)
+    dout = (torch.randn(inp["v"].shape, generator=gen) * 0.5).to(torch.bfloat16)
+    H = inp["q"].shape[2]
+    dfin = torch.randn((inp["N"], H, 128, 128), generator=gen) * 0.1 if inp["initial_state"] is not None else None
+    d = tl.to_device(inp)
+    lb = inp["lower_bound"] if inp["gate"] == "safe" else None
+    grads = K.kda_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], inp["scale"], dout.cuda(), d["A_log"],
+                      d["dt_bias"], lb, d["initial_state"], None if dfin is None else dfin.cuda(),
+                      d["cu_seqlens"], qk_l2norm=inp["qk_l2norm"], gate=inp["gate"])
+    torch.cuda.synchronize()
+    for h in heads:
+        a = _head_slice(inp, h, dout, dfin)
+        ref = oracle.chunk_backward(a["q"], a["k"], a["v"], a["g"], a["beta"], a["dout"], scale=inp["scale"],
+                                    A_log=a["A_log"], dt_bias=a["dt_bias"], lower_bound=inp["lower_bound"],
+                                    gate=inp["gate"], qk_l2norm=inp["qk_l2norm"], initial_state=a["initial_state"],
+                                    dfinal=a["dfinal"], cu_seqlens=a["cu_seqlens"])
+        errs = {}
+        for name in ("q", "k", "v", "g", "beta"):
+            errs[name] = _check(f"{workload} h={h} d{name}", grads[name][:, :, h:h + 1].double().cpu().numpy(),
+                                ref[name])
+        errs["A_log"] = _check(f"{workload} h={h} dA_log", grads["A_log"][h:h + 1].double().cpu().numpy(),
+                               ref["A_log"])
+        errs["dt_bias"] = _check(f"{workload} h={h} ddt_bias", grads["dt_bias"][h:h + 1].double().cpu().numpy(),
+                                 ref["dt_bias"])
+        if dfin is not None:
+            errs["initial_state"] = _check(f"{workload} h={h} dinit",
+                                           grads["initial_state"][:, h:h + 1].double().cpu().numpy(),
+                                           ref["initial_state"])
+        tl.record_grad_margin(f"{workload} full h={h}", errs)
