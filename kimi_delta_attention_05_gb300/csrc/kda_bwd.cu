@@ -29,15 +29,16 @@
 //
 // Launches:
 //  1. prep, one CTA per (chunk, head): Gamma, G, P, Minv, W, U, Khat, Qg, Kg, gC
-//     into the chunk's workspace item;
+//     into the chunk's workspace item, with the normalised rows, beta, the norm
+//     factors and the gate's derivatives for launch 5;
 //  2. forward state pass, one CTA per (sequence, head, 32 value rows): walks the
 //     chunks, storing S before each chunk and Unew (value rows are independent);
 //  3. reverse state pass, same grid, chunks last to first from dfinal: stores
 //     dS_C and dU of each chunk, then dinitial;
 //  4. gradient products, one CTA per (chunk, head): dQg, dKhat, dKg, dP, dT, dgC, dv;
 //  5. chunk gradients, one CTA per (chunk, head): dM, dG, dbeta, the pairwise
-//     terms, the scalings, the cumulative sum, gate and norms: dq, dk, dg,
-//     dbeta, and the chunk's parts of dA_log and dt_bias;
+//     terms, the scalings, the cumulative sum, gate and norm derivatives: dq,
+//     dk, dg, dbeta, and the chunk's parts of dA_log and dt_bias;
 //  6. finalize, one CTA per head: those parts summed over the chunks in order.
 #include <atomic>
 
@@ -136,9 +137,9 @@ __device__ __forceinline__ f2_t fma2(f2_t a, f2_t b, f2_t c) {
   return d;
 }
 __device__ __forceinline__ ulonglong2 ld2x2(const float* p) { return *reinterpret_cast<const ulonglong2*>(p); }
-// e^x of a decay exponent (x <= 0 up to rounding): the hardware exponential,
-// relative error a few 1e-7 plus |x| 2^-24 from the base change, far inside
-// the gradients' tolerance
+// e^x of a decay exponent (x <= 0 up to rounding): the fast exponential, whose
+// error (a few ulp, growing with |x|) stays far inside the gradients'
+// tolerance; the accurate expf gives the same gradient errors at full size
 __device__ __forceinline__ float dexp(float x) { return __expf(x); }
 __device__ __forceinline__ void st4(float* p, float a, float b, float c, float d) {
   *reinterpret_cast<float4*>(p) = make_float4(a, b, c, d);
