@@ -187,3 +187,24 @@ def test_backward_full_size_sampled(workload, heads):
                                            grads["initial_state"][:, h:h + 1].double().cpu().numpy(),
                                            ref["initial_state"])
         tl.record_grad_margin(f"{workload} full h={h}", errs)
+
+
+def test_backward_is_deterministic():
+    """Two calls on the same inputs give the same bits for every gradient
+    (dA_log and dt_bias included: per-chunk parts summed in slot order)."""
+    inp = make_inputs(WORKLOADS["packed_varlen"], lengths=[130, 0, 77, 64, 1], H=4, seed=240)
+    gen = torch.Generator().manual_seed(241)
+    dout = (torch.randn(inp["v"].shape, generator=gen) * 0.5).to(torch.bfloat16).cuda()
+    dfin = (torch.randn((inp["N"], 4, 128, 128), generator=gen) * 0.1).cuda()
+    d = tl.to_device(inp)
+
+    def call():
+        g = K.kda_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], inp["scale"], dout, d["A_log"], d["dt_bias"],
+                      inp["lower_bound"], d["initial_state"], dfin, d["cu_seqlens"], qk_l2norm=True, gate="safe")
+        torch.cuda.synchronize()
+        return g
+
+    a, b = call(), call()
+    for name, x in a.items():
+        if x is not None:
+            assert torch.equal(x, b[name]), name
