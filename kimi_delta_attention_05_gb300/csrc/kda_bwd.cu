@@ -1045,7 +1045,7 @@ __global__ void __launch_bounds__(kSt, 1) kda_bwd_rev_state_kernel(BwdParams p) 
 }
 
 // ==== 4. gradient products ====
-__global__ void __launch_bounds__(256, 2) kda_bwd_prod_kernel(BwdParams p) {
+__global__ void __launch_bounds__(256, 3) kda_bwd_prod_kernel(BwdParams p) {
   extern __shared__ __align__(16) float sm[];
   float* dWs = sm;  // [64][kLd]
   float* stage = dWs + kC * kLd;
