@@ -656,13 +656,15 @@ constexpr int kRevFloats = 3 * kC * kLd + kC * kLs + kSv * kLd + 2 * kC * kSu + 
 // CTA = (sequence, head, 32 value rows v0 ..), 512 threads; S of the CTA's rows
 // in registers (product-2 ownership) and shared memory.  Per chunk, W and the
 // CTA's U columns arrive (cp.async) while the previous chunk's product 2 runs,
-// Khat and gC while product 1 runs.  Product 1 (Unew = U - W S^T, 64 x 32 over
-// 128 channels): thread = (2 tokens, 4 value rows, channel half), halves added
-// by a shuffle.  Product 2 (S = S Diag(gC) + Unew^T Khat, 32 x 128 over 64
-// tokens): thread = (4 value rows, channel quads c1 and c1 + 64, tokens t = 4 i + quarter),
-// quarters added by shuffles; every quarter keeps the full result.  Product 1's
-// value rows are v = pv + 8 i (i < 4): rows 8 apart keep its shared-memory
-// reads of S free of bank conflicts.
+// Khat and gC while product 1 runs.  Both products are bound by their
+// shared-memory reads, so each warp covers a block of outputs as square as the
+// register budget allows.  Product 1 (Unew = U - W S^T, 64 x 32 over 128
+// channels): thread = (4 tokens, 4 value rows, channel quads 4 k + quarter),
+// warp = 2 token quads x 4 value quads x 4 quarters, quarters added by
+// shuffles.  Product 2 (S = S Diag(gC) + Unew^T Khat, 32 x 128 over 64
+// tokens): thread = (4 value rows, channel quads c1 and c1 + 64, tokens
+// t = 4 i + quarter), warp = 2 value quads x 4 channel groups x 4 quarters,
+// quarters added by shuffles; every quarter keeps the full result.
 __global__ void __launch_bounds__(kSt, 1) kda_bwd_fwd_state_kernel(BwdParams p) {
   extern __shared__ __align__(16) float sm[];
   float* Wb = sm;                 // W [64][kLd]
@@ -676,9 +678,9 @@ __global__ void __launch_bounds__(kSt, 1) kda_bwd_fwd_state_kernel(BwdParams p) 
   const int v0 = kSv * (int)(blockIdx.x - unit * kSBlocks);
   const int64_t n = unit / p.H;
   const int h = (int)(unit - n * p.H);
-  const int tq = lane & 3, co = ((warp & 1) << 3) | (lane >> 2), vq = warp >> 1;  // product 2
+  const int tq = lane & 3, co = 4 * (warp & 3) + ((lane >> 2) & 3), vq = 2 * (warp >> 2) + (lane >> 4);  // product 2
   const int c1 = 4 * chp(co), c2 = c1 + 64;
-  const int ch = tid & 1, pv = (tid >> 1) & 7, pt = 2 * (tid >> 4);               // product 1
+  const int cq = lane & 3, pvq = 4 * (warp & 1) + ((lane >> 2) & 3), ptq = 2 * (warp >> 1) + (lane >> 4);  // product 1
   int64_t first, count;
   seq_chunks(p, n, first, count);
   auto item = [&](int64_t ci) { return p.ws + ((first + ci) * p.H + h) * (int64_t)kItemFloats; };
@@ -735,47 +737,40 @@ __global__ void __launch_bounds__(kSt, 1) kda_bwd_fwd_state_kernel(BwdParams p) 
         st4(d + 64, s[i][4], s[i][5], s[i][6], s[i][7]);
       }
     {
-      float acc[2][4];
-      {
-        f2_t a2[2][4];
+      f2_t a2[4][4];  // [token i][value row j]
 #pragma unroll
-        for (int r = 0; r < 2; ++r)
+      for (int i = 0; i < 4; ++i)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) a2[r][i] = 0ull;
-#pragma unroll 4
-        for (int k = 0; k < 16; ++k) {
-          const int c = cq(k, ch);
-          const ulonglong2 w0 = ld2x2(Wb + pt * kLd + c), w1 = ld2x2(Wb + (pt + 1) * kLd + c);
+        for (int j = 0; j < 4; ++j) a2[i][j] = 0ull;
+#pragma unroll 2
+      for (int ks = 0; ks < 8; ++ks) {
+        const int c = 4 * (4 * ks + cq);  // quarters interleaved by quad: distinct bank groups
+        ulonglong2 w[4], sv[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const ulonglong2 sv = ld2x2(Ss + (pv + 8 * i) * kLd + c);
-            a2[0][i] = fma2(w0.y, sv.y, fma2(w0.x, sv.x, a2[0][i]));
-            a2[1][i] = fma2(w1.y, sv.y, fma2(w1.x, sv.x, a2[1][i]));
-          }
+        for (int i = 0; i < 4; ++i) w[i] = ld2x2(Wb + (4 * ptq + i) * kLd + c);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sv[j] = ld2x2(Ss + (4 * pvq + j) * kLd + c);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) a2[i][j] = fma2(w[i].y, sv[j].y, fma2(w[i].x, sv[j].x, a2[i][j]));
+      }
+      float r[4] = {0.f, 0.f, 0.f, 0.f};  // the sums of token row 4 ptq + cq
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 v = up2(a2[i][j]);
+          float x = v.x + v.y;
+          x += __shfl_xor_sync(0xffffffffu, x, 1);
+          x += __shfl_xor_sync(0xffffffffu, x, 2);
+          if (cq == i) r[j] = x;
         }
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 v = up2(a2[r][i]);
-            acc[r][i] = v.x + v.y;
-          }
-      }
-#pragma unroll
-      for (int r = 0; r < 2; ++r)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[r][i] += __shfl_xor_sync(0xffffffffu, acc[r][i], 1);
-      if (ch == 0) {
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int v = pv + 8 * i;
-            const float un = Ub[(pt + r) * kSv + v] - acc[r][i];
-            it[kItemU + (pt + r) * kD + v0 + v] = un;
-            Un[(pt + r) * kSu + v] = un;
-          }
-      }
+      const int t = 4 * ptq + cq;
+      const float4 uu = ld4(Ub + t * kSv + 4 * pvq);
+      const float n0 = uu.x - r[0], n1 = uu.y - r[1], n2 = uu.z - r[2], n3 = uu.w - r[3];
+      st4(it + kItemU + t * kD + v0 + 4 * pvq, n0, n1, n2, n3);
+      st4(Un + t * kSu + 4 * pvq, n0, n1, n2, n3);
     }
     __syncthreads();  // Unew complete; Wb, Ub, Ss free
     issue_w(ci + 1);
