@@ -832,12 +832,13 @@ __global__ void __launch_bounds__(kSt, 1) kda_bwd_fwd_state_kernel(BwdParams p) 
 }
 
 // ==== 3. reverse state pass ====
-// Same grid, threads and ownership as the forward pass, chunks last to first.
+// Same grid, threads and warp shapes as the forward pass, chunks last to first.
 // Per chunk, Khat, P, the CTA's dout columns and gC arrive while the previous
 // chunk's product B runs, Qg and W while product A runs.  Product A (dU =
-// scale P^T dO + Khat dS^T, 64 x 32): thread = (2 tokens, 4 value rows, half of
-// the 128 channels and of the 64 tokens j, by parity).  Product B (dS = dS Diag(gC) +
-// scale dO^T Qg - dU^T W, 32 x 128 over 64 tokens).
+// scale P^T dO + Khat dS^T, 64 x 32): thread = (4 tokens, 4 value rows, quarter
+// of the channel quads and of the tokens j).  Product B (dS = dS Diag(gC) +
+// scale dO^T Qg - dU^T W, 32 x 128 over 64 tokens) as the forward pass's
+// product 2.
 __global__ void __launch_bounds__(kSt, 1) kda_bwd_rev_state_kernel(BwdParams p) {
   extern __shared__ __align__(16) float sm[];
   float* Kb = sm;                 // Khat [64][kLd]
@@ -854,9 +855,9 @@ __global__ void __launch_bounds__(kSt, 1) kda_bwd_rev_state_kernel(BwdParams p) 
   const int v0 = kSv * (int)(blockIdx.x - unit * kSBlocks);
   const int64_t n = unit / p.H;
   const int h = (int)(unit - n * p.H);
-  const int tq = lane & 3, co = ((warp & 1) << 3) | (lane >> 2), vq = warp >> 1;
+  const int tq = lane & 3, co = 4 * (warp & 3) + ((lane >> 2) & 3), vq = 2 * (warp >> 2) + (lane >> 4);
   const int c1 = 4 * chp(co), c2 = c1 + 64;
-  const int ch = tid & 1, pv = (tid >> 1) & 7, pt = 2 * (tid >> 4);
+  const int cq = lane & 3, pvq = 4 * (warp & 1) + ((lane >> 2) & 3), ptq = 2 * (warp >> 1) + (lane >> 4);
   int64_t first, count;
   seq_chunks(p, n, first, count);
   const int64_t bos = p.cu ? p.cu[n] : n * p.T, eos = p.cu ? p.cu[n + 1] : (n + 1) * p.T;
@@ -919,56 +920,55 @@ __global__ void __launch_bounds__(kSt, 1) kda_bwd_rev_state_kernel(BwdParams p) 
       }
     __syncthreads();
     {
-      float acc[2][4];
-      {
-        f2_t a2[2][4];
+      f2_t a2[4][4];  // [token i][value row j]: Khat dS^T over this quarter's channel quads
 #pragma unroll
-        for (int r = 0; r < 2; ++r)
+      for (int i = 0; i < 4; ++i)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) a2[r][i] = 0ull;
-#pragma unroll 4
-        for (int k = 0; k < 16; ++k) {
-          const int c = cq(k, ch);
-          const ulonglong2 k0 = ld2x2(Kb + pt * kLd + c), k1 = ld2x2(Kb + (pt + 1) * kLd + c);
+        for (int j = 0; j < 4; ++j) a2[i][j] = 0ull;
+#pragma unroll 2
+      for (int ks = 0; ks < 8; ++ks) {
+        const int c = 4 * (4 * ks + cq);
+        ulonglong2 kk[4], dd[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const ulonglong2 d = ld2x2(Ds + (pv + 8 * i) * kLd + c);
-            a2[0][i] = fma2(k0.y, d.y, fma2(k0.x, d.x, a2[0][i]));
-            a2[1][i] = fma2(k1.y, d.y, fma2(k1.x, d.x, a2[1][i]));
-          }
+        for (int i = 0; i < 4; ++i) kk[i] = ld2x2(Kb + (4 * ptq + i) * kLd + c);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dd[j] = ld2x2(Ds + (4 * pvq + j) * kLd + c);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) a2[i][j] = fma2(kk[i].y, dd[j].y, fma2(kk[i].x, dd[j].x, a2[i][j]));
+      }
+      float acc[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 v = up2(a2[i][j]);
+          acc[i][j] = v.x + v.y;
         }
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 v = up2(a2[r][i]);
-            acc[r][i] = v.x + v.y;
-          }
-      }
 #pragma unroll 4
-      for (int j = ch; j < kC; j += 2) {  // tokens split by parity: the halves' rows sit on different banks
-        const float2 pj = *reinterpret_cast<const float2*>(Pb + j * kLs + pt);
+      for (int j = cq; j < kC; j += 4) {  // scale P^T dO over this quarter's tokens j
+        const float4 pj = ld4(Pb + j * kLs + 4 * ptq);
+        const float4 o = ld4(Os + j * kSu + 4 * pvq);
+        const float pr[4] = {pj.x, pj.y, pj.z, pj.w}, orr[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float o = Os[j * kSu + pv + 8 * i];
-          acc[0][i] = fmaf(pj.x, o, acc[0][i]);
-          acc[1][i] = fmaf(pj.y, o, acc[1][i]);
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) acc[i][jj] = fmaf(pr[i], orr[jj], acc[i][jj]);
+      }
+      float r[4] = {0.f, 0.f, 0.f, 0.f};  // the sums of token row 4 ptq + cq
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float x = acc[i][j];
+          x += __shfl_xor_sync(0xffffffffu, x, 1);
+          x += __shfl_xor_sync(0xffffffffu, x, 2);
+          if (cq == i) r[j] = x;
         }
-      }
-#pragma unroll
-      for (int r = 0; r < 2; ++r)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[r][i] += __shfl_xor_sync(0xffffffffu, acc[r][i], 1);
-      if (ch == 0) {
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int v = pv + 8 * i;
-            it[kItemDU + (pt + r) * kD + v0 + v] = acc[r][i];
-            Us[(pt + r) * kSu + v] = acc[r][i];
-          }
-      }
+      const int t = 4 * ptq + cq;
+      st4(it + kItemDU + t * kD + v0 + 4 * pvq, r[0], r[1], r[2], r[3]);
+      st4(Us + t * kSu + 4 * pvq, r[0], r[1], r[2], r[3]);
     }
     __syncthreads();  // dU complete; Kb, Pb, Ob, Ds free
     const float4 g0 = ld4(gc + c1), g1 = ld4(gc + c2);
