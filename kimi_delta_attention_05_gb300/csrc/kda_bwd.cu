@@ -784,7 +784,7 @@ __global__ void __launch_bounds__(kSt, 1) kda_bwd_fwd_state_kernel(BwdParams p) 
         for (int a = 0; a < 4; ++a)
 #pragma unroll
           for (int j = 0; j < 4; ++j) a2[a][j] = 0ull;
-#pragma unroll 4
+#pragma unroll 8
         for (int i = 0; i < 16; ++i) {
           const int t = 4 * i + tq;
           const float4 u = ld4(Un + t * kSu + 4 * vq);
@@ -984,7 +984,7 @@ __global__ void __launch_bounds__(kSt, 1) kda_bwd_rev_state_kernel(BwdParams p) 
         for (int a = 0; a < 4; ++a)
 #pragma unroll
           for (int j = 0; j < 4; ++j) a2[a][j] = 0ull;
-#pragma unroll 2
+#pragma unroll 4
         for (int i = 0; i < 16; ++i) {
           const int t = 4 * i + tq;
           const float4 o = ld4(Os + t * kSu + 4 * vq), u = ld4(Us + t * kSu + 4 * vq);
