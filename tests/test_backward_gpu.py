@@ -151,7 +151,7 @@ def _head_slice(inp, h, dout, dfin):
                 cu_seqlens=inp["cu_seqlens"])
 
 
-@pytest.mark.parametrize("workload,heads", [("long_context", (0, 29)), ("dense_batch", (5,))])
+@pytest.mark.parametrize("workload,heads", [("long_context", (0, 29)), ("dense_batch", (5,)), ("extremes", (6,))])
 def test_backward_full_size_sampled(workload, heads):
     """The full-size workload through kda_bwd (every chunk of every head, the
     launch configuration the benchmark times), checked against the chunked fp64
@@ -168,6 +168,7 @@ def test_backward_full_size_sampled(workload, heads):
                       d["dt_bias"], lb, d["initial_state"], None if dfin is None else dfin.cuda(),
                       d["cu_seqlens"], qk_l2norm=inp["qk_l2norm"], gate=inp["gate"])
     torch.cuda.synchronize()
+    del d  # the extremes workload's 4.6 GB workspace is freed with the call; inputs go too
     for h in heads:
         a = _head_slice(inp, h, dout, dfin)
         ref = oracle.chunk_backward(a["q"], a["k"], a["v"], a["g"], a["beta"], a["dout"], scale=inp["scale"],
