@@ -2,7 +2,7 @@
 
 Every gradient (q, k, v, g, beta, A_log, dt_bias, initial state) element by
 element on small cases: every gate form, beta given or as logits, with and
-without the L2 norm, fp32 and bf16 initial states, a final-state gradient,
+without the L2 norm, g in bf16 or fp32, fp32 and bf16 initial states, a final-state gradient,
 packed sequences including empty ones, ragged lengths across the
 64-token chunks and their 16-token blocks, and many heads.  Tolerance (fp32
 arithmetic from bf16 inputs): rel-RMS <= 1e-3 and max-abs <= 1e-2 max|ref| for
@@ -91,6 +91,20 @@ def test_backward_logspace_beta_given():
     inp["beta"] = torch.sigmoid(inp["beta"].float()).to(torch.bfloat16)
     inp.update(gate="logspace", beta_prob=True)
     _run(inp, tag="logspace")
+
+
+@pytest.mark.parametrize("gate", ["logspace", "unsafe"])
+def test_backward_g_in_fp32(gate):
+    """g given in fp32 (KDA_G_FP32): the log decays themselves (logspace) or
+    unsafe-gate logits, read without a bf16 rounding."""
+    inp = make_inputs(WORKLOADS["long_context"], T=150, H=2, seed=250)
+    gen = torch.Generator().manual_seed(251)
+    if gate == "logspace":
+        inp["g"] = -(torch.rand(inp["g"].shape, generator=gen, dtype=torch.float32) * 0.3 + 1e-3)
+        inp.update(gate="logspace")
+    else:
+        inp["g"] = torch.randn(inp["g"].shape, generator=gen, dtype=torch.float32) * 2.0
+    _run(inp, tag=f"g fp32 {gate}")
 
 
 def test_backward_packed_with_empty_sequences():
