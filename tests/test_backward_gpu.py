@@ -118,6 +118,25 @@ def test_backward_safe_without_a_log():
     _run(inp, tag="no A_log")
 
 
+def test_backward_no_tokens():
+    """T = 0 (dense, two sequences with states): no chunk runs; the
+    initial-state gradient is dfinal and the A_log / dt_bias sums are zero."""
+    H = 3
+    gen = torch.Generator().manual_seed(260)
+    e = lambda *sh: torch.empty(sh, dtype=torch.bfloat16, device="cuda")
+    q, k, v, g = e(2, 0, H, 128), e(2, 0, H, 128), e(2, 0, H, 128), e(2, 0, H, 128)
+    beta = e(2, 0, H)
+    A_log = torch.rand(H, generator=gen).cuda()
+    dt_bias = torch.randn((H, 128), generator=gen).cuda()
+    init = torch.randn((2, H, 128, 128), generator=gen).cuda()
+    dfin = torch.randn((2, H, 128, 128), generator=gen).cuda()
+    grads = K.kda_bwd(q, k, v, g, beta, 0.1, e(2, 0, H, 128), A_log, dt_bias, -5.0, init, dfin, None,
+                      qk_l2norm=True, gate="safe")
+    torch.cuda.synchronize()
+    assert torch.equal(grads["initial_state"], dfin)
+    assert torch.count_nonzero(grads["A_log"]) == 0 and torch.count_nonzero(grads["dt_bias"]) == 0
+
+
 def test_backward_rejects_bad_arguments():
     lib = K.load_library()
     a = K.kda_bwd_args()
