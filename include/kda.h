@@ -291,7 +291,9 @@ typedef struct kda_bwd_args {
  * (N + 1) int64 chunk offsets; 0 if the forward arguments are invalid. */
 size_t kda_bwd_workspace_bytes(const kda_bwd_args *args);
 
-/* Enqueue the backward pass on `stream`.  Workspace as for kda_fwd (caller
+/* Enqueue the backward pass on `stream` (every launch and memset on that
+ * stream, so a call can be captured into a CUDA graph once the library has
+ * been used on the device).  Workspace as for kda_fwd (caller
  * owned, 256-byte aligned, at least kda_bwd_workspace_bytes).  Returns KDA_OK
  * or an error code before any launch (the kda_fwd checks; dout and the token
  * gradients must be given when B * T > 0; 16-byte alignment of the float

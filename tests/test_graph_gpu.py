@@ -1,4 +1,4 @@
-"""CUDA graph capture of kda_fwd.
+"""CUDA graph capture of kda_fwd and kda_bwd.
 
 A call captured into a CUDA graph replays to the same bits as the call run
 eagerly: for one-pass shapes (short, and two sequences of 256 chunks), a
@@ -111,3 +111,47 @@ def test_eager_call_while_another_stream_captures():
     torch.cuda.synchronize()
     assert torch.equal(out_x.view(torch.int16), out_r.view(torch.int16))
     assert torch.equal(fin_x, fin_r)
+
+
+BWD_CASES = [
+    ("dense", "long_context", dict(T=1000, H=4, seed=96)),
+    ("packed", "packed_varlen", dict(lengths=[70, 1, 0, 300, 64], H=2, seed=97)),
+]
+
+
+@pytest.mark.parametrize("tag,workload,kw", BWD_CASES, ids=[c[0] for c in BWD_CASES])
+def test_captured_backward_replays_bit_identical(tag, workload, kw):
+    """kda_bwd captured into a CUDA graph (every launch and memset on the
+    caller's stream, workspace and gradients preallocated) replays to the bits
+    of the eager call."""
+    from kimi_delta_attention_05_gb300 import kda as K
+    inp = make_inputs(WORKLOADS[workload], **kw)
+    d = tl.to_device(inp)
+    H = d["q"].shape[2]
+    gen = torch.Generator().manual_seed(kw["seed"] + 100)
+    dout = (torch.randn(d["v"].shape, generator=gen) * 0.5).to(torch.bfloat16).cuda()
+    dfin = (torch.randn((inp["N"], H, 128, 128), generator=gen) * 0.1).cuda()
+    lb = inp["lower_bound"] if inp["gate"] == "safe" else None
+    a, grads = K.make_bwd_args(d["q"], d["k"], d["v"], d["g"], d["beta"], inp["scale"], dout, d["A_log"],
+                               d["dt_bias"], lb, d["initial_state"], dfin, d["cu_seqlens"],
+                               qk_l2norm=inp["qk_l2norm"], gate=inp["gate"])
+    ws = torch.empty(max(K.bwd_workspace_bytes(a), 256), dtype=torch.uint8, device="cuda")
+    K.kda_bwd_args_call(a, ws, torch.cuda.current_stream())  # eager reference
+    torch.cuda.synchronize()
+    ref = {n: t.clone() for n, t in grads.items() if t is not None}
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        K.kda_bwd_args_call(a, ws, side)  # warm-up on a non-default stream
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        K.kda_bwd_args_call(a, ws, torch.cuda.current_stream())
+    for _ in range(2):
+        for t in ref:
+            grads[t].fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        for n, t in ref.items():
+            assert torch.equal(grads[n], t), (tag, n)
